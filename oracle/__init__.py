@@ -1,0 +1,186 @@
+"""The oracle: plain, slow, float64 CPU statements of what the paged GQA decode
+path computes.
+
+TEST INFRASTRUCTURE.  Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA library and never imports it; both sides only share the seeded
+input generators, which hold none of the method's arithmetic.
+
+Contents
+  * ``paged_attention`` / ``attention_weights`` / ``attention_part`` /
+    ``lse_merge`` / ``kv_append`` -- ctypes wrappers over ``pgd_oracle.c``
+    (plain C, float64, pthreads over (sequence, query head) rows).
+  * ``kv_formula`` -- the KV-cache byte count in closed form.
+  * ``block_model`` -- a plain-Python model of block tables, reference counts
+    and copy-on-write.
+
+Every function cites the page section it restates; see the C source header.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+from . import kv_formula  # noqa: F401  (re-exported)
+from . import block_model  # noqa: F401  (re-exported)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pgd_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "libpgd_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``pgd_oracle.c`` with gcc into ``oracle/_build/``.  Plain -O2, no
+    fast-math: the oracle's arithmetic must stay IEEE double."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC,
+           "-lpthread", "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.oracle_kv_append.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I]
+        lib.oracle_kv_append.restype = I
+        lib.oracle_paged_attention.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, D, I, I]
+        lib.oracle_paged_attention.restype = I
+        lib.oracle_attention_weights.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, D]
+        lib.oracle_attention_weights.restype = I
+        lib.oracle_attention_part.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, D]
+        lib.oracle_attention_part.restype = I
+        lib.oracle_lse_merge.argtypes = [P, P, P, P, I, I]
+        lib.oracle_lse_merge.restype = I
+        lib.oracle_threads_used.argtypes = [I, ctypes.c_long]
+        lib.oracle_threads_used.restype = I
+        _lib = lib
+        return lib
+
+
+def _u16(a) -> np.ndarray:
+    """bf16 data as its uint16 bit patterns (accepts torch bf16 tensors or
+    uint16 numpy arrays)."""
+    if isinstance(a, np.ndarray):
+        if a.dtype != np.uint16:
+            raise TypeError("expected bf16 bit patterns as uint16, got %s" % a.dtype)
+        return np.ascontiguousarray(a)
+    import torch  # local: the oracle itself does not need torch
+    if a.dtype != torch.bfloat16:
+        raise TypeError("expected a bfloat16 tensor, got %s" % a.dtype)
+    return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _i32(a) -> np.ndarray:
+    if isinstance(a, np.ndarray):
+        return np.ascontiguousarray(a, dtype=np.int32)
+    return np.ascontiguousarray(a.detach().cpu().numpy().astype(np.int32))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def threads_used(n_threads: int, rows: int) -> int:
+    return int(_load().oracle_threads_used(int(n_threads), int(rows)))
+
+
+def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                    n_threads: int = 0, mutation: int = 0) -> np.ndarray:
+    """float64 out[B][n_q][d] of single-token decode attention over the paged
+    cache.  q: [B][n_q][d] bf16; k_cache, v_cache: [NB][n_kv][bs][d] bf16;
+    block_tables: [B][MB] int32; context_lens: [B] int32 (includes the token
+    just appended).  Raises ValueError on an invalid length or block id."""
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    ta, ca = _i32(block_tables), _i32(context_lens)
+    B, n_q, d = qa.shape
+    NB, n_kv, bs, d2 = ka.shape
+    assert d2 == d and va.shape == ka.shape and ta.shape[0] == B and ca.shape == (B,)
+    MB = ta.shape[1]
+    out = np.zeros((B, n_q, d), dtype=np.float64)
+    st = _load().oracle_paged_attention(_p(out), _p(qa), _p(ka), _p(va), _p(ta), _p(ca), B, n_q,
+                                        n_kv, d, bs, MB, NB, float(scale), int(n_threads),
+                                        int(mutation))
+    if st:
+        raise ValueError("oracle: invalid context length or block id (status %d)" % st)
+    return out
+
+
+def attention_weights(q, k_cache, block_tables, context_lens, b: int, h: int,
+                      scale: float) -> np.ndarray:
+    """Softmax weights w[t], t < context_lens[b], of row (b, h)."""
+    qa, ka = _u16(q), _u16(k_cache)
+    ta, ca = _i32(block_tables), _i32(context_lens)
+    B, n_q, d = qa.shape
+    NB, n_kv, bs, _ = ka.shape
+    w = np.zeros(int(ca[b]), dtype=np.float64)
+    st = _load().oracle_attention_weights(_p(w), _p(qa), _p(ka), _p(ta), _p(ca), int(b), int(h),
+                                          n_q, n_kv, d, bs, ta.shape[1], NB, float(scale))
+    if st:
+        raise ValueError("oracle: invalid context length or block id")
+    return w
+
+
+def attention_part(q, k_cache, v_cache, block_tables, b: int, h: int, t0: int, t1: int,
+                   scale: float):
+    """Local state (m, l, o[d]) of row (b, h) over tokens [t0, t1)."""
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    ta = _i32(block_tables)
+    B, n_q, d = qa.shape
+    NB, n_kv, bs, _ = ka.shape
+    m = np.zeros(1, dtype=np.float64)
+    l = np.zeros(1, dtype=np.float64)
+    o = np.zeros(d, dtype=np.float64)
+    st = _load().oracle_attention_part(_p(m), _p(l), _p(o), _p(qa), _p(ka), _p(va), _p(ta),
+                                       int(b), int(h), int(t0), int(t1), n_q, n_kv, d, bs,
+                                       ta.shape[1], NB, float(scale))
+    if st:
+        raise ValueError("oracle: invalid block id")
+    return float(m[0]), float(l[0]), o
+
+
+def lse_merge(m, l, o) -> np.ndarray:
+    """Merge local states (m_i, l_i, o_i[d]) into the normalised row."""
+    m = np.ascontiguousarray(m, dtype=np.float64)
+    l = np.ascontiguousarray(l, dtype=np.float64)
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    n, d = o.shape
+    out = np.zeros(d, dtype=np.float64)
+    st = _load().oracle_lse_merge(_p(out), _p(m), _p(l), _p(o), n, d)
+    if st:
+        raise ValueError("oracle: every part is empty")
+    return out
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, block_tables, positions):
+    """Return copies of (k_cache, v_cache) as uint16 bit patterns with one new
+    token per sequence written at logical position positions[b]."""
+    kc = _u16(k_cache).copy()
+    vc = _u16(v_cache).copy()
+    kn, vn = _u16(k_new), _u16(v_new)
+    ta, pa = _i32(block_tables), _i32(positions)
+    NB, n_kv, bs, d = kc.shape
+    B = kn.shape[0]
+    st = _load().oracle_kv_append(_p(kc), _p(vc), _p(kn), _p(vn), _p(ta), _p(pa), B, n_kv, d, bs,
+                                  ta.shape[1], NB)
+    if st:
+        raise ValueError("oracle: position or block id out of range")
+    return kc, vc

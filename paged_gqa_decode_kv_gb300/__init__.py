@@ -1,0 +1,10 @@
+"""paged_gqa_decode_kv_gb300 -- paged GQA decode attention and KV append for
+GB300 (sm_103a), behind the C ABI declared in include/pgd.h.
+
+The compute path runs only in the CUDA library ``libpgd.so``; this package is
+argument marshalling over it.  Importing the package does not load the
+library; the first call does, and fails loudly if it was not built.
+"""
+from .inputs import WORKLOADS, Workload, PagedBatch, make_batch, make_workload  # noqa: F401
+
+__all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload"]

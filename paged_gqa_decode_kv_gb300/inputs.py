@@ -1,0 +1,241 @@
+"""Seeded synthetic inputs for the paged decode path.
+
+This module is shared by the tests, the benchmark and the oracle's callers.
+It holds none of the method's arithmetic: it only draws bf16 tensors, builds
+block tables (random permutations of a physical pool) and poisons every slot
+that must never be read with NaN.
+
+Workloads (all single layer, d_head = 128, scale 1/sqrt(128)):
+
+=====================  ====  =========  ===============================  ====  ==========
+name                   B     n_q/n_kv   context                          bs    K/V
+=====================  ====  =========  ===============================  ====  ==========
+single_ctx512          1     32/8       512                              16    N(0, 1)
+batch16_ctx8192        16    32/8       8192                             16    N(0, 1)
+mha40_batch4_ctx8192   4     40/40      8192                             16    N(0, 1)
+ragged64_g8            64    64/8       L ~ U[128, 32768], +1 appended   32    N(0, 0.5^2)
+shared_prefix32        32    32/8       4000 shared + U[1, 2000]         16    N(0, 1)
+single_ctx131072       1     32/8       131072                           16    N(0, 1)
+=====================  ====  =========  ===============================  ====  ==========
+
+Q is N(0, 1) everywhere.  Data seed 1234, table seed 4321.  The physical pool
+holds every needed block plus 5 % spare blocks; the table is a random
+permutation of it.  Spare blocks, unused tail slots and (when a workload
+appends) the slot of the token about to be appended are NaN, and unused table
+entries are -1, so any read outside the valid range shows up in the output.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, List, Optional
+
+import torch
+
+HEAD_DIM = 128
+DATA_SEED = 1234
+TABLE_SEED = 4321
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    n_q: int
+    n_kv: int
+    block_size: int
+    ctx: Optional[int] = None           # fixed context (all sequences)
+    ragged: Optional[tuple] = None      # (lo, hi) inclusive, drawn per sequence
+    shared_prefix: int = 0              # tokens shared by every sequence
+    suffix: Optional[tuple] = None      # (lo, hi) inclusive unique suffix
+    kv_std: float = 1.0
+    q_std: float = 1.0
+    append: bool = False                # one new token appended before attention
+    head_dim: int = HEAD_DIM
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+WORKLOADS: Dict[str, Workload] = {
+    w.name: w for w in [
+        Workload("single_ctx512", 1, 32, 8, 16, ctx=512),
+        Workload("batch16_ctx8192", 16, 32, 8, 16, ctx=8192),
+        Workload("mha40_batch4_ctx8192", 4, 40, 40, 16, ctx=8192),
+        Workload("ragged64_g8", 64, 64, 8, 32, ragged=(128, 32768), kv_std=0.5, append=True),
+        Workload("shared_prefix32", 32, 32, 8, 16, shared_prefix=4000, suffix=(1, 2000)),
+        Workload("single_ctx131072", 1, 32, 8, 16, ctx=131072),
+    ]
+}
+
+
+def context_lengths(w: Workload, seed: int = DATA_SEED) -> List[int]:
+    """Context length of every sequence after the append (if any)."""
+    g = torch.Generator().manual_seed(seed)
+    if w.ctx is not None:
+        return [w.ctx] * w.batch
+    if w.ragged is not None:
+        lo, hi = w.ragged
+        drawn = torch.randint(lo, hi + 1, (w.batch,), generator=g).tolist()
+        return [x + 1 for x in drawn] if w.append else drawn
+    if w.suffix is not None:
+        lo, hi = w.suffix
+        suf = torch.randint(lo, hi + 1, (w.batch,), generator=g).tolist()
+        return [w.shared_prefix + s for s in suf]
+    raise ValueError("workload %s has no length rule" % w.name)
+
+
+@dataclasses.dataclass
+class PagedBatch:
+    """Inputs of one decode step.  Tensors live on `device`."""
+    q: torch.Tensor              # bf16 [B][n_q][d]
+    k_cache: torch.Tensor        # bf16 [NB][n_kv][bs][d]
+    v_cache: torch.Tensor        # bf16 [NB][n_kv][bs][d]
+    block_tables: torch.Tensor   # int32 [B][MB], -1 where unused
+    context_lens: torch.Tensor   # int32 [B]
+    k_new: Optional[torch.Tensor]  # bf16 [B][n_kv][d] when appending
+    v_new: Optional[torch.Tensor]
+    positions: Optional[torch.Tensor]  # int32 [B] = context_lens - 1 when appending
+    scale: float
+    n_kv: int
+    block_size: int
+    unique_blocks: int           # physical blocks referenced by the tables
+    shared_blocks: int           # blocks referenced by more than one sequence
+
+    @property
+    def batch(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def n_q(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def head_dim(self) -> int:
+        return self.q.shape[2]
+
+    @property
+    def num_blocks(self) -> int:
+        return self.k_cache.shape[0]
+
+    @property
+    def max_blocks(self) -> int:
+        return self.block_tables.shape[1]
+
+
+def _randn_bf16(shape, std: float, gen: torch.Generator, device) -> torch.Tensor:
+    """N(0, std^2) rounded to bf16, drawn in chunks to bound temporaries."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(-1)
+    n = flat.numel()
+    chunk = 1 << 26
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        t = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32)
+        if std != 1.0:
+            t.mul_(std)
+        flat[s:e].copy_(t)
+    return out
+
+
+def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[int], *,
+               head_dim: int = HEAD_DIM, kv_std: float = 1.0, q_std: float = 1.0,
+               shared_prefix: int = 0, append: bool = False, spare_frac: float = 0.05,
+               max_blocks: Optional[int] = None, seed: int = DATA_SEED,
+               table_seed: int = TABLE_SEED, device="cpu", poison: bool = True,
+               scale: Optional[float] = None) -> PagedBatch:
+    """Build one decode step's inputs.
+
+    Every sequence b holds ctx_lens[b] tokens.  The first `shared_prefix`
+    tokens of every sequence live in the same physical blocks (shared_prefix
+    must then be a multiple of block_size, or the partial block is private).
+    With append=True, the last token of every sequence is returned as
+    k_new/v_new and its cache slot is left NaN."""
+    assert len(ctx_lens) == batch and n_q % n_kv == 0
+    bs = block_size
+    nblk = [(c + bs - 1) // bs for c in ctx_lens]
+    n_shared = shared_prefix // bs if batch > 1 else 0
+    if n_shared:
+        assert all(c >= n_shared * bs for c in ctx_lens)
+    private = [n - n_shared for n in nblk]
+    needed = n_shared + sum(private)
+    NB = max(1, needed + int(math.ceil(needed * spare_frac)))
+    MB = max(nblk) if max_blocks is None else max_blocks
+    assert MB >= max(nblk)
+
+    tgen = torch.Generator().manual_seed(table_seed)
+    perm = torch.randperm(NB, generator=tgen).to(torch.int32)
+    tables = torch.full((batch, MB), -1, dtype=torch.int32)
+    cursor = n_shared
+    shared_ids = perm[:n_shared]
+    for b in range(batch):
+        if n_shared:
+            tables[b, :n_shared] = shared_ids
+        tables[b, n_shared:nblk[b]] = perm[cursor:cursor + private[b]]
+        cursor += private[b]
+    used_ids = perm[:needed]
+    spare_ids = perm[needed:]
+
+    gen = torch.Generator(device=device).manual_seed(seed)
+    q = _randn_bf16((batch, n_q, head_dim), q_std, gen, device)
+    k_cache = _randn_bf16((NB, n_kv, bs, head_dim), kv_std, gen, device)
+    v_cache = _randn_bf16((NB, n_kv, bs, head_dim), kv_std, gen, device)
+
+    k_new = v_new = positions = None
+    if append:
+        positions = torch.tensor([c - 1 for c in ctx_lens], dtype=torch.int32)
+        blk = tables[torch.arange(batch), positions // bs].long().to(device)
+        slot = (positions % bs).long().to(device)
+        k_new = k_cache[blk, :, slot, :].clone()
+        v_new = v_cache[blk, :, slot, :].clone()
+
+    if poison:
+        nan = float("nan")
+        if spare_ids.numel():
+            sid = spare_ids.long().to(device)
+            k_cache[sid] = nan
+            v_cache[sid] = nan
+        for b in range(batch):
+            tail = ctx_lens[b] % bs
+            if tail:
+                last = int(tables[b, nblk[b] - 1])
+                k_cache[last, :, tail:, :] = nan
+                v_cache[last, :, tail:, :] = nan
+        if append:
+            k_cache[blk, :, slot, :] = nan
+            v_cache[blk, :, slot, :] = nan
+    del used_ids
+
+    return PagedBatch(
+        q=q, k_cache=k_cache, v_cache=v_cache,
+        block_tables=tables.to(device), context_lens=torch.tensor(ctx_lens, dtype=torch.int32).to(device),
+        k_new=k_new, v_new=v_new,
+        positions=None if positions is None else positions.to(device),
+        scale=(1.0 / math.sqrt(head_dim)) if scale is None else scale,
+        n_kv=n_kv, block_size=bs, unique_blocks=needed,
+        shared_blocks=n_shared)
+
+
+def make_workload(name: str, device="cpu", seed: int = DATA_SEED, **overrides) -> PagedBatch:
+    w = WORKLOADS[name]
+    if overrides:
+        w = dataclasses.replace(w, **overrides)
+    lens = context_lengths(w, seed)
+    return make_batch(w.batch, w.n_q, w.n_kv, w.block_size, lens, head_dim=w.head_dim,
+                      kv_std=w.kv_std, q_std=w.q_std, shared_prefix=w.shared_prefix,
+                      append=w.append, seed=seed, device=device, scale=w.scale)
+
+
+def kv_bytes_read(batch: PagedBatch, unique: bool = False) -> int:
+    """Algorithmic K+V bytes one attention call must read: every cached token
+    of every sequence, all KV heads, K and V, bf16 (logical), or each physical
+    block once (unique; only differs when blocks are shared)."""
+    per_token = 2 * batch.n_kv * batch.head_dim * batch.k_cache.element_size()
+    if not unique:
+        return int(batch.context_lens.sum().item()) * per_token
+    bs = batch.block_size
+    lens = batch.context_lens.tolist()
+    shared_tokens = batch.shared_blocks * bs
+    total = shared_tokens + sum(c - shared_tokens for c in lens) if batch.shared_blocks else sum(lens)
+    return total * per_token
