@@ -1,0 +1,425 @@
+#!/usr/bin/env python
+"""Benchmark of the paged GQA decode step on GB300.
+
+One step = one pass of the hot path over one batch: kv_append of the newest
+token of every sequence, then paged decode attention over every cached
+position (context includes the appended token).  Default workload:
+batch 16, context 8192, 32 query / 8 KV heads, d 128, block 16, bf16
+(512 MiB of K/V per step, larger than the 129 MB L2, so no flush is needed).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--splits S] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  value = algorithmic K/V bytes read per step
+summed over ranks / max-over-ranks time, in GB/s (1e9 B/s).  Under torchrun
+(N > 1) every rank runs an independent replica of the workload on its own GPU
+(the path shards by sequence and KV head with no exchange); timing
+collectives use gloo on the host.  --impl reference times the float64 CPU
+oracle on a bounded sample of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; seq-layer-steps/sec"
+NOMINAL_HBM_GBS = 8000.0     # nominal GB300 HBM3e bandwidth (~8 TB/s)
+FALLBACK_HBM_GBS = 6800.0    # profiling recipe's fallback when no measured peak exists
+L2_BYTES = 129 * 10**6
+ATTENTION_SRC = os.path.join(ROOT, "paged_gqa_decode_kv_gb300", "csrc", "attention.cu")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "paged_attention_batch16_ctx8192.md")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--workload", default="batch16_ctx8192")
+    ap.add_argument("--splits", type=int, default=0, help="0 = automatic")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------ distribution
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def dist_init(world: int):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling (every 100 ms) in the background."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+               "--format=csv,noheader,nounits", "-lms", "100"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm, smax = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            active = [r for r, v in zip(self.REASONS, parts[3:]) if v.lower() == "active"]
+            self.samples.append((time.time(), sm, smax, active))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        window = "warmup+timed"
+        if not win:
+            win = [s for s in self.samples if t0 <= s[0] <= t1 + 0.5]
+            window = "warmup+timed+0.5s"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "none"}
+        reasons = sorted({r for s in win for r in s[3]})
+        return {"sm_mhz": statistics.median(s[1] for s in win),
+                "sm_max_mhz": max(s[2] for s in win), "reasons": reasons,
+                "samples": len(win), "window": window}
+
+
+# ------------------------------------------------------------------- peaks
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since that capture."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    m_sha = re.search(r"attention_cu_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_bytes and m_sha):
+        return None
+    cur = hashlib.sha256(open(ATTENTION_SRC, "rb").read()).hexdigest()
+    return int(m_bytes.group(1)) if cur == m_sha.group(1) else None
+
+
+# ------------------------------------------------------------ CPU baseline
+def oracle_sample(pb_host, n_seq: int, n_threads: int = 0):
+    """Run the oracle on the first n_seq sequences; return (seconds, bytes)."""
+    import oracle
+    from paged_gqa_decode_kv_gb300 import inputs
+    q = pb_host["q"][:n_seq]
+    t = pb_host["tables"][:n_seq]
+    c = pb_host["lens"][:n_seq]
+    t0 = time.perf_counter()
+    oracle.paged_attention(q, pb_host["k"], pb_host["v"], t, c, pb_host["scale"],
+                           n_threads=n_threads)
+    dt = time.perf_counter() - t0
+    per_token = 2 * pb_host["n_kv"] * pb_host["d"] * 2
+    return dt, int(c.sum()) * per_token
+
+
+def host_copy(pb):
+    return {"q": pb.q.cpu(), "k": pb.k_cache.cpu(), "v": pb.v_cache.cpu(),
+            "tables": pb.block_tables.cpu(), "lens": pb.context_lens.cpu(), "scale": pb.scale,
+            "n_kv": pb.n_kv, "d": pb.head_dim, "B": pb.batch, "n_q": pb.n_q}
+
+
+def cpu_baseline(pb_host, seconds: float):
+    import oracle
+    B = pb_host["B"]
+    rows = B * pb_host["n_q"]
+    cores = oracle.threads_used(0, rows)
+    total_t, total_b, calls = 0.0, 0, 0
+    while total_t < seconds and calls < 200:
+        dt, nb = oracle_sample(pb_host, B)
+        total_t += dt
+        total_b += nb
+        calls += 1
+    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": "float64 oracle attention over the full batch (all %d sequences, %d query "
+                      "heads), %d call(s), %.1f s; kv_append excluded (a %d-byte copy)"
+                      % (B, pb_host["n_q"], calls, total_t, 2 * B * pb_host["n_kv"] * 256)}
+
+
+# --------------------------------------------------------------- our arm
+def config_block(pb, name, grid, splits):
+    return {"workload": name, "batch": pb.batch, "context": sorted(set(pb.context_lens.tolist()))
+            if pb.batch <= 4 else "%d..%d" % (int(pb.context_lens.min()),
+                                              int(pb.context_lens.max())),
+            "n_q": pb.n_q, "n_kv": pb.n_kv, "head_dim": pb.head_dim,
+            "block_size": pb.block_size, "kv_dtype": "bf16",
+            "splits": "auto" if splits == 0 else splits, "grid_ctas": grid,
+            "l2": "inputs %.0f MB > 129 MB L2, no flush" % (pb.k_cache.numel() * 4 / 1e6)
+            if pb.k_cache.numel() * 4 > L2_BYTES else "working set fits L2 (hot)"}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import __graft_entry__
+    import paged_gqa_decode_kv_gb300 as pgd
+    from paged_gqa_decode_kv_gb300 import inputs
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pb = inputs.make_workload(args.workload, device=dev, append=True)
+    B, n_q, n_kv = pb.batch, pb.n_q, pb.n_kv
+    ws = pgd.make_workspace(B, n_q, n_kv, args.splits, dev)
+    out = torch.empty_like(pb.q)
+    grid = pgd.attention_grid(B, n_q, n_kv, pb.block_size, args.splits)
+    stream = torch.cuda.current_stream()
+    kv_bytes = inputs.kv_bytes_read(pb)
+
+    def step(ev_a=None, ev_b=None):
+        pgd.kv_append(pb.k_new, pb.v_new, pb.k_cache, pb.v_cache, pb.block_tables, pb.positions,
+                      stream=stream)
+        if ev_a is not None:
+            ev_a.record(stream)
+        pgd.paged_decode_attention(out, pb.q, pb.k_cache, pb.v_cache, pb.block_tables,
+                                   pb.context_lens, pb.scale, num_splits=args.splits,
+                                   workspace=ws, stream=stream)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    sampler = ClockSampler(gpu_uuid)
+    sampler.start()
+    time.sleep(0.3)
+    t_wall0 = time.time()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = pgd.device_errors(clear=True, stream=stream)
+    if flags:
+        raise RuntimeError("device error word %d after warm-up" % flags)
+
+    K = args.steps
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(K):
+        step(ev_a[i], ev_b[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
+    flags = pgd.device_errors(clear=True, stream=stream)
+    if flags:
+        raise RuntimeError("device error word %d after the timed steps" % flags)
+
+    max_ms = max_over_ranks(elapsed_ms, world)
+    total_bytes = sum_over_ranks(kv_bytes * K, world)
+    value = total_bytes / (max_ms / 1e3) / 1e9
+    seq_steps = sum_over_ranks(B * K, world) / (max_ms / 1e3)
+
+    # end to end through the C ABI with host (pinned) inputs and outputs
+    q_h = pb.q.cpu().pin_memory()
+    kn_h, vn_h = pb.k_new.cpu().pin_memory(), pb.v_new.cpu().pin_memory()
+    cl_h = pb.context_lens.cpu().pin_memory()
+    out_h = torch.empty_like(q_h).pin_memory()
+    q_d, kn_d, vn_d = torch.empty_like(pb.q), torch.empty_like(pb.k_new), torch.empty_like(pb.v_new)
+    cl_d = torch.empty_like(pb.context_lens)
+    out_d = torch.empty_like(pb.q)
+
+    def e2e_step():
+        pgd.decode_step(out_h, q_h, kn_h, vn_h, cl_h, out_d, q_d, kn_d, vn_d, cl_d, pb.k_cache,
+                        pb.v_cache, pb.block_tables, pb.scale, args.splits, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
+    e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
+    h2d = (q_h.numel() + kn_h.numel() + vn_h.numel()) * 2 + cl_h.numel() * 4
+    d2h = out_h.numel() * 2
+
+    peak, peak_kind = hbm_peak()
+    achieved = kv_bytes / (attn_ms / 1e3) / 1e9
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(max_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "accumulate": "f32", "data": "synthetic (seeded N(0,1) bf16 K/V/Q, random block tables)",
+        "config": config_block(pb, args.workload, grid, args.splits),
+        "kv_bytes_per_step": kv_bytes,
+        "seq_layer_steps_per_s": round(seq_steps, 1),
+        "pct_of_hbm_peak": {"nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+                            peak_kind: round(100 * value / world / peak, 2)},
+        "roofline": {"bound": "hbm", "kernel": "paged_attention_kernel",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(), "launch_ms": round(attn_ms, 5),
+                     "bytes_per_launch": kv_bytes},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5)},
+        "gpu_launches": 2 * K,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "gpu": torch.cuda.get_device_name(local),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(host_copy(pb), args.cpu_seconds)
+    return result
+
+
+# --------------------------------------------------------- reference arm
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: each step a bounded sample
+    (the first n sequences) of the same workload."""
+    import oracle
+    from paged_gqa_decode_kv_gb300 import inputs
+
+    pb = inputs.make_workload(args.workload, device="cpu", append=False)
+    host = host_copy(pb)
+    B = pb.batch
+    # calibrate: one sequence, then size the sample so the run stays within ~2 minutes
+    dt1, _ = oracle_sample(host, 1)
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n_seq = int(max(1, min(B, per_step_budget / max(dt1, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_sample(host, n_seq)
+    t_total, b_total = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = oracle_sample(host, n_seq)
+        t_total += dt
+        b_total += nb
+    value = b_total / t_total / 1e9
+    cores = oracle.threads_used(0, n_seq * pb.n_q)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / max(1, args.steps), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 K/V/Q, random block tables)",
+        "config": config_block(pb, args.workload, 0, args.splits),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": "first %d of %d sequences per step (all heads, full context)"
+                                   % (n_seq, B)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    dist_init(world)
+    result = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,239 @@
+/*
+ * pgd.h -- C ABI of libpgd: paged GQA decode attention and KV append on one
+ * GB300 GPU (sm_103a).
+ *
+ * Terms (page title, section):
+ *   B      sequences in the batch
+ *   n_q    query heads; n_kv KV heads; G = n_q / n_kv query heads share one KV
+ *          head, query head h reading KV head h / G ("Module 10: inference and
+ *          serving", section "Deriving capacity from the configuration" and
+ *          Lab 2's repeat_interleave; "The math of Transformer inference",
+ *          section 5: MHA G = 1, MQA n_kv = 1, GQA in between)
+ *   d      head width (d_head); this library supports d = 128
+ *   bs     block size in tokens; a block holds bs consecutive positions of one
+ *          sequence ("Module 10", section "Mapping logical positions to
+ *          physical blocks"; "Ch. 6 Inference efficiency and serving", 6.4)
+ *   NB     physical blocks in the pool; MB = width of a block-table row
+ *
+ * Layouts (row-major, all device memory unless marked host):
+ *   k_cache, v_cache  bf16 [NB][n_kv][bs][d]   one (block, KV head) tile is a
+ *                     contiguous bs*d*2-byte run
+ *   block_tables      int32 [B][MB]  logical block j of sequence b lives in
+ *                     physical block block_tables[b][j]; entries past the
+ *                     sequence's last block are never read
+ *   context_lens      int32 [B]      cached positions of sequence b, counting
+ *                     the token appended in this step
+ *   q, out            bf16 [B][n_q][d]
+ *   k_new, v_new      bf16 [B][n_kv][d]
+ *
+ * Conventions:
+ *   - Ownership: the caller owns every buffer, including workspaces; no entry
+ *     point here allocates device memory.  Pointers to bf16 arrays must be
+ *     16-byte aligned; the workspace must be 256-byte aligned.
+ *   - Asynchrony: GPU entry points only enqueue work on `stream` (a
+ *     cudaStream_t passed as void*; NULL = the legacy default stream) and
+ *     return.  Argument errors are detected on the host before any launch.
+ *   - Device-side checks: kernels never read or write outside the pool.  A
+ *     block id outside [0, NB), a context length outside [1, MB*bs] or an
+ *     append position outside [0, MB*bs) skips the affected work and sets a
+ *     bit in the per-device error word (pgd_device_errors); outputs of the
+ *     affected sequences are then unspecified.
+ *   - Threading: entry points are thread-safe except that one pgd_alloc
+ *     handle must not be used from two threads at once.
+ */
+#ifndef PGD_H_
+#define PGD_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pgd_status {
+  PGD_OK = 0,
+  PGD_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or shape */
+  PGD_ERR_UNSUPPORTED = 2,   /* valid but not built: d != 128, bs, G, batch */
+  PGD_ERR_OUT_OF_BLOCKS = 3, /* allocator: not enough free blocks; no change made */
+  PGD_ERR_WORKSPACE = 4,     /* workspace missing, too small or misaligned */
+  PGD_ERR_CUDA = 5,          /* a CUDA runtime call failed (see detail) */
+  PGD_ERR_BLOCK_STATE = 6    /* allocator: block not held, double release, table gap */
+} pgd_status;
+
+/* Bits of the per-device error word written by the kernels. */
+#define PGD_DEVERR_BAD_BLOCK_ID 1 /* a needed table entry was outside [0, NB) */
+#define PGD_DEVERR_BAD_CONTEXT 2  /* a context length was < 1 or > MB*bs */
+#define PGD_DEVERR_BAD_POSITION 4 /* a kv_append position was outside [0, MB*bs) */
+#define PGD_DEVERR_TIMEOUT 8      /* a bounded wait inside a kernel gave up */
+
+/* Largest batch one attention call accepts (larger batches: split the call). */
+#define PGD_MAX_BATCH 4096
+
+/* Static description of a status code.  Never NULL. */
+const char *pgd_status_string(pgd_status s);
+
+/* Detail of the last non-OK status returned on the calling thread ("" if
+ * none).  Valid until the next call on that thread. */
+const char *pgd_last_error_detail(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t pgd_version(void);
+
+/* ---------------------------------------------------------------------- */
+/* kv_append                                                              */
+/* ---------------------------------------------------------------------- */
+/* Write the new token of every sequence into its paged slot.  The decode
+ * step forwards the pending token and commits its K/V to the cache, after
+ * which the cache holds exactly the positions already forwarded ("LLM
+ * inference systems engineering", 2.1.3 computation graph and generation
+ * loop; "The math of Transformer inference", section 1, decode bullet; the
+ * toy decoder of "Module 10", Lab 2, concatenates the new K/V before it
+ * attends).
+ *
+ * For every b < B and KV head g < n_kv, with p = positions[b] (the number of
+ * positions cached before this token):
+ *     k_cache[block_tables[b][p / bs]][g][p % bs][:] = k_new[b][g][:]
+ *     v_cache[...same slot...]                       = v_new[b][g][:]
+ * A bit-for-bit copy.  positions is a device array [B].  The caller must not
+ * append into a block that other sequences share (refcount > 1): take the
+ * copy-on-write path first (pgd_alloc_append_slot + pgd_copy_blocks).
+ * Returns PGD_OK after enqueueing; B == 0 is a no-op. */
+pgd_status pgd_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         const int32_t *block_tables, const int32_t *positions, int32_t B,
+                         int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB,
+                         void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* paged decode attention                                                 */
+/* ---------------------------------------------------------------------- */
+/* Single-query attention of every sequence over its own paged cache ("Module
+ * 10", section "Attention reads a different cache per sequence"; "The math
+ * of Transformer inference", section 4):
+ *     out[b][h][:] = sum_t softmax_t(scale * q[b][h] . k_t) v_t,
+ *     t in [0, context_lens[b]), k_t/v_t = KV head h / G of token t read
+ *     through block_tables[b] at block t / bs, slot t % bs.
+ * Only the valid positions of each sequence are read (section 9 of "The math
+ * of Transformer inference": ragged reads).  Each K/V tile is read once per
+ * (sequence, KV head) and serves all G query heads.  The context may be split
+ * into parts whose (max, sum, weighted-sum) states are merged by log-sum-exp
+ * ("The math of Transformer inference", section 8, sharding the KV cache
+ * along the sequence; "LLM inference systems engineering", 2.8.3).
+ * Arithmetic: bf16 inputs, fp32 accumulation, fp32 softmax, bf16 output
+ * rounded to nearest even.
+ *
+ * num_splits: 0 = automatic (the work is spread evenly over every SM);
+ *   k > 0 = k * B * n_kv parts of (nearly) equal size in blocks.
+ * workspace: device scratch of at least pgd_attention_workspace_size(...)
+ *   bytes, 256-byte aligned, zero-filled before its first use (cudaMemset);
+ *   every completed call leaves its counters at zero again, so one workspace
+ *   can serve any number of calls in stream order.  Concurrent calls on
+ *   different streams need separate workspaces.
+ * Supported: d = 128, bs in {16, 32}, G in {1, 2, 4, 8}, 0 <= B <=
+ * PGD_MAX_BATCH, B * MB < 2^31.  Returns PGD_OK after enqueueing. */
+size_t pgd_attention_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_t d,
+                                    int32_t num_splits);
+
+pgd_status pgd_paged_decode_attention(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      const int32_t *context_lens, int32_t B, int32_t n_q,
+                                      int32_t n_kv, int32_t d, int32_t bs, int32_t MB,
+                                      int32_t NB, float scale, int32_t num_splits,
+                                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Number of CTAs one pgd_paged_decode_attention call launches with these
+ * arguments on the current device (0 on invalid arguments). */
+int32_t pgd_attention_grid(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t num_splits);
+
+/* ---------------------------------------------------------------------- */
+/* one decode step with host inputs and outputs                            */
+/* ---------------------------------------------------------------------- */
+/* One decode step of one layer for a caller whose per-step tensors live in
+ * host memory: copies q_h, k_new_h, v_new_h and context_lens_h to the
+ * caller's device staging buffers, appends the new token at position
+ * context_lens[b] - 1 (pgd_kv_append), runs pgd_paged_decode_attention, and
+ * copies the result back to out_h -- all enqueued on `stream`.  For
+ * asynchronous copies the host buffers should be pinned.  The cache, block
+ * tables and workspace stay on the device.  Shapes and rules as above. */
+pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
+                           const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
+                           void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
+                           const int32_t *block_tables, int32_t B, int32_t n_q, int32_t n_kv,
+                           int32_t d, int32_t bs, int32_t MB, int32_t NB, float scale,
+                           int32_t num_splits, void *workspace, size_t workspace_bytes,
+                           void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* copy-on-write block copy                                               */
+/* ---------------------------------------------------------------------- */
+/* For i < n: copy physical block src_ids[i] to dst_ids[i] (all KV heads, all
+ * bs slots, K and V).  The device half of copy-on-write: a sequence that must
+ * write into a block other sequences share first gets a private copy ("Module
+ * 10", section "Share only identical state"; "Ch. 6", 6.4).  src_ids and
+ * dst_ids are device arrays; a pair with an id outside [0, NB) is skipped and
+ * flagged.  Source and destination blocks must not overlap. */
+pgd_status pgd_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_ids,
+                           const int32_t *dst_ids, int32_t n, int32_t n_kv, int32_t d,
+                           int32_t bs, int32_t NB, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* device error word                                                      */
+/* ---------------------------------------------------------------------- */
+/* Wait for `stream`, then read the current device's error word (PGD_DEVERR_*
+ * bits accumulated by every kernel of this library on that device) into
+ * *flags; clear it when `clear` is nonzero. */
+pgd_status pgd_device_errors(int32_t *flags, int32_t clear, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* host block allocator (host memory only)                                */
+/* ---------------------------------------------------------------------- */
+/* A pool of num_blocks physical block ids with a reference count each
+ * ("Module 10", sections "Mapping logical positions to physical blocks" and
+ * "Share only identical state"; "Ch. 6", 6.4; "The math of Transformer
+ * inference", section 9, PagedAttention: reference counts and copy-on-write).
+ * Ids are allocated on demand, one block when a sequence grows past a block
+ * boundary, so a sequence wastes at most bs - 1 slots. */
+typedef struct pgd_alloc pgd_alloc;
+
+/* Create a pool of num_blocks (> 0) free blocks. */
+pgd_status pgd_alloc_create(int32_t num_blocks, pgd_alloc **out);
+/* Destroy a pool (NULL is a no-op). */
+void pgd_alloc_destroy(pgd_alloc *a);
+/* Take n free ids (count 1 each) into ids_out[n]; all or nothing
+ * (PGD_ERR_OUT_OF_BLOCKS leaves the pool unchanged). */
+pgd_status pgd_alloc_allocate(pgd_alloc *a, int32_t n, int32_t *ids_out);
+/* Add one reference to each of ids[n] (each must be held). */
+pgd_status pgd_alloc_share(pgd_alloc *a, const int32_t *ids, int32_t n);
+/* Drop one reference from each of ids[n]; an id whose count reaches 0 is
+ * free again.  Checked first, applied only if every drop is valid. */
+pgd_status pgd_alloc_release(pgd_alloc *a, const int32_t *ids, int32_t n);
+/* Reference count of id (0 = free), or -1 if id is outside the pool. */
+int32_t pgd_alloc_refcount(const pgd_alloc *a, int32_t id);
+int32_t pgd_alloc_num_free(const pgd_alloc *a);
+int32_t pgd_alloc_num_blocks(const pgd_alloc *a);
+/* Make the slot of logical position pos writable in one table row (host
+ * int32 [MB], -1 = unassigned).  If pos opens a block that the row lacks,
+ * allocate it.  If the block holding pos is shared (count > 1), copy on
+ * write: allocate a private block, point the row at it, drop one reference to
+ * the old block, and return the pair in *cow_src / *cow_dst for the caller to
+ * copy on the device (pgd_copy_blocks) before appending.  Otherwise both are
+ * -1.  On PGD_ERR_OUT_OF_BLOCKS nothing changes. */
+pgd_status pgd_alloc_append_slot(pgd_alloc *a, int32_t *table_row, int32_t MB, int32_t bs,
+                                 int32_t pos, int32_t *cow_src, int32_t *cow_dst);
+/* Fork: make dst_row (host int32 [MB]) share every block that holds one of
+ * the first n_tokens tokens of src_row (a reference each, the partial last
+ * block included; its first write takes the copy-on-write path). */
+pgd_status pgd_alloc_fork(pgd_alloc *a, const int32_t *src_row, int32_t n_tokens, int32_t bs,
+                          int32_t *dst_row, int32_t MB);
+
+/* Host-side check of host copies of block tables and context lengths: every
+ * length in [1, MB*bs] and every needed entry in [0, NB).  Returns
+ * PGD_ERR_INVALID_ARG with a detail naming the first offender. */
+pgd_status pgd_validate_tables(const int32_t *block_tables_h, const int32_t *context_lens_h,
+                               int32_t B, int32_t MB, int32_t NB, int32_t bs);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PGD_H_ */

@@ -105,7 +105,8 @@ class BlockModel:
         if pos < 0 or j >= len(row):
             raise BlockError("position outside the table row")
         if row[j] < 0:
-            if pos % block_size != 0 and (j == 0 or row[j - 1] < 0):
+            # a block opens only at its first slot, right after the previous one
+            if pos % block_size != 0 or (j > 0 and row[j - 1] < 0):
                 raise BlockError("gap in the table row")
             (new,) = self.allocate(1, None if chosen is None else [chosen])
             row[j] = new

@@ -1,0 +1,276 @@
+"""ctypes binding of libpgd (include/pgd.h).  Argument marshalling only: every
+step of the path runs in the library's CUDA kernels; there is no fallback.
+The library is loaded on first use and a missing build is an error."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+HEAD_DIM = 128
+
+# status codes (pgd_status)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_OUT_OF_BLOCKS, ERR_WORKSPACE, ERR_CUDA, \
+    ERR_BLOCK_STATE = range(7)
+# device error bits (PGD_DEVERR_*)
+DEVERR_BAD_BLOCK_ID, DEVERR_BAD_CONTEXT, DEVERR_BAD_POSITION, DEVERR_TIMEOUT = 1, 2, 4, 8
+
+#: every symbol include/pgd.h declares, with (argtypes, restype)
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "pgd_status_string": ([_I], ctypes.c_char_p),
+    "pgd_last_error_detail": ([], ctypes.c_char_p),
+    "pgd_version": ([], _I),
+    "pgd_kv_append": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "pgd_attention_workspace_size": ([_I, _I, _I, _I, _I], _Z),
+    "pgd_paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                    _P, _Z, _P], _I),
+    "pgd_attention_grid": ([_I, _I, _I, _I, _I], _I),
+    "pgd_decode_step": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                         _I, _I, _F, _I, _P, _Z, _P], _I),
+    "pgd_copy_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
+    "pgd_device_errors": ([_P, _I, _P], _I),
+    "pgd_alloc_create": ([_I, _P], _I),
+    "pgd_alloc_destroy": ([_P], None),
+    "pgd_alloc_allocate": ([_P, _I, _P], _I),
+    "pgd_alloc_share": ([_P, _P, _I], _I),
+    "pgd_alloc_release": ([_P, _P, _I], _I),
+    "pgd_alloc_refcount": ([_P, _I], _I),
+    "pgd_alloc_num_free": ([_P], _I),
+    "pgd_alloc_num_blocks": ([_P], _I),
+    "pgd_alloc_append_slot": ([_P, _P, _I, _I, _I, _P, _P], _I),
+    "pgd_alloc_fork": ([_P, _P, _I, _I, _P, _I], _I),
+    "pgd_validate_tables": ([_P, _P, _I, _I, _I, _I], _I),
+}
+
+
+class PGDError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__("pgd status %d: %s" % (status, detail))
+        self.status = status
+        self.detail = detail
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpgd.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    "libpgd.so is not built (%s); run paged_gqa_decode_kv_gb300.build.build() "
+                    "or __graft_entry__.build()" % path)
+            L = ctypes.CDLL(path)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+        return _lib
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        L = lib()
+        raise PGDError(status, "%s: %s" % (L.pgd_status_string(status).decode(),
+                                           L.pgd_last_error_detail().decode()))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, name: str, cuda: bool = True) -> None:
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if cuda and not t.is_cuda:
+        raise ValueError("%s must be on a CUDA device" % name)
+
+
+def _cache_dims(k_cache: torch.Tensor) -> Tuple[int, int, int, int]:
+    if k_cache.dim() != 4:
+        raise ValueError("k_cache must be [NB][n_kv][bs][d]")
+    NB, n_kv, bs, d = k_cache.shape
+    return NB, n_kv, bs, d
+
+
+# --------------------------------------------------------------------- GPU ops
+def kv_append(k_new, v_new, k_cache, v_cache, block_tables, positions, stream=None) -> None:
+    """Write k_new/v_new [B][n_kv][d] at logical positions[b] of every sequence."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(positions, torch.int32, "positions")
+    NB, n_kv, bs, d = _cache_dims(k_cache)
+    B, MB = block_tables.shape
+    _check(lib().pgd_kv_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                               _ptr(block_tables), _ptr(positions), B, n_kv, d, bs, MB, NB,
+                               _stream(stream)))
+
+
+def workspace_size(B: int, n_q: int, n_kv: int, num_splits: int = 0, d: int = HEAD_DIM) -> int:
+    return int(lib().pgd_attention_workspace_size(B, n_q, n_kv, d, num_splits))
+
+
+def make_workspace(B: int, n_q: int, n_kv: int, num_splits: int = 0, device=None) -> torch.Tensor:
+    """A zero-filled workspace for these shapes (torch allocations are
+    256-byte aligned)."""
+    n = max(1, workspace_size(B, n_q, n_kv, num_splits))
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def attention_grid(B: int, n_q: int, n_kv: int, bs: int, num_splits: int = 0) -> int:
+    return int(lib().pgd_attention_grid(B, n_q, n_kv, bs, num_splits))
+
+
+def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """out[B][n_q][d] (bf16) = paged decode attention of q over the cache."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, n_q, d = q.shape
+    NB, n_kv, bs, d2 = _cache_dims(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = make_workspace(B, n_q, n_kv, num_splits, q.device)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_paged_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        B, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def decode_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d, v_new_d,
+                context_lens_d, k_cache, v_cache, block_tables, scale: float, num_splits: int,
+                workspace: torch.Tensor, stream=None) -> None:
+    """One decode step with host (pinned) inputs/outputs: H2D copies, append at
+    context_lens - 1, attention, D2H copy of the output; all on `stream`."""
+    for t, n in ((out_h, "out_h"), (q_h, "q_h"), (k_new_h, "k_new_h"), (v_new_h, "v_new_h")):
+        _need(t, torch.bfloat16, n, cuda=False)
+    _need(context_lens_h, torch.int32, "context_lens_h", cuda=False)
+    B, n_q, d = q_h.shape
+    NB, n_kv, bs, _ = _cache_dims(k_cache)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_decode_step(
+        _ptr(out_h), _ptr(q_h), _ptr(k_new_h), _ptr(v_new_h), _ptr(context_lens_h), _ptr(out_d),
+        _ptr(q_d), _ptr(k_new_d), _ptr(v_new_d), _ptr(context_lens_d), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), B, n_q, n_kv, d, bs, MB, NB, float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def copy_blocks(k_cache, v_cache, src_ids, dst_ids, stream=None) -> None:
+    """Copy whole physical blocks src_ids[i] -> dst_ids[i] (device int32)."""
+    _need(k_cache, torch.bfloat16, "k_cache")
+    _need(v_cache, torch.bfloat16, "v_cache")
+    _need(src_ids, torch.int32, "src_ids")
+    _need(dst_ids, torch.int32, "dst_ids")
+    NB, n_kv, bs, d = _cache_dims(k_cache)
+    _check(lib().pgd_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_ids), _ptr(dst_ids),
+                                 src_ids.numel(), n_kv, d, bs, NB, _stream(stream)))
+
+
+def device_errors(clear: bool = True, stream=None) -> int:
+    """Wait for `stream` and return (then clear) the device error bits."""
+    v = ctypes.c_int32(0)
+    _check(lib().pgd_device_errors(ctypes.addressof(v), 1 if clear else 0, _stream(stream)))
+    return int(v.value)
+
+
+# ------------------------------------------------------------ host allocator
+class BlockAllocator:
+    """Host pool of physical block ids with reference counts (pgd_alloc_*)."""
+
+    def __init__(self, num_blocks: int):
+        h = ctypes.c_void_p()
+        _check(lib().pgd_alloc_create(int(num_blocks), ctypes.addressof(h)))
+        self._h = h
+
+    def close(self) -> None:
+        if self._h:
+            lib().pgd_alloc_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _arr(ids: Sequence[int]):
+        return (ctypes.c_int32 * max(1, len(ids)))(*ids)
+
+    def allocate(self, n: int) -> list:
+        buf = (ctypes.c_int32 * max(1, n))()
+        _check(lib().pgd_alloc_allocate(self._h, int(n), buf))
+        return list(buf[:n])
+
+    def share(self, ids: Sequence[int]) -> None:
+        _check(lib().pgd_alloc_share(self._h, self._arr(ids), len(ids)))
+
+    def release(self, ids: Sequence[int]) -> None:
+        _check(lib().pgd_alloc_release(self._h, self._arr(ids), len(ids)))
+
+    def refcount(self, i: int) -> int:
+        return int(lib().pgd_alloc_refcount(self._h, int(i)))
+
+    @property
+    def num_free(self) -> int:
+        return int(lib().pgd_alloc_num_free(self._h))
+
+    @property
+    def num_blocks(self) -> int:
+        return int(lib().pgd_alloc_num_blocks(self._h))
+
+    def append_slot(self, row: list, pos: int, block_size: int) -> Tuple[int, int]:
+        """Make position `pos` of table `row` writable (row updated in place);
+        returns the (src, dst) copy-on-write pair or (-1, -1)."""
+        buf = (ctypes.c_int32 * len(row))(*row)
+        src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+        _check(lib().pgd_alloc_append_slot(self._h, buf, len(row), int(block_size), int(pos),
+                                           ctypes.addressof(src), ctypes.addressof(dst)))
+        row[:] = list(buf)
+        return int(src.value), int(dst.value)
+
+    def fork(self, src_row: Sequence[int], n_tokens: int, block_size: int, dst_row: list) -> None:
+        s = (ctypes.c_int32 * len(src_row))(*src_row)
+        d = (ctypes.c_int32 * len(dst_row))(*dst_row)
+        _check(lib().pgd_alloc_fork(self._h, s, int(n_tokens), int(block_size), d, len(dst_row)))
+        dst_row[:] = list(d)
+
+
+def validate_tables(block_tables_h: torch.Tensor, context_lens_h: torch.Tensor, num_blocks: int,
+                    block_size: int) -> None:
+    """Host check of host copies of the tables and lengths (raises PGDError)."""
+    t = block_tables_h.contiguous().to(torch.int32).cpu()
+    c = context_lens_h.contiguous().to(torch.int32).cpu()
+    B, MB = t.shape
+    _check(lib().pgd_validate_tables(_ptr(t), _ptr(c), B, MB, int(num_blocks), int(block_size)))

@@ -1,0 +1,365 @@
+// api.cu -- the C ABI declared in include/pgd.h: argument checks on the host,
+// workspace layout, kernel launches, the host-buffer decode step and the
+// per-device error word.
+#include <cuda_runtime.h>
+
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "pgd_device.cuh"
+
+namespace pgd {
+int attention_ctas_per_sm(int G, int bs, int B);
+cudaError_t attention_launch(const AttnParams &p, int G, int bs, int grid, cudaStream_t stream);
+cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int32_t *tables, const int32_t *pos, int pos_offset, int B,
+                             int n_kv, int bs, int MB, int NB, int32_t *err,
+                             cudaStream_t stream);
+cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src_ids,
+                               const int32_t *dst_ids, int n, int n_kv, int bs, int NB,
+                               int32_t *err, cudaStream_t stream);
+void set_error_detail(const char *msg);
+void clear_error_detail();
+const char *error_detail();
+}  // namespace pgd
+
+using namespace pgd;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// Automatic grids never exceed this many CTAs, so a workspace sized for it
+// serves every device.
+constexpr int kAutoMaxCtas = 2048;
+constexpr size_t kWsAlign = 256;
+
+pgd_status fail(pgd_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  set_error_detail(buf);
+  return s;
+}
+
+pgd_status ok() {
+  clear_error_detail();
+  return PGD_OK;
+}
+
+pgd_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(PGD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// The per-device error word lives in this translation unit; its device
+// address is looked up once per device.
+__device__ int32_t g_device_error_word;
+
+std::mutex g_mu;
+int32_t *g_err_ptr[kMaxDevices] = {};
+
+pgd_status error_word(int32_t **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PGD_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    g_err_ptr[dev] = static_cast<int32_t *>(p);
+  }
+  *out = g_err_ptr[dev];
+  return PGD_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool supported_group(int G) { return G == 1 || G == 2 || G == 4 || G == 8; }
+bool supported_bs(int bs) { return bs == 16 || bs == 32; }
+
+pgd_status check_cache_shape(int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB) {
+  if (n_kv <= 0 || MB <= 0 || NB <= 0 || bs <= 0)
+    return fail(PGD_ERR_INVALID_ARG, "n_kv, bs, MB and NB must be positive");
+  if (d != kHeadDim) return fail(PGD_ERR_UNSUPPORTED, "d = %d (only 128 is built)", d);
+  if (!supported_bs(bs)) return fail(PGD_ERR_UNSUPPORTED, "block size %d (16 or 32)", bs);
+  if ((long long)MB * bs > 0x7fffffffLL)
+    return fail(PGD_ERR_INVALID_ARG, "MB * bs overflows int32");
+  return PGD_OK;
+}
+
+struct WsLayout {
+  size_t counters, part_ml, part_o, total;
+  long long slots;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+long long grid_upper_bound(int32_t B, int32_t n_kv, int32_t num_splits) {
+  if (num_splits > 0) return (long long)num_splits * B * n_kv;
+  return kAutoMaxCtas;
+}
+
+WsLayout ws_layout(int32_t B, int32_t n_q, int32_t n_kv, int32_t num_splits) {
+  WsLayout L;
+  const int G = n_q / n_kv;
+  const long long units = (long long)B * n_kv;
+  L.slots = units + grid_upper_bound(B, n_kv, num_splits);
+  L.counters = 0;
+  L.part_ml = round_up((size_t)units * 4, kWsAlign);
+  L.part_o = L.part_ml + round_up((size_t)L.slots * G * 2 * 4, kWsAlign);
+  L.total = L.part_o + (size_t)L.slots * G * kHeadDim * 4;
+  return L;
+}
+
+std::map<std::tuple<int, int, int, int>, int> g_occ;
+
+pgd_status auto_grid(int G, int bs, int B, int *grid) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  const int bucket = (B + 255) / 256;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto key = std::make_tuple(dev, G, bs, bucket);
+  auto it = g_occ.find(key);
+  if (it == g_occ.end()) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    int per_sm = attention_ctas_per_sm(G, bs, bucket * 256);
+    if (per_sm <= 0) return fail(PGD_ERR_CUDA, "occupancy query failed for G=%d bs=%d", G, bs);
+    long long g = (long long)sms * per_sm;
+    if (g > kAutoMaxCtas) g = kAutoMaxCtas;
+    it = g_occ.emplace(key, (int)g).first;
+  }
+  *grid = it->second;
+  return PGD_OK;
+}
+
+pgd_status check_attention_args(const void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *tables, const int32_t *ctx,
+                                 int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                 int32_t MB, int32_t NB, float scale, int32_t num_splits) {
+  if (B < 0) return fail(PGD_ERR_INVALID_ARG, "B = %d", B);
+  if (B > PGD_MAX_BATCH) return fail(PGD_ERR_UNSUPPORTED, "B = %d > %d", B, PGD_MAX_BATCH);
+  pgd_status s = check_cache_shape(n_kv, d, bs, MB, NB);
+  if (s != PGD_OK) return s;
+  if (n_q <= 0 || n_q % n_kv) return fail(PGD_ERR_INVALID_ARG, "n_q %% n_kv != 0");
+  if (!supported_group(n_q / n_kv))
+    return fail(PGD_ERR_UNSUPPORTED, "group size G = %d (1, 2, 4 or 8)", n_q / n_kv);
+  if ((long long)B * MB >= 0x7fffffffLL) return fail(PGD_ERR_INVALID_ARG, "B * MB >= 2^31");
+  if (!(scale > 0.f) || !isfinite(scale)) return fail(PGD_ERR_INVALID_ARG, "scale must be > 0");
+  if (num_splits < 0) return fail(PGD_ERR_INVALID_ARG, "num_splits < 0");
+  if (num_splits > 0 && (long long)num_splits * B * n_kv > (1LL << 30))
+    return fail(PGD_ERR_INVALID_ARG, "num_splits too large");
+  if (B == 0) return PGD_OK;
+  if (!out || !q || !k_cache || !v_cache || !tables || !ctx)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  if (!aligned(tables, 4) || !aligned(ctx, 4))
+    return fail(PGD_ERR_INVALID_ARG, "int32 arrays must be 4-byte aligned");
+  return PGD_OK;
+}
+
+pgd_status launch_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *tables, const int32_t *ctx, int32_t B, int32_t n_q,
+                            int32_t n_kv, int32_t bs, int32_t MB, int32_t NB, float scale,
+                            int32_t num_splits, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  const WsLayout L = ws_layout(B, n_q, n_kv, num_splits);
+  if (!workspace) return fail(PGD_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, kWsAlign)) return fail(PGD_ERR_WORKSPACE, "workspace not 256-aligned");
+  if (workspace_bytes < L.total)
+    return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.total);
+  const int G = n_q / n_kv;
+  int grid = 0;
+  if (num_splits > 0) {
+    grid = (int)((long long)num_splits * B * n_kv);
+  } else {
+    pgd_status s = auto_grid(G, bs, B, &grid);
+    if (s != PGD_OK) return s;
+  }
+  int32_t *err = nullptr;
+  pgd_status s = error_word(&err);
+  if (s != PGD_OK) return s;
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  AttnParams p;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
+  p.v_cache = static_cast<const __nv_bfloat16 *>(v_cache);
+  p.tables = tables;
+  p.ctx = ctx;
+  p.B = B;
+  p.n_q = n_q;
+  p.n_kv = n_kv;
+  p.MB = MB;
+  p.NB = NB;
+  p.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
+  p.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
+  p.part_o = reinterpret_cast<float *>(ws + L.part_o);
+  p.err = err;
+  cudaError_t e = attention_launch(p, G, bs, grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "paged attention launch");
+  return PGD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pgd_status_string(pgd_status s) {
+  switch (s) {
+    case PGD_OK: return "ok";
+    case PGD_ERR_INVALID_ARG: return "invalid argument";
+    case PGD_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PGD_ERR_OUT_OF_BLOCKS: return "out of blocks";
+    case PGD_ERR_WORKSPACE: return "workspace missing or too small";
+    case PGD_ERR_CUDA: return "CUDA error";
+    case PGD_ERR_BLOCK_STATE: return "invalid block state";
+  }
+  return "unknown status";
+}
+
+const char *pgd_last_error_detail(void) { return error_detail(); }
+
+int32_t pgd_version(void) { return 100; }
+
+pgd_status pgd_kv_append(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                         const int32_t *block_tables, const int32_t *positions, int32_t B,
+                         int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB,
+                         void *stream) {
+  if (B < 0) return fail(PGD_ERR_INVALID_ARG, "B = %d", B);
+  pgd_status s = check_cache_shape(n_kv, d, bs, MB, NB);
+  if (s != PGD_OK) return s;
+  if ((long long)B * n_kv > 0x7fffffffLL) return fail(PGD_ERR_INVALID_ARG, "B * n_kv too large");
+  if (B == 0) return ok();
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !positions)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  int32_t *err = nullptr;
+  s = error_word(&err);
+  if (s != PGD_OK) return s;
+  cudaError_t e = kv_append_launch(k_new, v_new, k_cache, v_cache, block_tables, positions, 0, B,
+                                   n_kv, bs, MB, NB, err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return ok();
+}
+
+size_t pgd_attention_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_t d,
+                                    int32_t num_splits) {
+  if (B < 0 || n_kv <= 0 || n_q <= 0 || n_q % n_kv || d != kHeadDim || num_splits < 0) return 0;
+  return ws_layout(B, n_q, n_kv, num_splits).total;
+}
+
+int32_t pgd_attention_grid(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t num_splits) {
+  if (B <= 0 || n_kv <= 0 || n_q <= 0 || n_q % n_kv || num_splits < 0) return 0;
+  if (!supported_group(n_q / n_kv) || !supported_bs(bs)) return 0;
+  if (num_splits > 0) return (int32_t)((long long)num_splits * B * n_kv);
+  int grid = 0;
+  if (auto_grid(n_q / n_kv, bs, B, &grid) != PGD_OK) return 0;
+  return grid;
+}
+
+pgd_status pgd_paged_decode_attention(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      const int32_t *context_lens, int32_t B, int32_t n_q,
+                                      int32_t n_kv, int32_t d, int32_t bs, int32_t MB,
+                                      int32_t NB, float scale, int32_t num_splits,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
+  pgd_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, B,
+                                      n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  s = launch_attention(out, q, k_cache, v_cache, block_tables, context_lens, B, n_q, n_kv, bs,
+                       MB, NB, scale, num_splits, workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream));
+  return s == PGD_OK ? ok() : s;
+}
+
+pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
+                           const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
+                           void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
+                           const int32_t *block_tables, int32_t B, int32_t n_q, int32_t n_kv,
+                           int32_t d, int32_t bs, int32_t MB, int32_t NB, float scale,
+                           int32_t num_splits, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+  pgd_status s = check_attention_args(out_d, q_d, k_cache, v_cache, block_tables, context_lens_d,
+                                      B, n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  if (!out_h || !q_h || !k_new_h || !v_new_h || !context_lens_h || !k_new_d || !v_new_d)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_new_d, 16) || !aligned(v_new_d, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t qb = (size_t)B * n_q * kHeadDim * 2, kvb = (size_t)B * n_kv * kHeadDim * 2;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(k_new_d, k_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(v_new_d, v_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4, cudaMemcpyHostToDevice,
+                           st)) != cudaSuccess)
+    return cuda_fail(e, "decode step: host-to-device copy");
+  int32_t *err = nullptr;
+  s = error_word(&err);
+  if (s != PGD_OK) return s;
+  e = kv_append_launch(k_new_d, v_new_d, k_cache, v_cache, block_tables, context_lens_d, -1, B,
+                       n_kv, bs, MB, NB, err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode step: kv_append launch");
+  s = launch_attention(out_d, q_d, k_cache, v_cache, block_tables, context_lens_d, B, n_q, n_kv,
+                       bs, MB, NB, scale, num_splits, workspace, workspace_bytes, st);
+  if (s != PGD_OK) return s;
+  if ((e = cudaMemcpyAsync(out_h, out_d, qb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "decode step: device-to-host copy");
+  return ok();
+}
+
+pgd_status pgd_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_ids,
+                           const int32_t *dst_ids, int32_t n, int32_t n_kv, int32_t d,
+                           int32_t bs, int32_t NB, void *stream) {
+  if (n < 0) return fail(PGD_ERR_INVALID_ARG, "n = %d", n);
+  pgd_status s = check_cache_shape(n_kv, d, bs, 1, NB);
+  if (s != PGD_OK) return s;
+  if (n == 0) return ok();
+  if (!k_cache || !v_cache || !src_ids || !dst_ids) return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PGD_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  int32_t *err = nullptr;
+  s = error_word(&err);
+  if (s != PGD_OK) return s;
+  cudaError_t e = copy_blocks_launch(k_cache, v_cache, src_ids, dst_ids, n, n_kv, bs, NB, err,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return ok();
+}
+
+pgd_status pgd_device_errors(int32_t *flags, int32_t clear, void *stream) {
+  if (!flags) return fail(PGD_ERR_INVALID_ARG, "flags is NULL");
+  int32_t *err = nullptr;
+  pgd_status s = error_word(&err);
+  if (s != PGD_OK) return s;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  e = cudaMemcpy(flags, err, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (clear) {
+    e = cudaMemset(err, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  }
+  return ok();
+}
+
+}  // extern "C"

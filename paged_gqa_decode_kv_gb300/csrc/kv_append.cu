@@ -1,0 +1,95 @@
+// kv_append.cu -- write each sequence's new K/V into its paged slot, and the
+// device half of copy-on-write (whole-block copies).
+//
+// kv_append ("LLM inference systems engineering", 2.1.3: the step commits the
+// pending token's K/V; "The math of Transformer inference", section 1: decode
+// appends its own K and V to the cache): for sequence b at position p,
+//   k_cache[table[b][p / bs]][g][p % bs][:] = k_new[b][g][:]   (and V)
+// One warp per (sequence, KV head): lanes 0-15 move the 256-byte K row and
+// lanes 16-31 the V row, 16 bytes each.  A pure copy, bit exact.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "pgd_device.cuh"
+
+namespace pgd {
+
+__global__ void __launch_bounds__(128)
+kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                 uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                 const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
+                 int pos_offset, int B, int n_kv, int bs, int MB, int NB, int32_t *err) {
+  constexpr int kVecPerRow = kHeadDim * 2 / 16;  // 16 uint4 per 256-byte row
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= B * n_kv) return;
+  const int b = row / n_kv, g = row % n_kv;
+  const int p = __ldg(pos + b) + pos_offset;
+  if (p < 0 || p >= MB * bs) {
+    if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_POSITION);
+    return;
+  }
+  const int blk = __ldg(tables + (size_t)b * MB + p / bs);
+  if ((unsigned)blk >= (unsigned)NB) {
+    if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_BLOCK_ID);
+    return;
+  }
+  const size_t dst = ((((size_t)blk * n_kv + g) * bs) + (p % bs)) * kVecPerRow;
+  const size_t src = (size_t)row * kVecPerRow;
+  const int v = lane & 15;
+  if (lane < 16)
+    k_cache[dst + v] = __ldg(k_new + src + v);
+  else
+    v_cache[dst + v] = __ldg(v_new + src + v);
+}
+
+cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int32_t *tables, const int32_t *pos, int pos_offset, int B,
+                             int n_kv, int bs, int MB, int NB, int32_t *err,
+                             cudaStream_t stream) {
+  const int rows = B * n_kv;
+  if (rows == 0) return cudaSuccess;
+  const int grid = (rows + 3) / 4;
+  kv_append_kernel<<<grid, 128, 0, stream>>>(
+      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), tables, pos, pos_offset, B,
+      n_kv, bs, MB, NB, err);
+  return cudaGetLastError();
+}
+
+// Copy-on-write ("Module 10: inference and serving", section "Share only
+// identical state"): block src_ids[i] -> dst_ids[i], every KV head and slot,
+// K and V.  grid.x = pairs, grid.y = chunks of the block; 16-byte vectors.
+__global__ void __launch_bounds__(256)
+copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                   const int32_t *__restrict__ src_ids, const int32_t *__restrict__ dst_ids,
+                   int block_vecs, int NB, int32_t *err) {
+  const int i = blockIdx.x;
+  const int src = __ldg(src_ids + i), dst = __ldg(dst_ids + i);
+  if ((unsigned)src >= (unsigned)NB || (unsigned)dst >= (unsigned)NB) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(err, PGD_DEVERR_BAD_BLOCK_ID);
+    return;
+  }
+  const size_t s0 = (size_t)src * block_vecs, d0 = (size_t)dst * block_vecs;
+  for (int v = blockIdx.y * blockDim.x + threadIdx.x; v < block_vecs;
+       v += gridDim.y * blockDim.x) {
+    k_cache[d0 + v] = k_cache[s0 + v];
+    v_cache[d0 + v] = v_cache[s0 + v];
+  }
+}
+
+cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src_ids,
+                               const int32_t *dst_ids, int n, int n_kv, int bs, int NB,
+                               int32_t *err, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int block_vecs = n_kv * bs * kHeadDim * 2 / 16;
+  int chunks = (block_vecs + 255) / 256;
+  if (chunks > 64) chunks = 64;
+  dim3 grid(n, chunks);
+  copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4 *>(k_cache),
+                                               static_cast<uint4 *>(v_cache), src_ids, dst_ids,
+                                               block_vecs, NB, err);
+  return cudaGetLastError();
+}
+
+}  // namespace pgd

@@ -1,0 +1,132 @@
+// pgd_device.cuh -- device-side helpers shared by the libpgd kernels:
+// mbarrier and bulk-copy (TMA engine) wrappers in inline PTX, bounded waits,
+// bf16 unpacking and the kernel parameter blocks.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pgd.h"
+
+namespace pgd {
+
+constexpr int kHeadDim = 128;
+constexpr unsigned kFullMask = 0xffffffffu;
+// A bounded wait gives up after this long (ns of %globaltimer) and reports
+// PGD_DEVERR_TIMEOUT instead of hanging the GPU.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// ---- mbarrier (shared::cta) ------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Wait until the phase with the given parity has completed, or give up after
+// kWaitLimitNs.  Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// ---- bulk copy global -> shared through the TMA engine ---------------------
+// L2 policy for data read exactly once per call (the KV stream).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// dst (shared) and src (global) 16-byte aligned, bytes a multiple of 16.
+// Completion is signalled as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// ---- bf16 helpers ----------------------------------------------------------
+// Two bf16 packed in one 32-bit word (element 2i in the low half).  bf16 is
+// the upper half of a binary32, so widening is a shift or a mask.
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ void unpack8(const uint4 &r, float (&f)[8]) {
+  f[0] = bf16lo(r.x); f[1] = bf16hi(r.x);
+  f[2] = bf16lo(r.y); f[3] = bf16hi(r.y);
+  f[4] = bf16lo(r.z); f[5] = bf16hi(r.z);
+  f[6] = bf16lo(r.w); f[7] = bf16hi(r.w);
+}
+
+__device__ __forceinline__ void unpack4(const uint2 &r, float (&f)[4]) {
+  f[0] = bf16lo(r.x); f[1] = bf16hi(r.x);
+  f[2] = bf16lo(r.y); f[3] = bf16hi(r.y);
+}
+
+// ---- kernel parameter blocks ----------------------------------------------
+struct AttnParams {
+  __nv_bfloat16 *out;            // [B][n_q][D]
+  const __nv_bfloat16 *q;        // [B][n_q][D]
+  const __nv_bfloat16 *k_cache;  // [NB][n_kv][bs][D]
+  const __nv_bfloat16 *v_cache;
+  const int32_t *tables;         // [B][MB]
+  const int32_t *ctx;            // [B]
+  int B, n_q, n_kv, MB, NB;
+  float qk_scale_log2;           // scale * log2(e): scores live in the log2 domain
+  float *part_o;                 // [slots][G][D]  unnormalised partial outputs
+  float *part_ml;                // [slots][G][2]  partial (max, sum), log2 domain
+  int32_t *counters;             // [B * n_kv]     arrivals per split unit
+  int32_t *err;                  // device error word
+};
+
+}  // namespace pgd

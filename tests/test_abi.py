@@ -1,0 +1,107 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol
+include/pgd.h declares, and rejects bad arguments on the host before any CUDA
+call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_gqa_decode_kv_gb300 as pgd
+from paged_gqa_decode_kv_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pgd.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pgd_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from paged_gqa_decode_kv_gb300 import build
+    build.build()
+    return pgd.lib()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("pgd_kv_append", "pgd_paged_decode_attention", "pgd_attention_workspace_size",
+              "pgd_alloc_create", "pgd_copy_blocks", "pgd_decode_step"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    missing = [n for n in declared_symbols() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_declared_symbol():
+    assert set(declared_symbols()) <= set(_native.SIGNATURES)
+
+
+def test_status_strings(L):
+    for s in range(7):
+        assert L.pgd_status_string(s)
+    assert L.pgd_version() >= 100
+
+
+def _attn(L, **kw):
+    a = dict(out=16, q=16, k=16, v=16, t=16, c=16, B=2, n_q=8, n_kv=2, d=128, bs=16, MB=4, NB=8,
+             scale=0.1, splits=0, ws=None, wsb=0)
+    a.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.pgd_paged_decode_attention(P(a["out"]), P(a["q"]), P(a["k"]), P(a["v"]), P(a["t"]),
+                                        P(a["c"]), a["B"], a["n_q"], a["n_kv"], a["d"], a["bs"],
+                                        a["MB"], a["NB"], a["scale"], a["splits"], P(a["ws"]),
+                                        a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=64), _native.ERR_UNSUPPORTED),
+    (dict(bs=8), _native.ERR_UNSUPPORTED),
+    (dict(n_q=6, n_kv=2), _native.ERR_UNSUPPORTED),      # G = 3
+    (dict(n_q=32, n_kv=2), _native.ERR_UNSUPPORTED),     # G = 16
+    (dict(n_q=7, n_kv=2), _native.ERR_INVALID_ARG),
+    (dict(B=-1), _native.ERR_INVALID_ARG),
+    (dict(B=5000), _native.ERR_UNSUPPORTED),
+    (dict(scale=0.0), _native.ERR_INVALID_ARG),
+    (dict(scale=float("inf")), _native.ERR_INVALID_ARG),
+    (dict(q=None), _native.ERR_INVALID_ARG),
+    (dict(q=24), _native.ERR_INVALID_ARG),                # misaligned
+    (dict(NB=0), _native.ERR_INVALID_ARG),
+    (dict(splits=-1), _native.ERR_INVALID_ARG),
+    (dict(ws=None, wsb=0), _native.ERR_WORKSPACE),
+    (dict(ws=256, wsb=16), _native.ERR_WORKSPACE),
+    (dict(ws=264, wsb=1 << 30), _native.ERR_WORKSPACE),   # misaligned workspace
+])
+def test_attention_rejects_on_host(L, kw, status):
+    assert _attn(L, **kw) == status
+    assert L.pgd_last_error_detail()
+
+
+def test_empty_batch_is_a_noop(L):
+    assert _attn(L, B=0, out=None, q=None, k=None, v=None, t=None, c=None) == 0
+
+
+def test_kv_append_rejects_on_host(L):
+    P = ctypes.c_void_p
+    assert L.pgd_kv_append(P(16), P(16), P(16), P(16), P(16), P(16), 2, 2, 64, 16, 4, 8,
+                           None) == _native.ERR_UNSUPPORTED
+    assert L.pgd_kv_append(P(16), P(16), P(16), P(16), P(16), P(16), 2, 2, 128, 12, 4, 8,
+                           None) == _native.ERR_UNSUPPORTED
+    assert L.pgd_kv_append(None, P(16), P(16), P(16), P(16), P(16), 2, 2, 128, 16, 4, 8,
+                           None) == _native.ERR_INVALID_ARG
+    assert L.pgd_kv_append(P(18), P(16), P(16), P(16), P(16), P(16), 2, 2, 128, 16, 4, 8,
+                           None) == _native.ERR_INVALID_ARG
+    assert L.pgd_kv_append(None, None, None, None, None, None, 0, 2, 128, 16, 4, 8, None) == 0
+
+
+def test_workspace_size_grows_with_splits(L):
+    a = pgd.workspace_size(16, 32, 8, 0)
+    b = pgd.workspace_size(16, 32, 8, 64)
+    assert 0 < a < b
+    assert pgd.workspace_size(16, 32, 8, 0, d=64) == 0
