@@ -145,6 +145,36 @@ pgd_status pgd_paged_decode_attention(void *out, const void *q, const void *k_ca
  * arguments on the current device (0 on invalid arguments). */
 int32_t pgd_attention_grid(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t num_splits);
 
+/* Size of the library's own device scratch array used by
+ * pgd_paged_decode_attention_noalloc (16 MiB on every GPU that loads the
+ * library, held until the process exits). */
+#define PGD_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* pgd_paged_decode_attention for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for callers
+ * such as plugins or callbacks running inside another runtime's execution
+ * step, which receive inputs and outputs but no scratch and must not call
+ * cudaMalloc/cudaFree there (those calls can synchronize the device, fail
+ * under the host runtime's memory budget, and compete with its allocator).
+ * Same arguments, semantics and results as pgd_paged_decode_attention, minus
+ * the workspace: the split-merge scratch lives in a fixed __device__ array of
+ * PGD_NOALLOC_SCRATCH_BYTES inside the library.  Sizes whose workspace
+ * (pgd_attention_workspace_size) exceeds that array are rejected with
+ * PGD_ERR_WORKSPACE.  No device memory is allocated by this call.
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Every call on a device shares the one array and leaves its
+ * contents behind; the call clears the part that must start at zero (with
+ * cudaMemsetAsync on `stream`) before launching.  Calls that overlap on the
+ * same GPU -- on different streams, say -- race on the array and must be
+ * serialised by the caller. */
+pgd_status pgd_paged_decode_attention_noalloc(void *out, const void *q, const void *k_cache,
+                                              const void *v_cache, const int32_t *block_tables,
+                                              const int32_t *context_lens, int32_t B, int32_t n_q,
+                                              int32_t n_kv, int32_t d, int32_t bs, int32_t MB,
+                                              int32_t NB, float scale, int32_t num_splits,
+                                              void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* one decode step with host inputs and outputs                            */
 /* ---------------------------------------------------------------------- */

@@ -7,11 +7,13 @@ library; the first call does, and fails loudly if it was not built.
 """
 from .inputs import WORKLOADS, Workload, PagedBatch, make_batch, make_workload  # noqa: F401
 from ._native import (  # noqa: F401
-    PGDError, BlockAllocator, kv_append, paged_decode_attention, decode_step, copy_blocks,
+    PGDError, BlockAllocator, kv_append, paged_decode_attention,
+    paged_decode_attention_noalloc, decode_step, copy_blocks,
     device_errors, workspace_size, make_workspace, attention_grid, validate_tables, lib,
     library_path)
 
 __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "PGDError",
-           "BlockAllocator", "kv_append", "paged_decode_attention", "decode_step", "copy_blocks",
+           "BlockAllocator", "kv_append", "paged_decode_attention",
+           "paged_decode_attention_noalloc", "decode_step", "copy_blocks",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
            "validate_tables", "lib", "library_path"]

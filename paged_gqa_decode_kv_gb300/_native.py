@@ -34,6 +34,8 @@ SIGNATURES = {
     "pgd_paged_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
                                     _P, _Z, _P], _I),
     "pgd_attention_grid": ([_I, _I, _I, _I, _I], _I),
+    "pgd_paged_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                            _F, _I, _P], _I),
     "pgd_decode_step": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                          _I, _I, _F, _I, _P, _Z, _P], _I),
     "pgd_copy_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
@@ -164,6 +166,25 @@ def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         B, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                   scale: float, num_splits: int = 0, stream=None) -> torch.Tensor:
+    """paged_decode_attention without a workspace argument, for callers that
+    cannot allocate device memory: the library keeps the scratch in its own
+    fixed device array (shared by every call on a device; calls that overlap
+    on one GPU race).  `out` must be given -- this call allocates nothing."""
+    for t, n in ((out, "out"), (q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, n_q, d = q.shape
+    NB, n_kv, bs, _ = _cache_dims(k_cache)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_paged_decode_attention_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        B, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _stream(stream)))
     return out
 
 

@@ -216,6 +216,29 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
 
 }  // namespace
 
+namespace pgd {
+// Entry for other translation units of the library: the same checks and
+// launch as pgd_paged_decode_attention, with the scratch supplied by the
+// caller, and the scratch size the call needs.
+pgd_status paged_attention_with_scratch(void *out, const void *q, const void *k_cache,
+                                        const void *v_cache, const int32_t *tables,
+                                        const int32_t *ctx, int32_t B, int32_t n_q, int32_t n_kv,
+                                        int32_t d, int32_t bs, int32_t MB, int32_t NB,
+                                        float scale, int32_t num_splits, void *scratch,
+                                        size_t scratch_bytes, cudaStream_t stream) {
+  pgd_status s = check_attention_args(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, d, bs,
+                                      MB, NB, scale, num_splits);
+  if (s != PGD_OK || B == 0) return s;
+  return launch_attention(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, bs, MB, NB, scale,
+                          num_splits, scratch, scratch_bytes, stream);
+}
+
+pgd_status set_status_detail(pgd_status s, const char *msg) {
+  set_error_detail(msg);
+  return s;
+}
+}  // namespace pgd
+
 extern "C" {
 
 const char *pgd_status_string(pgd_status s) {
