@@ -174,14 +174,14 @@ def hbm_peak():
 
 
 def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, or None if the
-    kernel source changed since that capture."""
+    """DRAM bytes per launch from the committed ncu summary of the attention
+    kernel, or None if the kernel source changed since that capture."""
     try:
         text = open(PROFILE_SUMMARY).read()
     except OSError:
         return None
     m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    m_sha = re.search(r"attention_cu_sha256:\s*([0-9a-f]{64})", text)
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not (m_bytes and m_sha):
         return None
     cur = hashlib.sha256(open(ATTENTION_SRC, "rb").read()).hexdigest()
@@ -236,6 +236,7 @@ def config_block(pb, name, grid, splits):
             "n_q": pb.n_q, "n_kv": pb.n_kv, "head_dim": pb.head_dim,
             "block_size": pb.block_size, "kv_dtype": "bf16",
             "splits": "auto" if splits == 0 else splits, "grid_ctas": grid,
+            "kv_layout": "tiled 8x8 core matrices per (block, head)",
             "l2": "inputs %.0f MB > 129 MB L2, no flush" % (pb.k_cache.numel() * 4 / 1e6)
             if pb.k_cache.numel() * 4 > L2_BYTES else "working set fits L2 (hot)"}
 
@@ -348,7 +349,7 @@ def run_ours(args, rank, world, local):
         "seq_layer_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": {"nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
                             peak_kind: round(100 * value / world / peak, 2)},
-        "roofline": {"bound": "hbm", "kernel": "paged_attention_kernel",
+        "roofline": {"bound": "hbm", "kernel": "pgd::tc::paged_attention_kernel (tcgen05)",
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(), "launch_ms": round(attn_ms, 5),

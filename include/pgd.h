@@ -15,9 +15,16 @@
  *          physical blocks"; "Ch. 6 Inference efficiency and serving", 6.4)
  *   NB     physical blocks in the pool; MB = width of a block-table row
  *
- * Layouts (row-major, all device memory unless marked host):
- *   k_cache, v_cache  bf16 [NB][n_kv][bs][d]   one (block, KV head) tile is a
- *                     contiguous bs*d*2-byte run
+ * Layouts (all device memory unless marked host):
+ *   k_cache, v_cache  bf16 pools of NB blocks: [NB][n_kv][tile], one tile per
+ *                     (block, KV head), a contiguous bs*d*2-byte run holding
+ *                     the bs tokens x d dims as 8 x 8 core matrices --
+ *                     element (slot s, dim i) at ((s/8)*(d/8) + i/8)*64 +
+ *                     (s%8)*8 + i%8, i.e. [bs/8][d/8][8][8].  The pages fix
+ *                     only the logical shape (B, n_kv, T, d) and the block
+ *                     table; this tiling lets one bulk copy per tile land
+ *                     directly as a tensor-core operand.  bs must be a
+ *                     multiple of 8.
  *   block_tables      int32 [B][MB]  logical block j of sequence b lives in
  *                     physical block block_tables[b][j]; entries past the
  *                     sequence's last block are never read

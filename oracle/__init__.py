@@ -89,6 +89,14 @@ def _u16(a) -> np.ndarray:
     return np.ascontiguousarray(a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
 
 
+def _tile_dims(cache: np.ndarray):
+    """(NB, n_kv, bs, d) of a pool stored as [NB][n_kv][bs/8][d/8][8][8]."""
+    if cache.ndim != 6 or cache.shape[4:] != (8, 8):
+        raise ValueError("cache must be [NB][n_kv][bs/8][d/8][8][8] (8x8 core-matrix tiles)")
+    NB, n_kv, rg, nc = cache.shape[:4]
+    return NB, n_kv, rg * 8, nc * 8
+
+
 def _i32(a) -> np.ndarray:
     if isinstance(a, np.ndarray):
         return np.ascontiguousarray(a, dtype=np.int32)
@@ -106,13 +114,14 @@ def threads_used(n_threads: int, rows: int) -> int:
 def paged_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                     n_threads: int = 0, mutation: int = 0) -> np.ndarray:
     """float64 out[B][n_q][d] of single-token decode attention over the paged
-    cache.  q: [B][n_q][d] bf16; k_cache, v_cache: [NB][n_kv][bs][d] bf16;
+    cache.  q: [B][n_q][d] bf16; k_cache, v_cache: [NB][n_kv][bs/8][d/8][8][8]
+    bf16 (each (block, head) tile as 8x8 core matrices);
     block_tables: [B][MB] int32; context_lens: [B] int32 (includes the token
     just appended).  Raises ValueError on an invalid length or block id."""
     qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
     ta, ca = _i32(block_tables), _i32(context_lens)
     B, n_q, d = qa.shape
-    NB, n_kv, bs, d2 = ka.shape
+    NB, n_kv, bs, d2 = _tile_dims(ka)
     assert d2 == d and va.shape == ka.shape and ta.shape[0] == B and ca.shape == (B,)
     MB = ta.shape[1]
     out = np.zeros((B, n_q, d), dtype=np.float64)
@@ -130,7 +139,7 @@ def attention_weights(q, k_cache, block_tables, context_lens, b: int, h: int,
     qa, ka = _u16(q), _u16(k_cache)
     ta, ca = _i32(block_tables), _i32(context_lens)
     B, n_q, d = qa.shape
-    NB, n_kv, bs, _ = ka.shape
+    NB, n_kv, bs, _ = _tile_dims(ka)
     w = np.zeros(int(ca[b]), dtype=np.float64)
     st = _load().oracle_attention_weights(_p(w), _p(qa), _p(ka), _p(ta), _p(ca), int(b), int(h),
                                           n_q, n_kv, d, bs, ta.shape[1], NB, float(scale))
@@ -145,7 +154,7 @@ def attention_part(q, k_cache, v_cache, block_tables, b: int, h: int, t0: int, t
     qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
     ta = _i32(block_tables)
     B, n_q, d = qa.shape
-    NB, n_kv, bs, _ = ka.shape
+    NB, n_kv, bs, _ = _tile_dims(ka)
     m = np.zeros(1, dtype=np.float64)
     l = np.zeros(1, dtype=np.float64)
     o = np.zeros(d, dtype=np.float64)
@@ -177,7 +186,7 @@ def kv_append(k_cache, v_cache, k_new, v_new, block_tables, positions):
     vc = _u16(v_cache).copy()
     kn, vn = _u16(k_new), _u16(v_new)
     ta, pa = _i32(block_tables), _i32(positions)
-    NB, n_kv, bs, d = kc.shape
+    NB, n_kv, bs, d = _tile_dims(kc)
     B = kn.shape[0]
     st = _load().oracle_kv_append(_p(kc), _p(vc), _p(kn), _p(vn), _p(ta), _p(pa), B, n_kv, d, bs,
                                   ta.shape[1], NB)

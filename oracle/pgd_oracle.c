@@ -32,6 +32,12 @@
  *    "the KV cache must be sharded too": split the sequence, compute local
  *    attention per part, merge the parts by log-sum-exp.
  *
+ * Physical layout of the pool (the pages fix only the logical shape
+ * (B, n_kv, T, d_head) and the block table, so this is the library's choice):
+ * [NB][n_kv][tile], one tile per (block, KV head) holding bs x d bf16 values
+ * as 8 x 8 core matrices -- element (slot s, dim i) of a tile is at
+ * ((s / 8) * (d / 8) + i / 8) * 64 + (s % 8) * 8 + i % 8.
+ *
  * Readings where the pages are silent (each is listed in the design notes):
  *  - context_lens[b] counts every cached position including the token just
  *    appended; a decode query attends to all of them.
@@ -63,6 +69,12 @@ static double bf16_bits_to_double(uint16_t bits) {
   return (double)f;
 }
 
+/* Offset of element (slot, i) inside one (block, head) tile. */
+static size_t tile_offset(int slot, int i, int d) {
+  return ((size_t)(slot >> 3) * (size_t)(d >> 3) + (size_t)(i >> 3)) * 64 +
+         (size_t)(slot & 7) * 8 + (size_t)(i & 7);
+}
+
 /* ------------------------------------------------------------------ */
 /* kv_append: place one new token per sequence into its paged slot.   */
 /* ------------------------------------------------------------------ */
@@ -70,7 +82,7 @@ static double bf16_bits_to_double(uint16_t bits) {
 /* For every sequence b, the new token sits at logical position
  * positions[b]; its block is table[b][positions[b] / bs] and its slot is
  * positions[b] % bs.  K and V of every KV head are copied bit for bit.
- * Cache layout: [NB][n_kv][bs][d].  New-token layout: [B][n_kv][d].
+ * Cache layout: [NB][n_kv][tile] as above.  New-token layout: [B][n_kv][d].
  * Returns 0, or 1 if a position or a block id is out of range (nothing is
  * written for that sequence). */
 int oracle_kv_append(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
@@ -85,10 +97,12 @@ int oracle_kv_append(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new
     if (blk < 0 || blk >= NB) { status = 1; continue; }
     int slot = pos % bs;
     for (int g = 0; g < n_kv; ++g) {
-      size_t dst = (((size_t)blk * n_kv + g) * bs + slot) * d;
+      size_t tile = ((size_t)blk * n_kv + g) * (size_t)bs * d;
       size_t src = ((size_t)b * n_kv + g) * d;
-      memcpy(k_cache + dst, k_new + src, (size_t)d * sizeof(uint16_t));
-      memcpy(v_cache + dst, v_new + src, (size_t)d * sizeof(uint16_t));
+      for (int i = 0; i < d; ++i) {
+        k_cache[tile + tile_offset(slot, i, d)] = k_new[src + i];
+        v_cache[tile + tile_offset(slot, i, d)] = v_new[src + i];
+      }
     }
   }
   return status;
@@ -112,16 +126,17 @@ typedef struct {
   int status;
 } attn_job;
 
-/* Resolve logical token t of sequence b to the element offset of its
- * row [d] for KV head g, through the block table.  Returns -1 when the table
- * entry is not a valid block id. */
-static long token_row(const attn_job *J, int b, int g, int t) {
+/* Resolve logical token t of sequence b, KV head g, through the block
+ * table: the element offset of its tile and its slot in the tile.  Returns
+ * -1 when the table entry is not a valid block id. */
+static long token_tile(const attn_job *J, int b, int g, int t, int *slot_out) {
   int j = t / J->bs;
   int slot = t % J->bs;
   if (J->mutation == 1) slot = (t + 1) % J->bs;
   int32_t blk = J->tables[(size_t)b * J->MB + j];
   if (blk < 0 || blk >= J->NB) return -1;
-  return (long)((((size_t)blk * J->n_kv + g) * J->bs + slot) * J->d);
+  *slot_out = slot;
+  return (long)(((size_t)blk * J->n_kv + g) * (size_t)J->bs * J->d);
 }
 
 /* One (sequence b, query head h): scores over every cached position,
@@ -148,11 +163,12 @@ static int attend_row(const attn_job *J, int b, int h) {
   /* scores s_t = scale * sum_i q_i k_{t,i} */
   double smax = -INFINITY;
   for (int t = 0; t < n_tok; ++t) {
-    long r = token_row(J, b, g, t);
+    int slot = 0;
+    long r = token_tile(J, b, g, t, &slot);
     if (r < 0) { free(s); return 1; }
     double acc = 0.0;
     for (int i = 0; i < d; ++i)
-      acc += bf16_bits_to_double(qrow[i]) * bf16_bits_to_double(Kc[r + i]);
+      acc += bf16_bits_to_double(qrow[i]) * bf16_bits_to_double(Kc[r + tile_offset(slot, i, d)]);
     s[t] = scale * acc;
     if (J->mutation == 8) s[t] = -s[t];
     if (s[t] > smax) smax = s[t];
@@ -167,9 +183,10 @@ static int attend_row(const attn_job *J, int b, int h) {
   /* out = sum_t w_t v_t */
   for (int i = 0; i < d; ++i) orow[i] = 0.0;
   for (int t = 0; t < n_tok; ++t) {
-    long r = token_row(J, b, g, t);
+    int slot = 0;
+    long r = token_tile(J, b, g, t, &slot);
     double w = s[t] / denom;
-    for (int i = 0; i < d; ++i) orow[i] += w * bf16_bits_to_double(Vc[r + i]);
+    for (int i = 0; i < d; ++i) orow[i] += w * bf16_bits_to_double(Vc[r + tile_offset(slot, i, d)]);
   }
   free(s);
   return 0;
@@ -206,7 +223,8 @@ int oracle_paged_attention(double *out, const uint16_t *q, const uint16_t *k_cac
                            const int32_t *context_lens, int B, int n_q, int n_kv, int d,
                            int bs, int MB, int NB, double scale, int n_threads,
                            int mutation) {
-  if (B < 0 || n_q <= 0 || n_kv <= 0 || n_q % n_kv || d <= 0 || bs <= 0 || MB <= 0 || NB <= 0)
+  if (B < 0 || n_q <= 0 || n_kv <= 0 || n_q % n_kv || d <= 0 || bs <= 0 || MB <= 0 || NB <= 0 ||
+      d % 8 || bs % 8)
     return 1;
   long rows = (long)B * n_q;
   if (rows == 0) return 0;
@@ -246,11 +264,12 @@ int oracle_attention_weights(double *w, const uint16_t *q, const uint16_t *k_cac
   const uint16_t *qrow = q + ((size_t)b * n_q + h) * d;
   double smax = -INFINITY;
   for (int t = 0; t < ctx; ++t) {
-    long r = token_row(&J, b, g, t);
+    int slot = 0;
+    long r = token_tile(&J, b, g, t, &slot);
     if (r < 0) return 1;
     double acc = 0.0;
     for (int i = 0; i < d; ++i)
-      acc += bf16_bits_to_double(qrow[i]) * bf16_bits_to_double(k_cache[r + i]);
+      acc += bf16_bits_to_double(qrow[i]) * bf16_bits_to_double(k_cache[r + tile_offset(slot, i, d)]);
     w[t] = scale * acc;
     if (w[t] > smax) smax = w[t];
   }
@@ -280,22 +299,24 @@ int oracle_attention_part(double *m_out, double *l_out, double *o_out, const uin
   for (int i = 0; i < d; ++i) o_out[i] = 0.0;
   if (t1 > t0) {
     for (int t = t0; t < t1; ++t) {
-      long r = token_row(&J, b, g, t);
+      int slot = 0;
+      long r = token_tile(&J, b, g, t, &slot);
       if (r < 0) return 1;
       double acc = 0.0;
       for (int i = 0; i < d; ++i)
-        acc += bf16_bits_to_double(qrow[i]) * bf16_bits_to_double(k_cache[r + i]);
+        acc += bf16_bits_to_double(qrow[i]) * bf16_bits_to_double(k_cache[r + tile_offset(slot, i, d)]);
       double s = scale * acc;
       if (s > m) m = s;
     }
     for (int t = t0; t < t1; ++t) {
-      long r = token_row(&J, b, g, t);
+      int slot = 0;
+      long r = token_tile(&J, b, g, t, &slot);
       double acc = 0.0;
       for (int i = 0; i < d; ++i)
-        acc += bf16_bits_to_double(qrow[i]) * bf16_bits_to_double(k_cache[r + i]);
+        acc += bf16_bits_to_double(qrow[i]) * bf16_bits_to_double(k_cache[r + tile_offset(slot, i, d)]);
       double p = exp(scale * acc - m);
       l += p;
-      for (int i = 0; i < d; ++i) o_out[i] += p * bf16_bits_to_double(v_cache[r + i]);
+      for (int i = 0; i < d; ++i) o_out[i] += p * bf16_bits_to_double(v_cache[r + tile_offset(slot, i, d)]);
     }
   }
   *m_out = m;

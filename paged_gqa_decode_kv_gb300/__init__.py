@@ -5,14 +5,16 @@ The compute path runs only in the CUDA library ``libpgd.so``; this package is
 argument marshalling over it.  Importing the package does not load the
 library; the first call does, and fails loudly if it was not built.
 """
-from .inputs import WORKLOADS, Workload, PagedBatch, make_batch, make_workload  # noqa: F401
+from .inputs import (WORKLOADS, Workload, PagedBatch, make_batch, make_workload,  # noqa: F401
+                     tile_pool, untile_pool, pool_shape)
 from ._native import (  # noqa: F401
     PGDError, BlockAllocator, kv_append, paged_decode_attention,
     paged_decode_attention_noalloc, decode_step, copy_blocks,
     device_errors, workspace_size, make_workspace, attention_grid, validate_tables, lib,
     library_path)
 
-__all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "PGDError",
+__all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "tile_pool",
+           "untile_pool", "pool_shape", "PGDError",
            "BlockAllocator", "kv_append", "paged_decode_attention",
            "paged_decode_attention_noalloc", "decode_step", "copy_blocks",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",

@@ -111,10 +111,12 @@ def _need(t: torch.Tensor, dtype: torch.dtype, name: str, cuda: bool = True) -> 
 
 
 def _cache_dims(k_cache: torch.Tensor) -> Tuple[int, int, int, int]:
-    if k_cache.dim() != 4:
-        raise ValueError("k_cache must be [NB][n_kv][bs][d]")
-    NB, n_kv, bs, d = k_cache.shape
-    return NB, n_kv, bs, d
+    """(NB, n_kv, bs, d) of a pool [NB][n_kv][bs/8][d/8][8][8] (each (block,
+    head) tile stored as 8x8 core matrices)."""
+    if k_cache.dim() != 6 or tuple(k_cache.shape[4:]) != (8, 8):
+        raise ValueError("cache must be [NB][n_kv][bs/8][d/8][8][8]")
+    NB, n_kv, rg, nc = k_cache.shape[:4]
+    return NB, n_kv, rg * 8, nc * 8
 
 
 # --------------------------------------------------------------------- GPU ops

@@ -11,6 +11,7 @@
 #include <mutex>
 #include <string>
 #include <tuple>
+#include <atomic>
 
 #include "pgd_device.cuh"
 

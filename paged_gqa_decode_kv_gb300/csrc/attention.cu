@@ -1,4 +1,5 @@
-// attention.cu -- paged GQA decode attention for sm_103a.
+// attention.cu -- paged GQA decode attention for sm_103a on the fifth-
+// generation tensor cores (tcgen05, accumulators in tensor memory).
 //
 // What it computes ("Module 10: inference and serving", section "Attention
 // reads a different cache per sequence"; "The math of Transformer inference",
@@ -8,30 +9,52 @@
 //   table ("Module 10", section "Mapping logical positions to physical
 //   blocks").
 //
-// Work decomposition.  A unit is one (sequence, KV head); its K/V tiles are
-// read once and serve all G query heads.  The units' blocks are laid end to
-// end (sequence-major, then KV head, then block) into one range of X blocks,
-// and CTA c of P takes blocks [X*c/P, X*(c+1)/P): every CTA streams the same
-// number of bytes (+-1 block) whatever the length mix.  A CTA walks its range
-// unit by unit ("segments").  A segment that covers a whole unit writes the
-// output; otherwise it writes its (max, sum, weighted sum) state and the last
-// CTA of the unit to arrive merges the states by log-sum-exp ("The math of
+// Work split.  A unit is one (sequence, KV head); its K/V tiles are read once
+// and serve all G query heads.  The units' blocks are laid end to end
+// (sequence-major, then KV head, then block) into one range of X blocks and
+// CTA c of P takes blocks [X*c/P, X*(c+1)/P): every CTA streams the same bytes
+// (+-1 block) whatever the length mix.  A CTA walks its range unit by unit
+// ("segments").  A segment that covers a whole unit writes the output;
+// otherwise it writes its (max, sum, weighted sum) state and the last CTA of
+// the unit to arrive merges the states by log-sum-exp ("The math of
 // Transformer inference", section 8: split the sequence, attend locally,
-// merge by log-sum-exp; the state update is the one in "LLM inference
-// systems engineering", 2.8.3).  Arrival uses an atomic counter per unit; no
-// CTA ever waits for another.
+// merge by log-sum-exp; the running-state update is the one in "LLM
+// inference systems engineering", 2.8.3).  Arrival is an atomic counter per
+// unit; no CTA waits for another.
 //
-// Inside a CTA: one producer warp streams (block, head) K and V tiles -- each
-// a contiguous bs*256-byte run -- into a ring of shared-memory stages with
-// bulk copies on the TMA engine, signalled by mbarriers.  NW consumer warps
-// take stages round robin; each keeps its own online-softmax state in
-// registers (fp32) and the warps' states are merged at the end of a segment.
+// The two contractions of a 128-token stage run on the tensor cores with
+// tokens on the M side (decode attention is HBM bound; on CUDA cores the
+// 2 * G * 128 multiply-adds per token and KV head took most issue slots):
+//   S^T[128 tok][16]  = K[128 tok][128 d]   . Q^T[128 d][16 heads]
+//   O^T[128 d][16]   += V^T[128 d][128 tok] . P^T[128 tok][16 heads]
+// N = 16 is the smallest N for M = 128; the G <= 8 real heads use the first
+// columns, the rest are zeros.
 //
-// Consumer lane layout for q.k: 16 lanes cover one token (8 head-dim
-// elements each, one 16-byte shared load), two tokens per pass; the G partial
-// dot products are reduce-scattered over the 16 lanes so that each lane ends
-// with one (token, head) score.  For p.v each lane owns 4 of the 128 output
-// elements of all G heads.
+// Operands.  The pool stores every (block, KV head) tile as 8 x 8 core
+// matrices (row group of 8 tokens x 16 column chunks of 8 dims; element
+// (slot s, dim i) at ((s/8)*16 + i/8)*64 + (s%8)*8 + i%8).  One bulk copy per
+// tile therefore lands exactly in the tensor cores' no-swizzle layout, and
+// the tiles of a stage placed back to back form one operand with uniform
+// strides: K as the K-major A operand of q.k^T (8-row groups 2048 B apart,
+// 16-byte column chunks 128 B apart) and V as the MN-major A operand of p.v
+// (the same core matrices read the other way).  Q is written by threads as a
+// K-major, 128-byte-swizzled B operand and P as an MN-major B operand.
+//
+// Roles (224 threads, one CTA per SM):
+//   warps 0-3  softmax + epilogue; thread t owns TMEM lane t (token row t of
+//              S, head-dim row t of O)
+//   warp 4     K producer, warp 5 V producer: bulk copies on the TMA engine,
+//              one tile per lane, table entries prefetched a chunk ahead
+//   warp 6     allocates tensor memory and issues the MMAs (one lane)
+// Rings: 3 K stages and 3 V stages of 32 KiB; a K stage is free as soon as
+// its q.k^T has completed, a V stage after its p.v.  S and P are double
+// buffered by stage parity, O by segment parity.  Every wait is bounded.
+//
+// Softmax keeps one reference maximum per head.  A stage moves the reference
+// (and rescales O in tensor memory, after the previous p.v has completed)
+// only when its maximum exceeds the reference by more than 8 in log2 units,
+// so P <= 256 in bf16 and rescaling is rare; O and l share the reference, so
+// the final division is exact up to rounding.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -40,35 +63,140 @@
 #include "pgd_device.cuh"
 
 namespace pgd {
+namespace tc {
 
-template <int N>
-struct Log2 { static constexpr int value = 1 + Log2<N / 2>::value; };
-template <>
-struct Log2<1> { static constexpr int value = 0; };
+constexpr int TOK = 128;                    // tokens per stage (MMA M of q.k^T)
+constexpr int NPAD = 16;                    // MMA N: heads padded to 16
+constexpr int TILE_STAGE = TOK * 256;       // K (or V) bytes of one stage: 32 KiB
+constexpr int NSK = 3, NSV = 3;             // ring depths
+constexpr int Q_BYTES = 2 * NPAD * 128;     // [half][16 rows][128 B], 128B swizzle
+constexpr int P_BYTES = TOK * NPAD * 2;     // [16 token groups][2 head groups][8][16 B]
+constexpr int THREADS = 224;
+constexpr int WARP_KP = 4, WARP_VP = 5, WARP_MMA = 6;
+constexpr uint32_t TMEM_COLS = 64;
+constexpr float kRescaleLog2 = 8.f;         // move the reference when exceeded by 2^8
 
-__host__ __device__ constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+// shared memory (offsets from a 1024-byte aligned base)
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + NSK * TILE_STAGE;
+constexpr int OFF_Q = OFF_V + NSV * TILE_STAGE;
+constexpr int OFF_P = OFF_Q + Q_BYTES;
+constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+constexpr int OFF_RED = OFF_BAR + 512;      // f32 [2][4][8] warp maxima
+constexpr int OFF_LRED = OFF_RED + 256;     // f32 [4][8] warp sums
+constexpr int OFF_MISC = OFF_LRED + 128;    // tmem base, flags, stage masks
+constexpr int OFF_PRE = OFF_MISC + 64;      // int [B + 1]
+constexpr int SMEM_SLACK = 1024;
 
-template <int G_, int BS_, int NW_, int NS_>
-struct AttnCfg {
-  static constexpr int G = G_, BS = BS_, NW = NW_, NS = NS_;
-  static constexpr int D = kHeadDim;
-  static constexpr int THREADS = (NW + 1) * 32;
-  static constexpr int TILE_ELEMS = BS * D;
-  static constexpr int TILE_BYTES = TILE_ELEMS * 2;
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;  // K tile then V tile
-  static constexpr int OFF_BARS = NS * STAGE_BYTES;   // full[NS], empty[NS]
-  static constexpr int OFF_BAD = OFF_BARS + 2 * NS * 8;
-  static constexpr int OFF_PBUF = align_up(OFF_BAD + NS * 4, 16);   // f32 [NW][BS][G]
-  static constexpr int OFF_ABUF = OFF_PBUF + NW * BS * G * 4;       // f32 [NW][G]
-  static constexpr int OFF_MM = OFF_ABUF + NW * G * 4;              // f32 [NW][G]
-  static constexpr int OFF_ML = OFF_MM + NW * G * 4;                // f32 [NW][G]
-  static constexpr int OFF_MO = align_up(OFF_ML + NW * G * 4, 16);  // f32 [NW][G][D]
-  static constexpr int OFF_FLAG = OFF_MO + NW * G * D * 4;          // int [4]
-  static constexpr int OFF_PRE = OFF_FLAG + 16;                     // int [B + 1]
-  static size_t smem_bytes(int B) { return (size_t)OFF_PRE + (size_t)(B + 1) * 4; }
-};
+__host__ __device__ constexpr size_t smem_bytes(int B) {
+  return (size_t)SMEM_SLACK + OFF_PRE + (size_t)(B + 1) * 4;
+}
 
-// Segment: the part of the CTA's block range that lies in one unit.
+__device__ __forceinline__ uint32_t col_s(int sb) { return (uint32_t)sb * 16u; }
+__device__ __forceinline__ uint32_t col_o(int ob) { return 32u + (uint32_t)ob * 16u; }
+
+// ---------------------------------------------------------------- PTX helpers
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, layout
+// (0 = no swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, M = 128, N = 16;
+// a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t instr_desc(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(NPAD >> 3) << 17) | ((uint32_t)(TOK >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Generic-proxy shared-memory writes become visible to the tensor cores.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 8 consecutive fp32 columns of this warp's 32 TMEM lanes (wait included).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r0, r1, r2, r3, r4, r5, r6, r7;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6), "=r"(r7)
+      : "r"(taddr)
+      : "memory");
+  v[0] = __uint_as_float(r0); v[1] = __uint_as_float(r1);
+  v[2] = __uint_as_float(r2); v[3] = __uint_as_float(r3);
+  v[4] = __uint_as_float(r4); v[5] = __uint_as_float(r5);
+  v[6] = __uint_as_float(r6); v[7] = __uint_as_float(r7);
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+      : "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+  return v;
+}
+
+// Bounded wait that gives up at once after any earlier timeout in the CTA, so
+// that the control flow (and every named barrier) is the same for all threads
+// whatever happens.
+__device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort_flag, int32_t *err) {
+  if (*abort_flag) return;
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 31u) == 0) {
+      if (*abort_flag) return;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(err, PGD_DEVERR_TIMEOUT);
+        return;
+      }
+    }
+  }
+}
+
 struct Segment {
   int b, g, j0, nblk, n;
   long long unit_start, unit_end;
@@ -95,67 +223,151 @@ __device__ __forceinline__ Segment locate(const int *pre, int B, int n_kv, long 
   return s;
 }
 
-// Reduce-scatter G partial sums over the 16 lanes of a half warp (lane bits
-// 3..0).  Level k halves the vector along lane bit 3-k; the lanes then hold
-// one value for head ((lane & 15) >> (4 - log2 G)), and the remaining bits
-// all-reduce it.
-template <int G>
-__device__ __forceinline__ float reduce_scatter16(float (&a)[G], int lane) {
-  constexpr int LG = Log2<G>::value;
-  float w[G];
-#pragma unroll
-  for (int i = 0; i < G; ++i) w[i] = a[i];
-#pragma unroll
-  for (int k = 0; k < LG; ++k) {
-    const int bit = 3 - k;
-    const int half = G >> (k + 1);
-    const bool upper = (lane >> bit) & 1;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? w[i] : w[i + half];
-      const float keep = upper ? w[i + half] : w[i];
-      w[i] = keep + __shfl_xor_sync(kFullMask, send, 1 << bit);
+// One producer warp (K or V): walks the CTA's stages, copies one tile per
+// lane with the TMA engine.  Block ids come from 32-entry chunks of the table
+// row, each loaded one chunk before it is needed.  The K producer also
+// records which blocks of the stage had an invalid id.
+template <int BS>
+__device__ __forceinline__ void produce(const AttnParams &p, const __nv_bfloat16 *cache,
+                                        unsigned char *ring, uint64_t *full, uint64_t *empty,
+                                        int nstages_ring, const int *pre, long long x_begin,
+                                        long long x_end, volatile int *stage_mask,
+                                        volatile int *abort_flag, int lane) {
+  constexpr int SB = TOK / BS;  // blocks per stage
+  constexpr uint32_t TILE_BYTES = BS * 256;
+  const uint64_t policy = l2_policy_evict_first();
+  int s = 0;
+  for (long long x = x_begin; x < x_end;) {
+    const Segment sg = locate(pre, p.B, p.n_kv, x, x_end);
+    const int32_t *trow = p.tables + (size_t)sg.b * p.MB + sg.j0;
+    int cur = (lane < sg.n) ? __ldg(trow + lane) : 0;
+    int nxt = (32 + lane < sg.n) ? __ldg(trow + 32 + lane) : 0;
+    int chunk = 0;
+    const int nstages = (sg.n + SB - 1) / SB;
+    for (int st = 0; st < nstages; ++st, ++s) {
+      const int first = st * SB;
+      if ((first >> 5) != chunk) {  // next 32-entry chunk; prefetch the one after
+        chunk = first >> 5;
+        cur = nxt;
+        const int j = (chunk + 1) * 32 + lane;
+        nxt = (j < sg.n) ? __ldg(trow + j) : 0;
+      }
+      const int nb = min(SB, sg.n - first);
+      const int blk = __shfl_sync(kFullMask, cur, (first & 31) + (lane & (SB - 1)));
+      const bool ok = lane < nb && (unsigned)blk < (unsigned)p.NB;
+      const unsigned okmask = __ballot_sync(kFullMask, ok);
+      const unsigned want = (1u << nb) - 1u;
+      const int slot = s % nstages_ring;
+      if (lane == 0) {
+        wait_or_abort(&empty[slot], ((uint32_t)(s / nstages_ring) & 1u) ^ 1u, abort_flag, p.err);
+        if (stage_mask) {
+          stage_mask[s & 7] = (int)(want & ~okmask);
+          if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
+        }
+        const uint32_t bytes = (uint32_t)__popc(okmask) * TILE_BYTES;
+        if (*abort_flag || bytes == 0)
+          mbar_arrive(&full[slot]);
+        else
+          mbar_arrive_expect_tx(&full[slot], bytes);
+      }
+      __syncwarp();
+      if (ok && !*abort_flag) {
+        const __nv_bfloat16 *src = cache + ((size_t)blk * p.n_kv + sg.g) * (size_t)(BS * kHeadDim);
+        bulk_copy_g2s(ring + (size_t)slot * TILE_STAGE + (size_t)lane * TILE_BYTES, src,
+                      TILE_BYTES, &full[slot], policy);
+      }
+    }
+    x += sg.n;
+  }
+  // no copy may still be landing when the CTA exits
+  if (lane == 0) {
+    for (int k = 1; k <= nstages_ring && k <= s; ++k) {
+      const int last = s - k;
+      mbar_wait_bounded(&full[last % nstages_ring], (uint32_t)(last / nstages_ring) & 1u);
     }
   }
-  float v = w[0];
-#pragma unroll
-  for (int bit = 3 - LG; bit >= 0; --bit) v += __shfl_xor_sync(kFullMask, v, 1 << bit);
-  return v;
 }
 
-template <class C>
-__global__ void __launch_bounds__(C::THREADS)
-paged_attention_kernel(const AttnParams p) {
-  constexpr int G = C::G, BS = C::BS, NW = C::NW, NS = C::NS, D = C::D;
-  constexpr int LG = Log2<G>::value;
-  constexpr int DUPMASK = (1 << (4 - LG)) - 1;
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BARS);
-  uint64_t *empty = full + NS;
-  volatile int *bad = reinterpret_cast<volatile int *>(smem + C::OFF_BAD);
-  volatile int *flag = reinterpret_cast<volatile int *>(smem + C::OFF_FLAG);
-  int *pre = reinterpret_cast<int *>(smem + C::OFF_PRE);
+template <int G, int BS>
+__global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnParams p) {
+  constexpr int SB = TOK / BS;
+  constexpr uint32_t IDESC_QK = instr_desc(false, false);
+  constexpr uint32_t IDESC_PV = instr_desc(true, true);
+  static_assert(G >= 1 && G <= 8 && TOK % BS == 0 && BS % 8 == 0 && SB <= 32, "shape");
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+  uint64_t *full_k = bars;              // [NSK]
+  uint64_t *empty_k = full_k + NSK;     // [NSK]
+  uint64_t *full_v = empty_k + NSK;     // [NSV]
+  uint64_t *empty_v = full_v + NSV;     // [NSV]
+  uint64_t *s_full = empty_v + NSV;     // [2]
+  uint64_t *s_free = s_full + 2;        // [2]
+  uint64_t *p_full = s_free + 2;        // [2]
+  uint64_t *p_free = p_full + 2;        // [2]
+  uint64_t *o_full = p_free + 2;        // [2]
+  uint64_t *o_free = o_full + 2;        // [2]
+  uint64_t *m_ready = o_free + 2;       // [2]
+  uint64_t *q_ready = m_ready + 2;      // [1]
+  uint64_t *done = q_ready + 1;         // [1]
+  float *red = reinterpret_cast<float *>(smem + OFF_RED);
+  float *lred = reinterpret_cast<float *>(smem + OFF_LRED);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+  volatile int *flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);         // [3]
+  volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 32);  // [8]
+  int *pre = reinterpret_cast<int *>(smem + OFF_PRE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+    for (int i = 0; i < NSK; ++i) {
+      mbar_init(&full_k[i], 1);
+      mbar_init(&empty_k[i], 1);
     }
+    for (int i = 0; i < NSV; ++i) {
+      mbar_init(&full_v[i], 1);
+      mbar_init(&empty_v[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&p_free[i], 1);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_free[i], 4);
+      mbar_init(&m_ready[i], 1);
+    }
+    mbar_init(q_ready, 4);
+    mbar_init(done, 1);
     mbar_init_fence();
-    flag[0] = 0;  // abort
+    *abort_flag = 0;
+  }
+  // Q pad rows and P pad columns stay zero for the whole kernel.
+  {
+    uint4 *z = reinterpret_cast<uint4 *>(smem + OFF_Q);
+    for (int i = tid; i < (Q_BYTES + 2 * P_BYTES) / 16; i += THREADS) z[i] = make_uint4(0, 0, 0, 0);
   }
   // Blocks per sequence, then an exclusive prefix over the batch.
   const int max_tokens = p.MB * BS;
   bool bad_ctx = false;
-  for (int b = tid; b < p.B; b += C::THREADS) {
+  for (int b = tid; b < p.B; b += THREADS) {
     const int c = p.ctx[b];
     int nb = 0;
     if (c >= 1 && c <= max_tokens) nb = (c + BS - 1) / BS; else bad_ctx = true;
     pre[b + 1] = nb;
   }
   if (bad_ctx && blockIdx.x == 0) atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
+  if (warp == WARP_MMA) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_proxy_async();
   __syncthreads();
   if (warp == 0) {
     int carry = 0;
@@ -172,335 +384,393 @@ paged_attention_kernel(const AttnParams p) {
     }
     if (lane == 0) pre[0] = 0;
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
   const long long X = (long long)p.n_kv * pre[p.B];
   const long long P = X < (long long)gridDim.x ? X : (long long)gridDim.x;
   const long long cta = blockIdx.x;
-  if (cta >= P) return;  // more CTAs than blocks: the spare ones have nothing to do
-  const long long x_begin = X * cta / P, x_end = X * (cta + 1) / P;
-
-  if (warp == NW) {
-    // ------------------------------------------------------------ producer
-    const uint64_t policy = l2_policy_evict_first();
-    int s = 0;
-    bool abort = false;
-    for (long long x = x_begin; x < x_end && !abort;) {
-      const Segment sg = locate(pre, p.B, p.n_kv, x, x_end);
-      const int32_t *trow = p.tables + (size_t)sg.b * p.MB + sg.j0;
-      for (int base = 0; base < sg.n && !abort; base += 32) {
-        const int cnt = min(32, sg.n - base);
-        const int my_blk = (lane < cnt) ? __ldg(trow + base + lane) : 0;
-        for (int k = 0; k < cnt; ++k) {
-          const int blk = __shfl_sync(kFullMask, my_blk, k);
-          int stop = 0;
-          if (lane == 0) {
-            const int slot = s % NS;
-            const uint32_t phase = (uint32_t)(s / NS) & 1u;
-            if (flag[0] || !mbar_wait_bounded(&empty[slot], phase ^ 1u)) {
-              if (!flag[0]) atomicOr(p.err, PGD_DEVERR_TIMEOUT);
-              flag[0] = 1;
-              stop = 1;
-            } else if ((unsigned)blk >= (unsigned)p.NB) {
-              bad[slot] = 1;
-              atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
-              mbar_arrive(&full[slot]);
-            } else {
-              bad[slot] = 0;
-              unsigned char *dst = smem + (size_t)slot * C::STAGE_BYTES;
-              const size_t tile = ((size_t)blk * p.n_kv + sg.g) * C::TILE_ELEMS;
-              mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
-              bulk_copy_g2s(dst, p.k_cache + tile, C::TILE_BYTES, &full[slot], policy);
-              bulk_copy_g2s(dst + C::TILE_BYTES, p.v_cache + tile, C::TILE_BYTES, &full[slot],
-                            policy);
-            }
-          }
-          stop = __shfl_sync(kFullMask, stop, 0);
-          if (stop) { abort = true; break; }
-          ++s;
-        }
-      }
-      x += sg.n;
-    }
-    // Never leave a copy in flight into this CTA's shared memory: wait for
-    // the last phase issued on every slot (immediate unless aborted).
-    if (lane == 0) {
-      for (int k = 1; k <= NS && k <= s; ++k) {
-        const int last = s - k;
-        mbar_wait_bounded(&full[last % NS], (uint32_t)(last / NS) & 1u);
-      }
-    }
-    return;
+  long long x_begin = 0, x_end = 0;
+  if (cta < P) {  // more CTAs than blocks: the spare ones have nothing to do
+    x_begin = X * cta / P;
+    x_end = X * (cta + 1) / P;
   }
 
-  // -------------------------------------------------------------- consumers
-  const int w = warp;
-  const int part = lane & 15;   // head-dim elements [8 part, 8 part + 8) for q.k
-  const int jj = lane >> 4;     // token within a pass
-  const int hsel = (lane & 15) >> (4 - LG);
-  float *pbuf = reinterpret_cast<float *>(smem + C::OFF_PBUF) + w * BS * G;
-  float *abuf = reinterpret_cast<float *>(smem + C::OFF_ABUF) + w * G;
-  float *mrg_m = reinterpret_cast<float *>(smem + C::OFF_MM);
-  float *mrg_l = reinterpret_cast<float *>(smem + C::OFF_ML);
-  float *mrg_o = reinterpret_cast<float *>(smem + C::OFF_MO);
-  const int ct = w * 32 + lane;  // consumer thread index
-  constexpr int NCT = NW * 32;
-
-  int s = 0;
-  for (long long x = x_begin; x < x_end;) {
-    const Segment sg = locate(pre, p.B, p.n_kv, x, x_end);
-    const int unit = sg.b * p.n_kv + sg.g;
-    const int ctx_b = __ldg(p.ctx + sg.b);
-
-    float qr[G][8];
+  if (warp == WARP_KP) {
+    produce<BS>(p, p.k_cache, smem + OFF_K, full_k, empty_k, NSK, pre, x_begin, x_end,
+                stage_mask, abort_flag, lane);
+  } else if (warp == WARP_VP) {
+    produce<BS>(p, p.v_cache, smem + OFF_V, full_v, empty_v, NSV, pre, x_begin, x_end, nullptr,
+                abort_flag, lane);
+  } else if (warp == WARP_MMA) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t q_base = smem_addr(smem + OFF_Q);
+      int s_qk = 0, s_pv = 0;    // next stage for q.k^T and for p.v
+      int k_qk = 0, k_pv = 0;    // their segment index
+      int st_qk = 0, st_pv = 0;  // their stage index within the segment
+      long long x_qk = x_begin, x_pv = x_begin;
+      Segment seg_qk, seg_pv;
+      int ns_qk = 0, ns_pv = 0;
+      if (x_qk < x_end) {
+        seg_qk = locate(pre, p.B, p.n_kv, x_qk, x_end);
+        ns_qk = (seg_qk.n + SB - 1) / SB;
+        seg_pv = seg_qk;
+        ns_pv = ns_qk;
+      }
+      auto issue_qk = [&]() {
+        const int slot = s_qk % NSK, sb = s_qk & 1;
+        if (st_qk == 0) wait_or_abort(q_ready, (uint32_t)k_qk & 1u, abort_flag, p.err);
+        wait_or_abort(&full_k[slot], (uint32_t)(s_qk / NSK) & 1u, abort_flag, p.err);
+        wait_or_abort(&s_free[sb], ((uint32_t)(s_qk >> 1) & 1u) ^ 1u, abort_flag, p.err);
+        tc_fence_after();
+        if (!*abort_flag) {
+          const uint32_t k_base = smem_addr(smem + OFF_K + slot * TILE_STAGE);
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-          p.q + ((size_t)sg.b * p.n_q + sg.g * G + h) * D + 8 * part));
-      float f[8];
-      unpack8(raw, f);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t qoff = (uint32_t)((kk >> 2) * (NPAD * 128) + (kk & 3) * 32);
+            umma_bf16(tmem + col_s(sb), smem_desc(k_base + kk * 256, 128, 2048, 0),
+                      smem_desc(q_base + qoff, 16, 1024, 2), IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(&s_full[sb]);
+        umma_commit(&empty_k[slot]);
+        // Hand the stage's invalid-block mask (written by the K producer before
+        // it armed full_k, which this thread acquired) on to the softmax.
+        mbar_arrive(&m_ready[sb]);
+        ++s_qk;
+        if (++st_qk == ns_qk) {
+          st_qk = 0;
+          ++k_qk;
+          x_qk += seg_qk.n;
+          if (x_qk < x_end) {
+            seg_qk = locate(pre, p.B, p.n_kv, x_qk, x_end);
+            ns_qk = (seg_qk.n + SB - 1) / SB;
+          }
+        }
+      };
+      if (x_qk < x_end) issue_qk();
+      while (x_pv < x_end) {
+        if (x_qk < x_end) issue_qk();  // q.k^T of the next stage overlaps this softmax
+        const int slot = s_pv % NSV, sb = s_pv & 1, ob = k_pv & 1;
+        wait_or_abort(&p_full[sb], (uint32_t)(s_pv >> 1) & 1u, abort_flag, p.err);
+        wait_or_abort(&full_v[slot], (uint32_t)(s_pv / NSV) & 1u, abort_flag, p.err);
+        if (st_pv == 0)
+          wait_or_abort(&o_free[ob], ((uint32_t)(k_pv >> 1) & 1u) ^ 1u, abort_flag, p.err);
+        tc_fence_after();
+        if (!*abort_flag) {
+          const uint32_t v_base = smem_addr(smem + OFF_V + slot * TILE_STAGE);
+          const uint32_t p_base = smem_addr(smem + OFF_P + sb * P_BYTES);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qr[h][e] = f[e] * p.qk_scale_log2;
+          for (int kt = 0; kt < 8; ++kt) {
+            umma_bf16(tmem + col_o(ob), smem_desc(v_base + kt * 4096, 2048, 128, 0),
+                      smem_desc(p_base + kt * 512, 256, 128, 0), IDESC_PV,
+                      (st_pv > 0 || kt > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&empty_v[slot]);
+        umma_commit(&p_free[sb]);
+        const bool last = (st_pv + 1 == ns_pv);
+        if (last) umma_commit(&o_full[ob]);
+        ++s_pv;
+        if (last) {
+          st_pv = 0;
+          ++k_pv;
+          x_pv += seg_pv.n;
+          if (x_pv < x_end) {
+            seg_pv = locate(pre, p.B, p.n_kv, x_pv, x_end);
+            ns_pv = (seg_pv.n + SB - 1) / SB;
+          }
+        } else {
+          ++st_pv;
+        }
+      }
+      // every MMA has completed before tensor memory is released
+      if (s_qk > 0) {
+        umma_commit(done);
+        mbar_wait_bounded(done, 0);
+      }
     }
-    float m_run = -INFINITY, l_run = 0.f;
-    float o[G][4];
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[h][e] = 0.f;
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- softmax + epilogue
+    const int t = tid;  // 0..127: token row of S, head-dim row of O
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    constexpr int NCT = 128;
+    int s = 0, k = 0;
+    long long x = x_begin;
+    Segment sg;
+    if (x < x_end) sg = locate(pre, p.B, p.n_kv, x, x_end);
 
-    const int first = ((w - s) % NW + NW) % NW;
-    for (int i = first; i < sg.n; i += NW) {
-      const int S = s + i;
-      const int slot = S % NS;
-      const uint32_t phase = (uint32_t)(S / NS) & 1u;
-      bool ok = !flag[0] && mbar_wait_bounded(&full[slot], phase);
-      ok = __all_sync(kFullMask, ok);
-      if (!ok) {
-        if (lane == 0 && !flag[0]) atomicOr(p.err, PGD_DEVERR_TIMEOUT);
-        flag[0] = 1;
-      } else if (!bad[slot]) {
-        const __nv_bfloat16 *Ks =
-            reinterpret_cast<const __nv_bfloat16 *>(smem + (size_t)slot * C::STAGE_BYTES);
-        const __nv_bfloat16 *Vs = Ks + C::TILE_ELEMS;
-        const int nvalid = min(BS, ctx_b - (sg.j0 + i) * BS);
+    // Q of a segment into the B operand buffer: K-major, 128-byte swizzle,
+    // row = head, two 64-column halves.
+    auto write_q = [&](const Segment &q) {
+      if (t < 16 * G) {
+        const int r = t >> 4, c = t & 15, half = c >> 3, cc = c & 7;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
+            p.q + ((size_t)q.b * p.n_q + (size_t)q.g * G + r) * kHeadDim + c * 8));
+        *reinterpret_cast<uint4 *>(smem + OFF_Q + half * (NPAD * 128) + r * 128 +
+                                   ((cc ^ (r & 7)) << 4)) = v;
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+    };
+    if (x < x_end) write_q(sg);
 
-        // scores (log2 domain), one (token, head) per lane per pass
-        float sc[BS / 2];
+    while (x < x_end) {
+      const int unit = sg.b * p.n_kv + sg.g;
+      const int ctx_b = __ldg(p.ctx + sg.b);
+      const int nstages = (sg.n + SB - 1) / SB;
+      const int ob = k & 1;
+      float m_ref[G], l_part[G];
 #pragma unroll
-        for (int it = 0; it < BS / 2; ++it) {
-          const int t = 2 * it + jj;
-          const uint4 raw = *reinterpret_cast<const uint4 *>(Ks + t * D + 8 * part);
-          float kf[8];
-          unpack8(raw, kf);
-          float acc[G];
+      for (int h = 0; h < G; ++h) { m_ref[h] = -INFINITY; l_part[h] = 0.f; }
+
+      for (int st = 0; st < nstages; ++st, ++s) {
+        const int vslot = s % NSV, sb = s & 1;
+        const int nb = min(SB, sg.n - st * SB);
+        const int jfirst = sg.j0 + st * SB;
+        int nvalid = nb * BS;
+        if (jfirst + nb == sg.nblk) nvalid -= sg.nblk * BS - ctx_b;  // unit's last block
+
+        wait_or_abort(&s_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+        // Invalid-block mask of this stage: the K producer wrote it before
+        // arming full_k; the MMA thread acquired full_k and then released
+        // m_ready.  (Waiting on full_k here could alias: a K stage is freed
+        // after its q.k^T, so full_k may run two phases ahead.)  m_ready and
+        // the 8-entry mask ring cannot move on before this stage frees its S
+        // buffer.
+        wait_or_abort(&m_ready[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+        const int mask = stage_mask[s & 7];
+        tc_fence_after();
+        float sv[8];
+        tmem_ld8(tmem + lane_base + col_s(sb), sv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
+
+        const bool valid = (t < nvalid) && !((mask >> (t / BS)) & 1);
+        float sc[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) sc[h] = valid ? sv[h] * p.qk_scale_log2 : -INFINITY;
+
+        // tile maximum per head across the 128 rows
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float wm = warp_max(sc[h]);
+          if (lane == 0) red[(sb * 4 + warp) * 8 + h] = wm;
+        }
+        named_barrier_sync(1, NCT);
+        bool need = false;
+        float tmax[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          tmax[h] = fmaxf(fmaxf(red[(sb * 4 + 0) * 8 + h], red[(sb * 4 + 1) * 8 + h]),
+                          fmaxf(red[(sb * 4 + 2) * 8 + h], red[(sb * 4 + 3) * 8 + h]));
+          need |= tmax[h] > m_ref[h] + kRescaleLog2;
+        }
+        if (need) {
+          float alpha[8];
+#pragma unroll
+          for (int h = 0; h < 8; ++h) alpha[h] = 1.f;
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            float a = 0.f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) a = fmaf(qr[h][e], kf[e], a);
-            acc[h] = a;
+            const float mn = fmaxf(m_ref[h], tmax[h]);
+            alpha[h] = (m_ref[h] == -INFINITY) ? 0.f : exp2f(m_ref[h] - mn);
+            m_ref[h] = mn;
+            l_part[h] *= alpha[h];
           }
-          const float v = reduce_scatter16<G>(acc, lane);
-          sc[it] = (t < nvalid) ? v : -INFINITY;
-        }
-        // online softmax update for this lane's head
-        float tmax = sc[0];
+          if (st > 0) {
+            // rescale O in tensor memory once the previous p.v has completed
+            wait_or_abort(&p_free[(s - 1) & 1], (uint32_t)((s - 1) >> 1) & 1u, abort_flag, p.err);
+            tc_fence_after();
+            float ov[8];
+            tmem_ld8(tmem + lane_base + col_o(ob), ov);
 #pragma unroll
-        for (int it = 1; it < BS / 2; ++it) tmax = fmaxf(tmax, sc[it]);
-        tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 16));
-        const float m_new = fmaxf(m_run, tmax);
-        const float alpha = exp2f(m_run - m_new);
-        float psum = 0.f;
-#pragma unroll
-        for (int it = 0; it < BS / 2; ++it) {
-          const float pv = exp2f(sc[it] - m_new);
-          psum += pv;
-          if ((lane & DUPMASK) == 0) pbuf[(2 * it + jj) * G + hsel] = pv;
+            for (int h = 0; h < 8; ++h) ov[h] *= alpha[h];
+            tmem_st8(tmem + lane_base + col_o(ob), ov);
+            tc_fence_before();
+          }
         }
-        l_run = l_run * alpha + psum;
-        m_run = m_new;
-        if (lane < 16 && (lane & DUPMASK) == 0) abuf[hsel] = alpha;
+        // probabilities, rounded to bf16 as the tensor cores will see them
+        uint32_t packed[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float pv = valid ? exp2f(sc[h] - m_ref[h]) : 0.f;
+          const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
+          l_part[h] += __bfloat162float(pb);
+          packed[h >> 1] |= (uint32_t)__bfloat16_as_ushort(pb) << ((h & 1) * 16);
+        }
+        wait_or_abort(&p_free[sb], ((uint32_t)(s >> 1) & 1u) ^ 1u, abort_flag, p.err);
+        *reinterpret_cast<uint4 *>(smem + OFF_P + sb * P_BYTES + (t >> 3) * 256 + (t & 7) * 16) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        if (nvalid < TOK || mask) {
+          // rows that are not valid tokens must not feed NaN/Inf into p.v
+          wait_or_abort(&full_v[vslot], (uint32_t)(s / NSV) & 1u, abort_flag, p.err);
+          if (!valid) {
+            uint4 *vrow = reinterpret_cast<uint4 *>(smem + OFF_V + vslot * TILE_STAGE +
+                                                    (t >> 3) * 2048 + (t & 7) * 16);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) vrow[c * 8] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
         __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+      }
 
-        // o = alpha * o + sum_t p_t v_t over the valid tokens only
-        float al[G];
+      // ---- end of segment: next Q, then the epilogue
+      const long long x_next = x + sg.n;
+      Segment next = sg;
+      if (x_next < x_end) {
+        next = locate(pre, p.B, p.n_kv, x_next, x_end);
+        write_q(next);
+      }
+      float L[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) al[h] = abuf[h];
+      for (int h = 0; h < G; ++h) {
+        const float ws = warp_sum(l_part[h]);
+        if (lane == 0) lred[warp * 8 + h] = ws;
+      }
+      named_barrier_sync(1, NCT);
+#pragma unroll
+      for (int h = 0; h < G; ++h)
+        L[h] = (lred[0 * 8 + h] + lred[1 * 8 + h]) + (lred[2 * 8 + h] + lred[3 * 8 + h]);
+
+      wait_or_abort(&o_full[ob], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
+      tc_fence_after();
+      float ov[8];
+      tmem_ld8(tmem + lane_base + col_o(ob), ov);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[ob]);
+
+      const bool whole = (x == sg.unit_start) && (x + sg.n == sg.unit_end);
+      const size_t out_row = (size_t)sg.b * p.n_q + (size_t)sg.g * G;
+      if (whole) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[h][e] *= al[h];
-#pragma unroll 4
-        for (int t = 0; t < nvalid; ++t) {
-          const uint2 raw = *reinterpret_cast<const uint2 *>(Vs + t * D + 4 * lane);
-          float vf[4];
-          unpack4(raw, vf);
-          float pp[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) pp[h] = pbuf[t * G + h];
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[h][e] = fmaf(pp[h], vf[e], o[h][e]);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
-    }
-    s += sg.n;
-
-    // ---- merge the NW warp states of this segment
-    const float l_tot = l_run + __shfl_xor_sync(kFullMask, l_run, 16);
-    if (lane < 16 && (lane & DUPMASK) == 0) {
-      mrg_m[w * G + hsel] = m_run;
-      mrg_l[w * G + hsel] = l_tot;
-    }
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-      *reinterpret_cast<float4 *>(mrg_o + (w * G + h) * D + 4 * lane) =
-          make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-    named_barrier_sync(1, NCT);
-
-    const bool whole = (x == sg.unit_start) && (x + sg.n == sg.unit_end);
-    const size_t out_row = (size_t)sg.b * p.n_q + (size_t)sg.g * G;
-    const size_t slot_row = ((size_t)unit + (size_t)cta) * G;
-    for (int k = ct; k < G * D / 2; k += NCT) {
-      const int h = k / (D / 2), e = 2 * (k % (D / 2));
-      float M = -INFINITY;
-#pragma unroll
-      for (int ww = 0; ww < NW; ++ww) M = fmaxf(M, mrg_m[ww * G + h]);
-      float L = 0.f, O0 = 0.f, O1 = 0.f;
-#pragma unroll
-      for (int ww = 0; ww < NW; ++ww) {
-        const float mw = mrg_m[ww * G + h];
-        if (mw == -INFINITY) continue;
-        const float cf = exp2f(mw - M);
-        L = fmaf(cf, mrg_l[ww * G + h], L);
-        O0 = fmaf(cf, mrg_o[(ww * G + h) * D + e], O0);
-        O1 = fmaf(cf, mrg_o[(ww * G + h) * D + e + 1], O1);
-      }
-      if (whole) {
-        const float inv = 1.f / L;
-        *reinterpret_cast<__nv_bfloat162 *>(p.out + (out_row + h) * D + e) =
-            __floats2bfloat162_rn(O0 * inv, O1 * inv);
+          p.out[(out_row + h) * kHeadDim + t] = __float2bfloat16_rn(ov[h] / L[h]);
       } else {
-        *reinterpret_cast<float2 *>(p.part_o + (slot_row + h) * D + e) = make_float2(O0, O1);
-        if (e == 0)
-          *reinterpret_cast<float2 *>(p.part_ml + (slot_row + h) * 2) = make_float2(M, L);
-      }
-    }
-
-    if (!whole) {
-      // Publish this part; the last part of the unit to arrive merges all.
-      __threadfence();
-      named_barrier_sync(1, NCT);
-      if (ct == 0) {
-        const long long c_first = (P * (sg.unit_start + 1) - 1) / X;
-        const long long c_last = (P * sg.unit_end - 1) / X;
-        const int n_parts = (int)(c_last - c_first + 1);
-        const int before = atomicAdd(p.counters + unit, 1);
-        const int last = (before == n_parts - 1);
-        if (last) atomicExch(p.counters + unit, 0);  // ready for the next call
-        flag[1] = last;
-        flag[2] = (int)c_first;
-        flag[3] = n_parts;
-      }
-      named_barrier_sync(1, NCT);
-      if (flag[1]) {
+        const size_t srow = ((size_t)unit + (size_t)cta) * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) p.part_o[(srow + h) * kHeadDim + t] = ov[h];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          if (t == h)
+            *reinterpret_cast<float2 *>(p.part_ml + (srow + h) * 2) = make_float2(m_ref[h], L[h]);
+        // publish this part; the last part of the unit to arrive merges all
         __threadfence();
-        const int c_first = flag[2], n_parts = flag[3];
-        const size_t row0 = ((size_t)unit + (size_t)c_first) * G;
-        for (int k = ct; k < G * D / 2; k += NCT) {
-          const int h = k / (D / 2), e = 2 * (k % (D / 2));
-          float M = -INFINITY;
-          for (int i = 0; i < n_parts; ++i)
-            M = fmaxf(M, __ldcg(p.part_ml + (row0 + (size_t)i * G + h) * 2));
-          float L = 0.f, O0 = 0.f, O1 = 0.f;
-          for (int i = 0; i < n_parts; ++i) {
-            const size_t r = row0 + (size_t)i * G + h;
-            const float mi = __ldcg(p.part_ml + r * 2);
-            if (mi == -INFINITY) continue;
-            const float cf = exp2f(mi - M);
-            L = fmaf(cf, __ldcg(p.part_ml + r * 2 + 1), L);
-            const float2 oi = __ldcg(reinterpret_cast<const float2 *>(p.part_o + r * D + e));
-            O0 = fmaf(cf, oi.x, O0);
-            O1 = fmaf(cf, oi.y, O1);
+        named_barrier_sync(1, NCT);
+        if (t == 0) {
+          const long long c_first = (P * (sg.unit_start + 1) - 1) / X;
+          const long long c_last = (P * sg.unit_end - 1) / X;
+          const int n_parts = (int)(c_last - c_first + 1);
+          const int before = atomicAdd(p.counters + unit, 1);
+          const int last = (before == n_parts - 1);
+          if (last) atomicExch(p.counters + unit, 0);  // ready for the next call
+          flag[0] = last;
+          flag[1] = (int)c_first;
+          flag[2] = n_parts;
+        }
+        named_barrier_sync(1, NCT);
+        if (flag[0]) {
+          __threadfence();
+          const int c_first = flag[1], n_parts = flag[2];
+          const size_t row0 = ((size_t)unit + (size_t)c_first) * G;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            float M = -INFINITY;
+            for (int i = 0; i < n_parts; ++i)
+              M = fmaxf(M, __ldcg(p.part_ml + (row0 + (size_t)i * G + h) * 2));
+            float Lm = 0.f, O = 0.f;
+            for (int i = 0; i < n_parts; ++i) {
+              const size_t r = row0 + (size_t)i * G + h;
+              const float mi = __ldcg(p.part_ml + r * 2);
+              if (mi == -INFINITY) continue;
+              const float cf = exp2f(mi - M);
+              Lm = fmaf(cf, __ldcg(p.part_ml + r * 2 + 1), Lm);
+              O = fmaf(cf, __ldcg(p.part_o + r * kHeadDim + t), O);
+            }
+            p.out[(out_row + h) * kHeadDim + t] = __float2bfloat16_rn(O / Lm);
           }
-          const float inv = 1.f / L;
-          *reinterpret_cast<__nv_bfloat162 *>(p.out + (out_row + h) * D + e) =
-              __floats2bfloat162_rn(O0 * inv, O1 * inv);
         }
       }
+      named_barrier_sync(1, NCT);  // lred / flags are reused by the next segment
+      x = x_next;
+      sg = next;
+      ++k;
     }
-    named_barrier_sync(1, NCT);  // merge buffers and flags are reused next segment
-    x += sg.n;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == WARP_MMA) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
   }
 }
 
-// ---------------------------------------------------------------- launcher
 // The dynamic shared-memory limit is raised once per device, to the size the
 // largest accepted batch needs.
-template <class C>
+template <int G, int BS>
 static cudaError_t ensure_smem_limit() {
   static volatile int done[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(paged_attention_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)C::smem_bytes(PGD_MAX_BATCH));
+  e = cudaFuncSetAttribute(paged_attention_kernel<G, BS>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes(PGD_MAX_BATCH));
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
   return e;
 }
 
-template <class C>
+template <int G, int BS>
 static cudaError_t launch_cfg(const AttnParams &p, int grid, cudaStream_t stream) {
-  cudaError_t e = ensure_smem_limit<C>();
+  cudaError_t e = ensure_smem_limit<G, BS>();
   if (e != cudaSuccess) return e;
-  paged_attention_kernel<C><<<grid, C::THREADS, C::smem_bytes(p.B), stream>>>(p);
+  paged_attention_kernel<G, BS><<<grid, THREADS, smem_bytes(p.B), stream>>>(p);
   return cudaGetLastError();
 }
 
-template <class C>
+template <int G, int BS>
 static int occupancy_cfg(int B) {
-  if (ensure_smem_limit<C>() != cudaSuccess) return 0;
+  if (ensure_smem_limit<G, BS>() != cudaSuccess) return 0;
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_attention_kernel<C>, C::THREADS,
-                                                    C::smem_bytes(B)) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_attention_kernel<G, BS>, THREADS,
+                                                    smem_bytes(B)) != cudaSuccess)
     return 0;
   return n;
 }
 
-// Consumer warps and ring depth per (G, bs): 4 consumer warps; the ring holds
-// 64 KiB of K/V per CTA.
-template <int G, int BS>
-using Cfg = AttnCfg<G, BS, 4, (BS == 16 ? 8 : 4)>;
+}  // namespace tc
 
-#define PGD_DISPATCH(G_, BS_, CALL)                     \
-  if (G == G_ && bs == BS_) { using C = Cfg<G_, BS_>; CALL; }
+#define PGD_DISPATCH(CALL)                                          \
+  PGD_CASE(1, 16, CALL) PGD_CASE(2, 16, CALL) PGD_CASE(4, 16, CALL) \
+  PGD_CASE(8, 16, CALL) PGD_CASE(1, 32, CALL) PGD_CASE(2, 32, CALL) \
+  PGD_CASE(4, 32, CALL) PGD_CASE(8, 32, CALL)
 
 int attention_ctas_per_sm(int G, int bs, int B) {
-  PGD_DISPATCH(1, 16, return occupancy_cfg<C>(B))
-  PGD_DISPATCH(2, 16, return occupancy_cfg<C>(B))
-  PGD_DISPATCH(4, 16, return occupancy_cfg<C>(B))
-  PGD_DISPATCH(8, 16, return occupancy_cfg<C>(B))
-  PGD_DISPATCH(1, 32, return occupancy_cfg<C>(B))
-  PGD_DISPATCH(2, 32, return occupancy_cfg<C>(B))
-  PGD_DISPATCH(4, 32, return occupancy_cfg<C>(B))
-  PGD_DISPATCH(8, 32, return occupancy_cfg<C>(B))
+#define PGD_CASE(G_, BS_, CALL) \
+  if (G == G_ && bs == BS_) return tc::occupancy_cfg<G_, BS_>(B);
+  PGD_DISPATCH(0)
+#undef PGD_CASE
   return 0;
 }
 
 cudaError_t attention_launch(const AttnParams &p, int G, int bs, int grid, cudaStream_t stream) {
-  PGD_DISPATCH(1, 16, return launch_cfg<C>(p, grid, stream))
-  PGD_DISPATCH(2, 16, return launch_cfg<C>(p, grid, stream))
-  PGD_DISPATCH(4, 16, return launch_cfg<C>(p, grid, stream))
-  PGD_DISPATCH(8, 16, return launch_cfg<C>(p, grid, stream))
-  PGD_DISPATCH(1, 32, return launch_cfg<C>(p, grid, stream))
-  PGD_DISPATCH(2, 32, return launch_cfg<C>(p, grid, stream))
-  PGD_DISPATCH(4, 32, return launch_cfg<C>(p, grid, stream))
-  PGD_DISPATCH(8, 32, return launch_cfg<C>(p, grid, stream))
+#define PGD_CASE(G_, BS_, CALL) \
+  if (G == G_ && bs == BS_) return tc::launch_cfg<G_, BS_>(p, grid, stream);
+  PGD_DISPATCH(0)
+#undef PGD_CASE
   return cudaErrorInvalidValue;
 }
 

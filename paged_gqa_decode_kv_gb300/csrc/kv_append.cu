@@ -3,10 +3,11 @@
 //
 // kv_append ("LLM inference systems engineering", 2.1.3: the step commits the
 // pending token's K/V; "The math of Transformer inference", section 1: decode
-// appends its own K and V to the cache): for sequence b at position p,
-//   k_cache[table[b][p / bs]][g][p % bs][:] = k_new[b][g][:]   (and V)
-// One warp per (sequence, KV head): lanes 0-15 move the 256-byte K row and
-// lanes 16-31 the V row, 16 bytes each.  A pure copy, bit exact.
+// appends its own K and V to the cache): for sequence b at position p, the
+// token row of slot p % bs in tile (table[b][p / bs], g) becomes k_new[b][g]
+// (and V).  Tiles hold 8 x 8 core matrices, so the 256-byte row is sixteen
+// 16-byte chunks 128 bytes apart.  One warp per (sequence, KV head): lanes
+// 0-15 move the K chunks and lanes 16-31 the V chunks.  A pure copy, bit exact.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -34,13 +35,18 @@ kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_ne
     if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_BLOCK_ID);
     return;
   }
-  const size_t dst = ((((size_t)blk * n_kv + g) * bs) + (p % bs)) * kVecPerRow;
+  // Tile of (blk, g), then the token's slot inside it: 16-byte chunk v of the
+  // row sits in core matrix (slot / 8, v), row slot % 8 -- 128 uint4 per
+  // 8-token group, 8 uint4 per core matrix.
+  const int slot = p % bs;
+  const size_t tile = ((size_t)blk * n_kv + g) * (size_t)bs * kVecPerRow;
   const size_t src = (size_t)row * kVecPerRow;
   const int v = lane & 15;
+  const size_t dst = tile + (size_t)(slot >> 3) * 128 + (size_t)v * 8 + (size_t)(slot & 7);
   if (lane < 16)
-    k_cache[dst + v] = __ldg(k_new + src + v);
+    k_cache[dst] = __ldg(k_new + src + v);
   else
-    v_cache[dst + v] = __ldg(v_new + src + v);
+    v_cache[dst] = __ldg(v_new + src + v);
 }
 
 cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,

@@ -23,6 +23,11 @@ holds every needed block plus 5 % spare blocks; the table is a random
 permutation of it.  Spare blocks, unused tail slots and (when a workload
 appends) the slot of the token about to be appended are NaN, and unused table
 entries are -1, so any read outside the valid range shows up in the output.
+
+Pool layout: bf16 [NB][n_kv][bs/8][d/8][8][8] -- each (block, KV head) tile of
+bs tokens x d dims is stored as 8 x 8 core matrices, element (slot s, dim i)
+at ((s/8)*(d/8) + i/8)*64 + (s%8)*8 + i%8.  ``tile_pool`` / ``untile_pool``
+convert from / to the row-major view [NB][n_kv][bs][d].
 """
 from __future__ import annotations
 
@@ -86,12 +91,28 @@ def context_lengths(w: Workload, seed: int = DATA_SEED) -> List[int]:
     raise ValueError("workload %s has no length rule" % w.name)
 
 
+def tile_pool(x: torch.Tensor) -> torch.Tensor:
+    """Row-major pool [NB][n_kv][bs][d] -> tiled [NB][n_kv][bs/8][d/8][8][8]."""
+    NB, n_kv, bs, d = x.shape
+    return x.reshape(NB, n_kv, bs // 8, 8, d // 8, 8).permute(0, 1, 2, 4, 3, 5).contiguous()
+
+
+def untile_pool(x: torch.Tensor) -> torch.Tensor:
+    """Tiled pool [NB][n_kv][bs/8][d/8][8][8] -> row-major [NB][n_kv][bs][d]."""
+    NB, n_kv, rg, nc = x.shape[:4]
+    return x.permute(0, 1, 2, 4, 3, 5).reshape(NB, n_kv, rg * 8, nc * 8)
+
+
+def pool_shape(num_blocks: int, n_kv: int, block_size: int, head_dim: int = HEAD_DIM):
+    return (num_blocks, n_kv, block_size // 8, head_dim // 8, 8, 8)
+
+
 @dataclasses.dataclass
 class PagedBatch:
     """Inputs of one decode step.  Tensors live on `device`."""
     q: torch.Tensor              # bf16 [B][n_q][d]
-    k_cache: torch.Tensor        # bf16 [NB][n_kv][bs][d]
-    v_cache: torch.Tensor        # bf16 [NB][n_kv][bs][d]
+    k_cache: torch.Tensor        # bf16 [NB][n_kv][bs/8][d/8][8][8] (tiled)
+    v_cache: torch.Tensor        # bf16, same layout
     block_tables: torch.Tensor   # int32 [B][MB], -1 where unused
     context_lens: torch.Tensor   # int32 [B]
     k_new: Optional[torch.Tensor]  # bf16 [B][n_kv][d] when appending
@@ -114,6 +135,11 @@ class PagedBatch:
     @property
     def head_dim(self) -> int:
         return self.q.shape[2]
+
+    def token(self, cache: torch.Tensor, block: int, head: int, slot: int) -> torch.Tensor:
+        """The d-vector of one cached token (slot of a physical block)."""
+        t = cache[block, head, slot // 8, :, slot % 8, :]
+        return t.reshape(-1)
 
     @property
     def num_blocks(self) -> int:
@@ -151,8 +177,9 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
     tokens of every sequence live in the same physical blocks (shared_prefix
     must then be a multiple of block_size, or the partial block is private).
     With append=True, the last token of every sequence is returned as
-    k_new/v_new and its cache slot is left NaN."""
-    assert len(ctx_lens) == batch and n_q % n_kv == 0
+    k_new/v_new and its cache slot is left NaN.  The pool is drawn row-major,
+    poisoned, then tiled."""
+    assert len(ctx_lens) == batch and n_q % n_kv == 0 and block_size % 8 == 0
     bs = block_size
     nblk = [(c + bs - 1) // bs for c in ctx_lens]
     n_shared = shared_prefix // bs if batch > 1 else 0
@@ -206,6 +233,8 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
             k_cache[blk, :, slot, :] = nan
             v_cache[blk, :, slot, :] = nan
     del used_ids
+    k_cache = tile_pool(k_cache)
+    v_cache = tile_pool(v_cache)
 
     return PagedBatch(
         q=q, k_cache=k_cache, v_cache=v_cache,
@@ -232,6 +261,7 @@ def kv_bytes_read(batch: PagedBatch, unique: bool = False) -> int:
     of every sequence, all KV heads, K and V, bf16 (logical), or each physical
     block once (unique; only differs when blocks are shared)."""
     per_token = 2 * batch.n_kv * batch.head_dim * batch.k_cache.element_size()
+    assert batch.k_cache.dim() == 6
     if not unique:
         return int(batch.context_lens.sum().item()) * per_token
     bs = batch.block_size

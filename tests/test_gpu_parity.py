@@ -89,19 +89,21 @@ def test_ctx1_returns_v0_exactly():
     for b in range(4):
         blk = int(pb.block_tables[b, 0])
         for h in range(16):
-            assert torch.equal(got[b, h], pb.v_cache[blk, h // G, 0])
+            assert torch.equal(got[b, h], pb.token(pb.v_cache, blk, h // G, 0))
 
 
 def test_uniform_values():
     pb = _batch(2, 8, 2, 16, [333, 64])
     vec = torch.randn(128, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    vr = inputs.untile_pool(pb.v_cache).clone()
     for b in range(2):
         n = (int(pb.context_lens[b]) + 15) // 16
         ids = pb.block_tables[b, :n].long()
         tail = int(pb.context_lens[b]) % 16
-        pb.v_cache[ids] = vec
+        vr[ids] = vec
         if tail:
-            pb.v_cache[ids[-1], :, tail:] = float("nan")
+            vr[ids[-1], :, tail:] = float("nan")
+    pb.v_cache = inputs.tile_pool(vr)
     got = gpu_attention(pb)
     diff = (got.float() - vec.float()).abs().max().item()
     assert diff <= abs(vec.float()).max().item() * 2 ** -8

@@ -45,9 +45,16 @@ def contiguous_case(B, n_q, n_kv, lens, seed, d=D, kv_std=1.0):
     return q, K, V
 
 
+def tile(x):
+    """Row-major [NB][n_kv][bs][d] -> the pool's tiled layout
+    [NB][n_kv][bs/8][d/8][8][8] (8x8 core matrices), by reshape/permute."""
+    NB, n_kv, bs, d = x.shape
+    return x.reshape(NB, n_kv, bs // 8, 8, d // 8, 8).permute(0, 1, 2, 4, 3, 5).contiguous()
+
+
 def page(K, V, bs, seed, spare=3, share_prefix_blocks=0):
     """Scatter contiguous per-sequence K/V [n_kv][T][d] into a paged pool
-    [NB][n_kv][bs][d] through a random permutation.  Unused blocks, tail slots
+    through a random permutation (built row-major here, then tiled).  Unused blocks, tail slots
     and table entries are poisoned (NaN / -1).  The first
     `share_prefix_blocks` blocks of every sequence are taken from sequence 0
     and stored once."""
@@ -74,7 +81,7 @@ def page(K, V, bs, seed, spare=3, share_prefix_blocks=0):
             t0, t1 = j * bs, min((j + 1) * bs, K[b].shape[1])
             kc[pid, :, : t1 - t0] = K[b][:, t0:t1]
             vc[pid, :, : t1 - t0] = V[b][:, t0:t1]
-    return kc, vc, tables
+    return tile(kc), tile(vc), tables
 
 
 def sdpa_reference(q, K, V, scale):
@@ -93,11 +100,12 @@ def sdpa_reference(q, K, V, scale):
 
 CASES = [
     # B, n_q, n_kv, bs, lens
-    (1, 4, 4, 4, [1]),
-    (2, 8, 2, 4, [5, 16]),
+    (1, 4, 4, 8, [1]),
+    (2, 8, 2, 8, [5, 16]),
     (3, 8, 1, 16, [70, 17, 33]),
     (2, 16, 2, 16, [31, 64]),
-    (3, 4, 2, 4, [3, 9, 12]),
+    (3, 4, 2, 8, [3, 9, 12]),
+    (2, 8, 4, 32, [33, 95]),
 ]
 
 
@@ -132,7 +140,7 @@ def pin_uniform_v(mutation=0):
     V = [v.clone() for v in V]
     for v in V:
         v[:] = vec
-    kc, vc, tab = page(K, V, 4, seed=11)
+    kc, vc, tab = page(K, V, 8, seed=11)
     got = oracle.paged_attention(q, kc, vc, tab, np.array(lens, np.int32), 1 / math.sqrt(D),
                                  mutation=mutation)
     err = np.abs(got - vec.double().numpy()).max()
@@ -154,7 +162,7 @@ def pin_zero_query(mutation=0):
 
 def pin_two_tokens(mutation=0):
     q, K, V = contiguous_case(1, 2, 1, [2], seed=14)
-    kc, vc, tab = page(K, V, 4, seed=15)
+    kc, vc, tab = page(K, V, 8, seed=15)
     scale = 1 / math.sqrt(D)
     got = oracle.paged_attention(q, kc, vc, tab, np.array([2], np.int32), scale,
                                  mutation=mutation)
@@ -282,38 +290,46 @@ def test_lse_merge_closed_form_two_parts():
 
 def test_invalid_inputs_are_rejected():
     q, K, V = contiguous_case(1, 4, 2, [5], seed=50)
-    kc, vc, tab = page(K, V, 4, seed=51)
+    kc, vc, tab = page(K, V, 8, seed=51)
     with pytest.raises(ValueError):
         oracle.paged_attention(q, kc, vc, tab, np.array([0], np.int32), 0.1)
     with pytest.raises(ValueError):
-        oracle.paged_attention(q, kc, vc, tab, np.array([4 * tab.shape[1] + 1], np.int32), 0.1)
+        oracle.paged_attention(q, kc, vc, tab, np.array([8 * tab.shape[1] + 1], np.int32), 0.1)
     bad = tab.copy(); bad[0, 0] = kc.shape[0]
     with pytest.raises(ValueError):
         oracle.paged_attention(q, kc, vc, bad, np.array([5], np.int32), 0.1)
 
 
 def test_kv_append_places_bits():
-    B, n_kv, bs = 3, 2, 4
-    lens = [5, 8, 1]
+    B, n_kv, bs = 3, 2, 8
+    lens = [9, 16, 1]
     q, K, V = contiguous_case(B, 4, n_kv, lens, seed=60)
     kc, vc, tab = page(K, V, bs, seed=61)
     g = torch.Generator().manual_seed(62)
     k_new = bf16(torch.randn(B, n_kv, D, generator=g))
     v_new = bf16(torch.randn(B, n_kv, D, generator=g))
-    pos = np.array([5, 7, 0], np.int32)  # 5: new block slot 1; 7: last slot; 0: overwrite
-    tab = tab.copy()
-    tab[0, 1] = tab[0, 1]  # position 5 is inside block 1 (already held)
+    pos = np.array([9, 15, 0], np.int32)  # 9: slot 1 of block 1; 15: last slot; 0: overwrite
     k2, v2 = oracle.kv_append(kc, vc, k_new, v_new, tab, pos)
-    kb = kc.view(torch.int16).numpy().view(np.uint16)
-    vb = vc.view(torch.int16).numpy().view(np.uint16)
-    kn = k_new.view(torch.int16).numpy().view(np.uint16)
-    vn = v_new.view(torch.int16).numpy().view(np.uint16)
-    expect_k, expect_v = kb.copy(), vb.copy()
+    # expected: untile (test-local inverse permute), write rows, tile again
+    def untile(x):
+        NB, nkv, rg, nc = x.shape[:4]
+        return x.permute(0, 1, 2, 4, 3, 5).reshape(NB, nkv, rg * 8, nc * 8)
+    ek, ev = untile(kc).clone(), untile(vc).clone()
     for b in range(B):
-        blk, slot = tab[b, pos[b] // bs], pos[b] % bs
-        expect_k[blk, :, slot, :] = kn[b]
-        expect_v[blk, :, slot, :] = vn[b]
-    assert np.array_equal(k2, expect_k) and np.array_equal(v2, expect_v)
+        blk, slot = int(tab[b, pos[b] // bs]), int(pos[b] % bs)
+        ek[blk, :, slot, :] = k_new[b]
+        ev[blk, :, slot, :] = v_new[b]
+    want_k = tile(ek).view(torch.int16).numpy().view(np.uint16)
+    want_v = tile(ev).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(k2, want_k) and np.array_equal(v2, want_v)
     # out-of-range position is refused
     with pytest.raises(ValueError):
         oracle.kv_append(kc, vc, k_new, v_new, tab, np.array([5, 7, bs * tab.shape[1]], np.int32))
+
+
+def test_tile_layout_of_one_element():
+    # element (slot 13, dim 77) of a bs=16 tile sits at ((13//8)*16 + 77//8)*64 + (13%8)*8 + 77%8
+    x = torch.zeros(1, 1, 16, 128, dtype=torch.bfloat16)
+    x[0, 0, 13, 77] = 1.0
+    flat = tile(x).reshape(-1)
+    assert int(torch.nonzero(flat).item()) == ((13 // 8) * 16 + 77 // 8) * 64 + (13 % 8) * 8 + 77 % 8
