@@ -75,7 +75,7 @@ typedef enum pgd_status {
 #define PGD_DEVERR_TIMEOUT 8      /* a bounded wait inside a kernel gave up */
 
 /* Largest batch one attention call accepts (larger batches: split the call). */
-#define PGD_MAX_BATCH 4096
+#define PGD_MAX_BATCH 2048
 
 /* Static description of a status code.  Never NULL. */
 const char *pgd_status_string(pgd_status s);
@@ -129,8 +129,10 @@ pgd_status pgd_kv_append(const void *k_new, const void *v_new, void *k_cache, vo
  * Arithmetic: bf16 inputs, fp32 accumulation, fp32 softmax, bf16 output
  * rounded to nearest even.
  *
- * num_splits: 0 = automatic (the work is spread evenly over every SM);
- *   k > 0 = k * B * n_kv parts of (nearly) equal size in blocks.
+ * num_splits: 0 = automatic: one CTA per SM; each first takes an equal share
+ *   of two thirds of all blocks, then takes the rest in small chunks from a
+ *   counter as it finishes, so SMs that stream faster take more;
+ *   k > 0 = k * B * n_kv parts of (nearly) equal size in blocks, fixed.
  * workspace: device scratch of at least pgd_attention_workspace_size(...)
  *   bytes, 256-byte aligned, zero-filled before its first use (cudaMemset);
  *   every completed call leaves its counters at zero again, so one workspace

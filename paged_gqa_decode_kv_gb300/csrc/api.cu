@@ -104,18 +104,22 @@ struct WsLayout {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-long long grid_upper_bound(int32_t B, int32_t n_kv, int32_t num_splits) {
-  if (num_splits > 0) return (long long)num_splits * B * n_kv;
-  return kAutoMaxCtas;
+// Chunks one call can produce: one static share per CTA, plus (automatic
+// split only) at most eight dynamically taken chunks per CTA.
+long long max_chunks(int32_t num_splits, long long grid) {
+  return num_splits > 0 ? grid : 9 * grid;
 }
 
-WsLayout ws_layout(int32_t B, int32_t n_q, int32_t n_kv, int32_t num_splits) {
+// Workspace: [B*n_kv + 1] int32 counters (per-unit arrivals, then the
+// dynamic-chunk counter), then per partial slot (max, sum) and o[G][128].
+// A slot is unit + chunk, so slots = units + chunks.
+WsLayout ws_layout(int32_t B, int32_t n_q, int32_t n_kv, int32_t num_splits, long long grid) {
   WsLayout L;
   const int G = n_q / n_kv;
   const long long units = (long long)B * n_kv;
-  L.slots = units + grid_upper_bound(B, n_kv, num_splits);
+  L.slots = units + max_chunks(num_splits, grid);
   L.counters = 0;
-  L.part_ml = round_up((size_t)units * 4, kWsAlign);
+  L.part_ml = round_up((size_t)(units + 1) * 4, kWsAlign);
   L.part_o = L.part_ml + round_up((size_t)L.slots * G * 2 * 4, kWsAlign);
   L.total = L.part_o + (size_t)L.slots * G * kHeadDim * 4;
   return L;
@@ -176,11 +180,10 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
                             int32_t n_kv, int32_t bs, int32_t MB, int32_t NB, float scale,
                             int32_t num_splits, void *workspace, size_t workspace_bytes,
                             cudaStream_t stream) {
-  const WsLayout L = ws_layout(B, n_q, n_kv, num_splits);
   if (!workspace) return fail(PGD_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(workspace, kWsAlign)) return fail(PGD_ERR_WORKSPACE, "workspace not 256-aligned");
-  if (workspace_bytes < L.total)
-    return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.total);
+  if (workspace_bytes < ws_layout(B, n_q, n_kv, num_splits, 1).total)
+    return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes is too small", workspace_bytes);
   const int G = n_q / n_kv;
   int grid = 0;
   if (num_splits > 0) {
@@ -189,6 +192,9 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
     pgd_status s = auto_grid(G, bs, B, &grid);
     if (s != PGD_OK) return s;
   }
+  const WsLayout L = ws_layout(B, n_q, n_kv, num_splits, grid);
+  if (workspace_bytes < L.total)
+    return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.total);
   int32_t *err = nullptr;
   pgd_status s = error_word(&err);
   if (s != PGD_OK) return s;
@@ -207,6 +213,8 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
   p.NB = NB;
   p.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
   p.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  p.chunk_counter = p.counters + (size_t)B * n_kv;
+  p.dynamic = num_splits == 0 ? 1 : 0;
   p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.err = err;
@@ -284,7 +292,21 @@ pgd_status pgd_kv_append(const void *k_new, const void *v_new, void *k_cache, vo
 size_t pgd_attention_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_t d,
                                     int32_t num_splits) {
   if (B < 0 || n_kv <= 0 || n_q <= 0 || n_q % n_kv || d != kHeadDim || num_splits < 0) return 0;
-  return ws_layout(B, n_q, n_kv, num_splits).total;
+  long long grid = 0;
+  if (num_splits > 0) {
+    grid = (long long)num_splits * B * n_kv;
+  } else {
+    // the automatic grid of the current device (both block sizes), or the
+    // largest automatic grid when no device is usable
+    grid = kAutoMaxCtas;
+    const int G = n_q / n_kv;
+    int g16 = 0, g32 = 0;
+    if (supported_group(G) && auto_grid(G, 16, B, &g16) == PGD_OK &&
+        auto_grid(G, 32, B, &g32) == PGD_OK)
+      grid = g16 > g32 ? g16 : g32;
+    clear_error_detail();
+  }
+  return ws_layout(B, n_q, n_kv, num_splits, grid).total;
 }
 
 int32_t pgd_attention_grid(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t num_splits) {

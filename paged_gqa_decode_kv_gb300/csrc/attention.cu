@@ -40,15 +40,20 @@
 // (the same core matrices read the other way).  Q is written by threads as a
 // K-major, 128-byte-swizzled B operand and P as an MN-major B operand.
 //
-// Roles (224 threads, one CTA per SM):
-//   warps 0-3  softmax + epilogue; thread t owns TMEM lane t (token row t of
-//              S, head-dim row t of O)
+// Roles (384 threads, one CTA per SM):
+//   warps 0-3  softmax; thread t owns TMEM lane t (token row t of S)
 //   warp 4     K producer, warp 5 V producer: bulk copies on the TMA engine,
-//              one tile per lane, table entries prefetched a chunk ahead
-//   warp 6     allocates tensor memory and issues the MMAs (one lane)
+//              one tile per lane, table entries prefetched a chunk ahead; the
+//              K producer also takes the chunks and writes each segment's Q
+//   warp 6     allocates tensor memory and issues q.k^T (one lane)
+//   warp 7     issues p.v (one lane); with two issuers the q.k^T of the next
+//              stages never queues behind the p.v of the current one
+//   warps 8-11 epilogue: per segment, read O from tensor memory and write the
+//              output or a partial state (and merge a unit's partials when
+//              they are complete), off the softmax warps' critical path
 // Rings: 3 K stages and 3 V stages of 32 KiB; a K stage is free as soon as
 // its q.k^T has completed, a V stage after its p.v.  S and P are double
-// buffered by stage parity, O by segment parity.  Every wait is bounded.
+// buffered by stage parity, O and Q by segment parity.  Every wait is bounded.
 //
 // Softmax keeps one reference maximum per head.  A stage moves the reference
 // (and rescales O in tensor memory, after the previous p.v has completed)
@@ -71,8 +76,8 @@ constexpr int TILE_STAGE = TOK * 256;       // K (or V) bytes of one stage: 32 K
 constexpr int NSK = 3, NSV = 3;             // ring depths
 constexpr int Q_BYTES = 2 * NPAD * 128;     // [half][16 rows][128 B], 128B swizzle
 constexpr int P_BYTES = TOK * NPAD * 2;     // [16 token groups][2 head groups][8][16 B]
-constexpr int THREADS = 224;
-constexpr int WARP_KP = 4, WARP_VP = 5, WARP_MMA = 6;
+constexpr int THREADS = 384;
+constexpr int WARP_KP = 4, WARP_VP = 5, WARP_QK = 6, WARP_PV = 7, WARP_EPI = 8;
 constexpr uint32_t TMEM_COLS = 64;
 constexpr float kRescaleLog2 = 8.f;         // move the reference when exceeded by 2^8
 
@@ -80,12 +85,15 @@ constexpr float kRescaleLog2 = 8.f;         // move the reference when exceeded 
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + NSK * TILE_STAGE;
 constexpr int OFF_Q = OFF_V + NSV * TILE_STAGE;
-constexpr int OFF_P = OFF_Q + Q_BYTES;
+constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;  // Q double buffered by segment parity
 constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
 constexpr int OFF_RED = OFF_BAR + 512;      // f32 [2][4][8] warp maxima
-constexpr int OFF_LRED = OFF_RED + 256;     // f32 [4][8] warp sums
-constexpr int OFF_MISC = OFF_LRED + 128;    // tmem base, flags, stage masks
-constexpr int OFF_PRE = OFF_MISC + 64;      // int [B + 1]
+constexpr int OFF_LRED = OFF_RED + 256;     // f32 [2][4][8] warp sums per segment parity
+constexpr int OFF_MREF = OFF_LRED + 256;    // f32 [2][8] reference maxima per segment parity
+constexpr int OFF_MERGE = OFF_MREF + 64;    // float2 [MERGE_PAIRS] partial (max, sum)
+constexpr int MERGE_PAIRS = 128;
+constexpr int OFF_MISC = OFF_MERGE + MERGE_PAIRS * 8;  // tmem base, flags, chunk queue, masks
+constexpr int OFF_PRE = OFF_MISC + 128;     // int [B + 1]
 constexpr int SMEM_SLACK = 1024;
 
 __host__ __device__ constexpr size_t smem_bytes(int B) {
@@ -223,44 +231,170 @@ __device__ __forceinline__ Segment locate(const int *pre, int B, int n_kv, long 
   return s;
 }
 
-// One producer warp (K or V): walks the CTA's stages, copies one tile per
+// Chunk schedule of one call.  Chunks are contiguous ranges of the flattened
+// block space, in index order.  CTA c first takes chunk c (its static share);
+// in dynamic mode it then takes chunks P, P+1, ... from an atomic counter, so
+// SMs that stream faster take more of the remaining work.  Boundaries are a
+// closed form of the chunk index, so every thread can map a chunk to its
+// range and a block position to its chunk.
+struct Schedule {
+  long long X;   // blocks in all units
+  long long P;   // static chunks
+  long long Xs;  // blocks covered by the static chunks
+  long long S1;  // blocks per dynamic chunk
+  long long n1;  // dynamic chunks
+  __device__ __forceinline__ void range(long long i, long long &a, long long &b) const {
+    if (i < P) {
+      a = Xs * i / P;
+      b = Xs * (i + 1) / P;
+    } else {
+      a = Xs + (i - P) * S1;
+      b = a + S1 < X ? a + S1 : X;
+    }
+  }
+  __device__ __forceinline__ long long chunk_of(long long x) const {
+    return x < Xs ? (P * (x + 1) - 1) / Xs : P + (x - Xs) / S1;
+  }
+};
+
+// A role's position in the CTA's sequence of chunks and segments.
+struct SegCursor {
+  long long x = 0, b = 0;  // rest of the current chunk
+  int chunk = -1;
+  int q = 0;               // chunks taken so far
+  bool done = false;
+};
+
+// Next segment (the part of a chunk inside one unit); `fetch` yields the next
+// chunk id (-1 when there is none).  Empty chunks are skipped.
+template <class F>
+__device__ __forceinline__ bool next_segment(SegCursor &c, const Schedule &sc, const int *pre,
+                                             int B, int n_kv, Segment &sg, int &chunk, F fetch) {
+  while (c.x >= c.b) {
+    if (c.done) return false;
+    const int id = fetch(c.q++);
+    if (id < 0) {
+      c.done = true;
+      return false;
+    }
+    long long a, b;
+    sc.range(id, a, b);
+    c.x = a;
+    c.b = b;
+    c.chunk = id;
+  }
+  sg = locate(pre, B, n_kv, c.x, c.b);
+  c.x += sg.n;
+  chunk = c.chunk;
+  return true;
+}
+
+// Chunk queue shared by the roles of a CTA: the K producer pushes ids; the V
+// producer, the two MMA issuers, the four softmax warps and the four epilogue
+// warps (eleven arrivals) pop them.
+struct ChunkQueue {
+  uint64_t *full;        // [4], 1 arrival
+  uint64_t *empty;       // [4], 11 arrivals
+  volatile int *id;      // [4]
+  volatile int *abort_flag;
+  int32_t *err;
+  // Pop chunk number q (all lanes of a warp, or one lane); `arrive` is true
+  // on the one lane that releases the slot.
+  __device__ __forceinline__ int pop(int q, bool arrive, bool warp_wide) const {
+    const int slot = q & 3;
+    wait_or_abort(&full[slot], (uint32_t)(q >> 2) & 1u, abort_flag, err);
+    const int v = *abort_flag ? -1 : id[slot];
+    if (warp_wide) __syncwarp();
+    if (arrive) mbar_arrive(&empty[slot]);
+    return v;
+  }
+  __device__ __forceinline__ void push(int q, int v) const {
+    const int slot = q & 3;
+    wait_or_abort(&empty[slot], ((uint32_t)(q >> 2) & 1u) ^ 1u, abort_flag, err);
+    id[slot] = v;
+    mbar_arrive(&full[slot]);
+  }
+};
+
+// One producer warp (K or V): walks the CTA's stages and copies one tile per
 // lane with the TMA engine.  Block ids come from 32-entry chunks of the table
-// row, each loaded one chunk before it is needed.  The K producer also
-// records which blocks of the stage had an invalid id.
-template <int BS>
-__device__ __forceinline__ void produce(const AttnParams &p, const __nv_bfloat16 *cache,
+// row, each loaded one chunk before it is needed.  The K producer also owns
+// the chunk queue, records which blocks of a stage had an invalid id, and
+// writes each segment's Q (the B operand of q.k^T: K-major, 128-byte swizzle,
+// row = head, two 64-column halves) into buffer k & 1 as the segment starts.
+template <int G, int BS, bool IS_K>
+__device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
+                                        const ChunkQueue &cq, const __nv_bfloat16 *cache,
                                         unsigned char *ring, uint64_t *full, uint64_t *empty,
-                                        int nstages_ring, const int *pre, long long x_begin,
-                                        long long x_end, volatile int *stage_mask,
+                                        int nstages_ring, const int *pre,
+                                        volatile int *stage_mask, unsigned char *qbuf,
+                                        uint64_t *q_ready, uint64_t *q_free,
                                         volatile int *abort_flag, int lane) {
   constexpr int SB = TOK / BS;  // blocks per stage
   constexpr uint32_t TILE_BYTES = BS * 256;
   const uint64_t policy = l2_policy_evict_first();
-  int s = 0;
-  for (long long x = x_begin; x < x_end;) {
-    const Segment sg = locate(pre, p.B, p.n_kv, x, x_end);
+  auto fetch = [&](int q) -> int {
+    if (!IS_K) return cq.pop(q, lane == 0, true);
+    int v = -1;
+    if (lane == 0) {
+      if (q == 0 && blockIdx.x < sc.P) {
+        v = (int)blockIdx.x;
+      } else if (p.dynamic) {
+        const int j = atomicAdd(p.chunk_counter, 1);
+        if (j < sc.n1) {
+          v = (int)(sc.P + j);
+        } else if ((long long)j == sc.n1 + gridDim.x - 1) {
+          atomicExch(p.chunk_counter, 0);  // every CTA has failed once: ready for the next call
+        }
+      }
+      cq.push(q, v);
+    }
+    return __shfl_sync(kFullMask, v, 0);
+  };
+  SegCursor cur;
+  Segment sg;
+  int chunk;
+  int s = 0, k = 0;
+  while (next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch)) {
+    if (IS_K) {
+      const int qb = k & 1;
+      if (lane == 0)
+        wait_or_abort(&q_free[qb], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
+      __syncwarp();
+      for (int j = lane; j < 16 * G; j += 32) {
+        const int r = j >> 4, c = j & 15, half = c >> 3, cc = c & 7;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
+            p.q + ((size_t)sg.b * p.n_q + (size_t)sg.g * G + r) * kHeadDim + c * 8));
+        *reinterpret_cast<uint4 *>(qbuf + qb * Q_BYTES + half * (NPAD * 128) + r * 128 +
+                                   ((cc ^ (r & 7)) << 4)) = v;
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready[qb]);
+    }
+    ++k;
     const int32_t *trow = p.tables + (size_t)sg.b * p.MB + sg.j0;
-    int cur = (lane < sg.n) ? __ldg(trow + lane) : 0;
-    int nxt = (32 + lane < sg.n) ? __ldg(trow + 32 + lane) : 0;
-    int chunk = 0;
+    int tab = (lane < sg.n) ? __ldg(trow + lane) : 0;
+    int tab_next = (32 + lane < sg.n) ? __ldg(trow + 32 + lane) : 0;
+    int tchunk = 0;
     const int nstages = (sg.n + SB - 1) / SB;
     for (int st = 0; st < nstages; ++st, ++s) {
       const int first = st * SB;
-      if ((first >> 5) != chunk) {  // next 32-entry chunk; prefetch the one after
-        chunk = first >> 5;
-        cur = nxt;
-        const int j = (chunk + 1) * 32 + lane;
-        nxt = (j < sg.n) ? __ldg(trow + j) : 0;
+      if ((first >> 5) != tchunk) {  // next 32 table entries; prefetch the ones after
+        tchunk = first >> 5;
+        tab = tab_next;
+        const int j = (tchunk + 1) * 32 + lane;
+        tab_next = (j < sg.n) ? __ldg(trow + j) : 0;
       }
       const int nb = min(SB, sg.n - first);
-      const int blk = __shfl_sync(kFullMask, cur, (first & 31) + (lane & (SB - 1)));
+      const int blk = __shfl_sync(kFullMask, tab, (first & 31) + (lane & (SB - 1)));
       const bool ok = lane < nb && (unsigned)blk < (unsigned)p.NB;
       const unsigned okmask = __ballot_sync(kFullMask, ok);
       const unsigned want = (1u << nb) - 1u;
       const int slot = s % nstages_ring;
       if (lane == 0) {
         wait_or_abort(&empty[slot], ((uint32_t)(s / nstages_ring) & 1u) ^ 1u, abort_flag, p.err);
-        if (stage_mask) {
+        if (IS_K) {
           stage_mask[s & 7] = (int)(want & ~okmask);
           if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
         }
@@ -272,12 +406,12 @@ __device__ __forceinline__ void produce(const AttnParams &p, const __nv_bfloat16
       }
       __syncwarp();
       if (ok && !*abort_flag) {
-        const __nv_bfloat16 *src = cache + ((size_t)blk * p.n_kv + sg.g) * (size_t)(BS * kHeadDim);
+        const __nv_bfloat16 *src =
+            cache + ((size_t)blk * p.n_kv + sg.g) * (size_t)(BS * kHeadDim);
         bulk_copy_g2s(ring + (size_t)slot * TILE_STAGE + (size_t)lane * TILE_BYTES, src,
                       TILE_BYTES, &full[slot], policy);
       }
     }
-    x += sg.n;
   }
   // no copy may still be landing when the CTA exits
   if (lane == 0) {
@@ -310,14 +444,20 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   uint64_t *o_full = p_free + 2;        // [2]
   uint64_t *o_free = o_full + 2;        // [2]
   uint64_t *m_ready = o_free + 2;       // [2]
-  uint64_t *q_ready = m_ready + 2;      // [1]
-  uint64_t *done = q_ready + 1;         // [1]
+  uint64_t *q_ready = m_ready + 2;      // [2] per Q buffer
+  uint64_t *q_free = q_ready + 2;       // [2] per Q buffer
+  uint64_t *done = q_free + 2;          // [2] one per MMA issuer
+  uint64_t *cq_full = done + 2;         // [4]
+  uint64_t *cq_empty = cq_full + 4;     // [4]
+  uint64_t *seg_done = cq_empty + 4;    // [2] softmax -> epilogue, per segment parity
   float *red = reinterpret_cast<float *>(smem + OFF_RED);
   float *lred = reinterpret_cast<float *>(smem + OFF_LRED);
+  float *mref = reinterpret_cast<float *>(smem + OFF_MREF);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
   volatile int *flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);         // [3]
-  volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 32);  // [8]
+  volatile int *cq_id = reinterpret_cast<volatile int *>(smem + OFF_MISC + 20);       // [4]
+  volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 40);  // [8]
   int *pre = reinterpret_cast<int *>(smem + OFF_PRE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -339,16 +479,24 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
       mbar_init(&o_full[i], 1);
       mbar_init(&o_free[i], 4);
       mbar_init(&m_ready[i], 1);
+      mbar_init(&done[i], 1);
+      mbar_init(&seg_done[i], 4);
     }
-    mbar_init(q_ready, 4);
-    mbar_init(done, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&cq_full[i], 1);
+      mbar_init(&cq_empty[i], 11);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_ready[i], 1);
+      mbar_init(&q_free[i], 1);
+    }
     mbar_init_fence();
     *abort_flag = 0;
   }
   // Q pad rows and P pad columns stay zero for the whole kernel.
   {
     uint4 *z = reinterpret_cast<uint4 *>(smem + OFF_Q);
-    for (int i = tid; i < (Q_BYTES + 2 * P_BYTES) / 16; i += THREADS) z[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < (2 * Q_BYTES + 2 * P_BYTES) / 16; i += THREADS) z[i] = make_uint4(0, 0, 0, 0);
   }
   // Blocks per sequence, then an exclusive prefix over the batch.
   const int max_tokens = p.MB * BS;
@@ -360,7 +508,7 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
     pre[b + 1] = nb;
   }
   if (bad_ctx && blockIdx.x == 0) atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
-  if (warp == WARP_MMA) {
+  if (warp == WARP_QK) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(TMEM_COLS)
@@ -389,139 +537,141 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const long long X = (long long)p.n_kv * pre[p.B];
-  const long long P = X < (long long)gridDim.x ? X : (long long)gridDim.x;
-  const long long cta = blockIdx.x;
-  long long x_begin = 0, x_end = 0;
-  if (cta < P) {  // more CTAs than blocks: the spare ones have nothing to do
-    x_begin = X * cta / P;
-    x_end = X * (cta + 1) / P;
+  Schedule sc;
+  sc.X = (long long)p.n_kv * pre[p.B];
+  if (p.dynamic) {
+    // two thirds of the blocks as equal static shares, the rest in chunks of
+    // about 1/8 of the CTA's mean remaining share (at least one stage)
+    sc.P = gridDim.x;
+    long long xs = sc.X * 2 / 3;
+    if (xs < sc.P) xs = 0;
+    sc.Xs = xs;
+    const long long rest = sc.X - xs;
+    long long s1 = (rest + 8 * sc.P - 1) / (8 * sc.P);
+    s1 = (s1 + SB - 1) / SB * SB;  // whole stages
+    if (s1 < SB) s1 = SB;
+    sc.S1 = s1;
+    sc.n1 = (rest + s1 - 1) / s1;
+  } else {
+    // caller-fixed split: gridDim.x equal shares (no more than one per block)
+    sc.P = sc.X < (long long)gridDim.x ? sc.X : (long long)gridDim.x;
+    sc.Xs = sc.X;
+    sc.S1 = 1;
+    sc.n1 = 0;
   }
+  ChunkQueue cq{cq_full, cq_empty, cq_id, abort_flag, p.err};
 
   if (warp == WARP_KP) {
-    produce<BS>(p, p.k_cache, smem + OFF_K, full_k, empty_k, NSK, pre, x_begin, x_end,
-                stage_mask, abort_flag, lane);
+    produce<G, BS, true>(p, sc, cq, p.k_cache, smem + OFF_K, full_k, empty_k, NSK, pre,
+                         stage_mask, smem + OFF_Q, q_ready, q_free, abort_flag, lane);
   } else if (warp == WARP_VP) {
-    produce<BS>(p, p.v_cache, smem + OFF_V, full_v, empty_v, NSV, pre, x_begin, x_end, nullptr,
-                abort_flag, lane);
-  } else if (warp == WARP_MMA) {
-    // ----------------------------------------------------------------- MMA
+    produce<G, BS, false>(p, sc, cq, p.v_cache, smem + OFF_V, full_v, empty_v, NSV, pre, nullptr,
+                          nullptr, nullptr, nullptr, abort_flag, lane);
+  } else if (warp == WARP_QK) {
+    // ---------------------------------------------------- q.k^T issuer
     if (lane == 0) {
       const uint32_t q_base = smem_addr(smem + OFF_Q);
-      int s_qk = 0, s_pv = 0;    // next stage for q.k^T and for p.v
-      int k_qk = 0, k_pv = 0;    // their segment index
-      int st_qk = 0, st_pv = 0;  // their stage index within the segment
-      long long x_qk = x_begin, x_pv = x_begin;
-      Segment seg_qk, seg_pv;
-      int ns_qk = 0, ns_pv = 0;
-      if (x_qk < x_end) {
-        seg_qk = locate(pre, p.B, p.n_kv, x_qk, x_end);
-        ns_qk = (seg_qk.n + SB - 1) / SB;
-        seg_pv = seg_qk;
-        ns_pv = ns_qk;
-      }
-      auto issue_qk = [&]() {
-        const int slot = s_qk % NSK, sb = s_qk & 1;
-        if (st_qk == 0) wait_or_abort(q_ready, (uint32_t)k_qk & 1u, abort_flag, p.err);
-        wait_or_abort(&full_k[slot], (uint32_t)(s_qk / NSK) & 1u, abort_flag, p.err);
-        wait_or_abort(&s_free[sb], ((uint32_t)(s_qk >> 1) & 1u) ^ 1u, abort_flag, p.err);
-        tc_fence_after();
-        if (!*abort_flag) {
-          const uint32_t k_base = smem_addr(smem + OFF_K + slot * TILE_STAGE);
+      auto fetch = [&](int q) { return cq.pop(q, true, false); };
+      SegCursor cur;
+      Segment sg;
+      int chunk;
+      int s = 0, k = 0;
+      while (next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch)) {
+        const int nstages = (sg.n + SB - 1) / SB;
+        // Q of segment k is in buffer k & 1 (written by the K producer); it is
+        // rewritten for segment k + 2 only after q_free signals that every
+        // q.k^T of segment k has completed.
+        wait_or_abort(&q_ready[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
+        const uint32_t q_seg = q_base + (uint32_t)((k & 1) * Q_BYTES);
+        for (int st = 0; st < nstages; ++st, ++s) {
+          const int slot = s % NSK, sb = s & 1;
+          wait_or_abort(&full_k[slot], (uint32_t)(s / NSK) & 1u, abort_flag, p.err);
+          wait_or_abort(&s_free[sb], ((uint32_t)(s >> 1) & 1u) ^ 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (!*abort_flag) {
+            // Descriptors are built once; a k-step only moves the start
+            // address (the low field, in 16-byte units): K by 256 B, Q by 32 B
+            // within a 128-byte swizzle row and by 2048 B to the second half.
+            const uint64_t kd =
+                smem_desc(smem_addr(smem + OFF_K + slot * TILE_STAGE), 128, 2048, 0);
+            const uint64_t qd = smem_desc(q_seg, 16, 1024, 2);
+            const uint32_t dS = tmem + col_s(sb);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t qoff = (uint32_t)((kk >> 2) * (NPAD * 128) + (kk & 3) * 32);
-            umma_bf16(tmem + col_s(sb), smem_desc(k_base + kk * 256, 128, 2048, 0),
-                      smem_desc(q_base + qoff, 16, 1024, 2), IDESC_QK, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk)
+              umma_bf16(dS, kd + (uint64_t)(kk * 16),
+                        qd + (uint64_t)((kk >> 2) * 128 + (kk & 3) * 2), IDESC_QK,
+                        kk > 0 ? 1u : 0u);
           }
+          umma_commit(&s_full[sb]);
+          umma_commit(&empty_k[slot]);
+          // Hand the stage's invalid-block mask (written by the K producer
+          // before it armed full_k, which this thread acquired) to the softmax.
+          mbar_arrive(&m_ready[sb]);
         }
-        umma_commit(&s_full[sb]);
-        umma_commit(&empty_k[slot]);
-        // Hand the stage's invalid-block mask (written by the K producer before
-        // it armed full_k, which this thread acquired) on to the softmax.
-        mbar_arrive(&m_ready[sb]);
-        ++s_qk;
-        if (++st_qk == ns_qk) {
-          st_qk = 0;
-          ++k_qk;
-          x_qk += seg_qk.n;
-          if (x_qk < x_end) {
-            seg_qk = locate(pre, p.B, p.n_kv, x_qk, x_end);
-            ns_qk = (seg_qk.n + SB - 1) / SB;
-          }
-        }
-      };
-      if (x_qk < x_end) issue_qk();
-      while (x_pv < x_end) {
-        if (x_qk < x_end) issue_qk();  // q.k^T of the next stage overlaps this softmax
-        const int slot = s_pv % NSV, sb = s_pv & 1, ob = k_pv & 1;
-        wait_or_abort(&p_full[sb], (uint32_t)(s_pv >> 1) & 1u, abort_flag, p.err);
-        wait_or_abort(&full_v[slot], (uint32_t)(s_pv / NSV) & 1u, abort_flag, p.err);
-        if (st_pv == 0)
-          wait_or_abort(&o_free[ob], ((uint32_t)(k_pv >> 1) & 1u) ^ 1u, abort_flag, p.err);
-        tc_fence_after();
-        if (!*abort_flag) {
-          const uint32_t v_base = smem_addr(smem + OFF_V + slot * TILE_STAGE);
-          const uint32_t p_base = smem_addr(smem + OFF_P + sb * P_BYTES);
-#pragma unroll
-          for (int kt = 0; kt < 8; ++kt) {
-            umma_bf16(tmem + col_o(ob), smem_desc(v_base + kt * 4096, 2048, 128, 0),
-                      smem_desc(p_base + kt * 512, 256, 128, 0), IDESC_PV,
-                      (st_pv > 0 || kt > 0) ? 1u : 0u);
-          }
-        }
-        umma_commit(&empty_v[slot]);
-        umma_commit(&p_free[sb]);
-        const bool last = (st_pv + 1 == ns_pv);
-        if (last) umma_commit(&o_full[ob]);
-        ++s_pv;
-        if (last) {
-          st_pv = 0;
-          ++k_pv;
-          x_pv += seg_pv.n;
-          if (x_pv < x_end) {
-            seg_pv = locate(pre, p.B, p.n_kv, x_pv, x_end);
-            ns_pv = (seg_pv.n + SB - 1) / SB;
-          }
-        } else {
-          ++st_pv;
-        }
+        umma_commit(&q_free[k & 1]);  // Q buffer reusable once these q.k^T complete
+        ++k;
       }
       // every MMA has completed before tensor memory is released
-      if (s_qk > 0) {
-        umma_commit(done);
-        mbar_wait_bounded(done, 0);
+      if (s > 0) {
+        umma_commit(&done[0]);
+        mbar_wait_bounded(&done[0], 0);
       }
     }
-    __syncwarp();
-  } else {
-    // ------------------------------------------------- softmax + epilogue
-    const int t = tid;  // 0..127: token row of S, head-dim row of O
+  } else if (warp == WARP_PV) {
+    // ------------------------------------------------------- p.v issuer
+    if (lane == 0) {
+      auto fetch = [&](int q) { return cq.pop(q, true, false); };
+      SegCursor cur;
+      Segment sg;
+      int chunk;
+      int s = 0, k = 0;
+      while (next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch)) {
+        const int nstages = (sg.n + SB - 1) / SB;
+        const int ob = k & 1;
+        for (int st = 0; st < nstages; ++st, ++s) {
+          const int slot = s % NSV, sb = s & 1;
+          wait_or_abort(&p_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+          wait_or_abort(&full_v[slot], (uint32_t)(s / NSV) & 1u, abort_flag, p.err);
+          if (st == 0)
+            wait_or_abort(&o_free[ob], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (!*abort_flag) {
+            // 16 tokens per k-step: V moves by 4096 B, P by 512 B.
+            const uint64_t vd =
+                smem_desc(smem_addr(smem + OFF_V + slot * TILE_STAGE), 2048, 128, 0);
+            const uint64_t pd = smem_desc(smem_addr(smem + OFF_P + sb * P_BYTES), 256, 128, 0);
+            const uint32_t dO = tmem + col_o(ob);
+            const uint32_t acc0 = st > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt)
+              umma_bf16(dO, vd + (uint64_t)(kt * 256), pd + (uint64_t)(kt * 32), IDESC_PV,
+                        kt > 0 ? 1u : acc0);
+          }
+          umma_commit(&empty_v[slot]);
+          umma_commit(&p_free[sb]);
+          if (st + 1 == nstages) umma_commit(&o_full[ob]);
+        }
+        ++k;
+      }
+      if (s > 0) {
+        umma_commit(&done[1]);
+        mbar_wait_bounded(&done[1], 0);
+      }
+    }
+  } else if (warp < 4) {
+    // ----------------------------------------------------------- softmax
+    const int t = tid;  // 0..127: token row of S
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     constexpr int NCT = 128;
-    int s = 0, k = 0;
-    long long x = x_begin;
+    auto fetch = [&](int q) { return cq.pop(q, lane == 0, true); };
+    SegCursor cur;
     Segment sg;
-    if (x < x_end) sg = locate(pre, p.B, p.n_kv, x, x_end);
+    int chunk = -1;
+    int s = 0, k = 0;
 
-    // Q of a segment into the B operand buffer: K-major, 128-byte swizzle,
-    // row = head, two 64-column halves.
-    auto write_q = [&](const Segment &q) {
-      if (t < 16 * G) {
-        const int r = t >> 4, c = t & 15, half = c >> 3, cc = c & 7;
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
-            p.q + ((size_t)q.b * p.n_q + (size_t)q.g * G + r) * kHeadDim + c * 8));
-        *reinterpret_cast<uint4 *>(smem + OFF_Q + half * (NPAD * 128) + r * 128 +
-                                   ((cc ^ (r & 7)) << 4)) = v;
-      }
-      fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_ready);
-    };
-    if (x < x_end) write_q(sg);
+    bool have = next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch);
 
-    while (x < x_end) {
-      const int unit = sg.b * p.n_kv + sg.g;
+    while (have) {
       const int ctx_b = __ldg(p.ctx + sg.b);
       const int nstages = (sg.n + SB - 1) / SB;
       const int ob = k & 1;
@@ -538,7 +688,7 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
 
         wait_or_abort(&s_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
         // Invalid-block mask of this stage: the K producer wrote it before
-        // arming full_k; the MMA thread acquired full_k and then released
+        // arming full_k; the q.k^T issuer acquired full_k and then released
         // m_ready.  (Waiting on full_k here could alias: a K stage is freed
         // after its q.k^T, so full_k may run two phases ahead.)  m_ready and
         // the 8-entry mask ring cannot move on before this stage frees its S
@@ -553,14 +703,14 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
         if (lane == 0) mbar_arrive(&s_free[sb]);
 
         const bool valid = (t < nvalid) && !((mask >> (t / BS)) & 1);
-        float sc[G];
+        float sc_[G];
 #pragma unroll
-        for (int h = 0; h < G; ++h) sc[h] = valid ? sv[h] * p.qk_scale_log2 : -INFINITY;
+        for (int h = 0; h < G; ++h) sc_[h] = valid ? sv[h] * p.qk_scale_log2 : -INFINITY;
 
         // tile maximum per head across the 128 rows
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float wm = warp_max(sc[h]);
+          const float wm = warp_max(sc_[h]);
           if (lane == 0) red[(sb * 4 + warp) * 8 + h] = wm;
         }
         named_barrier_sync(1, NCT);
@@ -599,7 +749,7 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
         uint32_t packed[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float pv = valid ? exp2f(sc[h] - m_ref[h]) : 0.f;
+          const float pv = valid ? exp2f(sc_[h] - m_ref[h]) : 0.f;
           const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
           l_part[h] += __bfloat162float(pb);
           packed[h >> 1] |= (uint32_t)__bfloat16_as_ushort(pb) << ((h & 1) * 16);
@@ -623,24 +773,49 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
         if (lane == 0) mbar_arrive(&p_full[sb]);
       }
 
-      // ---- end of segment: next Q, then the epilogue
-      const long long x_next = x + sg.n;
-      Segment next = sg;
-      if (x_next < x_end) {
-        next = locate(pre, p.B, p.n_kv, x_next, x_end);
-        write_q(next);
-      }
-      float L[G];
+      // ---- end of segment: hand the segment's reference maxima and per-warp
+      // sums to the epilogue warps.
+      Segment nsg;
+      int nchunk = -1;
+      const bool have_next = next_segment(cur, sc, pre, p.B, p.n_kv, nsg, nchunk, fetch);
+      // lred/mref[ob] were last read by the epilogue of segment k - 2, which
+      // then released O buffer ob
+      wait_or_abort(&o_free[ob], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float ws = warp_sum(l_part[h]);
-        if (lane == 0) lred[warp * 8 + h] = ws;
+        if (lane == 0) lred[(ob * 4 + warp) * 8 + h] = ws;
+        if (t == 0) mref[ob * 8 + h] = m_ref[h];
       }
-      named_barrier_sync(1, NCT);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&seg_done[ob]);
+      sg = nsg;
+      chunk = nchunk;
+      have = have_next;
+      ++k;
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int e = tid - 32 * WARP_EPI;  // 0..127: head-dim row of O
+    const int ew = warp - WARP_EPI;     // TMEM lane quadrant
+    const uint32_t lane_base = (uint32_t)(ew * 32) << 16;
+    constexpr int NET = 128;
+    auto fetch = [&](int q) { return cq.pop(q, lane == 0, true); };
+    SegCursor cur;
+    Segment sg;
+    int chunk = -1;
+    int k = 0;
+    while (next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch)) {
+      const int ob = k & 1;
+      const int unit = sg.b * p.n_kv + sg.g;
+      wait_or_abort(&seg_done[ob], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
+      float L[G], M[G];
 #pragma unroll
-      for (int h = 0; h < G; ++h)
-        L[h] = (lred[0 * 8 + h] + lred[1 * 8 + h]) + (lred[2 * 8 + h] + lred[3 * 8 + h]);
-
+      for (int h = 0; h < G; ++h) {
+        L[h] = (lred[(ob * 4 + 0) * 8 + h] + lred[(ob * 4 + 1) * 8 + h]) +
+               (lred[(ob * 4 + 2) * 8 + h] + lred[(ob * 4 + 3) * 8 + h]);
+        M[h] = mref[ob * 8 + h];
+      }
       wait_or_abort(&o_full[ob], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
       tc_fence_after();
       float ov[8];
@@ -649,26 +824,27 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[ob]);
 
-      const bool whole = (x == sg.unit_start) && (x + sg.n == sg.unit_end);
+      const long long seg_start = sg.unit_start + sg.j0;
+      const bool whole = (seg_start == sg.unit_start) && (seg_start + sg.n == sg.unit_end);
       const size_t out_row = (size_t)sg.b * p.n_q + (size_t)sg.g * G;
       if (whole) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
-          p.out[(out_row + h) * kHeadDim + t] = __float2bfloat16_rn(ov[h] / L[h]);
+          p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(ov[h] / L[h]);
       } else {
-        const size_t srow = ((size_t)unit + (size_t)cta) * G;
+        const size_t srow = ((size_t)unit + (size_t)chunk) * G;
 #pragma unroll
-        for (int h = 0; h < G; ++h) p.part_o[(srow + h) * kHeadDim + t] = ov[h];
+        for (int h = 0; h < G; ++h) p.part_o[(srow + h) * kHeadDim + e] = ov[h];
 #pragma unroll
         for (int h = 0; h < G; ++h)
-          if (t == h)
-            *reinterpret_cast<float2 *>(p.part_ml + (srow + h) * 2) = make_float2(m_ref[h], L[h]);
+          if (e == h)
+            *reinterpret_cast<float2 *>(p.part_ml + (srow + h) * 2) = make_float2(M[h], L[h]);
         // publish this part; the last part of the unit to arrive merges all
         __threadfence();
-        named_barrier_sync(1, NCT);
-        if (t == 0) {
-          const long long c_first = (P * (sg.unit_start + 1) - 1) / X;
-          const long long c_last = (P * sg.unit_end - 1) / X;
+        named_barrier_sync(2, NET);
+        if (e == 0) {
+          const long long c_first = sc.chunk_of(sg.unit_start);
+          const long long c_last = sc.chunk_of(sg.unit_end - 1);
           const int n_parts = (int)(c_last - c_first + 1);
           const int before = atomicAdd(p.counters + unit, 1);
           const int last = (before == n_parts - 1);
@@ -677,32 +853,54 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
           flag[1] = (int)c_first;
           flag[2] = n_parts;
         }
-        named_barrier_sync(1, NCT);
+        named_barrier_sync(2, NET);
         if (flag[0]) {
           __threadfence();
           const int c_first = flag[1], n_parts = flag[2];
           const size_t row0 = ((size_t)unit + (size_t)c_first) * G;
+          float2 *mlb = reinterpret_cast<float2 *>(smem + OFF_MERGE);
+          constexpr int PPB = MERGE_PAIRS / G;  // parts per batch
+          float Mx[G], Lm[G], O[G];
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            float M = -INFINITY;
-            for (int i = 0; i < n_parts; ++i)
-              M = fmaxf(M, __ldcg(p.part_ml + (row0 + (size_t)i * G + h) * 2));
-            float Lm = 0.f, O = 0.f;
-            for (int i = 0; i < n_parts; ++i) {
-              const size_t r = row0 + (size_t)i * G + h;
-              const float mi = __ldcg(p.part_ml + r * 2);
-              if (mi == -INFINITY) continue;
-              const float cf = exp2f(mi - M);
-              Lm = fmaf(cf, __ldcg(p.part_ml + r * 2 + 1), Lm);
-              O = fmaf(cf, __ldcg(p.part_o + r * kHeadDim + t), O);
+          for (int h = 0; h < G; ++h) { Mx[h] = -INFINITY; Lm[h] = 0.f; O[h] = 0.f; }
+          for (int base = 0; base < n_parts; base += PPB) {
+            const int nb = min(PPB, n_parts - base);
+            // the (max, sum) of every part and head of the batch, one load each
+            for (int j = e; j < nb * G; j += NET)
+              mlb[j] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + row0 + (size_t)base * G + j);
+            named_barrier_sync(2, NET);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              float bm = Mx[h];
+              for (int i = 0; i < nb; ++i) bm = fmaxf(bm, mlb[i * G + h].x);
+              if (bm != Mx[h] && Mx[h] != -INFINITY) {
+                const float cf = exp2f(Mx[h] - bm);
+                Lm[h] *= cf;
+                O[h] *= cf;
+              }
+              Mx[h] = bm;
             }
-            p.out[(out_row + h) * kHeadDim + t] = __float2bfloat16_rn(O / Lm);
+#pragma unroll 4
+            for (int i = 0; i < nb; ++i) {
+              const size_t r = row0 + (size_t)(base + i) * G;
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+                const float2 ml = mlb[i * G + h];
+                const float o = __ldcg(p.part_o + (r + h) * kHeadDim + e);
+                if (ml.x == -INFINITY) continue;
+                const float cf = exp2f(ml.x - Mx[h]);
+                Lm[h] = fmaf(cf, ml.y, Lm[h]);
+                O[h] = fmaf(cf, o, O[h]);
+              }
+            }
+            named_barrier_sync(2, NET);  // mlb is reused by the next batch
           }
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(O[h] / Lm[h]);
         }
+        named_barrier_sync(2, NET);  // flags are reused by the next segment
       }
-      named_barrier_sync(1, NCT);  // lred / flags are reused by the next segment
-      x = x_next;
-      sg = next;
       ++k;
     }
   }
@@ -710,7 +908,7 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == WARP_MMA) {
+  if (warp == WARP_QK) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(TMEM_COLS)
                  : "memory");

@@ -101,7 +101,8 @@ def test_kv_append_rejects_on_host(L):
 
 
 def test_workspace_size_grows_with_splits(L):
-    a = pgd.workspace_size(16, 32, 8, 0)
+    assert pgd.workspace_size(16, 32, 8, 0) > 0
+    a = pgd.workspace_size(16, 32, 8, 1)
     b = pgd.workspace_size(16, 32, 8, 64)
     assert 0 < a < b
     assert pgd.workspace_size(16, 32, 8, 0, d=64) == 0
