@@ -129,9 +129,11 @@ pgd_status pgd_kv_append(const void *k_new, const void *v_new, void *k_cache, vo
  * Arithmetic: bf16 inputs, fp32 accumulation, fp32 softmax, bf16 output
  * rounded to nearest even.
  *
- * num_splits: 0 = automatic: one CTA per SM; each first takes an equal share
- *   of two thirds of all blocks, then takes the rest in small chunks from a
- *   counter as it finishes, so SMs that stream faster take more;
+ * num_splits: 0 = automatic: one CTA per SM; the kernel reads the context
+ *   lengths and either gives each (sequence, KV head) to one CTA whole (when
+ *   there are no more of them than CTAs and the longest is short enough to
+ *   hide behind the total HBM traffic) or cuts all blocks into one part of
+ *   (nearly) equal size per CTA;
  *   k > 0 = k * B * n_kv parts of (nearly) equal size in blocks, fixed.
  * workspace: device scratch of at least pgd_attention_workspace_size(...)
  *   bytes, 256-byte aligned, zero-filled before its first use (cudaMemset);

@@ -104,22 +104,16 @@ struct WsLayout {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Chunks one call can produce: one static share per CTA, plus (automatic
-// split only) at most eight dynamically taken chunks per CTA.
-long long max_chunks(int32_t num_splits, long long grid) {
-  return num_splits > 0 ? grid : 9 * grid;
-}
-
-// Workspace: [B*n_kv + 1] int32 counters (per-unit arrivals, then the
-// dynamic-chunk counter), then per partial slot (max, sum) and o[G][128].
-// A slot is unit + chunk, so slots = units + chunks.
-WsLayout ws_layout(int32_t B, int32_t n_q, int32_t n_kv, int32_t num_splits, long long grid) {
+// Workspace: [B*n_kv] int32 per-unit arrival counters, then per partial slot
+// (max, sum) and o[G][128].  A slot is unit + part (one part per CTA), so
+// slots = units + CTAs.
+WsLayout ws_layout(int32_t B, int32_t n_q, int32_t n_kv, long long grid) {
   WsLayout L;
   const int G = n_q / n_kv;
   const long long units = (long long)B * n_kv;
-  L.slots = units + max_chunks(num_splits, grid);
+  L.slots = units + grid;
   L.counters = 0;
-  L.part_ml = round_up((size_t)(units + 1) * 4, kWsAlign);
+  L.part_ml = round_up((size_t)units * 4, kWsAlign);
   L.part_o = L.part_ml + round_up((size_t)L.slots * G * 2 * 4, kWsAlign);
   L.total = L.part_o + (size_t)L.slots * G * kHeadDim * 4;
   return L;
@@ -182,7 +176,7 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
                             cudaStream_t stream) {
   if (!workspace) return fail(PGD_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(workspace, kWsAlign)) return fail(PGD_ERR_WORKSPACE, "workspace not 256-aligned");
-  if (workspace_bytes < ws_layout(B, n_q, n_kv, num_splits, 1).total)
+  if (workspace_bytes < ws_layout(B, n_q, n_kv, 1).total)
     return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes is too small", workspace_bytes);
   const int G = n_q / n_kv;
   int grid = 0;
@@ -192,7 +186,7 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
     pgd_status s = auto_grid(G, bs, B, &grid);
     if (s != PGD_OK) return s;
   }
-  const WsLayout L = ws_layout(B, n_q, n_kv, num_splits, grid);
+  const WsLayout L = ws_layout(B, n_q, n_kv, grid);
   if (workspace_bytes < L.total)
     return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.total);
   int32_t *err = nullptr;
@@ -213,8 +207,7 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
   p.NB = NB;
   p.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
   p.counters = reinterpret_cast<int32_t *>(ws + L.counters);
-  p.chunk_counter = p.counters + (size_t)B * n_kv;
-  p.dynamic = num_splits == 0 ? 1 : 0;
+  p.auto_split = num_splits == 0 ? 1 : 0;
   p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.err = err;
@@ -306,7 +299,7 @@ size_t pgd_attention_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_
       grid = g16 > g32 ? g16 : g32;
     clear_error_detail();
   }
-  return ws_layout(B, n_q, n_kv, num_splits, grid).total;
+  return ws_layout(B, n_q, n_kv, grid).total;
 }
 
 int32_t pgd_attention_grid(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t num_splits) {

@@ -11,16 +11,21 @@
 //
 // Work split.  A unit is one (sequence, KV head); its K/V tiles are read once
 // and serve all G query heads.  The units' blocks are laid end to end
-// (sequence-major, then KV head, then block) into one range of X blocks and
-// CTA c of P takes blocks [X*c/P, X*(c+1)/P): every CTA streams the same bytes
-// (+-1 block) whatever the length mix.  A CTA walks its range unit by unit
-// ("segments").  A segment that covers a whole unit writes the output;
-// otherwise it writes its (max, sum, weighted sum) state and the last CTA of
-// the unit to arrive merges the states by log-sum-exp ("The math of
-// Transformer inference", section 8: split the sequence, attend locally,
-// merge by log-sum-exp; the running-state update is the one in "LLM
-// inference systems engineering", 2.8.3).  Arrival is an atomic counter per
-// unit; no CTA waits for another.
+// (sequence-major, then KV head, then block) into one range of X blocks, cut
+// into one contiguous part per CTA in one of two ways, chosen by every CTA
+// alike from the context lengths:
+//   units     CTA c takes unit c whole (when there are no more units than
+//             CTAs and the longest unit still streams no longer than the
+//             whole job takes at the HBM rate): no partial states at all;
+//   balanced  CTA c of P takes blocks [X*c/P, X*(c+1)/P): every CTA streams
+//             the same bytes (+-1 block) whatever the length mix.
+// A CTA walks its part unit by unit ("segments").  A segment that covers a
+// whole unit writes the output; otherwise it writes its (max, sum, weighted
+// sum) state and the last CTA of the unit to arrive merges the states by
+// log-sum-exp ("The math of Transformer inference", section 8: split the
+// sequence, attend locally, merge by log-sum-exp; the running-state update is
+// the one in "LLM inference systems engineering", 2.8.3).  Arrival is an
+// atomic counter per unit; no CTA waits for another.
 //
 // The two contractions of a 128-token stage run on the tensor cores with
 // tokens on the M side (decode attention is HBM bound; on CUDA cores the
@@ -43,8 +48,8 @@
 // Roles (384 threads, one CTA per SM):
 //   warps 0-3  softmax; thread t owns TMEM lane t (token row t of S)
 //   warp 4     K producer, warp 5 V producer: bulk copies on the TMA engine,
-//              one tile per lane, table entries prefetched a chunk ahead; the
-//              K producer also takes the chunks and writes each segment's Q
+//              one tile per lane, table entries prefetched 32 ahead; the K
+//              producer also writes each segment's Q
 //   warp 6     allocates tensor memory and issues q.k^T (one lane)
 //   warp 7     issues p.v (one lane); with two issuers the q.k^T of the next
 //              stages never queues behind the p.v of the current one
@@ -80,6 +85,12 @@ constexpr int THREADS = 384;
 constexpr int WARP_KP = 4, WARP_VP = 5, WARP_QK = 6, WARP_PV = 7, WARP_EPI = 8;
 constexpr uint32_t TMEM_COLS = 64;
 constexpr float kRescaleLog2 = 8.f;         // move the reference when exceeded by 2^8
+// Split choice.  One CTA streams at most about 1/kCtaShare of the HBM rate
+// (its three 64 KiB K+V stages in flight over the load latency); a unit's
+// partial state costs the CTA that merges it about kMergeBytes of streaming
+// time (a store, a fence, an atomic and the reloads of the parts, in series).
+constexpr long long kCtaShare = 96;
+constexpr long long kMergeBytes = 32ll << 20;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr int OFF_K = 0;
@@ -92,7 +103,7 @@ constexpr int OFF_LRED = OFF_RED + 256;     // f32 [2][4][8] warp sums per segme
 constexpr int OFF_MREF = OFF_LRED + 256;    // f32 [2][8] reference maxima per segment parity
 constexpr int OFF_MERGE = OFF_MREF + 64;    // float2 [MERGE_PAIRS] partial (max, sum)
 constexpr int MERGE_PAIRS = 128;
-constexpr int OFF_MISC = OFF_MERGE + MERGE_PAIRS * 8;  // tmem base, flags, chunk queue, masks
+constexpr int OFF_MISC = OFF_MERGE + MERGE_PAIRS * 8;  // tmem base, flags, masks
 constexpr int OFF_PRE = OFF_MISC + 128;     // int [B + 1]
 constexpr int SMEM_SLACK = 1024;
 
@@ -231,142 +242,108 @@ __device__ __forceinline__ Segment locate(const int *pre, int B, int n_kv, long 
   return s;
 }
 
-// Chunk schedule of one call.  Chunks are contiguous ranges of the flattened
-// block space, in index order.  CTA c first takes chunk c (its static share);
-// in dynamic mode it then takes chunks P, P+1, ... from an atomic counter, so
-// SMs that stream faster take more of the remaining work.  Boundaries are a
-// closed form of the chunk index, so every thread can map a chunk to its
-// range and a block position to its chunk.
+// Parts of one call: part c (taken by CTA c) is a contiguous range of the
+// flattened block space, in index order; a closed form of c, so every thread
+// can map a part to its range and a block position to its part.
 struct Schedule {
-  long long X;   // blocks in all units
-  long long P;   // static chunks
-  long long Xs;  // blocks covered by the static chunks
-  long long S1;  // blocks per dynamic chunk
-  long long n1;  // dynamic chunks
+  long long X;     // blocks in all units
+  long long P;     // parts
+  bool units;      // part c = unit c (else X * c / P balanced cuts)
+  const int *pre;  // blocks before sequence b
+  int n_kv;
   __device__ __forceinline__ void range(long long i, long long &a, long long &b) const {
-    if (i < P) {
-      a = Xs * i / P;
-      b = Xs * (i + 1) / P;
+    if (units) {
+      const int sb = (int)(i / n_kv), g = (int)(i % n_kv);
+      const long long nb = pre[sb + 1] - pre[sb];
+      a = (long long)n_kv * pre[sb] + g * nb;
+      b = a + nb;
     } else {
-      a = Xs + (i - P) * S1;
-      b = a + S1 < X ? a + S1 : X;
+      a = X * i / P;
+      b = X * (i + 1) / P;
     }
   }
-  __device__ __forceinline__ long long chunk_of(long long x) const {
-    return x < Xs ? (P * (x + 1) - 1) / Xs : P + (x - Xs) / S1;
+  // Part holding block position x (only needed for units that are cut,
+  // which happens in balanced mode alone).
+  __device__ __forceinline__ long long part_of(long long x) const {
+    return (P * (x + 1) - 1) / X;
   }
 };
 
-// A role's position in the CTA's sequence of chunks and segments.
+// A role's walk over the CTA's part, one segment (the piece of the part
+// inside one unit) at a time.  Every role walks the same segments.
 struct SegCursor {
-  long long x = 0, b = 0;  // rest of the current chunk
-  int chunk = -1;
-  int q = 0;               // chunks taken so far
-  bool done = false;
-};
-
-// Next segment (the part of a chunk inside one unit); `fetch` yields the next
-// chunk id (-1 when there is none).  Empty chunks are skipped.
-template <class F>
-__device__ __forceinline__ bool next_segment(SegCursor &c, const Schedule &sc, const int *pre,
-                                             int B, int n_kv, Segment &sg, int &chunk, F fetch) {
-  while (c.x >= c.b) {
-    if (c.done) return false;
-    const int id = fetch(c.q++);
-    if (id < 0) {
-      c.done = true;
-      return false;
-    }
-    long long a, b;
-    sc.range(id, a, b);
-    c.x = a;
-    c.b = b;
-    c.chunk = id;
+  long long x, b;  // rest of the part
+  __device__ __forceinline__ SegCursor(const Schedule &sc) {
+    x = b = 0;
+    if ((long long)blockIdx.x < sc.P) sc.range(blockIdx.x, x, b);
   }
-  sg = locate(pre, B, n_kv, c.x, c.b);
-  c.x += sg.n;
-  chunk = c.chunk;
-  return true;
-}
-
-// Chunk queue shared by the roles of a CTA: the K producer pushes ids; the V
-// producer, the two MMA issuers, the four softmax warps and the four epilogue
-// warps (eleven arrivals) pop them.
-struct ChunkQueue {
-  uint64_t *full;        // [4], 1 arrival
-  uint64_t *empty;       // [4], 11 arrivals
-  volatile int *id;      // [4]
-  volatile int *abort_flag;
-  int32_t *err;
-  // Pop chunk number q (all lanes of a warp, or one lane); `arrive` is true
-  // on the one lane that releases the slot.
-  __device__ __forceinline__ int pop(int q, bool arrive, bool warp_wide) const {
-    const int slot = q & 3;
-    wait_or_abort(&full[slot], (uint32_t)(q >> 2) & 1u, abort_flag, err);
-    const int v = *abort_flag ? -1 : id[slot];
-    if (warp_wide) __syncwarp();
-    if (arrive) mbar_arrive(&empty[slot]);
-    return v;
-  }
-  __device__ __forceinline__ void push(int q, int v) const {
-    const int slot = q & 3;
-    wait_or_abort(&empty[slot], ((uint32_t)(q >> 2) & 1u) ^ 1u, abort_flag, err);
-    id[slot] = v;
-    mbar_arrive(&full[slot]);
+  __device__ __forceinline__ bool next(const Schedule &sc, int B, Segment &sg) {
+    if (x >= b) return false;
+    sg = locate(sc.pre, B, sc.n_kv, x, b);
+    x += sg.n;
+    return true;
   }
 };
 
 // One producer warp (K or V): walks the CTA's stages and copies one tile per
-// lane with the TMA engine.  Block ids come from 32-entry chunks of the table
-// row, each loaded one chunk before it is needed.  The K producer also owns
-// the chunk queue, records which blocks of a stage had an invalid id, and
-// writes each segment's Q (the B operand of q.k^T: K-major, 128-byte swizzle,
-// row = head, two 64-column halves) into buffer k & 1 as the segment starts.
+// lane with the TMA engine.  The K producer also records which blocks of a
+// stage had an invalid id and writes each segment's Q (the B operand of
+// q.k^T: K-major, 128-byte swizzle, row = head, two 64-column halves) into
+// buffer k & 1 as segment k starts.  Loads run one step ahead: the next
+// segment's Q and first 64 block ids while the current segment streams, and
+// within a segment the block ids 32 entries ahead.
 template <int G, int BS, bool IS_K>
 __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
-                                        const ChunkQueue &cq, const __nv_bfloat16 *cache,
-                                        unsigned char *ring, uint64_t *full, uint64_t *empty,
-                                        int nstages_ring, const int *pre,
+                                        const __nv_bfloat16 *cache, unsigned char *ring,
+                                        uint64_t *full, uint64_t *empty, int nstages_ring,
                                         volatile int *stage_mask, unsigned char *qbuf,
                                         uint64_t *q_ready, uint64_t *q_free,
                                         volatile int *abort_flag, int lane) {
   constexpr int SB = TOK / BS;  // blocks per stage
   constexpr uint32_t TILE_BYTES = BS * 256;
+  constexpr int QPL = (16 * G + 31) / 32;  // Q 16-byte pieces per lane
   const uint64_t policy = l2_policy_evict_first();
-  auto fetch = [&](int q) -> int {
-    if (!IS_K) return cq.pop(q, lane == 0, true);
-    int v = -1;
-    if (lane == 0) {
-      if (q == 0 && blockIdx.x < sc.P) {
-        v = (int)blockIdx.x;
-      } else if (p.dynamic) {
-        const int j = atomicAdd(p.chunk_counter, 1);
-        if (j < sc.n1) {
-          v = (int)(sc.P + j);
-        } else if ((long long)j == sc.n1 + gridDim.x - 1) {
-          atomicExch(p.chunk_counter, 0);  // every CTA has failed once: ready for the next call
-        }
-      }
-      cq.push(q, v);
-    }
-    return __shfl_sync(kFullMask, v, 0);
+
+  struct Ahead {
+    uint4 q[QPL];
+    int tab, tab_next;
   };
-  SegCursor cur;
-  Segment sg;
-  int chunk;
+  auto load_ahead = [&](const Segment &g, Ahead &a) {
+    if (IS_K) {
+#pragma unroll
+      for (int i = 0; i < QPL; ++i) {
+        const int j = lane + 32 * i, r = j >> 4, c = j & 15;
+        a.q[i] = (j < 16 * G) ? __ldg(reinterpret_cast<const uint4 *>(
+                                    p.q + ((size_t)g.b * p.n_q + (size_t)g.g * G + r) * kHeadDim +
+                                    c * 8))
+                              : make_uint4(0, 0, 0, 0);
+      }
+    }
+    const int32_t *trow = p.tables + (size_t)g.b * p.MB + g.j0;
+    a.tab = (lane < g.n) ? __ldg(trow + lane) : 0;
+    a.tab_next = (32 + lane < g.n) ? __ldg(trow + 32 + lane) : 0;
+  };
+
+  SegCursor cur(sc);
+  Segment sg, nsg;
+  Ahead cur_a{}, next_a{};
+  bool have = cur.next(sc, p.B, sg);
+  if (have) load_ahead(sg, cur_a);
   int s = 0, k = 0;
-  while (next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch)) {
+  while (have) {
+    const bool have_next = cur.next(sc, p.B, nsg);
+    if (have_next) load_ahead(nsg, next_a);
     if (IS_K) {
       const int qb = k & 1;
       if (lane == 0)
         wait_or_abort(&q_free[qb], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
       __syncwarp();
-      for (int j = lane; j < 16 * G; j += 32) {
-        const int r = j >> 4, c = j & 15, half = c >> 3, cc = c & 7;
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(
-            p.q + ((size_t)sg.b * p.n_q + (size_t)sg.g * G + r) * kHeadDim + c * 8));
-        *reinterpret_cast<uint4 *>(qbuf + qb * Q_BYTES + half * (NPAD * 128) + r * 128 +
-                                   ((cc ^ (r & 7)) << 4)) = v;
+#pragma unroll
+      for (int i = 0; i < QPL; ++i) {
+        const int j = lane + 32 * i, r = j >> 4, c = j & 15, half = c >> 3, cc = c & 7;
+        if (j < 16 * G)
+          *reinterpret_cast<uint4 *>(qbuf + qb * Q_BYTES + half * (NPAD * 128) + r * 128 +
+                                     ((cc ^ (r & 7)) << 4)) = cur_a.q[i];
       }
       fence_proxy_async();
       __syncwarp();
@@ -374,8 +351,7 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
     }
     ++k;
     const int32_t *trow = p.tables + (size_t)sg.b * p.MB + sg.j0;
-    int tab = (lane < sg.n) ? __ldg(trow + lane) : 0;
-    int tab_next = (32 + lane < sg.n) ? __ldg(trow + 32 + lane) : 0;
+    int tab = cur_a.tab, tab_next = cur_a.tab_next;
     int tchunk = 0;
     const int nstages = (sg.n + SB - 1) / SB;
     for (int st = 0; st < nstages; ++st, ++s) {
@@ -412,6 +388,9 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
                       TILE_BYTES, &full[slot], policy);
       }
     }
+    sg = nsg;
+    cur_a = next_a;
+    have = have_next;
   }
   // no copy may still be landing when the CTA exits
   if (lane == 0) {
@@ -447,16 +426,14 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   uint64_t *q_ready = m_ready + 2;      // [2] per Q buffer
   uint64_t *q_free = q_ready + 2;       // [2] per Q buffer
   uint64_t *done = q_free + 2;          // [2] one per MMA issuer
-  uint64_t *cq_full = done + 2;         // [4]
-  uint64_t *cq_empty = cq_full + 4;     // [4]
-  uint64_t *seg_done = cq_empty + 4;    // [2] softmax -> epilogue, per segment parity
+  uint64_t *seg_done = done + 2;        // [2] softmax -> epilogue, per segment parity
   float *red = reinterpret_cast<float *>(smem + OFF_RED);
   float *lred = reinterpret_cast<float *>(smem + OFF_LRED);
   float *mref = reinterpret_cast<float *>(smem + OFF_MREF);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
   volatile int *flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);         // [3]
-  volatile int *cq_id = reinterpret_cast<volatile int *>(smem + OFF_MISC + 20);       // [4]
+  int *nmax_slot = reinterpret_cast<int *>(smem + OFF_MISC + 20);
   volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 40);  // [8]
   int *pre = reinterpret_cast<int *>(smem + OFF_PRE);
 
@@ -481,10 +458,6 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
       mbar_init(&m_ready[i], 1);
       mbar_init(&done[i], 1);
       mbar_init(&seg_done[i], 4);
-    }
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(&cq_full[i], 1);
-      mbar_init(&cq_empty[i], 11);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_ready[i], 1);
@@ -518,10 +491,11 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   fence_proxy_async();
   __syncthreads();
   if (warp == 0) {
-    int carry = 0;
+    int carry = 0, longest = 0;
     for (int base = 0; base < p.B; base += 32) {
       const int i = base + lane;
       int v = (i < p.B) ? pre[i + 1] : 0;
+      longest = max(longest, v);
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int n = __shfl_up_sync(kFullMask, v, o);
@@ -530,7 +504,12 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
       if (i < p.B) pre[i + 1] = v + carry;
       carry += __shfl_sync(kFullMask, v, 31);
     }
-    if (lane == 0) pre[0] = 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) longest = max(longest, __shfl_xor_sync(kFullMask, longest, o));
+    if (lane == 0) {
+      pre[0] = 0;
+      *nmax_slot = longest;
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -539,44 +518,40 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
 
   Schedule sc;
   sc.X = (long long)p.n_kv * pre[p.B];
-  if (p.dynamic) {
-    // two thirds of the blocks as equal static shares, the rest in chunks of
-    // about 1/8 of the CTA's mean remaining share (at least one stage)
-    sc.P = gridDim.x;
-    long long xs = sc.X * 2 / 3;
-    if (xs < sc.P) xs = 0;
-    sc.Xs = xs;
-    const long long rest = sc.X - xs;
-    long long s1 = (rest + 8 * sc.P - 1) / (8 * sc.P);
-    s1 = (s1 + SB - 1) / SB * SB;  // whole stages
-    if (s1 < SB) s1 = SB;
-    sc.S1 = s1;
-    sc.n1 = (rest + s1 - 1) / s1;
-  } else {
-    // caller-fixed split: gridDim.x equal shares (no more than one per block)
-    sc.P = sc.X < (long long)gridDim.x ? sc.X : (long long)gridDim.x;
-    sc.Xs = sc.X;
-    sc.S1 = 1;
-    sc.n1 = 0;
+  sc.pre = pre;
+  sc.n_kv = p.n_kv;
+  sc.P = sc.X < (long long)gridDim.x ? sc.X : (long long)gridDim.x;
+  sc.units = false;
+  if (p.auto_split) {
+    // Whole units when they fit in the grid and the longest one streams no
+    // longer than the job at the HBM rate plus the merges the balanced cut
+    // would need; the cost of either is in blocks of HBM streaming time.
+    const long long U = (long long)p.B * p.n_kv, nmax = *nmax_slot;
+    if (U <= (long long)gridDim.x && sc.X > 0) {
+      const long long per_cta = (sc.X + gridDim.x - 1) / gridDim.x;
+      const long long cost_units = max(nmax * kCtaShare, sc.X);
+      const long long cost_cut = max(per_cta * kCtaShare, sc.X) + kMergeBytes / (BS * 512);
+      if (cost_units <= cost_cut) {
+        sc.units = true;
+        sc.P = U;
+      }
+    }
   }
-  ChunkQueue cq{cq_full, cq_empty, cq_id, abort_flag, p.err};
 
   if (warp == WARP_KP) {
-    produce<G, BS, true>(p, sc, cq, p.k_cache, smem + OFF_K, full_k, empty_k, NSK, pre,
-                         stage_mask, smem + OFF_Q, q_ready, q_free, abort_flag, lane);
+    produce<G, BS, true>(p, sc, p.k_cache, smem + OFF_K, full_k, empty_k, NSK, stage_mask,
+                         smem + OFF_Q, q_ready, q_free, abort_flag, lane);
   } else if (warp == WARP_VP) {
-    produce<G, BS, false>(p, sc, cq, p.v_cache, smem + OFF_V, full_v, empty_v, NSV, pre, nullptr,
+    produce<G, BS, false>(p, sc, p.v_cache, smem + OFF_V, full_v, empty_v, NSV, nullptr,
                           nullptr, nullptr, nullptr, abort_flag, lane);
   } else if (warp == WARP_QK) {
     // ---------------------------------------------------- q.k^T issuer
     if (lane == 0) {
       const uint32_t q_base = smem_addr(smem + OFF_Q);
-      auto fetch = [&](int q) { return cq.pop(q, true, false); };
-      SegCursor cur;
+      SegCursor cur(sc);
       Segment sg;
-      int chunk;
       int s = 0, k = 0;
-      while (next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch)) {
+      while (cur.next(sc, p.B, sg)) {
         const int nstages = (sg.n + SB - 1) / SB;
         // Q of segment k is in buffer k & 1 (written by the K producer); it is
         // rewritten for segment k + 2 only after q_free signals that every
@@ -620,12 +595,10 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   } else if (warp == WARP_PV) {
     // ------------------------------------------------------- p.v issuer
     if (lane == 0) {
-      auto fetch = [&](int q) { return cq.pop(q, true, false); };
-      SegCursor cur;
+      SegCursor cur(sc);
       Segment sg;
-      int chunk;
       int s = 0, k = 0;
-      while (next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch)) {
+      while (cur.next(sc, p.B, sg)) {
         const int nstages = (sg.n + SB - 1) / SB;
         const int ob = k & 1;
         for (int st = 0; st < nstages; ++st, ++s) {
@@ -663,15 +636,10 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
     const int t = tid;  // 0..127: token row of S
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     constexpr int NCT = 128;
-    auto fetch = [&](int q) { return cq.pop(q, lane == 0, true); };
-    SegCursor cur;
+    SegCursor cur(sc);
     Segment sg;
-    int chunk = -1;
     int s = 0, k = 0;
-
-    bool have = next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch);
-
-    while (have) {
+    while (cur.next(sc, p.B, sg)) {
       const int ctx_b = __ldg(p.ctx + sg.b);
       const int nstages = (sg.n + SB - 1) / SB;
       const int ob = k & 1;
@@ -775,9 +743,6 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
 
       // ---- end of segment: hand the segment's reference maxima and per-warp
       // sums to the epilogue warps.
-      Segment nsg;
-      int nchunk = -1;
-      const bool have_next = next_segment(cur, sc, pre, p.B, p.n_kv, nsg, nchunk, fetch);
       // lred/mref[ob] were last read by the epilogue of segment k - 2, which
       // then released O buffer ob
       wait_or_abort(&o_free[ob], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
@@ -789,9 +754,6 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&seg_done[ob]);
-      sg = nsg;
-      chunk = nchunk;
-      have = have_next;
       ++k;
     }
   } else {
@@ -800,12 +762,11 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
     const int ew = warp - WARP_EPI;     // TMEM lane quadrant
     const uint32_t lane_base = (uint32_t)(ew * 32) << 16;
     constexpr int NET = 128;
-    auto fetch = [&](int q) { return cq.pop(q, lane == 0, true); };
-    SegCursor cur;
+    SegCursor cur(sc);
     Segment sg;
-    int chunk = -1;
+    const int part = (int)blockIdx.x;
     int k = 0;
-    while (next_segment(cur, sc, pre, p.B, p.n_kv, sg, chunk, fetch)) {
+    while (cur.next(sc, p.B, sg)) {
       const int ob = k & 1;
       const int unit = sg.b * p.n_kv + sg.g;
       wait_or_abort(&seg_done[ob], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
@@ -832,7 +793,7 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
         for (int h = 0; h < G; ++h)
           p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(ov[h] / L[h]);
       } else {
-        const size_t srow = ((size_t)unit + (size_t)chunk) * G;
+        const size_t srow = ((size_t)unit + (size_t)part) * G;
 #pragma unroll
         for (int h = 0; h < G; ++h) p.part_o[(srow + h) * kHeadDim + e] = ov[h];
 #pragma unroll
@@ -843,8 +804,8 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
         __threadfence();
         named_barrier_sync(2, NET);
         if (e == 0) {
-          const long long c_first = sc.chunk_of(sg.unit_start);
-          const long long c_last = sc.chunk_of(sg.unit_end - 1);
+          const long long c_first = sc.part_of(sg.unit_start);
+          const long long c_last = sc.part_of(sg.unit_end - 1);
           const int n_parts = (int)(c_last - c_first + 1);
           const int before = atomicAdd(p.counters + unit, 1);
           const int last = (before == n_parts - 1);

@@ -126,8 +126,7 @@ struct AttnParams {
   float *part_o;                 // [slots][G][D]  unnormalised partial outputs
   float *part_ml;                // [slots][G][2]  partial (max, sum), log2 domain
   int32_t *counters;             // [B * n_kv]     arrivals per split unit
-  int32_t *chunk_counter;        // next dynamic chunk (self-resetting)
-  int dynamic;                   // 1: static share + dynamically grabbed chunks
+  int auto_split;                // 1: whole units or balanced cuts, chosen per call
   int32_t *err;                  // device error word
 };
 
