@@ -187,13 +187,36 @@ pgd_status pgd_paged_decode_attention_noalloc(void *out, const void *q, const vo
                                               void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* append, then attend (device buffers)                                   */
+/* ---------------------------------------------------------------------- */
+/* The decode step of one layer on device buffers: the new token's K/V
+ * (k_new, v_new: bf16 [B][n_kv][d]) are written at position
+ * context_lens[b] - 1 exactly as pgd_kv_append does ("LLM inference systems
+ * engineering", 2.1.3: the step commits the pending token's K/V), then
+ * out = pgd_paged_decode_attention over the updated caches.  Same shapes,
+ * rules, results and errors as those two calls made one after the other;
+ * every argument is checked before anything is enqueued.  The attention
+ * kernel is launched with programmatic stream serialization and, knowing
+ * that the kernel before it writes only the caches, runs its prologue (block
+ * counts, split choice, Q and block-table loads) while kv_append runs and
+ * waits for it only before its first cache read.  The block holding position
+ * context_lens[b] - 1 must be private to sequence b (copy-on-write), as for
+ * pgd_kv_append. */
+pgd_status pgd_append_decode_attention(void *out, const void *q, const void *k_new,
+                                       const void *v_new, void *k_cache, void *v_cache,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                       int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* one decode step with host inputs and outputs                            */
 /* ---------------------------------------------------------------------- */
 /* One decode step of one layer for a caller whose per-step tensors live in
  * host memory: copies q_h, k_new_h, v_new_h and context_lens_h to the
- * caller's device staging buffers, appends the new token at position
- * context_lens[b] - 1 (pgd_kv_append), runs pgd_paged_decode_attention, and
- * copies the result back to out_h -- all enqueued on `stream`.  For
+ * caller's device staging buffers, runs pgd_append_decode_attention on them
+ * (append at position context_lens[b] - 1, then attention), and copies the
+ * result back to out_h -- all enqueued on `stream`.  For
  * asynchronous copies the host buffers should be pinned.  The cache, block
  * tables and workspace stay on the device.  Shapes and rules as above. */
 pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,

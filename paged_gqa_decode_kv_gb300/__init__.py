@@ -9,13 +9,14 @@ from .inputs import (WORKLOADS, Workload, PagedBatch, make_batch, make_workload,
                      tile_pool, untile_pool, pool_shape)
 from ._native import (  # noqa: F401
     PGDError, BlockAllocator, kv_append, paged_decode_attention,
-    paged_decode_attention_noalloc, decode_step, copy_blocks,
+    paged_decode_attention_noalloc, append_decode_attention, decode_step, copy_blocks,
     device_errors, workspace_size, make_workspace, attention_grid, validate_tables, lib,
     library_path)
 
 __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "tile_pool",
            "untile_pool", "pool_shape", "PGDError",
            "BlockAllocator", "kv_append", "paged_decode_attention",
-           "paged_decode_attention_noalloc", "decode_step", "copy_blocks",
+           "paged_decode_attention_noalloc", "append_decode_attention", "decode_step",
+           "copy_blocks",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
            "validate_tables", "lib", "library_path"]

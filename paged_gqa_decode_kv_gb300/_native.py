@@ -36,6 +36,8 @@ SIGNATURES = {
     "pgd_attention_grid": ([_I, _I, _I, _I, _I], _I),
     "pgd_paged_decode_attention_noalloc": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                             _F, _I, _P], _I),
+    "pgd_append_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                     _F, _I, _P, _Z, _P], _I),
     "pgd_decode_step": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                          _I, _I, _F, _I, _P, _Z, _P], _I),
     "pgd_copy_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
@@ -187,6 +189,33 @@ def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, conte
     _check(lib().pgd_paged_decode_attention_noalloc(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         B, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _stream(stream)))
+    return out
+
+
+def append_decode_attention(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                            scale: float, num_splits: int = 0,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """kv_append of k_new/v_new at context_lens - 1, then paged decode
+    attention over the updated cache (one call, two kernels; the attention
+    prologue overlaps the append)."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"),
+                 (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, n_q, d = q.shape
+    NB, n_kv, bs, _ = _cache_dims(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = make_workspace(B, n_q, n_kv, num_splits, q.device)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_append_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), B, n_q, n_kv, d, bs, MB, NB, float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
     return out
 
 

@@ -169,11 +169,18 @@ pgd_status check_attention_args(const void *out, const void *q, const void *k_ca
   return PGD_OK;
 }
 
-pgd_status launch_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
-                            const int32_t *tables, const int32_t *ctx, int32_t B, int32_t n_q,
-                            int32_t n_kv, int32_t bs, int32_t MB, int32_t NB, float scale,
-                            int32_t num_splits, void *workspace, size_t workspace_bytes,
-                            cudaStream_t stream) {
+// Host-side half of an attention launch: workspace checks, grid and the
+// kernel's parameter block.  Nothing is enqueued.
+struct PreparedAttention {
+  AttnParams p;
+  int G, bs, grid;
+};
+
+pgd_status prepare_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *tables, const int32_t *ctx, int32_t B, int32_t n_q,
+                             int32_t n_kv, int32_t bs, int32_t MB, int32_t NB, float scale,
+                             int32_t num_splits, void *workspace, size_t workspace_bytes,
+                             PreparedAttention *pa) {
   if (!workspace) return fail(PGD_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(workspace, kWsAlign)) return fail(PGD_ERR_WORKSPACE, "workspace not 256-aligned");
   if (workspace_bytes < ws_layout(B, n_q, n_kv, 1).total)
@@ -211,9 +218,54 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
   p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.err = err;
-  cudaError_t e = attention_launch(p, G, bs, grid, stream);
+  p.wait_late = 0;
+  pa->p = p;
+  pa->G = G;
+  pa->bs = bs;
+  pa->grid = grid;
+  return PGD_OK;
+}
+
+pgd_status launch_prepared(const PreparedAttention &pa, cudaStream_t stream) {
+  cudaError_t e = attention_launch(pa.p, pa.G, pa.bs, pa.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "paged attention launch");
   return PGD_OK;
+}
+
+pgd_status launch_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *tables, const int32_t *ctx, int32_t B, int32_t n_q,
+                            int32_t n_kv, int32_t bs, int32_t MB, int32_t NB, float scale,
+                            int32_t num_splits, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  PreparedAttention pa;
+  pgd_status s = prepare_attention(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, bs, MB,
+                                   NB, scale, num_splits, workspace, workspace_bytes, &pa);
+  if (s != PGD_OK) return s;
+  return launch_prepared(pa, stream);
+}
+
+// kv_append at position context_lens[b] - 1, then attention over the updated
+// caches.  Every check runs before the first launch.  The attention kernel
+// is told that the kernel before it (kv_append) writes only the caches, so
+// its CTAs run their prologue while kv_append runs and wait only before the
+// first cache read.
+pgd_status append_then_attend(void *out, const void *q, const void *k_new, const void *v_new,
+                              void *k_cache, void *v_cache, const int32_t *tables,
+                              const int32_t *ctx, int32_t B, int32_t n_q, int32_t n_kv,
+                              int32_t bs, int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!k_new || !v_new) return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  PreparedAttention pa;
+  pgd_status s = prepare_attention(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, bs, MB,
+                                   NB, scale, num_splits, workspace, workspace_bytes, &pa);
+  if (s != PGD_OK) return s;
+  cudaError_t e = kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B, n_kv, bs,
+                                   MB, NB, pa.p.err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  pa.p.wait_late = 1;
+  return launch_prepared(pa, stream);
 }
 
 }  // namespace
@@ -327,6 +379,22 @@ pgd_status pgd_paged_decode_attention(void *out, const void *q, const void *k_ca
   return s == PGD_OK ? ok() : s;
 }
 
+pgd_status pgd_append_decode_attention(void *out, const void *q, const void *k_new,
+                                       const void *v_new, void *k_cache, void *v_cache,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                       int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                                       void *workspace, size_t workspace_bytes, void *stream) {
+  pgd_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, B,
+                                      n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  s = append_then_attend(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, B,
+                         n_q, n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
+  return s == PGD_OK ? ok() : s;
+}
+
 pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
                            const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
                            void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
@@ -342,6 +410,13 @@ pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, co
     return fail(PGD_ERR_INVALID_ARG, "null pointer");
   if (!aligned(k_new_d, 16) || !aligned(v_new_d, 16))
     return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  {
+    // every check of the device half runs before the first copy is enqueued
+    PreparedAttention pa;
+    s = prepare_attention(out_d, q_d, k_cache, v_cache, block_tables, context_lens_d, B, n_q,
+                          n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes, &pa);
+    if (s != PGD_OK) return s;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t qb = (size_t)B * n_q * kHeadDim * 2, kvb = (size_t)B * n_kv * kHeadDim * 2;
   cudaError_t e;
@@ -351,14 +426,9 @@ pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, co
       (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4, cudaMemcpyHostToDevice,
                            st)) != cudaSuccess)
     return cuda_fail(e, "decode step: host-to-device copy");
-  int32_t *err = nullptr;
-  s = error_word(&err);
-  if (s != PGD_OK) return s;
-  e = kv_append_launch(k_new_d, v_new_d, k_cache, v_cache, block_tables, context_lens_d, -1, B,
-                       n_kv, bs, MB, NB, err, st);
-  if (e != cudaSuccess) return cuda_fail(e, "decode step: kv_append launch");
-  s = launch_attention(out_d, q_d, k_cache, v_cache, block_tables, context_lens_d, B, n_q, n_kv,
-                       bs, MB, NB, scale, num_splits, workspace, workspace_bytes, st);
+  s = append_then_attend(out_d, q_d, k_new_d, v_new_d, k_cache, v_cache, block_tables,
+                         context_lens_d, B, n_q, n_kv, bs, MB, NB, scale, num_splits, workspace,
+                         workspace_bytes, st);
   if (s != PGD_OK) return s;
   if ((e = cudaMemcpyAsync(out_h, out_d, qb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
     return cuda_fail(e, "decode step: device-to-host copy");

@@ -329,6 +329,7 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
   Ahead cur_a{}, next_a{};
   bool have = cur.next(sc, p.B, sg);
   if (have) load_ahead(sg, cur_a);
+  if (p.wait_late) pdl_wait();  // kv_append has written the caches
   int s = 0, k = 0;
   while (have) {
     const bool have_next = cur.next(sc, p.B, nsg);
@@ -438,6 +439,10 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   int *pre = reinterpret_cast<int *>(smem + OFF_PRE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Launched with programmatic stream serialization: the previous kernel of
+  // the stream may still run.  Unless it is known to write only the caches,
+  // wait for it before reading anything.
+  if (!p.wait_late) pdl_wait();
 
   if (tid == 0) {
     for (int i = 0; i < NSK; ++i) {
@@ -820,15 +825,30 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
           const int c_first = flag[1], n_parts = flag[2];
           const size_t row0 = ((size_t)unit + (size_t)c_first) * G;
           float2 *mlb = reinterpret_cast<float2 *>(smem + OFF_MERGE);
-          constexpr int PPB = MERGE_PAIRS / G;  // parts per batch
+          constexpr int PPB = MERGE_PAIRS / G;  // parts per (max, sum) batch
+          constexpr int GP = 64 / G;            // parts per group of loads in flight
           float Mx[G], Lm[G], O[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) { Mx[h] = -INFINITY; Lm[h] = 0.f; O[h] = 0.f; }
           for (int base = 0; base < n_parts; base += PPB) {
             const int nb = min(PPB, n_parts - base);
-            // the (max, sum) of every part and head of the batch, one load each
+            const size_t rb = row0 + (size_t)base * G;
+            // Partial outputs are read GP parts at a time, all loads of a
+            // group issued before any is used; the first group's loads are
+            // in flight while the (max, sum) pairs arrive.
+            float ov[GP][G];
+            auto load_group = [&](int g0) {
+#pragma unroll
+              for (int i = 0; i < GP; ++i)
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                  ov[i][h] = (g0 + i < nb)
+                                 ? __ldcg(p.part_o + (rb + (size_t)(g0 + i) * G + h) * kHeadDim + e)
+                                 : 0.f;
+            };
+            load_group(0);
             for (int j = e; j < nb * G; j += NET)
-              mlb[j] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + row0 + (size_t)base * G + j);
+              mlb[j] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + rb + j);
             named_barrier_sync(2, NET);
 #pragma unroll
             for (int h = 0; h < G; ++h) {
@@ -841,17 +861,21 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
               }
               Mx[h] = bm;
             }
-#pragma unroll 4
-            for (int i = 0; i < nb; ++i) {
-              const size_t r = row0 + (size_t)(base + i) * G;
+            for (int g0 = 0; g0 < nb; g0 += GP) {
+              if (g0 > 0) load_group(g0);
 #pragma unroll
-              for (int h = 0; h < G; ++h) {
-                const float2 ml = mlb[i * G + h];
-                const float o = __ldcg(p.part_o + (r + h) * kHeadDim + e);
-                if (ml.x == -INFINITY) continue;
-                const float cf = exp2f(ml.x - Mx[h]);
-                Lm[h] = fmaf(cf, ml.y, Lm[h]);
-                O[h] = fmaf(cf, o, O[h]);
+              for (int i = 0; i < GP; ++i) {
+                if (g0 + i < nb) {
+#pragma unroll
+                  for (int h = 0; h < G; ++h) {
+                    const float2 ml = mlb[(g0 + i) * G + h];
+                    if (ml.x != -INFINITY) {
+                      const float cf = exp2f(ml.x - Mx[h]);
+                      Lm[h] = fmaf(cf, ml.y, Lm[h]);
+                      O[h] = fmaf(cf, ov[i][h], O[h]);
+                    }
+                  }
+                }
               }
             }
             named_barrier_sync(2, NET);  // mlb is reused by the next batch
@@ -896,8 +920,19 @@ template <int G, int BS>
 static cudaError_t launch_cfg(const AttnParams &p, int grid, cudaStream_t stream) {
   cudaError_t e = ensure_smem_limit<G, BS>();
   if (e != cudaSuccess) return e;
-  paged_attention_kernel<G, BS><<<grid, THREADS, smem_bytes(p.B), stream>>>(p);
-  return cudaGetLastError();
+  // Programmatic stream serialization: the CTAs may launch and run their
+  // prologue while the previous kernel finishes (see pdl_wait above).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem_bytes(p.B);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_attention_kernel<G, BS>, p);
 }
 
 template <int G, int BS>

@@ -21,6 +21,7 @@ kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_ne
                  const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
                  int pos_offset, int B, int n_kv, int bs, int MB, int NB, int32_t *err) {
   constexpr int kVecPerRow = kHeadDim * 2 / 16;  // 16 uint4 per 256-byte row
+  pdl_launch_dependents();  // the attention that follows may start its prologue
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= B * n_kv) return;

@@ -90,6 +90,15 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
       : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (launched with programmatic stream serialization) start its
+// prologue; wait blocks until every kernel this one depends on has completed
+// and its writes are visible.  Both are no-ops without such a neighbour.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -127,6 +136,8 @@ struct AttnParams {
   float *part_ml;                // [slots][G][2]  partial (max, sum), log2 domain
   int32_t *counters;             // [B * n_kv]     arrivals per split unit
   int auto_split;                // 1: whole units or balanced cuts, chosen per call
+  int wait_late;                 // 1: the previous kernel wrote only the caches (kv_append):
+                                 //    wait for it just before the first cache read
   int32_t *err;                  // device error word
 };
 

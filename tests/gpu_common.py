@@ -17,6 +17,21 @@ def oracle_attention(pb, n_threads: int = 0) -> np.ndarray:
                                   n_threads=n_threads)
 
 
+def oracle_append_then_attend(pb, n_threads: int = 0):
+    """The oracle's own kv_append (on CPU copies of the caches as generated,
+    before any GPU append), then its attention over the result.  Returns
+    (out, k_cache, v_cache) with the caches as uint16 bit patterns."""
+    k, v = oracle.kv_append(pb.k_cache.cpu(), pb.v_cache.cpu(), pb.k_new.cpu(), pb.v_new.cpu(),
+                            pb.block_tables.cpu(), pb.positions.cpu())
+    out = oracle.paged_attention(pb.q.cpu(), k, v, pb.block_tables.cpu(), pb.context_lens.cpu(),
+                                 pb.scale, n_threads=n_threads)
+    return out, k, v
+
+
+def cache_bits(t: torch.Tensor) -> np.ndarray:
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
 def gpu_attention(pb, num_splits: int = 0, workspace=None, out=None) -> torch.Tensor:
     return pgd.paged_decode_attention(out, pb.q, pb.k_cache, pb.v_cache, pb.block_tables,
                                       pb.context_lens, pb.scale, num_splits=num_splits,

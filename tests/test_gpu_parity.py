@@ -14,7 +14,8 @@ import torch
 import oracle
 import paged_gqa_decode_kv_gb300 as pgd
 from paged_gqa_decode_kv_gb300 import inputs
-from gpu_common import assert_no_device_errors, compare, gpu_attention, oracle_attention
+from gpu_common import (assert_no_device_errors, cache_bits, compare, gpu_attention,
+                        oracle_append_then_attend, oracle_attention)
 
 pytestmark = pytest.mark.gpu
 
@@ -188,8 +189,67 @@ def test_kv_append_bit_exact(bs):
 
 def test_append_then_attend_matches_oracle():
     pb = _batch(4, 32, 8, 32, [1, 300, 33, 1024], append=True)
+    want, _, _ = oracle_append_then_attend(pb)
     pgd.kv_append(pb.k_new, pb.v_new, pb.k_cache, pb.v_cache, pb.block_tables, pb.positions)
-    compare(gpu_attention(pb), oracle_attention(pb))
+    compare(gpu_attention(pb), want)
+
+
+APPEND_CASES = [
+    # (n_q, n_kv, bs, lens): the new token lands first, mid and last in a block
+    (32, 8, 16, [1, 16, 17, 700]),
+    (64, 8, 32, [32, 33, 1000, 2, 64]),
+    (8, 8, 16, [5, 4096]),
+    (16, 2, 32, [31]),
+]
+
+
+@pytest.mark.parametrize("case", APPEND_CASES, ids=lambda c: "nq%d_nkv%d_bs%d_%s" % (
+    c[0], c[1], c[2], "-".join(map(str, c[3]))))
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_append_decode_attention_one_call(case, num_splits):
+    """The one-call append + attention: caches bit exact with the oracle's
+    kv_append, output within tolerance of the oracle over those caches."""
+    n_q, n_kv, bs, lens = case
+    pb = _batch(len(lens), n_q, n_kv, bs, lens, append=True)
+    want, want_k, want_v = oracle_append_then_attend(pb)
+    got = pgd.append_decode_attention(None, pb.q, pb.k_new, pb.v_new, pb.k_cache, pb.v_cache,
+                                      pb.block_tables, pb.context_lens, pb.scale,
+                                      num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert np.array_equal(cache_bits(pb.k_cache), want_k)
+    assert np.array_equal(cache_bits(pb.v_cache), want_v)
+    compare(got, want, "append+attend splits=%d" % num_splits)
+
+
+def test_append_decode_attention_back_to_back():
+    """Steps issued back to back on one stream (each attention may start its
+    prologue while the append before it runs): every step sees its own
+    append.  Step i appends token i of a growing context."""
+    B, n_q, n_kv, bs = 3, 32, 8, 16
+    base = [40, 15, 300]
+    steps = 6
+    pb = _batch(B, n_q, n_kv, bs, [n + steps for n in base], append=True)
+    ws = pgd.make_workspace(B, n_q, n_kv)
+    g = torch.Generator().manual_seed(99)
+    k_seq = [torch.randn(B, n_kv, 128, generator=g).to(torch.bfloat16) for _ in range(steps)]
+    v_seq = [torch.randn(B, n_kv, 128, generator=g).to(torch.bfloat16) for _ in range(steps)]
+    k_ref, v_ref = pb.k_cache.cpu(), pb.v_cache.cpu()
+    outs, wants = [], []
+    for i in range(steps):
+        lens = torch.tensor([n + i + 1 for n in base], dtype=torch.int32)
+        kn, vn = k_seq[i].cuda(), v_seq[i].cuda()
+        outs.append(pgd.append_decode_attention(None, pb.q, kn, vn, pb.k_cache, pb.v_cache,
+                                                pb.block_tables, lens.cuda(), pb.scale,
+                                                workspace=ws))
+        k_ref, v_ref = oracle.kv_append(k_ref, v_ref, k_seq[i], v_seq[i], pb.block_tables.cpu(),
+                                        lens - 1)
+        wants.append(oracle.paged_attention(pb.q.cpu(), k_ref, v_ref, pb.block_tables.cpu(), lens,
+                                            pb.scale))
+    torch.cuda.synchronize()
+    for i in range(steps):
+        compare(outs[i], wants[i], "step %d" % i)
+    assert np.array_equal(cache_bits(pb.k_cache), k_ref)
+    assert np.array_equal(cache_bits(pb.v_cache), v_ref)
 
 
 def test_copy_blocks_bit_exact():
@@ -232,6 +292,8 @@ def test_decode_step_host_buffers_match_device_path():
 def test_workload_full_size(name):
     pb = inputs.make_workload(name, device="cuda")
     if pb.k_new is not None:
+        want, _, _ = oracle_append_then_attend(pb)
         pgd.kv_append(pb.k_new, pb.v_new, pb.k_cache, pb.v_cache, pb.block_tables, pb.positions)
-    got = gpu_attention(pb)
-    compare(got, oracle_attention(pb), name)
+    else:
+        want = oracle_attention(pb)
+    compare(gpu_attention(pb), want, name)
