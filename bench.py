@@ -39,7 +39,8 @@ METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; seq-layer-step
 NOMINAL_HBM_GBS = 8000.0     # nominal GB300 HBM3e bandwidth (~8 TB/s)
 FALLBACK_HBM_GBS = 6800.0    # profiling recipe's fallback when no measured peak exists
 L2_BYTES = 129 * 10**6
-ATTENTION_SRC = os.path.join(ROOT, "paged_gqa_decode_kv_gb300", "csrc", "attention.cu")
+ATTENTION_SOURCES = [os.path.join(ROOT, "paged_gqa_decode_kv_gb300", "csrc", f)
+                     for f in ("attention.cu", "pgd_device.cuh")]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "paged_attention_batch16_ctx8192.md")
 
 
@@ -185,8 +186,16 @@ def profiled_traffic():
     m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not (m_bytes and m_sha):
         return None
-    cur = hashlib.sha256(open(ATTENTION_SRC, "rb").read()).hexdigest()
-    return int(m_bytes.group(1)) if cur == m_sha.group(1) else None
+    return int(m_bytes.group(1)) if kernel_source_sha256() == m_sha.group(1) else None
+
+
+def kernel_source_sha256() -> str:
+    """sha256 of the attention kernel's sources (attention.cu, then the
+    device header it includes)."""
+    h = hashlib.sha256()
+    for path in ATTENTION_SOURCES:
+        h.update(open(path, "rb").read())
+    return h.hexdigest()
 
 
 # ------------------------------------------------------------ CPU baseline
