@@ -10,6 +10,9 @@ Contents
   * ``paged_attention`` / ``attention_weights`` / ``attention_part`` /
     ``lse_merge`` / ``kv_append`` -- ctypes wrappers over ``pgd_oracle.c``
     (plain C, float64, pthreads over (sequence, query head) rows).
+  * ``e4m3_decode`` / ``e4m3_encode`` / ``quantize_rows`` /
+    ``kv_append_fp8`` / ``paged_attention_fp8`` -- the 8-bit (FP8 E4M3,
+    per-(token, head) scale) cache, over ``pgd_oracle_fp8.c``.
   * ``kv_formula`` -- the KV-cache byte count in closed form.
   * ``block_model`` -- a plain-Python model of block tables, reference counts
     and copy-on-write.
@@ -29,7 +32,7 @@ from . import kv_formula  # noqa: F401  (re-exported)
 from . import block_model  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "pgd_oracle.c")
+_SRCS = [os.path.join(_HERE, "pgd_oracle.c"), os.path.join(_HERE, "pgd_oracle_fp8.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libpgd_oracle.so")
 _lock = threading.Lock()
@@ -37,14 +40,14 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile ``pgd_oracle.c`` with gcc into ``oracle/_build/``.  Plain -O2, no
-    fast-math: the oracle's arithmetic must stay IEEE double."""
+    """Compile the oracle's C sources with gcc into ``oracle/_build/``.  Plain
+    -O2, no fast-math: the oracle's arithmetic must stay IEEE."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-o", tmp, _SRC,
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-o", tmp] + _SRCS + [
            "-lpthread", "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
@@ -72,6 +75,17 @@ def _load():
         lib.oracle_lse_merge.restype = I
         lib.oracle_threads_used.argtypes = [I, ctypes.c_long]
         lib.oracle_threads_used.restype = I
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = D
+        lib.oracle_e4m3_encode_mode.argtypes = [ctypes.c_float, I]
+        lib.oracle_e4m3_encode_mode.restype = ctypes.c_uint8
+        lib.oracle_quantize_row.argtypes = [P, I, P, P, I]
+        lib.oracle_quantize_row.restype = None
+        lib.oracle_kv_append_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I]
+        lib.oracle_kv_append_fp8.restype = I
+        lib.oracle_paged_attention_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, D,
+                                                   I, I]
+        lib.oracle_paged_attention_fp8.restype = I
         _lib = lib
         return lib
 
@@ -193,3 +207,103 @@ def kv_append(k_cache, v_cache, k_new, v_new, block_tables, positions):
     if st:
         raise ValueError("oracle: position or block id out of range")
     return kc, vc
+
+
+# ------------------------------------------------------------------ 8-bit KV
+def _u8(a) -> np.ndarray:
+    if isinstance(a, np.ndarray):
+        if a.dtype != np.uint8:
+            raise TypeError("expected uint8 codes, got %s" % a.dtype)
+        return np.ascontiguousarray(a)
+    import torch
+    if a.dtype != torch.uint8:
+        raise TypeError("expected a uint8 tensor, got %s" % a.dtype)
+    return np.ascontiguousarray(a.detach().cpu().contiguous().numpy())
+
+
+def _f32(a) -> np.ndarray:
+    if isinstance(a, np.ndarray):
+        return np.ascontiguousarray(a, dtype=np.float32)
+    return np.ascontiguousarray(a.detach().cpu().contiguous().numpy().astype(np.float32))
+
+
+def _tile8_dims(cache: np.ndarray):
+    """(NB, n_kv, bs, d) of an 8-bit pool stored as [NB][n_kv][bs/8][d/16][8][16]."""
+    if cache.ndim != 6 or cache.shape[4:] != (8, 16):
+        raise ValueError("8-bit cache must be [NB][n_kv][bs/8][d/16][8][16]")
+    NB, n_kv, rg, nc = cache.shape[:4]
+    return NB, n_kv, rg * 8, nc * 16
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 values of E4M3 codes (NaN for the NaN codes)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    lib = _load()
+    return np.array([lib.oracle_e4m3_decode(int(v)) for v in c.ravel()],
+                    dtype=np.float64).reshape(c.shape)
+
+
+def e4m3_encode(x, truncate: bool = False) -> np.ndarray:
+    """Nearest E4M3 codes of binary32 values (ties to even, saturating)."""
+    a = np.asarray(x, dtype=np.float32)
+    lib = _load()
+    return np.array([lib.oracle_e4m3_encode_mode(float(v), 1 if truncate else 0)
+                     for v in a.ravel()], dtype=np.uint8).reshape(a.shape)
+
+
+def quantize_rows(x, mutation: int = 0):
+    """Per-row quantisation of bf16 rows x[..., d]: (codes uint8 [..., d],
+    scales float32 [...])."""
+    xa = _u16(x)
+    d = xa.shape[-1]
+    rows = xa.reshape(-1, d)
+    codes = np.zeros(rows.shape, dtype=np.uint8)
+    scales = np.zeros(rows.shape[0], dtype=np.float32)
+    lib = _load()
+    for r in range(rows.shape[0]):
+        row = np.ascontiguousarray(rows[r])
+        out = np.zeros(d, dtype=np.uint8)
+        sc = np.zeros(1, dtype=np.float32)
+        lib.oracle_quantize_row(_p(row), d, _p(out), _p(sc), int(mutation))
+        codes[r] = out
+        scales[r] = sc[0]
+    return codes.reshape(xa.shape), scales.reshape(xa.shape[:-1])
+
+
+def kv_append_fp8(k_cache, v_cache, k_scale, v_scale, k_new, v_new, block_tables, positions,
+                  mutation: int = 0):
+    """Return copies of (k_cache, v_cache, k_scale, v_scale) with one new token
+    per sequence quantised and written at logical position positions[b]."""
+    kc, vc = _u8(k_cache).copy(), _u8(v_cache).copy()
+    ks, vs = _f32(k_scale).copy(), _f32(v_scale).copy()
+    kn, vn = _u16(k_new), _u16(v_new)
+    ta, pa = _i32(block_tables), _i32(positions)
+    NB, n_kv, bs, d = _tile8_dims(kc)
+    assert ks.shape == (NB, n_kv, bs) and vs.shape == ks.shape
+    B = kn.shape[0]
+    st = _load().oracle_kv_append_fp8(_p(kc), _p(vc), _p(ks), _p(vs), _p(kn), _p(vn), _p(ta),
+                                      _p(pa), B, n_kv, d, bs, ta.shape[1], NB, int(mutation))
+    if st:
+        raise ValueError("oracle: position or block id out of range")
+    return kc, vc, ks, vs
+
+
+def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+                        scale: float, n_threads: int = 0, mutation: int = 0) -> np.ndarray:
+    """float64 out[B][n_q][d] of decode attention over the 8-bit cache: the
+    definition of ``paged_attention`` applied to the dequantised K and V.
+    k_cache, v_cache: uint8 [NB][n_kv][bs/8][d/16][8][16]; k_scale, v_scale:
+    float32 [NB][n_kv][bs]."""
+    qa, ka, va = _u16(q), _u8(k_cache), _u8(v_cache)
+    ks, vs = _f32(k_scale), _f32(v_scale)
+    ta, ca = _i32(block_tables), _i32(context_lens)
+    B, n_q, d = qa.shape
+    NB, n_kv, bs, d2 = _tile8_dims(ka)
+    assert d2 == d and va.shape == ka.shape and ks.shape == (NB, n_kv, bs)
+    out = np.zeros((B, n_q, d), dtype=np.float64)
+    st = _load().oracle_paged_attention_fp8(_p(out), _p(qa), _p(ka), _p(va), _p(ks), _p(vs),
+                                            _p(ta), _p(ca), B, n_q, n_kv, d, bs, ta.shape[1], NB,
+                                            float(scale), int(n_threads), int(mutation))
+    if st:
+        raise ValueError("oracle: invalid context length or block id (status %d)" % st)
+    return out

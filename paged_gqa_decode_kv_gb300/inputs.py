@@ -107,12 +107,32 @@ def pool_shape(num_blocks: int, n_kv: int, block_size: int, head_dim: int = HEAD
     return (num_blocks, n_kv, block_size // 8, head_dim // 8, 8, 8)
 
 
+def tile_pool8(x: torch.Tensor) -> torch.Tensor:
+    """Row-major 8-bit pool [NB][n_kv][bs][d] -> tiled [NB][n_kv][bs/8][d/16][8][16]
+    (8-row x 16-byte core matrices)."""
+    NB, n_kv, bs, d = x.shape
+    return x.reshape(NB, n_kv, bs // 8, 8, d // 16, 16).permute(0, 1, 2, 4, 3, 5).contiguous()
+
+
+def untile_pool8(x: torch.Tensor) -> torch.Tensor:
+    """Tiled 8-bit pool [NB][n_kv][bs/8][d/16][8][16] -> row-major [NB][n_kv][bs][d]."""
+    NB, n_kv, rg, nc = x.shape[:4]
+    return x.permute(0, 1, 2, 4, 3, 5).reshape(NB, n_kv, rg * 8, nc * 16)
+
+
+def pool_shape8(num_blocks: int, n_kv: int, block_size: int, head_dim: int = HEAD_DIM):
+    return (num_blocks, n_kv, block_size // 8, head_dim // 16, 8, 16)
+
+
 @dataclasses.dataclass
 class PagedBatch:
-    """Inputs of one decode step.  Tensors live on `device`."""
+    """Inputs of one decode step.  Tensors live on `device`.  With
+    kv_format "fp8" the pools hold E4M3 codes (uint8, tiled as
+    [NB][n_kv][bs/8][d/16][8][16]) and k_scale / v_scale their per-(token,
+    head) scales."""
     q: torch.Tensor              # bf16 [B][n_q][d]
-    k_cache: torch.Tensor        # bf16 [NB][n_kv][bs/8][d/8][8][8] (tiled)
-    v_cache: torch.Tensor        # bf16, same layout
+    k_cache: torch.Tensor        # bf16 [NB][n_kv][bs/8][d/8][8][8] (tiled), or uint8 codes
+    v_cache: torch.Tensor        # same layout
     block_tables: torch.Tensor   # int32 [B][MB], -1 where unused
     context_lens: torch.Tensor   # int32 [B]
     k_new: Optional[torch.Tensor]  # bf16 [B][n_kv][d] when appending
@@ -123,6 +143,9 @@ class PagedBatch:
     block_size: int
     unique_blocks: int           # physical blocks referenced by the tables
     shared_blocks: int           # blocks referenced by more than one sequence
+    kv_format: str = "bf16"      # "bf16" or "fp8" (E4M3 codes + scales)
+    k_scale: Optional[torch.Tensor] = None   # fp32 [NB][n_kv][bs] (fp8 only)
+    v_scale: Optional[torch.Tensor] = None
 
     @property
     def batch(self) -> int:
@@ -137,7 +160,7 @@ class PagedBatch:
         return self.q.shape[2]
 
     def token(self, cache: torch.Tensor, block: int, head: int, slot: int) -> torch.Tensor:
-        """The d-vector of one cached token (slot of a physical block)."""
+        """The d-vector (values, or codes for fp8) of one cached token."""
         t = cache[block, head, slot // 8, :, slot % 8, :]
         return t.reshape(-1)
 
@@ -170,7 +193,7 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
                shared_prefix: int = 0, append: bool = False, spare_frac: float = 0.05,
                max_blocks: Optional[int] = None, seed: int = DATA_SEED,
                table_seed: int = TABLE_SEED, device="cpu", poison: bool = True,
-               scale: Optional[float] = None) -> PagedBatch:
+               scale: Optional[float] = None, kv_format: str = "bf16") -> PagedBatch:
     """Build one decode step's inputs.
 
     Every sequence b holds ctx_lens[b] tokens.  The first `shared_prefix`
@@ -178,7 +201,14 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
     must then be a multiple of block_size, or the partial block is private).
     With append=True, the last token of every sequence is returned as
     k_new/v_new and its cache slot is left NaN.  The pool is drawn row-major,
-    poisoned, then tiled."""
+    poisoned, then tiled.
+
+    kv_format="fp8": the pools hold E4M3 codes drawn as N(0, 110^2) values
+    clamped to +-448 and cast to float8_e4m3fn, with per-(token, head) scales
+    uniform in kv_std * [0.5, 1.5] / 110 (so the dequantised values are about
+    N(0, kv_std^2)); poisoned slots hold the NaN code and a NaN scale.  The
+    appended token's k_new/v_new are fresh bf16 N(0, kv_std^2) draws."""
+    assert kv_format in ("bf16", "fp8")
     assert len(ctx_lens) == batch and n_q % n_kv == 0 and block_size % 8 == 0
     bs = block_size
     nblk = [(c + bs - 1) // bs for c in ctx_lens]
@@ -206,18 +236,33 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
 
     gen = torch.Generator(device=device).manual_seed(seed)
     q = _randn_bf16((batch, n_q, head_dim), q_std, gen, device)
-    k_cache = _randn_bf16((NB, n_kv, bs, head_dim), kv_std, gen, device)
-    v_cache = _randn_bf16((NB, n_kv, bs, head_dim), kv_std, gen, device)
+    fp8 = kv_format == "fp8"
+    k_scale = v_scale = None
+    if fp8:
+        k_cache = _codes_e4m3((NB, n_kv, bs, head_dim), gen, device)
+        v_cache = _codes_e4m3((NB, n_kv, bs, head_dim), gen, device)
+        k_scale = _scales((NB, n_kv, bs), kv_std, gen, device)
+        v_scale = _scales((NB, n_kv, bs), kv_std, gen, device)
+    else:
+        k_cache = _randn_bf16((NB, n_kv, bs, head_dim), kv_std, gen, device)
+        v_cache = _randn_bf16((NB, n_kv, bs, head_dim), kv_std, gen, device)
 
     k_new = v_new = positions = None
     if append:
         positions = torch.tensor([c - 1 for c in ctx_lens], dtype=torch.int32)
         blk = tables[torch.arange(batch), positions // bs].long().to(device)
         slot = (positions % bs).long().to(device)
-        k_new = k_cache[blk, :, slot, :].clone()
-        v_new = v_cache[blk, :, slot, :].clone()
+        if fp8:
+            k_new = _randn_bf16((batch, n_kv, head_dim), kv_std, gen, device)
+            v_new = _randn_bf16((batch, n_kv, head_dim), kv_std, gen, device)
+        else:
+            k_new = k_cache[blk, :, slot, :].clone()
+            v_new = v_cache[blk, :, slot, :].clone()
 
-    if poison:
+    if poison and fp8:
+        _poison8(k_cache, v_cache, k_scale, v_scale, tables, ctx_lens, bs, nblk, spare_ids,
+                 (blk, slot) if append else None, device)
+    elif poison:
         nan = float("nan")
         if spare_ids.numel():
             sid = spare_ids.long().to(device)
@@ -233,8 +278,12 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
             k_cache[blk, :, slot, :] = nan
             v_cache[blk, :, slot, :] = nan
     del used_ids
-    k_cache = tile_pool(k_cache)
-    v_cache = tile_pool(v_cache)
+    if fp8:
+        k_cache = tile_pool8(k_cache)
+        v_cache = tile_pool8(v_cache)
+    else:
+        k_cache = tile_pool(k_cache)
+        v_cache = tile_pool(v_cache)
 
     return PagedBatch(
         q=q, k_cache=k_cache, v_cache=v_cache,
@@ -243,24 +292,78 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
         positions=None if positions is None else positions.to(device),
         scale=(1.0 / math.sqrt(head_dim)) if scale is None else scale,
         n_kv=n_kv, block_size=bs, unique_blocks=needed,
-        shared_blocks=n_shared)
+        shared_blocks=n_shared, kv_format=kv_format, k_scale=k_scale, v_scale=v_scale)
 
 
-def make_workload(name: str, device="cpu", seed: int = DATA_SEED, **overrides) -> PagedBatch:
+NAN_CODE = 0x7F  # E4M3 S.1111.111
+
+
+def _codes_e4m3(shape, gen: torch.Generator, device) -> torch.Tensor:
+    """E4M3 codes (uint8): N(0, 110^2) draws clamped to the largest finite
+    code and cast by torch's float8_e4m3fn conversion."""
+    out = torch.empty(shape, dtype=torch.uint8, device=device)
+    flat = out.view(-1)
+    n = flat.numel()
+    chunk = 1 << 26
+    for s in range(0, n, chunk):
+        e = min(n, s + chunk)
+        t = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32)
+        t.mul_(110.0).clamp_(-448.0, 448.0)
+        flat[s:e].copy_(t.to(torch.float8_e4m3fn).view(torch.uint8))
+    return out
+
+
+def _scales(shape, kv_std: float, gen: torch.Generator, device) -> torch.Tensor:
+    u = torch.rand(shape, generator=gen, device=device, dtype=torch.float32)
+    return (u + 0.5) * (kv_std / 110.0)
+
+
+def _poison8(k8, v8, ks, vs, tables, ctx_lens, bs, nblk, spare_ids, appended, device):
+    """NaN codes and NaN scales wherever nothing valid is cached."""
+    nan = float("nan")
+    if spare_ids.numel():
+        sid = spare_ids.long().to(device)
+        k8[sid] = NAN_CODE
+        v8[sid] = NAN_CODE
+        ks[sid] = nan
+        vs[sid] = nan
+    for b in range(len(ctx_lens)):
+        tail = ctx_lens[b] % bs
+        if tail:
+            last = int(tables[b, nblk[b] - 1])
+            k8[last, :, tail:, :] = NAN_CODE
+            v8[last, :, tail:, :] = NAN_CODE
+            ks[last, :, tail:] = nan
+            vs[last, :, tail:] = nan
+    if appended is not None:
+        blk, slot = appended
+        k8[blk, :, slot, :] = NAN_CODE
+        v8[blk, :, slot, :] = NAN_CODE
+        ks[blk, :, slot] = nan
+        vs[blk, :, slot] = nan
+
+
+def make_workload(name: str, device="cpu", seed: int = DATA_SEED, kv_format: str = "bf16",
+                  **overrides) -> PagedBatch:
     w = WORKLOADS[name]
     if overrides:
         w = dataclasses.replace(w, **overrides)
     lens = context_lengths(w, seed)
     return make_batch(w.batch, w.n_q, w.n_kv, w.block_size, lens, head_dim=w.head_dim,
                       kv_std=w.kv_std, q_std=w.q_std, shared_prefix=w.shared_prefix,
-                      append=w.append, seed=seed, device=device, scale=w.scale)
+                      append=w.append, seed=seed, device=device, scale=w.scale,
+                      kv_format=kv_format)
 
 
 def kv_bytes_read(batch: PagedBatch, unique: bool = False) -> int:
     """Algorithmic K+V bytes one attention call must read: every cached token
-    of every sequence, all KV heads, K and V, bf16 (logical), or each physical
-    block once (unique; only differs when blocks are shared)."""
-    per_token = 2 * batch.n_kv * batch.head_dim * batch.k_cache.element_size()
+    of every sequence, all KV heads, K and V (logical), or each physical block
+    once (unique; only differs when blocks are shared).  bf16: 2 bytes per
+    element; fp8: 1 byte per element plus the token's fp32 scale."""
+    per_head = batch.head_dim * batch.k_cache.element_size()
+    if batch.kv_format == "fp8":
+        per_head += 4
+    per_token = 2 * batch.n_kv * per_head
     assert batch.k_cache.dim() == 6
     if not unique:
         return int(batch.context_lens.sum().item()) * per_token
