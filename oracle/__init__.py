@@ -81,10 +81,9 @@ def _load():
         lib.oracle_e4m3_encode_mode.restype = ctypes.c_uint8
         lib.oracle_quantize_row.argtypes = [P, I, P, P, I]
         lib.oracle_quantize_row.restype = None
-        lib.oracle_kv_append_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I]
+        lib.oracle_kv_append_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I]
         lib.oracle_kv_append_fp8.restype = I
-        lib.oracle_paged_attention_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, D,
-                                                   I, I]
+        lib.oracle_paged_attention_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, D, I, I]
         lib.oracle_paged_attention_fp8.restype = I
         _lib = lib
         return lib
@@ -221,18 +220,13 @@ def _u8(a) -> np.ndarray:
     return np.ascontiguousarray(a.detach().cpu().contiguous().numpy())
 
 
-def _f32(a) -> np.ndarray:
-    if isinstance(a, np.ndarray):
-        return np.ascontiguousarray(a, dtype=np.float32)
-    return np.ascontiguousarray(a.detach().cpu().contiguous().numpy().astype(np.float32))
-
-
-def _tile8_dims(cache: np.ndarray):
-    """(NB, n_kv, bs, d) of an 8-bit pool stored as [NB][n_kv][bs/8][d/16][8][16]."""
-    if cache.ndim != 6 or cache.shape[4:] != (8, 16):
-        raise ValueError("8-bit cache must be [NB][n_kv][bs/8][d/16][8][16]")
-    NB, n_kv, rg, nc = cache.shape[:4]
-    return NB, n_kv, rg * 8, nc * 16
+def _pool8_dims(cache: np.ndarray, bs: int):
+    """(NB, n_kv, d) of an 8-bit pool stored as [NB][n_kv][bs/8][8*d + 32]
+    (per 8-token group: codes as 8 x 16-byte core matrices, then 8 fp32
+    scales)."""
+    if cache.ndim != 4 or cache.shape[2] * 8 != bs or (cache.shape[3] - 32) % 8:
+        raise ValueError("8-bit cache must be [NB][n_kv][bs/8][8*d + 32] uint8")
+    return cache.shape[0], cache.shape[1], (cache.shape[3] - 32) // 8
 
 
 def e4m3_decode(codes) -> np.ndarray:
@@ -270,39 +264,36 @@ def quantize_rows(x, mutation: int = 0):
     return codes.reshape(xa.shape), scales.reshape(xa.shape[:-1])
 
 
-def kv_append_fp8(k_cache, v_cache, k_scale, v_scale, k_new, v_new, block_tables, positions,
+def kv_append_fp8(k_cache, v_cache, k_new, v_new, block_tables, positions, block_size: int,
                   mutation: int = 0):
-    """Return copies of (k_cache, v_cache, k_scale, v_scale) with one new token
-    per sequence quantised and written at logical position positions[b]."""
+    """Return copies of the 8-bit pools (k_cache, v_cache) with one new token
+    per sequence quantised and written, codes and scale, at logical position
+    positions[b]."""
     kc, vc = _u8(k_cache).copy(), _u8(v_cache).copy()
-    ks, vs = _f32(k_scale).copy(), _f32(v_scale).copy()
     kn, vn = _u16(k_new), _u16(v_new)
     ta, pa = _i32(block_tables), _i32(positions)
-    NB, n_kv, bs, d = _tile8_dims(kc)
-    assert ks.shape == (NB, n_kv, bs) and vs.shape == ks.shape
+    NB, n_kv, d = _pool8_dims(kc, block_size)
     B = kn.shape[0]
-    st = _load().oracle_kv_append_fp8(_p(kc), _p(vc), _p(ks), _p(vs), _p(kn), _p(vn), _p(ta),
-                                      _p(pa), B, n_kv, d, bs, ta.shape[1], NB, int(mutation))
+    st = _load().oracle_kv_append_fp8(_p(kc), _p(vc), _p(kn), _p(vn), _p(ta), _p(pa), B, n_kv, d,
+                                      block_size, ta.shape[1], NB, int(mutation))
     if st:
         raise ValueError("oracle: position or block id out of range")
-    return kc, vc, ks, vs
+    return kc, vc
 
 
-def paged_attention_fp8(q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
-                        scale: float, n_threads: int = 0, mutation: int = 0) -> np.ndarray:
+def paged_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                        block_size: int, n_threads: int = 0, mutation: int = 0) -> np.ndarray:
     """float64 out[B][n_q][d] of decode attention over the 8-bit cache: the
     definition of ``paged_attention`` applied to the dequantised K and V.
-    k_cache, v_cache: uint8 [NB][n_kv][bs/8][d/16][8][16]; k_scale, v_scale:
-    float32 [NB][n_kv][bs]."""
+    k_cache, v_cache: uint8 [NB][n_kv][bs/8][8*d + 32]."""
     qa, ka, va = _u16(q), _u8(k_cache), _u8(v_cache)
-    ks, vs = _f32(k_scale), _f32(v_scale)
     ta, ca = _i32(block_tables), _i32(context_lens)
     B, n_q, d = qa.shape
-    NB, n_kv, bs, d2 = _tile8_dims(ka)
-    assert d2 == d and va.shape == ka.shape and ks.shape == (NB, n_kv, bs)
+    NB, n_kv, d2 = _pool8_dims(ka, block_size)
+    assert d2 == d and va.shape == ka.shape
     out = np.zeros((B, n_q, d), dtype=np.float64)
-    st = _load().oracle_paged_attention_fp8(_p(out), _p(qa), _p(ka), _p(va), _p(ks), _p(vs),
-                                            _p(ta), _p(ca), B, n_q, n_kv, d, bs, ta.shape[1], NB,
+    st = _load().oracle_paged_attention_fp8(_p(out), _p(qa), _p(ka), _p(va), _p(ta), _p(ca), B,
+                                            n_q, n_kv, d, block_size, ta.shape[1], NB,
                                             float(scale), int(n_threads), int(mutation))
     if st:
         raise ValueError("oracle: invalid context length or block id (status %d)" % st)

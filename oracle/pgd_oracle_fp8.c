@@ -35,13 +35,14 @@
  *  - attention over the 8-bit cache is the attention of pgd_oracle.c over the
  *    dequantised K and V (the query stays bf16).
  *
- * Physical layout of an 8-bit pool: [NB][n_kv][tile], one tile per (block,
- * KV head) of bs x d codes as 8-row x 16-byte core matrices -- code (slot s,
- * dim i) at ((s / 8) * (d / 16) + i / 16) * 128 + (s % 8) * 16 + i % 16;
- * scales [NB][n_kv][bs] fp32.
+ * Physical layout of an 8-bit pool (the library's choice): [NB][n_kv][bs/8]
+ * groups of 8 tokens, each group 8*d + 32 bytes -- the codes of its 8 tokens
+ * as 8-row x 16-byte core matrices (code of group slot r, dim i at
+ * (i / 16) * 128 + r * 16 + i % 16), then the 8 tokens' fp32 scales (scale
+ * of group slot r at 8*d + 4*r, little-endian binary32).
  *
  * Mutations (tests plant them here to check the pins): 9 K scales ignored,
- * 10 V scales ignored, 11 code index uses the 16-bit tile formula,
+ * 10 V scales ignored, 11 codes read in 16-bit core-matrix order (8 x 8),
  * 12 quantiser truncates instead of rounding to nearest.
  */
 #include <math.h>
@@ -88,16 +89,32 @@ uint8_t oracle_e4m3_encode_mode(float x, int truncate) {
 
 uint8_t oracle_e4m3_encode(float x) { return oracle_e4m3_encode_mode(x, 0); }
 
-/* Offset of code (slot, i) inside one 8-bit tile. */
-static size_t tile8_offset(int slot, int i, int d) {
-  return ((size_t)(slot >> 3) * (size_t)(d >> 4) + (size_t)(i >> 4)) * 128 +
-         (size_t)(slot & 7) * 16 + (size_t)(i & 15);
+/* Bytes of one 8-token group: codes, then scales. */
+static size_t group_bytes(int d) { return (size_t)8 * d + 32; }
+
+/* Byte offset of the group holding `slot` of (block, head) in the pool. */
+static size_t group_base(int blk, int g, int slot, int n_kv, int bs, int d) {
+  return (((size_t)blk * n_kv + g) * (size_t)(bs >> 3) + (size_t)(slot >> 3)) * group_bytes(d);
 }
 
-/* Offset under the 16-bit tile formula (mutation 11 only). */
-static size_t tile16_offset(int slot, int i, int d) {
-  return ((size_t)(slot >> 3) * (size_t)(d >> 3) + (size_t)(i >> 3)) * 64 +
-         (size_t)(slot & 7) * 8 + (size_t)(i & 7);
+/* Offset of the code of dim i of group slot r inside its group. */
+static size_t code_offset(int r, int i) {
+  return (size_t)(i >> 4) * 128 + (size_t)r * 16 + (size_t)(i & 15);
+}
+
+/* Offset under the 16-bit (8 x 8) core-matrix order -- mutation 11 only. */
+static size_t code_offset16(int r, int i) {
+  return (size_t)(i >> 3) * 64 + (size_t)r * 8 + (size_t)(i & 7);
+}
+
+static float load_scale(const uint8_t *group, int d, int r) {
+  float f;
+  memcpy(&f, group + (size_t)8 * d + (size_t)4 * r, sizeof f);
+  return f;
+}
+
+static void store_scale(uint8_t *group, int d, int r, float f) {
+  memcpy(group + (size_t)8 * d + (size_t)4 * r, &f, sizeof f);
 }
 
 static float bf16_bits_to_float(uint16_t bits) {
@@ -128,13 +145,13 @@ void oracle_quantize_row(const uint16_t *x, int d, uint8_t *codes, float *scale_
 /* ------------------------------------------------------------ kv_append */
 
 /* For every sequence b and KV head g: quantise k_new[b][g][:] and
- * v_new[b][g][:] and store the codes at slot positions[b] % bs of block
- * table[b][positions[b] / bs], and the scales beside them.  Returns 0, or 1
- * if a position or block id is out of range (that sequence is skipped). */
-int oracle_kv_append_fp8(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
-                         const uint16_t *k_new, const uint16_t *v_new,
-                         const int32_t *block_tables, const int32_t *positions, int B,
-                         int n_kv, int d, int bs, int MB, int NB, int mutation) {
+ * v_new[b][g][:] and store the codes and the scale at slot positions[b] % bs
+ * of block table[b][positions[b] / bs].  Returns 0, or 1 if a position or
+ * block id is out of range (that sequence is skipped). */
+int oracle_kv_append_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new,
+                         const uint16_t *v_new, const int32_t *block_tables,
+                         const int32_t *positions, int B, int n_kv, int d, int bs, int MB,
+                         int NB, int mutation) {
   int status = 0;
   uint8_t *row = (uint8_t *)malloc((size_t)d);
   if (!row) return 2;
@@ -143,18 +160,17 @@ int oracle_kv_append_fp8(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, flo
     if (pos < 0 || pos >= MB * bs) { status = 1; continue; }
     int32_t blk = block_tables[(size_t)b * MB + pos / bs];
     if (blk < 0 || blk >= NB) { status = 1; continue; }
-    int slot = pos % bs;
+    int slot = pos % bs, r = slot & 7;
     for (int g = 0; g < n_kv; ++g) {
-      size_t tile = ((size_t)blk * n_kv + g) * (size_t)bs * d;
-      size_t sidx = ((size_t)blk * n_kv + g) * (size_t)bs + slot;
+      size_t base = group_base(blk, g, slot, n_kv, bs, d);
       size_t src = ((size_t)b * n_kv + g) * d;
       float sc;
       oracle_quantize_row(k_new + src, d, row, &sc, mutation);
-      for (int i = 0; i < d; ++i) k_cache[tile + tile8_offset(slot, i, d)] = row[i];
-      k_scale[sidx] = sc;
+      for (int i = 0; i < d; ++i) k_cache[base + code_offset(r, i)] = row[i];
+      store_scale(k_cache + base, d, r, sc);
       oracle_quantize_row(v_new + src, d, row, &sc, mutation);
-      for (int i = 0; i < d; ++i) v_cache[tile + tile8_offset(slot, i, d)] = row[i];
-      v_scale[sidx] = sc;
+      for (int i = 0; i < d; ++i) v_cache[base + code_offset(r, i)] = row[i];
+      store_scale(v_cache + base, d, r, sc);
     }
   }
   free(row);
@@ -167,7 +183,6 @@ typedef struct {
   double *out;
   const uint16_t *q;
   const uint8_t *k_cache, *v_cache;
-  const float *k_scale, *v_scale;
   const int32_t *tables, *ctx;
   int B, n_q, n_kv, d, bs, MB, NB;
   double scale;
@@ -176,17 +191,17 @@ typedef struct {
   int status;
 } job8;
 
-/* Dequantised element i of token t (sequence b, KV head g) from `cache`
- * with `scales`; 0 return on success, 1 on a bad block id. */
-static int elem8(const job8 *J, const uint8_t *cache, const float *scales, int use_scale, int b,
-                 int g, int t, int i, double *v) {
+/* Dequantised element i of token t (sequence b, KV head g) from `cache`;
+ * 0 on success, 1 on a bad block id. */
+static int elem8(const job8 *J, const uint8_t *cache, int use_scale, int b, int g, int t, int i,
+                 double *v) {
   int32_t blk = J->tables[(size_t)b * J->MB + t / J->bs];
   if (blk < 0 || blk >= J->NB) return 1;
-  int slot = t % J->bs;
-  size_t tile = ((size_t)blk * J->n_kv + g) * (size_t)J->bs * J->d;
-  size_t off = (J->mutation == 11) ? tile16_offset(slot, i, J->d) : tile8_offset(slot, i, J->d);
-  double s = use_scale ? (double)scales[((size_t)blk * J->n_kv + g) * (size_t)J->bs + slot] : 1.0;
-  *v = oracle_e4m3_decode(cache[tile + off]) * s;
+  int slot = t % J->bs, r = slot & 7;
+  const uint8_t *group = cache + group_base(blk, g, slot, J->n_kv, J->bs, J->d);
+  size_t off = (J->mutation == 11) ? code_offset16(r, i) : code_offset(r, i);
+  double s = use_scale ? (double)load_scale(group, J->d, r) : 1.0;
+  *v = oracle_e4m3_decode(group[off]) * s;
   return 0;
 }
 
@@ -204,7 +219,7 @@ static int attend_row8(const job8 *J, int b, int h) {
     double acc = 0.0;
     for (int i = 0; i < d; ++i) {
       double kv;
-      if (elem8(J, J->k_cache, J->k_scale, J->mutation != 9, b, g, t, i, &kv)) {
+      if (elem8(J, J->k_cache, J->mutation != 9, b, g, t, i, &kv)) {
         free(s);
         return 1;
       }
@@ -223,7 +238,7 @@ static int attend_row8(const job8 *J, int b, int h) {
     double w = s[t] / denom;
     for (int i = 0; i < d; ++i) {
       double vv;
-      elem8(J, J->v_cache, J->v_scale, J->mutation != 10, b, g, t, i, &vv);
+      elem8(J, J->v_cache, J->mutation != 10, b, g, t, i, &vv);
       orow[i] += w * vv;
     }
   }
@@ -241,12 +256,12 @@ static void *worker8(void *arg) {
 }
 
 /* out[b][h][:] = sum_t softmax_t(scale * q[b][h] . k~_t) v~_t over t <
- * context_lens[b], where k~, v~ are the dequantised codes of KV head h / G.
+ * context_lens[b], where k~, v~ are the dequantised codes (code value times
+ * the token's scale) of KV head h / G.
  * n_threads <= 0: one per online core.  Returns 0, or 1 on an invalid
  * context length or block id. */
 int oracle_paged_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
-                               const uint8_t *v_cache, const float *k_scale,
-                               const float *v_scale, const int32_t *block_tables,
+                               const uint8_t *v_cache, const int32_t *block_tables,
                                const int32_t *context_lens, int B, int n_q, int n_kv, int d,
                                int bs, int MB, int NB, double scale, int n_threads,
                                int mutation) {
@@ -261,7 +276,7 @@ int oracle_paged_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_
   }
   if (n_threads > 256) n_threads = 256;
   if (rows < n_threads) n_threads = (int)rows;
-  job8 base = {out, q, k_cache, v_cache, k_scale, v_scale, block_tables, context_lens,
+  job8 base = {out, q, k_cache, v_cache, block_tables, context_lens,
                B, n_q, n_kv, d, bs, MB, NB, scale, mutation, 0, 0, 0};
   job8 *jobs = (job8 *)calloc((size_t)n_threads, sizeof(job8));
   pthread_t *th = (pthread_t *)calloc((size_t)n_threads, sizeof(pthread_t));

@@ -107,29 +107,36 @@ def pool_shape(num_blocks: int, n_kv: int, block_size: int, head_dim: int = HEAD
     return (num_blocks, n_kv, block_size // 8, head_dim // 8, 8, 8)
 
 
-def tile_pool8(x: torch.Tensor) -> torch.Tensor:
-    """Row-major 8-bit pool [NB][n_kv][bs][d] -> tiled [NB][n_kv][bs/8][d/16][8][16]
-    (8-row x 16-byte core matrices)."""
-    NB, n_kv, bs, d = x.shape
-    return x.reshape(NB, n_kv, bs // 8, 8, d // 16, 16).permute(0, 1, 2, 4, 3, 5).contiguous()
+def pack_pool8(codes: torch.Tensor, scales: torch.Tensor) -> torch.Tensor:
+    """Row-major E4M3 codes [NB][n_kv][bs][d] (uint8) and fp32 scales
+    [NB][n_kv][bs] -> the 8-bit pool [NB][n_kv][bs/8][8*d + 32]: per 8-token
+    group, the codes as 8-row x 16-byte core matrices, then the 8 scales."""
+    NB, n_kv, bs, d = codes.shape
+    c = codes.reshape(NB, n_kv, bs // 8, 8, d // 16, 16).permute(0, 1, 2, 4, 3, 5)
+    c = c.reshape(NB, n_kv, bs // 8, 8 * d)
+    sc = scales.contiguous().reshape(NB, n_kv, bs // 8, 8).view(torch.uint8)
+    return torch.cat([c, sc], dim=3).contiguous()
 
 
-def untile_pool8(x: torch.Tensor) -> torch.Tensor:
-    """Tiled 8-bit pool [NB][n_kv][bs/8][d/16][8][16] -> row-major [NB][n_kv][bs][d]."""
-    NB, n_kv, rg, nc = x.shape[:4]
-    return x.permute(0, 1, 2, 4, 3, 5).reshape(NB, n_kv, rg * 8, nc * 16)
+def unpack_pool8(pool: torch.Tensor):
+    """The 8-bit pool -> (codes [NB][n_kv][bs][d] uint8, scales [NB][n_kv][bs] fp32)."""
+    NB, n_kv, ng, gb = pool.shape
+    d = (gb - 32) // 8
+    c = pool[..., :8 * d].reshape(NB, n_kv, ng, d // 16, 8, 16).permute(0, 1, 2, 4, 3, 5)
+    codes = c.reshape(NB, n_kv, ng * 8, d)
+    scales = pool[..., 8 * d:].contiguous().view(torch.float32).reshape(NB, n_kv, ng * 8)
+    return codes, scales
 
 
 def pool_shape8(num_blocks: int, n_kv: int, block_size: int, head_dim: int = HEAD_DIM):
-    return (num_blocks, n_kv, block_size // 8, head_dim // 16, 8, 16)
+    return (num_blocks, n_kv, block_size // 8, 8 * head_dim + 32)
 
 
 @dataclasses.dataclass
 class PagedBatch:
     """Inputs of one decode step.  Tensors live on `device`.  With
-    kv_format "fp8" the pools hold E4M3 codes (uint8, tiled as
-    [NB][n_kv][bs/8][d/16][8][16]) and k_scale / v_scale their per-(token,
-    head) scales."""
+    kv_format "fp8" the pools are uint8 [NB][n_kv][bs/8][8*d + 32]: E4M3
+    codes and per-(token, head) fp32 scales (see pack_pool8)."""
     q: torch.Tensor              # bf16 [B][n_q][d]
     k_cache: torch.Tensor        # bf16 [NB][n_kv][bs/8][d/8][8][8] (tiled), or uint8 codes
     v_cache: torch.Tensor        # same layout
@@ -144,8 +151,6 @@ class PagedBatch:
     unique_blocks: int           # physical blocks referenced by the tables
     shared_blocks: int           # blocks referenced by more than one sequence
     kv_format: str = "bf16"      # "bf16" or "fp8" (E4M3 codes + scales)
-    k_scale: Optional[torch.Tensor] = None   # fp32 [NB][n_kv][bs] (fp8 only)
-    v_scale: Optional[torch.Tensor] = None
 
     @property
     def batch(self) -> int:
@@ -160,7 +165,7 @@ class PagedBatch:
         return self.q.shape[2]
 
     def token(self, cache: torch.Tensor, block: int, head: int, slot: int) -> torch.Tensor:
-        """The d-vector (values, or codes for fp8) of one cached token."""
+        """The d-vector of one cached token (bf16 pools)."""
         t = cache[block, head, slot // 8, :, slot % 8, :]
         return t.reshape(-1)
 
@@ -206,8 +211,9 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
     kv_format="fp8": the pools hold E4M3 codes drawn as N(0, 110^2) values
     clamped to +-448 and cast to float8_e4m3fn, with per-(token, head) scales
     uniform in kv_std * [0.5, 1.5] / 110 (so the dequantised values are about
-    N(0, kv_std^2)); poisoned slots hold the NaN code and a NaN scale.  The
-    appended token's k_new/v_new are fresh bf16 N(0, kv_std^2) draws."""
+    N(0, kv_std^2)), packed by pack_pool8; poisoned slots hold the NaN code
+    and a NaN scale.  The appended token's k_new/v_new are fresh bf16
+    N(0, kv_std^2) draws."""
     assert kv_format in ("bf16", "fp8")
     assert len(ctx_lens) == batch and n_q % n_kv == 0 and block_size % 8 == 0
     bs = block_size
@@ -279,8 +285,8 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
             v_cache[blk, :, slot, :] = nan
     del used_ids
     if fp8:
-        k_cache = tile_pool8(k_cache)
-        v_cache = tile_pool8(v_cache)
+        k_cache = pack_pool8(k_cache, k_scale)
+        v_cache = pack_pool8(v_cache, v_scale)
     else:
         k_cache = tile_pool(k_cache)
         v_cache = tile_pool(v_cache)
@@ -292,7 +298,7 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
         positions=None if positions is None else positions.to(device),
         scale=(1.0 / math.sqrt(head_dim)) if scale is None else scale,
         n_kv=n_kv, block_size=bs, unique_blocks=needed,
-        shared_blocks=n_shared, kv_format=kv_format, k_scale=k_scale, v_scale=v_scale)
+        shared_blocks=n_shared, kv_format=kv_format)
 
 
 NAN_CODE = 0x7F  # E4M3 S.1111.111

@@ -111,13 +111,13 @@ def test_quantizer_truncation_mutation_is_caught():
 def test_kv_append_fp8_places_quantised_rows(bs):
     lens = [1, bs, bs + 1, 3 * bs - 2, 77]
     pb = inputs.make_batch(len(lens), 16, 4, bs, lens, append=True, kv_format="fp8")
-    k, v, ks, vs = oracle.kv_append_fp8(pb.k_cache, pb.v_cache, pb.k_scale, pb.v_scale,
-                                        pb.k_new, pb.v_new, pb.block_tables, pb.positions)
+    k, v = oracle.kv_append_fp8(pb.k_cache, pb.v_cache, pb.k_new, pb.v_new, pb.block_tables,
+                                pb.positions, bs)
     kc, ksc = oracle.quantize_rows(pb.k_new)
     vc, vsc = oracle.quantize_rows(pb.v_new)
-    k_rows = inputs.untile_pool8(torch.from_numpy(k)).numpy()
-    v_rows = inputs.untile_pool8(torch.from_numpy(v)).numpy()
-    before_k = inputs.untile_pool8(pb.k_cache).numpy()
+    k_rows, ks = (t.numpy() for t in inputs.unpack_pool8(torch.from_numpy(k)))
+    v_rows, vs = (t.numpy() for t in inputs.unpack_pool8(torch.from_numpy(v)))
+    before_k = inputs.unpack_pool8(pb.k_cache)[0].numpy()
     touched = np.zeros(k_rows.shape[:3], dtype=bool)
     for b, pos in enumerate(pb.positions.tolist()):
         blk = int(pb.block_tables[b, pos // bs])
@@ -131,15 +131,15 @@ def test_kv_append_fp8_places_quantised_rows(bs):
 
 
 # ------------------------------------------------------------- attention
-def _dequantised_rows(pb, cache, scales):
-    rows = inputs.untile_pool8(cache.cpu()).numpy()
-    return torch_decode(rows) * scales.cpu().double().numpy()[..., None]
+def _dequantised_rows(pool):
+    codes, scales = inputs.unpack_pool8(torch.as_tensor(pool).cpu())
+    return torch_decode(codes.numpy()) * scales.double().numpy()[..., None]
 
 
-def sdpa_fp8(pb, k, v, ks, vs):
+def sdpa_fp8(pb, k, v):
     """float64 SDPA over contiguous dequantised K/V gathered through the tables."""
-    K = _dequantised_rows(pb, torch.as_tensor(k), torch.as_tensor(ks))
-    V = _dequantised_rows(pb, torch.as_tensor(v), torch.as_tensor(vs))
+    K = _dequantised_rows(k)
+    V = _dequantised_rows(v)
     B, n_q, d = pb.q.shape
     G = n_q // pb.n_kv
     out = np.zeros((B, n_q, d))
@@ -163,27 +163,25 @@ CASES = [(8, 2, 16, [1, 16, 17, 70]), (32, 8, 32, [33, 100]), (4, 4, 16, [5]), (
 def test_attention_fp8_matches_sdpa_on_dequantised_values(case):
     n_q, n_kv, bs, lens = case
     pb = inputs.make_batch(len(lens), n_q, n_kv, bs, lens, kv_format="fp8")
-    got = oracle.paged_attention_fp8(pb.q, pb.k_cache, pb.v_cache, pb.k_scale, pb.v_scale,
-                                     pb.block_tables, pb.context_lens, pb.scale)
-    want = sdpa_fp8(pb, pb.k_cache, pb.v_cache, pb.k_scale, pb.v_scale)
+    got = oracle.paged_attention_fp8(pb.q, pb.k_cache, pb.v_cache, pb.block_tables,
+                                     pb.context_lens, pb.scale, bs)
+    want = sdpa_fp8(pb, pb.k_cache, pb.v_cache)
     assert np.abs(got - want).max() <= 1e-12
 
 
 def test_attention_fp8_after_append():
     pb = inputs.make_batch(3, 16, 4, 16, [20, 1, 48], append=True, kv_format="fp8")
-    k, v, ks, vs = oracle.kv_append_fp8(pb.k_cache, pb.v_cache, pb.k_scale, pb.v_scale,
-                                        pb.k_new, pb.v_new, pb.block_tables, pb.positions)
-    got = oracle.paged_attention_fp8(pb.q, k, v, ks, vs, pb.block_tables, pb.context_lens,
-                                     pb.scale)
+    k, v = oracle.kv_append_fp8(pb.k_cache, pb.v_cache, pb.k_new, pb.v_new, pb.block_tables,
+                                pb.positions, 16)
+    got = oracle.paged_attention_fp8(pb.q, k, v, pb.block_tables, pb.context_lens, pb.scale, 16)
     assert np.all(np.isfinite(got))
-    assert np.abs(got - sdpa_fp8(pb, k, v, ks, vs)).max() <= 1e-12
+    assert np.abs(got - sdpa_fp8(pb, k, v)).max() <= 1e-12
 
 
 @pytest.mark.parametrize("mutation", [9, 10, 11])
 def test_fp8_attention_mutations_are_caught(mutation):
     pb = inputs.make_batch(2, 8, 2, 16, [40, 70], kv_format="fp8")
-    want = sdpa_fp8(pb, pb.k_cache, pb.v_cache, pb.k_scale, pb.v_scale)
-    bad = oracle.paged_attention_fp8(pb.q, pb.k_cache, pb.v_cache, pb.k_scale, pb.v_scale,
-                                     pb.block_tables, pb.context_lens, pb.scale,
-                                     mutation=mutation)
+    want = sdpa_fp8(pb, pb.k_cache, pb.v_cache)
+    bad = oracle.paged_attention_fp8(pb.q, pb.k_cache, pb.v_cache, pb.block_tables,
+                                     pb.context_lens, pb.scale, 16, mutation=mutation)
     assert not np.all(np.abs(bad - want) <= 1e-6)  # NaN counts as caught
