@@ -210,6 +210,61 @@ pgd_status pgd_append_decode_attention(void *out, const void *q, const void *k_n
                                        void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* 8-bit KV cache: FP8 E4M3 codes with one fp32 scale per (token, head)    */
+/* ---------------------------------------------------------------------- */
+/* Storing the cache in 8 bits halves its memory and the bytes a decode step
+ * reads ("Module 10", section "Quantize the cache, evaluate the final
+ * artifact"; "The math of Transformer inference", section 11: KV in int8 /
+ * fp8, scales per head and per token, dequantisation fused into the kernel).
+ *
+ * Pool layout (k_cache, v_cache; the library's choice): uint8
+ * [NB][n_kv][bs/8][1056] -- each (block, KV head) tile is bs/8 groups of 8
+ * tokens; a group holds the 8 tokens' E4M3 codes (1024 bytes: code of group
+ * slot r, dim i at (i / 16) * 128 + r * 16 + i % 16) followed by their 8
+ * fp32 scales (byte 1024 + 4 r).  Token t of a sequence is code row
+ * t % bs of block block_tables[b][t / bs]; its value is E4M3(code) * scale.
+ * The pool must be 16-byte aligned.
+ *
+ * Quantisation (pgd_kv_append_fp8; "Ch. 6 Inference efficiency and
+ * serving", 6.6.1: symmetric, scale from the largest absolute value, never a
+ * zero scale): for each (sequence, KV head) row x of d = 128 bf16 values,
+ * scale = max_i |x_i| / 448 (1 when that max is 0) and code_i =
+ * E4M3(x_i / scale), both divisions IEEE binary32, the E4M3 conversion
+ * rounding to nearest even and saturating to +-448 (OCP E4M3: no
+ * infinities; S.1111.111 is NaN).  Same arguments, checks and errors as
+ * pgd_kv_append. */
+pgd_status pgd_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int32_t *block_tables, const int32_t *positions, int32_t B,
+                             int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB,
+                             void *stream);
+
+/* pgd_paged_decode_attention over an 8-bit pool: the same definition applied
+ * to the dequantised K and V, the same arguments (k_cache, v_cache as
+ * above), checks, errors and workspace (pgd_attention_workspace_size).
+ * Arithmetic: q.k^T on the tensor cores in E4M3 with the query split into a
+ * high and a low E4M3 part (about 8 bits of the bf16 query), the key and
+ * query scales applied in fp32; V converted to bf16 exactly and its scale
+ * folded into the bf16 probabilities; fp32 softmax and accumulation; bf16
+ * output.  The query must be finite. */
+pgd_status pgd_paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, int32_t B, int32_t n_q,
+                                          int32_t n_kv, int32_t d, int32_t bs, int32_t MB,
+                                          int32_t NB, float scale, int32_t num_splits,
+                                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* pgd_append_decode_attention for an 8-bit pool: pgd_kv_append_fp8 at
+ * position context_lens[b] - 1, then pgd_paged_decode_attention_fp8, with the
+ * same overlap of the attention prologue and the append. */
+pgd_status pgd_append_decode_attention_fp8(void *out, const void *q, const void *k_new,
+                                           const void *v_new, void *k_cache, void *v_cache,
+                                           const int32_t *block_tables,
+                                           const int32_t *context_lens, int32_t B, int32_t n_q,
+                                           int32_t n_kv, int32_t d, int32_t bs, int32_t MB,
+                                           int32_t NB, float scale, int32_t num_splits,
+                                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* one decode step with host inputs and outputs                            */
 /* ---------------------------------------------------------------------- */
 /* One decode step of one layer for a caller whose per-step tensors live in

@@ -89,6 +89,13 @@ uint8_t oracle_e4m3_encode_mode(float x, int truncate) {
 
 uint8_t oracle_e4m3_encode(float x) { return oracle_e4m3_encode_mode(x, 0); }
 
+/* The 256 code values, filled from oracle_e4m3_decode before any worker
+ * thread starts (a plain cache of the definition above). */
+static double e4m3_value[256];
+static void fill_e4m3_values(void) {
+  for (int c = 0; c < 256; ++c) e4m3_value[c] = oracle_e4m3_decode((uint8_t)c);
+}
+
 /* Bytes of one 8-token group: codes, then scales. */
 static size_t group_bytes(int d) { return (size_t)8 * d + 32; }
 
@@ -201,7 +208,7 @@ static int elem8(const job8 *J, const uint8_t *cache, int use_scale, int b, int 
   const uint8_t *group = cache + group_base(blk, g, slot, J->n_kv, J->bs, J->d);
   size_t off = (J->mutation == 11) ? code_offset16(r, i) : code_offset(r, i);
   double s = use_scale ? (double)load_scale(group, J->d, r) : 1.0;
-  *v = oracle_e4m3_decode(group[off]) * s;
+  *v = e4m3_value[group[off]] * s;
   return 0;
 }
 
@@ -276,6 +283,7 @@ int oracle_paged_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_
   }
   if (n_threads > 256) n_threads = 256;
   if (rows < n_threads) n_threads = (int)rows;
+  fill_e4m3_values();
   job8 base = {out, q, k_cache, v_cache, block_tables, context_lens,
                B, n_q, n_kv, d, bs, MB, NB, scale, mutation, 0, 0, 0};
   job8 *jobs = (job8 *)calloc((size_t)n_threads, sizeof(job8));

@@ -6,17 +6,19 @@ argument marshalling over it.  Importing the package does not load the
 library; the first call does, and fails loudly if it was not built.
 """
 from .inputs import (WORKLOADS, Workload, PagedBatch, make_batch, make_workload,  # noqa: F401
-                     tile_pool, untile_pool, pool_shape)
+                     tile_pool, untile_pool, pool_shape, pack_pool8, unpack_pool8, pool_shape8)
 from ._native import (  # noqa: F401
     PGDError, BlockAllocator, kv_append, paged_decode_attention,
     paged_decode_attention_noalloc, append_decode_attention, decode_step, copy_blocks,
+    kv_append_fp8, paged_decode_attention_fp8, append_decode_attention_fp8,
     device_errors, workspace_size, make_workspace, attention_grid, validate_tables, lib,
     library_path)
 
 __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "tile_pool",
-           "untile_pool", "pool_shape", "PGDError",
+           "untile_pool", "pool_shape", "pack_pool8", "unpack_pool8", "pool_shape8", "PGDError",
            "BlockAllocator", "kv_append", "paged_decode_attention",
            "paged_decode_attention_noalloc", "append_decode_attention", "decode_step",
-           "copy_blocks",
+           "copy_blocks", "kv_append_fp8", "paged_decode_attention_fp8",
+           "append_decode_attention_fp8",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
            "validate_tables", "lib", "library_path"]

@@ -38,6 +38,11 @@ SIGNATURES = {
                                             _F, _I, _P], _I),
     "pgd_append_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      _F, _I, _P, _Z, _P], _I),
+    "pgd_kv_append_fp8": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
+    "pgd_paged_decode_attention_fp8": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                        _I, _P, _Z, _P], _I),
+    "pgd_append_decode_attention_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I,
+                                         _I, _F, _I, _P, _Z, _P], _I),
     "pgd_decode_step": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                          _I, _I, _F, _I, _P, _Z, _P], _I),
     "pgd_copy_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
@@ -236,6 +241,83 @@ def decode_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_
         _ptr(v_cache), _ptr(block_tables), B, n_q, n_kv, d, bs, MB, NB, float(scale),
         int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+# ------------------------------------------------------------ 8-bit KV cache
+def _cache8_dims(pool: torch.Tensor) -> Tuple[int, int, int, int]:
+    """(NB, n_kv, bs, d) of an 8-bit pool uint8 [NB][n_kv][bs/8][8*d + 32]."""
+    if pool.dim() != 4 or pool.dtype != torch.uint8 or (pool.shape[3] - 32) % 8:
+        raise ValueError("8-bit cache must be uint8 [NB][n_kv][bs/8][8*d + 32]")
+    NB, n_kv, ng, gb = pool.shape
+    return NB, n_kv, ng * 8, (gb - 32) // 8
+
+
+def kv_append_fp8(k_new, v_new, k_cache, v_cache, block_tables, positions, stream=None) -> None:
+    """Quantise k_new/v_new [B][n_kv][d] (bf16) per (token, head) and write
+    codes and scales at logical positions[b] of the 8-bit pools."""
+    _need(k_new, torch.bfloat16, "k_new")
+    _need(v_new, torch.bfloat16, "v_new")
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(positions, torch.int32, "positions")
+    NB, n_kv, bs, d = _cache8_dims(k_cache)
+    B, MB = block_tables.shape
+    _check(lib().pgd_kv_append_fp8(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(block_tables), _ptr(positions), B, n_kv, d, bs, MB, NB,
+                                   _stream(stream)))
+
+
+def paged_decode_attention_fp8(out, q, k_cache, v_cache, block_tables, context_lens,
+                               scale: float, num_splits: int = 0,
+                               workspace: Optional[torch.Tensor] = None,
+                               stream=None) -> torch.Tensor:
+    """out[B][n_q][d] (bf16) = paged decode attention of q over the 8-bit cache."""
+    _need(q, torch.bfloat16, "q")
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, n_q, d = q.shape
+    NB, n_kv, bs, _ = _cache8_dims(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = make_workspace(B, n_q, n_kv, num_splits, q.device)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_paged_decode_attention_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        B, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def append_decode_attention_fp8(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                context_lens, scale: float, num_splits: int = 0,
+                                workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """kv_append_fp8 at context_lens - 1, then attention over the 8-bit cache."""
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, n)
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, n_q, d = q.shape
+    NB, n_kv, bs, _ = _cache8_dims(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = make_workspace(B, n_q, n_kv, num_splits, q.device)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_append_decode_attention_fp8(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), B, n_q, n_kv, d, bs, MB, NB, float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+    return out
 
 
 def copy_blocks(k_cache, v_cache, src_ids, dst_ids, stream=None) -> None:

@@ -7,6 +7,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <string>
@@ -18,6 +19,13 @@
 namespace pgd {
 int attention_ctas_per_sm(int G, int bs, int B);
 cudaError_t attention_launch(const AttnParams &p, int G, int bs, int grid, cudaStream_t stream);
+int attention_ctas_per_sm_fp8(int G, int bs, int B);
+cudaError_t attention_launch_fp8(const AttnParams &p, int G, int bs, int grid,
+                                 cudaStream_t stream);
+cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
+                                 void *v_cache, const int32_t *tables, const int32_t *pos,
+                                 int pos_offset, int B, int n_kv, int bs, int MB, int NB,
+                                 int32_t *err, cudaStream_t stream);
 cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                              const int32_t *tables, const int32_t *pos, int pos_offset, int B,
                              int n_kv, int bs, int MB, int NB, int32_t *err,
@@ -119,21 +127,22 @@ WsLayout ws_layout(int32_t B, int32_t n_q, int32_t n_kv, long long grid) {
   return L;
 }
 
-std::map<std::tuple<int, int, int, int>, int> g_occ;
+std::map<std::tuple<int, int, int, int, int>, int> g_occ;
 
-pgd_status auto_grid(int G, int bs, int B, int *grid) {
+pgd_status auto_grid(int G, int bs, int B, int *grid, bool fp8 = false) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   const int bucket = (B + 255) / 256;
   std::lock_guard<std::mutex> lk(g_mu);
-  auto key = std::make_tuple(dev, G, bs, bucket);
+  auto key = std::make_tuple(dev, G, bs, bucket, fp8 ? 1 : 0);
   auto it = g_occ.find(key);
   if (it == g_occ.end()) {
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
-    int per_sm = attention_ctas_per_sm(G, bs, bucket * 256);
+    int per_sm = fp8 ? attention_ctas_per_sm_fp8(G, bs, bucket * 256)
+                     : attention_ctas_per_sm(G, bs, bucket * 256);
     if (per_sm <= 0) return fail(PGD_ERR_CUDA, "occupancy query failed for G=%d bs=%d", G, bs);
     long long g = (long long)sms * per_sm;
     if (g > kAutoMaxCtas) g = kAutoMaxCtas;
@@ -174,13 +183,14 @@ pgd_status check_attention_args(const void *out, const void *q, const void *k_ca
 struct PreparedAttention {
   AttnParams p;
   int G, bs, grid;
+  bool fp8;
 };
 
 pgd_status prepare_attention(void *out, const void *q, const void *k_cache, const void *v_cache,
                              const int32_t *tables, const int32_t *ctx, int32_t B, int32_t n_q,
                              int32_t n_kv, int32_t bs, int32_t MB, int32_t NB, float scale,
                              int32_t num_splits, void *workspace, size_t workspace_bytes,
-                             PreparedAttention *pa) {
+                             PreparedAttention *pa, bool fp8 = false) {
   if (!workspace) return fail(PGD_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(workspace, kWsAlign)) return fail(PGD_ERR_WORKSPACE, "workspace not 256-aligned");
   if (workspace_bytes < ws_layout(B, n_q, n_kv, 1).total)
@@ -190,7 +200,7 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   if (num_splits > 0) {
     grid = (int)((long long)num_splits * B * n_kv);
   } else {
-    pgd_status s = auto_grid(G, bs, B, &grid);
+    pgd_status s = auto_grid(G, bs, B, &grid, fp8);
     if (s != PGD_OK) return s;
   }
   const WsLayout L = ws_layout(B, n_q, n_kv, grid);
@@ -203,8 +213,8 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   AttnParams p;
   p.out = static_cast<__nv_bfloat16 *>(out);
   p.q = static_cast<const __nv_bfloat16 *>(q);
-  p.k_cache = static_cast<const __nv_bfloat16 *>(k_cache);
-  p.v_cache = static_cast<const __nv_bfloat16 *>(v_cache);
+  p.k_cache = static_cast<const unsigned char *>(k_cache);
+  p.v_cache = static_cast<const unsigned char *>(v_cache);
   p.tables = tables;
   p.ctx = ctx;
   p.B = B;
@@ -223,11 +233,13 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   pa->G = G;
   pa->bs = bs;
   pa->grid = grid;
+  pa->fp8 = fp8;
   return PGD_OK;
 }
 
 pgd_status launch_prepared(const PreparedAttention &pa, cudaStream_t stream) {
-  cudaError_t e = attention_launch(pa.p, pa.G, pa.bs, pa.grid, stream);
+  cudaError_t e = pa.fp8 ? attention_launch_fp8(pa.p, pa.G, pa.bs, pa.grid, stream)
+                         : attention_launch(pa.p, pa.G, pa.bs, pa.grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "paged attention launch");
   return PGD_OK;
 }
@@ -253,16 +265,19 @@ pgd_status append_then_attend(void *out, const void *q, const void *k_new, const
                               void *k_cache, void *v_cache, const int32_t *tables,
                               const int32_t *ctx, int32_t B, int32_t n_q, int32_t n_kv,
                               int32_t bs, int32_t MB, int32_t NB, float scale, int32_t num_splits,
-                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream,
+                              bool fp8 = false) {
   if (!k_new || !v_new) return fail(PGD_ERR_INVALID_ARG, "null pointer");
   if (!aligned(k_new, 16) || !aligned(v_new, 16))
     return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
   PreparedAttention pa;
   pgd_status s = prepare_attention(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, bs, MB,
-                                   NB, scale, num_splits, workspace, workspace_bytes, &pa);
+                                   NB, scale, num_splits, workspace, workspace_bytes, &pa, fp8);
   if (s != PGD_OK) return s;
-  cudaError_t e = kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B, n_kv, bs,
-                                   MB, NB, pa.p.err, stream);
+  cudaError_t e = fp8 ? kv_append_fp8_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B,
+                                             n_kv, bs, MB, NB, pa.p.err, stream)
+                      : kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B, n_kv,
+                                         bs, MB, NB, pa.p.err, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   pa.p.wait_late = 1;
   return launch_prepared(pa, stream);
@@ -345,10 +360,11 @@ size_t pgd_attention_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_
     // largest automatic grid when no device is usable
     grid = kAutoMaxCtas;
     const int G = n_q / n_kv;
-    int g16 = 0, g32 = 0;
-    if (supported_group(G) && auto_grid(G, 16, B, &g16) == PGD_OK &&
-        auto_grid(G, 32, B, &g32) == PGD_OK)
-      grid = g16 > g32 ? g16 : g32;
+    int g[4] = {0, 0, 0, 0};
+    if (supported_group(G) && auto_grid(G, 16, B, &g[0]) == PGD_OK &&
+        auto_grid(G, 32, B, &g[1]) == PGD_OK && auto_grid(G, 16, B, &g[2], true) == PGD_OK &&
+        auto_grid(G, 32, B, &g[3], true) == PGD_OK)
+      grid = std::max(std::max(g[0], g[1]), std::max(g[2], g[3]));
     clear_error_detail();
   }
   return ws_layout(B, n_q, n_kv, grid).total;
@@ -392,6 +408,68 @@ pgd_status pgd_append_decode_attention(void *out, const void *q, const void *k_n
   s = append_then_attend(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, B,
                          n_q, n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes,
                          static_cast<cudaStream_t>(stream));
+  return s == PGD_OK ? ok() : s;
+}
+
+// ------------------------------------------------------------- 8-bit cache
+
+pgd_status pgd_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
+                             const int32_t *block_tables, const int32_t *positions, int32_t B,
+                             int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB,
+                             void *stream) {
+  if (B < 0) return fail(PGD_ERR_INVALID_ARG, "B = %d", B);
+  pgd_status s = check_cache_shape(n_kv, d, bs, MB, NB);
+  if (s != PGD_OK) return s;
+  if ((long long)B * n_kv > 0x7fffffffLL) return fail(PGD_ERR_INVALID_ARG, "B * n_kv too large");
+  if (B == 0) return ok();
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !positions)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PGD_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  int32_t *err = nullptr;
+  s = error_word(&err);
+  if (s != PGD_OK) return s;
+  cudaError_t e = kv_append_fp8_launch(k_new, v_new, k_cache, v_cache, block_tables, positions, 0,
+                                       B, n_kv, bs, MB, NB, err,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append_fp8 launch");
+  return ok();
+}
+
+pgd_status pgd_paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
+                                          const void *v_cache, const int32_t *block_tables,
+                                          const int32_t *context_lens, int32_t B, int32_t n_q,
+                                          int32_t n_kv, int32_t d, int32_t bs, int32_t MB,
+                                          int32_t NB, float scale, int32_t num_splits,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+  pgd_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, B,
+                                      n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  PreparedAttention pa;
+  s = prepare_attention(out, q, k_cache, v_cache, block_tables, context_lens, B, n_q, n_kv, bs, MB,
+                        NB, scale, num_splits, workspace, workspace_bytes, &pa, true);
+  if (s != PGD_OK) return s;
+  s = launch_prepared(pa, static_cast<cudaStream_t>(stream));
+  return s == PGD_OK ? ok() : s;
+}
+
+pgd_status pgd_append_decode_attention_fp8(void *out, const void *q, const void *k_new,
+                                           const void *v_new, void *k_cache, void *v_cache,
+                                           const int32_t *block_tables,
+                                           const int32_t *context_lens, int32_t B, int32_t n_q,
+                                           int32_t n_kv, int32_t d, int32_t bs, int32_t MB,
+                                           int32_t NB, float scale, int32_t num_splits,
+                                           void *workspace, size_t workspace_bytes,
+                                           void *stream) {
+  pgd_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, B,
+                                      n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  s = append_then_attend(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, B,
+                         n_q, n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream), true);
   return s == PGD_OK ? ok() : s;
 }
 

@@ -1,0 +1,1173 @@
+// attention_kernel.cuh -- paged GQA decode attention for sm_103a on the
+// fifth-generation tensor cores (tcgen05, accumulators in tensor memory),
+// for a bf16 cache and for an 8-bit (FP8 E4M3 + per-token scale) cache.
+// attention.cu and attention_fp8.cu instantiate it.
+//
+// What it computes ("Module 10: inference and serving", section "Attention
+// reads a different cache per sequence"; "The math of Transformer inference",
+// section 4): for every sequence b and query head h,
+//   out[b][h] = sum_t softmax_t(scale * q[b][h] . k_t) v_t over the
+//   context_lens[b] cached positions, K/V head h / G, read through the block
+//   table ("Module 10", section "Mapping logical positions to physical
+//   blocks").
+//
+// Work split.  A unit is one (sequence, KV head); its K/V tiles are read once
+// and serve all G query heads.  The units' blocks are laid end to end
+// (sequence-major, then KV head, then block) into one range of X blocks, cut
+// into one contiguous part per CTA in one of two ways, chosen by every CTA
+// alike from the context lengths:
+//   units     CTA c takes unit c whole (when there are no more units than
+//             CTAs and the longest unit still streams no longer than the
+//             whole job takes at the HBM rate): no partial states at all;
+//   balanced  CTA c of P takes blocks [X*c/P, X*(c+1)/P): every CTA streams
+//             the same bytes (+-1 block) whatever the length mix.
+// A CTA walks its part unit by unit ("segments").  A segment that covers a
+// whole unit writes the output; otherwise it writes its (max, sum, weighted
+// sum) state and the last CTA of the unit to arrive merges the states by
+// log-sum-exp ("The math of Transformer inference", section 8: split the
+// sequence, attend locally, merge by log-sum-exp; the running-state update is
+// the one in "LLM inference systems engineering", 2.8.3).  Arrival is an
+// atomic counter per unit; no CTA waits for another.
+//
+// The two contractions of a 128-token stage run on the tensor cores with
+// tokens on the M side (decode attention is HBM bound; on CUDA cores the
+// 2 * G * 128 multiply-adds per token and KV head took most issue slots):
+//   S^T[128 tok][16]  = K[128 tok][128 d]   . Q^T[128 d][16 heads]
+//   O^T[128 d][16]   += V^T[128 d][128 tok] . P^T[128 tok][16 heads]
+// N = 16 is the smallest N for M = 128; the G <= 8 real heads use the first
+// columns, the rest are zeros.
+//
+// Operands.  The pool stores every (block, KV head) tile as 8 x 8 core
+// matrices (row group of 8 tokens x 16 column chunks of 8 dims; element
+// (slot s, dim i) at ((s/8)*16 + i/8)*64 + (s%8)*8 + i%8).  One bulk copy per
+// tile therefore lands exactly in the tensor cores' no-swizzle layout, and
+// the tiles of a stage placed back to back form one operand with uniform
+// strides: K as the K-major A operand of q.k^T (8-row groups 2048 B apart,
+// 16-byte column chunks 128 B apart) and V as the MN-major A operand of p.v
+// (the same core matrices read the other way).  Q is written by threads as a
+// K-major, 128-byte-swizzled B operand and P as an MN-major B operand.
+//
+// Roles (384 threads, one CTA per SM):
+//   warps 0-3  softmax; thread t owns TMEM lane t (token row t of S)
+//   warp 4     K producer, warp 5 V producer: bulk copies on the TMA engine,
+//              one tile per lane, table entries prefetched 32 ahead; the K
+//              producer also writes each segment's Q
+//   warp 6     allocates tensor memory and issues q.k^T (one lane)
+//   warp 7     issues p.v (one lane); with two issuers the q.k^T of the next
+//              stages never queues behind the p.v of the current one
+//   warps 8-11 epilogue: per segment, read O from tensor memory and write the
+//              output or a partial state (and merge a unit's partials when
+//              they are complete), off the softmax warps' critical path
+// Rings: 3 K stages and 3 V stages of 32 KiB; a K stage is free as soon as
+// its q.k^T has completed, a V stage after its p.v.  S and P are double
+// buffered by stage parity, O and Q by segment parity.  Every wait is bounded.
+//
+// 8-bit cache ("Module 10", section "Quantize the cache, evaluate the final
+// artifact"; "The math of Transformer inference", section 11: KV in 8 bits
+// halves the bytes a step reads, scales per head and token, dequantisation
+// fused into the kernel).  A pool tile is (bs / 8) groups of 8 tokens, each
+// group the tokens' E4M3 codes as 8-row x 16-byte core matrices (1024 B)
+// followed by their 8 fp32 scales (32 B): one bulk copy per tile still lands
+// codes and scales, and the groups sit 1056 B apart -- a uniform stride the
+// MMA descriptors can step over.  q.k^T runs on the tensor cores in E4M3
+// (kind::f8f6f4): each query head h is split into a high and a low E4M3 part
+// (q / s_q = hi + lo, s_q = max |q| / 448), hi in column h and lo in column
+// 8 + h of the same N = 16 MMA, so the score keeps about 8 bits of the
+// query at no extra MMA; the softmax adds the two columns and applies s_q
+// and the key's scale.  V is converted to bf16 by the softmax threads (each
+// its own token row, exactly: every E4M3 value is a bf16 value) and the
+// token's V scale is folded into its probability before the bf16 p.v.
+//
+// Softmax keeps one reference maximum per head.  A stage moves the reference
+// (and rescales O in tensor memory, after the previous p.v has completed)
+// only when its maximum exceeds the reference by more than 8 in log2 units,
+// so P <= 256 in bf16 and rescaling is rare; O and l share the reference, so
+// the final division is exact up to rounding.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <math.h>
+
+#include "pgd_device.cuh"
+
+namespace pgd {
+namespace tc {
+
+constexpr int TOK = 128;                    // tokens per stage (MMA M of q.k^T)
+constexpr int NPAD = 16;                    // MMA N: heads padded to 16
+constexpr int P_BYTES = TOK * NPAD * 2;     // [16 token groups][2 head groups][8][16 B]
+constexpr int THREADS = 384;
+constexpr int WARP_KP = 4, WARP_VP = 5, WARP_QK = 6, WARP_PV = 7, WARP_EPI = 8;
+constexpr uint32_t TMEM_COLS = 64;
+constexpr float kRescaleLog2 = 8.f;         // move the reference when exceeded by 2^8
+// Split choice.  One CTA streams at most about 1/kCtaShare of the HBM rate
+// (its three 64 KiB K+V stages in flight over the load latency); a unit's
+// partial state costs the CTA that merges it about kMergeBytes of streaming
+// time (a store, a fence, an atomic and the reloads of the parts, in series).
+// (per kind of cache: three 64 KiB bf16 stages, or four 33 KiB 8-bit ones)
+template <bool FP8> constexpr long long kCtaShare = FP8 ? 140 : 96;
+constexpr long long kMergeBytes = 32ll << 20;
+constexpr int MERGE_PAIRS = 128;
+constexpr int SMEM_SLACK = 1024;
+
+// Shared memory of one CTA (offsets from a 1024-byte aligned base).
+template <bool FP8>
+struct Lay {
+  static constexpr int GROUP = FP8 ? 8 * 128 + 32 : 8 * 256;  // bytes per 8-token group
+  static constexpr int STAGE = (TOK / 8) * GROUP;              // K (or V) bytes of a stage
+  static constexpr int NSK = FP8 ? 4 : 3, NSV = FP8 ? 4 : 3;   // ring depths
+  // Q operand per buffer: bf16 [half][16 rows][128 B] with 128-byte swizzle,
+  // or E4M3 [16 rows][128 B] as 8 x 16-byte core matrices
+  static constexpr int Q_BYTES = FP8 ? NPAD * 128 : 2 * NPAD * 128;
+  static constexpr int VB_BYTES = FP8 ? 2 * TOK * 256 : 0;     // converted V, by stage parity
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + NSK * STAGE;
+  static constexpr int OFF_VB = OFF_V + NSV * STAGE;
+  static constexpr int OFF_Q = OFF_VB + VB_BYTES;  // Q double buffered by segment parity
+  static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_RED = OFF_BAR + 512;    // f32 [2][4][8] warp maxima
+  static constexpr int OFF_LRED = OFF_RED + 256;   // f32 [2][4][8] warp sums per segment parity
+  static constexpr int OFF_MREF = OFF_LRED + 256;  // f32 [2][8] reference maxima per segment parity
+  static constexpr int OFF_QS = OFF_MREF + 64;     // f32 [2][8] Q scales per Q buffer (8-bit)
+  static constexpr int OFF_MERGE = OFF_QS + 64;    // float2 [MERGE_PAIRS] partial (max, sum)
+  static constexpr int OFF_MISC = OFF_MERGE + MERGE_PAIRS * 8;  // tmem base, flags, masks
+  static constexpr int OFF_PRE = OFF_MISC + 128;   // int [B + 1]
+};
+
+template <bool FP8>
+__host__ __device__ constexpr size_t smem_bytes(int B) {
+  return (size_t)SMEM_SLACK + Lay<FP8>::OFF_PRE + (size_t)(B + 1) * 4;
+}
+static_assert(smem_bytes<false>(PGD_MAX_BATCH) <= 232448, "bf16 layout exceeds 227 KB");
+static_assert(smem_bytes<true>(PGD_MAX_BATCH) <= 232448, "8-bit layout exceeds 227 KB");
+
+__device__ __forceinline__ uint32_t col_s(int sb) { return (uint32_t)sb * 16u; }
+__device__ __forceinline__ uint32_t col_o(int ob) { return 32u + (uint32_t)ob * 16u; }
+
+// ---------------------------------------------------------------- PTX helpers
+// Shared-memory matrix descriptor (tcgen05): start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, layout
+// (0 = no swizzle, 2 = 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
+}
+
+// Instruction descriptor, kind::f16: D f32, A and B bf16, M = 128, N = 16;
+// a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t instr_desc(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(NPAD >> 3) << 17) | ((uint32_t)(TOK >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::f8f6f4: D f32, A and B E4M3 (format 0),
+// both K-major, M = 128, N = 16.
+__host__ __device__ constexpr uint32_t instr_desc_e4m3() {
+  return (1u << 4) | ((uint32_t)(NPAD >> 3) << 17) | ((uint32_t)(TOK >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every MMA issued so far by this thread has completed.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Generic-proxy shared-memory writes become visible to the tensor cores.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 8 consecutive fp32 columns of this warp's 32 TMEM lanes (wait included).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r0, r1, r2, r3, r4, r5, r6, r7;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5), "=r"(r6), "=r"(r7)
+      : "r"(taddr)
+      : "memory");
+  v[0] = __uint_as_float(r0); v[1] = __uint_as_float(r1);
+  v[2] = __uint_as_float(r2); v[3] = __uint_as_float(r3);
+  v[4] = __uint_as_float(r4); v[5] = __uint_as_float(r5);
+  v[6] = __uint_as_float(r6); v[7] = __uint_as_float(r7);
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+      : "memory");
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
+  return v;
+}
+
+// Bounded wait that gives up at once after any earlier timeout in the CTA, so
+// that the control flow (and every named barrier) is the same for all threads
+// whatever happens.
+__device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort_flag, int32_t *err) {
+  if (*abort_flag) return;
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 31u) == 0) {
+      if (*abort_flag) return;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(err, PGD_DEVERR_TIMEOUT);
+        return;
+      }
+    }
+  }
+}
+
+struct Segment {
+  int b, g, j0, nblk, n;
+  long long unit_start, unit_end;
+};
+
+__device__ __forceinline__ Segment locate(const int *pre, int B, int n_kv, long long x,
+                                          long long x_end) {
+  int lo = 0, hi = B - 1;  // largest b with n_kv * pre[b] <= x
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)n_kv * pre[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  Segment s;
+  s.b = lo;
+  s.nblk = pre[lo + 1] - pre[lo];
+  const long long base = (long long)n_kv * pre[lo];
+  const long long r = x - base;
+  s.g = (int)(r / s.nblk);
+  s.j0 = (int)(r % s.nblk);
+  s.unit_start = base + (long long)s.g * s.nblk;
+  s.unit_end = s.unit_start + s.nblk;
+  const long long e = x_end < s.unit_end ? x_end : s.unit_end;
+  s.n = (int)(e - x);
+  return s;
+}
+
+// Parts of one call: part c (taken by CTA c) is a contiguous range of the
+// flattened block space, in index order; a closed form of c, so every thread
+// can map a part to its range and a block position to its part.
+struct Schedule {
+  long long X;     // blocks in all units
+  long long P;     // parts
+  bool units;      // part c = unit c (else X * c / P balanced cuts)
+  const int *pre;  // blocks before sequence b
+  int n_kv;
+  __device__ __forceinline__ void range(long long i, long long &a, long long &b) const {
+    if (units) {
+      const int sb = (int)(i / n_kv), g = (int)(i % n_kv);
+      const long long nb = pre[sb + 1] - pre[sb];
+      a = (long long)n_kv * pre[sb] + g * nb;
+      b = a + nb;
+    } else {
+      a = X * i / P;
+      b = X * (i + 1) / P;
+    }
+  }
+  // Part holding block position x (only needed for units that are cut,
+  // which happens in balanced mode alone).
+  __device__ __forceinline__ long long part_of(long long x) const {
+    return (P * (x + 1) - 1) / X;
+  }
+};
+
+// A role's walk over the CTA's part, one segment (the piece of the part
+// inside one unit) at a time.  Every role walks the same segments.
+struct SegCursor {
+  long long x, b;  // rest of the part
+  __device__ __forceinline__ SegCursor(const Schedule &sc) {
+    x = b = 0;
+    if ((long long)blockIdx.x < sc.P) sc.range(blockIdx.x, x, b);
+  }
+  __device__ __forceinline__ bool next(const Schedule &sc, int B, Segment &sg) {
+    if (x >= b) return false;
+    sg = locate(sc.pre, B, sc.n_kv, x, b);
+    x += sg.n;
+    return true;
+  }
+};
+
+// E4M3 pair from two binary32 values (round to nearest even, saturating to
+// +-448; x.x in the low byte) and back to binary32.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+  const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3));
+  return __half22float2(h);
+}
+
+// 16 E4M3 codes -> 16 bf16 (two 16-byte rows of 8), exactly: every E4M3
+// value is a half and a bf16 value; the bf16 is the upper half of the
+// binary32 widening.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 &c, uint4 &lo, uint4 &hi) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = e4m3x2_to_float2((uint16_t)(w[i] & 0xFFFFu));
+    const float2 b = e4m3x2_to_float2((uint16_t)(w[i] >> 16));
+    o[2 * i] = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
+    o[2 * i + 1] = __byte_perm(__float_as_uint(b.x), __float_as_uint(b.y), 0x7632);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// One query head's 8 dims (one 16-byte piece of q) as E4M3 high and low
+// parts of q / s_q: hi = E4M3(x), lo = E4M3(x - hi).
+__device__ __forceinline__ void q_hi_lo(const uint4 &piece, float inv_sq, uint2 &hi, uint2 &lo) {
+  float f[8];
+  unpack8(piece, f);
+  uint16_t h[4], l[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float x0 = f[2 * j] * inv_sq, x1 = f[2 * j + 1] * inv_sq;
+    h[j] = e4m3x2(x0, x1);
+    const float2 hv = e4m3x2_to_float2(h[j]);
+    l[j] = e4m3x2(x0 - hv.x, x1 - hv.y);
+  }
+  hi = make_uint2(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16));
+  lo = make_uint2(l[0] | ((uint32_t)l[1] << 16), l[2] | ((uint32_t)l[3] << 16));
+}
+
+// One producer warp (K or V): walks the CTA's stages and copies one tile per
+// lane with the TMA engine.  The K producer also records which blocks of a
+// stage had an invalid id and writes each segment's Q (the B operand of
+// q.k^T) into buffer k & 1 as segment k starts: bf16 K-major with 128-byte
+// swizzle (row = head, two 64-column halves), or for the 8-bit cache E4M3
+// high parts in rows 0-7 and low parts in rows 8-15 (8 x 16-byte core
+// matrices) plus one scale per head.  Loads run one step ahead: the next
+// segment's Q and first 64 block ids while the current segment streams, and
+// within a segment the block ids 32 entries ahead.
+template <int G, int BS, bool FP8, bool IS_K>
+__device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
+                                        const unsigned char *cache, unsigned char *ring,
+                                        uint64_t *full, uint64_t *empty,
+                                        volatile int *stage_mask, unsigned char *qbuf,
+                                        float *qscale, uint64_t *q_ready, uint64_t *q_free,
+                                        volatile int *abort_flag, int lane) {
+  using L = Lay<FP8>;
+  constexpr int SB = TOK / BS;                         // blocks per stage
+  constexpr uint32_t TILE_BYTES = (BS / 8) * L::GROUP;  // one (block, head) tile
+  constexpr int NS = IS_K ? L::NSK : L::NSV;
+  constexpr int QPL = (16 * G + 31) / 32;  // Q 16-byte pieces per lane
+  const uint64_t policy = l2_policy_evict_first();
+
+  struct Ahead {
+    uint4 q[QPL];
+    int tab, tab_next;
+  };
+  auto load_ahead = [&](const Segment &g, Ahead &a) {
+    if (IS_K) {
+#pragma unroll
+      for (int i = 0; i < QPL; ++i) {
+        const int j = lane + 32 * i, r = j >> 4, c = j & 15;
+        a.q[i] = (j < 16 * G) ? __ldg(reinterpret_cast<const uint4 *>(
+                                    p.q + ((size_t)g.b * p.n_q + (size_t)g.g * G + r) * kHeadDim +
+                                    c * 8))
+                              : make_uint4(0, 0, 0, 0);
+      }
+    }
+    const int32_t *trow = p.tables + (size_t)g.b * p.MB + g.j0;
+    a.tab = (lane < g.n) ? __ldg(trow + lane) : 0;
+    a.tab_next = (32 + lane < g.n) ? __ldg(trow + 32 + lane) : 0;
+  };
+
+  SegCursor cur(sc);
+  Segment sg, nsg;
+  Ahead cur_a{}, next_a{};
+  bool have = cur.next(sc, p.B, sg);
+  if (have) load_ahead(sg, cur_a);
+  if (p.wait_late) pdl_wait();  // kv_append has written the caches
+  int s = 0, k = 0;
+  while (have) {
+    const bool have_next = cur.next(sc, p.B, nsg);
+    if (have_next) load_ahead(nsg, next_a);
+    if (IS_K) {
+      const int qb = k & 1;
+      if (lane == 0)
+        wait_or_abort(&q_free[qb], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
+      __syncwarp();
+      unsigned char *qdst = qbuf + qb * L::Q_BYTES;
+      if constexpr (FP8) {
+        // Lanes 16h'..16h'+15 of piece i hold head r = 2i + h': the head's
+        // max |q| is a reduction over those 16 lanes.
+#pragma unroll
+        for (int i = 0; i < QPL; ++i) {
+          const int j = lane + 32 * i, r = j >> 4, c = j & 15;
+          float f[8];
+          unpack8(cur_a.q[i], f);
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFullMask, a, o));
+          const float sq = a > 0.f ? a * (1.f / 448.f) : 1.f;
+          if (j < 16 * G) {
+            uint2 hi, lo;
+            q_hi_lo(cur_a.q[i], 1.f / sq, hi, lo);
+            // row n, dims 8c..8c+7: core matrix (n / 8, c / 2), row n % 8
+            const int off = (c >> 1) * 128 + (c & 1) * 8;
+            *reinterpret_cast<uint2 *>(qdst + r * 16 + off) = hi;
+            *reinterpret_cast<uint2 *>(qdst + 8 * 128 + r * 16 + off) = lo;
+            if (c == 0) qscale[qb * 8 + r] = sq;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < QPL; ++i) {
+          const int j = lane + 32 * i, r = j >> 4, c = j & 15, half = c >> 3, cc = c & 7;
+          if (j < 16 * G)
+            *reinterpret_cast<uint4 *>(qdst + half * (NPAD * 128) + r * 128 +
+                                       ((cc ^ (r & 7)) << 4)) = cur_a.q[i];
+        }
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_ready[qb]);
+    }
+    ++k;
+    const int32_t *trow = p.tables + (size_t)sg.b * p.MB + sg.j0;
+    int tab = cur_a.tab, tab_next = cur_a.tab_next;
+    int tchunk = 0;
+    const int nstages = (sg.n + SB - 1) / SB;
+    for (int st = 0; st < nstages; ++st, ++s) {
+      const int first = st * SB;
+      if ((first >> 5) != tchunk) {  // next 32 table entries; prefetch the ones after
+        tchunk = first >> 5;
+        tab = tab_next;
+        const int j = (tchunk + 1) * 32 + lane;
+        tab_next = (j < sg.n) ? __ldg(trow + j) : 0;
+      }
+      const int nb = min(SB, sg.n - first);
+      const int blk = __shfl_sync(kFullMask, tab, (first & 31) + (lane & (SB - 1)));
+      const bool ok = lane < nb && (unsigned)blk < (unsigned)p.NB;
+      const unsigned okmask = __ballot_sync(kFullMask, ok);
+      const unsigned want = (1u << nb) - 1u;
+      const int slot = s % NS;
+      if (lane == 0) {
+        wait_or_abort(&empty[slot], ((uint32_t)(s / NS) & 1u) ^ 1u, abort_flag, p.err);
+        if (IS_K) {
+          stage_mask[s & 7] = (int)(want & ~okmask);
+          if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
+        }
+        const uint32_t bytes = (uint32_t)__popc(okmask) * TILE_BYTES;
+        if (*abort_flag || bytes == 0)
+          mbar_arrive(&full[slot]);
+        else
+          mbar_arrive_expect_tx(&full[slot], bytes);
+      }
+      __syncwarp();
+      if (ok && !*abort_flag) {
+        const unsigned char *src = cache + ((size_t)blk * p.n_kv + sg.g) * (size_t)TILE_BYTES;
+        bulk_copy_g2s(ring + (size_t)slot * L::STAGE + (size_t)lane * TILE_BYTES, src,
+                      TILE_BYTES, &full[slot], policy);
+      }
+    }
+    sg = nsg;
+    cur_a = next_a;
+    have = have_next;
+  }
+  // no copy may still be landing when the CTA exits
+  if (lane == 0) {
+    for (int k = 1; k <= NS && k <= s; ++k) {
+      const int last = s - k;
+      mbar_wait_bounded(&full[last % NS], (uint32_t)(last / NS) & 1u);
+    }
+  }
+}
+
+template <int G, int BS, bool FP8>
+__global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnParams p) {
+  using L = Lay<FP8>;
+  constexpr int SB = TOK / BS;
+  constexpr uint32_t IDESC_QK = instr_desc(false, false);
+  constexpr uint32_t IDESC_QK8 = instr_desc_e4m3();
+  constexpr uint32_t IDESC_PV = instr_desc(true, true);
+  static_assert(G >= 1 && G <= 8 && TOK % BS == 0 && BS % 8 == 0 && SB <= 32, "shape");
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::OFF_BAR);
+  uint64_t *full_k = bars;                 // [NSK]
+  uint64_t *empty_k = full_k + L::NSK;     // [NSK]
+  uint64_t *full_v = empty_k + L::NSK;     // [NSV]
+  uint64_t *empty_v = full_v + L::NSV;     // [NSV]
+  uint64_t *s_full = empty_v + L::NSV;     // [2]
+  uint64_t *s_free = s_full + 2;        // [2]
+  uint64_t *p_full = s_free + 2;        // [2]
+  uint64_t *p_free = p_full + 2;        // [2]
+  uint64_t *o_full = p_free + 2;        // [2]
+  uint64_t *o_free = o_full + 2;        // [2]
+  uint64_t *m_ready = o_free + 2;       // [2]
+  uint64_t *q_ready = m_ready + 2;      // [2] per Q buffer
+  uint64_t *q_free = q_ready + 2;       // [2] per Q buffer
+  uint64_t *done = q_free + 2;          // [2] one per MMA issuer
+  uint64_t *seg_done = done + 2;        // [2] softmax -> epilogue, per segment parity
+  float *red = reinterpret_cast<float *>(smem + L::OFF_RED);
+  float *lred = reinterpret_cast<float *>(smem + L::OFF_LRED);
+  float *mref = reinterpret_cast<float *>(smem + L::OFF_MREF);
+  float *qscale = reinterpret_cast<float *>(smem + L::OFF_QS);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+  volatile int *flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 8);         // [3]
+  int *nmax_slot = reinterpret_cast<int *>(smem + L::OFF_MISC + 20);
+  volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 40);  // [8]
+  int *pre = reinterpret_cast<int *>(smem + L::OFF_PRE);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Launched with programmatic stream serialization: the previous kernel of
+  // the stream may still run.  Unless it is known to write only the caches,
+  // wait for it before reading anything.
+  if (!p.wait_late) pdl_wait();
+
+  if (tid == 0) {
+    // 8-bit cache: the softmax warps read each K stage's scales and convert
+    // each V stage themselves, so they too release K and V slots, and they
+    // release a Q buffer once they hold its scales.
+    for (int i = 0; i < L::NSK; ++i) {
+      mbar_init(&full_k[i], 1);
+      mbar_init(&empty_k[i], FP8 ? 1 + 4 : 1);
+    }
+    for (int i = 0; i < L::NSV; ++i) {
+      mbar_init(&full_v[i], 1);
+      mbar_init(&empty_v[i], FP8 ? 4 : 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&p_free[i], 1);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_free[i], 4);
+      mbar_init(&m_ready[i], 1);
+      mbar_init(&done[i], 1);
+      mbar_init(&seg_done[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_ready[i], 1);
+      mbar_init(&q_free[i], FP8 ? 1 + 4 : 1);
+    }
+    mbar_init_fence();
+    *abort_flag = 0;
+  }
+  // Q pad rows and P pad columns stay zero for the whole kernel.
+  {
+    uint4 *z = reinterpret_cast<uint4 *>(smem + L::OFF_Q);
+    for (int i = tid; i < (2 * L::Q_BYTES + 2 * P_BYTES) / 16; i += THREADS) z[i] = make_uint4(0, 0, 0, 0);
+  }
+  // Blocks per sequence, then an exclusive prefix over the batch.
+  const int max_tokens = p.MB * BS;
+  bool bad_ctx = false;
+  for (int b = tid; b < p.B; b += THREADS) {
+    const int c = p.ctx[b];
+    int nb = 0;
+    if (c >= 1 && c <= max_tokens) nb = (c + BS - 1) / BS; else bad_ctx = true;
+    pre[b + 1] = nb;
+  }
+  if (bad_ctx && blockIdx.x == 0) atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
+  if (warp == WARP_QK) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_proxy_async();
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0, longest = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int i = base + lane;
+      int v = (i < p.B) ? pre[i + 1] : 0;
+      longest = max(longest, v);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(kFullMask, v, o);
+        if (lane >= o) v += n;
+      }
+      if (i < p.B) pre[i + 1] = v + carry;
+      carry += __shfl_sync(kFullMask, v, 31);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) longest = max(longest, __shfl_xor_sync(kFullMask, longest, o));
+    if (lane == 0) {
+      pre[0] = 0;
+      *nmax_slot = longest;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  Schedule sc;
+  sc.X = (long long)p.n_kv * pre[p.B];
+  sc.pre = pre;
+  sc.n_kv = p.n_kv;
+  sc.P = sc.X < (long long)gridDim.x ? sc.X : (long long)gridDim.x;
+  sc.units = false;
+  if (p.auto_split) {
+    // Whole units when they fit in the grid and the longest one streams no
+    // longer than the job at the HBM rate plus the merges the balanced cut
+    // would need; the cost of either is in blocks of HBM streaming time.
+    const long long U = (long long)p.B * p.n_kv, nmax = *nmax_slot;
+    if (U <= (long long)gridDim.x && sc.X > 0) {
+      const long long per_cta = (sc.X + gridDim.x - 1) / gridDim.x;
+      constexpr long long kBlockBytes = 2ll * (BS / 8) * L::GROUP;  // K and V of one block
+      const long long cost_units = max(nmax * kCtaShare<FP8>, sc.X);
+      const long long cost_cut = max(per_cta * kCtaShare<FP8>, sc.X) + kMergeBytes / kBlockBytes;
+      if (cost_units <= cost_cut) {
+        sc.units = true;
+        sc.P = U;
+      }
+    }
+  }
+
+  if (warp == WARP_KP) {
+    produce<G, BS, FP8, true>(p, sc, p.k_cache, smem + L::OFF_K, full_k, empty_k, stage_mask,
+                              smem + L::OFF_Q, qscale, q_ready, q_free, abort_flag, lane);
+  } else if (warp == WARP_VP) {
+    produce<G, BS, FP8, false>(p, sc, p.v_cache, smem + L::OFF_V, full_v, empty_v, nullptr,
+                               nullptr, nullptr, nullptr, nullptr, abort_flag, lane);
+  } else if (warp == WARP_QK) {
+    // ---------------------------------------------------- q.k^T issuer
+    if (lane == 0) {
+      const uint32_t q_base = smem_addr(smem + L::OFF_Q);
+      SegCursor cur(sc);
+      Segment sg;
+      int s = 0, k = 0;
+      while (cur.next(sc, p.B, sg)) {
+        const int nstages = (sg.n + SB - 1) / SB;
+        // Q of segment k is in buffer k & 1 (written by the K producer); it is
+        // rewritten for segment k + 2 only after q_free signals that every
+        // q.k^T of segment k has completed.
+        wait_or_abort(&q_ready[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
+        const uint32_t q_seg = q_base + (uint32_t)((k & 1) * L::Q_BYTES);
+        for (int st = 0; st < nstages; ++st, ++s) {
+          const int slot = s % L::NSK, sb = s & 1;
+          wait_or_abort(&full_k[slot], (uint32_t)(s / L::NSK) & 1u, abort_flag, p.err);
+          wait_or_abort(&s_free[sb], ((uint32_t)(s >> 1) & 1u) ^ 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (!*abort_flag) {
+            const uint32_t dS = tmem + col_s(sb);
+            const uint32_t k_st = smem_addr(smem + L::OFF_K + slot * L::STAGE);
+            if constexpr (FP8) {
+              // E4M3, K = 32 per MMA: K core matrices 128 B apart along d,
+              // token groups 1056 B apart; Q rows 8 apart at 1024 B.  A k-step
+              // moves both by two core matrices (256 B).
+              const uint64_t kd = smem_desc(k_st, 128, L::GROUP, 0);
+              const uint64_t qd = smem_desc(q_seg, 128, 1024, 0);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                umma_e4m3(dS, kd + (uint64_t)(kk * 16), qd + (uint64_t)(kk * 16), IDESC_QK8,
+                          kk > 0 ? 1u : 0u);
+            } else {
+              // Descriptors are built once; a k-step only moves the start
+              // address (the low field, in 16-byte units): K by 256 B, Q by
+              // 32 B within a 128-byte swizzle row and by 2048 B to the second
+              // half.
+              const uint64_t kd = smem_desc(k_st, 128, 2048, 0);
+              const uint64_t qd = smem_desc(q_seg, 16, 1024, 2);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                umma_bf16(dS, kd + (uint64_t)(kk * 16),
+                          qd + (uint64_t)((kk >> 2) * 128 + (kk & 3) * 2), IDESC_QK,
+                          kk > 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&s_full[sb]);
+          umma_commit(&empty_k[slot]);
+          // Hand the stage's invalid-block mask (written by the K producer
+          // before it armed full_k, which this thread acquired) to the softmax.
+          mbar_arrive(&m_ready[sb]);
+        }
+        umma_commit(&q_free[k & 1]);  // Q buffer reusable once these q.k^T complete
+        ++k;
+      }
+      // every MMA has completed before tensor memory is released
+      if (s > 0) {
+        umma_commit(&done[0]);
+        mbar_wait_bounded(&done[0], 0);
+      }
+    }
+  } else if (warp == WARP_PV) {
+    // ------------------------------------------------------- p.v issuer
+    if (lane == 0) {
+      SegCursor cur(sc);
+      Segment sg;
+      int s = 0, k = 0;
+      while (cur.next(sc, p.B, sg)) {
+        const int nstages = (sg.n + SB - 1) / SB;
+        const int ob = k & 1;
+        for (int st = 0; st < nstages; ++st, ++s) {
+          const int slot = s % L::NSV, sb = s & 1;
+          wait_or_abort(&p_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+          // (8-bit cache: p_full also means the softmax has converted this
+          // stage's V into the bf16 buffer of parity sb)
+          if (!FP8) wait_or_abort(&full_v[slot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
+          if (st == 0)
+            wait_or_abort(&o_free[ob], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (!*abort_flag) {
+            // 16 tokens per k-step: V moves by 4096 B, P by 512 B.
+            const uint64_t vd = smem_desc(
+                smem_addr(smem + (FP8 ? L::OFF_VB + sb * (TOK * 256) : L::OFF_V + slot * L::STAGE)),
+                2048, 128, 0);
+            const uint64_t pd = smem_desc(smem_addr(smem + L::OFF_P + sb * P_BYTES), 256, 128, 0);
+            const uint32_t dO = tmem + col_o(ob);
+            const uint32_t acc0 = st > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt)
+              umma_bf16(dO, vd + (uint64_t)(kt * 256), pd + (uint64_t)(kt * 32), IDESC_PV,
+                        kt > 0 ? 1u : acc0);
+          }
+          if (!FP8) umma_commit(&empty_v[slot]);
+          umma_commit(&p_free[sb]);  // P (and converted V) of parity sb reusable
+          if (st + 1 == nstages) umma_commit(&o_full[ob]);
+        }
+        ++k;
+      }
+      if (s > 0) {
+        umma_commit(&done[1]);
+        mbar_wait_bounded(&done[1], 0);
+      }
+    }
+  } else if (warp < 4) {
+    // ----------------------------------------------------------- softmax
+    const int t = tid;  // 0..127: token row of S
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    constexpr int NCT = 128;
+    SegCursor cur(sc);
+    Segment sg;
+    int s = 0, k = 0;
+    while (cur.next(sc, p.B, sg)) {
+      const int ctx_b = __ldg(p.ctx + sg.b);
+      const int nstages = (sg.n + SB - 1) / SB;
+      const int ob = k & 1;
+      float m_ref[G], l_part[G];
+      float qsc[G];  // 8-bit cache: Q scale of each head times scale * log2(e)
+#pragma unroll
+      for (int h = 0; h < G; ++h) { m_ref[h] = -INFINITY; l_part[h] = 0.f; qsc[h] = 0.f; }
+
+      for (int st = 0; st < nstages; ++st, ++s) {
+        const int vslot = s % L::NSV, sb = s & 1;
+        const int nb = min(SB, sg.n - st * SB);
+        const int jfirst = sg.j0 + st * SB;
+        int nvalid = nb * BS;
+        if (jfirst + nb == sg.nblk) nvalid -= sg.nblk * BS - ctx_b;  // unit's last block
+
+        wait_or_abort(&s_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+        // Invalid-block mask of this stage: the K producer wrote it before
+        // arming full_k; the q.k^T issuer acquired full_k and then released
+        // m_ready.  (Waiting on full_k here could alias: a K stage is freed
+        // after its q.k^T, so full_k may run two phases ahead.)  m_ready and
+        // the 8-entry mask ring cannot move on before this stage frees its S
+        // buffer.
+        wait_or_abort(&m_ready[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+        const int mask = stage_mask[s & 7];
+        tc_fence_after();
+        float sv[FP8 ? 16 : 8];
+        tmem_ld8(tmem + lane_base + col_s(sb), *reinterpret_cast<float(*)[8]>(sv));
+        if constexpr (FP8)
+          tmem_ld8(tmem + lane_base + col_s(sb) + 8, *reinterpret_cast<float(*)[8]>(sv + 8));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
+
+        const bool valid = (t < nvalid) && !((mask >> (t / BS)) & 1);
+        float sc_[G];
+        if constexpr (FP8) {
+          // Key scale of this token (the K slot is refilled only after these
+          // four warps release it, so waiting on full_k cannot alias), and at
+          // a segment's first stage the Q scales (the K producer wrote them
+          // before q_ready, which the q.k^T issuer acquired before m_ready).
+          const int kslot = s % L::NSK;
+          wait_or_abort(&full_k[kslot], (uint32_t)(s / L::NSK) & 1u, abort_flag, p.err);
+          const float ks = *reinterpret_cast<const float *>(
+              smem + L::OFF_K + kslot * L::STAGE + (t >> 3) * L::GROUP + 1024 + (t & 7) * 4);
+          if (st == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) qsc[h] = qscale[(k & 1) * 8 + h] * p.qk_scale_log2;
+          }
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&empty_k[kslot]);
+            if (st == 0) mbar_arrive(&q_free[k & 1]);
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h) sc_[h] = valid ? (sv[h] + sv[8 + h]) * (qsc[h] * ks) : -INFINITY;
+        } else {
+#pragma unroll
+          for (int h = 0; h < G; ++h) sc_[h] = valid ? sv[h] * p.qk_scale_log2 : -INFINITY;
+        }
+
+        // tile maximum per head across the 128 rows
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float wm = warp_max(sc_[h]);
+          if (lane == 0) red[(sb * 4 + warp) * 8 + h] = wm;
+        }
+        named_barrier_sync(1, NCT);
+        bool need = false;
+        float tmax[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          tmax[h] = fmaxf(fmaxf(red[(sb * 4 + 0) * 8 + h], red[(sb * 4 + 1) * 8 + h]),
+                          fmaxf(red[(sb * 4 + 2) * 8 + h], red[(sb * 4 + 3) * 8 + h]));
+          need |= tmax[h] > m_ref[h] + kRescaleLog2;
+        }
+        if (need) {
+          float alpha[8];
+#pragma unroll
+          for (int h = 0; h < 8; ++h) alpha[h] = 1.f;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float mn = fmaxf(m_ref[h], tmax[h]);
+            alpha[h] = (m_ref[h] == -INFINITY) ? 0.f : exp2f(m_ref[h] - mn);
+            m_ref[h] = mn;
+            l_part[h] *= alpha[h];
+          }
+          if (st > 0) {
+            // rescale O in tensor memory once the previous p.v has completed
+            wait_or_abort(&p_free[(s - 1) & 1], (uint32_t)((s - 1) >> 1) & 1u, abort_flag, p.err);
+            tc_fence_after();
+            float ov[8];
+            tmem_ld8(tmem + lane_base + col_o(ob), ov);
+#pragma unroll
+            for (int h = 0; h < 8; ++h) ov[h] *= alpha[h];
+            tmem_st8(tmem + lane_base + col_o(ob), ov);
+            tc_fence_before();
+          }
+        }
+        // probabilities, rounded to bf16 as the tensor cores will see them
+        // (8-bit cache: times the token's V scale; the sum takes them unscaled)
+        uint32_t packed[4] = {0, 0, 0, 0};
+        const unsigned char *vst = smem + L::OFF_V + vslot * L::STAGE;
+        float vscale = 1.f;
+        if constexpr (FP8) {
+          wait_or_abort(&full_v[vslot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
+          vscale = *reinterpret_cast<const float *>(vst + (t >> 3) * L::GROUP + 1024 + (t & 7) * 4);
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float pv = valid ? exp2f(sc_[h] - m_ref[h]) : 0.f;
+          __nv_bfloat16 pb;
+          if constexpr (FP8) {
+            pb = __float2bfloat16_rn(valid ? pv * vscale : 0.f);
+            l_part[h] += pv;
+          } else {
+            pb = __float2bfloat16_rn(pv);
+            l_part[h] += __bfloat162float(pb);
+          }
+          packed[h >> 1] |= (uint32_t)__bfloat16_as_ushort(pb) << ((h & 1) * 16);
+        }
+        wait_or_abort(&p_free[sb], ((uint32_t)(s >> 1) & 1u) ^ 1u, abort_flag, p.err);
+        *reinterpret_cast<uint4 *>(smem + L::OFF_P + sb * P_BYTES + (t >> 3) * 256 + (t & 7) * 16) =
+            make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        if constexpr (FP8) {
+          // this token's V row, E4M3 -> bf16, into the operand of parity sb
+          // (free: p_free says the p.v that last read it has completed); rows
+          // that are not valid tokens become zeros
+          const unsigned char *src = vst + (t >> 3) * L::GROUP + (t & 7) * 16;
+          unsigned char *dst = smem + L::OFF_VB + sb * (TOK * 256) + (t >> 3) * 2048 + (t & 7) * 16;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+            if (valid) e4m3x16_to_bf16(*reinterpret_cast<const uint4 *>(src + c * 128), lo, hi);
+            *reinterpret_cast<uint4 *>(dst + (2 * c) * 128) = lo;
+            *reinterpret_cast<uint4 *>(dst + (2 * c + 1) * 128) = hi;
+          }
+        } else if (nvalid < TOK || mask) {
+          // rows that are not valid tokens must not feed NaN/Inf into p.v
+          wait_or_abort(&full_v[vslot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
+          if (!valid) {
+            uint4 *vrow = reinterpret_cast<uint4 *>(smem + L::OFF_V + vslot * L::STAGE +
+                                                    (t >> 3) * 2048 + (t & 7) * 16);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) vrow[c * 8] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (FP8) mbar_arrive(&empty_v[vslot]);
+          mbar_arrive(&p_full[sb]);
+        }
+      }
+
+      // ---- end of segment: hand the segment's reference maxima and per-warp
+      // sums to the epilogue warps.
+      // lred/mref[ob] were last read by the epilogue of segment k - 2, which
+      // then released O buffer ob
+      wait_or_abort(&o_free[ob], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float ws = warp_sum(l_part[h]);
+        if (lane == 0) lred[(ob * 4 + warp) * 8 + h] = ws;
+        if (t == 0) mref[ob * 8 + h] = m_ref[h];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&seg_done[ob]);
+      ++k;
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int e = tid - 32 * WARP_EPI;  // 0..127: head-dim row of O
+    const int ew = warp - WARP_EPI;     // TMEM lane quadrant
+    const uint32_t lane_base = (uint32_t)(ew * 32) << 16;
+    constexpr int NET = 128;
+    SegCursor cur(sc);
+    Segment sg;
+    const int part = (int)blockIdx.x;
+    int k = 0;
+    while (cur.next(sc, p.B, sg)) {
+      const int ob = k & 1;
+      const int unit = sg.b * p.n_kv + sg.g;
+      wait_or_abort(&seg_done[ob], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
+      float Lsum[G], M[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        Lsum[h] = (lred[(ob * 4 + 0) * 8 + h] + lred[(ob * 4 + 1) * 8 + h]) +
+               (lred[(ob * 4 + 2) * 8 + h] + lred[(ob * 4 + 3) * 8 + h]);
+        M[h] = mref[ob * 8 + h];
+      }
+      wait_or_abort(&o_full[ob], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
+      tc_fence_after();
+      float ov[8];
+      tmem_ld8(tmem + lane_base + col_o(ob), ov);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[ob]);
+
+      const long long seg_start = sg.unit_start + sg.j0;
+      const bool whole = (seg_start == sg.unit_start) && (seg_start + sg.n == sg.unit_end);
+      const size_t out_row = (size_t)sg.b * p.n_q + (size_t)sg.g * G;
+      if (whole) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(ov[h] / Lsum[h]);
+      } else {
+        const size_t srow = ((size_t)unit + (size_t)part) * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) p.part_o[(srow + h) * kHeadDim + e] = ov[h];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          if (e == h)
+            *reinterpret_cast<float2 *>(p.part_ml + (srow + h) * 2) = make_float2(M[h], Lsum[h]);
+        // publish this part; the last part of the unit to arrive merges all
+        __threadfence();
+        named_barrier_sync(2, NET);
+        if (e == 0) {
+          const long long c_first = sc.part_of(sg.unit_start);
+          const long long c_last = sc.part_of(sg.unit_end - 1);
+          const int n_parts = (int)(c_last - c_first + 1);
+          const int before = atomicAdd(p.counters + unit, 1);
+          const int last = (before == n_parts - 1);
+          if (last) atomicExch(p.counters + unit, 0);  // ready for the next call
+          flag[0] = last;
+          flag[1] = (int)c_first;
+          flag[2] = n_parts;
+        }
+        named_barrier_sync(2, NET);
+        if (flag[0]) {
+          __threadfence();
+          const int c_first = flag[1], n_parts = flag[2];
+          const size_t row0 = ((size_t)unit + (size_t)c_first) * G;
+          float2 *mlb = reinterpret_cast<float2 *>(smem + L::OFF_MERGE);
+          constexpr int PPB = MERGE_PAIRS / G;  // parts per (max, sum) batch
+          constexpr int GP = 64 / G;            // parts per group of loads in flight
+          float Mx[G], Lm[G], O[G];
+#pragma unroll
+          for (int h = 0; h < G; ++h) { Mx[h] = -INFINITY; Lm[h] = 0.f; O[h] = 0.f; }
+          for (int base = 0; base < n_parts; base += PPB) {
+            const int nb = min(PPB, n_parts - base);
+            const size_t rb = row0 + (size_t)base * G;
+            // Partial outputs are read GP parts at a time, all loads of a
+            // group issued before any is used; the first group's loads are
+            // in flight while the (max, sum) pairs arrive.
+            float ov[GP][G];
+            auto load_group = [&](int g0) {
+#pragma unroll
+              for (int i = 0; i < GP; ++i)
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                  ov[i][h] = (g0 + i < nb)
+                                 ? __ldcg(p.part_o + (rb + (size_t)(g0 + i) * G + h) * kHeadDim + e)
+                                 : 0.f;
+            };
+            load_group(0);
+            for (int j = e; j < nb * G; j += NET)
+              mlb[j] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + rb + j);
+            named_barrier_sync(2, NET);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+              float bm = Mx[h];
+              for (int i = 0; i < nb; ++i) bm = fmaxf(bm, mlb[i * G + h].x);
+              if (bm != Mx[h] && Mx[h] != -INFINITY) {
+                const float cf = exp2f(Mx[h] - bm);
+                Lm[h] *= cf;
+                O[h] *= cf;
+              }
+              Mx[h] = bm;
+            }
+            for (int g0 = 0; g0 < nb; g0 += GP) {
+              if (g0 > 0) load_group(g0);
+#pragma unroll
+              for (int i = 0; i < GP; ++i) {
+                if (g0 + i < nb) {
+#pragma unroll
+                  for (int h = 0; h < G; ++h) {
+                    const float2 ml = mlb[(g0 + i) * G + h];
+                    if (ml.x != -INFINITY) {
+                      const float cf = exp2f(ml.x - Mx[h]);
+                      Lm[h] = fmaf(cf, ml.y, Lm[h]);
+                      O[h] = fmaf(cf, ov[i][h], O[h]);
+                    }
+                  }
+                }
+              }
+            }
+            named_barrier_sync(2, NET);  // mlb is reused by the next batch
+          }
+#pragma unroll
+          for (int h = 0; h < G; ++h)
+            p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(O[h] / Lm[h]);
+        }
+        named_barrier_sync(2, NET);  // flags are reused by the next segment
+      }
+      ++k;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == WARP_QK) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// The dynamic shared-memory limit is raised once per device, to the size the
+// largest accepted batch needs.
+template <int G, int BS, bool FP8>
+static cudaError_t ensure_smem_limit() {
+  static volatile int done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(paged_attention_kernel<G, BS, FP8>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes<FP8>(PGD_MAX_BATCH));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+  return e;
+}
+
+template <int G, int BS, bool FP8>
+static cudaError_t launch_cfg(const AttnParams &p, int grid, cudaStream_t stream) {
+  cudaError_t e = ensure_smem_limit<G, BS, FP8>();
+  if (e != cudaSuccess) return e;
+  // Programmatic stream serialization: the CTAs may launch and run their
+  // prologue while the previous kernel finishes (see pdl_wait above).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem_bytes<FP8>(p.B);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_attention_kernel<G, BS, FP8>, p);
+}
+
+template <int G, int BS, bool FP8>
+static int occupancy_cfg(int B) {
+  if (ensure_smem_limit<G, BS, FP8>() != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_attention_kernel<G, BS, FP8>,
+                                                    THREADS, smem_bytes<FP8>(B)) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+}  // namespace tc
+
+// Dispatch over the supported (G, block size) pairs for one kind of cache.
+template <bool FP8>
+int attention_ctas_per_sm_t(int G, int bs, int B) {
+#define PGD_CASE(G_, BS_) \
+  if (G == G_ && bs == BS_) return tc::occupancy_cfg<G_, BS_, FP8>(B);
+  PGD_CASE(1, 16) PGD_CASE(2, 16) PGD_CASE(4, 16) PGD_CASE(8, 16)
+  PGD_CASE(1, 32) PGD_CASE(2, 32) PGD_CASE(4, 32) PGD_CASE(8, 32)
+#undef PGD_CASE
+  return 0;
+}
+
+template <bool FP8>
+cudaError_t attention_launch_t(const AttnParams &p, int G, int bs, int grid,
+                               cudaStream_t stream) {
+#define PGD_CASE(G_, BS_) \
+  if (G == G_ && bs == BS_) return tc::launch_cfg<G_, BS_, FP8>(p, grid, stream);
+  PGD_CASE(1, 16) PGD_CASE(2, 16) PGD_CASE(4, 16) PGD_CASE(8, 16)
+  PGD_CASE(1, 32) PGD_CASE(2, 32) PGD_CASE(4, 32) PGD_CASE(8, 32)
+#undef PGD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pgd

@@ -9,6 +9,7 @@
 // 16-byte chunks 128 bytes apart.  One warp per (sequence, KV head): lanes
 // 0-15 move the K chunks and lanes 16-31 the V chunks.  A pure copy, bit exact.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "pgd_device.cuh"
@@ -61,6 +62,82 @@ cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache
       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), tables, pos, pos_offset, B,
       n_kv, bs, MB, NB, err);
+  return cudaGetLastError();
+}
+
+// kv_append into an 8-bit cache ("Ch. 6 Inference efficiency and serving",
+// 6.6.1: symmetric quantisation, the scale from the largest absolute value,
+// a zero row takes a positive scale; "The math of Transformer inference",
+// section 11: KV scales per head and per token).  For each (sequence, KV
+// head) row x of 128 bf16 values: scale = max|x| / 448 (1 if that is 0),
+// code_i = E4M3(x_i / scale), both divisions IEEE binary32, the conversion
+// rounding to nearest even and saturating to +-448.  The pool keeps each
+// 8-token group as its codes (8-row x 16-byte core matrices) then its 8
+// fp32 scales.  One warp per row pair: lanes 0-15 quantise K, 16-31 V, 8
+// values per lane; the max is a shuffle reduction inside each 16-lane half.
+__global__ void __launch_bounds__(128)
+kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
+                     unsigned char *__restrict__ k_cache, unsigned char *__restrict__ v_cache,
+                     const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
+                     int pos_offset, int B, int n_kv, int bs, int MB, int NB, int32_t *err) {
+  constexpr int kGroupBytes = 8 * kHeadDim + 32;
+  pdl_launch_dependents();  // the attention that follows may start its prologue
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= B * n_kv) return;
+  const int b = row / n_kv, g = row % n_kv;
+  const int p = __ldg(pos + b) + pos_offset;
+  if (p < 0 || p >= MB * bs) {
+    if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_POSITION);
+    return;
+  }
+  const int blk = __ldg(tables + (size_t)b * MB + p / bs);
+  if ((unsigned)blk >= (unsigned)NB) {
+    if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_BLOCK_ID);
+    return;
+  }
+  const int l = lane & 15;
+  const uint4 raw = __ldg((lane < 16 ? k_new : v_new) + (size_t)row * 16 + l);
+  float f[8];
+  unpack8(raw, f);
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, o));
+  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint32_t w[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const uint16_t c0 = (uint16_t)__nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(f[4 * j], scale), __fdiv_rn(f[4 * j + 1], scale)), __NV_SATFINITE,
+        __NV_E4M3);
+    const uint16_t c1 = (uint16_t)__nv_cvt_float2_to_fp8x2(
+        make_float2(__fdiv_rn(f[4 * j + 2], scale), __fdiv_rn(f[4 * j + 3], scale)),
+        __NV_SATFINITE, __NV_E4M3);
+    w[j] = (uint32_t)c0 | ((uint32_t)c1 << 16);
+  }
+  // group of the slot, then dims 8l..8l+7: core matrix l / 2, half l % 2
+  const int slot = p % bs;
+  unsigned char *group = (lane < 16 ? k_cache : v_cache) +
+                         (((size_t)blk * n_kv + g) * (size_t)(bs / 8) + (size_t)(slot / 8)) *
+                             (size_t)kGroupBytes;
+  *reinterpret_cast<uint2 *>(group + (l >> 1) * 128 + (slot & 7) * 16 + (l & 1) * 8) =
+      make_uint2(w[0], w[1]);
+  if (l == 0) *reinterpret_cast<float *>(group + 8 * kHeadDim + (slot & 7) * 4) = scale;
+}
+
+cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
+                                 void *v_cache, const int32_t *tables, const int32_t *pos,
+                                 int pos_offset, int B, int n_kv, int bs, int MB, int NB,
+                                 int32_t *err, cudaStream_t stream) {
+  const int rows = B * n_kv;
+  if (rows == 0) return cudaSuccess;
+  const int grid = (rows + 3) / 4;
+  kv_append_fp8_kernel<<<grid, 128, 0, stream>>>(
+      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
+      static_cast<unsigned char *>(k_cache), static_cast<unsigned char *>(v_cache), tables, pos,
+      pos_offset, B, n_kv, bs, MB, NB, err);
   return cudaGetLastError();
 }
 

@@ -126,8 +126,8 @@ __device__ __forceinline__ void unpack4(const uint2 &r, float (&f)[4]) {
 struct AttnParams {
   __nv_bfloat16 *out;            // [B][n_q][D]
   const __nv_bfloat16 *q;        // [B][n_q][D]
-  const __nv_bfloat16 *k_cache;  // [NB][n_kv][bs][D]
-  const __nv_bfloat16 *v_cache;
+  const unsigned char *k_cache;  // pool bytes: bf16 tiles, or 8-bit groups (codes + scales)
+  const unsigned char *v_cache;
   const int32_t *tables;         // [B][MB]
   const int32_t *ctx;            // [B]
   int B, n_q, n_kv, MB, NB;
