@@ -40,8 +40,9 @@ NOMINAL_HBM_GBS = 8000.0     # nominal GB300 HBM3e bandwidth (~8 TB/s)
 FALLBACK_HBM_GBS = 6800.0    # profiling recipe's fallback when no measured peak exists
 L2_BYTES = 129 * 10**6
 ATTENTION_SOURCES = [os.path.join(ROOT, "paged_gqa_decode_kv_gb300", "csrc", f)
-                     for f in ("attention.cu", "pgd_device.cuh")]
+                     for f in ("attention_kernel.cuh", "pgd_device.cuh")]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "paged_attention_batch16_ctx8192.md")
+PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "paged_attention_fp8_batch16_ctx8192.md")
 
 
 def parse_args(argv=None):
@@ -51,6 +52,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--workload", default="batch16_ctx8192")
     ap.add_argument("--splits", type=int, default=0, help="0 = automatic")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="cache format: bf16, or FP8 E4M3 codes + per-(token, head) scales")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -175,11 +178,14 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
+def profiled_traffic(kv: str = "bf16", workload: str = "batch16_ctx8192"):
     """DRAM bytes per launch from the committed ncu summary of the attention
-    kernel, or None if the kernel source changed since that capture."""
+    kernel on this workload, or None if there is none or the kernel source
+    changed since that capture."""
+    if workload != "batch16_ctx8192":
+        return None
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(PROFILE_SUMMARY_FP8 if kv == "fp8" else PROFILE_SUMMARY).read()
     except OSError:
         return None
     m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
@@ -190,8 +196,8 @@ def profiled_traffic():
 
 
 def kernel_source_sha256() -> str:
-    """sha256 of the attention kernel's sources (attention.cu, then the
-    device header it includes)."""
+    """sha256 of the attention kernel's sources (attention_kernel.cuh, then
+    the device header it includes)."""
     h = hashlib.sha256()
     for path in ATTENTION_SOURCES:
         h.update(open(path, "rb").read())
@@ -207,17 +213,23 @@ def oracle_sample(pb_host, n_seq: int, n_threads: int = 0):
     t = pb_host["tables"][:n_seq]
     c = pb_host["lens"][:n_seq]
     t0 = time.perf_counter()
-    oracle.paged_attention(q, pb_host["k"], pb_host["v"], t, c, pb_host["scale"],
-                           n_threads=n_threads)
+    if pb_host["kv"] == "fp8":
+        oracle.paged_attention_fp8(q, pb_host["k"], pb_host["v"], t, c, pb_host["scale"],
+                                   pb_host["bs"], n_threads=n_threads)
+        per_token = 2 * pb_host["n_kv"] * (pb_host["d"] + 4)
+    else:
+        oracle.paged_attention(q, pb_host["k"], pb_host["v"], t, c, pb_host["scale"],
+                               n_threads=n_threads)
+        per_token = 2 * pb_host["n_kv"] * pb_host["d"] * 2
     dt = time.perf_counter() - t0
-    per_token = 2 * pb_host["n_kv"] * pb_host["d"] * 2
     return dt, int(c.sum()) * per_token
 
 
 def host_copy(pb):
     return {"q": pb.q.cpu(), "k": pb.k_cache.cpu(), "v": pb.v_cache.cpu(),
             "tables": pb.block_tables.cpu(), "lens": pb.context_lens.cpu(), "scale": pb.scale,
-            "n_kv": pb.n_kv, "d": pb.head_dim, "B": pb.batch, "n_q": pb.n_q}
+            "n_kv": pb.n_kv, "d": pb.head_dim, "B": pb.batch, "n_q": pb.n_q,
+            "kv": pb.kv_format, "bs": pb.block_size}
 
 
 def cpu_baseline(pb_host, seconds: float):
@@ -244,9 +256,12 @@ def config_block(pb, name, splits, n_pools):
             if pb.batch <= 4 else "%d..%d" % (int(pb.context_lens.min()),
                                               int(pb.context_lens.max())),
             "n_q": pb.n_q, "n_kv": pb.n_kv, "head_dim": pb.head_dim,
-            "block_size": pb.block_size, "kv_dtype": "bf16",
+            "block_size": pb.block_size,
+            "kv_dtype": "bf16" if pb.kv_format == "bf16" else
+            "fp8_e4m3 codes + fp32 scale per (token, head)",
             "splits": "auto" if splits == 0 else splits,
-            "kv_layout": "tiled 8x8 core matrices per (block, head)",
+            "kv_layout": "tiled 8x8 core matrices per (block, head)" if pb.kv_format == "bf16"
+            else "per 8-token group: 8x16-byte core matrices of codes, then 8 scales",
             "l2": ("K/V pool %.0f MB > 129 MB L2, no flush" % (pool_bytes(pb) / 1e6))
             if n_pools == 1 else
             ("%d copies of the %.1f MB K/V pool rotated step by step (%.0f MB > 2 x L2), "
@@ -275,7 +290,10 @@ def run_ours(args, rank, world, local):
     __graft_entry__.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    pb = inputs.make_workload(args.workload, device=dev, append=True)
+    pb = inputs.make_workload(args.workload, device=dev, append=True, kv_format=args.kv)
+    fp8 = args.kv == "fp8"
+    append_attend = pgd.append_decode_attention_fp8 if fp8 else pgd.append_decode_attention
+    attend = pgd.paged_decode_attention_fp8 if fp8 else pgd.paged_decode_attention
     B, n_q, n_kv = pb.batch, pb.n_q, pb.n_kv
     ws = pgd.make_workspace(B, n_q, n_kv, args.splits, dev)
     out = torch.empty_like(pb.q)
@@ -298,14 +316,13 @@ def run_ours(args, rank, world, local):
     def step():
         # kv_append at context_lens - 1, then attention: one C-ABI call, two kernels
         kc, vc = next_pool()
-        pgd.append_decode_attention(out, pb.q, pb.k_new, pb.v_new, kc, vc, pb.block_tables,
-                                    pb.context_lens, pb.scale, num_splits=args.splits,
-                                    workspace=ws, stream=stream)
+        append_attend(out, pb.q, pb.k_new, pb.v_new, kc, vc, pb.block_tables, pb.context_lens,
+                      pb.scale, num_splits=args.splits, workspace=ws, stream=stream)
 
     def attention_only():
         kc, vc = next_pool()
-        pgd.paged_decode_attention(out, pb.q, kc, vc, pb.block_tables, pb.context_lens,
-                                   pb.scale, num_splits=args.splits, workspace=ws, stream=stream)
+        attend(out, pb.q, kc, vc, pb.block_tables, pb.context_lens, pb.scale,
+               num_splits=args.splits, workspace=ws, stream=stream)
 
     gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     sampler = ClockSampler(gpu_uuid)
@@ -389,8 +406,12 @@ def run_ours(args, rank, world, local):
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(max_ms / K, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "accumulate": "f32", "data": "synthetic (seeded N(0,1) bf16 K/V/Q, random block tables)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3 (q.k^T), bf16 (p.v)" if fp8 else "bf16",
+        "accumulate": "f32",
+        "data": ("synthetic (seeded E4M3 K/V codes + per-token scales, N(0,1) bf16 Q, random "
+                 "block tables)") if fp8 else
+                "synthetic (seeded N(0,1) bf16 K/V/Q, random block tables)",
         "config": config_block(pb, args.workload, args.splits, n_pools),
         "grid_ctas": grid,
         "kv_bytes_per_step": kv_bytes,
@@ -400,10 +421,13 @@ def run_ours(args, rank, world, local):
         "seq_layer_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": {"nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
                             peak_kind: round(100 * value / world / peak, 2)},
-        "roofline": {"bound": "hbm", "kernel": "pgd::tc::paged_attention_kernel (tcgen05)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "pgd::tc::paged_attention_kernel<G, bs, %s> (tcgen05)"
+                               % ("fp8" if fp8 else "bf16"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(), "launch_ms": round(attn_ms, 5),
+                     "traffic": profiled_traffic(args.kv, args.workload),
+                     "launch_ms": round(attn_ms, 5),
                      "bytes_per_launch": kv_bytes},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5)},
@@ -423,7 +447,7 @@ def run_reference(args):
     import oracle
     from paged_gqa_decode_kv_gb300 import inputs
 
-    pb = inputs.make_workload(args.workload, device="cpu", append=False)
+    pb = inputs.make_workload(args.workload, device="cpu", append=False, kv_format=args.kv)
     host = host_copy(pb)
     B = pb.batch
     # calibrate: one sequence, then size the sample so the run stays within ~2 minutes
@@ -444,7 +468,8 @@ def run_reference(args):
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(1e3 * t_total / max(1, args.steps), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) bf16 K/V/Q, random block tables)",
+        "data": "synthetic (seeded %s K/V, N(0,1) bf16 Q, random block tables)"
+                % ("E4M3 + per-token scale" if args.kv == "fp8" else "N(0,1) bf16"),
         "config": config_block(pb, args.workload, args.splits, pool_copies(pb)),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",

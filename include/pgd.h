@@ -243,9 +243,10 @@ pgd_status pgd_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache
  * above), checks, errors and workspace (pgd_attention_workspace_size).
  * Arithmetic: q.k^T on the tensor cores in E4M3 with the query split into a
  * high and a low E4M3 part (about 8 bits of the bf16 query), the key and
- * query scales applied in fp32; V converted to bf16 exactly and its scale
- * folded into the bf16 probabilities; fp32 softmax and accumulation; bf16
- * output.  The query must be finite. */
+ * query scales applied in fp32; V dequantised to f16 (code times the scale
+ * rounded to f16) and probabilities in f16 for the p.v; fp32 softmax and
+ * accumulation; bf16 output.  The query must be finite and the dequantised
+ * V values within the f16 range (|v| < 65504). */
 pgd_status pgd_paged_decode_attention_fp8(void *out, const void *q, const void *k_cache,
                                           const void *v_cache, const int32_t *block_tables,
                                           const int32_t *context_lens, int32_t B, int32_t n_q,
@@ -281,6 +282,16 @@ pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, co
                            int32_t d, int32_t bs, int32_t MB, int32_t NB, float scale,
                            int32_t num_splits, void *workspace, size_t workspace_bytes,
                            void *stream);
+
+/* pgd_decode_step for an 8-bit pool: the same host-to-device copies, then
+ * pgd_append_decode_attention_fp8, then the copy of the output back. */
+pgd_status pgd_decode_step_fp8(void *out_h, const void *q_h, const void *k_new_h,
+                               const void *v_new_h, const int32_t *context_lens_h, void *out_d,
+                               void *q_d, void *k_new_d, void *v_new_d, int32_t *context_lens_d,
+                               void *k_cache, void *v_cache, const int32_t *block_tables,
+                               int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                               int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                               void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* copy-on-write block copy                                               */

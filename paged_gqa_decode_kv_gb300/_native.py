@@ -45,6 +45,8 @@ SIGNATURES = {
                                          _I, _F, _I, _P, _Z, _P], _I),
     "pgd_decode_step": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                          _I, _I, _F, _I, _P, _Z, _P], _I),
+    "pgd_decode_step_fp8": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
+                             _I, _I, _I, _F, _I, _P, _Z, _P], _I),
     "pgd_copy_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "pgd_device_errors": ([_P, _I, _P], _I),
     "pgd_alloc_create": ([_I, _P], _I),
@@ -228,14 +230,17 @@ def decode_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_
                 context_lens_d, k_cache, v_cache, block_tables, scale: float, num_splits: int,
                 workspace: torch.Tensor, stream=None) -> None:
     """One decode step with host (pinned) inputs/outputs: H2D copies, append at
-    context_lens - 1, attention, D2H copy of the output; all on `stream`."""
+    context_lens - 1, attention, D2H copy of the output; all on `stream`.  An
+    8-bit pool (uint8) selects the FP8 path."""
     for t, n in ((out_h, "out_h"), (q_h, "q_h"), (k_new_h, "k_new_h"), (v_new_h, "v_new_h")):
         _need(t, torch.bfloat16, n, cuda=False)
     _need(context_lens_h, torch.int32, "context_lens_h", cuda=False)
     B, n_q, d = q_h.shape
-    NB, n_kv, bs, _ = _cache_dims(k_cache)
+    fp8 = k_cache.dtype == torch.uint8
+    NB, n_kv, bs, _ = _cache8_dims(k_cache) if fp8 else _cache_dims(k_cache)
     MB = block_tables.shape[1]
-    _check(lib().pgd_decode_step(
+    fn = lib().pgd_decode_step_fp8 if fp8 else lib().pgd_decode_step
+    _check(fn(
         _ptr(out_h), _ptr(q_h), _ptr(k_new_h), _ptr(v_new_h), _ptr(context_lens_h), _ptr(out_d),
         _ptr(q_d), _ptr(k_new_d), _ptr(v_new_d), _ptr(context_lens_d), _ptr(k_cache),
         _ptr(v_cache), _ptr(block_tables), B, n_q, n_kv, d, bs, MB, NB, float(scale),

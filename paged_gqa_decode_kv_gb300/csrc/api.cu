@@ -473,7 +473,7 @@ pgd_status pgd_append_decode_attention_fp8(void *out, const void *q, const void 
   return s == PGD_OK ? ok() : s;
 }
 
-pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
+static pgd_status decode_step_impl(bool fp8, void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
                            const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
                            void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
                            const int32_t *block_tables, int32_t B, int32_t n_q, int32_t n_kv,
@@ -492,7 +492,8 @@ pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, co
     // every check of the device half runs before the first copy is enqueued
     PreparedAttention pa;
     s = prepare_attention(out_d, q_d, k_cache, v_cache, block_tables, context_lens_d, B, n_q,
-                          n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes, &pa);
+                          n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes, &pa,
+                          fp8);
     if (s != PGD_OK) return s;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -506,11 +507,35 @@ pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, co
     return cuda_fail(e, "decode step: host-to-device copy");
   s = append_then_attend(out_d, q_d, k_new_d, v_new_d, k_cache, v_cache, block_tables,
                          context_lens_d, B, n_q, n_kv, bs, MB, NB, scale, num_splits, workspace,
-                         workspace_bytes, st);
+                         workspace_bytes, st, fp8);
   if (s != PGD_OK) return s;
   if ((e = cudaMemcpyAsync(out_h, out_d, qb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
     return cuda_fail(e, "decode step: device-to-host copy");
   return ok();
+}
+
+pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
+                           const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
+                           void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
+                           const int32_t *block_tables, int32_t B, int32_t n_q, int32_t n_kv,
+                           int32_t d, int32_t bs, int32_t MB, int32_t NB, float scale,
+                           int32_t num_splits, void *workspace, size_t workspace_bytes,
+                           void *stream) {
+  return decode_step_impl(false, out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d,
+                          v_new_d, context_lens_d, k_cache, v_cache, block_tables, B, n_q, n_kv, d,
+                          bs, MB, NB, scale, num_splits, workspace, workspace_bytes, stream);
+}
+
+pgd_status pgd_decode_step_fp8(void *out_h, const void *q_h, const void *k_new_h,
+                               const void *v_new_h, const int32_t *context_lens_h, void *out_d,
+                               void *q_d, void *k_new_d, void *v_new_d, int32_t *context_lens_d,
+                               void *k_cache, void *v_cache, const int32_t *block_tables,
+                               int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                               int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                               void *workspace, size_t workspace_bytes, void *stream) {
+  return decode_step_impl(true, out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d,
+                          v_new_d, context_lens_d, k_cache, v_cache, block_tables, B, n_q, n_kv, d,
+                          bs, MB, NB, scale, num_splits, workspace, workspace_bytes, stream);
 }
 
 pgd_status pgd_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_ids,

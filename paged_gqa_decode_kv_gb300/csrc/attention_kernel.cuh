@@ -58,6 +58,7 @@
 //   warps 8-11 epilogue: per segment, read O from tensor memory and write the
 //              output or a partial state (and merge a unit's partials when
 //              they are complete), off the softmax warps' critical path
+//   warps 12-15 (8-bit cache only) V dequantisation into f16 operands
 // Rings: 3 K stages and 3 V stages of 32 KiB; a K stage is free as soon as
 // its q.k^T has completed, a V stage after its p.v.  S and P are double
 // buffered by stage parity, O and Q by segment parity.  Every wait is bounded.
@@ -74,9 +75,8 @@
 // (q / s_q = hi + lo, s_q = max |q| / 448), hi in column h and lo in column
 // 8 + h of the same N = 16 MMA, so the score keeps about 8 bits of the
 // query at no extra MMA; the softmax adds the two columns and applies s_q
-// and the key's scale.  V is converted to bf16 by the softmax threads (each
-// its own token row, exactly: every E4M3 value is a bf16 value) and the
-// token's V scale is folded into its probability before the bf16 p.v.
+// and the key's scale.  Four more warps dequantise V to f16 (code * scale,
+// each thread its own token row) for an f16 p.v with f16 probabilities.
 //
 // Softmax keeps one reference maximum per head.  A stage moves the reference
 // (and rescales O in tensor memory, after the previous p.v has completed)
@@ -100,9 +100,12 @@ namespace tc {
 constexpr int TOK = 128;                    // tokens per stage (MMA M of q.k^T)
 constexpr int NPAD = 16;                    // MMA N: heads padded to 16
 constexpr int P_BYTES = TOK * NPAD * 2;     // [16 token groups][2 head groups][8][16 B]
-constexpr int THREADS = 384;
-constexpr int WARP_KP = 4, WARP_VP = 5, WARP_QK = 6, WARP_PV = 7, WARP_EPI = 8;
-constexpr uint32_t TMEM_COLS = 64;
+constexpr int WARP_KP = 4, WARP_VP = 5, WARP_QK = 6, WARP_PV = 7, WARP_EPI = 8, WARP_CVT = 12;
+// 12 warps; the 8-bit kernel adds NCVT warps that dequantise V (warps 12..)
+constexpr int NCVT = 4;
+template <bool FP8> constexpr int kThreads = FP8 ? 384 + 32 * NCVT : 384;
+constexpr int NSB = 4;                      // S buffers (q.k^T may run 4 stages ahead)
+constexpr uint32_t TMEM_COLS = 128;
 constexpr float kRescaleLog2 = 8.f;         // move the reference when exceeded by 2^8
 // Split choice.  One CTA streams at most about 1/kCtaShare of the HBM rate
 // (its three 64 KiB K+V stages in flight over the load latency); a unit's
@@ -146,8 +149,8 @@ __host__ __device__ constexpr size_t smem_bytes(int B) {
 static_assert(smem_bytes<false>(PGD_MAX_BATCH) <= 232448, "bf16 layout exceeds 227 KB");
 static_assert(smem_bytes<true>(PGD_MAX_BATCH) <= 232448, "8-bit layout exceeds 227 KB");
 
-__device__ __forceinline__ uint32_t col_s(int sb) { return (uint32_t)sb * 16u; }
-__device__ __forceinline__ uint32_t col_o(int ob) { return 32u + (uint32_t)ob * 16u; }
+__device__ __forceinline__ uint32_t col_s(int sb) { return (uint32_t)sb * 16u; }  // sb < NSB
+__device__ __forceinline__ uint32_t col_o(int ob) { return 64u + (uint32_t)ob * 16u; }
 
 // ---------------------------------------------------------------- PTX helpers
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
@@ -159,11 +162,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
 }
 
-// Instruction descriptor, kind::f16: D f32, A and B bf16, M = 128, N = 16;
-// a_mn / b_mn select MN-major operands.
-__host__ __device__ constexpr uint32_t instr_desc(bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
-         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(NPAD >> 3) << 17) | ((uint32_t)(TOK >> 4) << 24);
+// Instruction descriptor, kind::f16: D f32, A and B bf16 (or both f16),
+// M = 128, N = 16; a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t instr_desc(bool a_mn, bool b_mn, bool bf16 = true) {
+  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+         ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(NPAD >> 3) << 17) |
+         ((uint32_t)(TOK >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -224,6 +228,25 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   v[6] = __uint_as_float(r6); v[7] = __uint_as_float(r7);
 }
 
+// 8 columns of this warp's 32 lanes, without the wait: the registers are
+// valid only after tmem_wait8 on them (which names them, so the compiler
+// cannot use them earlier).
+__device__ __forceinline__ void tmem_ld8_async(uint32_t taddr, uint32_t *r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait8(uint32_t *r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7])
+               :
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n\t"
@@ -250,8 +273,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // whatever happens.
 __device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, int32_t *err) {
-  if (*abort_flag) return;
   if (mbar_try_wait(bar, parity)) return;
+  if (*abort_flag) return;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return;
@@ -345,18 +368,19 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
   return __half22float2(h);
 }
 
-// 16 E4M3 codes -> 16 bf16 (two 16-byte rows of 8), exactly: every E4M3
-// value is a half and a bf16 value; the bf16 is the upper half of the
-// binary32 widening.
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 &c, uint4 &lo, uint4 &hi) {
+// 16 E4M3 codes of one token -> 16 dequantised f16 values code * scale (two
+// 16-byte rows of 8): the code widens to f16 exactly, the product rounds to
+// nearest.
+__device__ __forceinline__ void e4m3x16_dequant_f16(const uint4 &c, __half2 scale, uint4 &lo,
+                                                    uint4 &hi) {
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
   uint32_t o[8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 a = e4m3x2_to_float2((uint16_t)(w[i] & 0xFFFFu));
-    const float2 b = e4m3x2_to_float2((uint16_t)(w[i] >> 16));
-    o[2 * i] = __byte_perm(__float_as_uint(a.x), __float_as_uint(a.y), 0x7632);
-    o[2 * i + 1] = __byte_perm(__float_as_uint(b.x), __float_as_uint(b.y), 0x7632);
+  for (int i = 0; i < 8; ++i) {
+    const uint16_t pair = (uint16_t)(w[i >> 1] >> ((i & 1) * 16));
+    const __half2 h = __hmul2(
+        __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair, __NV_E4M3)), scale);
+    o[i] = *reinterpret_cast<const uint32_t *>(&h);
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
@@ -499,6 +523,8 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
         if (IS_K) {
           stage_mask[s & 7] = (int)(want & ~okmask);
           if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
+        } else if (FP8) {
+          stage_mask[slot] = (int)(want & ~okmask);  // per V slot, for the V converters
         }
         const uint32_t bytes = (uint32_t)__popc(okmask) * TILE_BYTES;
         if (*abort_flag || bytes == 0)
@@ -527,12 +553,13 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
 }
 
 template <int G, int BS, bool FP8>
-__global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const AttnParams p) {
   using L = Lay<FP8>;
   constexpr int SB = TOK / BS;
   constexpr uint32_t IDESC_QK = instr_desc(false, false);
   constexpr uint32_t IDESC_QK8 = instr_desc_e4m3();
   constexpr uint32_t IDESC_PV = instr_desc(true, true);
+  constexpr uint32_t IDESC_PV16 = instr_desc(true, true, false);  // f16 V and P
   static_assert(G >= 1 && G <= 8 && TOK % BS == 0 && BS % 8 == 0 && SB <= 32, "shape");
 
   extern __shared__ unsigned char smem_raw[];
@@ -543,17 +570,18 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   uint64_t *empty_k = full_k + L::NSK;     // [NSK]
   uint64_t *full_v = empty_k + L::NSK;     // [NSV]
   uint64_t *empty_v = full_v + L::NSV;     // [NSV]
-  uint64_t *s_full = empty_v + L::NSV;     // [2]
-  uint64_t *s_free = s_full + 2;        // [2]
-  uint64_t *p_full = s_free + 2;        // [2]
+  uint64_t *s_full = empty_v + L::NSV;     // [NSB]
+  uint64_t *s_free = s_full + NSB;         // [NSB]
+  uint64_t *p_full = s_free + NSB;         // [2]
   uint64_t *p_free = p_full + 2;        // [2]
   uint64_t *o_full = p_free + 2;        // [2]
   uint64_t *o_free = o_full + 2;        // [2]
-  uint64_t *m_ready = o_free + 2;       // [2]
-  uint64_t *q_ready = m_ready + 2;      // [2] per Q buffer
+  uint64_t *m_ready = o_free + 2;       // [NSB]
+  uint64_t *q_ready = m_ready + NSB;    // [2] per Q buffer
   uint64_t *q_free = q_ready + 2;       // [2] per Q buffer
   uint64_t *done = q_free + 2;          // [2] one per MMA issuer
   uint64_t *seg_done = done + 2;        // [2] softmax -> epilogue, per segment parity
+  uint64_t *vb_full = seg_done + 2;     // [2] 8-bit: V converters -> p.v, by stage parity
   float *red = reinterpret_cast<float *>(smem + L::OFF_RED);
   float *lred = reinterpret_cast<float *>(smem + L::OFF_LRED);
   float *mref = reinterpret_cast<float *>(smem + L::OFF_MREF);
@@ -563,6 +591,7 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   volatile int *flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 8);         // [3]
   int *nmax_slot = reinterpret_cast<int *>(smem + L::OFF_MISC + 20);
   volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 40);  // [8]
+  volatile int *vmask = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 72);       // [NSV]
   int *pre = reinterpret_cast<int *>(smem + L::OFF_PRE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -572,27 +601,30 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   if (!p.wait_late) pdl_wait();
 
   if (tid == 0) {
-    // 8-bit cache: the softmax warps read each K stage's scales and convert
-    // each V stage themselves, so they too release K and V slots, and they
-    // release a Q buffer once they hold its scales.
+    // 8-bit cache: the softmax warps read each K stage's scales, so they too
+    // release K slots, and a Q buffer once they hold its scales; the V
+    // converter warps release the V slots.
     for (int i = 0; i < L::NSK; ++i) {
       mbar_init(&full_k[i], 1);
       mbar_init(&empty_k[i], FP8 ? 1 + 4 : 1);
     }
     for (int i = 0; i < L::NSV; ++i) {
       mbar_init(&full_v[i], 1);
-      mbar_init(&empty_v[i], FP8 ? 4 : 1);
+      mbar_init(&empty_v[i], FP8 ? NCVT : 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSB; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
+      mbar_init(&m_ready[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 4);
       mbar_init(&p_free[i], 1);
       mbar_init(&o_full[i], 1);
       mbar_init(&o_free[i], 4);
-      mbar_init(&m_ready[i], 1);
       mbar_init(&done[i], 1);
       mbar_init(&seg_done[i], 4);
+      mbar_init(&vb_full[i], NCVT);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_ready[i], 1);
@@ -604,12 +636,13 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
   // Q pad rows and P pad columns stay zero for the whole kernel.
   {
     uint4 *z = reinterpret_cast<uint4 *>(smem + L::OFF_Q);
-    for (int i = tid; i < (2 * L::Q_BYTES + 2 * P_BYTES) / 16; i += THREADS) z[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < (2 * L::Q_BYTES + 2 * P_BYTES) / 16; i += kThreads<FP8>)
+      z[i] = make_uint4(0, 0, 0, 0);
   }
   // Blocks per sequence, then an exclusive prefix over the batch.
   const int max_tokens = p.MB * BS;
   bool bad_ctx = false;
-  for (int b = tid; b < p.B; b += THREADS) {
+  for (int b = tid; b < p.B; b += kThreads<FP8>) {
     const int c = p.ctx[b];
     int nb = 0;
     if (c >= 1 && c <= max_tokens) nb = (c + BS - 1) / BS; else bad_ctx = true;
@@ -678,7 +711,7 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
     produce<G, BS, FP8, true>(p, sc, p.k_cache, smem + L::OFF_K, full_k, empty_k, stage_mask,
                               smem + L::OFF_Q, qscale, q_ready, q_free, abort_flag, lane);
   } else if (warp == WARP_VP) {
-    produce<G, BS, FP8, false>(p, sc, p.v_cache, smem + L::OFF_V, full_v, empty_v, nullptr,
+    produce<G, BS, FP8, false>(p, sc, p.v_cache, smem + L::OFF_V, full_v, empty_v, vmask,
                                nullptr, nullptr, nullptr, nullptr, abort_flag, lane);
   } else if (warp == WARP_QK) {
     // ---------------------------------------------------- q.k^T issuer
@@ -695,9 +728,9 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
         wait_or_abort(&q_ready[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
         const uint32_t q_seg = q_base + (uint32_t)((k & 1) * L::Q_BYTES);
         for (int st = 0; st < nstages; ++st, ++s) {
-          const int slot = s % L::NSK, sb = s & 1;
+          const int slot = s % L::NSK, sb = s % NSB;
           wait_or_abort(&full_k[slot], (uint32_t)(s / L::NSK) & 1u, abort_flag, p.err);
-          wait_or_abort(&s_free[sb], ((uint32_t)(s >> 1) & 1u) ^ 1u, abort_flag, p.err);
+          wait_or_abort(&s_free[sb], ((uint32_t)(s / NSB) & 1u) ^ 1u, abort_flag, p.err);
           tc_fence_after();
           if (!*abort_flag) {
             const uint32_t dS = tmem + col_s(sb);
@@ -753,9 +786,10 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
         for (int st = 0; st < nstages; ++st, ++s) {
           const int slot = s % L::NSV, sb = s & 1;
           wait_or_abort(&p_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
-          // (8-bit cache: p_full also means the softmax has converted this
-          // stage's V into the bf16 buffer of parity sb)
-          if (!FP8) wait_or_abort(&full_v[slot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
+          if (FP8)  // V dequantised into the f16 buffer of parity sb
+            wait_or_abort(&vb_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
+          else
+            wait_or_abort(&full_v[slot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
           if (st == 0)
             wait_or_abort(&o_free[ob], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
           tc_fence_after();
@@ -769,8 +803,8 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
             const uint32_t acc0 = st > 0 ? 1u : 0u;
 #pragma unroll
             for (int kt = 0; kt < 8; ++kt)
-              umma_bf16(dO, vd + (uint64_t)(kt * 256), pd + (uint64_t)(kt * 32), IDESC_PV,
-                        kt > 0 ? 1u : acc0);
+              umma_bf16(dO, vd + (uint64_t)(kt * 256), pd + (uint64_t)(kt * 32),
+                        FP8 ? IDESC_PV16 : IDESC_PV, kt > 0 ? 1u : acc0);
           }
           if (!FP8) umma_commit(&empty_v[slot]);
           umma_commit(&p_free[sb]);  // P (and converted V) of parity sb reusable
@@ -785,12 +819,17 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
     }
   } else if (warp < 4) {
     // ----------------------------------------------------------- softmax
+    // Two MMA stages (256 tokens) per iteration: one tile maximum, one named
+    // barrier and one rescale decision serve both, so the fixed latency of a
+    // step (waits, tensor-memory loads, barrier, fences) is paid once per 256
+    // tokens.  Thread t owns token row t of each of the two stages.
     const int t = tid;  // 0..127: token row of S
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     constexpr int NCT = 128;
+    constexpr int NSC = FP8 ? 16 : 8;  // S columns per stage (8-bit: high and low parts)
     SegCursor cur(sc);
     Segment sg;
-    int s = 0, k = 0;
+    int s = 0, k = 0, it = 0;
     while (cur.next(sc, p.B, sg)) {
       const int ctx_b = __ldg(p.ctx + sg.b);
       const int nstages = (sg.n + SB - 1) / SB;
@@ -800,73 +839,129 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
 #pragma unroll
       for (int h = 0; h < G; ++h) { m_ref[h] = -INFINITY; l_part[h] = 0.f; qsc[h] = 0.f; }
 
-      for (int st = 0; st < nstages; ++st, ++s) {
-        const int vslot = s % L::NSV, sb = s & 1;
-        const int nb = min(SB, sg.n - st * SB);
-        const int jfirst = sg.j0 + st * SB;
-        int nvalid = nb * BS;
-        if (jfirst + nb == sg.nblk) nvalid -= sg.nblk * BS - ctx_b;  // unit's last block
-
-        wait_or_abort(&s_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
-        // Invalid-block mask of this stage: the K producer wrote it before
+      for (int st = 0; st < nstages; st += 2, ++it) {
+        const int n2 = min(2, nstages - st);  // stages in this iteration
+        bool valid[2] = {false, false};
+        int msk[2] = {0, 0};
+        // Invalid-block mask of each stage: the K producer wrote it before
         // arming full_k; the q.k^T issuer acquired full_k and then released
-        // m_ready.  (Waiting on full_k here could alias: a K stage is freed
-        // after its q.k^T, so full_k may run two phases ahead.)  m_ready and
-        // the 8-entry mask ring cannot move on before this stage frees its S
-        // buffer.
-        wait_or_abort(&m_ready[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
-        const int mask = stage_mask[s & 7];
+        // m_ready.  (Waiting on full_k here could alias under the bf16
+        // cache: a K stage is freed after its q.k^T alone, so full_k may run
+        // two phases ahead.)  The 8-entry mask ring cannot move on before
+        // these stages free their S buffers.
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (u < n2) {
+            const int su = s + u, sbu = su % NSB;
+            wait_or_abort(&s_full[sbu], (uint32_t)(su / NSB) & 1u, abort_flag, p.err);
+            // (8-bit cache: K slots are released by these warps too, so
+            // full_k cannot run ahead and is waited on directly)
+            if (FP8)
+              wait_or_abort(&full_k[su % L::NSK], (uint32_t)(su / L::NSK) & 1u, abort_flag, p.err);
+            else
+              wait_or_abort(&m_ready[sbu], (uint32_t)(su / NSB) & 1u, abort_flag, p.err);
+            msk[u] = stage_mask[su & 7];
+            const int nb = min(SB, sg.n - (st + u) * SB);
+            int nvalid = nb * BS;
+            if (sg.j0 + (st + u) * SB + nb == sg.nblk) nvalid -= sg.nblk * BS - ctx_b;  // last block
+            valid[u] = (t < nvalid) && !((msk[u] >> (t / BS)) & 1);
+          }
+        }
         tc_fence_after();
-        float sv[FP8 ? 16 : 8];
-        tmem_ld8(tmem + lane_base + col_s(sb), *reinterpret_cast<float(*)[8]>(sv));
-        if constexpr (FP8)
-          tmem_ld8(tmem + lane_base + col_s(sb) + 8, *reinterpret_cast<float(*)[8]>(sv + 8));
+        uint32_t sv[2][NSC];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (u < n2) {
+            const uint32_t a0 = tmem + lane_base + col_s((s + u) % NSB);
+            tmem_ld8_async(a0, sv[u]);
+            if (FP8) tmem_ld8_async(a0 + 8, sv[u] + 8);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (u < n2) {
+            tmem_wait8(sv[u]);
+            if (FP8) tmem_wait8(sv[u] + 8);
+          }
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[sb]);
+        if (lane == 0) {
+          mbar_arrive(&s_free[s % NSB]);
+          if (n2 > 1) mbar_arrive(&s_free[(s + 1) % NSB]);
+        }
 
-        const bool valid = (t < nvalid) && !((mask >> (t / BS)) & 1);
-        float sc_[G];
+        float sc_[2][G];
         if constexpr (FP8) {
-          // Key scale of this token (the K slot is refilled only after these
+          // Key scale of each token (the K slot is refilled only after these
           // four warps release it, so waiting on full_k cannot alias), and at
           // a segment's first stage the Q scales (the K producer wrote them
           // before q_ready, which the q.k^T issuer acquired before m_ready).
-          const int kslot = s % L::NSK;
-          wait_or_abort(&full_k[kslot], (uint32_t)(s / L::NSK) & 1u, abort_flag, p.err);
-          const float ks = *reinterpret_cast<const float *>(
-              smem + L::OFF_K + kslot * L::STAGE + (t >> 3) * L::GROUP + 1024 + (t & 7) * 4);
+          float ks[2] = {0.f, 0.f};
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (u < n2) {
+              const int kslot = (s + u) % L::NSK;  // full_k already waited on above
+              ks[u] = *reinterpret_cast<const float *>(
+                  smem + L::OFF_K + kslot * L::STAGE + (t >> 3) * L::GROUP + 1024 + (t & 7) * 4);
+            }
+          }
           if (st == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h) qsc[h] = qscale[(k & 1) * 8 + h] * p.qk_scale_log2;
           }
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&empty_k[kslot]);
+            mbar_arrive(&empty_k[s % L::NSK]);
+            if (n2 > 1) mbar_arrive(&empty_k[(s + 1) % L::NSK]);
             if (st == 0) mbar_arrive(&q_free[k & 1]);
           }
 #pragma unroll
-          for (int h = 0; h < G; ++h) sc_[h] = valid ? (sv[h] + sv[8 + h]) * (qsc[h] * ks) : -INFINITY;
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+              sc_[u][h] = valid[u] ? (__uint_as_float(sv[u][h]) + __uint_as_float(sv[u][8 + h])) *
+                                         (qsc[h] * ks[u])
+                                   : -INFINITY;
         } else {
 #pragma unroll
-          for (int h = 0; h < G; ++h) sc_[h] = valid ? sv[h] * p.qk_scale_log2 : -INFINITY;
+          for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+              sc_[u][h] = valid[u] ? __uint_as_float(sv[u][h]) * p.qk_scale_log2 : -INFINITY;
         }
 
-        // tile maximum per head across the 128 rows
+        // tile maximum per head across the 2 x 128 rows
+        const int rb = it & 1;
+        float wm[8];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float wm = warp_max(sc_[h]);
-          if (lane == 0) red[(sb * 4 + warp) * 8 + h] = wm;
+        for (int h = 0; h < 8; ++h) wm[h] = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < G; ++h) wm[h] = warp_max(fmaxf(sc_[0][h], sc_[1][h]));
+        if (lane == 0) {
+          float4 *dst = reinterpret_cast<float4 *>(red + (rb * 4 + warp) * 8);
+          dst[0] = make_float4(wm[0], wm[1], wm[2], wm[3]);
+          if (G > 4) dst[1] = make_float4(wm[4], wm[5], wm[6], wm[7]);
         }
         named_barrier_sync(1, NCT);
         bool need = false;
-        float tmax[G];
+        float tmax[8];
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          tmax[h] = fmaxf(fmaxf(red[(sb * 4 + 0) * 8 + h], red[(sb * 4 + 1) * 8 + h]),
-                          fmaxf(red[(sb * 4 + 2) * 8 + h], red[(sb * 4 + 3) * 8 + h]));
-          need |= tmax[h] > m_ref[h] + kRescaleLog2;
+        for (int h = 0; h < 8; ++h) tmax[h] = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const float4 *src = reinterpret_cast<const float4 *>(red + (rb * 4 + w) * 8);
+          const float4 a = src[0];
+          tmax[0] = fmaxf(tmax[0], a.x); tmax[1] = fmaxf(tmax[1], a.y);
+          tmax[2] = fmaxf(tmax[2], a.z); tmax[3] = fmaxf(tmax[3], a.w);
+          if (G > 4) {
+            const float4 b4 = src[1];
+            tmax[4] = fmaxf(tmax[4], b4.x); tmax[5] = fmaxf(tmax[5], b4.y);
+            tmax[6] = fmaxf(tmax[6], b4.z); tmax[7] = fmaxf(tmax[7], b4.w);
+          }
         }
+#pragma unroll
+        for (int h = 0; h < G; ++h) need |= tmax[h] > m_ref[h] + kRescaleLog2;
         if (need) {
           float alpha[8];
 #pragma unroll
@@ -890,61 +985,53 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
             tc_fence_before();
           }
         }
-        // probabilities, rounded to bf16 as the tensor cores will see them
-        // (8-bit cache: times the token's V scale; the sum takes them unscaled)
-        uint32_t packed[4] = {0, 0, 0, 0};
-        const unsigned char *vst = smem + L::OFF_V + vslot * L::STAGE;
-        float vscale = 1.f;
-        if constexpr (FP8) {
-          wait_or_abort(&full_v[vslot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
-          vscale = *reinterpret_cast<const float *>(vst + (t >> 3) * L::GROUP + 1024 + (t & 7) * 4);
-        }
+        // probabilities, rounded as the tensor cores will see them (bf16, or
+        // f16 beside the 8-bit cache's f16 V; p <= 2^8 either way)
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float pv = valid ? exp2f(sc_[h] - m_ref[h]) : 0.f;
-          __nv_bfloat16 pb;
-          if constexpr (FP8) {
-            pb = __float2bfloat16_rn(valid ? pv * vscale : 0.f);
-            l_part[h] += pv;
-          } else {
-            pb = __float2bfloat16_rn(pv);
-            l_part[h] += __bfloat162float(pb);
-          }
-          packed[h >> 1] |= (uint32_t)__bfloat16_as_ushort(pb) << ((h & 1) * 16);
-        }
-        wait_or_abort(&p_free[sb], ((uint32_t)(s >> 1) & 1u) ^ 1u, abort_flag, p.err);
-        *reinterpret_cast<uint4 *>(smem + L::OFF_P + sb * P_BYTES + (t >> 3) * 256 + (t & 7) * 16) =
-            make_uint4(packed[0], packed[1], packed[2], packed[3]);
-        if constexpr (FP8) {
-          // this token's V row, E4M3 -> bf16, into the operand of parity sb
-          // (free: p_free says the p.v that last read it has completed); rows
-          // that are not valid tokens become zeros
-          const unsigned char *src = vst + (t >> 3) * L::GROUP + (t & 7) * 16;
-          unsigned char *dst = smem + L::OFF_VB + sb * (TOK * 256) + (t >> 3) * 2048 + (t & 7) * 16;
+        for (int u = 0; u < 2; ++u) {
+          if (u < n2) {
+            const int su = s + u, pbuf = su & 1;
+            uint32_t packed[4] = {0, 0, 0, 0};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-            if (valid) e4m3x16_to_bf16(*reinterpret_cast<const uint4 *>(src + c * 128), lo, hi);
-            *reinterpret_cast<uint4 *>(dst + (2 * c) * 128) = lo;
-            *reinterpret_cast<uint4 *>(dst + (2 * c + 1) * 128) = hi;
-          }
-        } else if (nvalid < TOK || mask) {
-          // rows that are not valid tokens must not feed NaN/Inf into p.v
-          wait_or_abort(&full_v[vslot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
-          if (!valid) {
-            uint4 *vrow = reinterpret_cast<uint4 *>(smem + L::OFF_V + vslot * L::STAGE +
-                                                    (t >> 3) * 2048 + (t & 7) * 16);
+            for (int h = 0; h < G; ++h) {
+              const float pv = valid[u] ? exp2f(sc_[u][h] - m_ref[h]) : 0.f;
+              uint16_t bits;
+              if constexpr (FP8) {
+                const __half ph = __float2half_rn(pv);
+                l_part[h] += __half2float(ph);
+                bits = __half_as_ushort(ph);
+              } else {
+                const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
+                l_part[h] += __bfloat162float(pb);
+                bits = __bfloat16_as_ushort(pb);
+              }
+              packed[h >> 1] |= (uint32_t)bits << ((h & 1) * 16);
+            }
+            wait_or_abort(&p_free[pbuf], ((uint32_t)(su >> 1) & 1u) ^ 1u, abort_flag, p.err);
+            *reinterpret_cast<uint4 *>(smem + L::OFF_P + pbuf * P_BYTES + (t >> 3) * 256 +
+                                       (t & 7) * 16) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            if (!FP8 && (!valid[u] || msk[u])) {
+              // rows that are not valid tokens must not feed NaN/Inf into p.v
+              const int vslot = su % L::NSV;
+              wait_or_abort(&full_v[vslot], (uint32_t)(su / L::NSV) & 1u, abort_flag, p.err);
+              if (!valid[u]) {
+                uint4 *vrow = reinterpret_cast<uint4 *>(smem + L::OFF_V + vslot * L::STAGE +
+                                                        (t >> 3) * 2048 + (t & 7) * 16);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) vrow[c * 8] = make_uint4(0, 0, 0, 0);
+                for (int c = 0; c < 16; ++c) vrow[c * 8] = make_uint4(0, 0, 0, 0);
+              }
+            }
           }
         }
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (FP8) mbar_arrive(&empty_v[vslot]);
-          mbar_arrive(&p_full[sb]);
+          mbar_arrive(&p_full[s & 1]);
+          if (n2 > 1) mbar_arrive(&p_full[(s + 1) & 1]);
         }
+        s += n2;
       }
 
       // ---- end of segment: hand the segment's reference maxima and per-warp
@@ -962,7 +1049,7 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
       if (lane == 0) mbar_arrive(&seg_done[ob]);
       ++k;
     }
-  } else {
+  } else if (warp < WARP_CVT) {
     // ---------------------------------------------------------- epilogue
     const int e = tid - 32 * WARP_EPI;  // 0..127: head-dim row of O
     const int ew = warp - WARP_EPI;     // TMEM lane quadrant
@@ -1027,7 +1114,9 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
           const size_t row0 = ((size_t)unit + (size_t)c_first) * G;
           float2 *mlb = reinterpret_cast<float2 *>(smem + L::OFF_MERGE);
           constexpr int PPB = MERGE_PAIRS / G;  // parts per (max, sum) batch
-          constexpr int GP = 64 / G;            // parts per group of loads in flight
+          // parts per group of loads in flight (fewer under the 8-bit
+          // kernel's 128-register budget)
+          constexpr int GP = (FP8 ? 16 : 64) / G;
           float Mx[G], Lm[G], O[G];
 #pragma unroll
           for (int h = 0; h < G; ++h) { Mx[h] = -INFINITY; Lm[h] = 0.f; O[h] = 0.f; }
@@ -1089,6 +1178,54 @@ __global__ void __launch_bounds__(THREADS, 1) paged_attention_kernel(const AttnP
       }
       ++k;
     }
+  } else if constexpr (FP8) {
+    // ------------------------------------------------ V converters (8-bit)
+    // NPART threads per token row t of each stage, each a part of the row:
+    // they dequantise the codes (code * scale, f16) into the p.v operand of
+    // parity s & 1 once the p.v that last read that buffer has completed,
+    // and zero rows that are not valid tokens (past the context, or in a
+    // block whose id was bad).
+    constexpr int NPART = NCVT * 32 / TOK, NCH = 8 / NPART;  // 16-dim chunks per thread
+    const int ct = tid - 32 * WARP_CVT;
+    const int t = ct & (TOK - 1), part = ct / TOK;
+    SegCursor cur(sc);
+    Segment sg;
+    int s = 0;
+    while (cur.next(sc, p.B, sg)) {
+      const int ctx_b = __ldg(p.ctx + sg.b);
+      const int nstages = (sg.n + SB - 1) / SB;
+      for (int st = 0; st < nstages; ++st, ++s) {
+        const int vslot = s % L::NSV, sb = s & 1;
+        const int nb = min(SB, sg.n - st * SB);
+        int nvalid = nb * BS;
+        if (sg.j0 + st * SB + nb == sg.nblk) nvalid -= sg.nblk * BS - ctx_b;  // unit's last block
+        wait_or_abort(&full_v[vslot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
+        const bool valid = (t < nvalid) && !((vmask[vslot] >> (t / BS)) & 1);
+        const unsigned char *grp = smem + L::OFF_V + vslot * L::STAGE + (t >> 3) * L::GROUP;
+        const __half2 vs2 =
+            __float2half2_rn(*reinterpret_cast<const float *>(grp + 1024 + (t & 7) * 4));
+        uint4 codes[NCH];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i)
+          codes[i] = *reinterpret_cast<const uint4 *>(grp + (NCH * part + i) * 128 + (t & 7) * 16);
+        wait_or_abort(&p_free[sb], ((uint32_t)(s >> 1) & 1u) ^ 1u, abort_flag, p.err);
+        unsigned char *dst = smem + L::OFF_VB + sb * (TOK * 256) + (t >> 3) * 2048 + (t & 7) * 16;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          const int c = NCH * part + i;  // 16-dim chunk
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+          if (valid) e4m3x16_dequant_f16(codes[i], vs2, lo, hi);
+          *reinterpret_cast<uint4 *>(dst + (2 * c) * 128) = lo;
+          *reinterpret_cast<uint4 *>(dst + (2 * c + 1) * 128) = hi;
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&empty_v[vslot]);
+          mbar_arrive(&vb_full[sb]);
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -1125,7 +1262,7 @@ static cudaError_t launch_cfg(const AttnParams &p, int grid, cudaStream_t stream
   // prologue while the previous kernel finishes (see pdl_wait above).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(THREADS);
+  cfg.blockDim = dim3(kThreads<FP8>);
   cfg.dynamicSmemBytes = smem_bytes<FP8>(p.B);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1141,7 +1278,8 @@ static int occupancy_cfg(int B) {
   if (ensure_smem_limit<G, BS, FP8>() != cudaSuccess) return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_attention_kernel<G, BS, FP8>,
-                                                    THREADS, smem_bytes<FP8>(B)) != cudaSuccess)
+                                                    kThreads<FP8>, smem_bytes<FP8>(B)) !=
+      cudaSuccess)
     return 0;
   return n;
 }

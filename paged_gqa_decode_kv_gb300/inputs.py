@@ -370,7 +370,7 @@ def kv_bytes_read(batch: PagedBatch, unique: bool = False) -> int:
     if batch.kv_format == "fp8":
         per_head += 4
     per_token = 2 * batch.n_kv * per_head
-    assert batch.k_cache.dim() == 6
+    assert batch.k_cache.dim() == (4 if batch.kv_format == "fp8" else 6)
     if not unique:
         return int(batch.context_lens.sum().item()) * per_token
     bs = batch.block_size
