@@ -592,6 +592,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   int *nmax_slot = reinterpret_cast<int *>(smem + L::OFF_MISC + 20);
   volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 40);  // [8]
   volatile int *vmask = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 72);       // [NSV]
+  int *over_flag = reinterpret_cast<int *>(smem + L::OFF_MISC + 96);  // [2][4] softmax votes
   int *pre = reinterpret_cast<int *>(smem + L::OFF_PRE);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -931,38 +932,46 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
               sc_[u][h] = valid[u] ? __uint_as_float(sv[u][h]) * p.qk_scale_log2 : -INFINITY;
         }
 
-        // tile maximum per head across the 2 x 128 rows
+        // Does any score of the 2 x 128 rows exceed its head's reference by
+        // more than 2^8?  (Always at a segment's first iteration, where the
+        // reference is -inf; rarely after.)  One vote per warp; only then are
+        // the exact tile maxima reduced and the reference moved.
         const int rb = it & 1;
-        float wm[8];
+        bool over = false;
 #pragma unroll
-        for (int h = 0; h < 8; ++h) wm[h] = -INFINITY;
-#pragma unroll
-        for (int h = 0; h < G; ++h) wm[h] = warp_max(fmaxf(sc_[0][h], sc_[1][h]));
-        if (lane == 0) {
-          float4 *dst = reinterpret_cast<float4 *>(red + (rb * 4 + warp) * 8);
-          dst[0] = make_float4(wm[0], wm[1], wm[2], wm[3]);
-          if (G > 4) dst[1] = make_float4(wm[4], wm[5], wm[6], wm[7]);
-        }
+        for (int h = 0; h < G; ++h)
+          over |= fmaxf(sc_[0][h], sc_[1][h]) > m_ref[h] + kRescaleLog2;
+        const bool wover = __any_sync(kFullMask, over);
+        if (lane == 0) over_flag[rb * 4 + warp] = wover ? 1 : 0;
         named_barrier_sync(1, NCT);
-        bool need = false;
-        float tmax[8];
+        const int4 votes = *reinterpret_cast<const int4 *>(over_flag + rb * 4);
+        if (votes.x | votes.y | votes.z | votes.w) {
+          float wm[8];
 #pragma unroll
-        for (int h = 0; h < 8; ++h) tmax[h] = -INFINITY;
+          for (int h = 0; h < 8; ++h) wm[h] = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float4 *src = reinterpret_cast<const float4 *>(red + (rb * 4 + w) * 8);
-          const float4 a = src[0];
-          tmax[0] = fmaxf(tmax[0], a.x); tmax[1] = fmaxf(tmax[1], a.y);
-          tmax[2] = fmaxf(tmax[2], a.z); tmax[3] = fmaxf(tmax[3], a.w);
-          if (G > 4) {
-            const float4 b4 = src[1];
-            tmax[4] = fmaxf(tmax[4], b4.x); tmax[5] = fmaxf(tmax[5], b4.y);
-            tmax[6] = fmaxf(tmax[6], b4.z); tmax[7] = fmaxf(tmax[7], b4.w);
+          for (int h = 0; h < G; ++h) wm[h] = warp_max(fmaxf(sc_[0][h], sc_[1][h]));
+          if (lane == 0) {
+            float4 *dst = reinterpret_cast<float4 *>(red + (rb * 4 + warp) * 8);
+            dst[0] = make_float4(wm[0], wm[1], wm[2], wm[3]);
+            if (G > 4) dst[1] = make_float4(wm[4], wm[5], wm[6], wm[7]);
           }
-        }
+          named_barrier_sync(1, NCT);
+          float tmax[8];
 #pragma unroll
-        for (int h = 0; h < G; ++h) need |= tmax[h] > m_ref[h] + kRescaleLog2;
-        if (need) {
+          for (int h = 0; h < 8; ++h) tmax[h] = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const float4 *src = reinterpret_cast<const float4 *>(red + (rb * 4 + w) * 8);
+            const float4 a = src[0];
+            tmax[0] = fmaxf(tmax[0], a.x); tmax[1] = fmaxf(tmax[1], a.y);
+            tmax[2] = fmaxf(tmax[2], a.z); tmax[3] = fmaxf(tmax[3], a.w);
+            if (G > 4) {
+              const float4 b4 = src[1];
+              tmax[4] = fmaxf(tmax[4], b4.x); tmax[5] = fmaxf(tmax[5], b4.y);
+              tmax[6] = fmaxf(tmax[6], b4.z); tmax[7] = fmaxf(tmax[7], b4.w);
+            }
+          }
           float alpha[8];
 #pragma unroll
           for (int h = 0; h < 8; ++h) alpha[h] = 1.f;
