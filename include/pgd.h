@@ -210,6 +210,47 @@ pgd_status pgd_append_decode_attention(void *out, const void *q, const void *k_n
                                        void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* cascade: shared prefixes read once per group                            */
+/* ---------------------------------------------------------------------- */
+/* pgd_paged_decode_attention for a batch in which groups of sequences share
+ * their leading blocks ("Module 10", section "Share only identical state":
+ * sequences point at the same read-only prefix blocks; same page: sharing
+ * the storage does not by itself share the traffic).  Same definition,
+ * arguments, rules and result; the work is split in two passes merged by
+ * log-sum-exp ("The math of Transformer inference", section 8; "LLM
+ * inference systems engineering", 2.8.3):
+ *   1. for each group and KV head, each shared prefix tile is read once and
+ *      multiplied against all of the group's query rows together on the
+ *      tensor cores (up to 128 rows = sequences x G per pass; larger groups
+ *      take several), giving a partial state per (sequence, query head);
+ *   2. each sequence's own suffix is attended as pgd_paged_decode_attention
+ *      does, and its output merges the prefix's partial states.
+ * Groups (device int32 arrays of n_groups entries): sequences
+ * group_first[i] .. group_first[i] + group_size[i] - 1 (consecutive; a
+ * sequence in at most one group) share their first group_blocks[i] block
+ * table entries (the same physical block ids, read from the table of
+ * group_first[i]).  seq_prefix_blocks (device int32 [B]) gives each
+ * sequence's shared block count: group_blocks of its group, or 0.  Every
+ * sequence must keep at least one block after its shared ones
+ * (context_lens[b] > seq_prefix_blocks[b] * bs; else PGD_DEVERR_BAD_CONTEXT).
+ * max_group_size and max_group_blocks are host upper bounds of group_size
+ * and group_blocks (they size the grid and the workspace).  workspace: at
+ * least pgd_cascade_workspace_size(...) bytes, 256-byte aligned, zero-filled
+ * before first use.  bf16 pools only.  The shared-prefix pass and the
+ * suffix pass are two kernels; the second starts while the first runs and
+ * waits for it only before merging. */
+size_t pgd_cascade_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                  int32_t num_splits, int32_t max_group_size,
+                                  int32_t max_group_blocks);
+pgd_status pgd_cascade_decode_attention(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, const int32_t *seq_prefix_blocks,
+    const int32_t *group_first, const int32_t *group_size, const int32_t *group_blocks,
+    int32_t n_groups, int32_t max_group_size, int32_t max_group_blocks, int32_t B, int32_t n_q,
+    int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB, float scale, int32_t num_splits,
+    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* 8-bit KV cache: FP8 E4M3 codes with one fp32 scale per (token, head)    */
 /* ---------------------------------------------------------------------- */
 /* Storing the cache in 8 bits halves its memory and the bytes a decode step

@@ -11,6 +11,7 @@ from ._native import (  # noqa: F401
     PGDError, BlockAllocator, kv_append, paged_decode_attention,
     paged_decode_attention_noalloc, append_decode_attention, decode_step, copy_blocks,
     kv_append_fp8, paged_decode_attention_fp8, append_decode_attention_fp8,
+    cascade_decode_attention, cascade_workspace_size,
     device_errors, workspace_size, make_workspace, attention_grid, validate_tables, lib,
     library_path)
 
@@ -19,6 +20,6 @@ __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload",
            "BlockAllocator", "kv_append", "paged_decode_attention",
            "paged_decode_attention_noalloc", "append_decode_attention", "decode_step",
            "copy_blocks", "kv_append_fp8", "paged_decode_attention_fp8",
-           "append_decode_attention_fp8",
+           "append_decode_attention_fp8", "cascade_decode_attention", "cascade_workspace_size",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
            "validate_tables", "lib", "library_path"]

@@ -38,6 +38,9 @@ SIGNATURES = {
                                             _F, _I, _P], _I),
     "pgd_append_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      _F, _I, _P, _Z, _P], _I),
+    "pgd_cascade_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _Z),
+    "pgd_cascade_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                      _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P], _I),
     "pgd_kv_append_fp8": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P], _I),
     "pgd_paged_decode_attention_fp8": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                         _I, _P, _Z, _P], _I),
@@ -246,6 +249,44 @@ def decode_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_
         _ptr(v_cache), _ptr(block_tables), B, n_q, n_kv, d, bs, MB, NB, float(scale),
         int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+# ---------------------------------------------------------------- cascade
+def cascade_workspace_size(B: int, n_q: int, n_kv: int, bs: int, max_group_size: int,
+                           max_group_blocks: int, num_splits: int = 0, d: int = HEAD_DIM) -> int:
+    return int(lib().pgd_cascade_workspace_size(B, n_q, n_kv, d, bs, num_splits, max_group_size,
+                                                max_group_blocks))
+
+
+def cascade_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens,
+                             seq_prefix_blocks, group_first, group_size, group_blocks,
+                             max_group_size: int, max_group_blocks: int, scale: float,
+                             num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """Paged decode attention with shared prefixes read once per group (see
+    pgd_cascade_decode_attention); group arrays are device int32."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    for t, n in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                 (seq_prefix_blocks, "seq_prefix_blocks"), (group_first, "group_first"),
+                 (group_size, "group_size"), (group_blocks, "group_blocks")):
+        _need(t, torch.int32, n)
+    B, n_q, d = q.shape
+    NB, n_kv, bs, _ = _cache_dims(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        n = cascade_workspace_size(B, n_q, n_kv, bs, max_group_size, max_group_blocks, num_splits)
+        workspace = torch.zeros(max(1, n), dtype=torch.uint8, device=q.device)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_cascade_decode_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(seq_prefix_blocks), _ptr(group_first), _ptr(group_size), _ptr(group_blocks),
+        group_first.numel(), int(max_group_size), int(max_group_blocks), B, n_q, n_kv, d, bs, MB,
+        NB, float(scale), int(num_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
 
 
 # ------------------------------------------------------------ 8-bit KV cache

@@ -22,6 +22,8 @@ cudaError_t attention_launch(const AttnParams &p, int G, int bs, int grid, cudaS
 int attention_ctas_per_sm_fp8(int G, int bs, int B);
 cudaError_t attention_launch_fp8(const AttnParams &p, int G, int bs, int grid,
                                  cudaStream_t stream);
+cudaError_t prefix_attention_launch(const PrefixParams &p, int G, int bs, int grid,
+                                    cudaStream_t stream);
 cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
                                  void *v_cache, const int32_t *tables, const int32_t *pos,
                                  int pos_offset, int B, int n_kv, int bs, int MB, int NB,
@@ -229,6 +231,10 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.err = err;
   p.wait_late = 0;
+  p.seq_prefix_blocks = nullptr;
+  p.pre_ml = nullptr;
+  p.pre_o = nullptr;
+  p.n_tsplit = 0;
   pa->p = p;
   pa->G = G;
   pa->bs = bs;
@@ -281,6 +287,28 @@ pgd_status append_then_attend(void *out, const void *q, const void *k_new, const
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   pa.p.wait_late = 1;
   return launch_prepared(pa, stream);
+}
+
+// Cascade plan: the shared-prefix pass splits each group's prefix into
+// n_tsplit parts (about 4 MMA stages of 128 tokens each, at most 16) and each
+// group's sequences into chunks of 128 / G.
+struct CascadePlan {
+  int n_tsplit, n_rchunk;
+  size_t pre_ml, pre_o, total;  // byte offsets / size past the decode workspace
+};
+
+CascadePlan cascade_plan(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t max_group_size,
+                         int32_t max_group_blocks, size_t decode_bytes) {
+  CascadePlan c;
+  const int G = n_q / n_kv;
+  const long long stages = ((long long)max_group_blocks * bs + 127) / 128;
+  c.n_tsplit = (int)std::max(1LL, std::min(16LL, stages / 4));
+  c.n_rchunk = std::max(1, (max_group_size * G + 127) / 128);
+  const size_t rows = (size_t)B * n_q * c.n_tsplit;
+  c.pre_ml = round_up(decode_bytes, kWsAlign);
+  c.pre_o = c.pre_ml + round_up(rows * 2 * 4, kWsAlign);
+  c.total = c.pre_o + rows * kHeadDim * 4;
+  return c;
 }
 
 }  // namespace
@@ -408,6 +436,81 @@ pgd_status pgd_append_decode_attention(void *out, const void *q, const void *k_n
   s = append_then_attend(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, B,
                          n_q, n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes,
                          static_cast<cudaStream_t>(stream));
+  return s == PGD_OK ? ok() : s;
+}
+
+// -------------------------------------------------- cascade (shared prefix)
+
+size_t pgd_cascade_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                  int32_t num_splits, int32_t max_group_size,
+                                  int32_t max_group_blocks) {
+  if (max_group_size < 0 || max_group_blocks < 0 || bs <= 0) return 0;
+  const size_t dec = pgd_attention_workspace_size(B, n_q, n_kv, d, num_splits);
+  if (dec == 0) return 0;
+  return cascade_plan(B, n_q, n_kv, bs, max_group_size, max_group_blocks, dec).total;
+}
+
+pgd_status pgd_cascade_decode_attention(
+    void *out, const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_tables, const int32_t *context_lens, const int32_t *seq_prefix_blocks,
+    const int32_t *group_first, const int32_t *group_size, const int32_t *group_blocks,
+    int32_t n_groups, int32_t max_group_size, int32_t max_group_blocks, int32_t B, int32_t n_q,
+    int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB, float scale, int32_t num_splits,
+    void *workspace, size_t workspace_bytes, void *stream) {
+  pgd_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, B,
+                                      n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  if (n_groups < 0 || max_group_size < 0 || max_group_blocks < 0 || max_group_blocks > MB ||
+      (n_groups > 0 && (max_group_size < 1 || max_group_size > B)))
+    return fail(PGD_ERR_INVALID_ARG, "bad group bounds");
+  if ((long long)n_groups * n_kv * 16 * ((max_group_size * (n_q / n_kv) + 127) / 128) > (1LL << 30))
+    return fail(PGD_ERR_INVALID_ARG, "too many groups");
+  if (n_groups > 0 && (!seq_prefix_blocks || !group_first || !group_size || !group_blocks))
+    return fail(PGD_ERR_INVALID_ARG, "null group array");
+  if (!workspace || !aligned(workspace, kWsAlign))
+    return fail(PGD_ERR_WORKSPACE, "workspace is NULL or not 256-aligned");
+  const size_t dec = pgd_attention_workspace_size(B, n_q, n_kv, d, num_splits);
+  const CascadePlan plan = cascade_plan(B, n_q, n_kv, bs, max_group_size, max_group_blocks, dec);
+  if (workspace_bytes < plan.total)
+    return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, plan.total);
+  PreparedAttention pa;
+  s = prepare_attention(out, q, k_cache, v_cache, block_tables, context_lens, B, n_q, n_kv, bs, MB,
+                        NB, scale, num_splits, workspace, dec, &pa);
+  if (s != PGD_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n_groups > 0) {
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    PrefixParams pp;
+    pp.q = static_cast<const __nv_bfloat16 *>(q);
+    pp.k_cache = static_cast<const unsigned char *>(k_cache);
+    pp.v_cache = static_cast<const unsigned char *>(v_cache);
+    pp.tables = block_tables;
+    pp.group_first = group_first;
+    pp.group_size = group_size;
+    pp.group_blocks = group_blocks;
+    pp.n_groups = n_groups;
+    pp.B = B;
+    pp.n_q = n_q;
+    pp.n_kv = n_kv;
+    pp.MB = MB;
+    pp.NB = NB;
+    pp.n_rchunk = plan.n_rchunk;
+    pp.n_tsplit = plan.n_tsplit;
+    pp.qk_scale_log2 = pa.p.qk_scale_log2;
+    pp.pre_ml = reinterpret_cast<float *>(ws + plan.pre_ml);
+    pp.pre_o = reinterpret_cast<float *>(ws + plan.pre_o);
+    pp.err = pa.p.err;
+    const int grid = n_groups * n_kv * plan.n_rchunk * plan.n_tsplit;
+    cudaError_t e = prefix_attention_launch(pp, pa.G, bs, grid, st);
+    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix pass launch");
+    pa.p.seq_prefix_blocks = seq_prefix_blocks;
+    pa.p.pre_ml = pp.pre_ml;
+    pa.p.pre_o = pp.pre_o;
+    pa.p.n_tsplit = plan.n_tsplit;
+    pa.p.wait_late = 2;
+  }
+  s = launch_prepared(pa, st);
   return s == PGD_OK ? ok() : s;
 }
 

@@ -342,6 +342,12 @@ struct Schedule {
   }
 };
 
+// First block of sequence b that this kernel attends (the blocks before it
+// were attended by the shared-prefix pass of a cascade call).
+__device__ __forceinline__ int start_block(const AttnParams &p, int b) {
+  return p.seq_prefix_blocks ? __ldg(p.seq_prefix_blocks + b) : 0;
+}
+
 // A role's walk over the CTA's part, one segment (the piece of the part
 // inside one unit) at a time.  Every role walks the same segments.
 struct SegCursor {
@@ -441,7 +447,7 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
                               : make_uint4(0, 0, 0, 0);
       }
     }
-    const int32_t *trow = p.tables + (size_t)g.b * p.MB + g.j0;
+    const int32_t *trow = p.tables + (size_t)g.b * p.MB + start_block(p, g.b) + g.j0;
     a.tab = (lane < g.n) ? __ldg(trow + lane) : 0;
     a.tab_next = (32 + lane < g.n) ? __ldg(trow + 32 + lane) : 0;
   };
@@ -451,7 +457,7 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
   Ahead cur_a{}, next_a{};
   bool have = cur.next(sc, p.B, sg);
   if (have) load_ahead(sg, cur_a);
-  if (p.wait_late) pdl_wait();  // kv_append has written the caches
+  if (p.wait_late == 1) pdl_wait();  // kv_append has written the caches
   int s = 0, k = 0;
   while (have) {
     const bool have_next = cur.next(sc, p.B, nsg);
@@ -500,7 +506,7 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
       if (lane == 0) mbar_arrive(&q_ready[qb]);
     }
     ++k;
-    const int32_t *trow = p.tables + (size_t)sg.b * p.MB + sg.j0;
+    const int32_t *trow = p.tables + (size_t)sg.b * p.MB + start_block(p, sg.b) + sg.j0;
     int tab = cur_a.tab, tab_next = cur_a.tab_next;
     int tchunk = 0;
     const int nstages = (sg.n + SB - 1) / SB;
@@ -647,7 +653,9 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     const int c = p.ctx[b];
     int nb = 0;
     if (c >= 1 && c <= max_tokens) nb = (c + BS - 1) / BS; else bad_ctx = true;
-    pre[b + 1] = nb;
+    const int s0 = start_block(p, b);
+    if (s0 < 0 || (nb > 0 && s0 >= nb)) bad_ctx = true;  // the suffix must keep >= 1 block
+    pre[b + 1] = (s0 >= 0 && s0 < nb) ? nb - s0 : 0;
   }
   if (bad_ctx && blockIdx.x == 0) atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
   if (warp == WARP_QK) {
@@ -833,6 +841,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     int s = 0, k = 0, it = 0;
     while (cur.next(sc, p.B, sg)) {
       const int ctx_b = __ldg(p.ctx + sg.b);
+      const int sb0 = start_block(p, sg.b);
       const int nstages = (sg.n + SB - 1) / SB;
       const int ob = k & 1;
       float m_ref[G], l_part[G];
@@ -864,7 +873,8 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             msk[u] = stage_mask[su & 7];
             const int nb = min(SB, sg.n - (st + u) * SB);
             int nvalid = nb * BS;
-            if (sg.j0 + (st + u) * SB + nb == sg.nblk) nvalid -= sg.nblk * BS - ctx_b;  // last block
+            if (sg.j0 + (st + u) * SB + nb == sg.nblk)  // the sequence's last block
+              nvalid -= (sg.nblk + sb0) * BS - ctx_b;
             valid[u] = (t < nvalid) && !((msk[u] >> (t / BS)) & 1);
           }
         }
@@ -1088,7 +1098,11 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
       if (lane == 0) mbar_arrive(&o_free[ob]);
 
       const long long seg_start = sg.unit_start + sg.j0;
-      const bool whole = (seg_start == sg.unit_start) && (seg_start + sg.n == sg.unit_end);
+      // a cascade unit with a shared prefix always merges: its prefix
+      // partial states come from the shared-prefix pass
+      const bool has_prefix = p.pre_ml != nullptr && start_block(p, sg.b) > 0;
+      const bool whole = (seg_start == sg.unit_start) && (seg_start + sg.n == sg.unit_end) &&
+                         !has_prefix;
       const size_t out_row = (size_t)sg.b * p.n_q + (size_t)sg.g * G;
       if (whole) {
 #pragma unroll
@@ -1106,8 +1120,9 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         __threadfence();
         named_barrier_sync(2, NET);
         if (e == 0) {
-          const long long c_first = sc.part_of(sg.unit_start);
-          const long long c_last = sc.part_of(sg.unit_end - 1);
+          // (whole-unit parts: the unit's only part is this CTA's)
+          const long long c_first = sc.units ? (long long)part : sc.part_of(sg.unit_start);
+          const long long c_last = sc.units ? (long long)part : sc.part_of(sg.unit_end - 1);
           const int n_parts = (int)(c_last - c_first + 1);
           const int before = atomicAdd(p.counters + unit, 1);
           const int last = (before == n_parts - 1);
@@ -1179,6 +1194,26 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             }
             named_barrier_sync(2, NET);  // mlb is reused by the next batch
           }
+          if (has_prefix) {
+            // the shared-prefix pass's parts of these rows (written by the
+            // previous kernel: wait for it first)
+            if (p.wait_late == 2) pdl_wait();
+            for (int ts = 0; ts < p.n_tsplit; ++ts) {
+#pragma unroll
+              for (int h = 0; h < G; ++h) {
+                const size_t pr = ((size_t)sg.b * p.n_q + (size_t)sg.g * G + h) * p.n_tsplit + ts;
+                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.pre_ml) + pr);
+                const float o = __ldcg(p.pre_o + pr * kHeadDim + e);
+                if (ml.x == -INFINITY) continue;
+                const float nm = fmaxf(Mx[h], ml.x);
+                const float ca = (Mx[h] == -INFINITY) ? 0.f : exp2f(Mx[h] - nm);
+                const float cb = exp2f(ml.x - nm);
+                Lm[h] = Lm[h] * ca + ml.y * cb;
+                O[h] = O[h] * ca + o * cb;
+                Mx[h] = nm;
+              }
+            }
+          }
 #pragma unroll
           for (int h = 0; h < G; ++h)
             p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(O[h] / Lm[h]);
@@ -1202,12 +1237,14 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     int s = 0;
     while (cur.next(sc, p.B, sg)) {
       const int ctx_b = __ldg(p.ctx + sg.b);
+      const int sb0 = start_block(p, sg.b);
       const int nstages = (sg.n + SB - 1) / SB;
       for (int st = 0; st < nstages; ++st, ++s) {
         const int vslot = s % L::NSV, sb = s & 1;
         const int nb = min(SB, sg.n - st * SB);
         int nvalid = nb * BS;
-        if (sg.j0 + st * SB + nb == sg.nblk) nvalid -= sg.nblk * BS - ctx_b;  // unit's last block
+        if (sg.j0 + st * SB + nb == sg.nblk)  // the sequence's last block
+          nvalid -= (sg.nblk + sb0) * BS - ctx_b;
         wait_or_abort(&full_v[vslot], (uint32_t)(s / L::NSV) & 1u, abort_flag, p.err);
         const bool valid = (t < nvalid) && !((vmask[vslot] >> (t / BS)) & 1);
         const unsigned char *grp = smem + L::OFF_V + vslot * L::STAGE + (t >> 3) * L::GROUP;

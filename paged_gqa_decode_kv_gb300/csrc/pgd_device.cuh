@@ -137,8 +137,35 @@ struct AttnParams {
   int32_t *counters;             // [B * n_kv]     arrivals per split unit
   int auto_split;                // 1: whole units or balanced cuts, chosen per call
   int wait_late;                 // 1: the previous kernel wrote only the caches (kv_append):
-                                 //    wait for it just before the first cache read
+                                 //    wait for it just before the first cache read;
+                                 // 2: it is the shared-prefix pass: wait for it only before
+                                 //    merging its partial states
+  // cascade (all null / 0 otherwise): sequence b's first seq_prefix_blocks[b]
+  // blocks were attended by the shared-prefix pass, whose partial states for
+  // (b, h) are pre_ml / pre_o[(b * n_q + h) * n_tsplit + part]
+  const int32_t *seq_prefix_blocks;
+  const float *pre_ml;
+  const float *pre_o;
+  int n_tsplit;
   int32_t *err;                  // device error word
+};
+
+// Shared-prefix pass of cascade attention (prefix_attention.cu).
+struct PrefixParams {
+  const __nv_bfloat16 *q;        // [B][n_q][D]
+  const unsigned char *k_cache;  // bf16 tiled pools
+  const unsigned char *v_cache;
+  const int32_t *tables;         // [B][MB]
+  const int32_t *group_first;    // [n_groups] first sequence of each group
+  const int32_t *group_size;     // [n_groups] sequences in the group (consecutive)
+  const int32_t *group_blocks;   // [n_groups] leading table blocks shared by the group
+  int n_groups, B, n_q, n_kv, MB, NB;
+  int n_rchunk;                  // chunks of 128 / G sequences per group
+  int n_tsplit;                  // parts of each prefix
+  float qk_scale_log2;
+  float *pre_ml;                 // [B][n_q][n_tsplit][2]   partial (max, sum), log2 domain
+  float *pre_o;                  // [B][n_q][n_tsplit][D]   unnormalised partial outputs
+  int32_t *err;
 };
 
 }  // namespace pgd

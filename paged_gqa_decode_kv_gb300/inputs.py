@@ -378,3 +378,23 @@ def kv_bytes_read(batch: PagedBatch, unique: bool = False) -> int:
     shared_tokens = batch.shared_blocks * bs
     total = shared_tokens + sum(c - shared_tokens for c in lens) if batch.shared_blocks else sum(lens)
     return total * per_token
+
+
+def prefix_groups(batch: PagedBatch, groups):
+    """Group arrays for cascade attention, as int32 tensors on the batch's
+    device.  groups: list of (first sequence, number of sequences, shared
+    blocks); the listed sequences must share those leading table entries
+    (true of any sequences of a batch built with shared_prefix, up to its
+    shared block count).  Returns (seq_prefix_blocks [B], group_first,
+    group_size, group_blocks, max_group_size, max_group_blocks)."""
+    dev = batch.q.device
+    seq = [0] * batch.batch
+    for first, size, blocks in groups:
+        for b in range(first, first + size):
+            seq[b] = blocks
+    t = lambda v: torch.tensor(v, dtype=torch.int32, device=dev)
+    firsts = [g[0] for g in groups]
+    sizes = [g[1] for g in groups]
+    blocks = [g[2] for g in groups]
+    return (t(seq), t(firsts), t(sizes), t(blocks), max(sizes, default=0),
+            max(blocks, default=0))
