@@ -52,6 +52,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--workload", default="batch16_ctx8192")
     ap.add_argument("--splits", type=int, default=0, help="0 = automatic")
+    ap.add_argument("--cascade", action="store_true",
+                    help="shared-prefix workloads: read each shared prefix once per group "
+                         "(pgd_cascade_decode_attention)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="cache format: bf16, or FP8 E4M3 codes + per-(token, head) scales")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -291,10 +294,30 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pb = inputs.make_workload(args.workload, device=dev, append=True, kv_format=args.kv)
+    B, n_q, n_kv = pb.batch, pb.n_q, pb.n_kv
     fp8 = args.kv == "fp8"
     append_attend = pgd.append_decode_attention_fp8 if fp8 else pgd.append_decode_attention
     attend = pgd.paged_decode_attention_fp8 if fp8 else pgd.paged_decode_attention
-    B, n_q, n_kv = pb.batch, pb.n_q, pb.n_kv
+    if args.cascade:
+        if fp8 or not pb.shared_blocks:
+            raise SystemExit("--cascade needs a bf16 shared-prefix workload")
+        groups = inputs.prefix_groups(pb, [(0, B, pb.shared_blocks)])
+        cws = torch.zeros(pgd.cascade_workspace_size(B, n_q, n_kv, pb.block_size, groups[4],
+                                                     groups[5], args.splits),
+                          dtype=torch.uint8, device=dev)
+
+        def attend(out_, q_, kc, vc, tables, lens, scale, num_splits=0, workspace=None,
+                   stream=None):
+            return pgd.cascade_decode_attention(out_, q_, kc, vc, tables, lens, *groups[:4],
+                                                groups[4], groups[5], scale,
+                                                num_splits=num_splits, workspace=cws,
+                                                stream=stream)
+
+        def append_attend(out_, q_, kn, vn, kc, vc, tables, lens, scale, num_splits=0,
+                          workspace=None, stream=None):
+            pgd.kv_append(kn, vn, kc, vc, tables, pb.positions, stream=stream)
+            return attend(out_, q_, kc, vc, tables, lens, scale, num_splits=num_splits,
+                          stream=stream)
     ws = pgd.make_workspace(B, n_q, n_kv, args.splits, dev)
     out = torch.empty_like(pb.q)
     grid = pgd.attention_grid(B, n_q, n_kv, pb.block_size, args.splits)
@@ -412,7 +435,8 @@ def run_ours(args, rank, world, local):
         "data": ("synthetic (seeded E4M3 K/V codes + per-token scales, N(0,1) bf16 Q, random "
                  "block tables)") if fp8 else
                 "synthetic (seeded N(0,1) bf16 K/V/Q, random block tables)",
-        "config": config_block(pb, args.workload, args.splits, n_pools),
+        "config": dict(config_block(pb, args.workload, args.splits, n_pools),
+                       **({"cascade": True} if args.cascade else {})),
         "grid_ctas": grid,
         "kv_bytes_per_step": kv_bytes,
         "kv_bytes_per_step_logical": kv_bytes_logical,
@@ -422,16 +446,20 @@ def run_ours(args, rank, world, local):
         "pct_of_hbm_peak": {"nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
                             peak_kind: round(100 * value / world / peak, 2)},
         "roofline": {"bound": "hbm",
-                     "kernel": "pgd::tc::paged_attention_kernel<G, bs, %s> (tcgen05)"
+                     "kernel": ("pgd::pf::prefix_attention_kernel + pgd::tc::paged_attention_kernel"
+                                " (cascade, tcgen05)") if args.cascade else
+                               "pgd::tc::paged_attention_kernel<G, bs, %s> (tcgen05)"
                                % ("fp8" if fp8 else "bf16"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": profiled_traffic(args.kv, args.workload),
+                     "traffic": None if args.cascade else profiled_traffic(args.kv, args.workload),
                      "launch_ms": round(attn_ms, 5),
                      "bytes_per_launch": kv_bytes},
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5)},
-        "gpu_launches": 2 * K,  # kv_append + attention per timed step
+        "e2e": dict({"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5)},
+                    **({"path": "pgd_decode_step (host buffers; no cascade)"}
+                       if args.cascade else {})),
+        "gpu_launches": (3 if args.cascade else 2) * K,  # kv_append (+ prefix pass) + attention
         "clocks": sampler.summary(t_wall0, t_wall1),
         "gpu": torch.cuda.get_device_name(local),
     }

@@ -24,6 +24,7 @@ cudaError_t attention_launch_fp8(const AttnParams &p, int G, int bs, int grid,
                                  cudaStream_t stream);
 cudaError_t prefix_attention_launch(const PrefixParams &p, int G, int bs, int grid,
                                     cudaStream_t stream);
+cudaError_t cascade_combine_launch(const CombineParams &p, int G, cudaStream_t stream);
 cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
                                  void *v_cache, const int32_t *tables, const int32_t *pos,
                                  int pos_offset, int B, int n_kv, int bs, int MB, int NB,
@@ -235,6 +236,7 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   p.pre_ml = nullptr;
   p.pre_o = nullptr;
   p.n_tsplit = 0;
+  p.part_info = nullptr;
   pa->p = p;
   pa->G = G;
   pa->bs = bs;
@@ -289,25 +291,42 @@ pgd_status append_then_attend(void *out, const void *q, const void *k_new, const
   return launch_prepared(pa, stream);
 }
 
-// Cascade plan: the shared-prefix pass splits each group's prefix into
-// n_tsplit parts (about 4 MMA stages of 128 tokens each, at most 16) and each
-// group's sequences into chunks of 128 / G.
+// Cascade plan: the shared-prefix pass cuts each group's sequences into
+// chunks of 128 / G and each group's prefix into n_tsplit parts -- enough
+// parts for the pass to cover the GPU (at most 16, at least one 128-token
+// stage each).
 struct CascadePlan {
   int n_tsplit, n_rchunk;
-  size_t pre_ml, pre_o, total;  // byte offsets / size past the decode workspace
+  size_t pre_ml, pre_o, part_info, total;  // byte offsets / size past the decode workspace
 };
 
-CascadePlan cascade_plan(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t max_group_size,
-                         int32_t max_group_blocks, size_t decode_bytes) {
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+CascadePlan cascade_plan(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t n_groups,
+                         int32_t max_group_size, int32_t max_group_blocks, size_t decode_bytes,
+                         int sms) {
   CascadePlan c;
   const int G = n_q / n_kv;
-  const long long stages = ((long long)max_group_blocks * bs + 127) / 128;
-  c.n_tsplit = (int)std::max(1LL, std::min(16LL, stages / 4));
+  const long long stages = std::max(1LL, ((long long)max_group_blocks * bs + 127) / 128);
   c.n_rchunk = std::max(1, (max_group_size * G + 127) / 128);
+  const long long items = std::max(1LL, (long long)std::max(n_groups, 1) * n_kv * c.n_rchunk);
+  c.n_tsplit = (int)std::max(1LL, std::min({16LL, stages, (sms + items - 1) / items}));
   const size_t rows = (size_t)B * n_q * c.n_tsplit;
   c.pre_ml = round_up(decode_bytes, kWsAlign);
   c.pre_o = c.pre_ml + round_up(rows * 2 * 4, kWsAlign);
-  c.total = c.pre_o + rows * kHeadDim * 4;
+  c.part_info = c.pre_o + round_up(rows * kHeadDim * 4, kWsAlign);
+  c.total = c.part_info + (size_t)B * n_kv * 8;
   return c;
 }
 
@@ -447,7 +466,8 @@ size_t pgd_cascade_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_t 
   if (max_group_size < 0 || max_group_blocks < 0 || bs <= 0) return 0;
   const size_t dec = pgd_attention_workspace_size(B, n_q, n_kv, d, num_splits);
   if (dec == 0) return 0;
-  return cascade_plan(B, n_q, n_kv, bs, max_group_size, max_group_blocks, dec).total;
+  // (sized for the largest split of the prefix: one group)
+  return cascade_plan(B, n_q, n_kv, bs, 1, max_group_size, max_group_blocks, dec, 1 << 20).total;
 }
 
 pgd_status pgd_cascade_decode_attention(
@@ -471,7 +491,8 @@ pgd_status pgd_cascade_decode_attention(
   if (!workspace || !aligned(workspace, kWsAlign))
     return fail(PGD_ERR_WORKSPACE, "workspace is NULL or not 256-aligned");
   const size_t dec = pgd_attention_workspace_size(B, n_q, n_kv, d, num_splits);
-  const CascadePlan plan = cascade_plan(B, n_q, n_kv, bs, max_group_size, max_group_blocks, dec);
+  const CascadePlan plan =
+      cascade_plan(B, n_q, n_kv, bs, n_groups, max_group_size, max_group_blocks, dec, sm_count());
   if (workspace_bytes < plan.total)
     return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, plan.total);
   PreparedAttention pa;
@@ -508,10 +529,30 @@ pgd_status pgd_cascade_decode_attention(
     pa.p.pre_ml = pp.pre_ml;
     pa.p.pre_o = pp.pre_o;
     pa.p.n_tsplit = plan.n_tsplit;
+    pa.p.part_info = reinterpret_cast<int2 *>(ws + plan.part_info);
     pa.p.wait_late = 2;
   }
   s = launch_prepared(pa, st);
-  return s == PGD_OK ? ok() : s;
+  if (s != PGD_OK || n_groups == 0) return s == PGD_OK ? ok() : s;
+  CombineParams cp;
+  cp.out = pa.p.out;
+  cp.seq_prefix_blocks = seq_prefix_blocks;
+  cp.part_ml = pa.p.part_ml;
+  cp.part_o = pa.p.part_o;
+  cp.part_info = pa.p.part_info;
+  cp.pre_ml = pa.p.pre_ml;
+  cp.pre_o = pa.p.pre_o;
+  cp.B = B;
+  cp.n_q = n_q;
+  cp.n_kv = n_kv;
+  cp.n_tsplit = plan.n_tsplit;
+  cp.ctx = context_lens;
+  cp.bs = bs;
+  cp.MB = MB;
+  cp.parts = pa.grid;
+  cudaError_t e = cascade_combine_launch(cp, pa.G, st);
+  if (e != cudaSuccess) return cuda_fail(e, "cascade combine launch");
+  return ok();
 }
 
 // ------------------------------------------------------------- 8-bit cache

@@ -1108,6 +1108,21 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
 #pragma unroll
         for (int h = 0; h < G; ++h)
           p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(ov[h] / Lsum[h]);
+      } else if (has_prefix && p.part_info) {
+        // cascade unit: the combine kernel merges all its parts; record
+        // where they are (every part writes the same pair)
+        const size_t srow = ((size_t)unit + (size_t)part) * G;
+#pragma unroll
+        for (int h = 0; h < G; ++h) p.part_o[(srow + h) * kHeadDim + e] = ov[h];
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          if (e == h)
+            *reinterpret_cast<float2 *>(p.part_ml + (srow + h) * 2) = make_float2(M[h], Lsum[h]);
+        if (e == 0) {
+          const long long c_first = sc.units ? (long long)part : sc.part_of(sg.unit_start);
+          const long long c_last = sc.units ? (long long)part : sc.part_of(sg.unit_end - 1);
+          p.part_info[unit] = make_int2((int)c_first, (int)(c_last - c_first + 1));
+        }
       } else {
         const size_t srow = ((size_t)unit + (size_t)part) * G;
 #pragma unroll
@@ -1198,20 +1213,34 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             // the shared-prefix pass's parts of these rows (written by the
             // previous kernel: wait for it first)
             if (p.wait_late == 2) pdl_wait();
-            for (int ts = 0; ts < p.n_tsplit; ++ts) {
+            // PPG parts at a time, every load of a group issued before use
+            constexpr int PPG = 4;
+            for (int t0 = 0; t0 < p.n_tsplit; t0 += PPG) {
+              float2 ml[PPG][G];
+              float o[PPG][G];
 #pragma unroll
-              for (int h = 0; h < G; ++h) {
-                const size_t pr = ((size_t)sg.b * p.n_q + (size_t)sg.g * G + h) * p.n_tsplit + ts;
-                const float2 ml = __ldcg(reinterpret_cast<const float2 *>(p.pre_ml) + pr);
-                const float o = __ldcg(p.pre_o + pr * kHeadDim + e);
-                if (ml.x == -INFINITY) continue;
-                const float nm = fmaxf(Mx[h], ml.x);
-                const float ca = (Mx[h] == -INFINITY) ? 0.f : exp2f(Mx[h] - nm);
-                const float cb = exp2f(ml.x - nm);
-                Lm[h] = Lm[h] * ca + ml.y * cb;
-                O[h] = O[h] * ca + o * cb;
-                Mx[h] = nm;
-              }
+              for (int i = 0; i < PPG; ++i)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                  const bool in = t0 + i < p.n_tsplit;
+                  const size_t pr =
+                      ((size_t)sg.b * p.n_q + (size_t)sg.g * G + h) * p.n_tsplit + (in ? t0 + i : 0);
+                  ml[i][h] = in ? __ldcg(reinterpret_cast<const float2 *>(p.pre_ml) + pr)
+                                : make_float2(-INFINITY, 0.f);
+                  o[i][h] = in ? __ldcg(p.pre_o + pr * kHeadDim + e) : 0.f;
+                }
+#pragma unroll
+              for (int i = 0; i < PPG; ++i)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                  if (ml[i][h].x == -INFINITY) continue;
+                  const float nm = fmaxf(Mx[h], ml[i][h].x);
+                  const float ca = (Mx[h] == -INFINITY) ? 0.f : exp2f(Mx[h] - nm);
+                  const float cb = exp2f(ml[i][h].x - nm);
+                  Lm[h] = Lm[h] * ca + ml[i][h].y * cb;
+                  O[h] = O[h] * ca + o[i][h] * cb;
+                  Mx[h] = nm;
+                }
             }
           }
 #pragma unroll
@@ -1274,6 +1303,9 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     }
   }
 
+  // (cascade: this grid completes only after the shared-prefix pass, so the
+  // combine kernel that waits on it sees both passes' parts)
+  if (p.wait_late == 2) pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

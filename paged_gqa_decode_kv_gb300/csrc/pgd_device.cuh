@@ -147,7 +147,23 @@ struct AttnParams {
   const float *pre_ml;
   const float *pre_o;
   int n_tsplit;
+  int2 *part_info;               // cascade: per unit (first part, parts); such units are
+                                 // merged with their prefix parts by the combine kernel
   int32_t *err;                  // device error word
+};
+
+// Final merge of cascade attention (prefix_attention.cu): decode parts of
+// each unit with a shared prefix, then the prefix parts, into the output.
+struct CombineParams {
+  __nv_bfloat16 *out;
+  const int32_t *seq_prefix_blocks;
+  const float *part_ml, *part_o;   // decode parts [slots][G][2] / [slots][G][D]
+  const int2 *part_info;           // [units] (first part, parts)
+  const float *pre_ml, *pre_o;     // prefix parts [B][n_q][n_tsplit][2] / [..][D]
+  const int32_t *ctx;              // context lengths [B]
+  int B, n_q, n_kv, n_tsplit;
+  int bs, MB;                      // block size, blocks per table row
+  int parts;                       // parts of the suffix pass (its grid)
 };
 
 // Shared-prefix pass of cascade attention (prefix_attention.cu).

@@ -429,7 +429,94 @@ static cudaError_t launch_g(const PrefixParams &p, int grid, cudaStream_t stream
   return cudaLaunchKernelEx(&cfg, prefix_attention_kernel<G, BS>, p);
 }
 
+// Final merge of a cascade call: one CTA per unit (sequence, KV head) with a
+// shared prefix, one thread per output dim: the unit's suffix parts, then its
+// prefix parts, combined by log-sum-exp into the bf16 output.
+template <int G>
+__global__ void __launch_bounds__(kHeadDim) cascade_combine_kernel(const CombineParams p) {
+  pdl_wait();  // the suffix pass, which waits for the prefix pass, has completed
+  const int unit = (int)blockIdx.x;
+  const int b = unit / p.n_kv, g = unit % p.n_kv;
+  if (b >= p.B) return;
+  // Sequences the suffix pass rejected (flagged there) have no parts.
+  const int s0 = __ldg(p.seq_prefix_blocks + b), c = __ldg(p.ctx + b);
+  if (s0 <= 0 || c < 1 || c > p.MB * p.bs || s0 >= (c + p.bs - 1) / p.bs) return;
+  const int e = threadIdx.x;
+  const int2 info = __ldcg(p.part_info + unit);
+  if (info.x < 0 || info.y < 1 || info.x + info.y > p.parts) return;
+  float Mx[G], Lm[G], O[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) { Mx[h] = -INFINITY; Lm[h] = 0.f; O[h] = 0.f; }
+  auto fold = [&](int h, float2 ml, float o) {
+    if (ml.x == -INFINITY) return;
+    const float nm = fmaxf(Mx[h], ml.x);
+    const float ca = (Mx[h] == -INFINITY) ? 0.f : exp2f(Mx[h] - nm);
+    const float cb = exp2f(ml.x - nm);
+    Lm[h] = Lm[h] * ca + ml.y * cb;
+    O[h] = O[h] * ca + o * cb;
+    Mx[h] = nm;
+  };
+  constexpr int PPG = 4;  // parts per group of loads in flight
+  const int n_dec = info.y;
+  for (int i0 = 0; i0 < n_dec + p.n_tsplit; i0 += PPG) {
+    float2 ml[PPG][G];
+    float o[PPG][G];
+#pragma unroll
+    for (int i = 0; i < PPG; ++i) {
+      const int j = i0 + i;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        if (j < n_dec) {
+          const size_t row = ((size_t)unit + (size_t)(info.x + j)) * G + h;
+          ml[i][h] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + row);
+          o[i][h] = __ldcg(p.part_o + row * kHeadDim + e);
+        } else if (j < n_dec + p.n_tsplit) {
+          const size_t pr = ((size_t)b * p.n_q + (size_t)g * G + h) * p.n_tsplit + (j - n_dec);
+          ml[i][h] = __ldcg(reinterpret_cast<const float2 *>(p.pre_ml) + pr);
+          o[i][h] = __ldcg(p.pre_o + pr * kHeadDim + e);
+        } else {
+          ml[i][h] = make_float2(-INFINITY, 0.f);
+          o[i][h] = 0.f;
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < PPG; ++i)
+#pragma unroll
+      for (int h = 0; h < G; ++h) fold(h, ml[i][h], o[i][h]);
+  }
+  const size_t orow = (size_t)b * p.n_q + (size_t)g * G;
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+    p.out[(orow + h) * kHeadDim + e] = __float2bfloat16_rn(O[h] / Lm[h]);
+}
+
+template <int G>
+static cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * p.n_kv));
+  cfg.blockDim = dim3(kHeadDim);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, cascade_combine_kernel<G>, p);
+}
+
 }  // namespace pf
+
+cudaError_t cascade_combine_launch(const CombineParams &p, int G, cudaStream_t stream) {
+  switch (G) {
+    case 1: return pf::launch_combine<1>(p, stream);
+    case 2: return pf::launch_combine<2>(p, stream);
+    case 4: return pf::launch_combine<4>(p, stream);
+    case 8: return pf::launch_combine<8>(p, stream);
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t prefix_attention_launch(const PrefixParams &p, int G, int bs, int grid,
                                     cudaStream_t stream) {
