@@ -237,6 +237,7 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   p.pre_o = nullptr;
   p.n_tsplit = 0;
   p.part_info = nullptr;
+  p.trigger_early = 0;
   pa->p = p;
   pa->G = G;
   pa->bs = bs;
@@ -500,48 +501,58 @@ pgd_status pgd_cascade_decode_attention(
                         NB, scale, num_splits, workspace, dec, &pa);
   if (s != PGD_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (n_groups > 0) {
-    unsigned char *ws = static_cast<unsigned char *>(workspace);
-    PrefixParams pp;
-    pp.q = static_cast<const __nv_bfloat16 *>(q);
-    pp.k_cache = static_cast<const unsigned char *>(k_cache);
-    pp.v_cache = static_cast<const unsigned char *>(v_cache);
-    pp.tables = block_tables;
-    pp.group_first = group_first;
-    pp.group_size = group_size;
-    pp.group_blocks = group_blocks;
-    pp.n_groups = n_groups;
-    pp.B = B;
-    pp.n_q = n_q;
-    pp.n_kv = n_kv;
-    pp.MB = MB;
-    pp.NB = NB;
-    pp.n_rchunk = plan.n_rchunk;
-    pp.n_tsplit = plan.n_tsplit;
-    pp.qk_scale_log2 = pa.p.qk_scale_log2;
-    pp.pre_ml = reinterpret_cast<float *>(ws + plan.pre_ml);
-    pp.pre_o = reinterpret_cast<float *>(ws + plan.pre_o);
-    pp.err = pa.p.err;
-    const int grid = n_groups * n_kv * plan.n_rchunk * plan.n_tsplit;
-    cudaError_t e = prefix_attention_launch(pp, pa.G, bs, grid, st);
-    if (e != cudaSuccess) return cuda_fail(e, "shared-prefix pass launch");
-    pa.p.seq_prefix_blocks = seq_prefix_blocks;
-    pa.p.pre_ml = pp.pre_ml;
-    pa.p.pre_o = pp.pre_o;
-    pa.p.n_tsplit = plan.n_tsplit;
-    pa.p.part_info = reinterpret_cast<int2 *>(ws + plan.part_info);
-    pa.p.wait_late = 2;
+  if (n_groups == 0) {
+    s = launch_prepared(pa, st);
+    return s == PGD_OK ? ok() : s;
   }
+  // 1. suffix pass: each sequence's own blocks, partial states only; it lets
+  //    the prefix pass launch once it has waited for its inputs
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  float *pre_ml = reinterpret_cast<float *>(ws + plan.pre_ml);
+  float *pre_o = reinterpret_cast<float *>(ws + plan.pre_o);
+  pa.p.seq_prefix_blocks = seq_prefix_blocks;
+  pa.p.pre_ml = pre_ml;
+  pa.p.pre_o = pre_o;
+  pa.p.n_tsplit = plan.n_tsplit;
+  pa.p.part_info = reinterpret_cast<int2 *>(ws + plan.part_info);
+  pa.p.trigger_early = 1;
   s = launch_prepared(pa, st);
-  if (s != PGD_OK || n_groups == 0) return s == PGD_OK ? ok() : s;
+  if (s != PGD_OK) return s;
+  // 2. shared-prefix pass: its CTAs take the SMs the suffix pass frees; it
+  //    completes only after the suffix pass
+  PrefixParams pp;
+  pp.q = static_cast<const __nv_bfloat16 *>(q);
+  pp.k_cache = static_cast<const unsigned char *>(k_cache);
+  pp.v_cache = static_cast<const unsigned char *>(v_cache);
+  pp.tables = block_tables;
+  pp.group_first = group_first;
+  pp.group_size = group_size;
+  pp.group_blocks = group_blocks;
+  pp.n_groups = n_groups;
+  pp.B = B;
+  pp.n_q = n_q;
+  pp.n_kv = n_kv;
+  pp.MB = MB;
+  pp.NB = NB;
+  pp.n_rchunk = plan.n_rchunk;
+  pp.n_tsplit = plan.n_tsplit;
+  pp.wait_at_end = 1;
+  pp.qk_scale_log2 = pa.p.qk_scale_log2;
+  pp.pre_ml = pre_ml;
+  pp.pre_o = pre_o;
+  pp.err = pa.p.err;
+  const int grid = n_groups * n_kv * plan.n_rchunk * plan.n_tsplit;
+  cudaError_t e = prefix_attention_launch(pp, pa.G, bs, grid, st);
+  if (e != cudaSuccess) return cuda_fail(e, "shared-prefix pass launch");
+  // 3. combine: suffix and prefix parts of every unit with a shared prefix
   CombineParams cp;
   cp.out = pa.p.out;
   cp.seq_prefix_blocks = seq_prefix_blocks;
   cp.part_ml = pa.p.part_ml;
   cp.part_o = pa.p.part_o;
   cp.part_info = pa.p.part_info;
-  cp.pre_ml = pa.p.pre_ml;
-  cp.pre_o = pa.p.pre_o;
+  cp.pre_ml = pre_ml;
+  cp.pre_o = pre_o;
   cp.B = B;
   cp.n_q = n_q;
   cp.n_kv = n_kv;
@@ -550,7 +561,7 @@ pgd_status pgd_cascade_decode_attention(
   cp.bs = bs;
   cp.MB = MB;
   cp.parts = pa.grid;
-  cudaError_t e = cascade_combine_launch(cp, pa.G, st);
+  e = cascade_combine_launch(cp, pa.G, st);
   if (e != cudaSuccess) return cuda_fail(e, "cascade combine launch");
   return ok();
 }

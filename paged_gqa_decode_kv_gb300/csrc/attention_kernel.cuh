@@ -114,6 +114,9 @@ constexpr float kRescaleLog2 = 8.f;         // move the reference when exceeded 
 // (per kind of cache: three 64 KiB bf16 stages, or four 33 KiB 8-bit ones)
 template <bool FP8> constexpr long long kCtaShare = FP8 ? 140 : 96;
 constexpr long long kMergeBytes = 32ll << 20;
+// Fixed cost of a segment in blocks of streaming time: about two stages
+// (measured on a batch of short sequences).
+template <int BS> constexpr int kSegCost = 2 * TOK / BS;
 constexpr int MERGE_PAIRS = 128;
 constexpr int SMEM_SLACK = 1024;
 
@@ -257,23 +260,43 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
       : "memory");
 }
 
-__device__ __forceinline__ float warp_max(float v) {
+template <int G> constexpr int kLog2 = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+
+// Max (or sum) over the warp of G per-lane values, one per head, with the
+// values halved at each of the first log2(G) exchange steps (a lane keeps one
+// half and sends the other), so G - 1 + 5 - log2(G) shuffles instead of 5 G.
+// Lane l returns the result of head l >> (5 - log2(G)).
+template <int G, bool MAX>
+__device__ __forceinline__ float warp_reduce_heads(const float (&v)[G], int lane) {
+  float a[G];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFullMask, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_sum(float v) {
+  for (int i = 0; i < G; ++i) a[i] = v[i];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFullMask, v, o);
-  return v;
+  for (int n = G, off = 16; n > 1; n >>= 1, off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float keep = up ? a[i + n / 2] : a[i];
+      const float send = up ? a[i] : a[i + n / 2];
+      const float r = __shfl_xor_sync(kFullMask, send, off);
+      a[i] = MAX ? fmaxf(keep, r) : keep + r;
+    }
+  }
+#pragma unroll
+  for (int off = 16 >> kLog2<G>; off > 0; off >>= 1) {
+    const float r = __shfl_xor_sync(kFullMask, a[0], off);
+    a[0] = MAX ? fmaxf(a[0], r) : a[0] + r;
+  }
+  return a[0];
 }
 
 // Bounded wait that gives up at once after any earlier timeout in the CTA, so
 // that the control flow (and every named barrier) is the same for all threads
 // whatever happens.
-__device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity,
+// (The spin is a function of its own: one copy of it instead of one per
+// wait keeps the kernel's code small enough for the instruction caches.)
+static __device__ __noinline__ void wait_spin(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, int32_t *err) {
-  if (mbar_try_wait(bar, parity)) return;
   if (*abort_flag) return;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -288,41 +311,31 @@ __device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity,
     }
   }
 }
-
-struct Segment {
-  int b, g, j0, nblk, n;
-  long long unit_start, unit_end;
-};
-
-__device__ __forceinline__ Segment locate(const int *pre, int B, int n_kv, long long x,
-                                          long long x_end) {
-  int lo = 0, hi = B - 1;  // largest b with n_kv * pre[b] <= x
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)n_kv * pre[mid] <= x) lo = mid; else hi = mid - 1;
-  }
-  Segment s;
-  s.b = lo;
-  s.nblk = pre[lo + 1] - pre[lo];
-  const long long base = (long long)n_kv * pre[lo];
-  const long long r = x - base;
-  s.g = (int)(r / s.nblk);
-  s.j0 = (int)(r % s.nblk);
-  s.unit_start = base + (long long)s.g * s.nblk;
-  s.unit_end = s.unit_start + s.nblk;
-  const long long e = x_end < s.unit_end ? x_end : s.unit_end;
-  s.n = (int)(e - x);
-  return s;
+__device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort_flag, int32_t *err) {
+  if (!mbar_try_wait(bar, parity)) wait_spin(bar, parity, abort_flag, err);
 }
 
+// The piece of a CTA's part inside one unit (sequence b, KV head g): blocks
+// j0 .. j0 + n - 1 of the nblk blocks the kernel attends for sequence b; the
+// unit spans [ucs, uce) of the cost space.
+struct Segment {
+  int b, g, j0, nblk, n;
+  long long ucs, uce;
+};
+
 // Parts of one call: part c (taken by CTA c) is a contiguous range of the
-// flattened block space, in index order; a closed form of c, so every thread
-// can map a part to its range and a block position to its part.
+// flattened cost space, in index order; a closed form of c, so every thread
+// can map a part to its range and a cost position to its part.  Each unit
+// costs its blocks plus ov: the ov positions in front of its first block
+// stand for the fixed time of starting a segment (latency the softmax and
+// epilogue pay per unit), so balanced cuts also balance the units per CTA.
 struct Schedule {
-  long long X;     // blocks in all units
+  long long X;     // cost of all units
   long long P;     // parts
   bool units;      // part c = unit c (else X * c / P balanced cuts)
-  const int *pre;  // blocks before sequence b
+  const int *pre;  // cost of one head of the sequences before b
+  int ov;          // cost of a unit beyond its blocks (0 for sequences without blocks)
   int n_kv;
   __device__ __forceinline__ void range(long long i, long long &a, long long &b) const {
     if (units) {
@@ -335,7 +348,7 @@ struct Schedule {
       b = X * (i + 1) / P;
     }
   }
-  // Part holding block position x (only needed for units that are cut,
+  // Part holding cost position x (only needed for units that are cut,
   // which happens in balanced mode alone).
   __device__ __forceinline__ long long part_of(long long x) const {
     return (P * (x + 1) - 1) / X;
@@ -349,18 +362,53 @@ __device__ __forceinline__ int start_block(const AttnParams &p, int b) {
 }
 
 // A role's walk over the CTA's part, one segment (the piece of the part
-// inside one unit) at a time.  Every role walks the same segments.
+// inside one unit that holds blocks) at a time.  Every role walks the same
+// segments.  Only the first unit is found by search; the cursor then steps
+// to the next unit (next head, or the next sequence with blocks).
 struct SegCursor {
-  long long x, b;  // rest of the part
+  long long x, end;  // rest of the part
+  int b, g;          // unit of the last segment (b = -1 before the first)
   __device__ __forceinline__ SegCursor(const Schedule &sc) {
-    x = b = 0;
-    if ((long long)blockIdx.x < sc.P) sc.range(blockIdx.x, x, b);
+    x = end = 0;
+    b = -1;
+    g = 0;
+    if ((long long)blockIdx.x < sc.P) sc.range(blockIdx.x, x, end);
   }
   __device__ __forceinline__ bool next(const Schedule &sc, int B, Segment &sg) {
-    if (x >= b) return false;
-    sg = locate(sc.pre, B, sc.n_kv, x, b);
-    x += sg.n;
-    return true;
+    const int *pre = sc.pre;
+    while (x < end) {
+      if (b < 0) {
+        int lo = 0, hi = B - 1;  // largest b with n_kv * pre[b] <= x
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if ((long long)sc.n_kv * pre[mid] <= x) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        const int cost = pre[b + 1] - pre[b];
+        g = (int)((x - (long long)sc.n_kv * pre[b]) / cost);
+      } else if (++g == sc.n_kv) {  // x is the start of the unit after (b, g)
+        g = 0;
+        do { ++b; } while (b < B - 1 && pre[b + 1] == pre[b]);
+      }
+      const int cost = pre[b + 1] - pre[b];
+      const long long ucs = (long long)sc.n_kv * pre[b] + (long long)g * cost;
+      const long long uce = ucs + cost;
+      const long long e = end < uce ? end : uce;
+      const int j0 = (int)max(0ll, x - ucs - sc.ov);
+      const int j1 = (int)max(0ll, e - ucs - sc.ov);
+      x = e;
+      if (j1 > j0) {
+        sg.b = b;
+        sg.g = g;
+        sg.j0 = j0;
+        sg.nblk = cost - sc.ov;
+        sg.n = j1 - j0;
+        sg.ucs = ucs;
+        sg.uce = uce;
+        return true;
+      }
+    }
+    return false;
   }
 };
 
@@ -558,6 +606,71 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
   }
 }
 
+// Last-arriver merge of a unit's n_parts partial states (parts c0 ..), by
+// log-sum-exp, into the bf16 output rows; run by the 128 epilogue threads,
+// thread e owning dim e.  The (max, sum) pairs are staged in shared memory
+// PPB parts at a time; the partial outputs are read U parts at a time, every
+// load of a group issued before any is used.  Cold (once per cut unit), so
+// out of line and not unrolled beyond one group.
+template <int G, bool FP8>
+__device__ __noinline__ void merge_parts(const float *__restrict__ part_o,
+                                         const float *__restrict__ part_ml,
+                                         __nv_bfloat16 *__restrict__ out, int unit, int c0,
+                                         int n_parts, size_t out_row, int e, float2 *mlb) {
+  constexpr int NET = 128;
+  constexpr int PPB = MERGE_PAIRS / G;
+  constexpr int U = (FP8 ? 16 : 32) / G;  // (fewer under the 8-bit kernel's register budget)
+  const size_t row0 = ((size_t)unit + (size_t)c0) * G;
+  float Mx[G], Lm[G], O[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) { Mx[h] = -INFINITY; Lm[h] = 0.f; O[h] = 0.f; }
+#pragma unroll 1
+  for (int base = 0; base < n_parts; base += PPB) {
+    const int nb = min(PPB, n_parts - base);
+    const size_t rb = row0 + (size_t)base * G;
+#pragma unroll 1
+    for (int j = e; j < nb * G; j += NET)
+      mlb[j] = __ldcg(reinterpret_cast<const float2 *>(part_ml) + rb + j);
+    named_barrier_sync(2, NET);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float bm = Mx[h];
+#pragma unroll 1
+      for (int i = 0; i < nb; ++i) bm = fmaxf(bm, mlb[i * G + h].x);
+      if (bm != Mx[h] && Mx[h] != -INFINITY) {
+        const float cf = exp2f(Mx[h] - bm);
+        Lm[h] *= cf;
+        O[h] *= cf;
+      }
+      Mx[h] = bm;
+    }
+#pragma unroll 1
+    for (int i0 = 0; i0 < nb; i0 += U) {
+      float ov[U][G];
+#pragma unroll
+      for (int i = 0; i < U; ++i)
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          ov[i][h] = (i0 + i < nb)
+                         ? __ldcg(part_o + (rb + (size_t)(i0 + i) * G + h) * kHeadDim + e)
+                         : 0.f;
+#pragma unroll
+      for (int i = 0; i < U; ++i)
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float2 ml = (i0 + i < nb) ? mlb[(i0 + i) * G + h] : make_float2(-INFINITY, 0.f);
+          const float cf = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx[h]);
+          Lm[h] = fmaf(cf, ml.y, Lm[h]);
+          O[h] = fmaf(cf, ov[i][h], O[h]);
+        }
+    }
+    named_barrier_sync(2, NET);  // mlb is reused by the next batch
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+    out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(O[h] / Lm[h]);
+}
+
 template <int G, int BS, bool FP8>
 __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const AttnParams p) {
   using L = Lay<FP8>;
@@ -606,6 +719,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   // the stream may still run.  Unless it is known to write only the caches,
   // wait for it before reading anything.
   if (!p.wait_late) pdl_wait();
+  if (p.trigger_early) pdl_launch_dependents();
 
   if (tid == 0) {
     // 8-bit cache: the softmax warps read each K stage's scales, so they too
@@ -655,7 +769,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     if (c >= 1 && c <= max_tokens) nb = (c + BS - 1) / BS; else bad_ctx = true;
     const int s0 = start_block(p, b);
     if (s0 < 0 || (nb > 0 && s0 >= nb)) bad_ctx = true;  // the suffix must keep >= 1 block
-    pre[b + 1] = (s0 >= 0 && s0 < nb) ? nb - s0 : 0;
+    pre[b + 1] = (s0 >= 0 && s0 < nb) ? nb - s0 + kSegCost<BS> : 0;
   }
   if (bad_ctx && blockIdx.x == 0) atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
   if (warp == WARP_QK) {
@@ -697,6 +811,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   sc.X = (long long)p.n_kv * pre[p.B];
   sc.pre = pre;
   sc.n_kv = p.n_kv;
+  sc.ov = kSegCost<BS>;
   sc.P = sc.X < (long long)gridDim.x ? sc.X : (long long)gridDim.x;
   sc.units = false;
   if (p.auto_split) {
@@ -790,10 +905,18 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
       Segment sg;
       int s = 0, k = 0;
       while (cur.next(sc, p.B, sg)) {
+        const int ctx_b = __ldg(p.ctx + sg.b);
+        const int sb0 = start_block(p, sg.b);
         const int nstages = (sg.n + SB - 1) / SB;
         const int ob = k & 1;
         for (int st = 0; st < nstages; ++st, ++s) {
           const int slot = s % L::NSV, sb = s & 1;
+          // k-steps past the sequence's last token are not issued (their
+          // rows hold no valid token and were never zeroed)
+          const int nb = min(SB, sg.n - st * SB);
+          int nvalid = nb * BS;
+          if (sg.j0 + st * SB + nb == sg.nblk) nvalid -= (sg.nblk + sb0) * BS - ctx_b;
+          const int nkt = min(8, max(1, (nvalid + 15) >> 4));
           wait_or_abort(&p_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
           if (FP8)  // V dequantised into the f16 buffer of parity sb
             wait_or_abort(&vb_full[sb], (uint32_t)(s >> 1) & 1u, abort_flag, p.err);
@@ -812,8 +935,9 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             const uint32_t acc0 = st > 0 ? 1u : 0u;
 #pragma unroll
             for (int kt = 0; kt < 8; ++kt)
-              umma_bf16(dO, vd + (uint64_t)(kt * 256), pd + (uint64_t)(kt * 32),
-                        FP8 ? IDESC_PV16 : IDESC_PV, kt > 0 ? 1u : acc0);
+              if (kt < nkt)
+                umma_bf16(dO, vd + (uint64_t)(kt * 256), pd + (uint64_t)(kt * 32),
+                          FP8 ? IDESC_PV16 : IDESC_PV, kt > 0 ? 1u : acc0);
           }
           if (!FP8) umma_commit(&empty_v[slot]);
           umma_commit(&p_free[sb]);  // P (and converted V) of parity sb reusable
@@ -837,11 +961,15 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     constexpr int NCT = 128;
     constexpr int NSC = FP8 ? 16 : 8;  // S columns per stage (8-bit: high and low parts)
     SegCursor cur(sc);
-    Segment sg;
+    Segment sg, nsg;
     int s = 0, k = 0, it = 0;
-    while (cur.next(sc, p.B, sg)) {
-      const int ctx_b = __ldg(p.ctx + sg.b);
-      const int sb0 = start_block(p, sg.b);
+    // each segment's context length and first block, loaded a segment ahead
+    bool have = cur.next(sc, p.B, sg);
+    int ctx_b = have ? __ldg(p.ctx + sg.b) : 0, sb0 = have ? start_block(p, sg.b) : 0;
+    while (have) {
+      const bool have_next = cur.next(sc, p.B, nsg);
+      const int ctx_n = have_next ? __ldg(p.ctx + nsg.b) : 0;
+      const int sb0_n = have_next ? start_block(p, nsg.b) : 0;
       const int nstages = (sg.n + SB - 1) / SB;
       const int ob = k & 1;
       float m_ref[G], l_part[G];
@@ -853,6 +981,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         const int n2 = min(2, nstages - st);  // stages in this iteration
         bool valid[2] = {false, false};
         int msk[2] = {0, 0};
+        int lim[2] = {0, 0};  // rows p.v reads: the valid length rounded up to 16
         // Invalid-block mask of each stage: the K producer wrote it before
         // arming full_k; the q.k^T issuer acquired full_k and then released
         // m_ready.  (Waiting on full_k here could alias under the bf16
@@ -876,6 +1005,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             if (sg.j0 + (st + u) * SB + nb == sg.nblk)  // the sequence's last block
               nvalid -= (sg.nblk + sb0) * BS - ctx_b;
             valid[u] = (t < nvalid) && !((msk[u] >> (t / BS)) & 1);
+            lim[u] = (nvalid + 15) & ~15;
           }
         }
         tc_fence_after();
@@ -943,29 +1073,29 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         }
 
         // Does any score of the 2 x 128 rows exceed its head's reference by
-        // more than 2^8?  (Always at a segment's first iteration, where the
-        // reference is -inf; rarely after.)  One vote per warp; only then are
-        // the exact tile maxima reduced and the reference moved.
+        // more than 2^8?  One vote per warp (rarely yes); only then are the
+        // exact tile maxima reduced and the reference moved.  A segment's
+        // first iteration, where the reference is -inf, moves it unasked.
         const int rb = it & 1;
-        bool over = false;
+        bool move = true;  // (a segment's first iteration always moves it)
+        if (st > 0) {
+          bool over = false;
 #pragma unroll
-        for (int h = 0; h < G; ++h)
-          over |= fmaxf(sc_[0][h], sc_[1][h]) > m_ref[h] + kRescaleLog2;
-        const bool wover = __any_sync(kFullMask, over);
-        if (lane == 0) over_flag[rb * 4 + warp] = wover ? 1 : 0;
-        named_barrier_sync(1, NCT);
-        const int4 votes = *reinterpret_cast<const int4 *>(over_flag + rb * 4);
-        if (votes.x | votes.y | votes.z | votes.w) {
-          float wm[8];
+          for (int h = 0; h < G; ++h)
+            over |= fmaxf(sc_[0][h], sc_[1][h]) > m_ref[h] + kRescaleLog2;
+          const bool wover = __any_sync(kFullMask, over);
+          if (lane == 0) over_flag[rb * 4 + warp] = wover ? 1 : 0;
+          named_barrier_sync(1, NCT);
+          const int4 votes = *reinterpret_cast<const int4 *>(over_flag + rb * 4);
+          move = (votes.x | votes.y | votes.z | votes.w) != 0;
+        }
+        if (move) {
+          float v2[G];
 #pragma unroll
-          for (int h = 0; h < 8; ++h) wm[h] = -INFINITY;
-#pragma unroll
-          for (int h = 0; h < G; ++h) wm[h] = warp_max(fmaxf(sc_[0][h], sc_[1][h]));
-          if (lane == 0) {
-            float4 *dst = reinterpret_cast<float4 *>(red + (rb * 4 + warp) * 8);
-            dst[0] = make_float4(wm[0], wm[1], wm[2], wm[3]);
-            if (G > 4) dst[1] = make_float4(wm[4], wm[5], wm[6], wm[7]);
-          }
+          for (int h = 0; h < G; ++h) v2[h] = fmaxf(sc_[0][h], sc_[1][h]);
+          const float wm = warp_reduce_heads<G, true>(v2, lane);
+          constexpr int SH = 5 - kLog2<G>;  // lanes per head after the reduction
+          if ((lane & ((1 << SH) - 1)) == 0) red[(rb * 4 + warp) * 8 + (lane >> SH)] = wm;
           named_barrier_sync(1, NCT);
           float tmax[8];
 #pragma unroll
@@ -1030,16 +1160,16 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             *reinterpret_cast<uint4 *>(smem + L::OFF_P + pbuf * P_BYTES + (t >> 3) * 256 +
                                        (t & 7) * 16) =
                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            if (!FP8 && (!valid[u] || msk[u])) {
-              // rows that are not valid tokens must not feed NaN/Inf into p.v
+            if (!FP8 && !valid[u] && t < lim[u]) {
+              // rows that p.v reads but that are not valid tokens (the tail
+              // of the last block, a block whose id was bad) must not feed
+              // NaN/Inf into it: zero them once their copy has landed
               const int vslot = su % L::NSV;
               wait_or_abort(&full_v[vslot], (uint32_t)(su / L::NSV) & 1u, abort_flag, p.err);
-              if (!valid[u]) {
-                uint4 *vrow = reinterpret_cast<uint4 *>(smem + L::OFF_V + vslot * L::STAGE +
-                                                        (t >> 3) * 2048 + (t & 7) * 16);
+              uint4 *vrow = reinterpret_cast<uint4 *>(smem + L::OFF_V + vslot * L::STAGE +
+                                                      (t >> 3) * 2048 + (t & 7) * 16);
 #pragma unroll
-                for (int c = 0; c < 16; ++c) vrow[c * 8] = make_uint4(0, 0, 0, 0);
-              }
+              for (int c = 0; c < 16; ++c) vrow[c * 8] = make_uint4(0, 0, 0, 0);
             }
           }
         }
@@ -1058,15 +1188,22 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
       // lred/mref[ob] were last read by the epilogue of segment k - 2, which
       // then released O buffer ob
       wait_or_abort(&o_free[ob], ((uint32_t)(k >> 1) & 1u) ^ 1u, abort_flag, p.err);
+      {
+        const float ws = warp_reduce_heads<G, false>(l_part, lane);
+        constexpr int SH = 5 - kLog2<G>;
+        if ((lane & ((1 << SH) - 1)) == 0) lred[(ob * 4 + warp) * 8 + (lane >> SH)] = ws;
+      }
+      if (t == 0) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float ws = warp_sum(l_part[h]);
-        if (lane == 0) lred[(ob * 4 + warp) * 8 + h] = ws;
-        if (t == 0) mref[ob * 8 + h] = m_ref[h];
+        for (int h = 0; h < G; ++h) mref[ob * 8 + h] = m_ref[h];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&seg_done[ob]);
       ++k;
+      sg = nsg;
+      ctx_b = ctx_n;
+      sb0 = sb0_n;
+      have = have_next;
     }
   } else if (warp < WARP_CVT) {
     // ---------------------------------------------------------- epilogue
@@ -1097,18 +1234,19 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[ob]);
 
-      const long long seg_start = sg.unit_start + sg.j0;
       // a cascade unit with a shared prefix always merges: its prefix
       // partial states come from the shared-prefix pass
       const bool has_prefix = p.pre_ml != nullptr && start_block(p, sg.b) > 0;
-      const bool whole = (seg_start == sg.unit_start) && (seg_start + sg.n == sg.unit_end) &&
-                         !has_prefix;
+      const bool whole = sg.j0 == 0 && sg.n == sg.nblk && !has_prefix;
+      // parts holding the unit's first and last blocks
+      const long long c_first = sc.units ? (long long)part : sc.part_of(sg.ucs + sc.ov);
+      const long long c_last = sc.units ? (long long)part : sc.part_of(sg.uce - 1);
       const size_t out_row = (size_t)sg.b * p.n_q + (size_t)sg.g * G;
       if (whole) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
           p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(ov[h] / Lsum[h]);
-      } else if (has_prefix && p.part_info) {
+      } else if (has_prefix) {
         // cascade unit: the combine kernel merges all its parts; record
         // where they are (every part writes the same pair)
         const size_t srow = ((size_t)unit + (size_t)part) * G;
@@ -1118,11 +1256,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         for (int h = 0; h < G; ++h)
           if (e == h)
             *reinterpret_cast<float2 *>(p.part_ml + (srow + h) * 2) = make_float2(M[h], Lsum[h]);
-        if (e == 0) {
-          const long long c_first = sc.units ? (long long)part : sc.part_of(sg.unit_start);
-          const long long c_last = sc.units ? (long long)part : sc.part_of(sg.unit_end - 1);
-          p.part_info[unit] = make_int2((int)c_first, (int)(c_last - c_first + 1));
-        }
+        if (e == 0) p.part_info[unit] = make_int2((int)c_first, (int)(c_last - c_first + 1));
       } else {
         const size_t srow = ((size_t)unit + (size_t)part) * G;
 #pragma unroll
@@ -1136,8 +1270,6 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         named_barrier_sync(2, NET);
         if (e == 0) {
           // (whole-unit parts: the unit's only part is this CTA's)
-          const long long c_first = sc.units ? (long long)part : sc.part_of(sg.unit_start);
-          const long long c_last = sc.units ? (long long)part : sc.part_of(sg.unit_end - 1);
           const int n_parts = (int)(c_last - c_first + 1);
           const int before = atomicAdd(p.counters + unit, 1);
           const int last = (before == n_parts - 1);
@@ -1149,103 +1281,8 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         named_barrier_sync(2, NET);
         if (flag[0]) {
           __threadfence();
-          const int c_first = flag[1], n_parts = flag[2];
-          const size_t row0 = ((size_t)unit + (size_t)c_first) * G;
-          float2 *mlb = reinterpret_cast<float2 *>(smem + L::OFF_MERGE);
-          constexpr int PPB = MERGE_PAIRS / G;  // parts per (max, sum) batch
-          // parts per group of loads in flight (fewer under the 8-bit
-          // kernel's 128-register budget)
-          constexpr int GP = (FP8 ? 16 : 64) / G;
-          float Mx[G], Lm[G], O[G];
-#pragma unroll
-          for (int h = 0; h < G; ++h) { Mx[h] = -INFINITY; Lm[h] = 0.f; O[h] = 0.f; }
-          for (int base = 0; base < n_parts; base += PPB) {
-            const int nb = min(PPB, n_parts - base);
-            const size_t rb = row0 + (size_t)base * G;
-            // Partial outputs are read GP parts at a time, all loads of a
-            // group issued before any is used; the first group's loads are
-            // in flight while the (max, sum) pairs arrive.
-            float ov[GP][G];
-            auto load_group = [&](int g0) {
-#pragma unroll
-              for (int i = 0; i < GP; ++i)
-#pragma unroll
-                for (int h = 0; h < G; ++h)
-                  ov[i][h] = (g0 + i < nb)
-                                 ? __ldcg(p.part_o + (rb + (size_t)(g0 + i) * G + h) * kHeadDim + e)
-                                 : 0.f;
-            };
-            load_group(0);
-            for (int j = e; j < nb * G; j += NET)
-              mlb[j] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + rb + j);
-            named_barrier_sync(2, NET);
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-              float bm = Mx[h];
-              for (int i = 0; i < nb; ++i) bm = fmaxf(bm, mlb[i * G + h].x);
-              if (bm != Mx[h] && Mx[h] != -INFINITY) {
-                const float cf = exp2f(Mx[h] - bm);
-                Lm[h] *= cf;
-                O[h] *= cf;
-              }
-              Mx[h] = bm;
-            }
-            for (int g0 = 0; g0 < nb; g0 += GP) {
-              if (g0 > 0) load_group(g0);
-#pragma unroll
-              for (int i = 0; i < GP; ++i) {
-                if (g0 + i < nb) {
-#pragma unroll
-                  for (int h = 0; h < G; ++h) {
-                    const float2 ml = mlb[(g0 + i) * G + h];
-                    if (ml.x != -INFINITY) {
-                      const float cf = exp2f(ml.x - Mx[h]);
-                      Lm[h] = fmaf(cf, ml.y, Lm[h]);
-                      O[h] = fmaf(cf, ov[i][h], O[h]);
-                    }
-                  }
-                }
-              }
-            }
-            named_barrier_sync(2, NET);  // mlb is reused by the next batch
-          }
-          if (has_prefix) {
-            // the shared-prefix pass's parts of these rows (written by the
-            // previous kernel: wait for it first)
-            if (p.wait_late == 2) pdl_wait();
-            // PPG parts at a time, every load of a group issued before use
-            constexpr int PPG = 4;
-            for (int t0 = 0; t0 < p.n_tsplit; t0 += PPG) {
-              float2 ml[PPG][G];
-              float o[PPG][G];
-#pragma unroll
-              for (int i = 0; i < PPG; ++i)
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                  const bool in = t0 + i < p.n_tsplit;
-                  const size_t pr =
-                      ((size_t)sg.b * p.n_q + (size_t)sg.g * G + h) * p.n_tsplit + (in ? t0 + i : 0);
-                  ml[i][h] = in ? __ldcg(reinterpret_cast<const float2 *>(p.pre_ml) + pr)
-                                : make_float2(-INFINITY, 0.f);
-                  o[i][h] = in ? __ldcg(p.pre_o + pr * kHeadDim + e) : 0.f;
-                }
-#pragma unroll
-              for (int i = 0; i < PPG; ++i)
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                  if (ml[i][h].x == -INFINITY) continue;
-                  const float nm = fmaxf(Mx[h], ml[i][h].x);
-                  const float ca = (Mx[h] == -INFINITY) ? 0.f : exp2f(Mx[h] - nm);
-                  const float cb = exp2f(ml[i][h].x - nm);
-                  Lm[h] = Lm[h] * ca + ml[i][h].y * cb;
-                  O[h] = O[h] * ca + o[i][h] * cb;
-                  Mx[h] = nm;
-                }
-            }
-          }
-#pragma unroll
-          for (int h = 0; h < G; ++h)
-            p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(O[h] / Lm[h]);
+          merge_parts<G, FP8>(p.part_o, p.part_ml, p.out, unit, flag[1], flag[2], out_row, e,
+                              reinterpret_cast<float2 *>(smem + L::OFF_MERGE));
         }
         named_barrier_sync(2, NET);  // flags are reused by the next segment
       }
@@ -1303,9 +1340,6 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     }
   }
 
-  // (cascade: this grid completes only after the shared-prefix pass, so the
-  // combine kernel that waits on it sees both passes' parts)
-  if (p.wait_late == 2) pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

@@ -151,8 +151,10 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Inputs (q, tables, the prefix blocks) may come from the previous kernel:
-  // wait for it, then let the decode pass that follows start its own work.
-  pdl_wait();
+  // wait for it -- unless that is the cascade's suffix pass, which waited for
+  // them before letting this grid launch -- then let the kernel that follows
+  // (which waits for this grid's completion) launch.
+  if (!p.wait_at_end) pdl_wait();
   pdl_launch_dependents();
 
   int w = (int)blockIdx.x;
@@ -395,6 +397,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
     if (row_ok) *reinterpret_cast<float2 *>(p.pre_ml + slot_row * 2) = make_float2(m_ref, l);
   }
 
+  // (cascade: this grid then completes only after the suffix pass, so the
+  // combine kernel that waits for it sees both passes' partial states)
+  if (p.wait_at_end) pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -429,14 +434,16 @@ static cudaError_t launch_g(const PrefixParams &p, int grid, cudaStream_t stream
   return cudaLaunchKernelEx(&cfg, prefix_attention_kernel<G, BS>, p);
 }
 
-// Final merge of a cascade call: one CTA per unit (sequence, KV head) with a
-// shared prefix, one thread per output dim: the unit's suffix parts, then its
-// prefix parts, combined by log-sum-exp into the bf16 output.
+// Final merge of a cascade call: one CTA per output row (sequence b, query
+// head h) with a shared prefix, one thread per dim: the row's suffix parts,
+// then its prefix parts, folded by log-sum-exp into the bf16 output.  Parts
+// are read PPG at a time, every load of a group issued before any is used.
 template <int G>
 __global__ void __launch_bounds__(kHeadDim) cascade_combine_kernel(const CombineParams p) {
-  pdl_wait();  // the suffix pass, which waits for the prefix pass, has completed
-  const int unit = (int)blockIdx.x;
-  const int b = unit / p.n_kv, g = unit % p.n_kv;
+  pdl_wait();  // the prefix pass, which waits for the suffix pass, has completed
+  const int row = (int)blockIdx.x;  // b * n_q + h
+  const int b = row / p.n_q, h = row % p.n_q;
+  const int unit = b * p.n_kv + h / G, hh = h % G;
   if (b >= p.B) return;
   // Sequences the suffix pass rejected (flagged there) have no parts.
   const int s0 = __ldg(p.seq_prefix_blocks + b), c = __ldg(p.ctx + b);
@@ -444,57 +451,53 @@ __global__ void __launch_bounds__(kHeadDim) cascade_combine_kernel(const Combine
   const int e = threadIdx.x;
   const int2 info = __ldcg(p.part_info + unit);
   if (info.x < 0 || info.y < 1 || info.x + info.y > p.parts) return;
-  float Mx[G], Lm[G], O[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) { Mx[h] = -INFINITY; Lm[h] = 0.f; O[h] = 0.f; }
-  auto fold = [&](int h, float2 ml, float o) {
-    if (ml.x == -INFINITY) return;
-    const float nm = fmaxf(Mx[h], ml.x);
-    const float ca = (Mx[h] == -INFINITY) ? 0.f : exp2f(Mx[h] - nm);
-    const float cb = exp2f(ml.x - nm);
-    Lm[h] = Lm[h] * ca + ml.y * cb;
-    O[h] = O[h] * ca + o * cb;
-    Mx[h] = nm;
-  };
-  constexpr int PPG = 4;  // parts per group of loads in flight
-  const int n_dec = info.y;
-  for (int i0 = 0; i0 < n_dec + p.n_tsplit; i0 += PPG) {
-    float2 ml[PPG][G];
-    float o[PPG][G];
+  const int n_dec = info.y, n_all = n_dec + p.n_tsplit;
+  const float2 *dec_ml = reinterpret_cast<const float2 *>(p.part_ml);
+  const float2 *pre_ml = reinterpret_cast<const float2 *>(p.pre_ml);
+  float Mx = -INFINITY, Lm = 0.f, O = 0.f;
+  constexpr int PPG = 8;
+#pragma unroll 1
+  for (int i0 = 0; i0 < n_all; i0 += PPG) {
+    float2 ml[PPG];
+    float o[PPG];
 #pragma unroll
     for (int i = 0; i < PPG; ++i) {
       const int j = i0 + i;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        if (j < n_dec) {
-          const size_t row = ((size_t)unit + (size_t)(info.x + j)) * G + h;
-          ml[i][h] = __ldcg(reinterpret_cast<const float2 *>(p.part_ml) + row);
-          o[i][h] = __ldcg(p.part_o + row * kHeadDim + e);
-        } else if (j < n_dec + p.n_tsplit) {
-          const size_t pr = ((size_t)b * p.n_q + (size_t)g * G + h) * p.n_tsplit + (j - n_dec);
-          ml[i][h] = __ldcg(reinterpret_cast<const float2 *>(p.pre_ml) + pr);
-          o[i][h] = __ldcg(p.pre_o + pr * kHeadDim + e);
-        } else {
-          ml[i][h] = make_float2(-INFINITY, 0.f);
-          o[i][h] = 0.f;
-        }
+      if (j < n_dec) {
+        const size_t r = ((size_t)unit + (size_t)(info.x + j)) * G + hh;
+        ml[i] = __ldcg(dec_ml + r);
+        o[i] = __ldcg(p.part_o + r * kHeadDim + e);
+      } else if (j < n_all) {
+        const size_t r = (size_t)row * p.n_tsplit + (j - n_dec);
+        ml[i] = __ldcg(pre_ml + r);
+        o[i] = __ldcg(p.pre_o + r * kHeadDim + e);
+      } else {
+        ml[i] = make_float2(-INFINITY, 0.f);
+        o[i] = 0.f;
       }
     }
+    float nm = Mx;
 #pragma unroll
-    for (int i = 0; i < PPG; ++i)
+    for (int i = 0; i < PPG; ++i) nm = fmaxf(nm, ml[i].x);
+    if (nm == -INFINITY) continue;
+    const float ca = (Mx == -INFINITY) ? 0.f : exp2f(Mx - nm);
+    Lm *= ca;
+    O *= ca;
 #pragma unroll
-      for (int h = 0; h < G; ++h) fold(h, ml[i][h], o[i][h]);
+    for (int i = 0; i < PPG; ++i) {
+      const float cb = (ml[i].x == -INFINITY) ? 0.f : exp2f(ml[i].x - nm);
+      Lm = fmaf(ml[i].y, cb, Lm);
+      O = fmaf(o[i], cb, O);
+    }
+    Mx = nm;
   }
-  const size_t orow = (size_t)b * p.n_q + (size_t)g * G;
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-    p.out[(orow + h) * kHeadDim + e] = __float2bfloat16_rn(O[h] / Lm[h]);
+  p.out[(size_t)row * kHeadDim + e] = __float2bfloat16_rn(O / Lm);
 }
 
 template <int G>
 static cudaError_t launch_combine(const CombineParams &p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.B * p.n_kv));
+  cfg.gridDim = dim3((unsigned)(p.B * p.n_q));
   cfg.blockDim = dim3(kHeadDim);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
