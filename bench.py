@@ -447,7 +447,8 @@ def run_ours(args, rank, world, local):
                             peak_kind: round(100 * value / world / peak, 2)},
         "roofline": {"bound": "hbm",
                      "kernel": ("pgd::pf::prefix_attention_kernel + pgd::tc::paged_attention_kernel"
-                                " (cascade, tcgen05)") if args.cascade else
+                                " + pgd::pf::cascade_combine_kernel (cascade, tcgen05)")
+                               if args.cascade else
                                "pgd::tc::paged_attention_kernel<G, bs, %s> (tcgen05)"
                                % ("fp8" if fp8 else "bf16"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
@@ -459,7 +460,8 @@ def run_ours(args, rank, world, local):
                      "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5)},
                     **({"path": "pgd_decode_step (host buffers; no cascade)"}
                        if args.cascade else {})),
-        "gpu_launches": (3 if args.cascade else 2) * K,  # kv_append (+ prefix pass) + attention
+        # kv_append + attention (cascade: + the prefix pass and the combine)
+        "gpu_launches": (4 if args.cascade else 2) * K,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "gpu": torch.cuda.get_device_name(local),
     }

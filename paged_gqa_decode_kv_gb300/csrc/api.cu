@@ -237,7 +237,6 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   p.pre_o = nullptr;
   p.n_tsplit = 0;
   p.part_info = nullptr;
-  p.trigger_early = 0;
   pa->p = p;
   pa->G = G;
   pa->bs = bs;
@@ -293,13 +292,14 @@ pgd_status append_then_attend(void *out, const void *q, const void *k_new, const
 }
 
 // Cascade plan: the shared-prefix pass cuts each group's sequences into
-// chunks of 128 / G and each group's prefix into n_tsplit parts -- enough
-// parts for the pass to cover the GPU (at most 16, at least one 128-token
-// stage each).
+// chunks of 128 / G and each group's prefix into n_tsplit parts (at most 16,
+// at least one 128-token stage each), so that it takes about a quarter of the
+// SMs -- one CTA each -- beside the suffix pass on the rest.
 struct CascadePlan {
   int n_tsplit, n_rchunk;
   size_t pre_ml, pre_o, part_info, total;  // byte offsets / size past the decode workspace
 };
+constexpr int kPrefixSmShare = 4;
 
 int sm_count() {
   static int cached[64] = {0};
@@ -322,7 +322,8 @@ CascadePlan cascade_plan(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32
   const long long stages = std::max(1LL, ((long long)max_group_blocks * bs + 127) / 128);
   c.n_rchunk = std::max(1, (max_group_size * G + 127) / 128);
   const long long items = std::max(1LL, (long long)std::max(n_groups, 1) * n_kv * c.n_rchunk);
-  c.n_tsplit = (int)std::max(1LL, std::min({16LL, stages, (sms + items - 1) / items}));
+  const long long want = std::max(1LL, (long long)sms / kPrefixSmShare);
+  c.n_tsplit = (int)std::max(1LL, std::min({16LL, stages, (want + items - 1) / items}));
   const size_t rows = (size_t)B * n_q * c.n_tsplit;
   c.pre_ml = round_up(decode_bytes, kWsAlign);
   c.pre_o = c.pre_ml + round_up(rows * 2 * 4, kWsAlign);
@@ -505,21 +506,11 @@ pgd_status pgd_cascade_decode_attention(
     s = launch_prepared(pa, st);
     return s == PGD_OK ? ok() : s;
   }
-  // 1. suffix pass: each sequence's own blocks, partial states only; it lets
-  //    the prefix pass launch once it has waited for its inputs
+  // 1. shared-prefix pass, on a few SMs; it lets the suffix pass launch at
+  //    once on the others
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   float *pre_ml = reinterpret_cast<float *>(ws + plan.pre_ml);
   float *pre_o = reinterpret_cast<float *>(ws + plan.pre_o);
-  pa.p.seq_prefix_blocks = seq_prefix_blocks;
-  pa.p.pre_ml = pre_ml;
-  pa.p.pre_o = pre_o;
-  pa.p.n_tsplit = plan.n_tsplit;
-  pa.p.part_info = reinterpret_cast<int2 *>(ws + plan.part_info);
-  pa.p.trigger_early = 1;
-  s = launch_prepared(pa, st);
-  if (s != PGD_OK) return s;
-  // 2. shared-prefix pass: its CTAs take the SMs the suffix pass frees; it
-  //    completes only after the suffix pass
   PrefixParams pp;
   pp.q = static_cast<const __nv_bfloat16 *>(q);
   pp.k_cache = static_cast<const unsigned char *>(k_cache);
@@ -536,7 +527,6 @@ pgd_status pgd_cascade_decode_attention(
   pp.NB = NB;
   pp.n_rchunk = plan.n_rchunk;
   pp.n_tsplit = plan.n_tsplit;
-  pp.wait_at_end = 1;
   pp.qk_scale_log2 = pa.p.qk_scale_log2;
   pp.pre_ml = pre_ml;
   pp.pre_o = pre_o;
@@ -544,6 +534,21 @@ pgd_status pgd_cascade_decode_attention(
   const int grid = n_groups * n_kv * plan.n_rchunk * plan.n_tsplit;
   cudaError_t e = prefix_attention_launch(pp, pa.G, bs, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "shared-prefix pass launch");
+  // 2. suffix pass: each sequence's own blocks, partial states only, on the
+  //    SMs the prefix pass leaves (an automatic grid shrinks by its CTAs); it
+  //    waits for the prefix pass only before exiting
+  pa.p.seq_prefix_blocks = seq_prefix_blocks;
+  pa.p.pre_ml = pre_ml;
+  pa.p.pre_o = pre_o;
+  pa.p.n_tsplit = plan.n_tsplit;
+  pa.p.part_info = reinterpret_cast<int2 *>(ws + plan.part_info);
+  pa.p.wait_late = 2;
+  if (num_splits == 0) {
+    const int sms = sm_count();
+    pa.grid = std::max(std::min(pa.grid, sms - grid), std::max(1, sms / 2));
+  }
+  s = launch_prepared(pa, st);
+  if (s != PGD_OK) return s;
   // 3. combine: suffix and prefix parts of every unit with a shared prefix
   CombineParams cp;
   cp.out = pa.p.out;

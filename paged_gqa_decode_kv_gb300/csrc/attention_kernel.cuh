@@ -719,7 +719,6 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   // the stream may still run.  Unless it is known to write only the caches,
   // wait for it before reading anything.
   if (!p.wait_late) pdl_wait();
-  if (p.trigger_early) pdl_launch_dependents();
 
   if (tid == 0) {
     // 8-bit cache: the softmax warps read each K stage's scales, so they too
@@ -1342,6 +1341,12 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
 
   tc_fence_before();
   __syncthreads();
+  // (cascade: this grid completes only after the shared-prefix pass, so the
+  // combine kernel that waits for it sees both passes' partial states.  The
+  // wait comes after the barrier: a lane blocked in it would hold up the
+  // lanes of its warp that still have work, like the issuing lane 0 of the
+  // MMA warps.)
+  if (p.wait_late == 2) pdl_wait();
   tc_fence_after();
   if (warp == WARP_QK) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),

@@ -137,10 +137,11 @@ struct AttnParams {
   int32_t *counters;             // [B * n_kv]     arrivals per split unit
   int auto_split;                // 1: whole units or balanced cuts, chosen per call
   int wait_late;                 // 1: the previous kernel wrote only the caches (kv_append):
-                                 //    wait for it just before the first cache read
-  int trigger_early;             // 1: let the next kernel (a cascade's shared-prefix pass,
-                                 //    independent of this one) launch as soon as this
-                                 //    kernel has waited for its own inputs
+                                 //    wait for it just before the first cache read;
+                                 // 2: it is a cascade's shared-prefix pass, independent of
+                                 //    this one, which waited for the inputs before letting
+                                 //    this grid launch: wait for it only before exiting, so
+                                 //    that this grid completes after it
   // cascade (all null / 0 otherwise): sequence b's first seq_prefix_blocks[b]
   // blocks were attended by the shared-prefix pass, whose partial states for
   // (b, h) are pre_ml / pre_o[(b * n_q + h) * n_tsplit + part]
@@ -179,9 +180,6 @@ struct PrefixParams {
   int n_groups, B, n_q, n_kv, MB, NB;
   int n_rchunk;                  // chunks of 128 / G sequences per group
   int n_tsplit;                  // parts of each prefix
-  int wait_at_end;               // 1: the previous kernel (the suffix pass) is independent of
-                                 //    this one: do not wait for it before starting, only
-                                 //    before exiting, so that this grid completes after it
   float qk_scale_log2;
   float *pre_ml;                 // [B][n_q][n_tsplit][2]   partial (max, sum), log2 domain
   float *pre_o;                  // [B][n_q][n_tsplit][D]   unnormalised partial outputs

@@ -151,10 +151,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Inputs (q, tables, the prefix blocks) may come from the previous kernel:
-  // wait for it -- unless that is the cascade's suffix pass, which waited for
-  // them before letting this grid launch -- then let the kernel that follows
-  // (which waits for this grid's completion) launch.
-  if (!p.wait_at_end) pdl_wait();
+  // wait for it, then let the suffix pass that follows launch on the SMs this
+  // grid leaves free (it waits for this grid only before it exits).
+  pdl_wait();
   pdl_launch_dependents();
 
   int w = (int)blockIdx.x;
@@ -223,12 +222,14 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
   // Q rows as the K-major A operand: row r, dims 8c..8c+7 in core matrix
   // (r / 8, c), row r % 8; rows past the chunk are zeros.
   if (r < ROWS) {
+    // (all 16 loads of the row in flight before the first store)
     const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((size_t)rb * p.n_q + rh) * kHeadDim);
-#pragma unroll 4
-    for (int c = 0; c < 16; ++c) {
-      const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4 *>(smem + OFF_Q + ((r >> 3) * 16 + c) * 128 + (r & 7) * 16) = v;
-    }
+    uint4 v[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) v[c] = row_ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      *reinterpret_cast<uint4 *>(smem + OFF_Q + ((r >> 3) * 16 + c) * 128 + (r & 7) * 16) = v[c];
   }
   if (warp == 6) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -397,9 +398,6 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
     if (row_ok) *reinterpret_cast<float2 *>(p.pre_ml + slot_row * 2) = make_float2(m_ref, l);
   }
 
-  // (cascade: this grid then completes only after the suffix pass, so the
-  // combine kernel that waits for it sees both passes' partial states)
-  if (p.wait_at_end) pdl_wait();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -440,7 +438,7 @@ static cudaError_t launch_g(const PrefixParams &p, int grid, cudaStream_t stream
 // are read PPG at a time, every load of a group issued before any is used.
 template <int G>
 __global__ void __launch_bounds__(kHeadDim) cascade_combine_kernel(const CombineParams p) {
-  pdl_wait();  // the prefix pass, which waits for the suffix pass, has completed
+  pdl_wait();  // the suffix pass, which waits for the prefix pass, has completed
   const int row = (int)blockIdx.x;  // b * n_q + h
   const int b = row / p.n_q, h = row % p.n_q;
   const int unit = b * p.n_kv + h / G, hh = h % G;
