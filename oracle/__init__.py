@@ -13,6 +13,10 @@ Contents
   * ``e4m3_decode`` / ``e4m3_encode`` / ``quantize_rows`` /
     ``kv_append_fp8`` / ``paged_attention_fp8`` -- the 8-bit (FP8 E4M3,
     per-(token, head) scale) cache, over ``pgd_oracle_fp8.c``.
+  * ``paged_verify_attention`` / ``kv_append_tokens`` -- multi-query
+    (speculative verify) attention, T new query tokens per sequence with the
+    causal mask among them, and appending T tokens, over
+    ``pgd_oracle_verify.c``.
   * ``kv_formula`` -- the KV-cache byte count in closed form.
   * ``block_model`` -- a plain-Python model of block tables, reference counts
     and copy-on-write.
@@ -32,7 +36,8 @@ from . import kv_formula  # noqa: F401  (re-exported)
 from . import block_model  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "pgd_oracle.c"), os.path.join(_HERE, "pgd_oracle_fp8.c")]
+_SRCS = [os.path.join(_HERE, "pgd_oracle.c"), os.path.join(_HERE, "pgd_oracle_fp8.c"),
+         os.path.join(_HERE, "pgd_oracle_verify.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libpgd_oracle.so")
 _lock = threading.Lock()
@@ -85,6 +90,11 @@ def _load():
         lib.oracle_kv_append_fp8.restype = I
         lib.oracle_paged_attention_fp8.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, D, I, I]
         lib.oracle_paged_attention_fp8.restype = I
+        lib.oracle_kv_append_tokens.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I]
+        lib.oracle_kv_append_tokens.restype = I
+        lib.oracle_paged_verify_attention.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, D,
+                                                      I, I]
+        lib.oracle_paged_verify_attention.restype = I
         _lib = lib
         return lib
 
@@ -295,6 +305,40 @@ def paged_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: 
     st = _load().oracle_paged_attention_fp8(_p(out), _p(qa), _p(ka), _p(va), _p(ta), _p(ca), B,
                                             n_q, n_kv, d, block_size, ta.shape[1], NB,
                                             float(scale), int(n_threads), int(mutation))
+    if st:
+        raise ValueError("oracle: invalid context length or block id (status %d)" % st)
+    return out
+
+
+def kv_append_tokens(k_cache, v_cache, k_new, v_new, block_tables, positions):
+    """Return copies of the tiled bf16 pools with T new tokens per sequence
+    (k_new / v_new [B][T][n_kv][d]) written at positions[b] + j."""
+    kc, vc = _u16(k_cache).copy(), _u16(v_cache).copy()
+    kn, vn = _u16(k_new), _u16(v_new)
+    ta, pa = _i32(block_tables), _i32(positions)
+    NB, n_kv, bs, d = _tile_dims(kc)
+    B, T = kn.shape[0], kn.shape[1]
+    st = _load().oracle_kv_append_tokens(_p(kc), _p(vc), _p(kn), _p(vn), _p(ta), _p(pa), B, T,
+                                         n_kv, d, bs, ta.shape[1], NB)
+    if st:
+        raise ValueError("oracle: position or block id out of range")
+    return kc, vc
+
+
+def paged_verify_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           n_threads: int = 0, mutation: int = 0) -> np.ndarray:
+    """float64 out[B][T][n_q][d]: query token i of sequence b attends to its
+    cached positions 0 .. context_lens[b] - T + i (the T new tokens are the
+    last T cached positions)."""
+    qa, ka, va = _u16(q), _u16(k_cache), _u16(v_cache)
+    ta, ca = _i32(block_tables), _i32(context_lens)
+    B, T, n_q, d = qa.shape
+    NB, n_kv, bs, d2 = _tile_dims(ka)
+    assert d2 == d and va.shape == ka.shape
+    out = np.zeros((B, T, n_q, d), dtype=np.float64)
+    st = _load().oracle_paged_verify_attention(_p(out), _p(qa), _p(ka), _p(va), _p(ta), _p(ca),
+                                               B, T, n_q, n_kv, d, bs, ta.shape[1], NB,
+                                               float(scale), int(n_threads), int(mutation))
     if st:
         raise ValueError("oracle: invalid context length or block id (status %d)" % st)
     return out
