@@ -55,6 +55,9 @@ def parse_args(argv=None):
     ap.add_argument("--cascade", action="store_true",
                     help="shared-prefix workloads: read each shared prefix once per group "
                          "(pgd_cascade_decode_attention)")
+    ap.add_argument("--verify", type=int, default=0, metavar="T",
+                    help="speculative verify: T new query tokens per sequence (appended with "
+                         "pgd_kv_append_tokens, attended causally with pgd_paged_verify_attention)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="cache format: bf16, or FP8 E4M3 codes + per-(token, head) scales")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -216,7 +219,11 @@ def oracle_sample(pb_host, n_seq: int, n_threads: int = 0):
     t = pb_host["tables"][:n_seq]
     c = pb_host["lens"][:n_seq]
     t0 = time.perf_counter()
-    if pb_host["kv"] == "fp8":
+    if pb_host.get("T", 0):
+        oracle.paged_verify_attention(q, pb_host["k"], pb_host["v"], t, c, pb_host["scale"],
+                                      n_threads=n_threads)
+        per_token = 2 * pb_host["n_kv"] * pb_host["d"] * 2
+    elif pb_host["kv"] == "fp8":
         oracle.paged_attention_fp8(q, pb_host["k"], pb_host["v"], t, c, pb_host["scale"],
                                    pb_host["bs"], n_threads=n_threads)
         per_token = 2 * pb_host["n_kv"] * (pb_host["d"] + 4)
@@ -228,17 +235,24 @@ def oracle_sample(pb_host, n_seq: int, n_threads: int = 0):
     return dt, int(c.sum()) * per_token
 
 
-def host_copy(pb):
-    return {"q": pb.q.cpu(), "k": pb.k_cache.cpu(), "v": pb.v_cache.cpu(),
+def host_copy(pb, T: int = 0):
+    """Host copies of a batch for the oracle.  Verify batches (T > 0) get the
+    oracle's own append of their new tokens first (untimed)."""
+    k, v = pb.k_cache.cpu(), pb.v_cache.cpu()
+    if T:
+        import oracle
+        k, v = oracle.kv_append_tokens(k, v, pb.k_new.cpu(), pb.v_new.cpu(),
+                                       pb.block_tables.cpu(), pb.positions.cpu())
+    return {"q": pb.q.cpu(), "k": k, "v": v,
             "tables": pb.block_tables.cpu(), "lens": pb.context_lens.cpu(), "scale": pb.scale,
-            "n_kv": pb.n_kv, "d": pb.head_dim, "B": pb.batch, "n_q": pb.n_q,
-            "kv": pb.kv_format, "bs": pb.block_size}
+            "n_kv": pb.n_kv, "d": pb.head_dim, "B": pb.batch, "n_q": pb.q.shape[-2],
+            "kv": pb.kv_format, "bs": pb.block_size, "T": T}
 
 
 def cpu_baseline(pb_host, seconds: float):
     import oracle
     B = pb_host["B"]
-    rows = B * pb_host["n_q"]
+    rows = B * pb_host["n_q"] * max(1, pb_host.get("T", 0))
     cores = oracle.threads_used(0, rows)
     total_t, total_b, calls = 0.0, 0, 0
     while total_t < seconds and calls < 200:
@@ -248,9 +262,11 @@ def cpu_baseline(pb_host, seconds: float):
         calls += 1
     return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle",
-            "sample": "float64 oracle attention over the full batch (all %d sequences, %d query "
+            "sample": "float64 oracle %s over the full batch (all %d sequences, %d query "
                       "heads), %d call(s), %.1f s; kv_append excluded (a %d-byte copy)"
-                      % (B, pb_host["n_q"], calls, total_t, 2 * B * pb_host["n_kv"] * 256)}
+                      % ("verify attention (%d query tokens per sequence)" % pb_host["T"]
+                         if pb_host.get("T", 0) else "attention", B, pb_host["n_q"], calls,
+                         total_t, 2 * B * max(1, pb_host.get("T", 0)) * pb_host["n_kv"] * 256)}
 
 
 # --------------------------------------------------------------- our arm
@@ -293,8 +309,16 @@ def run_ours(args, rank, world, local):
     __graft_entry__.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    pb = inputs.make_workload(args.workload, device=dev, append=True, kv_format=args.kv)
-    B, n_q, n_kv = pb.batch, pb.n_q, pb.n_kv
+    T = args.verify
+    if T:
+        if args.kv != "bf16" or args.cascade:
+            raise SystemExit("--verify needs the bf16 cache and no --cascade")
+        vb = inputs.make_verify_workload(args.workload, T, device=dev)
+        pb = vb.paged
+        pb.q, pb.k_new, pb.v_new, pb.positions = vb.q, vb.k_new, vb.v_new, vb.positions
+    else:
+        pb = inputs.make_workload(args.workload, device=dev, append=True, kv_format=args.kv)
+    B, n_q, n_kv = pb.batch, pb.q.shape[-2], pb.n_kv
     fp8 = args.kv == "fp8"
     append_attend = pgd.append_decode_attention_fp8 if fp8 else pgd.append_decode_attention
     attend = pgd.paged_decode_attention_fp8 if fp8 else pgd.paged_decode_attention
@@ -318,7 +342,22 @@ def run_ours(args, rank, world, local):
             pgd.kv_append(kn, vn, kc, vc, tables, pb.positions, stream=stream)
             return attend(out_, q_, kc, vc, tables, lens, scale, num_splits=num_splits,
                           stream=stream)
-    ws = pgd.make_workspace(B, n_q, n_kv, args.splits, dev)
+    if T:
+        ws = torch.zeros(max(1, pgd.verify_workspace_size(B, T, n_q, n_kv, args.splits)),
+                         dtype=torch.uint8, device=dev)
+
+        def attend(out_, q_, kc, vc, tables, lens, scale, num_splits=0, workspace=None,
+                   stream=None):
+            return pgd.paged_verify_attention(out_, q_, kc, vc, tables, lens, scale,
+                                              num_splits=num_splits, workspace=ws, stream=stream)
+
+        def append_attend(out_, q_, kn, vn, kc, vc, tables, lens, scale, num_splits=0,
+                          workspace=None, stream=None):
+            pgd.kv_append_tokens(kn, vn, kc, vc, tables, pb.positions, stream=stream)
+            return attend(out_, q_, kc, vc, tables, lens, scale, num_splits=num_splits,
+                          stream=stream)
+    else:
+        ws = pgd.make_workspace(B, n_q, n_kv, args.splits, dev)
     out = torch.empty_like(pb.q)
     grid = pgd.attention_grid(B, n_q, n_kv, pb.block_size, args.splits)
     stream = torch.cuda.current_stream()
@@ -405,6 +444,16 @@ def run_ours(args, rank, world, local):
 
     def e2e_step():
         kc, vc = next_pool()
+        if T:  # host buffers through the Python binding: H2D, append + verify, D2H
+            with torch.cuda.stream(stream):
+                q_d.copy_(q_h, non_blocking=True)
+                kn_d.copy_(kn_h, non_blocking=True)
+                vn_d.copy_(vn_h, non_blocking=True)
+                cl_d.copy_(cl_h, non_blocking=True)
+                append_attend(out_d, q_d, kn_d, vn_d, kc, vc, pb.block_tables, cl_d, pb.scale,
+                              num_splits=args.splits, stream=stream)
+                out_h.copy_(out_d, non_blocking=True)
+            return
         pgd.decode_step(out_h, q_h, kn_h, vn_h, cl_h, out_d, q_d, kn_d, vn_d, cl_d, kc, vc,
                         pb.block_tables, pb.scale, args.splits, ws, stream=stream)
 
@@ -436,7 +485,8 @@ def run_ours(args, rank, world, local):
                  "block tables)") if fp8 else
                 "synthetic (seeded N(0,1) bf16 K/V/Q, random block tables)",
         "config": dict(config_block(pb, args.workload, args.splits, n_pools),
-                       **({"cascade": True} if args.cascade else {})),
+                       **({"cascade": True} if args.cascade else {}),
+                       **({"verify_tokens": T} if T else {})),
         "grid_ctas": grid,
         "kv_bytes_per_step": kv_bytes,
         "kv_bytes_per_step_logical": kv_bytes_logical,
@@ -449,24 +499,30 @@ def run_ours(args, rank, world, local):
                      "kernel": ("pgd::pf::prefix_attention_kernel + pgd::tc::paged_attention_kernel"
                                 " + pgd::pf::cascade_combine_kernel (cascade, tcgen05)")
                                if args.cascade else
+                               ("pgd::tc::paged_attention_kernel<%d rows, bs, bf16> (tcgen05, "
+                                "multi-query verify)" % (T * (n_q // n_kv))) if T else
                                "pgd::tc::paged_attention_kernel<G, bs, %s> (tcgen05)"
                                % ("fp8" if fp8 else "bf16"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None if args.cascade else profiled_traffic(args.kv, args.workload),
+                     "traffic": None if (args.cascade or T) else
+                     profiled_traffic(args.kv, args.workload),
                      "launch_ms": round(attn_ms, 5),
                      "bytes_per_launch": kv_bytes},
         "e2e": dict({"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                      "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5)},
                     **({"path": "pgd_decode_step (host buffers; no cascade)"}
-                       if args.cascade else {})),
+                       if args.cascade else
+                       {"path": "pinned host buffers copied on the stream, pgd_kv_append_tokens "
+                                "+ pgd_paged_verify_attention, output copied back"}
+                       if T else {})),
         # kv_append + attention (cascade: + the prefix pass and the combine)
         "gpu_launches": (4 if args.cascade else 2) * K,
         "clocks": sampler.summary(t_wall0, t_wall1),
         "gpu": torch.cuda.get_device_name(local),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(host_copy(pb), args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(host_copy(pb, T), args.cpu_seconds)
     return result
 
 

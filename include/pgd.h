@@ -210,6 +210,53 @@ pgd_status pgd_append_decode_attention(void *out, const void *q, const void *k_n
                                        void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* multi-query (speculative verify) attention                              */
+/* ---------------------------------------------------------------------- */
+/* A draft proposes gamma tokens; the target model scores the pending token
+ * and the gamma proposals in one forward, each position conditioned on the
+ * proposed prefix before it, and the caches are cut back to the committed
+ * boundary afterwards ("Module 10", section "Verify a chain, then roll back
+ * uncommitted state"; "The math of Transformer inference", section 10,
+ * greedy version: one target forward over prefix + k tokens gives k + 1
+ * positions' logits; "LLM inference systems engineering", 2.1.3, the
+ * verify_target interface).  At the attention level of one layer that is T =
+ * gamma + 1 query tokens per sequence over the paged cache with the causal
+ * mask of "Module 10", Lab 2 (new position i sees every cached position up to
+ * and including its own).
+ *
+ * pgd_kv_append_tokens: write T new tokens per sequence, k_new / v_new bf16
+ * [B][T][n_kv][d], token j at position positions[b] + j (positions: device
+ * int32 [B], the number of positions cached before them); otherwise exactly
+ * pgd_kv_append (bit-for-bit, same layout, same rules on shared blocks).
+ * Rolling back rejected tokens needs no device work: the caller lowers the
+ * sequence's length (and may release blocks past it); slots past a context
+ * length are never read.
+ *
+ * pgd_paged_verify_attention: for every b < B, query token i < T, query head
+ * h < n_q, with c = context_lens[b] (which counts the T new tokens, already
+ * appended: c >= T, else PGD_DEVERR_BAD_CONTEXT) and g = h / (n_q / n_kv):
+ *     out[b][i][h][:] = sum_{t <= c - T + i} softmax_t(scale * q[b][i][h] . k_t) v_t
+ * with k_t, v_t the cached K/V of token t of sequence b, KV head g (as in
+ * pgd_paged_decode_attention, which is the case T = 1).  q and out: bf16
+ * [B][T][n_q][d].  T * (n_q / n_kv) <= 16 (the query rows served per KV
+ * head and pass over the cache), else PGD_ERR_UNSUPPORTED; bf16 pools only.
+ * Same arithmetic, tolerance, workspace rules and errors as
+ * pgd_paged_decode_attention; workspace: pgd_verify_workspace_size(...) bytes.
+ * Each KV tile is read once per call for all T x G query rows of its head. */
+pgd_status pgd_kv_append_tokens(const void *k_new, const void *v_new, void *k_cache,
+                                void *v_cache, const int32_t *block_tables,
+                                const int32_t *positions, int32_t B, int32_t T, int32_t n_kv,
+                                int32_t d, int32_t bs, int32_t MB, int32_t NB, void *stream);
+size_t pgd_verify_workspace_size(int32_t B, int32_t T, int32_t n_q, int32_t n_kv, int32_t d,
+                                 int32_t num_splits);
+pgd_status pgd_paged_verify_attention(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      const int32_t *context_lens, int32_t B, int32_t T,
+                                      int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                      int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* cascade: shared prefixes read once per group                            */
 /* ---------------------------------------------------------------------- */
 /* pgd_paged_decode_attention for a batch in which groups of sequences share

@@ -11,8 +11,8 @@ from ._native import (  # noqa: F401
     PGDError, BlockAllocator, kv_append, paged_decode_attention,
     paged_decode_attention_noalloc, append_decode_attention, decode_step, copy_blocks,
     kv_append_fp8, paged_decode_attention_fp8, append_decode_attention_fp8,
-    cascade_decode_attention, cascade_workspace_size,
-    device_errors, workspace_size, make_workspace, attention_grid, validate_tables, lib,
+    cascade_decode_attention, cascade_workspace_size, kv_append_tokens, paged_verify_attention,
+    verify_workspace_size, device_errors, workspace_size, make_workspace, attention_grid, validate_tables, lib,
     library_path)
 
 __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "tile_pool",
@@ -21,5 +21,6 @@ __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload",
            "paged_decode_attention_noalloc", "append_decode_attention", "decode_step",
            "copy_blocks", "kv_append_fp8", "paged_decode_attention_fp8",
            "append_decode_attention_fp8", "cascade_decode_attention", "cascade_workspace_size",
+           "kv_append_tokens", "paged_verify_attention", "verify_workspace_size",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
            "validate_tables", "lib", "library_path"]

@@ -38,6 +38,10 @@ SIGNATURES = {
                                             _F, _I, _P], _I),
     "pgd_append_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                                      _F, _I, _P, _Z, _P], _I),
+    "pgd_kv_append_tokens": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P], _I),
+    "pgd_verify_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
+    "pgd_paged_verify_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                                    _I, _P, _Z, _P], _I),
     "pgd_cascade_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _Z),
     "pgd_cascade_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P], _I),
@@ -252,6 +256,52 @@ def decode_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_
 
 
 # ---------------------------------------------------------------- cascade
+def kv_append_tokens(k_new, v_new, k_cache, v_cache, block_tables, positions,
+                     stream=None) -> None:
+    """Write k_new/v_new [B][T][n_kv][d]: token j of sequence b at logical
+    position positions[b] + j."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(positions, torch.int32, "positions")
+    NB, n_kv, bs, d = _cache_dims(k_cache)
+    B, MB = block_tables.shape
+    T = k_new.shape[1]
+    _check(lib().pgd_kv_append_tokens(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(block_tables), _ptr(positions), B, T, n_kv, d, bs, MB,
+                                      NB, _stream(stream)))
+
+
+def verify_workspace_size(B: int, T: int, n_q: int, n_kv: int, num_splits: int = 0,
+                          d: int = HEAD_DIM) -> int:
+    return int(lib().pgd_verify_workspace_size(B, T, n_q, n_kv, d, num_splits))
+
+
+def paged_verify_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """out[B][T][n_q][d] (bf16): each of the T new query tokens of a sequence
+    attends to its cached context up to and including its own position."""
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, T, n_q, d = q.shape
+    NB, n_kv, bs, d2 = _cache_dims(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        n = max(1, verify_workspace_size(B, T, n_q, n_kv, num_splits))
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_paged_verify_attention(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        B, T, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
 def cascade_workspace_size(B: int, n_q: int, n_kv: int, bs: int, max_group_size: int,
                            max_group_blocks: int, num_splits: int = 0, d: int = HEAD_DIM) -> int:
     return int(lib().pgd_cascade_workspace_size(B, n_q, n_kv, d, bs, num_splits, max_group_size,

@@ -31,7 +31,7 @@ cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_c
                                  int32_t *err, cudaStream_t stream);
 cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                              const int32_t *tables, const int32_t *pos, int pos_offset, int B,
-                             int n_kv, int bs, int MB, int NB, int32_t *err,
+                             int T, int n_kv, int bs, int MB, int NB, int32_t *err,
                              cudaStream_t stream);
 cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src_ids,
                                const int32_t *dst_ids, int n, int n_kv, int bs, int NB,
@@ -118,6 +118,16 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Workspace: [B*n_kv] int32 per-unit arrival counters, then per partial slot
 // (max, sum) and o[G][128].  A slot is unit + part (one part per CTA), so
 // slots = units + CTAs.
+// Kernel row count for T query tokens of Gh heads each: the next power of
+// two of T * Gh, or 0 past 16 rows.
+int unit_rows(int T, int Gh) {
+  const int r = T * Gh;
+  if (T < 1 || r > 16) return 0;
+  int g = 1;
+  while (g < r) g <<= 1;
+  return g;
+}
+
 WsLayout ws_layout(int32_t B, int32_t n_q, int32_t n_kv, long long grid) {
   WsLayout L;
   const int G = n_q / n_kv;
@@ -193,12 +203,18 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
                              const int32_t *tables, const int32_t *ctx, int32_t B, int32_t n_q,
                              int32_t n_kv, int32_t bs, int32_t MB, int32_t NB, float scale,
                              int32_t num_splits, void *workspace, size_t workspace_bytes,
-                             PreparedAttention *pa, bool fp8 = false) {
+                             PreparedAttention *pa, bool fp8 = false, int32_t T = 1) {
   if (!workspace) return fail(PGD_ERR_WORKSPACE, "workspace is NULL");
   if (!aligned(workspace, kWsAlign)) return fail(PGD_ERR_WORKSPACE, "workspace not 256-aligned");
-  if (workspace_bytes < ws_layout(B, n_q, n_kv, 1).total)
+  // query rows per unit: T tokens x the KV head's query heads, padded to a
+  // power of two (the kernel's row count)
+  const int Gh = n_q / n_kv;
+  const int G = unit_rows(T, Gh);
+  if (G == 0 || (fp8 && T != 1))
+    return fail(PGD_ERR_UNSUPPORTED, "T = %d x %d heads per KV head (at most 16 rows)", T, Gh);
+  const int32_t n_rows = G * n_kv;
+  if (workspace_bytes < ws_layout(B, n_rows, n_kv, 1).total)
     return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes is too small", workspace_bytes);
-  const int G = n_q / n_kv;
   int grid = 0;
   if (num_splits > 0) {
     grid = (int)((long long)num_splits * B * n_kv);
@@ -206,7 +222,7 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
     pgd_status s = auto_grid(G, bs, B, &grid, fp8);
     if (s != PGD_OK) return s;
   }
-  const WsLayout L = ws_layout(B, n_q, n_kv, grid);
+  const WsLayout L = ws_layout(B, n_rows, n_kv, grid);
   if (workspace_bytes < L.total)
     return fail(PGD_ERR_WORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, L.total);
   int32_t *err = nullptr;
@@ -225,6 +241,9 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   p.n_kv = n_kv;
   p.MB = MB;
   p.NB = NB;
+  p.T = T;
+  p.lg_gh = Gh == 1 ? 0 : Gh == 2 ? 1 : Gh == 4 ? 2 : 3;
+  p.rows = T * Gh;
   p.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
   p.counters = reinterpret_cast<int32_t *>(ws + L.counters);
   p.auto_split = num_splits == 0 ? 1 : 0;
@@ -284,8 +303,8 @@ pgd_status append_then_attend(void *out, const void *q, const void *k_new, const
   if (s != PGD_OK) return s;
   cudaError_t e = fp8 ? kv_append_fp8_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B,
                                              n_kv, bs, MB, NB, pa.p.err, stream)
-                      : kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B, n_kv,
-                                         bs, MB, NB, pa.p.err, stream);
+                      : kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B, 1,
+                                         n_kv, bs, MB, NB, pa.p.err, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   pa.p.wait_late = 1;
   return launch_prepared(pa, stream);
@@ -393,7 +412,30 @@ pgd_status pgd_kv_append(const void *k_new, const void *v_new, void *k_cache, vo
   s = error_word(&err);
   if (s != PGD_OK) return s;
   cudaError_t e = kv_append_launch(k_new, v_new, k_cache, v_cache, block_tables, positions, 0, B,
-                                   n_kv, bs, MB, NB, err, static_cast<cudaStream_t>(stream));
+                                   1, n_kv, bs, MB, NB, err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  return ok();
+}
+
+pgd_status pgd_kv_append_tokens(const void *k_new, const void *v_new, void *k_cache,
+                                void *v_cache, const int32_t *block_tables,
+                                const int32_t *positions, int32_t B, int32_t T, int32_t n_kv,
+                                int32_t d, int32_t bs, int32_t MB, int32_t NB, void *stream) {
+  if (B < 0 || T < 1) return fail(PGD_ERR_INVALID_ARG, "B = %d, T = %d", B, T);
+  pgd_status s = check_cache_shape(n_kv, d, bs, MB, NB);
+  if (s != PGD_OK) return s;
+  if ((long long)B * T * n_kv > 0x7ffffffcLL)
+    return fail(PGD_ERR_INVALID_ARG, "B * T * n_kv too large");
+  if (B == 0) return ok();
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !positions)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  int32_t *err = nullptr;
+  s = error_word(&err);
+  if (s != PGD_OK) return s;
+  cudaError_t e = kv_append_launch(k_new, v_new, k_cache, v_cache, block_tables, positions, 0, B,
+                                   T, n_kv, bs, MB, NB, err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   return ok();
 }
@@ -426,6 +468,49 @@ int32_t pgd_attention_grid(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int
   int grid = 0;
   if (auto_grid(n_q / n_kv, bs, B, &grid) != PGD_OK) return 0;
   return grid;
+}
+
+size_t pgd_verify_workspace_size(int32_t B, int32_t T, int32_t n_q, int32_t n_kv, int32_t d,
+                                 int32_t num_splits) {
+  if (B < 0 || n_kv <= 0 || n_q <= 0 || n_q % n_kv || d != kHeadDim || num_splits < 0) return 0;
+  const int Gh = n_q / n_kv;
+  if (!supported_group(Gh)) return 0;
+  const int G = unit_rows(T, Gh);
+  if (G == 0) return 0;
+  long long grid = 0;
+  if (num_splits > 0) {
+    grid = (long long)num_splits * B * n_kv;
+  } else {
+    grid = kAutoMaxCtas;
+    int g[2] = {0, 0};
+    if (auto_grid(G, 16, B, &g[0]) == PGD_OK && auto_grid(G, 32, B, &g[1]) == PGD_OK)
+      grid = std::max(g[0], g[1]);
+    clear_error_detail();
+  }
+  return ws_layout(B, G * n_kv, n_kv, grid).total;
+}
+
+pgd_status pgd_paged_verify_attention(void *out, const void *q, const void *k_cache,
+                                      const void *v_cache, const int32_t *block_tables,
+                                      const int32_t *context_lens, int32_t B, int32_t T,
+                                      int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                      int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                                      void *workspace, size_t workspace_bytes, void *stream) {
+  pgd_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, B,
+                                      n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if (T < 1) return fail(PGD_ERR_INVALID_ARG, "T = %d", T);
+  if (unit_rows(T, n_q / n_kv) == 0)
+    return fail(PGD_ERR_UNSUPPORTED, "T * (n_q / n_kv) = %d > 16 query rows per KV head",
+                T * (n_q / n_kv));
+  if ((long long)B * T * n_q >= 0x7fffffffLL) return fail(PGD_ERR_INVALID_ARG, "B * T * n_q");
+  if (B == 0) return ok();
+  PreparedAttention pa;
+  s = prepare_attention(out, q, k_cache, v_cache, block_tables, context_lens, B, n_q, n_kv, bs, MB,
+                        NB, scale, num_splits, workspace, workspace_bytes, &pa, false, T);
+  if (s != PGD_OK) return s;
+  s = launch_prepared(pa, static_cast<cudaStream_t>(stream));
+  return s == PGD_OK ? ok() : s;
 }
 
 pgd_status pgd_paged_decode_attention(void *out, const void *q, const void *k_cache,

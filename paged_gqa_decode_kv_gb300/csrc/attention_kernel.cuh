@@ -98,7 +98,8 @@ namespace pgd {
 namespace tc {
 
 constexpr int TOK = 128;                    // tokens per stage (MMA M of q.k^T)
-constexpr int NPAD = 16;                    // MMA N: heads padded to 16
+constexpr int NPAD = 16;                    // MMA N: query rows padded to 16
+constexpr int RMAX = 16;                    // query rows per unit at most (= NPAD)
 constexpr int P_BYTES = TOK * NPAD * 2;     // [16 token groups][2 head groups][8][16 B]
 constexpr int WARP_KP = 4, WARP_VP = 5, WARP_QK = 6, WARP_PV = 7, WARP_EPI = 8, WARP_CVT = 12;
 // 12 warps; the 8-bit kernel adds NCVT warps that dequantise V (warps 12..)
@@ -136,10 +137,10 @@ struct Lay {
   static constexpr int OFF_Q = OFF_VB + VB_BYTES;  // Q double buffered by segment parity
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int OFF_RED = OFF_BAR + 512;    // f32 [2][4][8] warp maxima
-  static constexpr int OFF_LRED = OFF_RED + 256;   // f32 [2][4][8] warp sums per segment parity
-  static constexpr int OFF_MREF = OFF_LRED + 256;  // f32 [2][8] reference maxima per segment parity
-  static constexpr int OFF_QS = OFF_MREF + 64;     // f32 [2][8] Q scales per Q buffer (8-bit)
+  static constexpr int OFF_RED = OFF_BAR + 512;    // f32 [2][4][RMAX] warp maxima
+  static constexpr int OFF_LRED = OFF_RED + 2 * 4 * RMAX * 4;  // f32 [2][4][RMAX] warp sums
+  static constexpr int OFF_MREF = OFF_LRED + 2 * 4 * RMAX * 4;  // f32 [2][RMAX] reference maxima
+  static constexpr int OFF_QS = OFF_MREF + 2 * RMAX * 4;  // f32 [2][8] Q scales per Q buffer (8-bit)
   static constexpr int OFF_MERGE = OFF_QS + 64;    // float2 [MERGE_PAIRS] partial (max, sum)
   static constexpr int OFF_MISC = OFF_MERGE + MERGE_PAIRS * 8;  // tmem base, flags, masks
   static constexpr int OFF_PRE = OFF_MISC + 128;   // int [B + 1]
@@ -260,7 +261,7 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&v)[8]) {
       : "memory");
 }
 
-template <int G> constexpr int kLog2 = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+template <int G> constexpr int kLog2 = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : G == 8 ? 3 : 4;
 
 // Max (or sum) over the warp of G per-lane values, one per head, with the
 // values halved at each of the first log2(G) exchange steps (a lane keeps one
@@ -354,6 +355,14 @@ struct Schedule {
     return (P * (x + 1) - 1) / X;
   }
 };
+
+// Query row r of unit (b, g) -- query token r >> lg_gh of the sequence's T,
+// query head g * 2^lg_gh + (r & (2^lg_gh - 1)) -- as a row index of q and of
+// out ([B][T][n_q] rows of d values; T = 1 for decode).
+__device__ __forceinline__ size_t q_index(const AttnParams &p, int b, int g, int r) {
+  return ((size_t)b * p.T + (size_t)(r >> p.lg_gh)) * p.n_q + ((size_t)g << p.lg_gh) +
+         (size_t)(r & ((1 << p.lg_gh) - 1));
+}
 
 // First block of sequence b that this kernel attends (the blocks before it
 // were attended by the shared-prefix pass of a cascade call).
@@ -489,10 +498,10 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
 #pragma unroll
       for (int i = 0; i < QPL; ++i) {
         const int j = lane + 32 * i, r = j >> 4, c = j & 15;
-        a.q[i] = (j < 16 * G) ? __ldg(reinterpret_cast<const uint4 *>(
-                                    p.q + ((size_t)g.b * p.n_q + (size_t)g.g * G + r) * kHeadDim +
-                                    c * 8))
-                              : make_uint4(0, 0, 0, 0);
+        a.q[i] = (j < 16 * G && r < p.rows)
+                     ? __ldg(reinterpret_cast<const uint4 *>(p.q + q_index(p, g.b, g.g, r) *
+                                                                       kHeadDim + c * 8))
+                     : make_uint4(0, 0, 0, 0);
       }
     }
     const int32_t *trow = p.tables + (size_t)g.b * p.MB + start_block(p, g.b) + g.j0;
@@ -607,7 +616,8 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
 }
 
 // Last-arriver merge of a unit's n_parts partial states (parts c0 ..), by
-// log-sum-exp, into the bf16 output rows; run by the 128 epilogue threads,
+// log-sum-exp, into the bf16 output rows of query rows h < rows (row h at
+// obase + (h >> lg_gh) * n_q + h mod 2^lg_gh); run by the 128 epilogue threads,
 // thread e owning dim e.  The (max, sum) pairs are staged in shared memory
 // PPB parts at a time; the partial outputs are read U parts at a time, every
 // load of a group issued before any is used.  Cold (once per cut unit), so
@@ -616,7 +626,8 @@ template <int G, bool FP8>
 __device__ __noinline__ void merge_parts(const float *__restrict__ part_o,
                                          const float *__restrict__ part_ml,
                                          __nv_bfloat16 *__restrict__ out, int unit, int c0,
-                                         int n_parts, size_t out_row, int e, float2 *mlb) {
+                                         int n_parts, size_t obase, int lg_gh, int n_q,
+                                         int rows, int e, float2 *mlb) {
   constexpr int NET = 128;
   constexpr int PPB = MERGE_PAIRS / G;
   constexpr int U = (FP8 ? 16 : 32) / G;  // (fewer under the 8-bit kernel's register budget)
@@ -668,7 +679,9 @@ __device__ __noinline__ void merge_parts(const float *__restrict__ part_o,
   }
 #pragma unroll
   for (int h = 0; h < G; ++h)
-    out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(O[h] / Lm[h]);
+    if (h < rows)
+      out[(obase + (size_t)(h >> lg_gh) * n_q + (h & ((1 << lg_gh) - 1))) * kHeadDim + e] =
+          __float2bfloat16_rn(O[h] / Lm[h]);
 }
 
 template <int G, int BS, bool FP8>
@@ -679,7 +692,10 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   constexpr uint32_t IDESC_QK8 = instr_desc_e4m3();
   constexpr uint32_t IDESC_PV = instr_desc(true, true);
   constexpr uint32_t IDESC_PV16 = instr_desc(true, true, false);  // f16 V and P
-  static_assert(G >= 1 && G <= 8 && TOK % BS == 0 && BS % 8 == 0 && SB <= 32, "shape");
+  // G: query rows per unit (heads per KV head x query tokens), padded to a
+  // power of two; the 8-bit kernel keeps its query split in rows h and 8 + h.
+  static_assert(G >= 1 && G <= (FP8 ? 8 : RMAX) && TOK % BS == 0 && BS % 8 == 0 && SB <= 32,
+                "shape");
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -765,7 +781,8 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   for (int b = tid; b < p.B; b += kThreads<FP8>) {
     const int c = p.ctx[b];
     int nb = 0;
-    if (c >= 1 && c <= max_tokens) nb = (c + BS - 1) / BS; else bad_ctx = true;
+    // (a multi-query call's T new tokens are the last T of the context)
+    if (c >= max(1, p.T) && c <= max_tokens) nb = (c + BS - 1) / BS; else bad_ctx = true;
     const int s0 = start_block(p, b);
     if (s0 < 0 || (nb > 0 && s0 >= nb)) bad_ctx = true;  // the suffix must keep >= 1 block
     pre[b + 1] = (s0 >= 0 && s0 < nb) ? nb - s0 + kSegCost<BS> : 0;
@@ -958,7 +975,13 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     const int t = tid;  // 0..127: token row of S
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     constexpr int NCT = 128;
-    constexpr int NSC = FP8 ? 16 : 8;  // S columns per stage (8-bit: high and low parts)
+    constexpr int NSC = (FP8 || G > 8) ? 16 : 8;  // S columns per stage (8-bit: high and low parts)
+    // Query token of each column, for the causal mask among a multi-query
+    // call's T new tokens (token a of the context is seen by column h iff
+    // a - (ctx - T) <= tok[h]); padding columns see nothing.
+    int tok[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) tok[h] = h < p.rows ? (h >> p.lg_gh) : -(1 << 30);
     SegCursor cur(sc);
     Segment sg, nsg;
     int s = 0, k = 0, it = 0;
@@ -981,6 +1004,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         bool valid[2] = {false, false};
         int msk[2] = {0, 0};
         int lim[2] = {0, 0};  // rows p.v reads: the valid length rounded up to 16
+        int epos[2] = {0, 0};  // this row's token minus the first new token (T > 1)
         // Invalid-block mask of each stage: the K producer wrote it before
         // arming full_k; the q.k^T issuer acquired full_k and then released
         // m_ready.  (Waiting on full_k here could alias under the bf16
@@ -1005,6 +1029,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
               nvalid -= (sg.nblk + sb0) * BS - ctx_b;
             valid[u] = (t < nvalid) && !((msk[u] >> (t / BS)) & 1);
             lim[u] = (nvalid + 15) & ~15;
+            epos[u] = (sb0 + sg.j0 + (st + u) * SB) * BS + t - (ctx_b - p.T);
           }
         }
         tc_fence_after();
@@ -1014,14 +1039,14 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
           if (u < n2) {
             const uint32_t a0 = tmem + lane_base + col_s((s + u) % NSB);
             tmem_ld8_async(a0, sv[u]);
-            if (FP8) tmem_ld8_async(a0 + 8, sv[u] + 8);
+            if (NSC > 8) tmem_ld8_async(a0 + 8, sv[u] + 8);
           }
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           if (u < n2) {
             tmem_wait8(sv[u]);
-            if (FP8) tmem_wait8(sv[u] + 8);
+            if (NSC > 8) tmem_wait8(sv[u] + 8);
           }
         }
         tc_fence_before();
@@ -1068,7 +1093,9 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
           for (int u = 0; u < 2; ++u)
 #pragma unroll
             for (int h = 0; h < G; ++h)
-              sc_[u][h] = valid[u] ? __uint_as_float(sv[u][h]) * p.qk_scale_log2 : -INFINITY;
+              sc_[u][h] = (valid[u] && tok[h] >= epos[u])
+                              ? __uint_as_float(sv[u][h]) * p.qk_scale_log2
+                              : -INFINITY;
         }
 
         // Does any score of the 2 x 128 rows exceed its head's reference by
@@ -1094,26 +1121,28 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
           for (int h = 0; h < G; ++h) v2[h] = fmaxf(sc_[0][h], sc_[1][h]);
           const float wm = warp_reduce_heads<G, true>(v2, lane);
           constexpr int SH = 5 - kLog2<G>;  // lanes per head after the reduction
-          if ((lane & ((1 << SH) - 1)) == 0) red[(rb * 4 + warp) * 8 + (lane >> SH)] = wm;
+          if ((lane & ((1 << SH) - 1)) == 0) red[(rb * 4 + warp) * RMAX + (lane >> SH)] = wm;
           named_barrier_sync(1, NCT);
-          float tmax[8];
+          constexpr int G4 = (G + 3) / 4;  // float4s of maxima per warp
+          float tmax[4 * G4];
 #pragma unroll
-          for (int h = 0; h < 8; ++h) tmax[h] = -INFINITY;
+          for (int h = 0; h < 4 * G4; ++h) tmax[h] = -INFINITY;
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            const float4 *src = reinterpret_cast<const float4 *>(red + (rb * 4 + w) * 8);
-            const float4 a = src[0];
-            tmax[0] = fmaxf(tmax[0], a.x); tmax[1] = fmaxf(tmax[1], a.y);
-            tmax[2] = fmaxf(tmax[2], a.z); tmax[3] = fmaxf(tmax[3], a.w);
-            if (G > 4) {
-              const float4 b4 = src[1];
-              tmax[4] = fmaxf(tmax[4], b4.x); tmax[5] = fmaxf(tmax[5], b4.y);
-              tmax[6] = fmaxf(tmax[6], b4.z); tmax[7] = fmaxf(tmax[7], b4.w);
+            const float4 *src = reinterpret_cast<const float4 *>(red + (rb * 4 + w) * RMAX);
+#pragma unroll
+            for (int j = 0; j < G4; ++j) {
+              const float4 a = src[j];
+              tmax[4 * j + 0] = fmaxf(tmax[4 * j + 0], a.x);
+              tmax[4 * j + 1] = fmaxf(tmax[4 * j + 1], a.y);
+              tmax[4 * j + 2] = fmaxf(tmax[4 * j + 2], a.z);
+              tmax[4 * j + 3] = fmaxf(tmax[4 * j + 3], a.w);
             }
           }
-          float alpha[8];
+          constexpr int GO = G > 8 ? 16 : 8;  // O columns held per TMEM lane
+          float alpha[GO];
 #pragma unroll
-          for (int h = 0; h < 8; ++h) alpha[h] = 1.f;
+          for (int h = 0; h < GO; ++h) alpha[h] = 1.f;
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             const float mn = fmaxf(m_ref[h], tmax[h]);
@@ -1125,11 +1154,14 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             // rescale O in tensor memory once the previous p.v has completed
             wait_or_abort(&p_free[(s - 1) & 1], (uint32_t)((s - 1) >> 1) & 1u, abort_flag, p.err);
             tc_fence_after();
-            float ov[8];
-            tmem_ld8(tmem + lane_base + col_o(ob), ov);
 #pragma unroll
-            for (int h = 0; h < 8; ++h) ov[h] *= alpha[h];
-            tmem_st8(tmem + lane_base + col_o(ob), ov);
+            for (int c8 = 0; c8 < GO / 8; ++c8) {
+              float ov[8];
+              tmem_ld8(tmem + lane_base + col_o(ob) + 8 * c8, ov);
+#pragma unroll
+              for (int h = 0; h < 8; ++h) ov[h] *= alpha[8 * c8 + h];
+              tmem_st8(tmem + lane_base + col_o(ob) + 8 * c8, ov);
+            }
             tc_fence_before();
           }
         }
@@ -1139,10 +1171,11 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         for (int u = 0; u < 2; ++u) {
           if (u < n2) {
             const int su = s + u, pbuf = su & 1;
-            uint32_t packed[4] = {0, 0, 0, 0};
+            uint32_t packed[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              const float pv = valid[u] ? exp2f(sc_[u][h] - m_ref[h]) : 0.f;
+              const float pv =
+                  (valid[u] && tok[h] >= epos[u]) ? exp2f(sc_[u][h] - m_ref[h]) : 0.f;
               uint16_t bits;
               if constexpr (FP8) {
                 const __half ph = __float2half_rn(pv);
@@ -1159,6 +1192,10 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             *reinterpret_cast<uint4 *>(smem + L::OFF_P + pbuf * P_BYTES + (t >> 3) * 256 +
                                        (t & 7) * 16) =
                 make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            if (G > 8)  // rows 8..15: the second 8-column group of the MN-major P
+              *reinterpret_cast<uint4 *>(smem + L::OFF_P + pbuf * P_BYTES + (t >> 3) * 256 +
+                                         128 + (t & 7) * 16) =
+                  make_uint4(packed[4], packed[5], packed[6], packed[7]);
             if (!FP8 && !valid[u] && t < lim[u]) {
               // rows that p.v reads but that are not valid tokens (the tail
               // of the last block, a block whose id was bad) must not feed
@@ -1190,11 +1227,11 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
       {
         const float ws = warp_reduce_heads<G, false>(l_part, lane);
         constexpr int SH = 5 - kLog2<G>;
-        if ((lane & ((1 << SH) - 1)) == 0) lred[(ob * 4 + warp) * 8 + (lane >> SH)] = ws;
+        if ((lane & ((1 << SH) - 1)) == 0) lred[(ob * 4 + warp) * RMAX + (lane >> SH)] = ws;
       }
       if (t == 0) {
 #pragma unroll
-        for (int h = 0; h < G; ++h) mref[ob * 8 + h] = m_ref[h];
+        for (int h = 0; h < G; ++h) mref[ob * RMAX + h] = m_ref[h];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&seg_done[ob]);
@@ -1221,14 +1258,17 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
       float Lsum[G], M[G];
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        Lsum[h] = (lred[(ob * 4 + 0) * 8 + h] + lred[(ob * 4 + 1) * 8 + h]) +
-               (lred[(ob * 4 + 2) * 8 + h] + lred[(ob * 4 + 3) * 8 + h]);
-        M[h] = mref[ob * 8 + h];
+        Lsum[h] = (lred[(ob * 4 + 0) * RMAX + h] + lred[(ob * 4 + 1) * RMAX + h]) +
+               (lred[(ob * 4 + 2) * RMAX + h] + lred[(ob * 4 + 3) * RMAX + h]);
+        M[h] = mref[ob * RMAX + h];
       }
       wait_or_abort(&o_full[ob], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
       tc_fence_after();
-      float ov[8];
-      tmem_ld8(tmem + lane_base + col_o(ob), ov);
+      constexpr int GO = G > 8 ? 16 : 8;
+      float ov[GO];
+#pragma unroll
+      for (int c8 = 0; c8 < GO / 8; ++c8)
+        tmem_ld8(tmem + lane_base + col_o(ob) + 8 * c8, *reinterpret_cast<float(*)[8]>(ov + 8 * c8));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_free[ob]);
@@ -1240,11 +1280,13 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
       // parts holding the unit's first and last blocks
       const long long c_first = sc.units ? (long long)part : sc.part_of(sg.ucs + sc.ov);
       const long long c_last = sc.units ? (long long)part : sc.part_of(sg.uce - 1);
-      const size_t out_row = (size_t)sg.b * p.n_q + (size_t)sg.g * G;
+      const size_t obase = q_index(p, sg.b, sg.g, 0);  // output row of query row 0
       if (whole) {
 #pragma unroll
         for (int h = 0; h < G; ++h)
-          p.out[(out_row + h) * kHeadDim + e] = __float2bfloat16_rn(ov[h] / Lsum[h]);
+          if (h < p.rows)
+            p.out[(obase + (size_t)(h >> p.lg_gh) * p.n_q + (h & ((1 << p.lg_gh) - 1))) *
+                      kHeadDim + e] = __float2bfloat16_rn(ov[h] / Lsum[h]);
       } else if (has_prefix) {
         // cascade unit: the combine kernel merges all its parts; record
         // where they are (every part writes the same pair)
@@ -1280,8 +1322,8 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         named_barrier_sync(2, NET);
         if (flag[0]) {
           __threadfence();
-          merge_parts<G, FP8>(p.part_o, p.part_ml, p.out, unit, flag[1], flag[2], out_row, e,
-                              reinterpret_cast<float2 *>(smem + L::OFF_MERGE));
+          merge_parts<G, FP8>(p.part_o, p.part_ml, p.out, unit, flag[1], flag[2], obase, p.lg_gh,
+                              p.n_q, p.rows, e, reinterpret_cast<float2 *>(smem + L::OFF_MERGE));
         }
         named_barrier_sync(2, NET);  // flags are reused by the next segment
       }
@@ -1410,6 +1452,9 @@ int attention_ctas_per_sm_t(int G, int bs, int B) {
   if (G == G_ && bs == BS_) return tc::occupancy_cfg<G_, BS_, FP8>(B);
   PGD_CASE(1, 16) PGD_CASE(2, 16) PGD_CASE(4, 16) PGD_CASE(8, 16)
   PGD_CASE(1, 32) PGD_CASE(2, 32) PGD_CASE(4, 32) PGD_CASE(8, 32)
+  if constexpr (!FP8) {
+    PGD_CASE(16, 16) PGD_CASE(16, 32)
+  }
 #undef PGD_CASE
   return 0;
 }
@@ -1421,6 +1466,9 @@ cudaError_t attention_launch_t(const AttnParams &p, int G, int bs, int grid,
   if (G == G_ && bs == BS_) return tc::launch_cfg<G_, BS_, FP8>(p, grid, stream);
   PGD_CASE(1, 16) PGD_CASE(2, 16) PGD_CASE(4, 16) PGD_CASE(8, 16)
   PGD_CASE(1, 32) PGD_CASE(2, 32) PGD_CASE(4, 32) PGD_CASE(8, 32)
+  if constexpr (!FP8) {
+    PGD_CASE(16, 16) PGD_CASE(16, 32)
+  }
 #undef PGD_CASE
   return cudaErrorInvalidValue;
 }

@@ -6,8 +6,10 @@
 // appends its own K and V to the cache): for sequence b at position p, the
 // token row of slot p % bs in tile (table[b][p / bs], g) becomes k_new[b][g]
 // (and V).  Tiles hold 8 x 8 core matrices, so the 256-byte row is sixteen
-// 16-byte chunks 128 bytes apart.  One warp per (sequence, KV head): lanes
-// 0-15 move the K chunks and lanes 16-31 the V chunks.  A pure copy, bit exact.
+// 16-byte chunks 128 bytes apart.  A multi-query call appends T tokens per
+// sequence (k_new [B][T][n_kv][d]) at positions p .. p + T - 1.  One warp per
+// (sequence, token, KV head): lanes 0-15 move the K chunks and lanes 16-31
+// the V chunks.  A pure copy, bit exact.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -20,18 +22,20 @@ __global__ void __launch_bounds__(128)
 kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                  uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                  const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
-                 int pos_offset, int B, int n_kv, int bs, int MB, int NB, int32_t *err) {
+                 int pos_offset, int B, int T, int n_kv, int bs, int MB, int NB, int32_t *err) {
   constexpr int kVecPerRow = kHeadDim * 2 / 16;  // 16 uint4 per 256-byte row
   pdl_launch_dependents();  // the attention that follows may start its prologue
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (b * T + j) * n_kv + g
   const int lane = threadIdx.x & 31;
-  if (row >= B * n_kv) return;
-  const int b = row / n_kv, g = row % n_kv;
-  const int p = __ldg(pos + b) + pos_offset;
-  if (p < 0 || p >= MB * bs) {
+  if (row >= B * T * n_kv) return;
+  const int bj = row / n_kv, g = row % n_kv;
+  const int b = bj / T, j = bj % T;
+  const long long pl = (long long)__ldg(pos + b) + pos_offset + j;
+  if (pl < 0 || pl >= (long long)MB * bs) {
     if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_POSITION);
     return;
   }
+  const int p = (int)pl;
   const int blk = __ldg(tables + (size_t)b * MB + p / bs);
   if ((unsigned)blk >= (unsigned)NB) {
     if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_BLOCK_ID);
@@ -53,15 +57,15 @@ kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_ne
 
 cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                              const int32_t *tables, const int32_t *pos, int pos_offset, int B,
-                             int n_kv, int bs, int MB, int NB, int32_t *err,
+                             int T, int n_kv, int bs, int MB, int NB, int32_t *err,
                              cudaStream_t stream) {
-  const int rows = B * n_kv;
+  const long long rows = (long long)B * T * n_kv;
   if (rows == 0) return cudaSuccess;
-  const int grid = (rows + 3) / 4;
+  const int grid = (int)((rows + 3) / 4);
   kv_append_kernel<<<grid, 128, 0, stream>>>(
       static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
       static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), tables, pos, pos_offset, B,
-      n_kv, bs, MB, NB, err);
+      T, n_kv, bs, MB, NB, err);
   return cudaGetLastError();
 }
 

@@ -131,6 +131,10 @@ struct AttnParams {
   const int32_t *tables;         // [B][MB]
   const int32_t *ctx;            // [B]
   int B, n_q, n_kv, MB, NB;
+  int T;                         // query tokens per sequence: 1 (decode) or the new tokens of
+                                 // a multi-query call, which attend causally among themselves
+  int lg_gh;                     // log2 of the query heads per KV head
+  int rows;                      // query rows per unit, T << lg_gh (<= the kernel's G)
   float qk_scale_log2;           // scale * log2(e): scores live in the log2 domain
   float *part_o;                 // [slots][G][D]  unnormalised partial outputs
   float *part_ml;                // [slots][G][2]  partial (max, sum), log2 domain

@@ -137,7 +137,7 @@ class PagedBatch:
     """Inputs of one decode step.  Tensors live on `device`.  With
     kv_format "fp8" the pools are uint8 [NB][n_kv][bs/8][8*d + 32]: E4M3
     codes and per-(token, head) fp32 scales (see pack_pool8)."""
-    q: torch.Tensor              # bf16 [B][n_q][d]
+    q: torch.Tensor              # bf16 [B][n_q][d] (verify steps: [B][T][n_q][d])
     k_cache: torch.Tensor        # bf16 [NB][n_kv][bs/8][d/8][8][8] (tiled), or uint8 codes
     v_cache: torch.Tensor        # same layout
     block_tables: torch.Tensor   # int32 [B][MB], -1 where unused
@@ -158,11 +158,11 @@ class PagedBatch:
 
     @property
     def n_q(self) -> int:
-        return self.q.shape[1]
+        return self.q.shape[-2]  # (q may carry a token axis: [B][T][n_q][d])
 
     @property
     def head_dim(self) -> int:
-        return self.q.shape[2]
+        return self.q.shape[-1]
 
     def token(self, cache: torch.Tensor, block: int, head: int, slot: int) -> torch.Tensor:
         """The d-vector of one cached token (bf16 pools)."""
@@ -299,6 +299,59 @@ def make_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[
         scale=(1.0 / math.sqrt(head_dim)) if scale is None else scale,
         n_kv=n_kv, block_size=bs, unique_blocks=needed,
         shared_blocks=n_shared, kv_format=kv_format)
+
+
+@dataclasses.dataclass
+class VerifyBatch:
+    """Inputs of one speculative-verify step: T new tokens per sequence (the
+    pending token and T - 1 draft proposals) whose K/V are still to be
+    appended at positions .. positions + T - 1 (their cache slots are NaN
+    until then); context_lens of `paged` already count them."""
+    paged: PagedBatch
+    q: torch.Tensor          # bf16 [B][T][n_q][d]
+    k_new: torch.Tensor      # bf16 [B][T][n_kv][d]
+    v_new: torch.Tensor
+    positions: torch.Tensor  # int32 [B] = context_lens - T
+
+    @property
+    def T(self) -> int:
+        return self.q.shape[1]
+
+
+def make_verify_batch(batch: int, n_q: int, n_kv: int, block_size: int, ctx_lens: List[int],
+                      T: int, *, seed: int = DATA_SEED, table_seed: int = TABLE_SEED,
+                      device="cpu", kv_std: float = 1.0, poison: bool = True) -> VerifyBatch:
+    """make_batch's cache and tables for contexts of ctx_lens[b] tokens (the
+    last T of them new), fresh N(0, 1) queries [B][T][n_q][d], and the new
+    tokens' K/V taken from the drawn cache before their slots are poisoned."""
+    assert T >= 1 and all(c >= T for c in ctx_lens)
+    pb = make_batch(batch, n_q, n_kv, block_size, ctx_lens, seed=seed, table_seed=table_seed,
+                    device=device, kv_std=kv_std, poison=poison)
+    gen = torch.Generator(device=device).manual_seed(seed + 17)
+    q = _randn_bf16((batch, T, n_q, pb.head_dim), 1.0, gen, device)
+    bs = block_size
+    pos = torch.tensor([c - T for c in ctx_lens], dtype=torch.int64)
+    P = pos[:, None] + torch.arange(T)[None, :]
+    blk = pb.block_tables.cpu().long()[torch.arange(batch)[:, None], P // bs].to(device)
+    slot = (P % bs).to(device)
+    kr, vr = untile_pool(pb.k_cache), untile_pool(pb.v_cache)
+    k_new = kr[blk, :, slot, :].clone()  # [B][T][n_kv][d]
+    v_new = vr[blk, :, slot, :].clone()
+    if poison:
+        kr[blk, :, slot, :] = float("nan")
+        vr[blk, :, slot, :] = float("nan")
+    pb.k_cache = tile_pool(kr)
+    pb.v_cache = tile_pool(vr)
+    return VerifyBatch(paged=pb, q=q, k_new=k_new, v_new=v_new,
+                       positions=pos.to(torch.int32).to(device))
+
+
+def make_verify_workload(name: str, T: int, device="cpu") -> VerifyBatch:
+    """A named workload's batch, tables and context lengths (which then
+    count the T new tokens of every sequence) as a verify step."""
+    w = WORKLOADS[name]
+    return make_verify_batch(w.batch, w.n_q, w.n_kv, w.block_size, context_lengths(w), T,
+                             device=device, kv_std=w.kv_std)
 
 
 NAN_CODE = 0x7F  # E4M3 S.1111.111

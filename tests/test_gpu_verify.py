@@ -1,0 +1,118 @@
+"""Parity of multi-query (speculative verify) attention and the multi-token
+append, through the C ABI, with the float64 oracle on the same seeded inputs.
+
+pgd_kv_append_tokens: the pools bit exact against the oracle's own append of
+the same tokens into CPU copies of the caches as generated.  Attention:
+max abs error <= 2e-2 and mean abs error <= 2e-3 against the oracle, every
+element; T = 1 is bit-identical to the decode entry point.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_kv_gb300 as pgd
+from paged_gqa_decode_kv_gb300 import inputs
+from gpu_common import assert_no_device_errors, cache_bits, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_errors():
+    pgd.device_errors(clear=True)
+    yield
+    assert_no_device_errors()
+
+
+def _batch(n_q, n_kv, bs, lens, T, seed=1234):
+    return inputs.make_verify_batch(len(lens), n_q, n_kv, bs, lens, T, seed=seed,
+                                    table_seed=seed + 7, device="cuda")
+
+
+def _oracle(vb):
+    """The oracle's own append into CPU copies of the generated caches, then
+    its verify attention over them."""
+    pb = vb.paged
+    k, v = oracle.kv_append_tokens(pb.k_cache.cpu(), pb.v_cache.cpu(), vb.k_new.cpu(),
+                                   vb.v_new.cpu(), pb.block_tables.cpu(), vb.positions.cpu())
+    out = oracle.paged_verify_attention(vb.q.cpu(), k, v, pb.block_tables.cpu(),
+                                        pb.context_lens.cpu(), pb.scale)
+    return out, k, v
+
+
+def _gpu(vb, num_splits=0):
+    pb = vb.paged
+    pgd.kv_append_tokens(vb.k_new, vb.v_new, pb.k_cache, pb.v_cache, pb.block_tables,
+                         vb.positions)
+    return pgd.paged_verify_attention(None, vb.q, pb.k_cache, pb.v_cache, pb.block_tables,
+                                      pb.context_lens, pb.scale, num_splits=num_splits)
+
+
+SMALL = [
+    # (n_q, n_kv, bs, T, lens)
+    (4, 4, 16, 2, [2]),
+    (8, 4, 16, 4, [4, 5, 17]),
+    (16, 4, 16, 4, [33, 200, 513]),
+    (16, 4, 32, 3, [31, 32, 33, 700]),
+    (32, 8, 16, 4, [64, 4, 95]),
+    (32, 8, 32, 2, [512, 129]),
+    (64, 8, 16, 2, [129, 1000, 32]),
+    (8, 1, 16, 2, [300, 5]),
+    (2, 1, 16, 8, [47, 8]),
+    (4, 4, 16, 16, [16, 300]),
+    (8, 8, 32, 5, [90, 250]),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "nq%d_nkv%d_bs%d_T%d_%s" % (
+    c[0], c[1], c[2], c[3], "-".join(map(str, c[4]))))
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_verify_small(case, num_splits):
+    n_q, n_kv, bs, T, lens = case
+    vb = _batch(n_q, n_kv, bs, lens, T)
+    want, k, v = _oracle(vb)
+    got = _gpu(vb, num_splits)
+    torch.cuda.synchronize()
+    assert np.array_equal(cache_bits(vb.paged.k_cache), k)
+    assert np.array_equal(cache_bits(vb.paged.v_cache), v)
+    compare(got, want, "verify T=%d splits=%d" % (T, num_splits))
+
+
+@pytest.mark.parametrize("G,T", [(1, 16), (2, 8), (4, 4), (4, 3), (8, 2)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_verify_ragged(G, T, bs):
+    g = torch.Generator().manual_seed(G * 100 + T * 10 + bs)
+    lens = torch.randint(T, 1500, (19,), generator=g).tolist()
+    vb = _batch(4 * G, 4, bs, lens, T, seed=77 + G)
+    want, _, _ = _oracle(vb)
+    compare(_gpu(vb), want, "verify ragged G=%d T=%d bs=%d" % (G, T, bs))
+
+
+def test_t1_equals_decode_bit_exactly():
+    vb = _batch(32, 8, 16, [1, 17, 300, 2048], 1)
+    pb = vb.paged
+    pgd.kv_append_tokens(vb.k_new, vb.v_new, pb.k_cache, pb.v_cache, pb.block_tables,
+                         vb.positions)
+    a = pgd.paged_verify_attention(None, vb.q, pb.k_cache, pb.v_cache, pb.block_tables,
+                                   pb.context_lens, pb.scale)
+    b = pgd.paged_decode_attention(None, vb.q[:, 0].contiguous(), pb.k_cache, pb.v_cache,
+                                   pb.block_tables, pb.context_lens, pb.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a[:, 0].view(torch.int16), b.view(torch.int16))
+
+
+def test_rows_past_16_are_refused():
+    vb = _batch(8, 1, 16, [40], 4)
+    pb = vb.paged
+    with pytest.raises(pgd.PGDError):
+        pgd.paged_verify_attention(None, vb.q, pb.k_cache, pb.v_cache, pb.block_tables,
+                                   pb.context_lens, pb.scale)
+
+
+def test_verify_full_size_batch16_ctx8192_t4():
+    """The benchmark's batch (16 x 8192 tokens, 32/8 heads) verifying 4
+    tokens per sequence: 16 query rows per KV head on one pass."""
+    vb = _batch(32, 8, 16, [8192] * 16, 4)
+    want, _, _ = _oracle(vb)
+    compare(_gpu(vb), want, "verify batch16 ctx8192 T=4")
