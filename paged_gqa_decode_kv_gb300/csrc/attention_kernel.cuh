@@ -971,11 +971,21 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     // Two MMA stages (256 tokens) per iteration: one tile maximum, one named
     // barrier and one rescale decision serve both, so the fixed latency of a
     // step (waits, tensor-memory loads, barrier, fences) is paid once per 256
-    // tokens.  Thread t owns token row t of each of the two stages.
+    // tokens.  Thread t owns token row t of each of the two stages.  (One
+    // stage per iteration for 16 query rows.)
     const int t = tid;  // 0..127: token row of S
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     constexpr int NCT = 128;
     constexpr int NSC = (FP8 || G > 8) ? 16 : 8;  // S columns per stage (8-bit: high and low parts)
+    // MMA stages per iteration: two, or one for 16 query rows (whose per-row
+    // arrays would not fit the register budget twice over)
+    constexpr int SPI = G > 8 ? 1 : 2;
+    auto stage_max = [](const float (&x)[SPI][G], int h) {
+      float m = x[0][h];
+#pragma unroll
+      for (int u = 1; u < SPI; ++u) m = fmaxf(m, x[u][h]);
+      return m;
+    };
     // Query token of each column, for the causal mask among a multi-query
     // call's T new tokens (token a of the context is seen by column h iff
     // a - (ctx - T) <= tok[h]); padding columns see nothing.
@@ -999,12 +1009,12 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
 #pragma unroll
       for (int h = 0; h < G; ++h) { m_ref[h] = -INFINITY; l_part[h] = 0.f; qsc[h] = 0.f; }
 
-      for (int st = 0; st < nstages; st += 2, ++it) {
-        const int n2 = min(2, nstages - st);  // stages in this iteration
-        bool valid[2] = {false, false};
-        int msk[2] = {0, 0};
-        int lim[2] = {0, 0};  // rows p.v reads: the valid length rounded up to 16
-        int epos[2] = {0, 0};  // this row's token minus the first new token (T > 1)
+      for (int st = 0; st < nstages; st += SPI, ++it) {
+        const int n2 = min(SPI, nstages - st);  // stages in this iteration
+        bool valid[SPI] = {};
+        int msk[SPI] = {};
+        int lim[SPI] = {};  // rows p.v reads: the valid length rounded up to 16
+        int epos[SPI] = {};  // this row's token minus the first new token (T > 1)
         // Invalid-block mask of each stage: the K producer wrote it before
         // arming full_k; the q.k^T issuer acquired full_k and then released
         // m_ready.  (Waiting on full_k here could alias under the bf16
@@ -1012,7 +1022,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         // two phases ahead.)  The 8-entry mask ring cannot move on before
         // these stages free their S buffers.
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < SPI; ++u) {
           if (u < n2) {
             const int su = s + u, sbu = su % NSB;
             wait_or_abort(&s_full[sbu], (uint32_t)(su / NSB) & 1u, abort_flag, p.err);
@@ -1033,9 +1043,9 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
           }
         }
         tc_fence_after();
-        uint32_t sv[2][NSC];
+        uint32_t sv[SPI][NSC];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < SPI; ++u) {
           if (u < n2) {
             const uint32_t a0 = tmem + lane_base + col_s((s + u) % NSB);
             tmem_ld8_async(a0, sv[u]);
@@ -1043,7 +1053,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
           }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < SPI; ++u) {
           if (u < n2) {
             tmem_wait8(sv[u]);
             if (NSC > 8) tmem_wait8(sv[u] + 8);
@@ -1056,15 +1066,15 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
           if (n2 > 1) mbar_arrive(&s_free[(s + 1) % NSB]);
         }
 
-        float sc_[2][G];
+        float sc_[SPI][G];
         if constexpr (FP8) {
           // Key scale of each token (the K slot is refilled only after these
           // four warps release it, so waiting on full_k cannot alias), and at
           // a segment's first stage the Q scales (the K producer wrote them
           // before q_ready, which the q.k^T issuer acquired before m_ready).
-          float ks[2] = {0.f, 0.f};
+          float ks[SPI] = {};
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
+          for (int u = 0; u < SPI; ++u) {
             if (u < n2) {
               const int kslot = (s + u) % L::NSK;  // full_k already waited on above
               ks[u] = *reinterpret_cast<const float *>(
@@ -1082,7 +1092,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
             if (st == 0) mbar_arrive(&q_free[k & 1]);
           }
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
+          for (int u = 0; u < SPI; ++u)
 #pragma unroll
             for (int h = 0; h < G; ++h)
               sc_[u][h] = valid[u] ? (__uint_as_float(sv[u][h]) + __uint_as_float(sv[u][8 + h])) *
@@ -1090,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
                                    : -INFINITY;
         } else {
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
+          for (int u = 0; u < SPI; ++u)
 #pragma unroll
             for (int h = 0; h < G; ++h)
               sc_[u][h] = (valid[u] && tok[h] >= epos[u])
@@ -1098,7 +1108,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
                               : -INFINITY;
         }
 
-        // Does any score of the 2 x 128 rows exceed its head's reference by
+        // Does any score of the SPI x 128 rows exceed its head's reference by
         // more than 2^8?  One vote per warp (rarely yes); only then are the
         // exact tile maxima reduced and the reference moved.  A segment's
         // first iteration, where the reference is -inf, moves it unasked.
@@ -1108,7 +1118,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
           bool over = false;
 #pragma unroll
           for (int h = 0; h < G; ++h)
-            over |= fmaxf(sc_[0][h], sc_[1][h]) > m_ref[h] + kRescaleLog2;
+            over |= stage_max(sc_, h) > m_ref[h] + kRescaleLog2;
           const bool wover = __any_sync(kFullMask, over);
           if (lane == 0) over_flag[rb * 4 + warp] = wover ? 1 : 0;
           named_barrier_sync(1, NCT);
@@ -1118,7 +1128,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         if (move) {
           float v2[G];
 #pragma unroll
-          for (int h = 0; h < G; ++h) v2[h] = fmaxf(sc_[0][h], sc_[1][h]);
+          for (int h = 0; h < G; ++h) v2[h] = stage_max(sc_, h);
           const float wm = warp_reduce_heads<G, true>(v2, lane);
           constexpr int SH = 5 - kLog2<G>;  // lanes per head after the reduction
           if ((lane & ((1 << SH) - 1)) == 0) red[(rb * 4 + warp) * RMAX + (lane >> SH)] = wm;
@@ -1168,7 +1178,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         // probabilities, rounded as the tensor cores will see them (bf16, or
         // f16 beside the 8-bit cache's f16 V; p <= 2^8 either way)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < SPI; ++u) {
           if (u < n2) {
             const int su = s + u, pbuf = su & 1;
             uint32_t packed[8] = {0, 0, 0, 0, 0, 0, 0, 0};
