@@ -17,6 +17,9 @@ Contents
     (speculative verify) attention, T new query tokens per sequence with the
     causal mask among them, and appending T tokens, over
     ``pgd_oracle_verify.c``.
+  * ``mla_attention`` / ``mla_append`` -- decode attention over an MLA
+    latent cache (576 values per token shared by all heads; absorbed query;
+    512-d latent output), over ``pgd_oracle_mla.c``.
   * ``kv_formula`` -- the KV-cache byte count in closed form.
   * ``block_model`` -- a plain-Python model of block tables, reference counts
     and copy-on-write.
@@ -37,7 +40,7 @@ from . import block_model  # noqa: F401  (re-exported)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRCS = [os.path.join(_HERE, "pgd_oracle.c"), os.path.join(_HERE, "pgd_oracle_fp8.c"),
-         os.path.join(_HERE, "pgd_oracle_verify.c")]
+         os.path.join(_HERE, "pgd_oracle_verify.c"), os.path.join(_HERE, "pgd_oracle_mla.c")]
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "libpgd_oracle.so")
 _lock = threading.Lock()
@@ -95,6 +98,10 @@ def _load():
         lib.oracle_paged_verify_attention.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, D,
                                                       I, I]
         lib.oracle_paged_verify_attention.restype = I
+        lib.oracle_mla_append.argtypes = [P, P, P, P, I, I, I, I, I]
+        lib.oracle_mla_append.restype = I
+        lib.oracle_mla_attention.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D, I, I]
+        lib.oracle_mla_attention.restype = I
         _lib = lib
         return lib
 
@@ -341,4 +348,45 @@ def paged_verify_attention(q, k_cache, v_cache, block_tables, context_lens, scal
                                                float(scale), int(n_threads), int(mutation))
     if st:
         raise ValueError("oracle: invalid context length or block id (status %d)" % st)
+    return out
+
+
+def _mla_dims(cache: np.ndarray):
+    """(NB, bs, D) of a latent pool stored as [NB][bs/8][D/8][8][8]."""
+    if cache.ndim != 5 or cache.shape[3:] != (8, 8):
+        raise ValueError("latent pool must be [NB][bs/8][D/8][8][8] (8x8 core-matrix tiles)")
+    NB, rg, nc = cache.shape[:3]
+    return NB, rg * 8, nc * 8
+
+
+def mla_append(cache, c_new, block_tables, positions):
+    """Return a copy of the latent pool with c_new[b] ([B][D] bf16) written at
+    logical position positions[b]."""
+    ca = _u16(cache).copy()
+    cn = _u16(c_new)
+    ta, pa = _i32(block_tables), _i32(positions)
+    NB, bs, D = _mla_dims(ca)
+    st = _load().oracle_mla_append(_p(ca), _p(cn), _p(ta), _p(pa), cn.shape[0], D, bs,
+                                   ta.shape[1], NB)
+    if st:
+        raise ValueError("oracle: position or block id out of range")
+    return ca
+
+
+def mla_attention(q, cache, block_tables, context_lens, scale: float, dv: int = 512,
+                  n_threads: int = 0, mutation: int = 0) -> np.ndarray:
+    """float64 out[B][H][dv]: softmax over t < context_lens[b] of
+    scale * q[b][h] . c_t (all D cached values of token t), weighting the
+    first dv values of each c_t."""
+    qa, ca = _u16(q), _u16(cache)
+    ta, la = _i32(block_tables), _i32(context_lens)
+    B, H, D = qa.shape
+    NB, bs, D2 = _mla_dims(ca)
+    assert D2 == D
+    out = np.zeros((B, H, dv), dtype=np.float64)
+    st = _load().oracle_mla_attention(_p(out), _p(qa), _p(ca), _p(ta), _p(la), B, H, D, dv, bs,
+                                      ta.shape[1], NB, float(scale), int(n_threads),
+                                      int(mutation))
+    if st:
+        raise ValueError("oracle: invalid argument, context length or block id (status %d)" % st)
     return out

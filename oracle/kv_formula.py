@@ -11,6 +11,12 @@ Sources (page title, section):
   * "The math of Transformer inference", section 5: 819,200 B per token for
     LLaMA-2-13B (L=40, K=40, H=128, bf16), 327,680 B for LLaMA-3-70B (L=80,
     K=8, H=128).
+  * "LLM inference systems engineering", 2.4.2 (MLA): a latent cache stores
+    (d_c + d_r) * L * b bytes per token -- 36,864 B (36 KiB) at d_c=512,
+    d_r=64, L=32, bf16, 131072 / 36864 = 3.56 x less than the GQA case.
+  * "The math of Transformer inference", MLA section: 61 x 576 x 2 = 70,272
+    bytes per token for DeepSeek-V3; MHA with the same heads would store
+    128 x (192 + 128) = 40,960 elements per layer, 71 x MLA's 576.
   * "Module 10: inference and serving", Lab 2: a 4-layer toy decoder with two
     KV heads of width 32 in float32 holds 555,008 bytes at 271 cached tokens,
     equal to 2*4*2*32*4*t.
@@ -32,3 +38,9 @@ def paged_pool_bytes(num_blocks: int, block_size: int, H_kv: int, d_h: int, b: i
     """Physical bytes of a paged pool of num_blocks blocks of block_size
     tokens: the same closed form with B*T replaced by the slots it holds."""
     return kv_bytes(L, 1, num_blocks * block_size, H_kv, d_h, b)
+
+
+def mla_bytes_per_token(L: int, d_c: int, d_r: int, b: int) -> int:
+    """Bytes per token of an MLA latent cache: the latent and the decoupled
+    RoPE key of every layer."""
+    return (d_c + d_r) * L * b
