@@ -257,6 +257,40 @@ pgd_status pgd_paged_verify_attention(void *out, const void *q, const void *k_ca
                                       void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* MLA latent cache (multi-head latent attention, absorbed form)           */
+/* ---------------------------------------------------------------------- */
+/* A latent cache stores, per layer and token, the latent c_t (d_c = 512) and
+ * a decoupled RoPE key k_t^R (d_r = 64): 576 values shared by every head
+ * ("The math of Transformer inference", MLA section; "LLM inference systems
+ * engineering", 2.4.2).  With W^UK absorbed into the query and W^UV into the
+ * output projection (same book, 2.8.2), decode attention of head h is
+ *     s_t = scale * q[b][h] . c_t       (all 576 values; q = [W_h^{UK T} q_h^C ; q_h^R])
+ *     out[b][h][j] = sum_t softmax(s)_t c_t[j]     (j < 512, t < context_lens[b])
+ * -- MQA with every head reading the one cache.
+ *
+ * Latent pool: bf16 [NB][bs/8][72][8][8] (block tiles of bs x 576 values as
+ * 8 x 8 core matrices: element (slot s, value i) at
+ * ((s / 8) * 72 + i / 8) * 64 + (s % 8) * 8 + i % 8); bs in {16, 32, 64};
+ * block tables and context lengths as for the GQA cache.  q: bf16 [B][H][576];
+ * out: bf16 [B][H][512].  d must be 576 and dv 512 (else UNSUPPORTED).
+ * pgd_mla_append writes c_new[b] (bf16 [B][576]) at position positions[b]
+ * (bit exact).  pgd_mla_decode_attention: fp32 scores and softmax, bf16
+ * probabilities and latent values on the tensor cores, fp32 accumulation,
+ * bf16 output; num_splits = parts of each context (0 = automatic); with more
+ * than one part it needs pgd_mla_workspace_size(B, H, num_splits) bytes of
+ * 256-byte-aligned workspace (no zeroing needed), else workspace may be NULL.
+ * Device errors as for pgd_paged_decode_attention. */
+size_t pgd_mla_workspace_size(int32_t B, int32_t H, int32_t num_splits);
+pgd_status pgd_mla_append(const void *c_new, void *cache, const int32_t *block_tables,
+                          const int32_t *positions, int32_t B, int32_t d, int32_t bs, int32_t MB,
+                          int32_t NB, void *stream);
+pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
+                                    const int32_t *block_tables, const int32_t *context_lens,
+                                    int32_t B, int32_t H, int32_t d, int32_t dv, int32_t bs,
+                                    int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* ---------------------------------------------------------------------- */
 /* cascade: shared prefixes read once per group                            */
 /* ---------------------------------------------------------------------- */
 /* pgd_paged_decode_attention for a batch in which groups of sequences share

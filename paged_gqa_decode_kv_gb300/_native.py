@@ -42,6 +42,10 @@ SIGNATURES = {
     "pgd_verify_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
     "pgd_paged_verify_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                                     _I, _P, _Z, _P], _I),
+    "pgd_mla_workspace_size": ([_I, _I, _I], _Z),
+    "pgd_mla_append": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
+    "pgd_mla_decode_attention": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
+                                  _P], _I),
     "pgd_cascade_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _Z),
     "pgd_cascade_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P], _I),
@@ -298,6 +302,54 @@ def paged_verify_attention(out, q, k_cache, v_cache, block_tables, context_lens,
     _check(lib().pgd_paged_verify_attention(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         B, T, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def _mla_pool_dims(pool: torch.Tensor) -> Tuple[int, int, int]:
+    """(NB, bs, D) of a latent pool bf16 [NB][bs/8][D/8][8][8]."""
+    if pool.dim() != 5 or tuple(pool.shape[3:]) != (8, 8):
+        raise ValueError("latent pool must be [NB][bs/8][D/8][8][8]")
+    return pool.shape[0], pool.shape[1] * 8, pool.shape[2] * 8
+
+
+def mla_append(c_new, cache, block_tables, positions, stream=None) -> None:
+    """Write c_new[b] ([B][576] bf16) at logical position positions[b]."""
+    _need(c_new, torch.bfloat16, "c_new")
+    _need(cache, torch.bfloat16, "cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(positions, torch.int32, "positions")
+    NB, bs, D = _mla_pool_dims(cache)
+    B, MB = block_tables.shape
+    _check(lib().pgd_mla_append(_ptr(c_new), _ptr(cache), _ptr(block_tables), _ptr(positions),
+                                B, D, bs, MB, NB, _stream(stream)))
+
+
+def mla_workspace_size(B: int, H: int, num_splits: int = 0) -> int:
+    return int(lib().pgd_mla_workspace_size(B, H, num_splits))
+
+
+def mla_decode_attention(out, q, cache, block_tables, context_lens, scale: float,
+                         num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """out[B][H][512] (bf16) = decode attention of the absorbed queries q
+    ([B][H][576]) over the latent cache."""
+    _need(q, torch.bfloat16, "q")
+    _need(cache, torch.bfloat16, "cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, H, D = q.shape
+    NB, bs, D2 = _mla_pool_dims(cache)
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = torch.empty(max(256, mla_workspace_size(B, H, num_splits)), dtype=torch.uint8,
+                                device=q.device)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_mla_decode_attention(
+        _ptr(out), _ptr(q), _ptr(cache), _ptr(block_tables), _ptr(context_lens), B, H, D, 512,
+        bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 

@@ -25,6 +25,11 @@ cudaError_t attention_launch_fp8(const AttnParams &p, int G, int bs, int grid,
 cudaError_t prefix_attention_launch(const PrefixParams &p, int G, int bs, int grid,
                                     cudaStream_t stream);
 cudaError_t cascade_combine_launch(const CombineParams &p, int G, cudaStream_t stream);
+cudaError_t mla_attention_launch(const MlaParams &p, cudaStream_t stream);
+cudaError_t mla_append_launch(const void *c_new, void *cache, const int32_t *tables,
+                              const int32_t *pos, int B, int bs, int MB, int NB, int32_t *err,
+                              cudaStream_t stream);
+int mla_heads_per_cta();
 cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
                                  void *v_cache, const int32_t *tables, const int32_t *pos,
                                  int pos_offset, int B, int n_kv, int bs, int MB, int NB,
@@ -653,6 +658,103 @@ pgd_status pgd_cascade_decode_attention(
   cp.parts = pa.grid;
   e = cascade_combine_launch(cp, pa.G, st);
   if (e != cudaSuccess) return cuda_fail(e, "cascade combine launch");
+  return ok();
+}
+
+// ------------------------------------------------------------- MLA latent cache
+
+constexpr int kMlaD = 576, kMlaDv = 512;
+
+// Parts of each sequence's context for an automatic MLA call: as many as
+// fill the SMs with one CTA each (the kernel's shared memory allows one per
+// SM), at least one.
+int mla_auto_parts(int32_t B, int32_t H) {
+  const long long units = (long long)B * ((H + mla_heads_per_cta() - 1) / mla_heads_per_cta()) * 2;
+  if (units <= 0) return 1;
+  return (int)std::max(1LL, std::min(64LL, (long long)sm_count() / units));
+}
+
+size_t mla_ws_bytes(int32_t B, int32_t H, int parts) {
+  if (parts <= 1) return 0;
+  const size_t rows = (size_t)B * H * parts;
+  return round_up(rows * 2 * 4, kWsAlign) + rows * kMlaDv * 4;
+}
+
+size_t pgd_mla_workspace_size(int32_t B, int32_t H, int32_t num_splits) {
+  if (B < 0 || H <= 0 || num_splits < 0) return 0;
+  const int parts = num_splits > 0 ? num_splits : mla_auto_parts(B, H);
+  clear_error_detail();
+  return std::max<size_t>(mla_ws_bytes(B, H, parts), 256);
+}
+
+pgd_status pgd_mla_append(const void *c_new, void *cache, const int32_t *block_tables,
+                          const int32_t *positions, int32_t B, int32_t d, int32_t bs, int32_t MB,
+                          int32_t NB, void *stream) {
+  if (B < 0) return fail(PGD_ERR_INVALID_ARG, "B = %d", B);
+  if (d != kMlaD) return fail(PGD_ERR_UNSUPPORTED, "d = %d (576 cached values per token)", d);
+  if (bs != 16 && bs != 32 && bs != 64) return fail(PGD_ERR_UNSUPPORTED, "block size %d", bs);
+  if (MB <= 0 || NB <= 0) return fail(PGD_ERR_INVALID_ARG, "MB, NB must be > 0");
+  if ((long long)B * MB >= 0x7fffffffLL) return fail(PGD_ERR_INVALID_ARG, "B * MB >= 2^31");
+  if (B == 0) return ok();
+  if (!c_new || !cache || !block_tables || !positions)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(c_new, 16) || !aligned(cache, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  int32_t *err = nullptr;
+  pgd_status s = error_word(&err);
+  if (s != PGD_OK) return s;
+  cudaError_t e = mla_append_launch(c_new, cache, block_tables, positions, B, bs, MB, NB, err,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "MLA append launch");
+  return ok();
+}
+
+pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
+                                    const int32_t *block_tables, const int32_t *context_lens,
+                                    int32_t B, int32_t H, int32_t d, int32_t dv, int32_t bs,
+                                    int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+  if (B < 0 || H <= 0) return fail(PGD_ERR_INVALID_ARG, "B = %d, H = %d", B, H);
+  if (d != kMlaD || dv != kMlaDv)
+    return fail(PGD_ERR_UNSUPPORTED, "d = %d, dv = %d (576 and 512)", d, dv);
+  if (bs != 16 && bs != 32 && bs != 64) return fail(PGD_ERR_UNSUPPORTED, "block size %d", bs);
+  if (MB <= 0 || NB <= 0) return fail(PGD_ERR_INVALID_ARG, "MB, NB must be > 0");
+  if (!(scale > 0.f) || !isfinite(scale)) return fail(PGD_ERR_INVALID_ARG, "scale must be > 0");
+  if (num_splits < 0 || num_splits > 1024) return fail(PGD_ERR_INVALID_ARG, "num_splits");
+  if ((long long)B * MB >= 0x7fffffffLL || (long long)B * H * 1024 >= 0x7fffffffLL)
+    return fail(PGD_ERR_INVALID_ARG, "sizes too large");
+  if (B == 0) return ok();
+  if (!out || !q || !cache || !block_tables || !context_lens)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(cache, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  const int parts = num_splits > 0 ? num_splits : mla_auto_parts(B, H);
+  const size_t need = mla_ws_bytes(B, H, parts);
+  if (need > 0 && (!workspace || !aligned(workspace, kWsAlign) || workspace_bytes < need))
+    return fail(PGD_ERR_WORKSPACE, "workspace: %zu bytes (256-aligned) needed", need);
+  int32_t *err = nullptr;
+  pgd_status s = error_word(&err);
+  if (s != PGD_OK) return s;
+  MlaParams p;
+  p.out = static_cast<__nv_bfloat16 *>(out);
+  p.q = static_cast<const __nv_bfloat16 *>(q);
+  p.cache = static_cast<const unsigned char *>(cache);
+  p.tables = block_tables;
+  p.ctx = context_lens;
+  p.B = B;
+  p.H = H;
+  p.MB = MB;
+  p.NB = NB;
+  p.bs = bs;
+  p.n_parts = parts;
+  p.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);
+  unsigned char *ws = static_cast<unsigned char *>(workspace);
+  const size_t rows = (size_t)B * H * parts;
+  p.part_ml = need ? reinterpret_cast<float *>(ws) : nullptr;
+  p.part_o = need ? reinterpret_cast<float *>(ws + round_up(rows * 2 * 4, kWsAlign)) : nullptr;
+  p.err = err;
+  cudaError_t e = mla_attention_launch(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "MLA attention launch");
   return ok();
 }
 

@@ -1,0 +1,537 @@
+// mla_attention.cu -- decode attention over an MLA latent cache (multi-head
+// latent attention in its absorbed form), and the append of latent rows.
+//
+// "The math of Transformer inference", MLA section: per layer and token the
+// cache holds the latent c_t (d_c = 512) and a decoupled RoPE key k_t^R
+// (d_r = 64), 576 values shared by every head; with W^UK absorbed into the
+// query and W^UV into the output projection, head h scores
+//     s_t = scale * q_h . c_t          (q_h = [W_h^{UK T} q_h^C ; q_h^R], 576)
+// and returns the 512-d latent  o_h = sum_t softmax(s)_t c_t[0 .. 512)
+// ("LLM inference systems engineering", 2.8.2: the identities behind the
+// absorption).  Decode is then MQA with G = n_h: one cache, all heads.
+//
+// On the tensor cores the head rows sit on the MMA's M side and the tokens on
+// N, as in the shared-prefix pass:
+//   S[128 rows][64 tok]  = Q[128 rows][576] . C^T        (A = Q, B = C, both K-major)
+//   O[128 rows][256 d]  += P[128 rows][64 tok] . C[:, half] (A = P K-major, B = C MN-major)
+// with 64 real head rows per CTA.  The A operands are 128 rows tall; rows
+// 64..127 are read from whatever follows Q and P in shared memory and only
+// produce rows of S and O that nothing reads (the layout keeps those reads
+// inside the allocation).  A 576-d latent row is 1152 B, so a 64-token stage
+// is 72 KiB; two stages, Q (64 heads) and P fill the 227 KB.  The 512 output
+// dims do not fit tensor memory beside S (256 fp32 columns each), so a CTA
+// computes one half of them: CTA (sequence, 64-head group, half, part).  The
+// latent pool is tiled as 8 x 8 core matrices per 8 tokens, so one bulk copy
+// per block lands an MMA-ready operand: element (slot s, dim i) of a block at
+// ((s / 8) * 72 + i / 8) * 64 + (s % 8) * 8 + i % 8.
+//
+// Roles (128 threads): warps 0-1 softmax and epilogue (thread = head row,
+// row statistics thread-local), warp 2 producer, warp 3 MMA issuer and
+// tensor-memory owner.  Every wait is bounded.  A context longer than one
+// part is split over CTAs; the parts' (max, sum, output) states are merged by
+// mla_combine_kernel.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "attention_kernel.cuh"
+
+namespace pgd {
+namespace mla {
+
+using tc::fence_proxy_async;
+using tc::smem_desc;
+using tc::tc_fence_after;
+using tc::tc_fence_before;
+using tc::umma_bf16;
+using tc::umma_commit;
+using tc::wait_or_abort;
+
+constexpr int D = 576;          // cached values per token (latent + RoPE key)
+constexpr int DV = 512;         // latent dims (the value)
+constexpr int DH = 256;         // output dims per CTA
+constexpr int TOKS = 64;        // tokens per stage
+constexpr int NH = 64;          // head rows per CTA
+constexpr int THREADS = 128;
+constexpr int GRP = (D / 8) * 128;   // bytes per 8 rows of 576 values: 9216
+constexpr int STAGE = (TOKS / 8) * GRP;  // 73,728
+constexpr int Q_BYTES = (NH / 8) * GRP;  // 73,728
+constexpr int P_BYTES = (NH / 8) * 1024; // [8 row groups][8 token groups][8][16 B] = 8192
+// P, then Q, then the two stages: the 128-row A operands P and Q read their
+// rows 64..127 from the next 8 KiB (Q) and the next 72 KiB (stage 0).
+constexpr int OFF_P = 0;
+constexpr int OFF_Q = OFF_P + P_BYTES;
+constexpr int OFF_C = OFF_Q + Q_BYTES;
+constexpr int OFF_BAR = OFF_C + 2 * STAGE;
+constexpr int OFF_MISC = OFF_BAR + 128;
+constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
+static_assert(SMEM_BYTES <= 232448, "MLA kernel exceeds 227 KB of shared memory");
+static_assert(OFF_Q - OFF_P >= P_BYTES && OFF_C - OFF_Q == Q_BYTES, "over-read layout");
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_O = 256;     // O: 256 columns; S buffers at 0 and 64
+
+// kind::f16, D f32, A and B bf16, M = 128, N = n; b_mn: B MN-major.
+__host__ __device__ constexpr uint32_t idesc(int n, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes (wait included).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
+      "%10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, "
+      "%27, %28, %29, %30, %31, %32};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+
+// Stages [first, last) of a sequence's ceil(ctx / 64) for part `part` of n.
+__device__ __forceinline__ void part_stages(int nst_seq, int part, int n_parts, int &first,
+                                            int &last) {
+  first = (int)((long long)nst_seq * part / n_parts);
+  last = (int)((long long)nst_seq * (part + 1) / n_parts);
+}
+
+template <int BS>
+__global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaParams p) {
+  constexpr int SBLK = TOKS / BS;          // blocks per stage
+  constexpr uint32_t TILE = BS * D * 2;    // one block's latent rows
+  constexpr uint32_t IDESC_QK = idesc(TOKS, false);
+  constexpr uint32_t IDESC_PV = idesc(DH, true);
+  static_assert(TOKS % BS == 0 && BS % 8 == 0, "block size");
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();  // q, the cache and the tables may come from the previous kernel
+
+  int w = (int)blockIdx.x;
+  const int part = w % p.n_parts;
+  w /= p.n_parts;
+  const int half = w & 1;
+  w >>= 1;
+  const int n_hg = (p.H + NH - 1) / NH;
+  const int hg = w % n_hg, b = w / n_hg;
+  if (b >= p.B) return;
+  const int rows = min(NH, p.H - hg * NH);  // real head rows of this CTA
+  const int ctx = __ldg(p.ctx + b);
+  const bool ctx_ok = ctx >= 1 && ctx <= p.MB * BS;
+  const int nst_seq = ctx_ok ? (ctx + TOKS - 1) / TOKS : 0;
+  int st0, st1;
+  part_stages(nst_seq, part, p.n_parts, st0, st1);
+  const int nst = st1 - st0;
+  if (!ctx_ok && tid == 0 && half == 0 && hg == 0 && part == 0)
+    atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
+
+  const int r = tid;  // head row (warps 0-1)
+  const bool row_ok = r < rows;
+  const int h = hg * NH + r;
+  // partial state slot of (b, h, part)
+  const size_t slot = ((size_t)b * p.H + h) * p.n_parts + part;
+
+  if (nst <= 0) {  // an empty part (or a rejected sequence): a -inf maximum
+    if (warp < 2 && row_ok && p.n_parts > 1) {
+      if (half == 0)
+        *reinterpret_cast<float2 *>(p.part_ml + slot * 2) = make_float2(-INFINITY, 0.f);
+      float4 *o = reinterpret_cast<float4 *>(p.part_o + slot * DV + half * DH);
+      for (int i = 0; i < DH / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *smem = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+  uint64_t *c_full = bars, *c_empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6;
+  uint64_t *p_full = bars + 8, *p_free = bars + 9, *o_done = bars + 10;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+  volatile int *bad_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);  // [2]
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&c_full[i], 1);
+      mbar_init(&c_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], 2);  // one arrival per softmax warp
+    }
+    mbar_init(p_full, 2);
+    mbar_init(p_free, 1);
+    mbar_init(o_done, 1);
+    mbar_init_fence();
+    *abort_flag = 0;
+  }
+  // Q rows as the K-major A operand: head row r, dims 8c..8c+7 in core
+  // matrix (r / 8, c), row r % 8; rows past the real heads are zeros.
+  {
+    const uint4 *qsrc = reinterpret_cast<const uint4 *>(p.q);
+    for (int i = tid; i < NH * (D / 8); i += THREADS) {
+      const int qr = i / (D / 8), c = i % (D / 8);
+      const uint4 v = (qr < rows) ? __ldg(qsrc + ((size_t)b * p.H + hg * NH + qr) * (D / 8) + c)
+                                  : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4 *>(smem + OFF_Q + (qr >> 3) * GRP + c * 128 + (qr & 7) * 16) = v;
+    }
+  }
+  if (warp == 3) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  fence_proxy_async();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int32_t *trow = p.tables + (size_t)b * p.MB;
+
+  // valid tokens of local stage i (the sequence's last stage may be partial)
+  auto stage_tokens = [&](int i) { return min(TOKS, ctx - (st0 + i) * TOKS); };
+
+  if (warp == 2) {
+    // ------------------------------------------------------------ producer
+    const uint64_t policy = l2_policy_evict_first();
+    for (int i = 0; i < nst; ++i) {
+      const int buf = i & 1;
+      const int nb = (stage_tokens(i) + BS - 1) / BS;
+      const int j = (st0 + i) * SBLK + lane;
+      const int blk = (lane < nb) ? __ldg(trow + j) : -1;
+      const bool ok = lane < nb && (unsigned)blk < (unsigned)p.NB;
+      const unsigned okmask = __ballot_sync(kFullMask, ok);
+      const unsigned want = (nb >= 32) ? ~0u : ((1u << nb) - 1u);
+      if (lane == 0) {
+        wait_or_abort(&c_empty[buf], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, p.err);
+        bad_mask[buf] = (int)(want & ~okmask);
+        if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
+        const uint32_t bytes = (uint32_t)__popc(okmask) * TILE;
+        if (*abort_flag || bytes == 0)
+          mbar_arrive(&c_full[buf]);
+        else
+          mbar_arrive_expect_tx(&c_full[buf], bytes);
+      }
+      __syncwarp();
+      if (ok && !*abort_flag)
+        bulk_copy_g2s(smem + OFF_C + buf * STAGE + lane * (BS / 8) * GRP,
+                      p.cache + (size_t)blk * TILE, TILE, &c_full[buf], policy);
+    }
+    if (lane == 0) {  // no copy may still be landing when the CTA exits
+      for (int k = 1; k <= 2 && k <= nst; ++k) {
+        const int last = nst - k;
+        mbar_wait_bounded(&c_full[last & 1], (uint32_t)(last >> 1) & 1u);
+      }
+    }
+  } else if (warp == 3) {
+    // ------------------------------------------------------- MMA issuer
+    // q.c^T of stage i before p.c of stage i - 1, so it overlaps the softmax
+    // of stage i - 1.
+    if (lane == 0) {
+      const uint64_t qd = smem_desc(smem_addr(smem + OFF_Q), 128, GRP, 0);
+      const uint64_t pd = smem_desc(smem_addr(smem + OFF_P), 128, 1024, 0);
+      for (int i = 0; i <= nst; ++i) {
+        if (i < nst) {
+          const int buf = i & 1;
+          wait_or_abort(&c_full[buf], (uint32_t)(i >> 1) & 1u, abort_flag, p.err);
+          wait_or_abort(&s_free[buf], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, p.err);
+          tc_fence_after();
+          if (!*abort_flag) {
+            // A = Q, B = C, both K-major: a k-step of 16 dims moves both by
+            // two core matrices (256 B)
+            const uint64_t cd = smem_desc(smem_addr(smem + OFF_C + buf * STAGE), 128, GRP, 0);
+#pragma unroll 4
+            for (int kk = 0; kk < D / 16; ++kk)
+              umma_bf16(tmem + (uint32_t)(buf * TOKS), qd + (uint64_t)(kk * 16),
+                        cd + (uint64_t)(kk * 16), IDESC_QK, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[buf]);
+        }
+        if (i >= 1) {
+          const int j = i - 1, buf = j & 1;
+          const int nkt = (stage_tokens(j) + 15) >> 4;  // 16-token steps with a valid token
+          wait_or_abort(p_full, (uint32_t)(j & 1), abort_flag, p.err);
+          tc_fence_after();
+          if (!*abort_flag) {
+            // A = P (K-major, tokens along K: 256 B per 16 tokens); B = C
+            // MN-major (dims along N, 128 B per 8 dims; 2 token groups =
+            // 18,432 B per 16 tokens), starting at this CTA's 256 dims
+            const uint64_t cvd =
+                smem_desc(smem_addr(smem + OFF_C + buf * STAGE + half * (DH / 8) * 128), GRP,
+                          128, 0);
+            for (int kt = 0; kt < nkt; ++kt)
+              umma_bf16(tmem + COL_O, pd + (uint64_t)(kt * 16),
+                        cvd + (uint64_t)(kt * (2 * GRP / 16)), IDESC_PV,
+                        (j > 0 || kt > 0) ? 1u : 0u);
+          }
+          umma_commit(&c_empty[buf]);  // the stage buffer may be refilled
+          umma_commit(p_free);         // P may be rewritten
+        }
+      }
+      umma_commit(o_done);
+      mbar_wait_bounded(o_done, 0);
+    }
+  } else {
+    // ------------------------------------- softmax, one head row per thread
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    for (int i = 0; i < nst; ++i) {
+      const int buf = i & 1;
+      const int nv = stage_tokens(i);
+      wait_or_abort(&s_full[buf], (uint32_t)(i >> 1) & 1u, abort_flag, p.err);
+      // (the producer wrote the stage's bad-block mask before arming c_full;
+      // that phase has completed and cannot move on before this stage's p.c)
+      wait_or_abort(&c_full[buf], (uint32_t)(i >> 1) & 1u, abort_flag, p.err);
+      const int bad = bad_mask[buf];
+      tc_fence_after();
+      float sv[TOKS];
+      tmem_ld32(tmem + lane_base + (uint32_t)(buf * TOKS), sv);
+      tmem_ld32(tmem + lane_base + (uint32_t)(buf * TOKS + 32), sv + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[buf]);
+      float rmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < TOKS; ++c) {
+        const bool ok = c < nv && !((bad >> (c / BS)) & 1);
+        sv[c] = ok ? sv[c] * p.qk_scale_log2 : -INFINITY;
+        rmax = fmaxf(rmax, sv[c]);
+      }
+      // lazy rescale: move the row's reference when exceeded by 2^8; the
+      // warp's O rows are rescaled together (tensor memory is warp-wide)
+      const bool need = rmax > m_ref + tc::kRescaleLog2;
+      float alpha = 1.f;
+      if (need) {
+        alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - rmax);
+        m_ref = rmax;
+        l *= alpha;
+      }
+      // P and the O rescale both wait for the previous p.c
+      wait_or_abort(p_free, ((uint32_t)(i & 1)) ^ 1u, abort_flag, p.err);
+      if (i > 0 && __any_sync(kFullMask, need)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < DH / 32; ++c) {
+          float ov[32];
+          tmem_ld32(tmem + lane_base + COL_O + c * 32, ov);
+#pragma unroll
+          for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+          tmem_st32(tmem + lane_base + COL_O + c * 32, ov);
+        }
+        tc_fence_before();
+      }
+      // probabilities in bf16, summed as the tensor cores see them; row r's
+      // 8-token pieces at core matrix (r / 8, token group), row r % 8
+      unsigned char *prow = smem + OFF_P + (r >> 3) * 1024 + (r & 7) * 16;
+#pragma unroll
+      for (int g = 0; g < TOKS / 8; ++g) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = g * 8 + 2 * k;
+          const __nv_bfloat16 a = __float2bfloat16_rn(sv[c] == -INFINITY ? 0.f : exp2f(sv[c] - m_ref));
+          const __nv_bfloat16 bb =
+              __float2bfloat16_rn(sv[c + 1] == -INFINITY ? 0.f : exp2f(sv[c + 1] - m_ref));
+          l += __bfloat162float(a) + __bfloat162float(bb);
+          pk[k] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(bb) << 16);
+        }
+        *reinterpret_cast<uint4 *>(prow + g * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      // Latent rows p.c reads that hold no valid token (the tail of the last
+      // block, blocks with a bad id) must not feed NaN into it: zero them
+      // (their copies have landed -- q.c^T waited for them -- and p.c of
+      // this stage has not been issued).
+      const int lim = ((nv + 15) & ~15);
+      if (nv < lim || bad) {
+        unsigned char *cs = smem + OFF_C + buf * STAGE;
+        for (int k = tid; k < lim * (D / 8); k += 64) {
+          const int t = k / (D / 8), c = k % (D / 8);
+          if (t >= nv || ((bad >> (t / BS)) & 1))
+            *reinterpret_cast<uint4 *>(cs + (t >> 3) * GRP + c * 128 + (t & 7) * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      named_barrier_sync(1, 64);  // both softmax warps have written P and zeroed
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    // ---- epilogue: this row's output (one part) or partial state
+    wait_or_abort(o_done, 0, abort_flag, p.err);
+    tc_fence_after();
+#pragma unroll 1
+    for (int c = 0; c < DH / 32; ++c) {
+      float ov[32];
+      tmem_ld32(tmem + lane_base + COL_O + c * 32, ov);  // warp-wide; stores by real rows
+      if (row_ok) {
+        if (p.n_parts == 1) {
+          const float inv = 1.f / l;
+          __nv_bfloat16 *o = p.out + ((size_t)b * p.H + h) * DV + half * DH + c * 32;
+#pragma unroll
+          for (int k = 0; k < 32; k += 2)
+            *reinterpret_cast<__nv_bfloat162 *>(o + k) =
+                __floats2bfloat162_rn(ov[k] * inv, ov[k + 1] * inv);
+        } else {
+          float4 *o = reinterpret_cast<float4 *>(p.part_o + slot * DV + half * DH + c * 32);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            o[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
+        }
+      }
+    }
+    if (row_ok && p.n_parts > 1 && half == 0)
+      *reinterpret_cast<float2 *>(p.part_ml + slot * 2) = make_float2(m_ref, l);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 3)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(TMEM_COLS)
+                 : "memory");
+}
+
+// Merge of the parts of each (sequence, head) by log-sum-exp: one CTA per
+// row, thread e owning dims e and e + 256.
+__global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p) {
+  pdl_wait();
+  const int row = (int)blockIdx.x;  // b * H + h
+  const int b = row / p.H;
+  if (b >= p.B) return;
+  const int c = __ldg(p.ctx + b);
+  if (c < 1 || c > p.MB * p.bs) return;  // rejected (flagged by the attention kernel)
+  const int e = threadIdx.x;
+  const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml) + (size_t)row * p.n_parts;
+  const float *po = p.part_o + (size_t)row * p.n_parts * DV;
+  float M = -INFINITY;
+  for (int k = 0; k < p.n_parts; ++k) M = fmaxf(M, __ldcg(&ml[k].x));
+  float L = 0.f, o0 = 0.f, o1 = 0.f;
+  for (int k = 0; k < p.n_parts; ++k) {
+    const float2 v = __ldcg(&ml[k]);
+    if (v.x == -INFINITY) continue;
+    const float w = exp2f(v.x - M);
+    L = fmaf(w, v.y, L);
+    o0 = fmaf(w, __ldcg(po + (size_t)k * DV + e), o0);
+    o1 = fmaf(w, __ldcg(po + (size_t)k * DV + e + DH), o1);
+  }
+  p.out[(size_t)row * DV + e] = __float2bfloat16_rn(o0 / L);
+  p.out[(size_t)row * DV + e + DH] = __float2bfloat16_rn(o1 / L);
+}
+
+// One warp per sequence: the new token's 576 values into its slot (72
+// 16-byte pieces, piece c of slot s at ((s / 8) * 72 + c) * 8 + s % 8 uint4s
+// into the block's tile).  A bit copy.
+__global__ void __launch_bounds__(128)
+mla_append_kernel(const uint4 *__restrict__ c_new, uint4 *__restrict__ cache,
+                  const int32_t *__restrict__ tables, const int32_t *__restrict__ pos, int B,
+                  int bs, int MB, int NB, int32_t *err) {
+  pdl_launch_dependents();
+  const int b = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (b >= B) return;
+  const int pp = __ldg(pos + b);
+  if (pp < 0 || pp >= MB * bs) {
+    if (lane == 0) atomicOr(err, PGD_DEVERR_BAD_POSITION);
+    return;
+  }
+  const int blk = __ldg(tables + (size_t)b * MB + pp / bs);
+  if ((unsigned)blk >= (unsigned)NB) {
+    if (lane == 0) atomicOr(err, PGD_DEVERR_BAD_BLOCK_ID);
+    return;
+  }
+  const int s = pp % bs;
+  uint4 *tile = cache + (size_t)blk * bs * (D / 8);
+  for (int c = lane; c < D / 8; c += 32)
+    tile[((size_t)(s >> 3) * (D / 8) + c) * 8 + (s & 7)] = __ldg(c_new + (size_t)b * (D / 8) + c);
+}
+
+template <int BS>
+static cudaError_t launch_bs(const MlaParams &p, int grid, cudaStream_t stream) {
+  static volatile int done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!(dev >= 0 && dev < 64 && done[dev])) {
+    e = cudaFuncSetAttribute(mla_attention_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) done[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_attention_kernel<BS>, p);
+}
+
+}  // namespace mla
+
+int mla_heads_per_cta() { return mla::NH; }
+
+cudaError_t mla_attention_launch(const MlaParams &p, cudaStream_t stream) {
+  const int n_hg = (p.H + mla::NH - 1) / mla::NH;
+  const long long grid = (long long)p.B * n_hg * 2 * p.n_parts;
+  if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (p.bs) {
+    case 16: e = mla::launch_bs<16>(p, (int)grid, stream); break;
+    case 32: e = mla::launch_bs<32>(p, (int)grid, stream); break;
+    case 64: e = mla::launch_bs<64>(p, (int)grid, stream); break;
+  }
+  if (e != cudaSuccess || p.n_parts == 1) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * p.H));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla::mla_combine_kernel, p);
+}
+
+cudaError_t mla_append_launch(const void *c_new, void *cache, const int32_t *tables,
+                              const int32_t *pos, int B, int bs, int MB, int NB, int32_t *err,
+                              cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  mla::mla_append_kernel<<<(B + 3) / 4, 128, 0, stream>>>(
+      static_cast<const uint4 *>(c_new), static_cast<uint4 *>(cache), tables, pos, B, bs, MB, NB,
+      err);
+  return cudaGetLastError();
+}
+
+}  // namespace pgd

@@ -190,4 +190,19 @@ struct PrefixParams {
   int32_t *err;
 };
 
+// Decode attention over an MLA latent cache (mla_attention.cu).
+struct MlaParams {
+  __nv_bfloat16 *out;            // [B][H][512] latent outputs
+  const __nv_bfloat16 *q;        // [B][H][576] absorbed queries
+  const unsigned char *cache;    // latent pool, bf16 [NB][bs/8][72][8][8]
+  const int32_t *tables;         // [B][MB]
+  const int32_t *ctx;            // [B]
+  int B, H, MB, NB, bs;
+  int n_parts;                   // parts of each sequence's context (1: no merge)
+  float qk_scale_log2;           // scale * log2(e)
+  float *part_ml;                // [B][H][n_parts][2] partial (max, sum), log2 domain
+  float *part_o;                 // [B][H][n_parts][512] unnormalised partial outputs
+  int32_t *err;
+};
+
 }  // namespace pgd

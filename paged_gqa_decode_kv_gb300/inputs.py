@@ -354,6 +354,110 @@ def make_verify_workload(name: str, T: int, device="cpu") -> VerifyBatch:
                              device=device, kv_std=w.kv_std)
 
 
+# ---------------------------------------------------------------- MLA latent cache
+MLA_D, MLA_DV = 576, 512  # cached values per token (latent 512 + RoPE key 64); value dims
+
+
+def tile_latent(x: torch.Tensor) -> torch.Tensor:
+    """Row-major latent rows [NB][bs][576] -> the latent pool's tiled layout
+    [NB][bs/8][72][8][8] (8x8 core matrices per 8 tokens)."""
+    NB, bs, D = x.shape
+    return x.reshape(NB, bs // 8, 8, D // 8, 8).permute(0, 1, 3, 2, 4).contiguous()
+
+
+def untile_latent(x: torch.Tensor) -> torch.Tensor:
+    NB, rg, nc = x.shape[:3]
+    return x.permute(0, 1, 3, 2, 4).reshape(NB, rg * 8, nc * 8)
+
+
+@dataclasses.dataclass
+class MlaBatch:
+    """One decode step over an MLA latent cache: absorbed queries [B][H][576],
+    the tiled latent pool, tables and lengths; with append, the newest
+    token's row (c_new [B][576]) still to be written at `positions`."""
+    q: torch.Tensor
+    cache: torch.Tensor
+    block_tables: torch.Tensor
+    context_lens: torch.Tensor
+    c_new: Optional[torch.Tensor]
+    positions: Optional[torch.Tensor]
+    scale: float
+    block_size: int
+    unique_blocks: int
+
+    @property
+    def batch(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def heads(self) -> int:
+        return self.q.shape[1]
+
+
+def make_mla_batch(batch: int, heads: int, block_size: int, ctx_lens: List[int], *,
+                   append: bool = False, kv_std: float = 1.0, spare_frac: float = 0.05,
+                   seed: int = DATA_SEED, table_seed: int = TABLE_SEED, device="cpu",
+                   poison: bool = True, scale: Optional[float] = None) -> MlaBatch:
+    """Latent rows N(0, kv_std^2) and queries N(0, 1), bf16; a pool of the
+    needed blocks plus 5 % spare under a random permutation; spare blocks,
+    tail slots and (append) the newest slot NaN; scale 1/sqrt(128 + 64) by
+    default (the query-key width of the heads the latent stands for)."""
+    bs = block_size
+    nblk = [(c + bs - 1) // bs for c in ctx_lens]
+    needed = sum(nblk)
+    NB = max(1, needed + int(math.ceil(needed * spare_frac)))
+    MB = max(nblk)
+    perm = torch.randperm(NB, generator=torch.Generator().manual_seed(table_seed)).to(torch.int32)
+    tables = torch.full((batch, MB), -1, dtype=torch.int32)
+    cur = 0
+    for b in range(batch):
+        tables[b, :nblk[b]] = perm[cur:cur + nblk[b]]
+        cur += nblk[b]
+    gen = torch.Generator(device=device).manual_seed(seed)
+    q = _randn_bf16((batch, heads, MLA_D), 1.0, gen, device)
+    rows = _randn_bf16((NB, bs, MLA_D), kv_std, gen, device)
+    c_new = positions = None
+    if append:
+        positions = torch.tensor([c - 1 for c in ctx_lens], dtype=torch.int32)
+        blk = tables[torch.arange(batch), positions // bs].long().to(device)
+        slot = (positions % bs).long().to(device)
+        c_new = rows[blk, slot].clone()
+    if poison:
+        nan = float("nan")
+        spare = perm[needed:].long().to(device)
+        if spare.numel():
+            rows[spare] = nan
+        for b in range(batch):
+            tail = ctx_lens[b] % bs
+            if tail:
+                rows[int(tables[b, nblk[b] - 1]), tail:] = nan
+        if append:
+            rows[blk, slot] = nan
+    return MlaBatch(q=q, cache=tile_latent(rows), block_tables=tables.to(device),
+                    context_lens=torch.tensor(ctx_lens, dtype=torch.int32).to(device),
+                    c_new=c_new, positions=None if positions is None else positions.to(device),
+                    scale=(1.0 / math.sqrt(192.0)) if scale is None else scale,
+                    block_size=bs, unique_blocks=needed)
+
+
+# Latent-cache workloads: (batch, heads, block size, context)
+MLA_WORKLOADS = {
+    "mla128_batch16_ctx8192": (16, 128, 64, 8192),
+    "mla128_batch64_ctx4096": (64, 128, 64, 4096),
+}
+
+
+def make_mla_workload(name: str, device="cpu", append: bool = True) -> MlaBatch:
+    B, H, bs, ctx = MLA_WORKLOADS[name]
+    return make_mla_batch(B, H, bs, [ctx] * B, append=append, device=device)
+
+
+def mla_bytes_read(batch: MlaBatch) -> int:
+    """Algorithmic bytes of one latent decode call: every cached token's 576
+    bf16 values, read once for all heads."""
+    return int(batch.context_lens.sum().item()) * MLA_D * 2
+
+
 NAN_CODE = 0x7F  # E4M3 S.1111.111
 
 

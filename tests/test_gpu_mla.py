@@ -1,0 +1,95 @@
+"""Parity of decode attention over an MLA latent cache, through the C ABI,
+with the float64 oracle on the same seeded inputs.
+
+pgd_mla_append: the pool bit exact against the oracle's own append into a
+CPU copy of the pool as generated.  Attention: max abs error <= 2e-2 and mean
+abs error <= 2e-3 against the oracle, every element.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_gqa_decode_kv_gb300 as pgd
+from paged_gqa_decode_kv_gb300 import inputs
+from gpu_common import assert_no_device_errors, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_errors():
+    pgd.device_errors(clear=True)
+    yield
+    assert_no_device_errors()
+
+
+def _bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _run(mb, num_splits=0):
+    """Oracle append on a CPU copy, then the oracle's attention; GPU append,
+    then attention.  Returns (gpu out, oracle out, oracle pool)."""
+    pool = oracle.mla_append(mb.cache.cpu(), mb.c_new.cpu(), mb.block_tables.cpu(),
+                             mb.positions.cpu()) if mb.c_new is not None else _bits(mb.cache)
+    want = oracle.mla_attention(mb.q.cpu(), pool, mb.block_tables.cpu(), mb.context_lens.cpu(),
+                                mb.scale)
+    if mb.c_new is not None:
+        pgd.mla_append(mb.c_new, mb.cache, mb.block_tables, mb.positions)
+    got = pgd.mla_decode_attention(None, mb.q, mb.cache, mb.block_tables, mb.context_lens,
+                                   mb.scale, num_splits=num_splits)
+    torch.cuda.synchronize()
+    return got, want, pool
+
+
+SMALL = [
+    # (heads, bs, lens)
+    (16, 16, [1]),
+    (16, 16, [16, 17, 63, 64, 65]),
+    (64, 32, [100, 7, 129]),
+    (128, 64, [64, 300, 1000]),
+    (128, 16, [513, 2]),
+    (32, 64, [1, 640]),
+    (100, 32, [77, 200]),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "H%d_bs%d_%s" % (
+    c[0], c[1], "-".join(map(str, c[2]))))
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_mla_small(case, num_splits):
+    H, bs, lens = case
+    mb = inputs.make_mla_batch(len(lens), H, bs, lens, append=True, device="cuda",
+                               seed=91 + H, table_seed=92)
+    got, want, pool = _run(mb, num_splits)
+    assert np.array_equal(_bits(mb.cache), pool)
+    compare(got, want, "mla H=%d bs=%d splits=%d" % (H, bs, num_splits))
+
+
+@pytest.mark.parametrize("bs", [16, 64])
+def test_mla_ragged(bs):
+    g = torch.Generator().manual_seed(bs)
+    lens = torch.randint(1, 3000, (13,), generator=g).tolist()
+    mb = inputs.make_mla_batch(len(lens), 128, bs, lens, append=True, device="cuda", seed=7)
+    got, want, _ = _run(mb)
+    compare(got, want, "mla ragged bs=%d" % bs)
+
+
+def test_mla_ctx1_is_the_latent():
+    """One cached token: each head returns its first 512 values (a bf16
+    value through a bf16 probability of exactly 1)."""
+    mb = inputs.make_mla_batch(3, 64, 16, [1, 1, 1], device="cuda")
+    got = pgd.mla_decode_attention(None, mb.q, mb.cache, mb.block_tables, mb.context_lens,
+                                   mb.scale)
+    rows = inputs.untile_latent(mb.cache)
+    for b in range(3):
+        want = rows[int(mb.block_tables[b, 0]), 0, :512]
+        assert torch.equal(got[b].view(torch.int16), want.expand(64, 512).view(torch.int16))
+
+
+def test_mla_workload_batch16_ctx8192():
+    """16 sequences x 8192 tokens, 128 heads, block 64, at full size."""
+    mb = inputs.make_mla_workload("mla128_batch16_ctx8192", device="cuda")
+    got, want, _ = _run(mb)
+    compare(got, want, "mla128 batch16 ctx8192")
