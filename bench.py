@@ -58,6 +58,9 @@ def parse_args(argv=None):
     ap.add_argument("--verify", type=int, default=0, metavar="T",
                     help="speculative verify: T new query tokens per sequence (appended with "
                          "pgd_kv_append_tokens, attended causally with pgd_paged_verify_attention)")
+    ap.add_argument("--mla", action="store_true",
+                    help="MLA latent-cache decode (workloads mla128_batch16_ctx8192, "
+                         "mla128_batch64_ctx4096; default the first)")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="cache format: bf16, or FP8 E4M3 codes + per-(token, head) scales")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -526,6 +529,170 @@ def run_ours(args, rank, world, local):
     return result
 
 
+# ------------------------------------------------------ MLA latent cache
+def run_mla(args, rank, world, local):
+    """A step = pgd_mla_append of every sequence's newest latent row, then
+    pgd_mla_decode_attention of every head over its sequence's latent cache;
+    bytes = each cached token's 576 bf16 values once."""
+    import torch
+
+    import __graft_entry__
+    import paged_gqa_decode_kv_gb300 as pgd
+    from paged_gqa_decode_kv_gb300 import inputs
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload if args.workload in inputs.MLA_WORKLOADS else "mla128_batch16_ctx8192"
+    mb = inputs.make_mla_workload(name, device=dev, append=True)
+    B, H = mb.batch, mb.heads
+    nbytes = inputs.mla_bytes_read(mb)
+    flops = int(mb.context_lens.sum().item()) * H * (inputs.MLA_D + inputs.MLA_DV) * 2
+    pool_b = mb.cache.numel() * 2
+    n_pools = 1 if pool_b > 2 * L2_BYTES else -(-2 * L2_BYTES // pool_b)
+    pools = [mb.cache] + [mb.cache.clone() for _ in range(n_pools - 1)]
+    ws = torch.empty(max(256, pgd.mla_workspace_size(B, H, args.splits)), dtype=torch.uint8,
+                     device=dev)
+    out = torch.empty((B, H, inputs.MLA_DV), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    it = [0]
+
+    def next_pool():
+        c = pools[it[0] % n_pools]
+        it[0] += 1
+        return c
+
+    def attend(c, q_=None, out_=None, lens=None):
+        pgd.mla_decode_attention(out if out_ is None else out_, mb.q if q_ is None else q_, c,
+                                 mb.block_tables, mb.context_lens if lens is None else lens,
+                                 mb.scale, num_splits=args.splits, workspace=ws, stream=stream)
+
+    def step():
+        c = next_pool()
+        pgd.mla_append(mb.c_new, c, mb.block_tables, mb.positions, stream=stream)
+        attend(c)
+
+    gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    sampler = ClockSampler(gpu_uuid)
+    sampler.start()
+    time.sleep(0.3)
+    t_wall0 = time.time()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    flags = pgd.device_errors(clear=True, stream=stream)
+    if flags:
+        raise RuntimeError("device error word %d after warm-up" % flags)
+    K = args.steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        c = next_pool()
+        ev_a[i].record(stream)
+        attend(c)
+        ev_b[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
+    flags = pgd.device_errors(clear=True, stream=stream)
+    if flags:
+        raise RuntimeError("device error word %d after the timed steps" % flags)
+    max_ms = max_over_ranks(elapsed_ms, world)
+    value = sum_over_ranks(nbytes * K, world) / (max_ms / 1e3) / 1e9
+
+    # end to end: pinned host queries and new rows in, latent outputs back
+    q_h, cn_h = mb.q.cpu().pin_memory(), mb.c_new.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    q_d, cn_d = torch.empty_like(mb.q), torch.empty_like(mb.c_new)
+
+    def e2e_step():
+        c = next_pool()
+        with torch.cuda.stream(stream):
+            q_d.copy_(q_h, non_blocking=True)
+            cn_d.copy_(cn_h, non_blocking=True)
+            pgd.mla_append(cn_d, c, mb.block_tables, mb.positions, stream=stream)
+            attend(c, q_=q_d)
+            out_h.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(K):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
+    peak, peak_kind = hbm_peak()
+    achieved = nbytes / (attn_ms / 1e3) / 1e9
+    parts = args.splits if args.splits > 0 else max(1, min(
+        64, torch.cuda.get_device_properties(local).multi_processor_count // (B * -(-H // 64) * 2)))
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(max_ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "accumulate": "f32",
+        "data": "synthetic (seeded N(0,1) bf16 latent rows and absorbed queries, random block "
+                "tables)",
+        "config": {"workload": name, "batch": B, "heads": H, "context": int(mb.context_lens[0]),
+                   "latent": "576 bf16 per token (512 latent + 64 RoPE key), 512-d output",
+                   "block_size": mb.block_size, "parts": parts,
+                   "l2": ("latent pool %.0f MB, %d copies rotated (%.0f MB > 2 x L2), no flush"
+                          % (pool_b / 1e6, n_pools, n_pools * pool_b / 1e6))},
+        "kv_bytes_per_step": nbytes,
+        "seq_layer_steps_per_s": round(sum_over_ranks(B * K, world) / (max_ms / 1e3), 1),
+        "pct_of_hbm_peak": {"nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+                            peak_kind: round(100 * value / world / peak, 2)},
+        "roofline": {"bound": "hbm", "kernel": "pgd::mla::mla_attention_kernel<%d> (tcgen05)"
+                     % mb.block_size, "achieved": round(achieved, 2), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "launch_ms": round(attn_ms, 5), "bytes_per_launch": nbytes,
+                     "tflops_achieved": round(flops / (attn_ms / 1e3) / 1e12, 2),
+                     "flop_per_byte": round(flops / nbytes, 1)},
+        "e2e": {"value": round(sum_over_ranks(nbytes * K, world) / (e2e_ms / 1e3) / 1e9, 2),
+                "unit": "GB/s", "h2d_bytes_per_step": q_h.numel() * 2 + cn_h.numel() * 2,
+                "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": round(e2e_ms / K, 5)},
+        "gpu_launches": (2 + (1 if parts > 1 else 0)) * K,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "gpu": torch.cuda.get_device_name(local),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        q_c, c_c = mb.q.cpu(), mb.cache.cpu()
+        t_c, l_c = mb.block_tables.cpu(), mb.context_lens.cpu()
+        n = 1
+        t0 = time.perf_counter()
+        oracle.mla_attention(q_c[:n], c_c, t_c[:n], l_c[:n], mb.scale)
+        dt = time.perf_counter() - t0
+        total_t, total_b, calls = dt, int(l_c[:n].sum()) * inputs.MLA_D * 2, 1
+        while total_t < args.cpu_seconds and calls < 64:
+            t0 = time.perf_counter()
+            oracle.mla_attention(q_c[:n], c_c, t_c[:n], l_c[:n], mb.scale)
+            total_t += time.perf_counter() - t0
+            total_b += int(l_c[:n].sum()) * inputs.MLA_D * 2
+            calls += 1
+        result["cpu_baseline"] = {
+            "value": round(total_b / total_t / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.threads_used(0, n * H), "kind": "oracle",
+            "sample": "float64 oracle latent attention over the first sequence (%d heads, %d "
+                      "tokens), %d call(s), %.1f s" % (H, int(l_c[0]), calls, total_t)}
+    return result
+
+
 # --------------------------------------------------------- reference arm
 def run_reference(args):
     """The oracle, as it stands, on the host cores: each step a bounded sample
@@ -575,7 +742,7 @@ def main(argv=None):
         print(json.dumps(run_reference(args)), flush=True)
         return 0
     dist_init(world)
-    result = run_ours(args, rank, world, local)
+    result = run_mla(args, rank, world, local) if args.mla else run_ours(args, rank, world, local)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:

@@ -18,16 +18,21 @@
 // 64..127 are read from whatever follows Q and P in shared memory and only
 // produce rows of S and O that nothing reads (the layout keeps those reads
 // inside the allocation).  A 576-d latent row is 1152 B, so a 64-token stage
-// is 72 KiB; two stages, Q (64 heads) and P fill the 227 KB.  The 512 output
+// is 72 KiB; two stages, Q (64 heads) and P fill the 227 KB.  (A ring of four
+// 32-token stages measured slower: the per-stage cost is the q.c^T re-reading
+// Q from shared memory and the stage's fixed synchronisation, not the load
+// latency.)  The 512 output
 // dims do not fit tensor memory beside S (256 fp32 columns each), so a CTA
 // computes one half of them: CTA (sequence, 64-head group, half, part).  The
 // latent pool is tiled as 8 x 8 core matrices per 8 tokens, so one bulk copy
 // per block lands an MMA-ready operand: element (slot s, dim i) of a block at
 // ((s / 8) * 72 + i / 8) * 64 + (s % 8) * 8 + i % 8.
 //
-// Roles (128 threads): warps 0-1 softmax and epilogue (thread = head row,
-// row statistics thread-local), warp 2 producer, warp 3 MMA issuer and
-// tensor-memory owner.  Every wait is bounded.  A context longer than one
+// Roles (160 threads): warps 0-1 softmax and epilogue (thread = head row,
+// row statistics thread-local), warp 2 producer, warp 3 q.c^T issuer and
+// tensor-memory owner, warp 4 p.c issuer (a separate thread, so that a p.c
+// -- which frees its stage for the next load -- is not queued behind the
+// issue of the next stage's 36 q.c^T steps).  Every wait is bounded.  A context longer than one
 // part is split over CTAs; the parts' (max, sum, output) states are merged by
 // mla_combine_kernel.
 #include <cuda_bf16.h>
@@ -50,22 +55,25 @@ constexpr int D = 576;          // cached values per token (latent + RoPE key)
 constexpr int DV = 512;         // latent dims (the value)
 constexpr int DH = 256;         // output dims per CTA
 constexpr int TOKS = 64;        // tokens per stage
+constexpr int NSTG = 2;         // stage buffers (and S buffers)
 constexpr int NH = 64;          // head rows per CTA
-constexpr int THREADS = 128;
+constexpr int THREADS = 160;
 constexpr int GRP = (D / 8) * 128;   // bytes per 8 rows of 576 values: 9216
 constexpr int STAGE = (TOKS / 8) * GRP;  // 73,728
 constexpr int Q_BYTES = (NH / 8) * GRP;  // 73,728
-constexpr int P_BYTES = (NH / 8) * 1024; // [8 row groups][8 token groups][8][16 B] = 8192
-// P, then Q, then the two stages: the 128-row A operands P and Q read their
+constexpr int P_RG = (TOKS / 8) * 128;   // bytes per 8 rows of P: 1024
+constexpr int P_BYTES = (NH / 8) * P_RG; // [8 row groups][8 token groups][8][16 B] = 8192
+// P, then Q, then the stage ring: the 128-row A operands P and Q read their
 // rows 64..127 from the next 8 KiB (Q) and the next 72 KiB (stage 0).
 constexpr int OFF_P = 0;
 constexpr int OFF_Q = OFF_P + P_BYTES;
 constexpr int OFF_C = OFF_Q + Q_BYTES;
-constexpr int OFF_BAR = OFF_C + 2 * STAGE;
+constexpr int OFF_BAR = OFF_C + NSTG * STAGE;
 constexpr int OFF_MISC = OFF_BAR + 128;
 constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
 static_assert(SMEM_BYTES <= 232448, "MLA kernel exceeds 227 KB of shared memory");
-static_assert(OFF_Q - OFF_P >= P_BYTES && OFF_C - OFF_Q == Q_BYTES, "over-read layout");
+static_assert(OFF_Q - OFF_P >= P_BYTES && OFF_C - OFF_Q == Q_BYTES &&
+                  NSTG * STAGE >= Q_BYTES, "over-read layout");
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;     // O: 256 columns; S buffers at 0 and 64
 
@@ -124,11 +132,14 @@ __device__ __forceinline__ void part_stages(int nst_seq, int part, int n_parts, 
 
 template <int BS>
 __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaParams p) {
-  constexpr int SBLK = TOKS / BS;          // blocks per stage
+  // A stage is copied in pieces of PB tokens: whole blocks, or a slice of
+  // one block when blocks are longer than a stage.
+  constexpr int PB = BS < TOKS ? BS : TOKS;
   constexpr uint32_t TILE = BS * D * 2;    // one block's latent rows
+  constexpr uint32_t PIECE = PB * D * 2;
   constexpr uint32_t IDESC_QK = idesc(TOKS, false);
   constexpr uint32_t IDESC_PV = idesc(DH, true);
-  static_assert(TOKS % BS == 0 && BS % 8 == 0, "block size");
+  static_assert((TOKS % BS == 0 || BS % TOKS == 0) && BS % 8 == 0, "block size");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();  // q, the cache and the tables may come from the previous kernel
@@ -171,14 +182,15 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-  uint64_t *c_full = bars, *c_empty = bars + 2, *s_full = bars + 4, *s_free = bars + 6;
-  uint64_t *p_full = bars + 8, *p_free = bars + 9, *o_done = bars + 10;
+  uint64_t *c_full = bars, *c_empty = bars + NSTG, *s_full = bars + 2 * NSTG;
+  uint64_t *s_free = bars + 3 * NSTG;
+  uint64_t *p_full = bars + 4 * NSTG, *p_free = p_full + 1, *o_done = p_full + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
-  volatile int *bad_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);  // [2]
+  volatile int *bad_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);  // [NSTG]
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NSTG; ++i) {
       mbar_init(&c_full[i], 1);
       mbar_init(&c_empty[i], 1);
       mbar_init(&s_full[i], 1);
@@ -222,18 +234,19 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_policy_evict_first();
     for (int i = 0; i < nst; ++i) {
-      const int buf = i & 1;
-      const int nb = (stage_tokens(i) + BS - 1) / BS;
-      const int j = (st0 + i) * SBLK + lane;
-      const int blk = (lane < nb) ? __ldg(trow + j) : -1;
+      const int buf = i % NSTG;
+      const uint32_t par = (uint32_t)(i / NSTG) & 1u;
+      const int nb = (stage_tokens(i) + PB - 1) / PB;  // pieces with a valid token
+      const int t0 = (st0 + i) * TOKS + lane * PB;     // first token of this lane's piece
+      const int blk = (lane < nb) ? __ldg(trow + t0 / BS) : -1;
       const bool ok = lane < nb && (unsigned)blk < (unsigned)p.NB;
       const unsigned okmask = __ballot_sync(kFullMask, ok);
       const unsigned want = (nb >= 32) ? ~0u : ((1u << nb) - 1u);
       if (lane == 0) {
-        wait_or_abort(&c_empty[buf], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, p.err);
+        wait_or_abort(&c_empty[buf], par ^ 1u, abort_flag, p.err);
         bad_mask[buf] = (int)(want & ~okmask);
         if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
-        const uint32_t bytes = (uint32_t)__popc(okmask) * TILE;
+        const uint32_t bytes = (uint32_t)__popc(okmask) * PIECE;
         if (*abort_flag || bytes == 0)
           mbar_arrive(&c_full[buf]);
         else
@@ -241,60 +254,63 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       }
       __syncwarp();
       if (ok && !*abort_flag)
-        bulk_copy_g2s(smem + OFF_C + buf * STAGE + lane * (BS / 8) * GRP,
-                      p.cache + (size_t)blk * TILE, TILE, &c_full[buf], policy);
+        bulk_copy_g2s(smem + OFF_C + buf * STAGE + lane * (PB / 8) * GRP,
+                      p.cache + (size_t)blk * TILE + (size_t)((t0 % BS) / 8) * GRP, PIECE,
+                      &c_full[buf], policy);
     }
     if (lane == 0) {  // no copy may still be landing when the CTA exits
-      for (int k = 1; k <= 2 && k <= nst; ++k) {
+      for (int k = 1; k <= NSTG && k <= nst; ++k) {
         const int last = nst - k;
-        mbar_wait_bounded(&c_full[last & 1], (uint32_t)(last >> 1) & 1u);
+        mbar_wait_bounded(&c_full[last % NSTG], (uint32_t)(last / NSTG) & 1u);
       }
     }
   } else if (warp == 3) {
-    // ------------------------------------------------------- MMA issuer
-    // q.c^T of stage i before p.c of stage i - 1, so it overlaps the softmax
-    // of stage i - 1.
+    // ---------------------------------------------------- q.c^T issuer
     if (lane == 0) {
       const uint64_t qd = smem_desc(smem_addr(smem + OFF_Q), 128, GRP, 0);
-      const uint64_t pd = smem_desc(smem_addr(smem + OFF_P), 128, 1024, 0);
-      for (int i = 0; i <= nst; ++i) {
-        if (i < nst) {
-          const int buf = i & 1;
-          wait_or_abort(&c_full[buf], (uint32_t)(i >> 1) & 1u, abort_flag, p.err);
-          wait_or_abort(&s_free[buf], ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag, p.err);
-          tc_fence_after();
-          if (!*abort_flag) {
-            // A = Q, B = C, both K-major: a k-step of 16 dims moves both by
-            // two core matrices (256 B)
-            const uint64_t cd = smem_desc(smem_addr(smem + OFF_C + buf * STAGE), 128, GRP, 0);
+      for (int i = 0; i < nst; ++i) {
+        const int buf = i % NSTG;
+        const uint32_t par = (uint32_t)(i / NSTG) & 1u;
+        wait_or_abort(&c_full[buf], par, abort_flag, p.err);
+        wait_or_abort(&s_free[buf], par ^ 1u, abort_flag, p.err);
+        tc_fence_after();
+        if (!*abort_flag) {
+          // A = Q, B = C, both K-major: a k-step of 16 dims moves both by
+          // two core matrices (256 B)
+          const uint64_t cd = smem_desc(smem_addr(smem + OFF_C + buf * STAGE), 128, GRP, 0);
 #pragma unroll 4
-            for (int kk = 0; kk < D / 16; ++kk)
-              umma_bf16(tmem + (uint32_t)(buf * TOKS), qd + (uint64_t)(kk * 16),
-                        cd + (uint64_t)(kk * 16), IDESC_QK, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(&s_full[buf]);
+          for (int kk = 0; kk < D / 16; ++kk)
+            umma_bf16(tmem + (uint32_t)(buf * TOKS), qd + (uint64_t)(kk * 16),
+                      cd + (uint64_t)(kk * 16), IDESC_QK, kk > 0 ? 1u : 0u);
         }
-        if (i >= 1) {
-          const int j = i - 1, buf = j & 1;
-          const int nkt = (stage_tokens(j) + 15) >> 4;  // 16-token steps with a valid token
-          wait_or_abort(p_full, (uint32_t)(j & 1), abort_flag, p.err);
-          tc_fence_after();
-          if (!*abort_flag) {
-            // A = P (K-major, tokens along K: 256 B per 16 tokens); B = C
-            // MN-major (dims along N, 128 B per 8 dims; 2 token groups =
-            // 18,432 B per 16 tokens), starting at this CTA's 256 dims
-            const uint64_t cvd =
-                smem_desc(smem_addr(smem + OFF_C + buf * STAGE + half * (DH / 8) * 128), GRP,
-                          128, 0);
-            for (int kt = 0; kt < nkt; ++kt)
-              umma_bf16(tmem + COL_O, pd + (uint64_t)(kt * 16),
-                        cvd + (uint64_t)(kt * (2 * GRP / 16)), IDESC_PV,
-                        (j > 0 || kt > 0) ? 1u : 0u);
-          }
-          umma_commit(&c_empty[buf]);  // the stage buffer may be refilled
-          umma_commit(p_free);         // P may be rewritten
-        }
+        umma_commit(&s_full[buf]);
       }
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------ p.c issuer
+    if (lane == 0) {
+      const uint64_t pd = smem_desc(smem_addr(smem + OFF_P), 128, P_RG, 0);
+      for (int j = 0; j < nst; ++j) {
+        const int buf = j % NSTG;
+        const int nkt = (stage_tokens(j) + 15) >> 4;  // 16-token steps with a valid token
+        wait_or_abort(p_full, (uint32_t)(j & 1), abort_flag, p.err);
+        tc_fence_after();
+        if (!*abort_flag) {
+          // A = P (K-major, tokens along K: 256 B per 16 tokens); B = C
+          // MN-major (dims along N, 128 B per 8 dims; 2 token groups =
+          // 18,432 B per 16 tokens), starting at this CTA's 256 dims
+          const uint64_t cvd =
+              smem_desc(smem_addr(smem + OFF_C + buf * STAGE + half * (DH / 8) * 128), GRP, 128,
+                        0);
+          for (int kt = 0; kt < nkt; ++kt)
+            umma_bf16(tmem + COL_O, pd + (uint64_t)(kt * 16),
+                      cvd + (uint64_t)(kt * (2 * GRP / 16)), IDESC_PV,
+                      (j > 0 || kt > 0) ? 1u : 0u);
+        }
+        umma_commit(&c_empty[buf]);  // the stage buffer may be refilled
+        umma_commit(p_free);         // P may be rewritten
+      }
+      // (every q.c^T completed before its stage's softmax released p.c)
       umma_commit(o_done);
       mbar_wait_bounded(o_done, 0);
     }
@@ -303,24 +319,26 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     float m_ref = -INFINITY, l = 0.f;
     for (int i = 0; i < nst; ++i) {
-      const int buf = i & 1;
+      const int buf = i % NSTG;
+      const uint32_t par = (uint32_t)(i / NSTG) & 1u;
       const int nv = stage_tokens(i);
-      wait_or_abort(&s_full[buf], (uint32_t)(i >> 1) & 1u, abort_flag, p.err);
+      wait_or_abort(&s_full[buf], par, abort_flag, p.err);
       // (the producer wrote the stage's bad-block mask before arming c_full;
       // that phase has completed and cannot move on before this stage's p.c)
-      wait_or_abort(&c_full[buf], (uint32_t)(i >> 1) & 1u, abort_flag, p.err);
+      wait_or_abort(&c_full[buf], par, abort_flag, p.err);
       const int bad = bad_mask[buf];
       tc_fence_after();
       float sv[TOKS];
-      tmem_ld32(tmem + lane_base + (uint32_t)(buf * TOKS), sv);
-      tmem_ld32(tmem + lane_base + (uint32_t)(buf * TOKS + 32), sv + 32);
+#pragma unroll
+      for (int c = 0; c < TOKS / 32; ++c)
+        tmem_ld32(tmem + lane_base + (uint32_t)(buf * TOKS + c * 32), sv + c * 32);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[buf]);
       float rmax = -INFINITY;
 #pragma unroll
       for (int c = 0; c < TOKS; ++c) {
-        const bool ok = c < nv && !((bad >> (c / BS)) & 1);
+        const bool ok = c < nv && !((bad >> (c / PB)) & 1);
         sv[c] = ok ? sv[c] * p.qk_scale_log2 : -INFINITY;
         rmax = fmaxf(rmax, sv[c]);
       }
@@ -349,7 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       }
       // probabilities in bf16, summed as the tensor cores see them; row r's
       // 8-token pieces at core matrix (r / 8, token group), row r % 8
-      unsigned char *prow = smem + OFF_P + (r >> 3) * 1024 + (r & 7) * 16;
+      unsigned char *prow = smem + OFF_P + (r >> 3) * P_RG + (r & 7) * 16;
 #pragma unroll
       for (int g = 0; g < TOKS / 8; ++g) {
         uint32_t pk[4];
@@ -373,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
         unsigned char *cs = smem + OFF_C + buf * STAGE;
         for (int k = tid; k < lim * (D / 8); k += 64) {
           const int t = k / (D / 8), c = k % (D / 8);
-          if (t >= nv || ((bad >> (t / BS)) & 1))
+          if (t >= nv || ((bad >> (t / PB)) & 1))
             *reinterpret_cast<uint4 *>(cs + (t >> 3) * GRP + c * 128 + (t & 7) * 16) =
                 make_uint4(0, 0, 0, 0);
         }
