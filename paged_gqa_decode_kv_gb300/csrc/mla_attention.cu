@@ -28,11 +28,13 @@
 // per block lands an MMA-ready operand: element (slot s, dim i) of a block at
 // ((s / 8) * 72 + i / 8) * 64 + (s % 8) * 8 + i % 8.
 //
-// Roles (160 threads): warps 0-1 softmax and epilogue (thread = head row,
-// row statistics thread-local), warp 2 producer, warp 3 q.c^T issuer and
-// tensor-memory owner, warp 4 p.c issuer (a separate thread, so that a p.c
-// -- which frees its stage for the next load -- is not queued behind the
-// issue of the next stage's 36 q.c^T steps).  Every wait is bounded.  A context longer than one
+// Roles (224 threads): warps 0, 1, 4, 5 softmax and epilogue (two threads
+// per head row, each with half of the stage's tokens and half of the output
+// dims; the row maximum and sum combine the pair's through shared memory),
+// warp 2 producer, warp 3 q.c^T issuer and tensor-memory owner, warp 6 p.c
+// issuer (a separate thread, so that a p.c -- which frees its stage for the
+// next load -- is not queued behind the issue of the next stage's 36 q.c^T
+// steps).  Every wait is bounded.  A context longer than one
 // part is split over CTAs; the parts' (max, sum, output) states are merged by
 // mla_combine_kernel.
 #include <cuda_bf16.h>
@@ -57,7 +59,10 @@ constexpr int DH = 256;         // output dims per CTA
 constexpr int TOKS = 64;        // tokens per stage
 constexpr int NSTG = 2;         // stage buffers (and S buffers)
 constexpr int NH = 64;          // head rows per CTA
-constexpr int THREADS = 160;
+constexpr int THREADS = 224;
+// Softmax warps: 0, 1 (token columns 0..31 of head rows 0..63) and 4, 5
+// (columns 32..63 of the same rows: warp w reaches TMEM lanes 32 (w % 4) ..).
+__device__ __forceinline__ bool is_softmax_warp(int w) { return w < 2 || w == 4 || w == 5; }
 constexpr int GRP = (D / 8) * 128;   // bytes per 8 rows of 576 values: 9216
 constexpr int STAGE = (TOKS / 8) * GRP;  // 73,728
 constexpr int Q_BYTES = (NH / 8) * GRP;  // 73,728
@@ -70,7 +75,9 @@ constexpr int OFF_Q = OFF_P + P_BYTES;
 constexpr int OFF_C = OFF_Q + Q_BYTES;
 constexpr int OFF_BAR = OFF_C + NSTG * STAGE;
 constexpr int OFF_MISC = OFF_BAR + 128;
-constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
+constexpr int OFF_X = OFF_MISC + 64;  // f32 [2 parities][2 halves][64 rows] row maxima, then
+                                      // f32 [2 halves][64 rows] row sums
+constexpr int SMEM_BYTES = 1024 + OFF_X + 6 * NH * 4;
 static_assert(SMEM_BYTES <= 232448, "MLA kernel exceeds 227 KB of shared memory");
 static_assert(OFF_Q - OFF_P >= P_BYTES && OFF_C - OFF_Q == Q_BYTES &&
                   NSTG * STAGE >= Q_BYTES, "over-read layout");
@@ -162,14 +169,14 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   if (!ctx_ok && tid == 0 && half == 0 && hg == 0 && part == 0)
     atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
 
-  const int r = tid;  // head row (warps 0-1)
+  const int r = tid;  // head row of warps 0-1 (empty parts)
   const bool row_ok = r < rows;
   const int h = hg * NH + r;
   // partial state slot of (b, h, part)
   const size_t slot = ((size_t)b * p.H + h) * p.n_parts + part;
 
   if (nst <= 0) {  // an empty part (or a rejected sequence): a -inf maximum
-    if (warp < 2 && row_ok && p.n_parts > 1) {
+    if (warp < 2 && row_ok && p.n_parts > 1) {  // (both halves of the row's dims)
       if (half == 0)
         *reinterpret_cast<float2 *>(p.part_ml + slot * 2) = make_float2(-INFINITY, 0.f);
       float4 *o = reinterpret_cast<float4 *>(p.part_o + slot * DV + half * DH);
@@ -194,9 +201,9 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       mbar_init(&c_full[i], 1);
       mbar_init(&c_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 2);  // one arrival per softmax warp
+      mbar_init(&s_free[i], 4);  // one arrival per softmax warp
     }
-    mbar_init(p_full, 2);
+    mbar_init(p_full, 1);
     mbar_init(p_free, 1);
     mbar_init(o_done, 1);
     mbar_init_fence();
@@ -286,7 +293,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
         umma_commit(&s_full[buf]);
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == 6) {
     // ------------------------------------------------------ p.c issuer
     if (lane == 0) {
       const uint64_t pd = smem_desc(smem_addr(smem + OFF_P), 128, P_RG, 0);
@@ -314,9 +321,17 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       umma_commit(o_done);
       mbar_wait_bounded(o_done, 0);
     }
-  } else {
-    // ------------------------------------- softmax, one head row per thread
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  } else if (is_softmax_warp(warp)) {
+    // ------------------------------ softmax, two threads per head row
+    const int sh = warp >= 4 ? 1 : 0;      // token half (and output-dims half) of this thread
+    const int r = (warp & 1) * 32 + lane;  // head row
+    const int st = sh * 64 + r;            // 0..127 over the four warps
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const bool rok = r < rows;
+    const int hr = hg * NH + r;
+    const size_t slot_r = ((size_t)b * p.H + hr) * p.n_parts + part;
+    float *xmax = reinterpret_cast<float *>(smem + OFF_X);  // [parity][half][row]
+    constexpr int TH = TOKS / 2;           // token columns per thread
     float m_ref = -INFINITY, l = 0.f;
     for (int i = 0; i < nst; ++i) {
       const int buf = i % NSTG;
@@ -328,20 +343,24 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       wait_or_abort(&c_full[buf], par, abort_flag, p.err);
       const int bad = bad_mask[buf];
       tc_fence_after();
-      float sv[TOKS];
-#pragma unroll
-      for (int c = 0; c < TOKS / 32; ++c)
-        tmem_ld32(tmem + lane_base + (uint32_t)(buf * TOKS + c * 32), sv + c * 32);
+      float sv[TH];
+      tmem_ld32(tmem + lane_base + (uint32_t)(buf * TOKS + sh * TH), sv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[buf]);
-      float rmax = -INFINITY;
+      float hmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < TOKS; ++c) {
-        const bool ok = c < nv && !((bad >> (c / PB)) & 1);
+      for (int c = 0; c < TH; ++c) {
+        const int t = sh * TH + c;
+        const bool ok = t < nv && !((bad >> (t / PB)) & 1);
         sv[c] = ok ? sv[c] * p.qk_scale_log2 : -INFINITY;
-        rmax = fmaxf(rmax, sv[c]);
+        hmax = fmaxf(hmax, sv[c]);
       }
+      // the row maximum: this half's and the pair's (one exchange a stage,
+      // by stage parity so that no second barrier is needed)
+      xmax[((i & 1) * 2 + sh) * NH + r] = hmax;
+      named_barrier_sync(1, 128);
+      const float rmax = fmaxf(hmax, xmax[((i & 1) * 2 + (sh ^ 1)) * NH + r]);
       // lazy rescale: move the row's reference when exceeded by 2^8; the
       // warp's O rows are rescaled together (tensor memory is warp-wide)
       const bool need = rmax > m_ref + tc::kRescaleLog2;
@@ -356,20 +375,21 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       if (i > 0 && __any_sync(kFullMask, need)) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < DH / 32; ++c) {
+        for (int c = 0; c < DH / 64; ++c) {  // this thread's 128 of the 256 O columns
           float ov[32];
-          tmem_ld32(tmem + lane_base + COL_O + c * 32, ov);
+          const uint32_t col = COL_O + (uint32_t)(sh * (DH / 2) + c * 32);
+          tmem_ld32(tmem + lane_base + col, ov);
 #pragma unroll
           for (int k = 0; k < 32; ++k) ov[k] *= alpha;
-          tmem_st32(tmem + lane_base + COL_O + c * 32, ov);
+          tmem_st32(tmem + lane_base + col, ov);
         }
         tc_fence_before();
       }
       // probabilities in bf16, summed as the tensor cores see them; row r's
       // 8-token pieces at core matrix (r / 8, token group), row r % 8
-      unsigned char *prow = smem + OFF_P + (r >> 3) * P_RG + (r & 7) * 16;
+      unsigned char *prow = smem + OFF_P + (r >> 3) * P_RG + (sh * (TH / 8)) * 128 + (r & 7) * 16;
 #pragma unroll
-      for (int g = 0; g < TOKS / 8; ++g) {
+      for (int g = 0; g < TH / 8; ++g) {
         uint32_t pk[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -389,7 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       const int lim = ((nv + 15) & ~15);
       if (nv < lim || bad) {
         unsigned char *cs = smem + OFF_C + buf * STAGE;
-        for (int k = tid; k < lim * (D / 8); k += 64) {
+        for (int k = st; k < lim * (D / 8); k += 128) {
           const int t = k / (D / 8), c = k % (D / 8);
           if (t >= nv || ((bad >> (t / PB)) & 1))
             *reinterpret_cast<uint4 *>(cs + (t >> 3) * GRP + c * 128 + (t & 7) * 16) =
@@ -398,34 +418,40 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       }
       fence_proxy_async();
       tc_fence_before();
-      named_barrier_sync(1, 64);  // both softmax warps have written P and zeroed
-      if (lane == 0) mbar_arrive(p_full);
+      named_barrier_sync(1, 128);  // all four softmax warps have written P and zeroed
+      if (st == 0) mbar_arrive(p_full);
     }
-    // ---- epilogue: this row's output (one part) or partial state
+    // ---- epilogue: the row's sum over both halves, then this thread's 128
+    // output dims (one part) or partial state
+    float *lx = xmax + 4 * NH;  // [2 halves][64 rows] (past both parities' maxima)
+    lx[sh * NH + r] = l;
+    named_barrier_sync(1, 128);
+    const float l_row = l + lx[(sh ^ 1) * NH + r];
     wait_or_abort(o_done, 0, abort_flag, p.err);
     tc_fence_after();
 #pragma unroll 1
-    for (int c = 0; c < DH / 32; ++c) {
+    for (int c = 0; c < DH / 64; ++c) {
       float ov[32];
-      tmem_ld32(tmem + lane_base + COL_O + c * 32, ov);  // warp-wide; stores by real rows
-      if (row_ok) {
+      const int d0 = sh * (DH / 2) + c * 32;  // first of these 32 dims within the CTA's half
+      tmem_ld32(tmem + lane_base + COL_O + d0, ov);  // warp-wide; stores by real rows
+      if (rok) {
         if (p.n_parts == 1) {
-          const float inv = 1.f / l;
-          __nv_bfloat16 *o = p.out + ((size_t)b * p.H + h) * DV + half * DH + c * 32;
+          const float inv = 1.f / l_row;
+          __nv_bfloat16 *o = p.out + ((size_t)b * p.H + hr) * DV + half * DH + d0;
 #pragma unroll
           for (int k = 0; k < 32; k += 2)
             *reinterpret_cast<__nv_bfloat162 *>(o + k) =
                 __floats2bfloat162_rn(ov[k] * inv, ov[k + 1] * inv);
         } else {
-          float4 *o = reinterpret_cast<float4 *>(p.part_o + slot * DV + half * DH + c * 32);
+          float4 *o = reinterpret_cast<float4 *>(p.part_o + slot_r * DV + half * DH + d0);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             o[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
         }
       }
     }
-    if (row_ok && p.n_parts > 1 && half == 0)
-      *reinterpret_cast<float2 *>(p.part_ml + slot * 2) = make_float2(m_ref, l);
+    if (rok && p.n_parts > 1 && half == 0 && sh == 0)
+      *reinterpret_cast<float2 *>(p.part_ml + slot_r * 2) = make_float2(m_ref, l_row);
   }
 
   tc_fence_before();
