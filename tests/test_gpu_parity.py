@@ -297,3 +297,24 @@ def test_workload_full_size(name):
     else:
         want = oracle_attention(pb)
     compare(gpu_attention(pb), want, name)
+
+
+def test_bad_block_id_is_flagged_and_contained():
+    """A table entry outside [0, NB) inside a sequence's context is caught by
+    the kernel's range check: nothing is read through it, the device error
+    word gets PGD_DEVERR_BAD_BLOCK_ID, and the other sequences' outputs are
+    unaffected."""
+    lens = [300, 300, 300]
+    pb = inputs.make_batch(3, 32, 8, 16, lens, device="cuda", seed=5, table_seed=6)
+    want = oracle_attention(pb)
+    tables = pb.block_tables.clone()
+    tables[1, 7] = pb.num_blocks + 5
+    out = pgd.paged_decode_attention(None, pb.q, pb.k_cache, pb.v_cache, tables,
+                                     pb.context_lens, pb.scale)
+    torch.cuda.synchronize()
+    flags = pgd.device_errors(clear=True)
+    assert flags & 1, "device error word %d lacks the bad-block bit" % flags
+    got = out.float().cpu().double().numpy()
+    for b in (0, 2):
+        err = np.abs(got[b] - want[b])
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3
