@@ -11,14 +11,12 @@
 // absorption).  Decode is then MQA with G = n_h: one cache, all heads.
 //
 // On the tensor cores the head rows sit on the MMA's M side and the tokens on
-// N, as in the shared-prefix pass:
-//   S[128 rows][64 tok]  = Q[128 rows][576] . C^T        (A = Q, B = C, both K-major)
-//   O[128 rows][256 d]  += P[128 rows][64 tok] . C[:, half] (A = P K-major, B = C MN-major)
-// with 64 real head rows per CTA.  The A operands are 128 rows tall; rows
-// 64..127 are read from whatever follows Q and P in shared memory and only
-// produce rows of S and O that nothing reads (the layout keeps those reads
-// inside the allocation).  A 576-d latent row is 1152 B, so a 64-token stage
-// is 72 KiB; two stages, Q (64 heads) and P fill the 227 KB.  (A ring of four
+// N, as in the shared-prefix pass, with M = 64 (64 heads per CTA):
+//   S[64 rows][64 tok]  = Q[64 rows][576] . C^T        (A = Q, B = C, both K-major)
+//   O[64 rows][256 d]  += P[64 rows][64 tok] . C[:, half] (A = P K-major, B = C MN-major)
+// An M = 64 accumulator keeps row r in tensor-memory lane 32 (r / 16) + r % 16
+// (16 rows in each warp quadrant).  A 576-d latent row is 1152 B, so a
+// 64-token stage is 72 KiB; two stages, Q (64 heads) and P fill the 227 KB.  (A ring of four
 // 32-token stages measured slower: the per-stage cost is the q.c^T re-reading
 // Q from shared memory and the stage's fixed synchronisation, not the load
 // latency.)  The 512 output
@@ -28,12 +26,12 @@
 // per block lands an MMA-ready operand: element (slot s, dim i) of a block at
 // ((s / 8) * 72 + i / 8) * 64 + (s % 8) * 8 + i % 8.
 //
-// Roles (224 threads): warps 0, 1, 4, 5 softmax and epilogue (two threads
-// per head row, each with half of the stage's tokens and half of the output
-// dims; the row maximum and sum combine the pair's through shared memory),
-// warp 2 producer, warp 3 q.c^T issuer and tensor-memory owner, warp 6 p.c
-// issuer (a separate thread, so that a p.c -- which frees its stage for the
-// next load -- is not queued behind the issue of the next stage's 36 q.c^T
+// Roles (352 threads): warps 0-7 softmax and epilogue (two threads per head
+// row, each with half of the stage's tokens and half of the output dims; the
+// row maximum and sum combine the pair's through shared memory), warp 8
+// producer, warp 9 q.c^T issuer and tensor-memory owner, warp 10 p.c issuer
+// (a separate thread, so that a p.c -- which frees its stage for the next
+// load -- is not queued behind the issue of the next stage's 36 q.c^T
 // steps).  Every wait is bounded.  A context longer than one
 // part is split over CTAs; the parts' (max, sum, output) states are merged by
 // mla_combine_kernel.
@@ -59,17 +57,18 @@ constexpr int DH = 256;         // output dims per CTA
 constexpr int TOKS = 64;        // tokens per stage
 constexpr int NSTG = 2;         // stage buffers (and S buffers)
 constexpr int NH = 64;          // head rows per CTA
-constexpr int THREADS = 224;
-// Softmax warps: 0, 1 (token columns 0..31 of head rows 0..63) and 4, 5
-// (columns 32..63 of the same rows: warp w reaches TMEM lanes 32 (w % 4) ..).
-__device__ __forceinline__ bool is_softmax_warp(int w) { return w < 2 || w == 4 || w == 5; }
+constexpr int THREADS = 352;
+// Softmax warps 0-7: warp w reaches TMEM lane quadrant w % 4, whose lanes
+// 0..15 hold head rows 16 (w % 4) ..; warps 0-3 take token columns 0..31,
+// warps 4-7 columns 32..63 of the same rows.  Warp 8 produces, warp 9 issues
+// q.c^T (and owns tensor memory), warp 10 issues p.c.
+constexpr int WARP_PROD = 8, WARP_QK = 9, WARP_PV = 10;
 constexpr int GRP = (D / 8) * 128;   // bytes per 8 rows of 576 values: 9216
 constexpr int STAGE = (TOKS / 8) * GRP;  // 73,728
 constexpr int Q_BYTES = (NH / 8) * GRP;  // 73,728
 constexpr int P_RG = (TOKS / 8) * 128;   // bytes per 8 rows of P: 1024
 constexpr int P_BYTES = (NH / 8) * P_RG; // [8 row groups][8 token groups][8][16 B] = 8192
-// P, then Q, then the stage ring: the 128-row A operands P and Q read their
-// rows 64..127 from the next 8 KiB (Q) and the next 72 KiB (stage 0).
+// P, then Q, then the stage ring.
 constexpr int OFF_P = 0;
 constexpr int OFF_Q = OFF_P + P_BYTES;
 constexpr int OFF_C = OFF_Q + Q_BYTES;
@@ -79,15 +78,14 @@ constexpr int OFF_X = OFF_MISC + 64;  // f32 [2 parities][2 halves][64 rows] row
                                       // f32 [2 halves][64 rows] row sums
 constexpr int SMEM_BYTES = 1024 + OFF_X + 6 * NH * 4;
 static_assert(SMEM_BYTES <= 232448, "MLA kernel exceeds 227 KB of shared memory");
-static_assert(OFF_Q - OFF_P >= P_BYTES && OFF_C - OFF_Q == Q_BYTES &&
-                  NSTG * STAGE >= Q_BYTES, "over-read layout");
+
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;     // O: 256 columns; S buffers at 0 and 64
 
-// kind::f16, D f32, A and B bf16, M = 128, N = n; b_mn: B MN-major.
+// kind::f16, D f32, A and B bf16, M = 64, N = n; b_mn: B MN-major.
 __host__ __device__ constexpr uint32_t idesc(int n, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(NH >> 4) << 24);
 }
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (wait included).
@@ -201,7 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       mbar_init(&c_full[i], 1);
       mbar_init(&c_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);  // one arrival per softmax warp
+      mbar_init(&s_free[i], 8);  // one arrival per softmax warp
     }
     mbar_init(p_full, 1);
     mbar_init(p_free, 1);
@@ -220,7 +218,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       *reinterpret_cast<uint4 *>(smem + OFF_Q + (qr >> 3) * GRP + c * 128 + (qr & 7) * 16) = v;
     }
   }
-  if (warp == 3) {
+  if (warp == WARP_QK) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(TMEM_COLS)
@@ -237,7 +235,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   // valid tokens of local stage i (the sequence's last stage may be partial)
   auto stage_tokens = [&](int i) { return min(TOKS, ctx - (st0 + i) * TOKS); };
 
-  if (warp == 2) {
+  if (warp == WARP_PROD) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_policy_evict_first();
     for (int i = 0; i < nst; ++i) {
@@ -271,7 +269,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
         mbar_wait_bounded(&c_full[last % NSTG], (uint32_t)(last / NSTG) & 1u);
       }
     }
-  } else if (warp == 3) {
+  } else if (warp == WARP_QK) {
     // ---------------------------------------------------- q.c^T issuer
     if (lane == 0) {
       const uint64_t qd = smem_desc(smem_addr(smem + OFF_Q), 128, GRP, 0);
@@ -293,7 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
         umma_commit(&s_full[buf]);
       }
     }
-  } else if (warp == 6) {
+  } else if (warp == WARP_PV) {
     // ------------------------------------------------------ p.c issuer
     if (lane == 0) {
       const uint64_t pd = smem_desc(smem_addr(smem + OFF_P), 128, P_RG, 0);
@@ -321,13 +319,13 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       umma_commit(o_done);
       mbar_wait_bounded(o_done, 0);
     }
-  } else if (is_softmax_warp(warp)) {
+  } else if (warp < 8) {
     // ------------------------------ softmax, two threads per head row
-    const int sh = warp >= 4 ? 1 : 0;      // token half (and output-dims half) of this thread
-    const int r = (warp & 1) * 32 + lane;  // head row
-    const int st = sh * 64 + r;            // 0..127 over the four warps
+    const int sh = warp >> 2;              // token half (and output-dims half) of this thread
+    const int r = (warp & 3) * 16 + (lane & 15);  // head row (lanes 0..15 of the quadrant)
+    const int st = tid;                    // 0..255 over the eight warps
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const bool rok = r < rows;
+    const bool rok = lane < 16 && r < rows;
     const int hr = hg * NH + r;
     const size_t slot_r = ((size_t)b * p.H + hr) * p.n_parts + part;
     float *xmax = reinterpret_cast<float *>(smem + OFF_X);  // [parity][half][row]
@@ -358,12 +356,12 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       }
       // the row maximum: this half's and the pair's (one exchange a stage,
       // by stage parity so that no second barrier is needed)
-      xmax[((i & 1) * 2 + sh) * NH + r] = hmax;
-      named_barrier_sync(1, 128);
+      if (lane < 16) xmax[((i & 1) * 2 + sh) * NH + r] = hmax;
+      named_barrier_sync(1, 256);
       const float rmax = fmaxf(hmax, xmax[((i & 1) * 2 + (sh ^ 1)) * NH + r]);
       // lazy rescale: move the row's reference when exceeded by 2^8; the
       // warp's O rows are rescaled together (tensor memory is warp-wide)
-      const bool need = rmax > m_ref + tc::kRescaleLog2;
+      const bool need = lane < 16 && rmax > m_ref + tc::kRescaleLog2;
       float alpha = 1.f;
       if (need) {
         alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - rmax);
@@ -390,6 +388,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       unsigned char *prow = smem + OFF_P + (r >> 3) * P_RG + (sh * (TH / 8)) * 128 + (r & 7) * 16;
 #pragma unroll
       for (int g = 0; g < TH / 8; ++g) {
+        if (lane >= 16) break;  // (lanes 16..31 of a quadrant hold no row)
         uint32_t pk[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -409,7 +408,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       const int lim = ((nv + 15) & ~15);
       if (nv < lim || bad) {
         unsigned char *cs = smem + OFF_C + buf * STAGE;
-        for (int k = st; k < lim * (D / 8); k += 128) {
+        for (int k = st; k < lim * (D / 8); k += 256) {
           const int t = k / (D / 8), c = k % (D / 8);
           if (t >= nv || ((bad >> (t / PB)) & 1))
             *reinterpret_cast<uint4 *>(cs + (t >> 3) * GRP + c * 128 + (t & 7) * 16) =
@@ -418,14 +417,14 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       }
       fence_proxy_async();
       tc_fence_before();
-      named_barrier_sync(1, 128);  // all four softmax warps have written P and zeroed
+      named_barrier_sync(1, 256);  // all eight softmax warps have written P and zeroed
       if (st == 0) mbar_arrive(p_full);
     }
     // ---- epilogue: the row's sum over both halves, then this thread's 128
     // output dims (one part) or partial state
     float *lx = xmax + 4 * NH;  // [2 halves][64 rows] (past both parities' maxima)
-    lx[sh * NH + r] = l;
-    named_barrier_sync(1, 128);
+    if (lane < 16) lx[sh * NH + r] = l;
+    named_barrier_sync(1, 256);
     const float l_row = l + lx[(sh ^ 1) * NH + r];
     wait_or_abort(o_done, 0, abort_flag, p.err);
     tc_fence_after();
@@ -457,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 3)
+  if (warp == WARP_QK)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(TMEM_COLS)
                  : "memory");
