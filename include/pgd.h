@@ -305,7 +305,9 @@ pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
  *      tensor cores (up to 128 rows = sequences x G per pass; larger groups
  *      take several), giving a partial state per (sequence, query head);
  *   2. each sequence's own suffix is attended as pgd_paged_decode_attention
- *      does, and its output merges the prefix's partial states.
+ *      does, giving partial states too;
+ *   3. a combine kernel merges both passes' partial states of every
+ *      (sequence, query head) into the output.
  * Groups (device int32 arrays of n_groups entries): sequences
  * group_first[i] .. group_first[i] + group_size[i] - 1 (consecutive; a
  * sequence in at most one group) share their first group_blocks[i] block
@@ -317,9 +319,11 @@ pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
  * max_group_size and max_group_blocks are host upper bounds of group_size
  * and group_blocks (they size the grid and the workspace).  workspace: at
  * least pgd_cascade_workspace_size(...) bytes, 256-byte aligned, zero-filled
- * before first use.  bf16 pools only.  The shared-prefix pass and the
- * suffix pass are two kernels; the second starts while the first runs and
- * waits for it only before merging. */
+ * before first use.  bf16 pools only.  Three kernels on `stream`: the
+ * shared-prefix pass runs on about a quarter of the SMs and lets the suffix
+ * pass start at once on the others (with num_splits = 0 the suffix pass's
+ * grid shrinks by the prefix pass's CTAs); the suffix pass completes only
+ * after the prefix pass, and the combine kernel waits for both. */
 size_t pgd_cascade_workspace_size(int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
                                   int32_t num_splits, int32_t max_group_size,
                                   int32_t max_group_blocks);

@@ -9,18 +9,23 @@
 //   out[b][h] = sum_t softmax_t(scale * q[b][h] . k_t) v_t over the
 //   context_lens[b] cached positions, K/V head h / G, read through the block
 //   table ("Module 10", section "Mapping logical positions to physical
-//   blocks").
+//   blocks").  The template's G is the number of query rows a unit serves:
+//   the heads of a KV head, times the T new tokens of a multi-query
+//   (speculative verify) call, whose token i sees positions up to
+//   context_lens[b] - T + i ("Module 10", Lab 2's mask) -- up to 16 rows.
 //
 // Work split.  A unit is one (sequence, KV head); its K/V tiles are read once
-// and serve all G query heads.  The units' blocks are laid end to end
-// (sequence-major, then KV head, then block) into one range of X blocks, cut
-// into one contiguous part per CTA in one of two ways, chosen by every CTA
-// alike from the context lengths:
+// and serve all G query rows.  The units are laid end to end (sequence-major,
+// then KV head) in a cost space -- each unit costs its blocks plus a fixed
+// charge for a segment's start and end -- cut into one contiguous part per
+// CTA in one of two ways, chosen by every CTA alike from the context lengths:
 //   units     CTA c takes unit c whole (when there are no more units than
 //             CTAs and the longest unit still streams no longer than the
 //             whole job takes at the HBM rate): no partial states at all;
-//   balanced  CTA c of P takes blocks [X*c/P, X*(c+1)/P): every CTA streams
-//             the same bytes (+-1 block) whatever the length mix.
+//   balanced  CTA c of P takes cost positions [X*c/P, X*(c+1)/P): every CTA
+//             carries the same cost whatever the length mix.
+// (Cascade calls start each sequence past its shared prefix and leave every
+// such unit's partial states to a combine kernel.)
 // A CTA walks its part unit by unit ("segments").  A segment that covers a
 // whole unit writes the output; otherwise it writes its (max, sum, weighted
 // sum) state and the last CTA of the unit to arrive merges the states by
