@@ -640,7 +640,7 @@ def run_mla(args, rank, world, local):
     peak, peak_kind = hbm_peak()
     achieved = nbytes / (attn_ms / 1e3) / 1e9
     parts = args.splits if args.splits > 0 else max(1, min(
-        64, torch.cuda.get_device_properties(local).multi_processor_count // (B * -(-H // 64) * 2)))
+        64, torch.cuda.get_device_properties(local).multi_processor_count // (B * -(-H // 64))))
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(max_ms / K, 5),

@@ -669,7 +669,7 @@ constexpr int kMlaD = 576, kMlaDv = 512;
 // fill the SMs with one CTA each (the kernel's shared memory allows one per
 // SM), at least one.
 int mla_auto_parts(int32_t B, int32_t H) {
-  const long long units = (long long)B * ((H + mla_heads_per_cta() - 1) / mla_heads_per_cta()) * 2;
+  const long long units = (long long)B * ((H + mla_heads_per_cta() - 1) / mla_heads_per_cta());
   if (units <= 0) return 1;
   return (int)std::max(1LL, std::min(64LL, (long long)sm_count() / units));
 }

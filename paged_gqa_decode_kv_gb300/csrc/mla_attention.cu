@@ -10,31 +10,39 @@
 // ("LLM inference systems engineering", 2.8.2: the identities behind the
 // absorption).  Decode is then MQA with G = n_h: one cache, all heads.
 //
-// On the tensor cores the head rows sit on the MMA's M side and the tokens on
-// N, as in the shared-prefix pass, with M = 64 (64 heads per CTA):
-//   S[64 rows][64 tok]  = Q[64 rows][576] . C^T        (A = Q, B = C, both K-major)
-//   O[64 rows][256 d]  += P[64 rows][64 tok] . C[:, half] (A = P K-major, B = C MN-major)
-// An M = 64 accumulator keeps row r in tensor-memory lane 32 (r / 16) + r % 16
-// (16 rows in each warp quadrant).  A 576-d latent row is 1152 B, so a
-// 64-token stage is 72 KiB; two stages, Q (64 heads) and P fill the 227 KB.  (A ring of four
-// 32-token stages measured slower: the per-stage cost is the q.c^T re-reading
-// Q from shared memory and the stage's fixed synchronisation, not the load
-// latency.)  The 512 output
-// dims do not fit tensor memory beside S (256 fp32 columns each), so a CTA
-// computes one half of them: CTA (sequence, 64-head group, half, part).  The
-// latent pool is tiled as 8 x 8 core matrices per 8 tokens, so one bulk copy
-// per block lands an MMA-ready operand: element (slot s, dim i) of a block at
-// ((s / 8) * 72 + i / 8) * 64 + (s % 8) * 8 + i % 8.
+// On the tensor cores a CTA takes 64 heads of one sequence and all 512 output
+// dims; q.c^T has the head rows on the MMA's M side, p.c is computed
+// transposed, with the latent dims on M:
+//   S[64 rows][64 tok]  = Q[64 rows][576] . C^T          (M = 64: A = Q, B = C, K-major)
+//   O^T[128 d][64 rows] += V^T[128 d][16 tok] . P^T       (M = 128, one MMA per 128-dim
+//                                                          block: A = the stage, MN-major;
+//                                                          B = P, K-major)
+// An MMA instruction costs about the larger of its math time (N / 2 cycles at
+// M = 128 and at M = 64), its operand bytes at 128 B per cycle and a floor of
+// about 44 cycles, so p.c at M = 128 runs at the full tensor rate and q.c^T
+// is not repeated for different output dims: per token the two 64-head CTAs
+// of a sequence spend ~25 cycles each (36 q.c^T steps at the floor over a
+// 64-token stage, 16 p.c MMAs of 48 cycles).  Tensor memory holds O^T in 256
+// columns (lanes = dims, a column per head) and the S buffers beside it; an
+// M = 64 accumulator keeps row r in lane 32 (r / 16) + r % 16 (16 rows in each
+// warp quadrant).  A 576-d latent row is 1152 B, so a 64-token stage is
+// 72 KiB; two stages, Q (64 heads) and P fill the 227 KB.  (Sharing the
+// q.c^T work of 128 heads between a CTA pair over distributed shared memory
+// would move a 32 KB fp32 score tile each way per stage at about 20 B per
+// cycle, more than the stage's own time.)  The latent pool is tiled as
+// 8 x 8 core matrices per 8 tokens, so one bulk copy per block lands an
+// MMA-ready operand for both contractions: element (slot s, dim i) of a block
+// at ((s / 8) * 72 + i / 8) * 64 + (s % 8) * 8 + i % 8.
 //
 // Roles (352 threads): warps 0-7 softmax and epilogue (two threads per head
-// row, each with half of the stage's tokens and half of the output dims; the
-// row maximum and sum combine the pair's through shared memory), warp 8
-// producer, warp 9 q.c^T issuer and tensor-memory owner, warp 10 p.c issuer
-// (a separate thread, so that a p.c -- which frees its stage for the next
-// load -- is not queued behind the issue of the next stage's 36 q.c^T
-// steps).  Every wait is bounded.  A context longer than one
-// part is split over CTAs; the parts' (max, sum, output) states are merged by
-// mla_combine_kernel.
+// row, each with half of the stage's tokens; the row maximum and sum combine
+// the pair's through shared memory; a moved reference rescales the O^T
+// columns of its head, 32 dims of two blocks per thread), warp 8 producer,
+// warp 9 q.c^T issuer and tensor-memory owner, warp 10 p.c issuer (a separate
+// thread, so that a p.c -- which frees its stage for the next load -- is not
+// queued behind the issue of the next stage's 36 q.c^T steps).  Every wait is
+// bounded.  A context longer than one part is split over CTAs; the parts'
+// (max, sum, output) states are merged by mla_combine_kernel.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -53,14 +61,15 @@ using tc::wait_or_abort;
 
 constexpr int D = 576;          // cached values per token (latent + RoPE key)
 constexpr int DV = 512;         // latent dims (the value)
-constexpr int DH = 256;         // output dims per CTA
 constexpr int TOKS = 64;        // tokens per stage
 constexpr int NSTG = 2;         // stage buffers (and S buffers)
 constexpr int NH = 64;          // head rows per CTA
+constexpr int NDB = DV / 128;   // 128-dim blocks of O^T (the M of one p.c MMA)
 constexpr int THREADS = 352;
 // Softmax warps 0-7: warp w reaches TMEM lane quadrant w % 4, whose lanes
-// 0..15 hold head rows 16 (w % 4) ..; warps 0-3 take token columns 0..31,
-// warps 4-7 columns 32..63 of the same rows.  Warp 8 produces, warp 9 issues
+// 0..15 hold head rows 16 (w % 4) .. of S; warps 0-3 take token columns
+// 0..31, warps 4-7 columns 32..63 of the same rows (and, for O^T, dims
+// 32 (w % 4) .. of blocks 0-1 and 2-3).  Warp 8 produces, warp 9 issues
 // q.c^T (and owns tensor memory), warp 10 issues p.c.
 constexpr int WARP_PROD = 8, WARP_QK = 9, WARP_PV = 10;
 constexpr int GRP = (D / 8) * 128;   // bytes per 8 rows of 576 values: 9216
@@ -74,18 +83,40 @@ constexpr int OFF_Q = OFF_P + P_BYTES;
 constexpr int OFF_C = OFF_Q + Q_BYTES;
 constexpr int OFF_BAR = OFF_C + NSTG * STAGE;
 constexpr int OFF_MISC = OFF_BAR + 128;
-constexpr int OFF_X = OFF_MISC + 64;  // f32 [2 parities][2 halves][64 rows] row maxima, then
-                                      // f32 [2 halves][64 rows] row sums
-constexpr int SMEM_BYTES = 1024 + OFF_X + 6 * NH * 4;
+constexpr int OFF_X = OFF_MISC + 64;  // f32 [2 parities][2 halves][64 rows] row maxima,
+                                      // [2 halves][64 rows] row sums, [64 rows] rescale factors
+constexpr int SMEM_BYTES = 1024 + OFF_X + 7 * NH * 4;
 static_assert(SMEM_BYTES <= 232448, "MLA kernel exceeds 227 KB of shared memory");
 
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_O = 256;     // O: 256 columns; S buffers at 0 and 64
+constexpr uint32_t COL_O = 0;          // O^T block k at columns 64 k .. 64 k + 63
+constexpr uint32_t COL_S = NDB * NH;   // S buffers at 256 and 320
 
-// kind::f16, D f32, A and B bf16, M = 64, N = n; b_mn: B MN-major.
-__host__ __device__ constexpr uint32_t idesc(int n, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(NH >> 4) << 24);
+// kind::f16, D f32, A and B bf16, M = m, N = n; a_mn / b_mn: MN-major operands.
+__host__ __device__ constexpr uint32_t idesc(int m, int n, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22, far below
+// the bf16 rounding of the probabilities; -inf gives +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Named barrier over `count` threads that also returns whether `pred` held
+// for any of them.
+__device__ __forceinline__ bool named_barrier_any(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // 32 consecutive fp32 columns of this warp's 32 TMEM lanes (wait included).
@@ -128,6 +159,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
       : "memory");
 }
 
+// Rows 0..15 of this warp's lane quadrant (an M = 64 accumulator's rows),
+// 32 consecutive columns: lanes t and t + 16 get row t's columns [0, 16) and
+// [16, 32) (wait included).
+__device__ __forceinline__ void tmem_ld_rows16(uint32_t taddr, float *v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16], 16;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Stages [first, last) of a sequence's ceil(ctx / 64) for part `part` of n.
 __device__ __forceinline__ void part_stages(int nst_seq, int part, int n_parts, int &first,
                                             int &last) {
@@ -142,8 +191,8 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   constexpr int PB = BS < TOKS ? BS : TOKS;
   constexpr uint32_t TILE = BS * D * 2;    // one block's latent rows
   constexpr uint32_t PIECE = PB * D * 2;
-  constexpr uint32_t IDESC_QK = idesc(TOKS, false);
-  constexpr uint32_t IDESC_PV = idesc(DH, true);
+  constexpr uint32_t IDESC_QK = idesc(NH, TOKS, false, false);
+  constexpr uint32_t IDESC_PV = idesc(128, NH, true, false);
   static_assert((TOKS % BS == 0 || BS % TOKS == 0) && BS % 8 == 0, "block size");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -152,8 +201,6 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   int w = (int)blockIdx.x;
   const int part = w % p.n_parts;
   w /= p.n_parts;
-  const int half = w & 1;
-  w >>= 1;
   const int n_hg = (p.H + NH - 1) / NH;
   const int hg = w % n_hg, b = w / n_hg;
   if (b >= p.B) return;
@@ -164,7 +211,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   int st0, st1;
   part_stages(nst_seq, part, p.n_parts, st0, st1);
   const int nst = st1 - st0;
-  if (!ctx_ok && tid == 0 && half == 0 && hg == 0 && part == 0)
+  if (!ctx_ok && tid == 0 && hg == 0 && part == 0)
     atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
 
   const int r = tid;  // head row of warps 0-1 (empty parts)
@@ -174,11 +221,10 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   const size_t slot = ((size_t)b * p.H + h) * p.n_parts + part;
 
   if (nst <= 0) {  // an empty part (or a rejected sequence): a -inf maximum
-    if (warp < 2 && row_ok && p.n_parts > 1) {  // (both halves of the row's dims)
-      if (half == 0)
-        *reinterpret_cast<float2 *>(p.part_ml + slot * 2) = make_float2(-INFINITY, 0.f);
-      float4 *o = reinterpret_cast<float4 *>(p.part_o + slot * DV + half * DH);
-      for (int i = 0; i < DH / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (warp < 2 && row_ok && p.n_parts > 1) {
+      *reinterpret_cast<float2 *>(p.part_ml + slot * 2) = make_float2(-INFINITY, 0.f);
+      float4 *o = reinterpret_cast<float4 *>(p.part_o + slot * DV);
+      for (int i = 0; i < DV / 4; ++i) o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     return;
   }
@@ -285,7 +331,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
           const uint64_t cd = smem_desc(smem_addr(smem + OFF_C + buf * STAGE), 128, GRP, 0);
 #pragma unroll 4
           for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16(tmem + (uint32_t)(buf * TOKS), qd + (uint64_t)(kk * 16),
+            umma_bf16(tmem + COL_S + (uint32_t)(buf * TOKS), qd + (uint64_t)(kk * 16),
                       cd + (uint64_t)(kk * 16), IDESC_QK, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[buf]);
@@ -294,6 +340,8 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   } else if (warp == WARP_PV) {
     // ------------------------------------------------------ p.c issuer
     if (lane == 0) {
+      // B = P^T: heads on N, K-major (8 tokens per 16-byte row, 128 B per
+      // token group, P_RG per 8 heads)
       const uint64_t pd = smem_desc(smem_addr(smem + OFF_P), 128, P_RG, 0);
       for (int j = 0; j < nst; ++j) {
         const int buf = j % NSTG;
@@ -301,16 +349,15 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
         wait_or_abort(p_full, (uint32_t)(j & 1), abort_flag, p.err);
         tc_fence_after();
         if (!*abort_flag) {
-          // A = P (K-major, tokens along K: 256 B per 16 tokens); B = C
-          // MN-major (dims along N, 128 B per 8 dims; 2 token groups =
-          // 18,432 B per 16 tokens), starting at this CTA's 256 dims
-          const uint64_t cvd =
-              smem_desc(smem_addr(smem + OFF_C + buf * STAGE + half * (DH / 8) * 128), GRP, 128,
-                        0);
+          // A = V^T: 128 dims on M, MN-major (8 dims per 16-byte row, 128 B
+          // per 8 dims; 8 tokens per core matrix, GRP per token group)
+          const uint64_t vd = smem_desc(smem_addr(smem + OFF_C + buf * STAGE), GRP, 128, 0);
           for (int kt = 0; kt < nkt; ++kt)
-            umma_bf16(tmem + COL_O, pd + (uint64_t)(kt * 16),
-                      cvd + (uint64_t)(kt * (2 * GRP / 16)), IDESC_PV,
-                      (j > 0 || kt > 0) ? 1u : 0u);
+#pragma unroll
+            for (int db = 0; db < NDB; ++db)
+              umma_bf16(tmem + COL_O + (uint32_t)(db * NH),
+                        vd + (uint64_t)((db * 16 * 128 + kt * 2 * GRP) >> 4),
+                        pd + (uint64_t)(kt * 16), IDESC_PV, (j > 0 || kt > 0) ? 1u : 0u);
         }
         umma_commit(&c_empty[buf]);  // the stage buffer may be refilled
         umma_commit(p_free);         // P may be rewritten
@@ -320,8 +367,9 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       mbar_wait_bounded(o_done, 0);
     }
   } else if (warp < 8) {
-    // ------------------------------ softmax, two threads per head row
-    const int sh = warp >> 2;              // token half (and output-dims half) of this thread
+    // ------------------------------ softmax, four threads per head row
+    const int sh = warp >> 2;              // token half of this warp (and O^T blocks 2 sh ..)
+    const int tq = lane >> 4;              // 16-token quarter of the half (lanes t, t + 16)
     const int r = (warp & 3) * 16 + (lane & 15);  // head row (lanes 0..15 of the quadrant)
     const int st = tid;                    // 0..255 over the eight warps
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -329,7 +377,9 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
     const int hr = hg * NH + r;
     const size_t slot_r = ((size_t)b * p.H + hr) * p.n_parts + part;
     float *xmax = reinterpret_cast<float *>(smem + OFF_X);  // [parity][half][row]
-    constexpr int TH = TOKS / 2;           // token columns per thread
+    float *lx = xmax + 4 * NH;                               // [half][row]
+    float *alpha_s = lx + 2 * NH;                            // [row]
+    constexpr int TT = TOKS / 4;           // token columns per thread
     float m_ref = -INFINITY, l = 0.f;
     for (int i = 0; i < nst; ++i) {
       const int buf = i % NSTG;
@@ -341,65 +391,80 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       wait_or_abort(&c_full[buf], par, abort_flag, p.err);
       const int bad = bad_mask[buf];
       tc_fence_after();
-      float sv[TH];
-      tmem_ld32(tmem + lane_base + (uint32_t)(buf * TOKS + sh * TH), sv);
+      float sv[TT];  // row r, tokens sh * 32 + tq * 16 + [0, 16)
+      tmem_ld_rows16(tmem + lane_base + COL_S + (uint32_t)(buf * TOKS + sh * 2 * TT), sv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[buf]);
-      float hmax = -INFINITY;
+      // Scores stay unscaled (the scale is > 0, so the maximum commutes with
+      // it); masked tokens become -inf.  A full stage needs no mask.
+      if (nv < TOKS || bad) {
 #pragma unroll
-      for (int c = 0; c < TH; ++c) {
-        const int t = sh * TH + c;
-        const bool ok = t < nv && !((bad >> (t / PB)) & 1);
-        sv[c] = ok ? sv[c] * p.qk_scale_log2 : -INFINITY;
-        hmax = fmaxf(hmax, sv[c]);
+        for (int c = 0; c < TT; ++c) {
+          const int t = (2 * sh + tq) * TT + c;
+          if (t >= nv || ((bad >> (t / PB)) & 1)) sv[c] = -INFINITY;
+        }
       }
+      float hm[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+      for (int c = 4; c < TT; ++c) hm[c & 3] = fmaxf(hm[c & 3], sv[c]);
+      float hmax = fmaxf(fmaxf(hm[0], hm[1]), fmaxf(hm[2], hm[3]));
+      hmax = fmaxf(hmax, __shfl_xor_sync(kFullMask, hmax, 16)) * p.qk_scale_log2;
       // the row maximum: this half's and the pair's (one exchange a stage,
       // by stage parity so that no second barrier is needed)
       if (lane < 16) xmax[((i & 1) * 2 + sh) * NH + r] = hmax;
       named_barrier_sync(1, 256);
       const float rmax = fmaxf(hmax, xmax[((i & 1) * 2 + (sh ^ 1)) * NH + r]);
-      // lazy rescale: move the row's reference when exceeded by 2^8; the
-      // warp's O rows are rescaled together (tensor memory is warp-wide)
-      const bool need = lane < 16 && rmax > m_ref + tc::kRescaleLog2;
+      // lazy rescale: move the row's reference when exceeded by 2^8.  O^T
+      // keeps a head per column, so a move rescales that column of every
+      // block; the pass runs when any row moved, with factor 1 elsewhere.
+      const bool need = rmax > m_ref + tc::kRescaleLog2;  // (alike in the row's four threads)
       float alpha = 1.f;
       if (need) {
         alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - rmax);
         m_ref = rmax;
         l *= alpha;
       }
-      // P and the O rescale both wait for the previous p.c
+      if (sh == 0 && lane < 16) alpha_s[r] = alpha;
+      const bool any = named_barrier_any(1, 256, need);
+      // P and the O^T rescale both wait for the previous p.c
       wait_or_abort(p_free, ((uint32_t)(i & 1)) ^ 1u, abort_flag, p.err);
-      if (i > 0 && __any_sync(kFullMask, need)) {
+      if (i > 0 && any) {
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < DH / 64; ++c) {  // this thread's 128 of the 256 O columns
+        for (int k = 0; k < 2 * (NH / 32); ++k) {  // blocks 2 sh, 2 sh + 1; 32 heads at a time
           float ov[32];
-          const uint32_t col = COL_O + (uint32_t)(sh * (DH / 2) + c * 32);
+          const uint32_t col = COL_O + (uint32_t)((2 * sh + (k >> 1)) * NH + (k & 1) * 32);
           tmem_ld32(tmem + lane_base + col, ov);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) ov[k] *= alpha;
+          for (int c = 0; c < 32; ++c) ov[c] *= alpha_s[(k & 1) * 32 + c];
           tmem_st32(tmem + lane_base + col, ov);
         }
         tc_fence_before();
       }
-      // probabilities in bf16, summed as the tensor cores see them; row r's
-      // 8-token pieces at core matrix (r / 8, token group), row r % 8
-      unsigned char *prow = smem + OFF_P + (r >> 3) * P_RG + (sh * (TH / 8)) * 128 + (r & 7) * 16;
+      // probabilities 2^(s * scale - m) in bf16 (one fma and one ex2 each; a
+      // masked -inf score gives 0), summed as the tensor cores see them; row
+      // r's 8-token pieces at core matrix (r / 8, token group), row r % 8
+      {
+        unsigned char *prow =
+            smem + OFF_P + (r >> 3) * P_RG + ((2 * sh + tq) * (TT / 8)) * 128 + (r & 7) * 16;
+        const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;  // (every score masked so far)
+        float ls[2] = {0.f, 0.f};
 #pragma unroll
-      for (int g = 0; g < TH / 8; ++g) {
-        if (lane >= 16) break;  // (lanes 16..31 of a quadrant hold no row)
-        uint32_t pk[4];
+        for (int g = 0; g < TT / 8; ++g) {
+          uint32_t pk[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = g * 8 + 2 * k;
-          const __nv_bfloat16 a = __float2bfloat16_rn(sv[c] == -INFINITY ? 0.f : exp2f(sv[c] - m_ref));
-          const __nv_bfloat16 bb =
-              __float2bfloat16_rn(sv[c + 1] == -INFINITY ? 0.f : exp2f(sv[c + 1] - m_ref));
-          l += __bfloat162float(a) + __bfloat162float(bb);
-          pk[k] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(bb) << 16);
+          for (int k = 0; k < 4; ++k) {
+            const int c = g * 8 + 2 * k;
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(
+                ex2_approx(fmaf(sv[c], p.qk_scale_log2, -mb)),
+                ex2_approx(fmaf(sv[c + 1], p.qk_scale_log2, -mb)));
+            pk[k] = *reinterpret_cast<const uint32_t *>(&pr);
+            ls[k & 1] += bf16lo(pk[k]) + bf16hi(pk[k]);
+          }
+          *reinterpret_cast<uint4 *>(prow + g * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        *reinterpret_cast<uint4 *>(prow + g * 128) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        l += ls[0] + ls[1];
       }
       // Latent rows p.c reads that hold no valid token (the tail of the last
       // block, blocks with a bad id) must not feed NaN into it: zero them
@@ -420,37 +485,38 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       named_barrier_sync(1, 256);  // all eight softmax warps have written P and zeroed
       if (st == 0) mbar_arrive(p_full);
     }
-    // ---- epilogue: the row's sum over both halves, then this thread's 128
-    // output dims (one part) or partial state
-    float *lx = xmax + 4 * NH;  // [2 halves][64 rows] (past both parities' maxima)
+    // ---- epilogue: the row's sum over both halves; then O^T by dims, 32
+    // dims of two blocks per thread, every head of the CTA
+    l += __shfl_xor_sync(kFullMask, l, 16);  // the row's two quarters of this half
     if (lane < 16) lx[sh * NH + r] = l;
     named_barrier_sync(1, 256);
     const float l_row = l + lx[(sh ^ 1) * NH + r];
+    float *linv = xmax;  // [row] 1 / sum (the maxima are no longer read)
+    if (sh == 0 && lane < 16) linv[r] = 1.f / l_row;
+    if (rok && p.n_parts > 1 && sh == 0)
+      *reinterpret_cast<float2 *>(p.part_ml + slot_r * 2) = make_float2(m_ref, l_row);
+    named_barrier_sync(1, 256);
     wait_or_abort(o_done, 0, abort_flag, p.err);
     tc_fence_after();
+    const size_t row0 = (size_t)b * p.H + (size_t)hg * NH;  // first head row of the CTA
 #pragma unroll 1
-    for (int c = 0; c < DH / 64; ++c) {
+    for (int k = 0; k < 2 * (NH / 32); ++k) {
       float ov[32];
-      const int d0 = sh * (DH / 2) + c * 32;  // first of these 32 dims within the CTA's half
-      tmem_ld32(tmem + lane_base + COL_O + d0, ov);  // warp-wide; stores by real rows
-      if (rok) {
-        if (p.n_parts == 1) {
-          const float inv = 1.f / l_row;
-          __nv_bfloat16 *o = p.out + ((size_t)b * p.H + hr) * DV + half * DH + d0;
-#pragma unroll
-          for (int k = 0; k < 32; k += 2)
-            *reinterpret_cast<__nv_bfloat162 *>(o + k) =
-                __floats2bfloat162_rn(ov[k] * inv, ov[k + 1] * inv);
-        } else {
-          float4 *o = reinterpret_cast<float4 *>(p.part_o + slot_r * DV + half * DH + d0);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            o[k] = make_float4(ov[4 * k], ov[4 * k + 1], ov[4 * k + 2], ov[4 * k + 3]);
-        }
+      const int db = 2 * sh + (k >> 1), h0 = (k & 1) * 32;
+      const int dim = db * 128 + (warp & 3) * 32 + lane;  // this lane's latent dim
+      tmem_ld32(tmem + lane_base + COL_O + (uint32_t)(db * NH + h0), ov);
+      if (p.n_parts == 1) {
+#pragma unroll 4
+        for (int c = 0; c < 32; ++c)
+          if (h0 + c < rows)
+            p.out[(row0 + h0 + c) * DV + dim] = __float2bfloat16_rn(ov[c] * linv[h0 + c]);
+      } else {
+#pragma unroll 4
+        for (int c = 0; c < 32; ++c)
+          if (h0 + c < rows)
+            p.part_o[((row0 + h0 + c) * p.n_parts + part) * DV + dim] = ov[c];
       }
     }
-    if (rok && p.n_parts > 1 && half == 0 && sh == 0)
-      *reinterpret_cast<float2 *>(p.part_ml + slot_r * 2) = make_float2(m_ref, l_row);
   }
 
   tc_fence_before();
@@ -483,10 +549,10 @@ __global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p) {
     const float w = exp2f(v.x - M);
     L = fmaf(w, v.y, L);
     o0 = fmaf(w, __ldcg(po + (size_t)k * DV + e), o0);
-    o1 = fmaf(w, __ldcg(po + (size_t)k * DV + e + DH), o1);
+    o1 = fmaf(w, __ldcg(po + (size_t)k * DV + e + DV / 2), o1);
   }
   p.out[(size_t)row * DV + e] = __float2bfloat16_rn(o0 / L);
-  p.out[(size_t)row * DV + e + DH] = __float2bfloat16_rn(o1 / L);
+  p.out[(size_t)row * DV + e + DV / 2] = __float2bfloat16_rn(o1 / L);
 }
 
 // One warp per sequence: the new token's 576 values into its slot (72
@@ -546,7 +612,7 @@ int mla_heads_per_cta() { return mla::NH; }
 
 cudaError_t mla_attention_launch(const MlaParams &p, cudaStream_t stream) {
   const int n_hg = (p.H + mla::NH - 1) / mla::NH;
-  const long long grid = (long long)p.B * n_hg * 2 * p.n_parts;
+  const long long grid = (long long)p.B * n_hg * p.n_parts;
   if (grid <= 0 || grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   cudaError_t e = cudaErrorInvalidValue;
   switch (p.bs) {
