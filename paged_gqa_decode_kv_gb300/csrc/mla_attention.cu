@@ -98,6 +98,12 @@ __host__ __device__ constexpr uint32_t idesc(int m, int n, bool a_mn, bool b_mn)
          ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
+// Bulk prefetch of global memory into L2 (src 16-byte aligned, bytes a
+// multiple of 16); a hint, with no completion to wait for.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2^x by the hardware approximation (relative error about 2^-22, far below
 // the bf16 rounding of the probabilities; -inf gives +0).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -308,6 +314,16 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
         bulk_copy_g2s(smem + OFF_C + buf * STAGE + lane * (PB / 8) * GRP,
                       p.cache + (size_t)blk * TILE + (size_t)((t0 % BS) / 8) * GRP, PIECE,
                       &c_full[buf], policy);
+      // The stage after next goes to L2 now: its buffer frees only after this
+      // stage's p.c, and its copy then finds the data on chip.
+      const int ip = i + NSTG;
+      if (ip < nst) {
+        const int nbp = (stage_tokens(ip) + PB - 1) / PB;
+        const int tp = (st0 + ip) * TOKS + lane * PB;
+        const int blkp = (lane < nbp) ? __ldg(trow + tp / BS) : -1;
+        if ((unsigned)blkp < (unsigned)p.NB)
+          prefetch_l2(p.cache + (size_t)blkp * TILE + (size_t)((tp % BS) / 8) * GRP, PIECE);
+      }
     }
     if (lane == 0) {  // no copy may still be landing when the CTA exits
       for (int k = 1; k <= NSTG && k <= nst; ++k) {
@@ -528,31 +544,52 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
                  : "memory");
 }
 
-// Merge of the parts of each (sequence, head) by log-sum-exp: one CTA per
-// row, thread e owning dims e and e + 256.
-__global__ void __launch_bounds__(256) mla_combine_kernel(const MlaParams p) {
+// Merge of the parts of each (sequence, head) by log-sum-exp: a warp per
+// row, lane e owning dims 4 (32 j + e) .. + 3 for j < 4 (coalesced float4s);
+// a part's four loads are issued together, ahead of their use.
+__global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p) {
   pdl_wait();
-  const int row = (int)blockIdx.x;  // b * H + h
-  const int b = row / p.H;
-  if (b >= p.B) return;
-  const int c = __ldg(p.ctx + b);
+  const int row = (int)blockIdx.x * 4 + (threadIdx.x >> 5);  // b * H + h
+  const int lane = threadIdx.x & 31;
+  if (row >= p.B * p.H) return;
+  const int c = __ldg(p.ctx + row / p.H);
   if (c < 1 || c > p.MB * p.bs) return;  // rejected (flagged by the attention kernel)
-  const int e = threadIdx.x;
   const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml) + (size_t)row * p.n_parts;
-  const float *po = p.part_o + (size_t)row * p.n_parts * DV;
+  const float4 *po = reinterpret_cast<const float4 *>(p.part_o) + (size_t)row * p.n_parts * (DV / 4);
   float M = -INFINITY;
-  for (int k = 0; k < p.n_parts; ++k) M = fmaxf(M, __ldcg(&ml[k].x));
-  float L = 0.f, o0 = 0.f, o1 = 0.f;
+  for (int k = lane; k < p.n_parts; k += 32) M = fmaxf(M, __ldcg(&ml[k].x));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFullMask, M, o));
+  float L = 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
   for (int k = 0; k < p.n_parts; ++k) {
     const float2 v = __ldcg(&ml[k]);
-    if (v.x == -INFINITY) continue;
+    float4 x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = __ldcg(po + (size_t)k * (DV / 4) + j * 32 + lane);
+    if (v.x == -INFINITY) continue;  // an empty part
     const float w = exp2f(v.x - M);
     L = fmaf(w, v.y, L);
-    o0 = fmaf(w, __ldcg(po + (size_t)k * DV + e), o0);
-    o1 = fmaf(w, __ldcg(po + (size_t)k * DV + e + DV / 2), o1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acc[j].x = fmaf(w, x[j].x, acc[j].x);
+      acc[j].y = fmaf(w, x[j].y, acc[j].y);
+      acc[j].z = fmaf(w, x[j].z, acc[j].z);
+      acc[j].w = fmaf(w, x[j].w, acc[j].w);
+    }
   }
-  p.out[(size_t)row * DV + e] = __float2bfloat16_rn(o0 / L);
-  p.out[(size_t)row * DV + e + DV / 2] = __float2bfloat16_rn(o1 / L);
+  const float inv = 1.f / L;
+  uint2 *o = reinterpret_cast<uint2 *>(p.out + (size_t)row * DV);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[j].x * inv, acc[j].y * inv);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc[j].z * inv, acc[j].w * inv);
+    o[j * 32 + lane] = make_uint2(*reinterpret_cast<const uint32_t *>(&lo),
+                                  *reinterpret_cast<const uint32_t *>(&hi));
+  }
 }
 
 // One warp per sequence: the new token's 576 values into its slot (72
@@ -622,8 +659,8 @@ cudaError_t mla_attention_launch(const MlaParams &p, cudaStream_t stream) {
   }
   if (e != cudaSuccess || p.n_parts == 1) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.B * p.H));
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3((unsigned)((p.B * p.H + 3) / 4));
+  cfg.blockDim = dim3(128);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
