@@ -43,6 +43,9 @@ ATTENTION_SOURCES = [os.path.join(ROOT, "paged_gqa_decode_kv_gb300", "csrc", f)
                      for f in ("attention_kernel.cuh", "pgd_device.cuh")]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "paged_attention_batch16_ctx8192.md")
 PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "paged_attention_fp8_batch16_ctx8192.md")
+MLA_SOURCES = [os.path.join(ROOT, "paged_gqa_decode_kv_gb300", "csrc", f)
+               for f in ("mla_attention.cu", "attention_kernel.cuh", "pgd_device.cuh")]
+PROFILE_SUMMARY_MLA = os.path.join(ROOT, "profiles", "mla_attention_batch16_ctx8192_h128.md")
 
 
 def parse_args(argv=None):
@@ -204,13 +207,29 @@ def profiled_traffic(kv: str = "bf16", workload: str = "batch16_ctx8192"):
     return int(m_bytes.group(1)) if kernel_source_sha256() == m_sha.group(1) else None
 
 
-def kernel_source_sha256() -> str:
-    """sha256 of the attention kernel's sources (attention_kernel.cuh, then
-    the device header it includes)."""
+def kernel_source_sha256(paths=None) -> str:
+    """sha256 of a kernel's sources (default: the attention kernel's,
+    attention_kernel.cuh, then the device header it includes)."""
     h = hashlib.sha256()
-    for path in ATTENTION_SOURCES:
+    for path in (paths or ATTENTION_SOURCES):
         h.update(open(path, "rb").read())
     return h.hexdigest()
+
+
+def profiled_mla_traffic(workload: str):
+    """DRAM bytes per launch of the MLA attention kernel from its committed ncu
+    summary (batch 16 x 8192 tokens), or None if the kernel changed since."""
+    if workload != "mla128_batch16_ctx8192":
+        return None
+    try:
+        text = open(PROFILE_SUMMARY_MLA).read()
+    except OSError:
+        return None
+    m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not (m_bytes and m_sha):
+        return None
+    return int(m_bytes.group(1)) if kernel_source_sha256(MLA_SOURCES) == m_sha.group(1) else None
 
 
 # ------------------------------------------------------------ CPU baseline
@@ -660,7 +679,8 @@ def run_mla(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": "pgd::mla::mla_attention_kernel<%d> (tcgen05)"
                      % mb.block_size, "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": None, "launch_ms": round(attn_ms, 5), "bytes_per_launch": nbytes,
+                     "traffic": profiled_mla_traffic(name) if args.splits == 0 else None,
+                     "launch_ms": round(attn_ms, 5), "bytes_per_launch": nbytes,
                      "tflops_achieved": round(flops / (attn_ms / 1e3) / 1e12, 2),
                      "flop_per_byte": round(flops / nbytes, 1)},
         "e2e": {"value": round(sum_over_ranks(nbytes * K, world) / (e2e_ms / 1e3) / 1e9, 2),
