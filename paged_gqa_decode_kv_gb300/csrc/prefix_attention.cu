@@ -11,18 +11,19 @@
 //   S[128 rows][128 tok] = Q[128 rows][128 d] . K^T   (A = Q, B = K, K-major)
 //   O[128 rows][128 d]  += P[128 rows][128 tok] . V    (A = P K-major, B = V MN-major)
 // with the same tiled pool as the decode kernel (one bulk copy per (block,
-// head) tile lands an MMA-ready operand).  Each softmax thread owns one row,
-// so the row maximum, the lazy rescale (reference moved when exceeded by 2^8)
-// and the row sum are thread-local.  The result is a partial state (max, sum,
+// head) tile lands an MMA-ready operand).  The lazy rescale moves a row's
+// reference when exceeded by 2^8.  The result is a partial state (max, sum,
 // unnormalised output) per (sequence, query head) and prefix part; the decode
 // pass over each sequence's own suffix merges these into its output by
 // log-sum-exp ("The math of Transformer inference", section 8; "LLM inference
 // systems engineering", 2.8.3).
 //
 // Work item (one CTA): (group, KV head, chunk of 128 / G sequences, part of
-// the prefix's blocks).  Roles (256 threads): warps 0-3 softmax and
-// epilogue (thread = row), warp 4 K producer, warp 5 V producer, warp 6 MMA
-// issuer and tensor-memory owner.  Every wait is bounded.
+// the prefix's blocks).  Roles (352 threads): warps 0-7 softmax and epilogue
+// (two threads per row: warps w and w + 4 take tokens 0..63 and 64..127 of
+// lane quadrant w's rows, and half of the output dims; the row maximum and
+// sum combine through shared memory), warp 8 K producer, warp 9 V producer,
+// warp 10 MMA issuer and tensor-memory owner.  Every wait is bounded.
 #include "attention_kernel.cuh"
 
 namespace pgd {
@@ -38,7 +39,8 @@ using tc::wait_or_abort;
 
 constexpr int TOKP = 128;     // tokens per stage (MMA N of q.k^T)
 constexpr int ROWS = 128;     // query rows per CTA (MMA M)
-constexpr int THREADS = 256;
+constexpr int THREADS = 352;
+constexpr int WARP_KP = 8, WARP_VP = 9, WARP_MMA = 10;
 constexpr int STAGE = TOKP * 256;  // bytes of one K (or V) stage
 constexpr int OFF_Q = 0;                       // [128 rows][128 d] bf16, K-major
 constexpr int OFF_K = OFF_Q + ROWS * 256;      // 2 stages
@@ -46,11 +48,22 @@ constexpr int OFF_V = OFF_K + 2 * STAGE;       // 2 stages
 constexpr int OFF_P = OFF_V + 2 * STAGE;       // 2 x [128 rows][128 tok] bf16, K-major
 constexpr int OFF_BAR = OFF_P + 2 * ROWS * 256;
 constexpr int OFF_MISC = OFF_BAR + 256;        // tmem base, abort flag, stage masks [4]
-constexpr int SMEM_BYTES = 1024 + OFF_MISC + 64;
+constexpr int OFF_X = OFF_MISC + 64;            // f32 [2 parities][2 halves][128 rows] maxima
+                                                // (finally one parity's: row sums)
+// (no swizzled operand: 128-byte alignment of the base suffices)
+constexpr int SMEM_BYTES = 128 + OFF_X + 4 * ROWS * 4;
 static_assert(SMEM_BYTES <= 232448, "prefix pass exceeds 227 KB of shared memory");
 constexpr uint32_t TMEM_COLS = 512;            // S 2 x 128 columns, O 128 columns
 
 __device__ __forceinline__ uint32_t col_s(int sb) { return (uint32_t)sb * 128u; }
+
+// 2^x by the hardware approximation (relative error about 2^-22, far below
+// the bf16 rounding of the probabilities; -inf gives +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 constexpr uint32_t COL_O = 256;
 
 // kind::f16 instruction descriptor for M = 128, N = 128, bf16 inputs, f32
@@ -194,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
 
   extern __shared__ unsigned char smem_raw[];
   unsigned char *smem = reinterpret_cast<unsigned char *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~(uintptr_t)127);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint64_t *full_k = bars, *empty_k = bars + 2, *full_v = bars + 4, *empty_v = bars + 6;
   uint64_t *s_full = bars + 8, *s_free = bars + 10, *p_full = bars + 12, *p_free = bars + 14;
@@ -210,8 +223,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
       mbar_init(&full_v[i], 1);
       mbar_init(&empty_v[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
-      mbar_init(&p_full[i], 4);
+      mbar_init(&s_free[i], 8);  // one arrival per softmax warp
+      mbar_init(&p_full[i], 8);
       mbar_init(&p_free[i], 1);
       mbar_init(&m_ready[i], 1);
     }
@@ -231,7 +244,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
     for (int c = 0; c < 16; ++c)
       *reinterpret_cast<uint4 *>(smem + OFF_Q + ((r >> 3) * 16 + c) * 128 + (r & 7) * 16) = v[c];
   }
-  if (warp == 6) {
+  if (warp == WARP_MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(tmem_slot)),
                  "r"(TMEM_COLS)
@@ -245,13 +258,13 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
   const uint32_t tmem = *tmem_slot;
   const int nst = (nblk + SB - 1) / SB;
 
-  if (warp == 4) {
+  if (warp == WARP_KP) {
     produce<BS>(p, trow, blk0, nblk, p.k_cache, g, smem + OFF_K, full_k, empty_k, stage_mask,
                 abort_flag, lane);
-  } else if (warp == 5) {
+  } else if (warp == WARP_VP) {
     produce<BS>(p, trow, blk0, nblk, p.v_cache, g, smem + OFF_V, full_v, empty_v, nullptr,
                 abort_flag, lane);
-  } else if (warp == 6) {
+  } else if (warp == WARP_MMA) {
     // ----------------------------------------------------- MMA issuer
     // q.k^T of stage i is issued before p.v of stage i - 1, so it overlaps
     // the softmax of stage i - 1.
@@ -299,9 +312,16 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
       }
       umma_commit(o_done);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------ softmax, one row each
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  } else if (warp < 8) {
+    // -------------------------------------- softmax, two threads per row
+    constexpr int TH = TOKP / 2;      // token columns per thread
+    const int sh = warp >> 2;         // token half (and output-dims half) of this thread
+    const int rr = (warp & 3) * 32 + lane;  // row (= tensor-memory lane)
+    const bool rok = rr < rows;
+    const int rbr = first + s0 + rr / G, rhr = g * G + rr % G;
+    const size_t slot_r = ((size_t)rbr * p.n_q + rhr) * p.n_tsplit + ts;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    float *xmax = reinterpret_cast<float *>(smem + OFF_X);  // [parity][half][row]
     float m_ref = -INFINITY, l = 0.f;
     for (int st = 0; st < nst; ++st) {
       const int slot = st & 1;
@@ -310,22 +330,32 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
       wait_or_abort(&m_ready[slot], (uint32_t)(st >> 1) & 1u, abort_flag, p.err);
       const int mask = stage_mask[st & 3];
       tc_fence_after();
-      float sv[TOKP];
+      float sv[TH];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + col_s(slot) + c * 32, sv + c * 32);
+      for (int c = 0; c < TH / 32; ++c)
+        tmem_ld32(tmem + lane_base + col_s(slot) + sh * TH + c * 32, sv + c * 32);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[slot]);
-      // scores in the log2 domain; columns past the stage's blocks or in a
-      // block with a bad id are -inf
-      float rmax = -INFINITY;
+      // Scores stay unscaled (the scale is > 0, so the maximum commutes with
+      // it); columns past the stage's blocks or in a block with a bad id are
+      // -inf.  A full stage needs no mask.
+      if (nb < SB || mask) {
 #pragma unroll
-      for (int c = 0; c < TOKP; ++c) {
-        const int blk = c / BS;
-        const bool ok = blk < nb && !((mask >> blk) & 1);
-        sv[c] = ok ? sv[c] * p.qk_scale_log2 : -INFINITY;
-        rmax = fmaxf(rmax, sv[c]);
+        for (int c = 0; c < TH; ++c) {
+          const int blk = (sh * TH + c) / BS;
+          if (blk >= nb || ((mask >> blk) & 1)) sv[c] = -INFINITY;
+        }
       }
+      float hm[4] = {sv[0], sv[1], sv[2], sv[3]};
+#pragma unroll
+      for (int c = 4; c < TH; ++c) hm[c & 3] = fmaxf(hm[c & 3], sv[c]);
+      const float hmax = fmaxf(fmaxf(hm[0], hm[1]), fmaxf(hm[2], hm[3])) * p.qk_scale_log2;
+      // the row maximum: this half's and the pair's (one exchange a stage, by
+      // stage parity so that no second barrier is needed)
+      xmax[((st & 1) * 2 + sh) * ROWS + rr] = hmax;
+      named_barrier_sync(1, 256);
+      const float rmax = fmaxf(hmax, xmax[((st & 1) * 2 + (sh ^ 1)) * ROWS + rr]);
       // move the row's reference when exceeded by 2^8; the O rows of the
       // warp are rescaled together (tensor-memory access is warp-wide), by 1
       // in the rows that keep their reference
@@ -341,39 +371,48 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
         wait_or_abort(&p_free[(st - 1) & 1], (uint32_t)((st - 1) >> 1) & 1u, abort_flag, p.err);
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {  // this thread's 64 of the 128 O columns
           float ov[32];
-          tmem_ld32(tmem + lane_base + COL_O + c * 32, ov);
+          const uint32_t col = COL_O + (uint32_t)(sh * 64 + c * 32);
+          tmem_ld32(tmem + lane_base + col, ov);
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-          tmem_st32(tmem + lane_base + COL_O + c * 32, ov);
+          tmem_st32(tmem + lane_base + col, ov);
         }
         tc_fence_before();
       }
-      // probabilities in bf16 (as the tensor cores see them), summed as such
-      uint32_t pk[TOKP / 2];
+      // probabilities 2^(s * scale - m) in bf16 (one fma and one ex2 each; a
+      // masked -inf score gives 0), summed as the tensor cores see them
+      uint32_t pk[TH / 2];
+      {
+        const float mb = (m_ref == -INFINITY) ? 0.f : m_ref;  // (every score masked so far)
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < TOKP; c += 2) {
-        const __nv_bfloat16 a = __float2bfloat16_rn(exp2f(sv[c] - m_ref));
-        const __nv_bfloat16 b = __float2bfloat16_rn(exp2f(sv[c + 1] - m_ref));
-        l += __bfloat162float(a) + __bfloat162float(b);
-        pk[c / 2] = (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+        for (int c = 0; c < TH; c += 2) {
+          const __nv_bfloat162 pr =
+              __floats2bfloat162_rn(ex2_approx(fmaf(sv[c], p.qk_scale_log2, -mb)),
+                                    ex2_approx(fmaf(sv[c + 1], p.qk_scale_log2, -mb)));
+          pk[c / 2] = *reinterpret_cast<const uint32_t *>(&pr);
+          ls[(c / 2) & 3] += bf16lo(pk[c / 2]) + bf16hi(pk[c / 2]);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       }
       wait_or_abort(&p_free[slot], ((uint32_t)(st >> 1) & 1u) ^ 1u, abort_flag, p.err);
-      unsigned char *prow = smem + OFF_P + slot * ROWS * 256 + (r >> 3) * 2048 + (r & 7) * 16;
+      unsigned char *prow = smem + OFF_P + slot * ROWS * 256 + (rr >> 3) * 2048 +
+                            (sh * (TH / 8)) * 128 + (rr & 7) * 16;
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < TH / 8; ++c)
         *reinterpret_cast<uint4 *>(prow + c * 128) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       if (nb < SB || mask) {
         // V rows that are not valid tokens must not feed NaN into p.v
-        // (thread r clears token row r of the stage)
+        // (the threads of row r clear token row r of the stage, half each)
         wait_or_abort(&full_v[slot], (uint32_t)(st >> 1) & 1u, abort_flag, p.err);
-        if (r / BS >= nb || ((mask >> (r / BS)) & 1)) {
-          uint4 *vrow =
-              reinterpret_cast<uint4 *>(smem + OFF_V + slot * STAGE + (r >> 3) * 2048 + (r & 7) * 16);
+        if (rr / BS >= nb || ((mask >> (rr / BS)) & 1)) {
+          uint4 *vrow = reinterpret_cast<uint4 *>(smem + OFF_V + slot * STAGE + (rr >> 3) * 2048 +
+                                                  (rr & 7) * 16);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) vrow[c * 8] = make_uint4(0, 0, 0, 0);
+          for (int c = 0; c < 8; ++c) vrow[(sh * 8 + c) * 8] = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async();
@@ -381,27 +420,35 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[slot]);
     }
-    // ---- epilogue: this row's partial state
+    // ---- epilogue: the row's sum over both halves, then this thread's 64
+    // dims of the row's partial state
+    // [half][row] sums over the maxima of the parity the last stage did not
+    // use (every thread read those before the last stage's barrier)
+    float *lx = xmax + (nst & 1) * 2 * ROWS;
+    lx[sh * ROWS + rr] = l;
+    named_barrier_sync(1, 256);
+    const float l_row = l + lx[(sh ^ 1) * ROWS + rr];
     wait_or_abort(o_done, 0, abort_flag, p.err);
     tc_fence_after();
-    float4 *o = reinterpret_cast<float4 *>(p.pre_o + slot_row * kHeadDim);
+    float4 *o = reinterpret_cast<float4 *>(p.pre_o + slot_r * kHeadDim + sh * 64);
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       float ov[32];
-      tmem_ld32(tmem + lane_base + COL_O + c * 32, ov);  // warp-wide; stores by valid rows
-      if (row_ok) {
+      tmem_ld32(tmem + lane_base + COL_O + (uint32_t)(sh * 64 + c * 32), ov);  // warp-wide
+      if (rok) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           o[c * 8 + i] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
       }
     }
-    if (row_ok) *reinterpret_cast<float2 *>(p.pre_ml + slot_row * 2) = make_float2(m_ref, l);
+    if (rok && sh == 0)
+      *reinterpret_cast<float2 *>(p.pre_ml + slot_r * 2) = make_float2(m_ref, l_row);
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 6)
+  if (warp == WARP_MMA)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(TMEM_COLS)
                  : "memory");
