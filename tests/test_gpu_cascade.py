@@ -91,3 +91,18 @@ def test_shared_prefix32_full_size():
     want = oracle_attention(pb)
     got = cascade(pb, [(0, pb.batch, pb.shared_blocks)])
     compare(got, want, "shared_prefix32")
+
+
+@pytest.mark.parametrize("G", [1, 4])
+def test_prefix_rescale_mid_prefix(G):
+    """The shared prefix's later blocks scaled by 8 and then by 32 (exact in
+    bf16): in the prefix pass each row with a nonzero query moves its
+    reference twice after the first stage and rescales its O half, while
+    rows with a zero query (scores all 0) keep factor 1."""
+    pb = _shared_batch(10, 4 * G, 4, 16, shared_blocks=48, suffix_max=100, seed=21 + G)
+    for j in range(48):
+        f = 32.0 if j >= 32 else (8.0 if j >= 16 else 1.0)
+        blk = int(pb.block_tables[0, j])
+        pb.k_cache[blk] *= f
+    pb.q[:, ::2] = 0
+    compare(cascade(pb, [(0, 10, 48)]), oracle_attention(pb), "rescale G=%d" % G)

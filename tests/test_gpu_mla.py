@@ -93,3 +93,24 @@ def test_mla_workload_batch16_ctx8192():
     mb = inputs.make_mla_workload("mla128_batch16_ctx8192", device="cuda")
     got, want, _ = _run(mb)
     compare(got, want, "mla128 batch16 ctx8192")
+
+
+def test_mla_rescale_mid_context():
+    """The RoPE part (values 512..575, tile columns 64..71) of later blocks
+    scaled by 8 and then by 32 (exact in bf16): scores grow, the latent
+    values the output averages do not.  The running maximum of each head with
+    a nonzero query jumps by far more than 2^8 twice after the first stage, so
+    the O^T columns of those heads are rescaled mid-context while the heads
+    with a zero query (scores all 0) keep factor 1 -- with one part per
+    context and with several."""
+    lens = [640, 600, 700]
+    mb = inputs.make_mla_batch(len(lens), 128, 64, lens, device="cuda", seed=13, table_seed=14)
+    for b, n in enumerate(lens):
+        for j in range(-(-n // 64)):
+            f = 32.0 if j >= 7 else (8.0 if j >= 4 else 1.0)
+            blk = int(mb.block_tables[b, j])
+            mb.cache[blk, :, 64:72] *= f
+    mb.q[:, :16] = 0
+    for splits in (0, 1, 2):
+        got, want, _ = _run(mb, splits)
+        compare(got, want, "mla rescale splits=%d" % splits)
