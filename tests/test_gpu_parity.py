@@ -318,3 +318,22 @@ def test_bad_block_id_is_flagged_and_contained():
     for b in (0, 2):
         err = np.abs(got[b] - want[b])
         assert err.max() <= 2e-2 and err.mean() <= 2e-3
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_reference_moves_mid_context(G, num_splits):
+    """K tiles of later blocks scaled by 8 and then by 32 (exact in bf16): the
+    scores of every head with a nonzero query jump by far more than 2^8 twice
+    after the first stages, so the softmax votes, moves the references and
+    rescales O mid-unit (and inside split parts); heads with a zero query
+    (scores all 0) keep factor 1."""
+    lens = [1500, 1300, 1700]
+    pb = _batch(len(lens), 2 * G, 2, 16, lens, seed=41 + G)
+    for b, n in enumerate(lens):
+        for j in range(-(-n // 16)):
+            f = 32.0 if j >= 64 else (8.0 if j >= 32 else 1.0)
+            pb.k_cache[int(pb.block_tables[b, j])] *= f
+    pb.q[:, ::3] = 0
+    compare(gpu_attention(pb, num_splits), oracle_attention(pb),
+            "G=%d splits=%d" % (G, num_splits))

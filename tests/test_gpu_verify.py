@@ -116,3 +116,22 @@ def test_verify_full_size_batch16_ctx8192_t4():
     vb = _batch(32, 8, 16, [8192] * 16, 4)
     want, _, _ = _oracle(vb)
     compare(_gpu(vb), want, "verify batch16 ctx8192 T=4")
+
+
+@pytest.mark.parametrize("G,T", [(4, 4), (2, 8)])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_verify_reference_moves_mid_context(G, T, num_splits):
+    """16 query rows per KV head; K tiles of later blocks scaled by 8 and then
+    by 32 (exact in bf16) before the append: every row with a nonzero query
+    moves its reference twice after the first stages, rows of zero-query
+    heads keep factor 1."""
+    lens = [1500, 1300, 1700]
+    vb = _batch(4 * G, 4, 16, lens, T, seed=55 + G)
+    pb = vb.paged
+    for b, n in enumerate(lens):
+        for j in range(-(-n // 16)):
+            f = 32.0 if j >= 64 else (8.0 if j >= 32 else 1.0)
+            pb.k_cache[int(pb.block_tables[b, j])] *= f
+    vb.q[:, :, ::3] = 0
+    want, _, _ = _oracle(vb)
+    compare(_gpu(vb, num_splits), want, "verify rescale G=%d T=%d splits=%d" % (G, T, num_splits))
