@@ -545,9 +545,12 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
 }
 
 // Merge of the parts of each (sequence, head) by log-sum-exp: a warp per
-// row, lane e owning dims 4 (32 j + e) .. + 3 for j < 4 (coalesced float4s);
-// a part's four loads are issued together, ahead of their use.
+// row, lane e owning dims 4 (32 j + e) .. + 3 for j < 4 (coalesced float4s).
+// The first four parts' outputs are loaded together with the maxima, ahead
+// of the reduction that needs the maxima: one memory round trip per row for
+// up to four parts.
 __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p) {
+  constexpr int KP = 4;  // parts whose outputs are loaded up front
   pdl_wait();
   const int row = (int)blockIdx.x * 4 + (threadIdx.x >> 5);  // b * H + h
   const int lane = threadIdx.x & 31;
@@ -556,6 +559,13 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p) {
   if (c < 1 || c > p.MB * p.bs) return;  // rejected (flagged by the attention kernel)
   const float2 *ml = reinterpret_cast<const float2 *>(p.part_ml) + (size_t)row * p.n_parts;
   const float4 *po = reinterpret_cast<const float4 *>(p.part_o) + (size_t)row * p.n_parts * (DV / 4);
+  float4 x0[KP][4];
+#pragma unroll
+  for (int k = 0; k < KP; ++k)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      x0[k][j] = (k < p.n_parts) ? __ldcg(po + (size_t)k * (DV / 4) + j * 32 + lane)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = -INFINITY;
   for (int k = lane; k < p.n_parts; k += 32) M = fmaxf(M, __ldcg(&ml[k].x));
 #pragma unroll
@@ -564,13 +574,8 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p) {
   float4 acc[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int k = 0; k < p.n_parts; ++k) {
-    const float2 v = __ldcg(&ml[k]);
-    float4 x[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] = __ldcg(po + (size_t)k * (DV / 4) + j * 32 + lane);
-    if (v.x == -INFINITY) continue;  // an empty part
+  auto fold = [&](const float2 v, const float4 (&x)[4]) {
+    if (v.x == -INFINITY) return;  // an empty part
     const float w = exp2f(v.x - M);
     L = fmaf(w, v.y, L);
 #pragma unroll
@@ -580,6 +585,16 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p) {
       acc[j].z = fmaf(w, x[j].z, acc[j].z);
       acc[j].w = fmaf(w, x[j].w, acc[j].w);
     }
+  };
+#pragma unroll
+  for (int k = 0; k < KP; ++k)
+    if (k < p.n_parts) fold(__ldcg(&ml[k]), x0[k]);
+#pragma unroll 2
+  for (int k = KP; k < p.n_parts; ++k) {
+    float4 x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) x[j] = __ldcg(po + (size_t)k * (DV / 4) + j * 32 + lane);
+    fold(__ldcg(&ml[k]), x);
   }
   const float inv = 1.f / L;
   uint2 *o = reinterpret_cast<uint2 *>(p.out + (size_t)row * DV);
