@@ -114,12 +114,16 @@ constexpr int NSB = 4;                      // S buffers (q.k^T may run 4 stages
 constexpr uint32_t TMEM_COLS = 128;
 constexpr float kRescaleLog2 = 8.f;         // move the reference when exceeded by 2^8
 // Split choice.  One CTA streams at most about 1/kCtaShare of the HBM rate
-// (its three 64 KiB K+V stages in flight over the load latency); a unit's
-// partial state costs the CTA that merges it about kMergeBytes of streaming
-// time (a store, a fence, an atomic and the reloads of the parts, in series).
+// (its three 64 KiB K+V stages in flight over the load latency); merging a
+// unit's partial states costs the CTA that merges them about
+// kMergeFixedBytes of streaming time plus kMergePartBytes per part (a store,
+// a fence and an atomic per part, then the reloads, in series).
 // (per kind of cache: three 64 KiB bf16 stages, or four 33 KiB 8-bit ones)
 template <bool FP8> constexpr long long kCtaShare = FP8 ? 140 : 96;
-constexpr long long kMergeBytes = 32ll << 20;
+// (measured on 8 units of 32 blocks: one part per unit 12.8 us a step, two
+// 16.5, nineteen 19.0)
+constexpr long long kMergeFixedBytes = 24ll << 20;
+constexpr long long kMergePartBytes = 1ll << 20;
 // Fixed cost of a segment in blocks of streaming time: about two stages
 // (measured on a batch of short sequences).
 template <int BS> constexpr int kSegCost = 2 * TOK / BS;
@@ -835,16 +839,25 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   sc.ov = kSegCost<BS>;
   sc.P = sc.X < (long long)gridDim.x ? sc.X : (long long)gridDim.x;
   sc.units = false;
-  if (p.auto_split) {
-    // Whole units when they fit in the grid and the longest one streams no
-    // longer than the job at the HBM rate plus the merges the balanced cut
-    // would need; the cost of either is in blocks of HBM streaming time.
+  if (p.auto_split && sc.X > 0) {
+    // The job's time in blocks of HBM streaming time: for P balanced cuts,
+    // the longest part at one CTA's share of HBM (or the whole job at the
+    // HBM rate), then the merge of a unit's parts -- a fixed cost and one per
+    // part, so a small job takes fewer, longer parts: X share / P + m1 P / U
+    // is least near P = sqrt(share X U / m1), within the grid.  Whole units
+    // (the longest at one CTA's share) when they fit in the grid and cost no
+    // more.
     const long long U = (long long)p.B * p.n_kv, nmax = *nmax_slot;
-    if (U <= (long long)gridDim.x && sc.X > 0) {
-      const long long per_cta = (sc.X + gridDim.x - 1) / gridDim.x;
-      constexpr long long kBlockBytes = 2ll * (BS / 8) * L::GROUP;  // K and V of one block
+    constexpr long long kBlockBytes = 2ll * (BS / 8) * L::GROUP;  // K and V of one block
+    constexpr long long m0 = kMergeFixedBytes / kBlockBytes, m1 = kMergePartBytes / kBlockBytes;
+    const long long grid = (long long)gridDim.x;
+    long long P = (long long)sqrtf((float)kCtaShare<FP8> * (float)sc.X * (float)U / (float)m1);
+    P = max(1ll, min(P, sc.P));
+    const long long cost_cut =
+        max((sc.X + P - 1) / P * kCtaShare<FP8>, sc.X) + m0 + m1 * ((P + U - 1) / U);
+    sc.P = P;
+    if (U <= grid) {
       const long long cost_units = max(nmax * kCtaShare<FP8>, sc.X);
-      const long long cost_cut = max(per_cta * kCtaShare<FP8>, sc.X) + kMergeBytes / kBlockBytes;
       if (cost_units <= cost_cut) {
         sc.units = true;
         sc.P = U;
