@@ -395,12 +395,17 @@ pgd_status pgd_append_decode_attention_fp8(void *out, const void *q, const void 
 /* one decode step with host inputs and outputs                            */
 /* ---------------------------------------------------------------------- */
 /* One decode step of one layer for a caller whose per-step tensors live in
- * host memory: copies q_h, k_new_h, v_new_h and context_lens_h to the
- * caller's device staging buffers, runs pgd_append_decode_attention on them
- * (append at position context_lens[b] - 1, then attention), and copies the
- * result back to out_h -- all enqueued on `stream`.  For
- * asynchronous copies the host buffers should be pinned.  The cache, block
- * tables and workspace stay on the device.  Shapes and rules as above. */
+ * host memory: pgd_append_decode_attention (append at position
+ * context_lens[b] - 1, then attention) on q_h, k_new_h, v_new_h and
+ * context_lens_h, with the result in out_h -- all enqueued on `stream`.
+ * q_h, k_new_h, v_new_h and out_h, when page-locked host memory that the
+ * device addresses (as the CUDA runtime reports it) and 16-byte aligned, are
+ * read and written in place by the kernels over the host link; otherwise
+ * they go through the caller's device buffers (q_d, k_new_d, v_new_d, out_d)
+ * and a copy each.  context_lens_h is always copied to context_lens_d.  The
+ * host buffers must stay untouched until the stream has completed the step.
+ * The cache, block tables and workspace stay on the device.  Shapes and rules
+ * as above. */
 pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
                            const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
                            void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
@@ -409,8 +414,8 @@ pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, co
                            int32_t num_splits, void *workspace, size_t workspace_bytes,
                            void *stream);
 
-/* pgd_decode_step for an 8-bit pool: the same host-to-device copies, then
- * pgd_append_decode_attention_fp8, then the copy of the output back. */
+/* pgd_decode_step for an 8-bit pool: the same handling of the host buffers
+ * around pgd_append_decode_attention_fp8. */
 pgd_status pgd_decode_step_fp8(void *out_h, const void *q_h, const void *k_new_h,
                                const void *v_new_h, const int32_t *context_lens_h, void *out_d,
                                void *q_d, void *k_new_d, void *v_new_d, int32_t *context_lens_d,

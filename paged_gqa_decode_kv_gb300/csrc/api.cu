@@ -820,6 +820,19 @@ pgd_status pgd_append_decode_attention_fp8(void *out, const void *q, const void 
   return s == PGD_OK ? ok() : s;
 }
 
+// The device's address of a page-locked host buffer that it can reach (and
+// that is 16-byte aligned, as the kernels' vector accesses need), else null.
+static void *device_alias(const void *h) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer || !aligned(a.devicePointer, 16))
+    return nullptr;
+  return a.devicePointer;
+}
+
 static pgd_status decode_step_impl(bool fp8, void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
                            const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
                            void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
@@ -845,18 +858,29 @@ static pgd_status decode_step_impl(bool fp8, void *out_h, const void *q_h, const
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t qb = (size_t)B * n_q * kHeadDim * 2, kvb = (size_t)B * n_kv * kHeadDim * 2;
-  cudaError_t e;
-  if ((e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(k_new_d, k_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(v_new_d, v_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+  // Page-locked host buffers that the device addresses (16-byte aligned)
+  // are read -- q, k_new, v_new -- and written -- out -- in place by the
+  // kernels over the host link, instead of through a copy each; any other
+  // buffer goes through its device buffer and a copy.  The context lengths,
+  // which every CTA reads in its prologue, are always copied.
+  const void *q_in = device_alias(q_h), *kn_in = device_alias(k_new_h),
+             *vn_in = device_alias(v_new_h);
+  void *out_to = device_alias(out_h);
+  cudaError_t e = cudaSuccess;
+  if ((!q_in && (e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
+      (!kn_in &&
+       (e = cudaMemcpyAsync(k_new_d, k_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
+      (!vn_in &&
+       (e = cudaMemcpyAsync(v_new_d, v_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
       (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4, cudaMemcpyHostToDevice,
                            st)) != cudaSuccess)
     return cuda_fail(e, "decode step: host-to-device copy");
-  s = append_then_attend(out_d, q_d, k_new_d, v_new_d, k_cache, v_cache, block_tables,
-                         context_lens_d, B, n_q, n_kv, bs, MB, NB, scale, num_splits, workspace,
-                         workspace_bytes, st, fp8);
+  s = append_then_attend(out_to ? out_to : out_d, q_in ? q_in : q_d, kn_in ? kn_in : k_new_d,
+                         vn_in ? vn_in : v_new_d, k_cache, v_cache, block_tables, context_lens_d,
+                         B, n_q, n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes,
+                         st, fp8);
   if (s != PGD_OK) return s;
-  if ((e = cudaMemcpyAsync(out_h, out_d, qb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+  if (!out_to && (e = cudaMemcpyAsync(out_h, out_d, qb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
     return cuda_fail(e, "decode step: device-to-host copy");
   return ok();
 }

@@ -267,14 +267,19 @@ def test_copy_blocks_bit_exact():
     assert torch.equal(pb.v_cache.view(torch.int16), v0v)
 
 
-def test_decode_step_host_buffers_match_device_path():
+@pytest.mark.parametrize("pinned", [True, False])
+def test_decode_step_host_buffers_match_device_path(pinned):
+    """Page-locked host buffers are read and written in place by the kernels,
+    pageable ones go through the device buffers and copies: both equal the
+    device path bit for bit."""
     B, n_q, n_kv, bs = 4, 32, 8, 16
     pb = _batch(B, n_q, n_kv, bs, [700, 16, 17, 1], append=True)
     ws = pgd.make_workspace(B, n_q, n_kv)
-    q_h = pb.q.cpu().pin_memory()
-    kn_h, vn_h = pb.k_new.cpu().pin_memory(), pb.v_new.cpu().pin_memory()
-    cl_h = pb.context_lens.cpu().pin_memory()
-    out_h = torch.empty_like(q_h).pin_memory()
+    host = (lambda t: t.cpu().pin_memory()) if pinned else (lambda t: t.cpu().clone())
+    q_h = host(pb.q)
+    kn_h, vn_h = host(pb.k_new), host(pb.v_new)
+    cl_h = host(pb.context_lens)
+    out_h = host(torch.zeros_like(pb.q))
     q_d, kn_d, vn_d = torch.empty_like(pb.q), torch.empty_like(pb.k_new), torch.empty_like(pb.v_new)
     cl_d = torch.empty_like(pb.context_lens)
     out_d = torch.empty_like(pb.q)
