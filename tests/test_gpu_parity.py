@@ -267,19 +267,22 @@ def test_copy_blocks_bit_exact():
     assert torch.equal(pb.v_cache.view(torch.int16), v0v)
 
 
-@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
 def test_decode_step_host_buffers_match_device_path(pinned):
     """Page-locked host buffers are read and written in place by the kernels,
-    pageable ones go through the device buffers and copies: both equal the
-    device path bit for bit."""
+    pageable ones go through the device buffers and copies (each buffer on its
+    own): every mix equals the device path bit for bit."""
     B, n_q, n_kv, bs = 4, 32, 8, 16
     pb = _batch(B, n_q, n_kv, bs, [700, 16, 17, 1], append=True)
     ws = pgd.make_workspace(B, n_q, n_kv)
-    host = (lambda t: t.cpu().pin_memory()) if pinned else (lambda t: t.cpu().clone())
-    q_h = host(pb.q)
-    kn_h, vn_h = host(pb.k_new), host(pb.v_new)
-    cl_h = host(pb.context_lens)
-    out_h = host(torch.zeros_like(pb.q))
+    pin = lambda t: t.cpu().pin_memory()
+    page = lambda t: t.cpu().clone()
+    hq, hk, hv, ho = {"all": (pin,) * 4, "none": (page,) * 4,
+                      "mixed": (pin, page, pin, page)}[pinned]
+    q_h = hq(pb.q)
+    kn_h, vn_h = hk(pb.k_new), hv(pb.v_new)
+    cl_h = pin(pb.context_lens)
+    out_h = ho(torch.zeros_like(pb.q))
     q_d, kn_d, vn_d = torch.empty_like(pb.q), torch.empty_like(pb.k_new), torch.empty_like(pb.v_new)
     cl_d = torch.empty_like(pb.context_lens)
     out_d = torch.empty_like(pb.q)
