@@ -147,3 +147,23 @@ def test_workload_full_size_fp8(name):
         pgd.kv_append_fp8(pb.k_new, pb.v_new, pb.k_cache, pb.v_cache, pb.block_tables,
                           pb.positions)
     compare(gpu_fp8(pb), oracle_fp8(pb, k, v), name + " fp8")
+
+
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_fp8_reference_moves_mid_context(G, num_splits):
+    """The per-token K scales (fp32, beside the codes) of later blocks
+    multiplied by 4 and then by 8 -- exact, and read alike by the kernel and
+    the oracle: every head with a nonzero query moves its reference (when its
+    maximum grows past 2^8) after the first stages and rescales O; zero-query
+    heads keep factor 1.  (The factors stay moderate: the kernel keeps about
+    8 bits of the query, so a score's error grows with its size.)"""
+    lens = [1500, 1300, 1700]
+    pb = _batch(len(lens), 2 * G, 2, 16, lens, seed=61 + G)
+    for b, n in enumerate(lens):
+        for j in range(-(-n // 16)):
+            f = 8.0 if j >= 64 else (4.0 if j >= 32 else 1.0)
+            if f != 1.0:
+                pb.k_cache[int(pb.block_tables[b, j]), :, :, 1024:].view(torch.float32).mul_(f)
+    pb.q[:, ::3] = 0
+    compare(gpu_fp8(pb, num_splits), oracle_fp8(pb), "fp8 rescale G=%d splits=%d" % (G, num_splits))
