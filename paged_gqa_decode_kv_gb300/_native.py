@@ -240,9 +240,11 @@ def append_decode_attention(out, q, k_new, v_new, k_cache, v_cache, block_tables
 def decode_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d, v_new_d,
                 context_lens_d, k_cache, v_cache, block_tables, scale: float, num_splits: int,
                 workspace: torch.Tensor, stream=None) -> None:
-    """One decode step with host (pinned) inputs/outputs: H2D copies, append at
-    context_lens - 1, attention, D2H copy of the output; all on `stream`.  An
-    8-bit pool (uint8) selects the FP8 path."""
+    """One decode step with host inputs/outputs: append at context_lens - 1,
+    then attention, all on `stream`.  Page-locked (pinned) host tensors are
+    read and written in place by the kernels; pageable ones go through the
+    given device tensors and a copy each.  An 8-bit pool (uint8) selects the
+    FP8 path."""
     for t, n in ((out_h, "out_h"), (q_h, "q_h"), (k_new_h, "k_new_h"), (v_new_h, "v_new_h")):
         _need(t, torch.bfloat16, n, cuda=False)
     _need(context_lens_h, torch.int32, "context_lens_h", cuda=False)
