@@ -367,8 +367,10 @@ pgd_status pgd_kv_append_fp8(const void *k_new, const void *v_new, void *k_cache
 /* pgd_paged_decode_attention over an 8-bit pool: the same definition applied
  * to the dequantised K and V, the same arguments (k_cache, v_cache as
  * above), checks, errors and workspace (pgd_attention_workspace_size).
- * Arithmetic: q.k^T on the tensor cores in E4M3 with the query split into a
- * high and a low E4M3 part (about 8 bits of the bf16 query), the key and
+ * Arithmetic: q.k^T on the tensor cores in E4M3 with each query head split
+ * into a high and a low E4M3 part after scaling by a power of two -- the
+ * bf16 query itself, except that elements more than 2^9 below the head's
+ * largest keep an absolute error under 2^-17 of that largest -- the key and
  * query scales applied in fp32; V dequantised to f16 (code times the scale
  * rounded to f16) and probabilities in f16 for the p.v; fp32 softmax and
  * accumulation; bf16 output.  The query must be finite and the dequantised
@@ -436,6 +438,27 @@ pgd_status pgd_decode_step_fp8(void *out_h, const void *q_h, const void *k_new_h
 pgd_status pgd_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_ids,
                            const int32_t *dst_ids, int32_t n, int32_t n_kv, int32_t d,
                            int32_t bs, int32_t NB, void *stream);
+
+/* ---------------------------------------------------------------------- */
+/* measurement: read-only streaming bandwidth                              */
+/* ---------------------------------------------------------------------- */
+/* One pass that reads every byte of src[0 .. bytes) once from device memory
+ * and discards it: the bandwidth a kernel that only reads can reach on this
+ * GPU, to be timed in the same job as the attention kernels so that their
+ * fractions of the HBM roofline have a denominator of their own kind beside
+ * a copy's ("LLM inference systems engineering", 3.8.2: keep peak and
+ * sustained bandwidth apart and calibrate on the access pattern measured).
+ *   mode 0  16-byte vector loads by a grid of four 512-thread CTAs per SM;
+ *           bytes a multiple of 16.
+ *   mode 1  the attention kernels' pattern: one CTA per SM streams its share
+ *           as 4 KiB bulk copies (TMA engine) into a three-stage ring of
+ *           64 KiB shared-memory stages; bytes a multiple of 4096.
+ * src is a device pointer, 16-byte aligned, owned by the caller and left
+ * unchanged.  Returns PGD_ERR_INVALID_ARG for another mode, a null or
+ * misaligned src or a size that is not a multiple of the mode's unit (0 bytes
+ * is a no-op); a wait that gives up sets PGD_DEVERR_TIMEOUT.  Only enqueues
+ * on `stream`.  Not part of the attention path. */
+pgd_status pgd_read_stream(const void *src, size_t bytes, int32_t mode, void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* device error word                                                      */

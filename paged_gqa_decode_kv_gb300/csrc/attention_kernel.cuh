@@ -77,11 +77,14 @@
 // codes and scales, and the groups sit 1056 B apart -- a uniform stride the
 // MMA descriptors can step over.  q.k^T runs on the tensor cores in E4M3
 // (kind::f8f6f4): each query head h is split into a high and a low E4M3 part
-// (q / s_q = hi + lo, s_q = max |q| / 448), hi in column h and lo in column
-// 8 + h of the same N = 16 MMA, so the score keeps about 8 bits of the
-// query at no extra MMA; the softmax adds the two columns and applies s_q
-// and the key's scale.  Four more warps dequantise V to f16 (code * scale,
-// each thread its own token row) for an f16 p.v with f16 probabilities.
+// (q / s_q = hi + lo, s_q a power of two that puts max |q| in [128, 256)),
+// hi in column h and lo in column 8 + h of the same N = 16 MMA.  A bf16
+// element has 8 significant bits, hi takes 4 and lo the other 4, so the
+// split is the bf16 query itself (up to 2^-10 s_q for elements more than
+// 2^9 below the head's largest) at no extra MMA; the softmax adds the two
+// columns and applies s_q and the key's scale.  Four more warps dequantise V
+// to f16 (code * scale, each thread its own token row) for an f16 p.v with
+// f16 probabilities.
 //
 // Softmax keeps one reference maximum per head.  A stage moves the reference
 // (and rescales O in tensor memory, after the previous p.v has completed)
@@ -459,7 +462,11 @@ __device__ __forceinline__ void e4m3x16_dequant_f16(const uint4 &c, __half2 scal
 }
 
 // One query head's 8 dims (one 16-byte piece of q) as E4M3 high and low
-// parts of q / s_q: hi = E4M3(x), lo = E4M3(x - hi).
+// parts of x = q / s_q: hi = E4M3(x), lo = E4M3(x - hi).  With s_q a power
+// of two, x has a bf16 element's 8 significant bits; hi holds the top 4 and
+// x - hi the rest (at most 4 bits), so hi + lo = x exactly whenever lo is
+// not below E4M3's subnormal step 2^-9 -- for every element within a factor
+// 2^9 of the head's largest -- and within 2^-10 of x otherwise.
 __device__ __forceinline__ void q_hi_lo(const uint4 &piece, float inv_sq, uint2 &hi, uint2 &lo) {
   float f[8];
   unpack8(piece, f);
@@ -547,10 +554,16 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
           for (int e = 0; e < 8; ++e) a = fmaxf(a, fabsf(f[e]));
 #pragma unroll
           for (int o = 8; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(kFullMask, a, o));
-          const float sq = a > 0.f ? a * (1.f / 448.f) : 1.f;
+          // s_q = 2^(e - 7), e = the exponent of max |q| (at least -119, so
+          // that both s_q and 1 / s_q are normal binary32): q / s_q is q with
+          // its exponent shifted, every element keeps its 8 significant bits,
+          // and the largest lands in [128, 256), inside E4M3's range.
+          const int e = max((int)((__float_as_uint(a) >> 23) & 0xffu) - 127, -119);
+          const float sq = __uint_as_float((uint32_t)(e + 120) << 23);
+          const float inv_sq = __uint_as_float((uint32_t)(134 - e) << 23);
           if (j < 16 * G) {
             uint2 hi, lo;
-            q_hi_lo(cur_a.q[i], 1.f / sq, hi, lo);
+            q_hi_lo(cur_a.q[i], inv_sq, hi, lo);
             // row n, dims 8c..8c+7: core matrix (n / 8, c / 2), row n % 8
             const int off = (c >> 1) * 128 + (c & 1) * 8;
             *reinterpret_cast<uint2 *>(qdst + r * 16 + off) = hi;

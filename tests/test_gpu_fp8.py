@@ -150,20 +150,37 @@ def test_workload_full_size_fp8(name):
 
 
 @pytest.mark.parametrize("G", [1, 4, 8])
-@pytest.mark.parametrize("num_splits", [0, 3])
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
 def test_fp8_reference_moves_mid_context(G, num_splits):
     """The per-token K scales (fp32, beside the codes) of later blocks
-    multiplied by 4 and then by 8 -- exact, and read alike by the kernel and
-    the oracle: every head with a nonzero query moves its reference (when its
-    maximum grows past 2^8) after the first stages and rescales O; zero-query
-    heads keep factor 1.  (The factors stay moderate: the kernel keeps about
-    8 bits of the query, so a score's error grows with its size.)"""
+    multiplied by 8 and then by 32 -- exact, and read alike by the kernel and
+    the oracle, as in the bf16 suite: scores reach about 190 in log2 units,
+    every head with a nonzero query moves its reference (when its maximum
+    grows past 2^8) after the first stages and rescales O; zero-query heads
+    keep factor 1.  The kernel's query split is exact for bf16 elements
+    within 2^9 of their head's largest, so the score error does not grow
+    with the score beyond fp32 accumulation."""
     lens = [1500, 1300, 1700]
     pb = _batch(len(lens), 2 * G, 2, 16, lens, seed=61 + G)
     for b, n in enumerate(lens):
         for j in range(-(-n // 16)):
-            f = 8.0 if j >= 64 else (4.0 if j >= 32 else 1.0)
+            f = 32.0 if j >= 64 else (8.0 if j >= 32 else 1.0)
             if f != 1.0:
                 pb.k_cache[int(pb.block_tables[b, j]), :, :, 1024:].view(torch.float32).mul_(f)
     pb.q[:, ::3] = 0
     compare(gpu_fp8(pb, num_splits), oracle_fp8(pb), "fp8 rescale G=%d splits=%d" % (G, num_splits))
+
+
+@pytest.mark.parametrize("G", [1, 8])
+def test_fp8_query_dynamic_range(G):
+    """Queries whose elements span many binades (a few of 2^12, most near 1,
+    some near 2^-12) and a head of only tiny values (2^-100): the scores stay
+    within tolerance of the oracle, which takes the bf16 query exactly."""
+    lens = [700, 300]
+    pb = _batch(len(lens), 2 * G, 2, 32, lens, seed=90 + G)
+    g = torch.Generator().manual_seed(5)
+    mag = torch.randint(-12, 13, pb.q.shape, generator=g).float()
+    q = (torch.randn(pb.q.shape, generator=g) * torch.exp2(mag) / 64.0)
+    q[:, 0] = torch.randn(q[:, 0].shape, generator=g) * 2.0 ** -100
+    pb.q.copy_(q.to(torch.bfloat16))
+    compare(gpu_fp8(pb), oracle_fp8(pb), "fp8 query range G=%d" % G)
