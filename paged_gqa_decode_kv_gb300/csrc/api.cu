@@ -41,6 +41,8 @@ cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache
 cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src_ids,
                                const int32_t *dst_ids, int n, int n_kv, int bs, int NB,
                                int32_t *err, cudaStream_t stream);
+cudaError_t read_stream_launch(const void *src, size_t bytes, int mode, int32_t *err,
+                               cudaStream_t stream);
 void set_error_detail(const char *msg);
 void clear_error_detail();
 const char *error_detail();
@@ -373,6 +375,17 @@ pgd_status paged_attention_with_scratch(void *out, const void *q, const void *k_
   if (s != PGD_OK || B == 0) return s;
   return launch_attention(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, bs, MB, NB, scale,
                           num_splits, scratch, scratch_bytes, stream);
+}
+
+// The argument checks of pgd_paged_decode_attention alone (nothing is
+// enqueued), for entry points that must reject a call before they touch
+// any device memory.
+pgd_status attention_args_status(const void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *tables, const int32_t *ctx,
+                                 int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                 int32_t MB, int32_t NB, float scale, int32_t num_splits) {
+  return check_attention_args(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, d, bs, MB, NB,
+                              scale, num_splits);
 }
 
 pgd_status set_status_detail(pgd_status s, const char *msg) {
@@ -925,6 +938,21 @@ pgd_status pgd_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_ids,
   cudaError_t e = copy_blocks_launch(k_cache, v_cache, src_ids, dst_ids, n, n_kv, bs, NB, err,
                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  return ok();
+}
+
+pgd_status pgd_read_stream(const void *src, size_t bytes, int32_t mode, void *stream) {
+  if (mode != 0 && mode != 1) return fail(PGD_ERR_INVALID_ARG, "mode %d (0 or 1)", mode);
+  if (bytes == 0) return ok();
+  if (!src) return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(src, 16)) return fail(PGD_ERR_INVALID_ARG, "src must be 16-byte aligned");
+  const size_t unit = mode == 1 ? 4096 : 16;
+  if (bytes % unit) return fail(PGD_ERR_INVALID_ARG, "bytes must be a multiple of %zu", unit);
+  int32_t *err = nullptr;
+  pgd_status s = error_word(&err);
+  if (s != PGD_OK) return s;
+  cudaError_t e = read_stream_launch(src, bytes, mode, err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "read stream launch");
   return ok();
 }
 

@@ -32,6 +32,10 @@ pgd_status paged_attention_with_scratch(void *out, const void *q, const void *k_
                                         int32_t d, int32_t bs, int32_t MB, int32_t NB,
                                         float scale, int32_t num_splits, void *scratch,
                                         size_t scratch_bytes, cudaStream_t stream);
+pgd_status attention_args_status(const void *out, const void *q, const void *k_cache,
+                                 const void *v_cache, const int32_t *tables, const int32_t *ctx,
+                                 int32_t B, int32_t n_q, int32_t n_kv, int32_t d, int32_t bs,
+                                 int32_t MB, int32_t NB, float scale, int32_t num_splits);
 pgd_status set_status_detail(pgd_status s, const char *msg);
 }  // namespace pgd
 
@@ -71,18 +75,19 @@ extern "C" pgd_status pgd_paged_decode_attention_noalloc(
     const int32_t *block_tables, const int32_t *context_lens, int32_t B, int32_t n_q,
     int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB, float scale,
     int32_t num_splits, void *stream) {
-  if (B <= 0 || n_kv <= 0 || n_q <= 0 || n_q % n_kv || num_splits < 0)
-    return pgd::paged_attention_with_scratch(out, q, k_cache, v_cache, block_tables,
-                                             context_lens, B, n_q, n_kv, d, bs, MB, NB, scale,
-                                             num_splits, nullptr, 0,
-                                             static_cast<cudaStream_t>(stream));
+  // The same checks, in the same order, as pgd_paged_decode_attention: a call
+  // it would refuse is refused here with the same status before the scratch
+  // is looked up, cleared or sized.
+  pgd_status s = pgd::attention_args_status(out, q, k_cache, v_cache, block_tables, context_lens,
+                                            B, n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK || B == 0) return s;
   const size_t need = pgd_attention_workspace_size(B, n_q, n_kv, d, num_splits);
   if (need == 0 || need > (size_t)PGD_NOALLOC_SCRATCH_BYTES)
     return pgd::set_status_detail(
         PGD_ERR_WORKSPACE,
         "these sizes need more scratch than the fixed PGD_NOALLOC_SCRATCH_BYTES array holds");
   void *scratch = nullptr;
-  pgd_status s = scratch_address(&scratch);
+  s = scratch_address(&scratch);
   if (s != PGD_OK) return s;
   // The arrival counters (first B * n_kv int32 of the scratch) must start at
   // zero; clear them on the caller's stream.

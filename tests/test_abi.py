@@ -83,6 +83,37 @@ def test_attention_rejects_on_host(L, kw, status):
     assert L.pgd_last_error_detail()
 
 
+def _attn_noalloc(L, **kw):
+    a = dict(out=16, q=16, k=16, v=16, t=16, c=16, B=2, n_q=8, n_kv=2, d=128, bs=16, MB=4, NB=8,
+             scale=0.1, splits=0)
+    a.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.pgd_paged_decode_attention_noalloc(P(a["out"]), P(a["q"]), P(a["k"]), P(a["v"]),
+                                                P(a["t"]), P(a["c"]), a["B"], a["n_q"], a["n_kv"],
+                                                a["d"], a["bs"], a["MB"], a["NB"], a["scale"],
+                                                a["splits"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(d=64), dict(bs=8), dict(n_q=6, n_kv=2), dict(n_q=32, n_kv=2), dict(n_q=7, n_kv=2),
+    dict(B=-1), dict(B=5000), dict(scale=0.0), dict(scale=float("inf")), dict(q=None),
+    dict(q=24), dict(out=None), dict(t=18), dict(NB=0), dict(splits=-1),
+], ids=lambda kw: "-".join("%s=%s" % i for i in kw.items()))
+def test_noalloc_rejects_like_the_regular_entry_point(L, kw):
+    """Every argument set the workspace entry point refuses on the host is
+    refused by the allocation-free one with the same status, before it looks
+    up, clears or sizes its scratch (no CUDA call is made here: there is no
+    GPU)."""
+    want = _attn(L, ws=256, wsb=1 << 30, **kw)
+    assert want != 0
+    assert _attn_noalloc(L, **kw) == want
+    assert L.pgd_last_error_detail()
+
+
+def test_noalloc_empty_batch_is_a_noop(L):
+    assert _attn_noalloc(L, B=0, out=None, q=None, k=None, v=None, t=None, c=None) == 0
+
+
 def test_empty_batch_is_a_noop(L):
     assert _attn(L, B=0, out=None, q=None, k=None, v=None, t=None, c=None) == 0
 
@@ -106,3 +137,13 @@ def test_workspace_size_grows_with_splits(L):
     b = pgd.workspace_size(16, 32, 8, 64)
     assert 0 < a < b
     assert pgd.workspace_size(16, 32, 8, 0, d=64) == 0
+
+
+def test_read_stream_rejects_on_host(L):
+    P = ctypes.c_void_p
+    assert L.pgd_read_stream(P(16), 4096, 2, None) == _native.ERR_INVALID_ARG   # mode
+    assert L.pgd_read_stream(None, 4096, 0, None) == _native.ERR_INVALID_ARG
+    assert L.pgd_read_stream(P(24), 4096, 0, None) == _native.ERR_INVALID_ARG   # misaligned
+    assert L.pgd_read_stream(P(16), 40, 0, None) == _native.ERR_INVALID_ARG     # not 16 B units
+    assert L.pgd_read_stream(P(16), 8192 + 16, 1, None) == _native.ERR_INVALID_ARG  # not 4 KiB
+    assert L.pgd_read_stream(None, 0, 1, None) == 0                              # no-op
