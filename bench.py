@@ -179,6 +179,76 @@ class ClockSampler:
                 "samples": len(win), "window": window}
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons read in-process through NVML (read-only
+    queries over ctypes) about every half millisecond in a background thread,
+    so that a timed region of a few milliseconds still holds samples.
+    Unavailable NVML leaves it empty (the nvidia-smi sampler stays)."""
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+            0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, gpu_uuid: str):
+        import ctypes
+        self.samples = []
+        self.ok = False
+        self._stop = threading.Event()
+        self.thread = None
+        try:
+            L = ctypes.CDLL("libnvidia-ml.so.1")
+            if L.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if L.nvmlDeviceGetHandleByUUID(gpu_uuid.encode(), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint(0)
+            L.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self.max_mhz = float(mx.value)
+            self.reasons_fn = getattr(L, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                L.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.L, self.h, self.ctypes = L, h, ctypes
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _run(self):
+        c, L, h = self.ctypes, self.L, self.h
+        mhz, bits = c.c_uint(0), c.c_ulonglong(0)
+        while not self._stop.is_set():
+            if L.nvmlDeviceGetClockInfo(h, 1, c.byref(mhz)) == 0 and \
+                    self.reasons_fn(h, c.byref(bits)) == 0:
+                self.samples.append((time.time(), float(mhz.value), int(bits.value)))
+            time.sleep(0.0005)
+
+    def start(self):
+        if self.ok:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not win:
+            return None
+        reasons = sorted({n for s in win for b, n in self.BITS.items() if s[2] & b})
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(win), "window": "timed steps",
+                "source": "NVML in-process, ~0.5 ms period"}
+
+
+def clocks_record(smi, nvml, t_wall0, t_wall1, t_timed0, t_timed1):
+    """The clock record of a run: NVML samples inside the timed steps when
+    there are any, else the nvidia-smi samples; both kept."""
+    smi_sum = smi.summary(t_wall0, t_wall1)
+    nv = nvml.summary(t_timed0, t_timed1) if nvml is not None else None
+    if nv is None:
+        return smi_sum
+    return dict(nv, nvidia_smi=smi_sum)
+
+
 # ------------------------------------------------------------------- peaks
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -282,13 +352,113 @@ def cpu_baseline(pb_host, seconds: float):
         total_t += dt
         total_b += nb
         calls += 1
+    one = one_thread_baseline(pb_host, min(5.0, seconds / 2))
     return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": cores,
-            "kind": "oracle",
+            "kind": "oracle", "one_thread": one,
             "sample": "float64 oracle %s over the full batch (all %d sequences, %d query "
                       "heads), %d call(s), %.1f s; kv_append excluded (a %d-byte copy)"
                       % ("verify attention (%d query tokens per sequence)" % pb_host["T"]
                          if pb_host.get("T", 0) else "attention", B, pb_host["n_q"], calls,
                          total_t, 2 * B * max(1, pb_host.get("T", 0)) * pb_host["n_kv"] * 256)}
+
+
+def one_thread_baseline(pb_host, seconds: float):
+    """The oracle on one host thread over the first sequence, repeated for
+    about `seconds`."""
+    total_t, total_b, calls = 0.0, 0, 0
+    while total_t < seconds and calls < 100:
+        dt, nb = oracle_sample(pb_host, 1, n_threads=1)
+        total_t += dt
+        total_b += nb
+        calls += 1
+    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "sample": "float64 oracle over the first sequence (all %d query heads), one "
+                      "thread, %d call(s), %.1f s" % (pb_host["n_q"], calls, total_t)}
+
+
+# ------------------------------------------------- read-only streaming peak
+READ_ONLY_BYTES = 2 << 30     # 2 GiB, > 15 x L2
+
+
+def read_only_peak(dev, stream, passes: int = 10):
+    """GB/s of the library's read-only streaming pass (pgd_read_stream) over a
+    2 GiB buffer, both access patterns (16-byte loads; 4 KiB bulk copies into
+    shared memory, the attention kernels' pattern), each the best and the mean
+    of `passes` CUDA-event-timed passes.  Returns (best of both, record)."""
+    import torch
+    import paged_gqa_decode_kv_gb300 as pgd
+    buf = torch.ones(READ_ONLY_BYTES // 4, dtype=torch.int32, device=dev)
+    rec = {}
+    for mode, name in ((0, "loads16"), (1, "bulk4k")):
+        for _ in range(3):
+            pgd.read_stream(buf, mode, stream=stream)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(passes)]
+        for a, b in evs:
+            a.record(stream)
+            pgd.read_stream(buf, mode, stream=stream)
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in evs]
+        rec[name] = {"gbs_best": round(READ_ONLY_BYTES / (min(ms) / 1e3) / 1e9, 1),
+                     "gbs_mean": round(READ_ONLY_BYTES / (statistics.fmean(ms) / 1e3) / 1e9, 1)}
+    flags = pgd.device_errors(clear=True, stream=stream)
+    if flags:
+        raise RuntimeError("device error word %d after the read-only passes" % flags)
+    del buf
+    best = max(r["gbs_best"] for r in rec.values())
+    rec.update({"bytes": READ_ONLY_BYTES, "passes": passes, "kernel": "pgd_read_stream"})
+    return best, rec
+
+
+# ------------------------------------------ PyTorch gather + SDPA (context)
+def torch_sdpa_context(pb, kv_bytes: int, iters: int, stream, ours):
+    """Context only (not the oracle, not a target): the same attention in
+    plain PyTorch on the GPU -- gather every sequence's blocks through the
+    block table from a row-major copy of the pool, then
+    scaled_dot_product_attention with GQA and a length mask."""
+    import torch
+    import torch.nn.functional as F
+    from paged_gqa_decode_kv_gb300 import inputs
+    B, n_q, d = pb.q.shape
+    n_kv, bs = pb.n_kv, pb.block_size
+    MB = pb.block_tables.shape[1]
+    L = MB * bs
+    # untimed preparation: row-major pools with the never-read slots zeroed
+    # (NaN there would reach the masked product)
+    kr = torch.nan_to_num(inputs.untile_pool(pb.k_cache).contiguous(), nan=0.0)
+    vr = torch.nan_to_num(inputs.untile_pool(pb.v_cache).contiguous(), nan=0.0)
+    tab = pb.block_tables.clamp(min=0).long()
+    lens = pb.context_lens.long()
+    mask = None
+    if int(lens.min()) != L:
+        mask = (torch.arange(L, device=tab.device)[None, :] < lens[:, None]).view(B, 1, 1, L)
+    q4 = pb.q.view(B, n_q, 1, d)
+
+    def run():
+        k = kr[tab].permute(0, 2, 1, 3, 4).reshape(B, n_kv, L, d)
+        v = vr[tab].permute(0, 2, 1, 3, 4).reshape(B, n_kv, L, d)
+        return F.scaled_dot_product_attention(q4, k, v, attn_mask=mask, scale=pb.scale,
+                                              enable_gqa=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            o = run()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            o = run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / iters
+    diff = (o.view(B, n_q, d).float() - ours.float()).abs().max().item()
+    del kr, vr
+    return {"kind": "context: PyTorch on the GPU (block gather by advanced indexing from a "
+                    "row-major copy of the pool, then scaled_dot_product_attention with "
+                    "enable_gqa and a length mask); not the oracle, not a target",
+            "ms_per_step": round(ms, 5), "gbs": round(kv_bytes / (ms / 1e3) / 1e9, 2),
+            "iters": iters, "max_abs_diff_vs_ours": round(diff, 5)}
 
 
 # --------------------------------------------------------------- our arm
@@ -411,6 +581,8 @@ def run_ours(args, rank, world, local):
     gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     sampler = ClockSampler(gpu_uuid)
     sampler.start()
+    nvml = NvmlClocks(gpu_uuid)
+    nvml.start()
     time.sleep(0.3)
     t_wall0 = time.time()
     for _ in range(args.warmup):
@@ -424,11 +596,13 @@ def run_ours(args, rank, world, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    t_timed0 = time.time()
     e0.record(stream)
     for i in range(K):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    t_timed1 = time.time()
     barrier(world)
     # The attention kernel alone, K launches each between two events on its
     # stream (inputs > L2, so every launch streams from HBM): the duration
@@ -444,6 +618,7 @@ def run_ours(args, rank, world, local):
     t_wall1 = time.time()
     time.sleep(0.25)
     sampler.stop()
+    nvml.stop()
     elapsed_ms = e0.elapsed_time(e1)
     attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
     flags = pgd.device_errors(clear=True, stream=stream)
@@ -495,6 +670,38 @@ def run_ours(args, rank, world, local):
     h2d = (q_h.numel() + kn_h.numel() + vn_h.numel()) * 2 + cl_h.numel() * 4
     d2h = out_h.numel() * 2
 
+    # Small working sets: the rotated pool copies above give the cold figure;
+    # the same step on one copy every time (pool resident in L2) is the hot one.
+    hot = None
+    if n_pools > 1:
+        kc0, vc0 = pools[0]
+
+        def hot_step():
+            append_attend(out, pb.q, pb.k_new, pb.v_new, kc0, vc0, pb.block_tables,
+                          pb.context_lens, pb.scale, num_splits=args.splits, workspace=ws,
+                          stream=stream)
+        for _ in range(max(3, args.warmup)):
+            hot_step()
+        h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        h0.record(stream)
+        for _ in range(K):
+            hot_step()
+        h1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        hot_ms = max_over_ranks(h0.elapsed_time(h1), world)
+        hot = {"ms_per_step": round(hot_ms / K, 5),
+               "value": round(total_bytes / (hot_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+               "note": "one %.1f MB pool copy every step (L2-resident after the first)"
+                       % (pool_bytes(pb) / 1e6)}
+
+    ro_best, ro_rec = read_only_peak(dev, stream)
+    ctx_rec = None
+    if not fp8 and not T:
+        ctx_rec = torch_sdpa_context(pb, kv_bytes, min(K, 50), stream, out)
+
     peak, peak_kind = hbm_peak()
     achieved = kv_bytes / (attn_ms / 1e3) / 1e9
     result = {
@@ -516,7 +723,9 @@ def run_ours(args, rank, world, local):
                                        / (max_ms / 1e3) / 1e9, 2),
         "seq_layer_steps_per_s": round(seq_steps, 1),
         "pct_of_hbm_peak": {"nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-                            peak_kind: round(100 * value / world / peak, 2)},
+                            peak_kind: round(100 * value / world / peak, 2),
+                            "read_only": round(100 * value / world / ro_best, 2)},
+        "read_only_stream": dict(ro_rec, gbs=ro_best),
         "roofline": {"bound": "hbm",
                      "kernel": ("pgd::pf::prefix_attention_kernel + pgd::tc::paged_attention_kernel"
                                 " + pgd::pf::cascade_combine_kernel (cascade, tcgen05)")
@@ -530,7 +739,8 @@ def run_ours(args, rank, world, local):
                      "traffic": None if (args.cascade or T) else
                      profiled_traffic(args.kv, args.workload),
                      "launch_ms": round(attn_ms, 5),
-                     "bytes_per_launch": kv_bytes},
+                     "bytes_per_launch": kv_bytes,
+                     "frac_of_read_only": round(achieved / ro_best, 4)},
         "e2e": dict({"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                      "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5)},
                     **({"path": "pgd_decode_step (host buffers; no cascade)"}
@@ -540,9 +750,16 @@ def run_ours(args, rank, world, local):
                        if T else {})),
         # kv_append + attention (cascade: + the prefix pass and the combine)
         "gpu_launches": (4 if args.cascade else 2) * K,
-        "clocks": sampler.summary(t_wall0, t_wall1),
+        "clocks": clocks_record(sampler, nvml, t_wall0, t_wall1, t_timed0, t_timed1),
         "gpu": torch.cuda.get_device_name(local),
     }
+    if hot is not None:
+        result["cold"] = {"ms_per_step": result["ms_per_step"], "value": result["value"],
+                          "unit": "GB/s", "note": "the headline: %d pool copies rotated"
+                                                  % n_pools}
+        result["hot"] = hot
+    if ctx_rec is not None:
+        result["torch_gather_sdpa"] = ctx_rec
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(host_copy(pb, T), args.cpu_seconds)
     return result

@@ -12,7 +12,8 @@ from ._native import (  # noqa: F401
     paged_decode_attention_noalloc, append_decode_attention, decode_step, copy_blocks,
     kv_append_fp8, paged_decode_attention_fp8, append_decode_attention_fp8,
     cascade_decode_attention, cascade_workspace_size, kv_append_tokens, paged_verify_attention,
-    verify_workspace_size, mla_append, mla_decode_attention, mla_workspace_size, device_errors, workspace_size, make_workspace, attention_grid, validate_tables, lib,
+    verify_workspace_size, mla_append, mla_decode_attention, mla_workspace_size, device_errors,
+    workspace_size, make_workspace, attention_grid, validate_tables, read_stream, lib,
     library_path)
 
 __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "tile_pool",
@@ -24,4 +25,4 @@ __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload",
            "kv_append_tokens", "paged_verify_attention", "verify_workspace_size",
            "mla_append", "mla_decode_attention", "mla_workspace_size",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
-           "validate_tables", "lib", "library_path"]
+           "validate_tables", "read_stream", "lib", "library_path"]

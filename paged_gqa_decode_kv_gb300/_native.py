@@ -60,6 +60,7 @@ SIGNATURES = {
                              _I, _I, _I, _F, _I, _P, _Z, _P], _I),
     "pgd_copy_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "pgd_device_errors": ([_P, _I, _P], _I),
+    "pgd_read_stream": ([_P, _Z, _I, _P], _I),
     "pgd_alloc_create": ([_I, _P], _I),
     "pgd_alloc_destroy": ([_P], None),
     "pgd_alloc_allocate": ([_P, _I, _P], _I),
@@ -486,6 +487,16 @@ def device_errors(clear: bool = True, stream=None) -> int:
     v = ctypes.c_int32(0)
     _check(lib().pgd_device_errors(ctypes.addressof(v), 1 if clear else 0, _stream(stream)))
     return int(v.value)
+
+
+def read_stream(src: torch.Tensor, mode: int = 0, stream=None) -> None:
+    """Read every byte of the CUDA tensor `src` once and discard it (the
+    read-only streaming calibration pass; mode 0: 16-byte loads, mode 1:
+    4 KiB bulk copies into shared memory)."""
+    if not src.is_cuda or not src.is_contiguous():
+        raise ValueError("src must be a contiguous CUDA tensor")
+    _check(lib().pgd_read_stream(_ptr(src), src.numel() * src.element_size(), int(mode),
+                                 _stream(stream)))
 
 
 # ------------------------------------------------------------ host allocator
