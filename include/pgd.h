@@ -461,6 +461,24 @@ pgd_status pgd_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_ids,
 pgd_status pgd_read_stream(const void *src, size_t bytes, int32_t mode, void *stream);
 
 /* ---------------------------------------------------------------------- */
+/* wait limit of the kernels' bounded waits (for tests of the exit path)  */
+/* ---------------------------------------------------------------------- */
+/* Every wait of a kernel's role on another role of its CTA (an mbarrier
+ * phase) gives up after a limit; the kernel then sets PGD_DEVERR_TIMEOUT,
+ * stops issuing copies and MMAs, lets every role run to the end of its walk
+ * with its remaining waits returning at once, waits (with the fixed 4 s
+ * limit) for the copies already in flight, frees its tensor memory and
+ * exits; its outputs are then unspecified, the caller's workspace counters
+ * are left at zero and the next call runs normally.  The limit is 4 s
+ * (4e9 ns); pgd_set_wait_limit_ns sets it, process-wide, for the launches
+ * made after the call (0 restores 4 s) -- a short limit makes the waits run
+ * out on purpose, which is what a test of that exit path needs; nothing else
+ * should change it.  Thread-safe; pgd_wait_limit_ns returns the value in
+ * force.  No counterpart on the pages. */
+void pgd_set_wait_limit_ns(uint64_t ns);
+uint64_t pgd_wait_limit_ns(void);
+
+/* ---------------------------------------------------------------------- */
 /* device error word                                                      */
 /* ---------------------------------------------------------------------- */
 /* Wait for `stream`, then read the current device's error word (PGD_DEVERR_*

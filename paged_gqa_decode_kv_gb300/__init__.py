@@ -13,8 +13,8 @@ from ._native import (  # noqa: F401
     kv_append_fp8, paged_decode_attention_fp8, append_decode_attention_fp8,
     cascade_decode_attention, cascade_workspace_size, kv_append_tokens, paged_verify_attention,
     verify_workspace_size, mla_append, mla_decode_attention, mla_workspace_size, device_errors,
-    workspace_size, make_workspace, attention_grid, validate_tables, read_stream, lib,
-    library_path)
+    workspace_size, make_workspace, attention_grid, validate_tables, read_stream, set_wait_limit_ns,
+    wait_limit_ns, lib, library_path)
 
 __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "tile_pool",
            "untile_pool", "pool_shape", "pack_pool8", "unpack_pool8", "pool_shape8", "PGDError",
@@ -25,4 +25,5 @@ __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload",
            "kv_append_tokens", "paged_verify_attention", "verify_workspace_size",
            "mla_append", "mla_decode_attention", "mla_workspace_size",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
-           "validate_tables", "read_stream", "lib", "library_path"]
+           "validate_tables", "read_stream", "set_wait_limit_ns", "wait_limit_ns", "lib",
+           "library_path"]

@@ -61,6 +61,8 @@ SIGNATURES = {
     "pgd_copy_blocks": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "pgd_device_errors": ([_P, _I, _P], _I),
     "pgd_read_stream": ([_P, _Z, _I, _P], _I),
+    "pgd_set_wait_limit_ns": ([ctypes.c_uint64], None),
+    "pgd_wait_limit_ns": ([], ctypes.c_uint64),
     "pgd_alloc_create": ([_I, _P], _I),
     "pgd_alloc_destroy": ([_P], None),
     "pgd_alloc_allocate": ([_P, _I, _P], _I),
@@ -497,6 +499,17 @@ def read_stream(src: torch.Tensor, mode: int = 0, stream=None) -> None:
         raise ValueError("src must be a contiguous CUDA tensor")
     _check(lib().pgd_read_stream(_ptr(src), src.numel() * src.element_size(), int(mode),
                                  _stream(stream)))
+
+
+def set_wait_limit_ns(ns: int) -> None:
+    """Limit of the kernels' bounded waits for launches made after this call
+    (0 restores the 4 s default).  A short limit makes waits run out on
+    purpose: for tests of the timeout exit only."""
+    lib().pgd_set_wait_limit_ns(int(ns))
+
+
+def wait_limit_ns() -> int:
+    return int(lib().pgd_wait_limit_ns())
 
 
 # ------------------------------------------------------------ host allocator

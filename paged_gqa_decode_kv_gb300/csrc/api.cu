@@ -73,6 +73,10 @@ pgd_status ok() {
   return PGD_OK;
 }
 
+// Wait limit handed to every launch (0: the kernels' default); set only by
+// pgd_set_wait_limit_ns, for tests of the timeout exit.
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+
 pgd_status cuda_fail(cudaError_t e, const char *what) {
   return fail(PGD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -257,6 +261,7 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.err = err;
+  p.wait_limit_ns = g_wait_limit_ns.load();
   p.wait_late = 0;
   p.seq_prefix_blocks = nullptr;
   p.pre_ml = nullptr;
@@ -634,6 +639,7 @@ pgd_status pgd_cascade_decode_attention(
   pp.pre_ml = pre_ml;
   pp.pre_o = pre_o;
   pp.err = pa.p.err;
+  pp.wait_limit_ns = pa.p.wait_limit_ns;
   const int grid = n_groups * n_kv * plan.n_rchunk * plan.n_tsplit;
   cudaError_t e = prefix_attention_launch(pp, pa.G, bs, grid, st);
   if (e != cudaSuccess) return cuda_fail(e, "shared-prefix pass launch");
@@ -766,6 +772,7 @@ pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
   p.part_ml = need ? reinterpret_cast<float *>(ws) : nullptr;
   p.part_o = need ? reinterpret_cast<float *>(ws + round_up(rows * 2 * 4, kWsAlign)) : nullptr;
   p.err = err;
+  p.wait_limit_ns = g_wait_limit_ns.load();
   cudaError_t e = mla_attention_launch(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "MLA attention launch");
   return ok();
@@ -954,6 +961,13 @@ pgd_status pgd_read_stream(const void *src, size_t bytes, int32_t mode, void *st
   cudaError_t e = read_stream_launch(src, bytes, mode, err, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "read stream launch");
   return ok();
+}
+
+void pgd_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store((unsigned long long)ns); }
+
+uint64_t pgd_wait_limit_ns(void) {
+  const unsigned long long v = g_wait_limit_ns.load();
+  return v ? (uint64_t)v : (uint64_t)kWaitLimitNs;
 }
 
 pgd_status pgd_device_errors(int32_t *flags, int32_t clear, void *stream) {

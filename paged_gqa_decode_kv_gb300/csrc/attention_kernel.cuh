@@ -163,6 +163,8 @@ __host__ __device__ constexpr size_t smem_bytes(int B) {
   return (size_t)SMEM_SLACK + Lay<FP8>::OFF_PRE + (size_t)(B + 1) * 4;
 }
 static_assert(smem_bytes<false>(PGD_MAX_BATCH) <= 232448, "bf16 layout exceeds 227 KB");
+static_assert((Lay<false>::OFF_MISC + 24) % 8 == 0 && (Lay<true>::OFF_MISC + 24) % 8 == 0,
+              "WaitCtl alignment");
 static_assert(smem_bytes<true>(PGD_MAX_BATCH) <= 232448, "8-bit layout exceeds 227 KB");
 
 __device__ __forceinline__ uint32_t col_s(int sb) { return (uint32_t)sb * 16u; }  // sb < NSB
@@ -305,18 +307,20 @@ __device__ __forceinline__ float warp_reduce_heads(const float (&v)[G], int lane
 
 // Bounded wait that gives up at once after any earlier timeout in the CTA, so
 // that the control flow (and every named barrier) is the same for all threads
-// whatever happens.
+// whatever happens.  abort_flag is the first member of the CTA's WaitCtl,
+// which also holds the launch's wait limit.
 // (The spin is a function of its own: one copy of it instead of one per
 // wait keeps the kernel's code small enough for the instruction caches.)
 static __device__ __noinline__ void wait_spin(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, int32_t *err) {
   if (*abort_flag) return;
+  const uint64_t limit = reinterpret_cast<const volatile WaitCtl *>(abort_flag)->limit_ns;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return;
     if ((i & 31u) == 0) {
       if (*abort_flag) return;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit) {
         *abort_flag = 1;
         atomicOr(err, PGD_DEVERR_TIMEOUT);
         return;
@@ -531,8 +535,9 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
   bool have = cur.next(sc, p.B, sg);
   if (have) load_ahead(sg, cur_a);
   if (p.wait_late == 1) pdl_wait();  // kv_append has written the caches
-  int s = 0, k = 0;
-  while (have) {
+  int s = 0, k = 0;  // s: stages armed so far
+  bool stop = false;  // after a timeout in the CTA: arm nothing more
+  while (have && !stop) {
     const bool have_next = cur.next(sc, p.B, nsg);
     if (have_next) load_ahead(nsg, next_a);
     if (IS_K) {
@@ -603,8 +608,20 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
       const unsigned okmask = __ballot_sync(kFullMask, ok);
       const unsigned want = (1u << nb) - 1u;
       const int slot = s % NS;
+      // One decision for the whole warp: after a timeout the slot's earlier
+      // copies may still be landing, so it is neither armed again (an
+      // arrival there could meet a phase whose bytes are still pending) nor
+      // written; the drain below waits for what was armed.
+      int go = 1;
       if (lane == 0) {
         wait_or_abort(&empty[slot], ((uint32_t)(s / NS) & 1u) ^ 1u, abort_flag, p.err);
+        go = *abort_flag ? 0 : 1;
+      }
+      if (!__shfl_sync(kFullMask, go, 0)) {
+        stop = true;
+        break;
+      }
+      if (lane == 0) {
         if (IS_K) {
           stage_mask[s & 7] = (int)(want & ~okmask);
           if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
@@ -612,13 +629,13 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
           stage_mask[slot] = (int)(want & ~okmask);  // per V slot, for the V converters
         }
         const uint32_t bytes = (uint32_t)__popc(okmask) * TILE_BYTES;
-        if (*abort_flag || bytes == 0)
+        if (bytes == 0)
           mbar_arrive(&full[slot]);
         else
           mbar_arrive_expect_tx(&full[slot], bytes);
       }
       __syncwarp();
-      if (ok && !*abort_flag) {
+      if (ok) {
         const unsigned char *src = cache + ((size_t)blk * p.n_kv + sg.g) * (size_t)TILE_BYTES;
         bulk_copy_g2s(ring + (size_t)slot * L::STAGE + (size_t)lane * TILE_BYTES, src,
                       TILE_BYTES, &full[slot], policy);
@@ -628,11 +645,14 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
     cur_a = next_a;
     have = have_next;
   }
-  // no copy may still be landing when the CTA exits
+  // no copy may still be landing when the CTA exits: wait for the last NS
+  // armed stages (every earlier one was consumed before its slot was armed
+  // again), with the fixed limit whatever the launch's
   if (lane == 0) {
     for (int k = 1; k <= NS && k <= s; ++k) {
       const int last = s - k;
-      mbar_wait_bounded(&full[last % NS], (uint32_t)(last / NS) & 1u);
+      if (!mbar_wait_bounded(&full[last % NS], (uint32_t)(last / NS) & 1u))
+        atomicOr(p.err, PGD_DEVERR_TIMEOUT);
     }
   }
 }
@@ -744,7 +764,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   float *mref = reinterpret_cast<float *>(smem + L::OFF_MREF);
   float *qscale = reinterpret_cast<float *>(smem + L::OFF_QS);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 24);  // WaitCtl
   volatile int *flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 8);         // [3]
   int *nmax_slot = reinterpret_cast<int *>(smem + L::OFF_MISC + 20);
   volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 40);  // [8]
@@ -789,7 +809,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
       mbar_init(&q_free[i], FP8 ? 1 + 4 : 1);
     }
     mbar_init_fence();
-    *abort_flag = 0;
+    init_wait_ctl(smem + L::OFF_MISC + 24, p.wait_limit_ns);
   }
   // Q pad rows and P pad columns stay zero for the whole kernel.
   {

@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   uint64_t *s_free = bars + 3 * NSTG;
   uint64_t *p_full = bars + 4 * NSTG, *p_free = p_full + 1, *o_done = p_full + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 16);  // WaitCtl
   volatile int *bad_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);  // [NSTG]
 
   if (tid == 0) {
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
     mbar_init(p_free, 1);
     mbar_init(o_done, 1);
     mbar_init_fence();
-    *abort_flag = 0;
+    init_wait_ctl(smem + OFF_MISC + 16, p.wait_limit_ns);
   }
   // Q rows as the K-major A operand: head row r, dims 8c..8c+7 in core
   // matrix (r / 8, c), row r % 8; rows past the real heads are zeros.
@@ -290,6 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   if (warp == WARP_PROD) {
     // ------------------------------------------------------------ producer
     const uint64_t policy = l2_policy_evict_first();
+    int armed = 0;  // stages armed; after a timeout in the CTA nothing more is
     for (int i = 0; i < nst; ++i) {
       const int buf = i % NSTG;
       const uint32_t par = (uint32_t)(i / NSTG) & 1u;
@@ -299,18 +300,26 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       const bool ok = lane < nb && (unsigned)blk < (unsigned)p.NB;
       const unsigned okmask = __ballot_sync(kFullMask, ok);
       const unsigned want = (nb >= 32) ? ~0u : ((1u << nb) - 1u);
+      // one decision for the warp: after a timeout the buffer's earlier copy
+      // may still be landing, so it is neither armed again nor written
+      int go = 1;
       if (lane == 0) {
         wait_or_abort(&c_empty[buf], par ^ 1u, abort_flag, p.err);
+        go = *abort_flag ? 0 : 1;
+      }
+      if (!__shfl_sync(kFullMask, go, 0)) break;
+      armed = i + 1;
+      if (lane == 0) {
         bad_mask[buf] = (int)(want & ~okmask);
         if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
         const uint32_t bytes = (uint32_t)__popc(okmask) * PIECE;
-        if (*abort_flag || bytes == 0)
+        if (bytes == 0)
           mbar_arrive(&c_full[buf]);
         else
           mbar_arrive_expect_tx(&c_full[buf], bytes);
       }
       __syncwarp();
-      if (ok && !*abort_flag)
+      if (ok)
         bulk_copy_g2s(smem + OFF_C + buf * STAGE + lane * (PB / 8) * GRP,
                       p.cache + (size_t)blk * TILE + (size_t)((t0 % BS) / 8) * GRP, PIECE,
                       &c_full[buf], policy);
@@ -326,9 +335,10 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       }
     }
     if (lane == 0) {  // no copy may still be landing when the CTA exits
-      for (int k = 1; k <= NSTG && k <= nst; ++k) {
-        const int last = nst - k;
-        mbar_wait_bounded(&c_full[last % NSTG], (uint32_t)(last / NSTG) & 1u);
+      for (int k = 1; k <= NSTG && k <= armed; ++k) {
+        const int last = armed - k;
+        if (!mbar_wait_bounded(&c_full[last % NSTG], (uint32_t)(last / NSTG) & 1u))
+          atomicOr(p.err, PGD_DEVERR_TIMEOUT);
       }
     }
   } else if (warp == WARP_QK) {

@@ -14,8 +14,26 @@ namespace pgd {
 constexpr int kHeadDim = 128;
 constexpr unsigned kFullMask = 0xffffffffu;
 // A bounded wait gives up after this long (ns of %globaltimer) and reports
-// PGD_DEVERR_TIMEOUT instead of hanging the GPU.
+// PGD_DEVERR_TIMEOUT instead of hanging the GPU.  Launches carry their own
+// limit for the waits on other roles of the CTA (0 = this default; a test of
+// the timeout exit sets a short one); the drains that make sure no copy is
+// still landing when a CTA exits always use this one.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+// Per-CTA wait control in shared memory: the abort flag that every bounded
+// wait of the CTA checks (first member, so a pointer to it is a pointer to
+// the whole), then the launch's wait limit.
+struct WaitCtl {
+  int abort;
+  int pad;
+  unsigned long long limit_ns;
+};
+__device__ __forceinline__ volatile int *init_wait_ctl(void *slot, unsigned long long limit_ns) {
+  volatile WaitCtl *c = reinterpret_cast<volatile WaitCtl *>(slot);
+  c->abort = 0;
+  c->limit_ns = limit_ns ? limit_ns : kWaitLimitNs;
+  return &c->abort;
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -156,6 +174,7 @@ struct AttnParams {
   int2 *part_info;               // cascade: per unit (first part, parts); such units are
                                  // merged with their prefix parts by the combine kernel
   int32_t *err;                  // device error word
+  unsigned long long wait_limit_ns;  // bounded waits give up after this (0: kWaitLimitNs)
 };
 
 // Final merge of cascade attention (prefix_attention.cu): decode parts of
@@ -188,6 +207,7 @@ struct PrefixParams {
   float *pre_ml;                 // [B][n_q][n_tsplit][2]   partial (max, sum), log2 domain
   float *pre_o;                  // [B][n_q][n_tsplit][D]   unnormalised partial outputs
   int32_t *err;
+  unsigned long long wait_limit_ns;  // bounded waits give up after this (0: kWaitLimitNs)
 };
 
 // Decode attention over an MLA latent cache (mla_attention.cu).
@@ -203,6 +223,7 @@ struct MlaParams {
   float *part_ml;                // [B][H][n_parts][2] partial (max, sum), log2 domain
   float *part_o;                 // [B][H][n_parts][512] unnormalised partial outputs
   int32_t *err;
+  unsigned long long wait_limit_ns;  // bounded waits give up after this (0: kWaitLimitNs)
 };
 
 }  // namespace pgd

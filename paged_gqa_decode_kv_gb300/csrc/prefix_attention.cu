@@ -124,33 +124,44 @@ __device__ __forceinline__ void produce(const PrefixParams &p, const int32_t *tr
   constexpr uint32_t TILE = BS * 256;
   const uint64_t policy = l2_policy_evict_first();
   const int nst = (nblk + SB - 1) / SB;
+  int armed = 0;  // stages armed; after a timeout in the CTA nothing more is
   for (int st = 0; st < nst; ++st) {
     const int first = st * SB, nb = min(SB, nblk - first), slot = st & 1;
     const int blk = (lane < nb) ? __ldg(trow + blk0 + first + lane) : -1;
     const bool ok = lane < nb && (unsigned)blk < (unsigned)p.NB;
     const unsigned okmask = __ballot_sync(kFullMask, ok);
     const unsigned want = (1u << nb) - 1u;
+    // one decision for the warp: after a timeout the slot's earlier copies
+    // may still be landing, so it is neither armed again nor written
+    int go = 1;
     if (lane == 0) {
       wait_or_abort(&empty[slot], ((uint32_t)(st >> 1) & 1u) ^ 1u, abort_flag, p.err);
+      go = *abort_flag ? 0 : 1;
+    }
+    if (!__shfl_sync(kFullMask, go, 0)) break;
+    armed = st + 1;
+    if (lane == 0) {
       if (mask) {
         mask[st & 3] = (int)(want & ~okmask);
         if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
       }
       const uint32_t bytes = (uint32_t)__popc(okmask) * TILE;
-      if (*abort_flag || bytes == 0)
+      if (bytes == 0)
         mbar_arrive(&full[slot]);
       else
         mbar_arrive_expect_tx(&full[slot], bytes);
     }
     __syncwarp();
-    if (ok && !*abort_flag)
+    if (ok)
       bulk_copy_g2s(ring + (size_t)slot * STAGE + (size_t)lane * TILE,
                     cache + ((size_t)blk * p.n_kv + g) * (size_t)TILE, TILE, &full[slot], policy);
   }
+  // no copy may still be landing when the CTA exits (fixed limit)
   if (lane == 0) {
-    for (int k = 1; k <= 2 && k <= nst; ++k) {
-      const int last = nst - k;
-      mbar_wait_bounded(&full[last & 1], (uint32_t)(last >> 1) & 1u);
+    for (int k = 1; k <= 2 && k <= armed; ++k) {
+      const int last = armed - k;
+      if (!mbar_wait_bounded(&full[last & 1], (uint32_t)(last >> 1) & 1u))
+        atomicOr(p.err, PGD_DEVERR_TIMEOUT);
     }
   }
 }
@@ -213,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
   uint64_t *s_full = bars + 8, *s_free = bars + 10, *p_full = bars + 12, *p_free = bars + 14;
   uint64_t *m_ready = bars + 16, *o_done = bars + 18;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 32);  // WaitCtl
   volatile int *stage_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 16);  // [4]
 
   if (tid == 0) {
@@ -230,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefix_attention_kernel(const Pref
     }
     mbar_init(o_done, 1);
     mbar_init_fence();
-    *abort_flag = 0;
+    init_wait_ctl(smem + OFF_MISC + 32, p.wait_limit_ns);
   }
   // Q rows as the K-major A operand: row r, dims 8c..8c+7 in core matrix
   // (r / 8, c), row r % 8; rows past the chunk are zeros.

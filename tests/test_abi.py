@@ -147,3 +147,15 @@ def test_read_stream_rejects_on_host(L):
     assert L.pgd_read_stream(P(16), 40, 0, None) == _native.ERR_INVALID_ARG     # not 16 B units
     assert L.pgd_read_stream(P(16), 8192 + 16, 1, None) == _native.ERR_INVALID_ARG  # not 4 KiB
     assert L.pgd_read_stream(None, 0, 1, None) == 0                              # no-op
+
+
+def test_wait_limit_setting(L):
+    """The bounded waits' limit: 4 s by default, set and restored process-wide
+    (a host-side setting; no GPU call)."""
+    assert pgd.wait_limit_ns() == 4_000_000_000
+    try:
+        pgd.set_wait_limit_ns(1234)
+        assert pgd.wait_limit_ns() == 1234
+    finally:
+        pgd.set_wait_limit_ns(0)
+    assert pgd.wait_limit_ns() == 4_000_000_000
