@@ -767,9 +767,10 @@ def run_ours(args, rank, world, local):
 
 # ------------------------------------------------------ MLA latent cache
 def run_mla(args, rank, world, local):
-    """A step = pgd_mla_append of every sequence's newest latent row, then
-    pgd_mla_decode_attention of every head over its sequence's latent cache;
-    bytes = each cached token's 576 bf16 values once."""
+    """A step = pgd_mla_append_decode_attention: every sequence's newest
+    latent row appended, then every head attends over its sequence's latent
+    cache (and cut units are merged); bytes = each cached token's 576 bf16
+    values once."""
     import torch
 
     import __graft_entry__
@@ -805,12 +806,15 @@ def run_mla(args, rank, world, local):
 
     def step():
         c = next_pool()
-        pgd.mla_append(mb.c_new, c, mb.block_tables, mb.positions, stream=stream)
-        attend(c)
+        pgd.mla_append_decode_attention(out, mb.q, mb.c_new, c, mb.block_tables,
+                                        mb.context_lens, mb.scale, num_splits=args.splits,
+                                        workspace=ws, stream=stream)
 
     gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     sampler = ClockSampler(gpu_uuid)
     sampler.start()
+    nvml = NvmlClocks(gpu_uuid)
+    nvml.start()
     time.sleep(0.3)
     t_wall0 = time.time()
     for _ in range(args.warmup):
@@ -823,11 +827,13 @@ def run_mla(args, rank, world, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    t_timed0 = time.time()
     e0.record(stream)
     for _ in range(K):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    t_timed1 = time.time()
     barrier(world)
     ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -841,6 +847,7 @@ def run_mla(args, rank, world, local):
     t_wall1 = time.time()
     time.sleep(0.25)
     sampler.stop()
+    nvml.stop()
     elapsed_ms = e0.elapsed_time(e1)
     attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
     flags = pgd.device_errors(clear=True, stream=stream)
@@ -859,8 +866,9 @@ def run_mla(args, rank, world, local):
         with torch.cuda.stream(stream):
             q_d.copy_(q_h, non_blocking=True)
             cn_d.copy_(cn_h, non_blocking=True)
-            pgd.mla_append(cn_d, c, mb.block_tables, mb.positions, stream=stream)
-            attend(c, q_=q_d)
+            pgd.mla_append_decode_attention(out, q_d, cn_d, c, mb.block_tables,
+                                            mb.context_lens, mb.scale, num_splits=args.splits,
+                                            workspace=ws, stream=stream)
             out_h.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -873,6 +881,7 @@ def run_mla(args, rank, world, local):
     f1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
+    ro_best, ro_rec = read_only_peak(dev, stream)
     peak, peak_kind = hbm_peak()
     achieved = nbytes / (attn_ms / 1e3) / 1e9
     parts = args.splits if args.splits > 0 else max(1, min(
@@ -892,19 +901,23 @@ def run_mla(args, rank, world, local):
         "kv_bytes_per_step": nbytes,
         "seq_layer_steps_per_s": round(sum_over_ranks(B * K, world) / (max_ms / 1e3), 1),
         "pct_of_hbm_peak": {"nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
-                            peak_kind: round(100 * value / world / peak, 2)},
+                            peak_kind: round(100 * value / world / peak, 2),
+                            "read_only": round(100 * value / world / ro_best, 2)},
+        "read_only_stream": dict(ro_rec, gbs=ro_best),
         "roofline": {"bound": "hbm", "kernel": "pgd::mla::mla_attention_kernel<%d> (tcgen05)"
                      % mb.block_size, "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": profiled_mla_traffic(name) if args.splits == 0 else None,
                      "launch_ms": round(attn_ms, 5), "bytes_per_launch": nbytes,
+                     "frac_of_read_only": round(achieved / ro_best, 4),
                      "tflops_achieved": round(flops / (attn_ms / 1e3) / 1e12, 2),
                      "flop_per_byte": round(flops / nbytes, 1)},
         "e2e": {"value": round(sum_over_ranks(nbytes * K, world) / (e2e_ms / 1e3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": q_h.numel() * 2 + cn_h.numel() * 2,
                 "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": round(e2e_ms / K, 5)},
+        # latent append, attention, merge of the parts
         "gpu_launches": (2 + (1 if parts > 1 else 0)) * K,
-        "clocks": sampler.summary(t_wall0, t_wall1),
+        "clocks": clocks_record(sampler, nvml, t_wall0, t_wall1, t_timed0, t_timed1),
         "gpu": torch.cuda.get_device_name(local),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

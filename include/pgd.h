@@ -289,6 +289,21 @@ pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
                                     int32_t B, int32_t H, int32_t d, int32_t dv, int32_t bs,
                                     int32_t MB, int32_t NB, float scale, int32_t num_splits,
                                     void *workspace, size_t workspace_bytes, void *stream);
+/* The decode step of one layer over a latent cache: c_new[b] (bf16 [B][576])
+ * written at position context_lens[b] - 1 exactly as pgd_mla_append does,
+ * then pgd_mla_decode_attention over the updated cache -- the same shapes,
+ * rules, results and errors as those two calls one after the other, every
+ * argument checked before anything is enqueued.  The attention kernel knows
+ * that the kernel before it writes only the cache: its prologue (queries,
+ * tensor memory, barriers) runs while the append does, and only its copies
+ * wait for it. */
+pgd_status pgd_mla_append_decode_attention(void *out, const void *q, const void *c_new,
+                                           void *cache, const int32_t *block_tables,
+                                           const int32_t *context_lens, int32_t B, int32_t H,
+                                           int32_t d, int32_t dv, int32_t bs, int32_t MB,
+                                           int32_t NB, float scale, int32_t num_splits,
+                                           void *workspace, size_t workspace_bytes,
+                                           void *stream);
 
 /* ---------------------------------------------------------------------- */
 /* cascade: shared prefixes read once per group                            */

@@ -46,6 +46,8 @@ SIGNATURES = {
     "pgd_mla_append": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "pgd_mla_decode_attention": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
                                   _P], _I),
+    "pgd_mla_append_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                         _I, _P, _Z, _P], _I),
     "pgd_cascade_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _Z),
     "pgd_cascade_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P], _I),
@@ -355,6 +357,33 @@ def mla_decode_attention(out, q, cache, block_tables, context_lens, scale: float
     _check(lib().pgd_mla_decode_attention(
         _ptr(out), _ptr(q), _ptr(cache), _ptr(block_tables), _ptr(context_lens), B, H, D, 512,
         bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+def mla_append_decode_attention(out, q, c_new, cache, block_tables, context_lens, scale: float,
+                                num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """mla_append of c_new at context_lens - 1, then mla_decode_attention over
+    the updated cache (one call, two kernels and the merge; the attention
+    prologue overlaps the append)."""
+    _need(q, torch.bfloat16, "q")
+    _need(c_new, torch.bfloat16, "c_new")
+    _need(cache, torch.bfloat16, "cache")
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, H, D = q.shape
+    NB, bs, D2 = _mla_pool_dims(cache)
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out")
+    if workspace is None:
+        workspace = torch.empty(max(256, mla_workspace_size(B, H, num_splits)), dtype=torch.uint8,
+                                device=q.device)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_mla_append_decode_attention(
+        _ptr(out), _ptr(q), _ptr(c_new), _ptr(cache), _ptr(block_tables), _ptr(context_lens), B,
+        H, D, 512, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
 

@@ -27,8 +27,8 @@ cudaError_t prefix_attention_launch(const PrefixParams &p, int G, int bs, int gr
 cudaError_t cascade_combine_launch(const CombineParams &p, int G, cudaStream_t stream);
 cudaError_t mla_attention_launch(const MlaParams &p, cudaStream_t stream);
 cudaError_t mla_append_launch(const void *c_new, void *cache, const int32_t *tables,
-                              const int32_t *pos, int B, int bs, int MB, int NB, int32_t *err,
-                              cudaStream_t stream);
+                              const int32_t *pos, int pos_offset, int B, int bs, int MB, int NB,
+                              int32_t *err, cudaStream_t stream);
 int mla_heads_per_cta();
 cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
                                  void *v_cache, const int32_t *tables, const int32_t *pos,
@@ -706,33 +706,27 @@ size_t pgd_mla_workspace_size(int32_t B, int32_t H, int32_t num_splits) {
   return std::max<size_t>(mla_ws_bytes(B, H, parts), 256);
 }
 
-pgd_status pgd_mla_append(const void *c_new, void *cache, const int32_t *block_tables,
-                          const int32_t *positions, int32_t B, int32_t d, int32_t bs, int32_t MB,
-                          int32_t NB, void *stream) {
+pgd_status check_mla_append(const void *c_new, const void *cache, const int32_t *block_tables,
+                            const int32_t *positions, int32_t B, int32_t d, int32_t bs,
+                            int32_t MB, int32_t NB) {
   if (B < 0) return fail(PGD_ERR_INVALID_ARG, "B = %d", B);
   if (d != kMlaD) return fail(PGD_ERR_UNSUPPORTED, "d = %d (576 cached values per token)", d);
   if (bs != 16 && bs != 32 && bs != 64) return fail(PGD_ERR_UNSUPPORTED, "block size %d", bs);
   if (MB <= 0 || NB <= 0) return fail(PGD_ERR_INVALID_ARG, "MB, NB must be > 0");
   if ((long long)B * MB >= 0x7fffffffLL) return fail(PGD_ERR_INVALID_ARG, "B * MB >= 2^31");
-  if (B == 0) return ok();
+  if (B == 0) return PGD_OK;
   if (!c_new || !cache || !block_tables || !positions)
     return fail(PGD_ERR_INVALID_ARG, "null pointer");
   if (!aligned(c_new, 16) || !aligned(cache, 16))
     return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
-  int32_t *err = nullptr;
-  pgd_status s = error_word(&err);
-  if (s != PGD_OK) return s;
-  cudaError_t e = mla_append_launch(c_new, cache, block_tables, positions, B, bs, MB, NB, err,
-                                    static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "MLA append launch");
-  return ok();
+  return PGD_OK;
 }
 
-pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
-                                    const int32_t *block_tables, const int32_t *context_lens,
-                                    int32_t B, int32_t H, int32_t d, int32_t dv, int32_t bs,
-                                    int32_t MB, int32_t NB, float scale, int32_t num_splits,
-                                    void *workspace, size_t workspace_bytes, void *stream) {
+// Checks and the parameter block of an MLA attention call; nothing enqueued.
+pgd_status mla_prepare(void *out, const void *q, const void *cache, const int32_t *block_tables,
+                       const int32_t *context_lens, int32_t B, int32_t H, int32_t d, int32_t dv,
+                       int32_t bs, int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                       void *workspace, size_t workspace_bytes, MlaParams *pp) {
   if (B < 0 || H <= 0) return fail(PGD_ERR_INVALID_ARG, "B = %d, H = %d", B, H);
   if (d != kMlaD || dv != kMlaDv)
     return fail(PGD_ERR_UNSUPPORTED, "d = %d, dv = %d (576 and 512)", d, dv);
@@ -742,7 +736,7 @@ pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
   if (num_splits < 0 || num_splits > 1024) return fail(PGD_ERR_INVALID_ARG, "num_splits");
   if ((long long)B * MB >= 0x7fffffffLL || (long long)B * H * 1024 >= 0x7fffffffLL)
     return fail(PGD_ERR_INVALID_ARG, "sizes too large");
-  if (B == 0) return ok();
+  if (B == 0) return PGD_OK;
   if (!out || !q || !cache || !block_tables || !context_lens)
     return fail(PGD_ERR_INVALID_ARG, "null pointer");
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(cache, 16))
@@ -766,6 +760,7 @@ pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
   p.NB = NB;
   p.bs = bs;
   p.n_parts = parts;
+  p.wait_late = 0;
   p.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);
   unsigned char *ws = static_cast<unsigned char *>(workspace);
   const size_t rows = (size_t)B * H * parts;
@@ -773,7 +768,61 @@ pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
   p.part_o = need ? reinterpret_cast<float *>(ws + round_up(rows * 2 * 4, kWsAlign)) : nullptr;
   p.err = err;
   p.wait_limit_ns = g_wait_limit_ns.load();
+  *pp = p;
+  return PGD_OK;
+}
+
+pgd_status pgd_mla_append(const void *c_new, void *cache, const int32_t *block_tables,
+                          const int32_t *positions, int32_t B, int32_t d, int32_t bs, int32_t MB,
+                          int32_t NB, void *stream) {
+  pgd_status s = check_mla_append(c_new, cache, block_tables, positions, B, d, bs, MB, NB);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  int32_t *err = nullptr;
+  s = error_word(&err);
+  if (s != PGD_OK) return s;
+  cudaError_t e = mla_append_launch(c_new, cache, block_tables, positions, 0, B, bs, MB, NB, err,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "MLA append launch");
+  return ok();
+}
+
+pgd_status pgd_mla_decode_attention(void *out, const void *q, const void *cache,
+                                    const int32_t *block_tables, const int32_t *context_lens,
+                                    int32_t B, int32_t H, int32_t d, int32_t dv, int32_t bs,
+                                    int32_t MB, int32_t NB, float scale, int32_t num_splits,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+  MlaParams p;
+  pgd_status s = mla_prepare(out, q, cache, block_tables, context_lens, B, H, d, dv, bs, MB, NB,
+                             scale, num_splits, workspace, workspace_bytes, &p);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
   cudaError_t e = mla_attention_launch(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "MLA attention launch");
+  return ok();
+}
+
+pgd_status pgd_mla_append_decode_attention(void *out, const void *q, const void *c_new,
+                                           void *cache, const int32_t *block_tables,
+                                           const int32_t *context_lens, int32_t B, int32_t H,
+                                           int32_t d, int32_t dv, int32_t bs, int32_t MB,
+                                           int32_t NB, float scale, int32_t num_splits,
+                                           void *workspace, size_t workspace_bytes,
+                                           void *stream) {
+  pgd_status s = check_mla_append(c_new, cache, block_tables, context_lens, B, d, bs, MB, NB);
+  if (s != PGD_OK) return s;
+  MlaParams p;
+  s = mla_prepare(out, q, cache, block_tables, context_lens, B, H, d, dv, bs, MB, NB, scale,
+                  num_splits, workspace, workspace_bytes, &p);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  // the append at context_lens[b] - 1, then the attention, told that the
+  // kernel before it writes only the cache
+  cudaError_t e = mla_append_launch(c_new, cache, block_tables, context_lens, -1, B, bs, MB, NB,
+                                    p.err, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "MLA append launch");
+  p.wait_late = 1;
+  e = mla_attention_launch(p, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "MLA attention launch");
   return ok();
 }

@@ -202,7 +202,11 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   static_assert((TOKS % BS == 0 || BS % TOKS == 0) && BS % 8 == 0, "block size");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_wait();  // q, the cache and the tables may come from the previous kernel
+  // Launched with programmatic stream serialization.  Unless the previous
+  // kernel is this library's latent append, which writes only the cache (the
+  // producer then waits for it before its first copy), wait for it now: q,
+  // the cache and the tables may come from it.
+  if (!p.wait_late) pdl_wait();
 
   int w = (int)blockIdx.x;
   const int part = w % p.n_parts;
@@ -289,6 +293,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
 
   if (warp == WARP_PROD) {
     // ------------------------------------------------------------ producer
+    if (p.wait_late == 1) pdl_wait();  // the latent append has written the cache
     const uint64_t policy = l2_policy_evict_first();
     int armed = 0;  // stages armed; after a timeout in the CTA nothing more is
     for (int i = 0; i < nst; ++i) {
@@ -622,12 +627,12 @@ __global__ void __launch_bounds__(128) mla_combine_kernel(const MlaParams p) {
 // into the block's tile).  A bit copy.
 __global__ void __launch_bounds__(128)
 mla_append_kernel(const uint4 *__restrict__ c_new, uint4 *__restrict__ cache,
-                  const int32_t *__restrict__ tables, const int32_t *__restrict__ pos, int B,
-                  int bs, int MB, int NB, int32_t *err) {
+                  const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
+                  int pos_offset, int B, int bs, int MB, int NB, int32_t *err) {
   pdl_launch_dependents();
   const int b = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (b >= B) return;
-  const int pp = __ldg(pos + b);
+  const int pp = __ldg(pos + b) + pos_offset;  // (pos_offset -1: pos are context lengths)
   if (pp < 0 || pp >= MB * bs) {
     if (lane == 0) atomicOr(err, PGD_DEVERR_BAD_POSITION);
     return;
@@ -696,12 +701,12 @@ cudaError_t mla_attention_launch(const MlaParams &p, cudaStream_t stream) {
 }
 
 cudaError_t mla_append_launch(const void *c_new, void *cache, const int32_t *tables,
-                              const int32_t *pos, int B, int bs, int MB, int NB, int32_t *err,
-                              cudaStream_t stream) {
+                              const int32_t *pos, int pos_offset, int B, int bs, int MB, int NB,
+                              int32_t *err, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
   mla::mla_append_kernel<<<(B + 3) / 4, 128, 0, stream>>>(
-      static_cast<const uint4 *>(c_new), static_cast<uint4 *>(cache), tables, pos, B, bs, MB, NB,
-      err);
+      static_cast<const uint4 *>(c_new), static_cast<uint4 *>(cache), tables, pos, pos_offset, B,
+      bs, MB, NB, err);
   return cudaGetLastError();
 }
 

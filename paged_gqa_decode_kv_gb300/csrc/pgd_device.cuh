@@ -219,6 +219,9 @@ struct MlaParams {
   const int32_t *ctx;            // [B]
   int B, H, MB, NB, bs;
   int n_parts;                   // parts of each sequence's context (1: no merge)
+  int wait_late;                 // 1: the previous kernel is this library's latent append,
+                                 //    which writes only the cache: wait for it just before
+                                 //    the first cache read
   float qk_scale_log2;           // scale * log2(e)
   float *part_ml;                // [B][H][n_parts][2] partial (max, sum), log2 domain
   float *part_o;                 // [B][H][n_parts][512] unnormalised partial outputs

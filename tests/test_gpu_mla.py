@@ -114,3 +114,60 @@ def test_mla_rescale_mid_context():
     for splits in (0, 1, 2):
         got, want, _ = _run(mb, splits)
         compare(got, want, "mla rescale splits=%d" % splits)
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 3])
+def test_mla_append_decode_attention_one_call(num_splits):
+    """The one-call step (append at context_lens - 1, then attention): the
+    pool bit exact with the oracle's own append, the output within tolerance
+    of the oracle over it."""
+    lens = [1, 64, 65, 700, 2500]
+    mb = inputs.make_mla_batch(len(lens), 128, 32, lens, append=True, device="cuda", seed=44,
+                               table_seed=45)
+    pool = oracle.mla_append(mb.cache.cpu(), mb.c_new.cpu(), mb.block_tables.cpu(),
+                             mb.positions.cpu())
+    want = oracle.mla_attention(mb.q.cpu(), pool, mb.block_tables.cpu(), mb.context_lens.cpu(),
+                                mb.scale)
+    got = pgd.mla_append_decode_attention(None, mb.q, mb.c_new, mb.cache, mb.block_tables,
+                                          mb.context_lens, mb.scale, num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(mb.cache), pool)
+    compare(got, want, "mla append+attend splits=%d" % num_splits)
+
+
+def test_mla_steps_back_to_back():
+    """Six one-call steps on one stream with a growing context (each
+    attention's prologue overlapping the append before it): every step sees
+    its own append."""
+    base, steps = [300, 63, 1500], 6
+    mb = inputs.make_mla_batch(3, 64, 64, [n + steps for n in base], append=True, device="cuda",
+                               seed=46, table_seed=47)
+    g = torch.Generator().manual_seed(48)
+    rows = [torch.randn(3, 576, generator=g).to(torch.bfloat16) for _ in range(steps)]
+    pool = _bits(mb.cache)
+    ws = torch.empty(pgd.mla_workspace_size(3, 64, 0), dtype=torch.uint8, device="cuda")
+    outs, wants = [], []
+    for i in range(steps):
+        lens = torch.tensor([n + i + 1 for n in base], dtype=torch.int32)
+        outs.append(pgd.mla_append_decode_attention(None, mb.q, rows[i].cuda(), mb.cache,
+                                                    mb.block_tables, lens.cuda(), mb.scale,
+                                                    workspace=ws))
+        pool = oracle.mla_append(pool, rows[i], mb.block_tables.cpu(), lens - 1)
+        wants.append(oracle.mla_attention(mb.q.cpu(), pool, mb.block_tables.cpu(), lens,
+                                          mb.scale))
+    torch.cuda.synchronize()
+    for i in range(steps):
+        compare(outs[i], wants[i], "step %d" % i)
+    assert np.array_equal(_bits(mb.cache), pool)
+
+
+@pytest.mark.parametrize("H", [64, 128])
+def test_mla_long_ragged_sequences(H):
+    """Few long sequences of different lengths under the automatic split:
+    every sequence is cut into the same number of parts, of different
+    lengths, merged by the combine kernel."""
+    lens = [9000, 5000, 3000, 257]
+    mb = inputs.make_mla_batch(len(lens), H, 64, lens, append=True, device="cuda", seed=50,
+                               table_seed=51)
+    got, want, _ = _run(mb)
+    compare(got, want, "mla long ragged H=%d" % H)
