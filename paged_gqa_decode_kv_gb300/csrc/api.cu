@@ -258,6 +258,7 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   p.qk_scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
   p.counters = reinterpret_cast<int32_t *>(ws + L.counters);
   p.auto_split = num_splits == 0 ? 1 : 0;
+  p.prefetch_units = (num_splits == 0 && (long long)B * n_kv <= grid) ? 1 : 0;
   p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
   p.part_o = reinterpret_cast<float *>(ws + L.part_o);
   p.err = err;
@@ -656,6 +657,7 @@ pgd_status pgd_cascade_decode_attention(
     const int sms = sm_count();
     pa.grid = std::max(std::min(pa.grid, sms - grid), std::max(1, sms / 2));
   }
+  pa.p.prefetch_units = (num_splits == 0 && (long long)B * n_kv <= pa.grid) ? 1 : 0;
   s = launch_prepared(pa, st);
   if (s != PGD_OK) return s;
   // 3. combine: suffix and prefix parts of every unit with a shared prefix

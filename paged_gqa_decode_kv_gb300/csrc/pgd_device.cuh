@@ -108,6 +108,12 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (src 16-byte aligned, bytes a
+// multiple of 16); a hint, with no completion to wait for.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch.  launch_dependents lets the next kernel of
 // the stream (launched with programmatic stream serialization) start its
 // prologue; wait blocks until every kernel this one depends on has completed
@@ -158,6 +164,9 @@ struct AttnParams {
   float *part_ml;                // [slots][G][2]  partial (max, sum), log2 domain
   int32_t *counters;             // [B * n_kv]     arrivals per split unit
   int auto_split;                // 1: whole units or balanced cuts, chosen per call
+  int prefetch_units;            // 1: no more units than CTAs (automatic split): CTA c most
+                                 //    likely streams unit c from its first block, whose first
+                                 //    stages it asks L2 for during the prologue
   int wait_late;                 // 1: the previous kernel wrote only the caches (kv_append):
                                  //    wait for it just before the first cache read;
                                  // 2: it is a cascade's shared-prefix pass, independent of
