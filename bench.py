@@ -594,7 +594,12 @@ def run_ours(args, rank, world, local):
     else:
         ws = pgd.make_workspace(B, n_q, n_kv, args.splits, dev)
     out = torch.empty_like(pb.q)
-    grid = pgd.attention_grid(B, n_q, n_kv, pb.block_size, args.splits)
+    # Short contexts (every context within 1024 tokens, at most 128 units)
+    # run the short-context kernel: one launch, the append fused.
+    short = (not args.cascade and not T and not fp8 and
+             pgd.uses_short_path(B, n_kv, pb.block_tables.shape[1], pb.block_size, args.splits))
+    grid = (8 * B * n_kv) if short else pgd.attention_grid(B, n_q, n_kv, pb.block_size,
+                                                            args.splits)
     stream = torch.cuda.current_stream()
     # Headline bytes: each physical block once (equal to the logical bytes
     # unless sequences share prefix blocks, whose re-reads may hit L2).
@@ -610,13 +615,36 @@ def run_ours(args, rank, world, local):
         it[0] += 1
         return kc, vc
 
+    # The plain decode paths time prepared C-ABI calls (arguments checked and
+    # marshalled once per pool copy): the Python side of a regular binding
+    # call costs about 10 us, more than a short-context step on the GPU.
+    prepared = not args.cascade and not T
+    if prepared:
+        op = "_fp8" if fp8 else ""
+        step_calls = [pgd.prepare("append_decode_attention" + op, out, pb.q, pb.k_new, pb.v_new,
+                                  kc, vc, pb.block_tables, pb.context_lens, pb.scale,
+                                  num_splits=args.splits, workspace=ws, stream=stream)
+                      for kc, vc in pools]
+        attn_calls = [pgd.prepare("paged_decode_attention" + op, out, pb.q, kc, vc,
+                                  pb.block_tables, pb.context_lens, pb.scale,
+                                  num_splits=args.splits, workspace=ws, stream=stream)
+                      for kc, vc in pools]
+
     def step():
-        # kv_append at context_lens - 1, then attention: one C-ABI call, two kernels
+        # kv_append at context_lens - 1, then attention: one C-ABI call
+        if prepared:
+            step_calls[it[0] % n_pools]()
+            it[0] += 1
+            return
         kc, vc = next_pool()
         append_attend(out, pb.q, pb.k_new, pb.v_new, kc, vc, pb.block_tables, pb.context_lens,
                       pb.scale, num_splits=args.splits, workspace=ws, stream=stream)
 
     def attention_only():
+        if prepared:
+            attn_calls[it[0] % n_pools]()
+            it[0] += 1
+            return
         kc, vc = next_pool()
         attend(out, pb.q, kc, vc, pb.block_tables, pb.context_lens, pb.scale,
                num_splits=args.splits, workspace=ws, stream=stream)
@@ -682,7 +710,16 @@ def run_ours(args, rank, world, local):
     cl_d = torch.empty_like(pb.context_lens)
     out_d = torch.empty_like(pb.q)
 
+    if prepared:
+        e2e_calls = [pgd.prepare("decode_step", out_h, q_h, kn_h, vn_h, cl_h, out_d, q_d, kn_d,
+                                 vn_d, cl_d, kc, vc, pb.block_tables, pb.scale, args.splits, ws,
+                                 stream=stream) for kc, vc in pools]
+
     def e2e_step():
+        if prepared:
+            e2e_calls[it[0] % n_pools]()
+            it[0] += 1
+            return
         kc, vc = next_pool()
         if T:  # host buffers through the Python binding: H2D, append + verify, D2H
             with torch.cuda.stream(stream):
@@ -720,6 +757,9 @@ def run_ours(args, rank, world, local):
         kc0, vc0 = pools[0]
 
         def hot_step():
+            if prepared:
+                step_calls[0]()
+                return
             append_attend(out, pb.q, pb.k_new, pb.v_new, kc0, vc0, pb.block_tables,
                           pb.context_lens, pb.scale, num_splits=args.splits, workspace=ws,
                           stream=stream)
@@ -778,6 +818,8 @@ def run_ours(args, rank, world, local):
                                if args.cascade else
                                ("pgd::tc::paged_attention_kernel<%d rows, bs, bf16> (tcgen05, "
                                 "multi-query verify)" % (T * (n_q // n_kv))) if T else
+                               ("pgd::sc::short_attention_kernel<G, bs> (short contexts: CUDA "
+                                "cores, cluster log-sum-exp merge; latency-bound)") if short else
                                "pgd::tc::paged_attention_kernel<G, bs, %s> (tcgen05)"
                                % ("fp8" if fp8 else "bf16"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
@@ -794,8 +836,11 @@ def run_ours(args, rank, world, local):
                        {"path": "pinned host buffers copied on the stream, pgd_kv_append_tokens "
                                 "+ pgd_paged_verify_attention, output copied back"}
                        if T else {})),
-        # kv_append + attention (cascade: + the prefix pass and the combine)
-        "gpu_launches": (4 if args.cascade else 2) * K,
+        # kv_append + attention (cascade: + the prefix pass and the combine;
+        # the short-context kernel appends in the same launch)
+        "gpu_launches": (4 if args.cascade else 1 if short else 2) * K,
+        "host_call": ("prepared C-ABI call (pgd.prepare: arguments checked and marshalled once "
+                      "per pool copy)") if prepared else "Python binding call per step",
         "clocks": clocks_record(sampler, nvml, t_wall0, t_wall1, t_timed0, t_timed1),
         "gpu": torch.cuda.get_device_name(local),
     }

@@ -153,7 +153,9 @@ pgd_status pgd_paged_decode_attention(void *out, const void *q, const void *k_ca
                                       void *workspace, size_t workspace_bytes, void *stream);
 
 /* Number of CTAs one pgd_paged_decode_attention call launches with these
- * arguments on the current device (0 on invalid arguments). */
+ * arguments on the current device when it runs the tensor-core kernel (0 on
+ * invalid arguments); a call routed to the short-context kernel (see
+ * pgd_set_short_context_tokens) launches 8 * B * n_kv. */
 int32_t pgd_attention_grid(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int32_t num_splits);
 
 /* Size of the library's own device scratch array used by
@@ -492,6 +494,28 @@ pgd_status pgd_read_stream(const void *src, size_t bytes, int32_t mode, void *st
  * force.  No counterpart on the pages. */
 void pgd_set_wait_limit_ns(uint64_t ns);
 uint64_t pgd_wait_limit_ns(void);
+
+/* ---------------------------------------------------------------------- */
+/* short-context path                                                     */
+/* ---------------------------------------------------------------------- */
+/* A call of pgd_paged_decode_attention, pgd_append_decode_attention,
+ * pgd_decode_step or pgd_paged_decode_attention_noalloc with num_splits = 0
+ * whose every possible context is short -- MB * bs at most the limit below,
+ * itself at most 1024 -- and that has at most 128 (sequence, KV head) units
+ * runs a latency-first kernel instead of the tensor-core one: such a call is
+ * bound by the start-up of a kernel, not by its bytes.  One cluster of 8
+ * CTAs per unit, each taking an eighth of the context; q.k and p.v on the
+ * CUDA cores in fp32 (exact exp2); the eight (max, sum, output) states merged
+ * by log-sum-exp through distributed shared memory ("The math of Transformer
+ * inference", section 8); for the append variants the new token's K/V are
+ * written by the same launch, bit for bit as pgd_kv_append writes them.  The
+ * results, errors and rules are those of the documented calls; the workspace
+ * is checked but not touched.  The limit is 1024 tokens;
+ * pgd_set_short_context_tokens sets it process-wide for the calls made after
+ * it (0 sends every call to the tensor-core kernel, a negative value restores
+ * 1024) and returns the previous limit.  Thread-safe.  No counterpart on the
+ * pages: a choice between two kernels for the same operation. */
+int32_t pgd_set_short_context_tokens(int32_t max_tokens);
 
 /* ---------------------------------------------------------------------- */
 /* device error word                                                      */

@@ -15,7 +15,8 @@ from ._native import (  # noqa: F401
     verify_workspace_size, mla_append, mla_decode_attention, mla_append_decode_attention,
     mla_workspace_size, device_errors,
     workspace_size, make_workspace, attention_grid, validate_tables, read_stream, set_wait_limit_ns,
-    wait_limit_ns, lib, library_path)
+    wait_limit_ns, set_short_context_tokens, uses_short_path, PreparedCall, prepare, lib,
+    library_path)
 
 __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload", "tile_pool",
            "untile_pool", "pool_shape", "pack_pool8", "unpack_pool8", "pool_shape8", "PGDError",
@@ -27,5 +28,6 @@ __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload",
            "mla_append", "mla_decode_attention", "mla_append_decode_attention",
            "mla_workspace_size",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
-           "validate_tables", "read_stream", "set_wait_limit_ns", "wait_limit_ns", "lib",
+           "validate_tables", "read_stream", "set_wait_limit_ns", "wait_limit_ns",
+           "set_short_context_tokens", "uses_short_path", "PreparedCall", "prepare", "lib",
            "library_path"]

@@ -65,6 +65,7 @@ SIGNATURES = {
     "pgd_read_stream": ([_P, _Z, _I, _P], _I),
     "pgd_set_wait_limit_ns": ([ctypes.c_uint64], None),
     "pgd_wait_limit_ns": ([], ctypes.c_uint64),
+    "pgd_set_short_context_tokens": ([_I], _I),
     "pgd_alloc_create": ([_I, _P], _I),
     "pgd_alloc_destroy": ([_P], None),
     "pgd_alloc_allocate": ([_P, _I, _P], _I),
@@ -173,26 +174,35 @@ def attention_grid(B: int, n_q: int, n_kv: int, bs: int, num_splits: int = 0) ->
     return int(lib().pgd_attention_grid(B, n_q, n_kv, bs, num_splits))
 
 
-def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
-                           num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
-                           stream=None) -> torch.Tensor:
-    """out[B][n_q][d] (bf16) = paged decode attention of q over the cache."""
-    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-        _need(t, torch.bfloat16, n)
+def _attention_call(fp8, out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                    num_splits=0, workspace=None, stream=None):
+    _need(q, torch.bfloat16, "q")
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.uint8 if fp8 else torch.bfloat16, n)
     _need(block_tables, torch.int32, "block_tables")
     _need(context_lens, torch.int32, "context_lens")
     B, n_q, d = q.shape
-    NB, n_kv, bs, d2 = _cache_dims(k_cache)
+    NB, n_kv, bs, _ = _cache8_dims(k_cache) if fp8 else _cache_dims(k_cache)
     if out is None:
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out")
     if workspace is None:
         workspace = make_workspace(B, n_q, n_kv, num_splits, q.device)
     MB = block_tables.shape[1]
-    _check(lib().pgd_paged_decode_attention(
+    name = "pgd_paged_decode_attention_fp8" if fp8 else "pgd_paged_decode_attention"
+    return name, (
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         B, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+        workspace.numel() * workspace.element_size(), _stream(stream)), out
+
+
+def paged_decode_attention(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                           num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """out[B][n_q][d] (bf16) = paged decode attention of q over the cache."""
+    name, args, out = _attention_call(False, out, q, k_cache, v_cache, block_tables,
+                                      context_lens, scale, num_splits, workspace, stream)
+    _check(getattr(lib(), name)(*args))
     return out
 
 
@@ -215,31 +225,61 @@ def paged_decode_attention_noalloc(out, q, k_cache, v_cache, block_tables, conte
     return out
 
 
-def append_decode_attention(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
-                            scale: float, num_splits: int = 0,
-                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """kv_append of k_new/v_new at context_lens - 1, then paged decode
-    attention over the updated cache (one call, two kernels; the attention
-    prologue overlaps the append)."""
-    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"),
-                 (v_cache, "v_cache")):
+def _append_attention_call(fp8, out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                           context_lens, scale, num_splits=0, workspace=None, stream=None):
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
         _need(t, torch.bfloat16, n)
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _need(t, torch.uint8 if fp8 else torch.bfloat16, n)
     _need(block_tables, torch.int32, "block_tables")
     _need(context_lens, torch.int32, "context_lens")
     B, n_q, d = q.shape
-    NB, n_kv, bs, _ = _cache_dims(k_cache)
+    NB, n_kv, bs, _ = _cache8_dims(k_cache) if fp8 else _cache_dims(k_cache)
     if out is None:
         out = torch.empty_like(q)
     _need(out, torch.bfloat16, "out")
     if workspace is None:
         workspace = make_workspace(B, n_q, n_kv, num_splits, q.device)
     MB = block_tables.shape[1]
-    _check(lib().pgd_append_decode_attention(
+    name = "pgd_append_decode_attention_fp8" if fp8 else "pgd_append_decode_attention"
+    return name, (
         _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), _ptr(context_lens), B, n_q, n_kv, d, bs, MB, NB, float(scale),
         int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+        _stream(stream)), out
+
+
+def append_decode_attention(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                            scale: float, num_splits: int = 0,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """kv_append of k_new/v_new at context_lens - 1, then paged decode
+    attention over the updated cache (one call; two kernels, the attention
+    prologue overlapping the append, or one short-context kernel that
+    appends itself)."""
+    name, args, out = _append_attention_call(False, out, q, k_new, v_new, k_cache, v_cache,
+                                             block_tables, context_lens, scale, num_splits,
+                                             workspace, stream)
+    _check(getattr(lib(), name)(*args))
     return out
+
+
+def _decode_step_call(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d,
+                      v_new_d, context_lens_d, k_cache, v_cache, block_tables, scale, num_splits,
+                      workspace, stream=None):
+    for t, n in ((out_h, "out_h"), (q_h, "q_h"), (k_new_h, "k_new_h"), (v_new_h, "v_new_h")):
+        _need(t, torch.bfloat16, n, cuda=False)
+    _need(context_lens_h, torch.int32, "context_lens_h", cuda=False)
+    B, n_q, d = q_h.shape
+    fp8 = k_cache.dtype == torch.uint8
+    NB, n_kv, bs, _ = _cache8_dims(k_cache) if fp8 else _cache_dims(k_cache)
+    MB = block_tables.shape[1]
+    name = "pgd_decode_step_fp8" if fp8 else "pgd_decode_step"
+    return name, (
+        _ptr(out_h), _ptr(q_h), _ptr(k_new_h), _ptr(v_new_h), _ptr(context_lens_h), _ptr(out_d),
+        _ptr(q_d), _ptr(k_new_d), _ptr(v_new_d), _ptr(context_lens_d), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), B, n_q, n_kv, d, bs, MB, NB, float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), None
 
 
 def decode_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d, v_new_d,
@@ -250,20 +290,51 @@ def decode_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_
     read and written in place by the kernels; pageable ones go through the
     given device tensors and a copy each.  An 8-bit pool (uint8) selects the
     FP8 path."""
-    for t, n in ((out_h, "out_h"), (q_h, "q_h"), (k_new_h, "k_new_h"), (v_new_h, "v_new_h")):
-        _need(t, torch.bfloat16, n, cuda=False)
-    _need(context_lens_h, torch.int32, "context_lens_h", cuda=False)
-    B, n_q, d = q_h.shape
-    fp8 = k_cache.dtype == torch.uint8
-    NB, n_kv, bs, _ = _cache8_dims(k_cache) if fp8 else _cache_dims(k_cache)
-    MB = block_tables.shape[1]
-    fn = lib().pgd_decode_step_fp8 if fp8 else lib().pgd_decode_step
-    _check(fn(
-        _ptr(out_h), _ptr(q_h), _ptr(k_new_h), _ptr(v_new_h), _ptr(context_lens_h), _ptr(out_d),
-        _ptr(q_d), _ptr(k_new_d), _ptr(v_new_d), _ptr(context_lens_d), _ptr(k_cache),
-        _ptr(v_cache), _ptr(block_tables), B, n_q, n_kv, d, bs, MB, NB, float(scale),
-        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+    name, args, _ = _decode_step_call(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d,
+                                      k_new_d, v_new_d, context_lens_d, k_cache, v_cache,
+                                      block_tables, scale, num_splits, workspace, stream)
+    _check(getattr(lib(), name)(*args))
+
+
+class PreparedCall:
+    """One C-ABI call whose arguments were checked and marshalled once;
+    calling the object enqueues the same call again (same buffers, same
+    stream) and returns its output tensor.  The Python side of a regular
+    binding call -- a dozen tensor checks and pointer conversions -- takes
+    about 10 us, longer than a short-context decode step on the GPU; a
+    prepared call leaves only the C call (a few us).  The buffers must stay
+    alive and unchanged in shape while the object is used."""
+    __slots__ = ("name", "_fn", "_args", "out")
+
+    def __init__(self, name: str, args: tuple, out=None):
+        self.name = name
+        self._fn = getattr(lib(), name)
+        self._args = args
+        self.out = out
+
+    def __call__(self):
+        s = self._fn(*self._args)
+        if s != OK:
+            _check(s)
+        return self.out
+
+
+def prepare(op: str, *args, **kwargs) -> PreparedCall:
+    """A PreparedCall of one of the step calls, with the arguments that call
+    takes: "paged_decode_attention", "paged_decode_attention_fp8",
+    "append_decode_attention", "append_decode_attention_fp8" or
+    "decode_step"."""
+    if op == "paged_decode_attention":
+        return PreparedCall(*_attention_call(False, *args, **kwargs))
+    if op == "paged_decode_attention_fp8":
+        return PreparedCall(*_attention_call(True, *args, **kwargs))
+    if op == "append_decode_attention":
+        return PreparedCall(*_append_attention_call(False, *args, **kwargs))
+    if op == "append_decode_attention_fp8":
+        return PreparedCall(*_append_attention_call(True, *args, **kwargs))
+    if op == "decode_step":
+        return PreparedCall(*_decode_step_call(*args, **kwargs))
+    raise ValueError("no prepared form of %r" % op)
 
 
 # ---------------------------------------------------------------- cascade
@@ -455,23 +526,9 @@ def paged_decode_attention_fp8(out, q, k_cache, v_cache, block_tables, context_l
                                workspace: Optional[torch.Tensor] = None,
                                stream=None) -> torch.Tensor:
     """out[B][n_q][d] (bf16) = paged decode attention of q over the 8-bit cache."""
-    _need(q, torch.bfloat16, "q")
-    _need(k_cache, torch.uint8, "k_cache")
-    _need(v_cache, torch.uint8, "v_cache")
-    _need(block_tables, torch.int32, "block_tables")
-    _need(context_lens, torch.int32, "context_lens")
-    B, n_q, d = q.shape
-    NB, n_kv, bs, _ = _cache8_dims(k_cache)
-    if out is None:
-        out = torch.empty_like(q)
-    _need(out, torch.bfloat16, "out")
-    if workspace is None:
-        workspace = make_workspace(B, n_q, n_kv, num_splits, q.device)
-    MB = block_tables.shape[1]
-    _check(lib().pgd_paged_decode_attention_fp8(
-        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
-        B, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _stream(stream)))
+    name, args, out = _attention_call(True, out, q, k_cache, v_cache, block_tables, context_lens,
+                                      scale, num_splits, workspace, stream)
+    _check(getattr(lib(), name)(*args))
     return out
 
 
@@ -480,25 +537,10 @@ def append_decode_attention_fp8(out, q, k_new, v_new, k_cache, v_cache, block_ta
                                 workspace: Optional[torch.Tensor] = None,
                                 stream=None) -> torch.Tensor:
     """kv_append_fp8 at context_lens - 1, then attention over the 8-bit cache."""
-    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new")):
-        _need(t, torch.bfloat16, n)
-    _need(k_cache, torch.uint8, "k_cache")
-    _need(v_cache, torch.uint8, "v_cache")
-    _need(block_tables, torch.int32, "block_tables")
-    _need(context_lens, torch.int32, "context_lens")
-    B, n_q, d = q.shape
-    NB, n_kv, bs, _ = _cache8_dims(k_cache)
-    if out is None:
-        out = torch.empty_like(q)
-    _need(out, torch.bfloat16, "out")
-    if workspace is None:
-        workspace = make_workspace(B, n_q, n_kv, num_splits, q.device)
-    MB = block_tables.shape[1]
-    _check(lib().pgd_append_decode_attention_fp8(
-        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-        _ptr(block_tables), _ptr(context_lens), B, n_q, n_kv, d, bs, MB, NB, float(scale),
-        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _stream(stream)))
+    name, args, out = _append_attention_call(True, out, q, k_new, v_new, k_cache, v_cache,
+                                             block_tables, context_lens, scale, num_splits,
+                                             workspace, stream)
+    _check(getattr(lib(), name)(*args))
     return out
 
 
@@ -539,6 +581,24 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def wait_limit_ns() -> int:
     return int(lib().pgd_wait_limit_ns())
+
+
+SHORT_MAX_UNITS = 128     # (sequence, KV head) units the short-context kernel takes at most
+
+
+def set_short_context_tokens(max_tokens: int) -> int:
+    """Largest MB * bs (at most 1024) for which an automatic single-query
+    bf16 call runs the short-context kernel (0: never; negative: the default
+    1024).  Returns the previous limit."""
+    return int(lib().pgd_set_short_context_tokens(int(max_tokens)))
+
+
+def uses_short_path(B: int, n_kv: int, MB: int, bs: int, num_splits: int = 0,
+                    limit: int = 1024) -> bool:
+    """Whether a call with these sizes runs the short-context kernel under
+    the given limit (the rule of pgd_set_short_context_tokens)."""
+    return (num_splits == 0 and B * n_kv <= SHORT_MAX_UNITS
+            and MB * bs <= min(limit, 1024))
 
 
 # ------------------------------------------------------------ host allocator

@@ -43,6 +43,9 @@ cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src_
                                int32_t *err, cudaStream_t stream);
 cudaError_t read_stream_launch(const void *src, size_t bytes, int mode, int32_t *err,
                                cudaStream_t stream);
+cudaError_t short_attention_launch(const ShortParams &p, int G, int bs, cudaStream_t stream);
+int short_max_tokens();
+int short_max_units();
 void set_error_detail(const char *msg);
 void clear_error_detail();
 const char *error_detail();
@@ -76,6 +79,9 @@ pgd_status ok() {
 // Wait limit handed to every launch (0: the kernels' default); set only by
 // pgd_set_wait_limit_ns, for tests of the timeout exit.
 std::atomic<unsigned long long> g_wait_limit_ns{0};
+
+// Largest MB * bs routed to the short-context kernel (pgd_set_short_context_tokens).
+std::atomic<int> g_short_tokens{1024};
 
 pgd_status cuda_fail(cudaError_t e, const char *what) {
   return fail(PGD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -277,6 +283,41 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   return PGD_OK;
 }
 
+// Whether an automatic single-query bf16 call goes to the short-context
+// kernel: every context it can hold (MB * bs tokens) is within the limit, and
+// its (sequence, KV head) units fit one wave of clusters.
+bool short_path(const PreparedAttention &pa, int32_t num_splits, int32_t MB, int32_t bs) {
+  const long long tokens = (long long)MB * bs;
+  return !pa.fp8 && pa.p.T == 1 && num_splits == 0 &&
+         (long long)pa.p.B * pa.p.n_kv <= short_max_units() &&
+         tokens <= std::min(g_short_tokens.load(), short_max_tokens());
+}
+
+// The short-context kernel on a prepared call's arguments; with k_new and
+// v_new it appends the new token first, in the same launch.
+pgd_status launch_short(const PreparedAttention &pa, const void *k_new, const void *v_new,
+                        void *k_cache, void *v_cache, cudaStream_t stream) {
+  ShortParams sp;
+  sp.out = pa.p.out;
+  sp.q = pa.p.q;
+  sp.k_cache = static_cast<unsigned char *>(k_cache);
+  sp.v_cache = static_cast<unsigned char *>(v_cache);
+  sp.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+  sp.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+  sp.tables = pa.p.tables;
+  sp.ctx = pa.p.ctx;
+  sp.B = pa.p.B;
+  sp.n_q = pa.p.n_q;
+  sp.n_kv = pa.p.n_kv;
+  sp.MB = pa.p.MB;
+  sp.NB = pa.p.NB;
+  sp.qk_scale_log2 = pa.p.qk_scale_log2;
+  sp.err = pa.p.err;
+  cudaError_t e = short_attention_launch(sp, pa.G, pa.bs, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "short-context attention launch");
+  return PGD_OK;
+}
+
 pgd_status launch_prepared(const PreparedAttention &pa, cudaStream_t stream) {
   cudaError_t e = pa.fp8 ? attention_launch_fp8(pa.p, pa.G, pa.bs, pa.grid, stream)
                          : attention_launch(pa.p, pa.G, pa.bs, pa.grid, stream);
@@ -293,6 +334,9 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
   pgd_status s = prepare_attention(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, bs, MB,
                                    NB, scale, num_splits, workspace, workspace_bytes, &pa);
   if (s != PGD_OK) return s;
+  if (short_path(pa, num_splits, MB, bs))
+    return launch_short(pa, nullptr, nullptr, const_cast<void *>(k_cache),
+                        const_cast<void *>(v_cache), stream);
   return launch_prepared(pa, stream);
 }
 
@@ -314,6 +358,8 @@ pgd_status append_then_attend(void *out, const void *q, const void *k_new, const
   pgd_status s = prepare_attention(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, bs, MB,
                                    NB, scale, num_splits, workspace, workspace_bytes, &pa, fp8);
   if (s != PGD_OK) return s;
+  if (short_path(pa, num_splits, MB, bs))  // one launch: the append is fused
+    return launch_short(pa, k_new, v_new, k_cache, v_cache, stream);
   cudaError_t e = fp8 ? kv_append_fp8_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B,
                                              n_kv, bs, MB, NB, pa.p.err, stream)
                       : kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B, 1,
@@ -1015,6 +1061,10 @@ pgd_status pgd_read_stream(const void *src, size_t bytes, int32_t mode, void *st
 }
 
 void pgd_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store((unsigned long long)ns); }
+
+int32_t pgd_set_short_context_tokens(int32_t max_tokens) {
+  return g_short_tokens.exchange(max_tokens < 0 ? 1024 : max_tokens);
+}
 
 uint64_t pgd_wait_limit_ns(void) {
   const unsigned long long v = g_wait_limit_ns.load();

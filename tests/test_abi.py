@@ -159,3 +159,14 @@ def test_wait_limit_setting(L):
     finally:
         pgd.set_wait_limit_ns(0)
     assert pgd.wait_limit_ns() == 4_000_000_000
+
+
+def test_short_context_setting(L):
+    prev = pgd.set_short_context_tokens(256)
+    try:
+        assert prev == 1024
+        assert pgd.set_short_context_tokens(0) == 256
+    finally:
+        pgd.set_short_context_tokens(-1)
+    assert pgd.set_short_context_tokens(-1) == 1024
+    assert pgd.uses_short_path(16, 8, 64, 16) and not pgd.uses_short_path(17, 8, 64, 16)
