@@ -155,6 +155,18 @@ __device__ __forceinline__ void produce(const PrefixParams &p, const int32_t *tr
     if (ok)
       bulk_copy_g2s(ring + (size_t)slot * STAGE + (size_t)lane * TILE,
                     cache + ((size_t)blk * p.n_kv + g) * (size_t)TILE, TILE, &full[slot], policy);
+    // Later stages go to L2 now (stage st + 2 at the first stage, then
+    // st + 3 at each): a slot frees only after its stage's MMA, and the copy
+    // issued then finds its tiles on chip instead of paying the HBM latency
+    // that the concurrent suffix pass's traffic lengthens.
+    for (int ahead = (st == 0 ? 2 : 3); ahead <= 3; ++ahead) {
+      const int sp = st + ahead;
+      if (sp >= nst) break;
+      const int fp = sp * SB, nbp = min(SB, nblk - fp);
+      const int blkp = (lane < nbp) ? __ldg(trow + blk0 + fp + lane) : -1;
+      if ((unsigned)blkp < (unsigned)p.NB)
+        bulk_prefetch_l2(cache + ((size_t)blkp * p.n_kv + g) * (size_t)TILE, TILE);
+    }
   }
   // no copy may still be landing when the CTA exits (fixed limit)
   if (lane == 0) {
