@@ -75,6 +75,18 @@ constexpr int WARP_PROD = 8, WARP_QK = 9, WARP_PV = 10;
 constexpr int GRP = (D / 8) * 128;   // bytes per 8 rows of 576 values: 9216
 constexpr int STAGE = (TOKS / 8) * GRP;  // 73,728
 constexpr int Q_BYTES = (NH / 8) * GRP;  // 73,728
+// A stage lands in NR ranges of latent dims, each on its own barrier, so
+// that q.c^T starts on the first range while the second is still landing:
+// one bulk copy per (8-token group, range) of RCH 16-byte chunks.  (One
+// 72 KiB copy per stage lands in about 1 us; 32 copies of 2304 B took about
+// 2 us for the last range, so finer ranges lose what the overlap gains:
+// measured 86.8 us a step with one copy per block, 85.8 / 85.7 / 86.4 /
+// 87.8 us with 1 / 2 / 3 / 4 ranges per token group.)
+constexpr int NR = 2;
+constexpr int RCH = (D / 8) / NR;         // 36 chunks (288 dims) per range
+constexpr int RBYTES = RCH * 128;         // 4608 bytes of a token group per range
+constexpr int KPR = (D / 16) / NR;        // 18 q.c^T k-steps per range
+static_assert((D / 8) % NR == 0 && (D / 16) % NR == 0 && RBYTES % 16 == 0, "dim ranges");
 constexpr int P_RG = (TOKS / 8) * 128;   // bytes per 8 rows of P: 1024
 constexpr int P_BYTES = (NH / 8) * P_RG; // [8 row groups][8 token groups][8][16 B] = 8192
 // P, then Q, then the stage ring.
@@ -83,6 +95,7 @@ constexpr int OFF_Q = OFF_P + P_BYTES;
 constexpr int OFF_C = OFF_Q + Q_BYTES;
 constexpr int OFF_BAR = OFF_C + NSTG * STAGE;
 constexpr int OFF_MISC = OFF_BAR + 128;
+static_assert((NSTG * NR + 3 * NSTG + 3) * 8 <= OFF_MISC - OFF_BAR, "barrier area");
 constexpr int OFF_X = OFF_MISC + 64;  // f32 [2 parities][2 halves][64 rows] row maxima,
                                       // [2 halves][64 rows] row sums, [64 rows] rescale factors
 constexpr int SMEM_BYTES = 1024 + OFF_X + 7 * NH * 4;
@@ -243,16 +256,17 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
   unsigned char *smem = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
-  uint64_t *c_full = bars, *c_empty = bars + NSTG, *s_full = bars + 2 * NSTG;
-  uint64_t *s_free = bars + 3 * NSTG;
-  uint64_t *p_full = bars + 4 * NSTG, *p_free = p_full + 1, *o_done = p_full + 2;
+  // c_full[buf * NR + r]: range r of stage buffer buf has landed
+  uint64_t *c_full = bars, *c_empty = bars + NSTG * NR, *s_full = c_empty + NSTG;
+  uint64_t *s_free = s_full + NSTG;
+  uint64_t *p_full = s_free + NSTG, *p_free = p_full + 1, *o_done = p_full + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 16);  // WaitCtl
   volatile int *bad_mask = reinterpret_cast<volatile int *>(smem + OFF_MISC + 8);  // [NSTG]
 
   if (tid == 0) {
     for (int i = 0; i < NSTG; ++i) {
-      mbar_init(&c_full[i], 1);
+      for (int r = 0; r < NR; ++r) mbar_init(&c_full[i * NR + r], 1);
       mbar_init(&c_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 8);  // one arrival per softmax warp
@@ -300,11 +314,20 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       const int buf = i % NSTG;
       const uint32_t par = (uint32_t)(i / NSTG) & 1u;
       const int nb = (stage_tokens(i) + PB - 1) / PB;  // pieces with a valid token
-      const int t0 = (st0 + i) * TOKS + lane * PB;     // first token of this lane's piece
-      const int blk = (lane < nb) ? __ldg(trow + t0 / BS) : -1;
-      const bool ok = lane < nb && (unsigned)blk < (unsigned)p.NB;
+      const int ng = (stage_tokens(i) + 7) / 8;        // token groups with a valid token
+      // lane = r * 8 + tg: range r of token group tg (ranges in order, so
+      // that the first lands first; lanes past 8 NR idle)
+      const int tg = lane & 7, rr = lane >> 3;
+      const int t0 = (st0 + i) * TOKS + tg * 8;        // first token of this lane's group
+      const int blk = (tg < ng && rr < NR) ? __ldg(trow + t0 / BS) : -1;
+      const bool ok = rr < NR && tg < ng && (unsigned)blk < (unsigned)p.NB;
       const unsigned okmask = __ballot_sync(kFullMask, ok);
-      const unsigned want = (nb >= 32) ? ~0u : ((1u << nb) - 1u);
+      // bad-block mask by piece (bit j: tokens [j PB, (j + 1) PB) of the stage)
+      unsigned bad = 0;
+      for (int j = 0; j < nb; ++j) {
+        const int l0 = (j * PB) / 8;  // a group of piece j, range 0
+        if (!((okmask >> l0) & 1u)) bad |= 1u << j;
+      }
       // one decision for the warp: after a timeout the buffer's earlier copy
       // may still be landing, so it is neither armed again nor written
       int go = 1;
@@ -315,19 +338,21 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       if (!__shfl_sync(kFullMask, go, 0)) break;
       armed = i + 1;
       if (lane == 0) {
-        bad_mask[buf] = (int)(want & ~okmask);
-        if (want & ~okmask) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
-        const uint32_t bytes = (uint32_t)__popc(okmask) * PIECE;
-        if (bytes == 0)
-          mbar_arrive(&c_full[buf]);
-        else
-          mbar_arrive_expect_tx(&c_full[buf], bytes);
+        bad_mask[buf] = (int)bad;
+        if (bad) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
+        const uint32_t bytes = (uint32_t)__popc(okmask & 0xffu) * RBYTES;  // per range
+        for (int r = 0; r < NR; ++r) {
+          if (bytes == 0)
+            mbar_arrive(&c_full[buf * NR + r]);
+          else
+            mbar_arrive_expect_tx(&c_full[buf * NR + r], bytes);
+        }
       }
       __syncwarp();
       if (ok)
-        bulk_copy_g2s(smem + OFF_C + buf * STAGE + lane * (PB / 8) * GRP,
-                      p.cache + (size_t)blk * TILE + (size_t)((t0 % BS) / 8) * GRP, PIECE,
-                      &c_full[buf], policy);
+        bulk_copy_g2s(smem + OFF_C + buf * STAGE + tg * GRP + rr * RBYTES,
+                      p.cache + (size_t)blk * TILE + (size_t)((t0 % BS) / 8) * GRP + rr * RBYTES,
+                      RBYTES, &c_full[buf * NR + rr], policy);
       // The stage after next goes to L2 now: its buffer frees only after this
       // stage's p.c, and its copy then finds the data on chip.
       const int ip = i + NSTG;
@@ -342,8 +367,9 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
     if (lane == 0) {  // no copy may still be landing when the CTA exits
       for (int k = 1; k <= NSTG && k <= armed; ++k) {
         const int last = armed - k;
-        if (!mbar_wait_bounded(&c_full[last % NSTG], (uint32_t)(last / NSTG) & 1u))
-          atomicOr(p.err, PGD_DEVERR_TIMEOUT);
+        for (int r = 0; r < NR; ++r)
+          if (!mbar_wait_bounded(&c_full[(last % NSTG) * NR + r], (uint32_t)(last / NSTG) & 1u))
+            atomicOr(p.err, PGD_DEVERR_TIMEOUT);
       }
     }
   } else if (warp == WARP_QK) {
@@ -353,17 +379,21 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       for (int i = 0; i < nst; ++i) {
         const int buf = i % NSTG;
         const uint32_t par = (uint32_t)(i / NSTG) & 1u;
-        wait_or_abort(&c_full[buf], par, abort_flag, p.err);
         wait_or_abort(&s_free[buf], par ^ 1u, abort_flag, p.err);
-        tc_fence_after();
-        if (!*abort_flag) {
-          // A = Q, B = C, both K-major: a k-step of 16 dims moves both by
-          // two core matrices (256 B)
-          const uint64_t cd = smem_desc(smem_addr(smem + OFF_C + buf * STAGE), 128, GRP, 0);
-#pragma unroll 4
-          for (int kk = 0; kk < D / 16; ++kk)
-            umma_bf16(tmem + COL_S + (uint32_t)(buf * TOKS), qd + (uint64_t)(kk * 16),
-                      cd + (uint64_t)(kk * 16), IDESC_QK, kk > 0 ? 1u : 0u);
+        // A = Q, B = C, both K-major: a k-step of 16 dims moves both by two
+        // core matrices (256 B); range r's k-steps are issued once it landed
+        const uint64_t cd = smem_desc(smem_addr(smem + OFF_C + buf * STAGE), 128, GRP, 0);
+        for (int r = 0; r < NR; ++r) {
+          wait_or_abort(&c_full[buf * NR + r], par, abort_flag, p.err);
+          tc_fence_after();
+          if (!*abort_flag) {
+#pragma unroll
+            for (int k = 0; k < KPR; ++k) {
+              const int kk = r * KPR + k;
+              umma_bf16(tmem + COL_S + (uint32_t)(buf * TOKS), qd + (uint64_t)(kk * 16),
+                        cd + (uint64_t)(kk * 16), IDESC_QK, kk > 0 ? 1u : 0u);
+            }
+          }
         }
         umma_commit(&s_full[buf]);
       }
@@ -419,7 +449,7 @@ __global__ void __launch_bounds__(THREADS, 1) mla_attention_kernel(const MlaPara
       wait_or_abort(&s_full[buf], par, abort_flag, p.err);
       // (the producer wrote the stage's bad-block mask before arming c_full;
       // that phase has completed and cannot move on before this stage's p.c)
-      wait_or_abort(&c_full[buf], par, abort_flag, p.err);
+      for (int rg = 0; rg < NR; ++rg) wait_or_abort(&c_full[buf * NR + rg], par, abort_flag, p.err);
       const int bad = bad_mask[buf];
       tc_fence_after();
       float sv[TT];  // row r, tokens sh * 32 + tq * 16 + [0, 16)
