@@ -15,6 +15,7 @@
 #include <atomic>
 
 #include "pgd_device.cuh"
+#include "short_attention.cuh"
 
 namespace pgd {
 int attention_ctas_per_sm(int G, int bs, int B);
@@ -43,9 +44,6 @@ cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src_
                                int32_t *err, cudaStream_t stream);
 cudaError_t read_stream_launch(const void *src, size_t bytes, int mode, int32_t *err,
                                cudaStream_t stream);
-cudaError_t short_attention_launch(const ShortParams &p, int G, int bs, cudaStream_t stream);
-int short_max_tokens();
-int short_max_units();
 void set_error_detail(const char *msg);
 void clear_error_detail();
 const char *error_detail();

@@ -186,22 +186,6 @@ struct AttnParams {
   unsigned long long wait_limit_ns;  // bounded waits give up after this (0: kWaitLimitNs)
 };
 
-// Short-context decode attention (short_attention.cu): one cluster of CTAs
-// per (sequence, KV head), optionally appending the new token first.
-struct ShortParams {
-  __nv_bfloat16 *out;            // [B][n_q][D]
-  const __nv_bfloat16 *q;        // [B][n_q][D]
-  unsigned char *k_cache;        // bf16 tiled pools (written only by the fused append)
-  unsigned char *v_cache;
-  const __nv_bfloat16 *k_new;    // [B][n_kv][D] token to append at ctx - 1, or null
-  const __nv_bfloat16 *v_new;
-  const int32_t *tables;         // [B][MB]
-  const int32_t *ctx;            // [B]
-  int B, n_q, n_kv, MB, NB;
-  float qk_scale_log2;           // scale * log2(e)
-  int32_t *err;
-};
-
 // Final merge of cascade attention (prefix_attention.cu): decode parts of
 // each unit with a shared prefix, then the prefix parts, into the output.
 struct CombineParams {

@@ -38,7 +38,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include "pgd_device.cuh"
+#include "short_attention.cuh"
 
 namespace pgd {
 namespace sc {
