@@ -596,7 +596,7 @@ def run_ours(args, rank, world, local):
     out = torch.empty_like(pb.q)
     # Short contexts (every context within 1024 tokens, at most 128 units)
     # run the short-context kernel: one launch, the append fused.
-    short = (not args.cascade and not T and not fp8 and
+    short = (not args.cascade and not T and
              pgd.uses_short_path(B, n_kv, pb.block_tables.shape[1], pb.block_size, args.splits))
     grid = (8 * B * n_kv) if short else pgd.attention_grid(B, n_q, n_kv, pb.block_size,
                                                             args.splits)
@@ -818,8 +818,9 @@ def run_ours(args, rank, world, local):
                                if args.cascade else
                                ("pgd::tc::paged_attention_kernel<%d rows, bs, bf16> (tcgen05, "
                                 "multi-query verify)" % (T * (n_q // n_kv))) if T else
-                               ("pgd::sc::short_attention_kernel<G, bs> (short contexts: CUDA "
-                                "cores, cluster log-sum-exp merge; latency-bound)") if short else
+                               ("pgd::sc::short_attention_kernel<G, bs, %s> (short contexts: "
+                                "CUDA cores, cluster log-sum-exp merge; latency-bound)"
+                                % ("fp8" if fp8 else "bf16")) if short else
                                "pgd::tc::paged_attention_kernel<G, bs, %s> (tcgen05)"
                                % ("fp8" if fp8 else "bf16"),
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,

@@ -281,12 +281,12 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   return PGD_OK;
 }
 
-// Whether an automatic single-query bf16 call goes to the short-context
+// Whether an automatic single-query call goes to the short-context
 // kernel: every context it can hold (MB * bs tokens) is within the limit, and
 // its (sequence, KV head) units fit one wave of clusters.
 bool short_path(const PreparedAttention &pa, int32_t num_splits, int32_t MB, int32_t bs) {
   const long long tokens = (long long)MB * bs;
-  return !pa.fp8 && pa.p.T == 1 && num_splits == 0 &&
+  return pa.p.T == 1 && num_splits == 0 &&
          (long long)pa.p.B * pa.p.n_kv <= short_max_units() &&
          tokens <= std::min(g_short_tokens.load(), short_max_tokens());
 }
@@ -310,6 +310,7 @@ pgd_status launch_short(const PreparedAttention &pa, const void *k_new, const vo
   sp.MB = pa.p.MB;
   sp.NB = pa.p.NB;
   sp.qk_scale_log2 = pa.p.qk_scale_log2;
+  sp.fp8 = pa.fp8 ? 1 : 0;
   sp.err = pa.p.err;
   cudaError_t e = short_attention_launch(sp, pa.G, pa.bs, stream);
   if (e != cudaSuccess) return cuda_fail(e, "short-context attention launch");
@@ -655,8 +656,11 @@ pgd_status pgd_cascade_decode_attention(
                         NB, scale, num_splits, workspace, dec, &pa);
   if (s != PGD_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (n_groups == 0) {
-    s = launch_prepared(pa, st);
+  if (n_groups == 0) {  // plain attention, through the same kernel choice
+    s = short_path(pa, num_splits, MB, bs)
+            ? launch_short(pa, nullptr, nullptr, const_cast<void *>(k_cache),
+                           const_cast<void *>(v_cache), st)
+            : launch_prepared(pa, st);
     return s == PGD_OK ? ok() : s;
   }
   // 1. shared-prefix pass, on a few SMs; it lets the suffix pass launch at
@@ -913,7 +917,10 @@ pgd_status pgd_paged_decode_attention_fp8(void *out, const void *q, const void *
   s = prepare_attention(out, q, k_cache, v_cache, block_tables, context_lens, B, n_q, n_kv, bs, MB,
                         NB, scale, num_splits, workspace, workspace_bytes, &pa, true);
   if (s != PGD_OK) return s;
-  s = launch_prepared(pa, static_cast<cudaStream_t>(stream));
+  s = short_path(pa, num_splits, MB, bs)
+          ? launch_short(pa, nullptr, nullptr, const_cast<void *>(k_cache),
+                         const_cast<void *>(v_cache), static_cast<cudaStream_t>(stream))
+          : launch_prepared(pa, static_cast<cudaStream_t>(stream));
   return s == PGD_OK ? ok() : s;
 }
 

@@ -14,6 +14,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include "kv_quant.cuh"
 #include "pgd_device.cuh"
 
 namespace pgd {
@@ -84,7 +85,6 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
                      unsigned char *__restrict__ k_cache, unsigned char *__restrict__ v_cache,
                      const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
                      int pos_offset, int B, int n_kv, int bs, int MB, int NB, int32_t *err) {
-  constexpr int kGroupBytes = 8 * kHeadDim + 32;
   pdl_launch_dependents();  // the attention that follows may start its prologue
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -102,33 +102,15 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
   }
   const int l = lane & 15;
   const uint4 raw = __ldg((lane < 16 ? k_new : v_new) + (size_t)row * 16 + l);
-  float f[8];
-  unpack8(raw, f);
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, o));
-  const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
   uint32_t w[2];
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint16_t c0 = (uint16_t)__nv_cvt_float2_to_fp8x2(
-        make_float2(__fdiv_rn(f[4 * j], scale), __fdiv_rn(f[4 * j + 1], scale)), __NV_SATFINITE,
-        __NV_E4M3);
-    const uint16_t c1 = (uint16_t)__nv_cvt_float2_to_fp8x2(
-        make_float2(__fdiv_rn(f[4 * j + 2], scale), __fdiv_rn(f[4 * j + 3], scale)),
-        __NV_SATFINITE, __NV_E4M3);
-    w[j] = (uint32_t)c0 | ((uint32_t)c1 << 16);
-  }
-  // group of the slot, then dims 8l..8l+7: core matrix l / 2, half l % 2
+  float scale;
+  quantize_row_e4m3(raw, w, scale);
   const int slot = p % bs;
   unsigned char *group = (lane < 16 ? k_cache : v_cache) +
                          (((size_t)blk * n_kv + g) * (size_t)(bs / 8) + (size_t)(slot / 8)) *
-                             (size_t)kGroupBytes;
-  *reinterpret_cast<uint2 *>(group + (l >> 1) * 128 + (slot & 7) * 16 + (l & 1) * 8) =
-      make_uint2(w[0], w[1]);
-  if (l == 0) *reinterpret_cast<float *>(group + 8 * kHeadDim + (slot & 7) * 4) = scale;
+                             (size_t)kGroupBytes8;
+  *reinterpret_cast<uint2 *>(group + code_offset8(slot, l)) = make_uint2(w[0], w[1]);
+  if (l == 0) *reinterpret_cast<float *>(group + scale_offset8(slot)) = scale;
 }
 
 cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,

@@ -78,6 +78,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
+// The same with a bound on how long the thread may be suspended inside the
+// poll (hint_ns), instead of the system's own bound.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Wait until the phase with the given parity has completed, or give up after
 // kWaitLimitNs.  Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {

@@ -38,6 +38,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
+#include "kv_quant.cuh"
 #include "short_attention.cuh"
 
 namespace pgd {
@@ -71,17 +74,23 @@ __device__ __forceinline__ float ld_cluster_f32(const float *local, uint32_t ran
   return v;
 }
 
-template <int G, int BS>
+template <int G, int BS, bool FP8>
 __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortParams p) {
-  constexpr int VEC = kHeadDim * 2 / 16;  // 16-byte chunks per 256-byte row
-  constexpr uint32_t TILE_VEC = BS * VEC;
+  constexpr int VEC = kHeadDim * 2 / 16;  // 16-byte chunks per bf16 row
+  // bytes of one (block, KV head) tile: bf16 rows, or 8-token groups of
+  // codes and scales
+  constexpr size_t TILE = FP8 ? (size_t)(BS / 8) * kGroupBytes8 : (size_t)BS * kHeadDim * 2;
+  using VT = typename std::conditional<FP8, unsigned char, __nv_bfloat16>::type;
   __shared__ __align__(16) float qs[G][kHeadDim];        // query rows, fp32
-  __shared__ __align__(16) __nv_bfloat16 vs[CH][kHeadDim];  // V rows of a piece
+  __shared__ __align__(16) VT vs[CH][kHeadDim];          // V rows of a piece (bf16, or codes)
+  __shared__ float vsc[CH];                              // their scales (8-bit cache)
   __shared__ __align__(16) float ps[CH][G];              // probabilities of a piece
   __shared__ float red[4][G];                            // per-warp maxima
   __shared__ int tbl[MAXB];                              // the sequence's table row
   __shared__ float st_m[G], st_l[G];                     // this CTA's state, for the merge
   __shared__ float st_o[G][kHeadDim];
+  __shared__ __align__(16) unsigned char nk8[kHeadDim], nv8[kHeadDim];  // the appended token,
+  __shared__ float nks, nvs;                                            // quantised (8-bit)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
@@ -114,25 +123,43 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
   const int t_new = (p.k_new && ctx_ok) ? n - 1 : -1;  // appended token (in the last range)
   __syncthreads();
 
-  // The fused append: the token row of slot t_new % BS in tile
-  // (table[b][t_new / BS], g) becomes k_new[b][g] (and V), bit for bit.
-  if (t_new >= t_lo && t_new < t_hi && tid < 32) {
+  // The fused append, by warp 0 of the CTA whose range holds t_new: the
+  // token row of slot t_new % BS in tile (table[b][t_new / BS], g) becomes
+  // k_new[b][g] (and V) bit for bit -- or, for the 8-bit cache, its codes and
+  // scale, quantised exactly as kv_append_fp8 does (lanes 0-15 K, 16-31 V);
+  // the 8-bit rows are also kept here for this CTA's own use.
+  if (t_new >= t_lo && t_new < t_hi && warp == 0) {
     const int blk = tbl[t_new / BS];
-    if ((unsigned)blk < (unsigned)p.NB) {
-      const int slot = t_new % BS, v = lane & 15;
-      const size_t dst = ((size_t)blk * p.n_kv + g) * TILE_VEC + (size_t)(slot >> 3) * 128 +
+    const bool blk_ok = (unsigned)blk < (unsigned)p.NB;
+    const int slot = t_new % BS, v = lane & 15;
+    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(lane < 16 ? p.k_new : p.v_new) +
+                            (size_t)unit * VEC + v);
+    unsigned char *pool = lane < 16 ? p.k_cache : p.v_cache;
+    if constexpr (FP8) {
+      uint32_t w[2];
+      float scale;
+      quantize_row_e4m3(raw, w, scale);
+      *reinterpret_cast<uint2 *>((lane < 16 ? nk8 : nv8) + 8 * v) = make_uint2(w[0], w[1]);
+      if (v == 0) *(lane < 16 ? &nks : &nvs) = scale;
+      if (blk_ok) {
+        unsigned char *group = pool + (size_t)blk * p.n_kv * TILE + (size_t)g * TILE +
+                               (size_t)(slot / 8) * kGroupBytes8;
+        *reinterpret_cast<uint2 *>(group + code_offset8(slot, v)) = make_uint2(w[0], w[1]);
+        if (v == 0) *reinterpret_cast<float *>(group + scale_offset8(slot)) = scale;
+      }
+    } else if (blk_ok) {
+      const size_t dst = ((size_t)blk * p.n_kv + g) * (TILE / 16) + (size_t)(slot >> 3) * 128 +
                          (size_t)v * 8 + (size_t)(slot & 7);
-      const uint4 *src = reinterpret_cast<const uint4 *>(lane < 16 ? p.k_new : p.v_new) +
-                         (size_t)unit * VEC + v;
-      reinterpret_cast<uint4 *>(lane < 16 ? p.k_cache : p.v_cache)[dst] = __ldg(src);
-    } else if (lane == 0) {
-      atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
+      reinterpret_cast<uint4 *>(pool)[dst] = raw;
     }
+    if (!blk_ok && lane == 0) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
   }
+  if (FP8) __syncthreads();  // the quantised row is read by the loaders below
 
   // Thread roles in a piece: q.k -- token j = tid / 2, dims [64 hf, 64 hf + 64);
-  // V staging -- token rows 8 k + tid / 16 (k < 8), chunk tid % 16; p.v --
-  // output dim tid.
+  // V staging -- bf16: token rows 8 k + tid / 16 (k < 8), 16-byte chunk
+  // tid % 16; 8-bit: rows 16 k + tid / 8 (k < 4), 16-code chunk tid % 8, and
+  // the scale of row tid (tid < 64); p.v -- output dim tid.
   const int j = tid >> 1, hf = tid & 1;
   float m_run[G], l_run[G], o_acc[G];
 #pragma unroll
@@ -141,81 +168,134 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
 
   for (int tb = t_lo; tb < t_hi; tb += CH) {
     const int nt = min(CH, t_hi - tb);
-    // K: this thread's 8 chunks of token tb + j
-    uint4 kr[8];
-    bool kval = false;
-    {
-      const int t = tb + j;
-      if (j < nt) {
-        const int blk = tbl[t / BS];
+    // ---- loads first, all in flight together: K of token tb + j (this
+    // thread's 64 dims), then this thread's share of the piece's V rows
+    // (zeros, and scale 0, for rows that take no weight, so that no NaN
+    // reaches p.v)
+    constexpr int NKV = FP8 ? 4 : 8;        // 16-byte K pieces per thread
+    constexpr int NVV = FP8 ? CH / 16 : CH / 8;  // 16-byte V pieces per thread
+    uint4 kr[NKV], vr[NVV];
+    float ksc = 0.f, vscl = 0.f;
+    const int t = tb + j;
+    const int kblk = (j < nt) ? tbl[t / BS] : -1;
+    const bool kval = j < nt && (unsigned)kblk < (unsigned)p.NB;
+    if (j < nt && !kval) bad_seen = true;
+#pragma unroll
+    for (int k = 0; k < NKV; ++k) kr[k] = make_uint4(0, 0, 0, 0);
+    if (kval) {
+      const int slot = t % BS;
+      const unsigned char *tile = p.k_cache + ((size_t)kblk * p.n_kv + g) * TILE;
+      if constexpr (FP8) {
+        // 4 chunks of 16 codes (dims 64 hf + 16 k ..) and the token's scale
         if (t == t_new) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(p.k_new) + (size_t)unit * VEC + hf * 8;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) kr[k] = __ldg(src + k);
-          kval = (unsigned)blk < (unsigned)p.NB;
-        } else if ((unsigned)blk < (unsigned)p.NB) {
-          const int slot = t % BS;
-          const uint4 *src = reinterpret_cast<const uint4 *>(p.k_cache) +
-                             ((size_t)blk * p.n_kv + g) * TILE_VEC + (size_t)(slot >> 3) * 128 +
-                             (size_t)(hf * 8) * 8 + (size_t)(slot & 7);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) kr[k] = __ldg(src + (size_t)k * 8);
-          kval = true;
+          for (int k = 0; k < 4; ++k) kr[k] = *reinterpret_cast<const uint4 *>(nk8 + 64 * hf + 16 * k);
+          ksc = nks;
         } else {
-          bad_seen = true;
-        }
-      }
-      if (!kval) {
+          const unsigned char *group = tile + (size_t)(slot / 8) * kGroupBytes8;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) kr[k] = make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 4; ++k)
+            kr[k] = __ldg(reinterpret_cast<const uint4 *>(group + (4 * hf + k) * 128 + (slot & 7) * 16));
+          ksc = __ldg(reinterpret_cast<const float *>(group + scale_offset8(slot)));
+        }
+      } else {
+        const uint4 *src = (t == t_new)
+            ? reinterpret_cast<const uint4 *>(p.k_new) + (size_t)unit * VEC + hf * 8
+            : reinterpret_cast<const uint4 *>(tile) + (size_t)(slot >> 3) * 128 +
+                  (size_t)(hf * 8) * 8 + (size_t)(slot & 7);
+        const int step = (t == t_new) ? 1 : 8;  // chunks 128 B apart in a tile
+#pragma unroll
+        for (int k = 0; k < 8; ++k) kr[k] = __ldg(src + (size_t)k * step);
       }
     }
-    // V: rows 8 k + tid / 16 of the piece, chunk tid % 16 (zeros for rows
-    // that take no weight, so that no NaN reaches p.v)
-    uint4 vr[CH / 8];
-    {
-      const int cv = tid & 15;
 #pragma unroll
-      for (int k = 0; k < CH / 8; ++k) {
-        const int jj = 8 * k + (tid >> 4), t = tb + jj;
-        vr[k] = make_uint4(0, 0, 0, 0);
-        if (jj < nt) {
-          const int blk = tbl[t / BS];
-          if ((unsigned)blk < (unsigned)p.NB) {
-            if (t == t_new) {
-              vr[k] = __ldg(reinterpret_cast<const uint4 *>(p.v_new) + (size_t)unit * VEC + cv);
-            } else {
-              const int slot = t % BS;
-              vr[k] = __ldg(reinterpret_cast<const uint4 *>(p.v_cache) +
-                            ((size_t)blk * p.n_kv + g) * TILE_VEC + (size_t)(slot >> 3) * 128 +
-                            (size_t)cv * 8 + (size_t)(slot & 7));
-            }
+    for (int k = 0; k < NVV; ++k) {
+      // bf16: row 8 k + tid / 16, chunk tid % 16; 8-bit: row 16 k + tid / 8,
+      // 16-code chunk tid % 8
+      const int jj = FP8 ? 16 * k + (tid >> 3) : 8 * k + (tid >> 4);
+      const int cv = FP8 ? (tid & 7) : (tid & 15);
+      const int tv = tb + jj;
+      vr[k] = make_uint4(0, 0, 0, 0);
+      if (jj < nt) {
+        const int blk = tbl[tv / BS];
+        if ((unsigned)blk < (unsigned)p.NB) {
+          const int slot = tv % BS;
+          const unsigned char *tile = p.v_cache + ((size_t)blk * p.n_kv + g) * TILE;
+          if constexpr (FP8) {
+            vr[k] = (tv == t_new) ? *reinterpret_cast<const uint4 *>(nv8 + 16 * cv)
+                                  : __ldg(reinterpret_cast<const uint4 *>(
+                                        tile + (size_t)(slot / 8) * kGroupBytes8 + cv * 128 +
+                                        (slot & 7) * 16));
+          } else {
+            vr[k] = (tv == t_new)
+                ? __ldg(reinterpret_cast<const uint4 *>(p.v_new) + (size_t)unit * VEC + cv)
+                : __ldg(reinterpret_cast<const uint4 *>(tile) + (size_t)(slot >> 3) * 128 +
+                        (size_t)cv * 8 + (size_t)(slot & 7));
           }
         }
       }
     }
-    // q.k over this thread's 64 dims, then the pair's sum
+    if (FP8 && tid < CH && tid < nt) {  // the V scale of row tid
+      const int tv = tb + tid, blk = tbl[tv / BS];
+      if ((unsigned)blk < (unsigned)p.NB) {
+        const int slot = tv % BS;
+        vscl = (tv == t_new) ? nvs
+                             : __ldg(reinterpret_cast<const float *>(
+                                   p.v_cache + ((size_t)blk * p.n_kv + g) * TILE +
+                                   (size_t)(slot / 8) * kGroupBytes8 + scale_offset8(slot)));
+      }
+    }
+    // ---- q.k over this thread's 64 dims
     float s[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) s[h] = 0.f;
+    if constexpr (FP8) {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      float f[8];
-      unpack8(kr[k], f);
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t wd[4] = {kr[k].x, kr[k].y, kr[k].z, kr[k].w};
 #pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float4 a = *reinterpret_cast<const float4 *>(&qs[h][hf * 64 + k * 8]);
-        const float4 bq = *reinterpret_cast<const float4 *>(&qs[h][hf * 64 + k * 8 + 4]);
-        s[h] = fmaf(a.x, f[0], s[h]);
-        s[h] = fmaf(a.y, f[1], s[h]);
-        s[h] = fmaf(a.z, f[2], s[h]);
-        s[h] = fmaf(a.w, f[3], s[h]);
-        s[h] = fmaf(bq.x, f[4], s[h]);
-        s[h] = fmaf(bq.y, f[5], s[h]);
-        s[h] = fmaf(bq.z, f[6], s[h]);
-        s[h] = fmaf(bq.w, f[7], s[h]);
+        for (int e = 0; e < 8; ++e) {
+          const float2 f2 = e4m3x2_to_f32x2((uint16_t)(wd[e >> 1] >> ((e & 1) * 16)));
+          const int d = 64 * hf + 16 * k + 2 * e;
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float2 q2 = *reinterpret_cast<const float2 *>(&qs[h][d]);
+            s[h] = fmaf(q2.x, f2.x, s[h]);
+            s[h] = fmaf(q2.y, f2.y, s[h]);
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) s[h] *= ksc;
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float f[8];
+        unpack8(kr[k], f);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float4 a = *reinterpret_cast<const float4 *>(&qs[h][hf * 64 + k * 8]);
+          const float4 bq = *reinterpret_cast<const float4 *>(&qs[h][hf * 64 + k * 8 + 4]);
+          s[h] = fmaf(a.x, f[0], s[h]);
+          s[h] = fmaf(a.y, f[1], s[h]);
+          s[h] = fmaf(a.z, f[2], s[h]);
+          s[h] = fmaf(a.w, f[3], s[h]);
+          s[h] = fmaf(bq.x, f[4], s[h]);
+          s[h] = fmaf(bq.y, f[5], s[h]);
+          s[h] = fmaf(bq.z, f[6], s[h]);
+          s[h] = fmaf(bq.w, f[7], s[h]);
+        }
       }
     }
+    // ---- V rows into shared memory (bf16: a warp writes two whole rows,
+    // 512 contiguous bytes; 8-bit: four rows of 128 codes)
+#pragma unroll
+    for (int k = 0; k < NVV; ++k) {
+      const int jj = FP8 ? 16 * k + (tid >> 3) : 8 * k + (tid >> 4);
+      const int col = FP8 ? 16 * (tid & 7) : 8 * (tid & 15);
+      *reinterpret_cast<uint4 *>(&vs[jj][col]) = vr[k];
+    }
+    if (FP8 && tid < CH) vsc[tid] = vscl;
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       s[h] += __shfl_xor_sync(kFullMask, s[h], 1);
@@ -229,11 +309,6 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
       for (int o = 2; o < 32; o <<= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
       if (lane == 0) red[warp][h] = m;
     }
-    // stage V rows (row jj, chunk cv: 16 B at column 8 cv; a warp writes two
-    // whole rows, 512 contiguous bytes)
-#pragma unroll
-    for (int k = 0; k < CH / 8; ++k)
-      *reinterpret_cast<uint4 *>(&vs[8 * k + (tid >> 4)][(tid & 15) * 8]) = vr[k];
     __syncthreads();
     float alpha[G], m_new[G];
 #pragma unroll
@@ -244,7 +319,7 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
       alpha[h] = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - m_new[h]);
       m_run[h] = m_new[h];
     }
-    if (hf == 0 && j < CH) {
+    if (hf == 0) {
 #pragma unroll
       for (int h = 0; h < G; ++h)
         ps[j][h] = (s[h] == -INFINITY) ? 0.f : exp2f(s[h] - m_new[h]);
@@ -255,7 +330,13 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
 #pragma unroll
     for (int h = 0; h < G; ++h) { acc[h] = 0.f; lsum[h] = 0.f; }
     for (int jj = 0; jj < nt; ++jj) {
-      const float v = __bfloat162float(vs[jj][tid]);
+      float v;
+      if constexpr (FP8) {
+        const __half h = __half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)vs[jj][tid], __NV_E4M3));
+        v = __half2float(h) * vsc[jj];
+      } else {
+        v = __bfloat162float(vs[jj][tid]);
+      }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float pw = ps[jj][h];
@@ -268,7 +349,7 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
       o_acc[h] = o_acc[h] * alpha[h] + acc[h];
       l_run[h] = l_run[h] * alpha[h] + lsum[h];
     }
-    __syncthreads();  // vs, ps and red are rewritten by the next piece
+    __syncthreads();  // vs, vsc, ps and red are rewritten by the next piece
   }
   if (bad_seen) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
 
@@ -307,7 +388,7 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
   cluster_sync();  // peers may still be reading this CTA's state
 }
 
-template <int G, int BS>
+template <int G, int BS, bool FP8>
 static cudaError_t launch_g(const ShortParams &p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.n_kv * CL));
@@ -323,16 +404,16 @@ static cudaError_t launch_g(const ShortParams &p, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, short_attention_kernel<G, BS>, p);
+  return cudaLaunchKernelEx(&cfg, short_attention_kernel<G, BS, FP8>, p);
 }
 
-template <int BS>
+template <int BS, bool FP8>
 static cudaError_t launch_bs(const ShortParams &p, int G, cudaStream_t stream) {
   switch (G) {
-    case 1: return launch_g<1, BS>(p, stream);
-    case 2: return launch_g<2, BS>(p, stream);
-    case 4: return launch_g<4, BS>(p, stream);
-    case 8: return launch_g<8, BS>(p, stream);
+    case 1: return launch_g<1, BS, FP8>(p, stream);
+    case 2: return launch_g<2, BS, FP8>(p, stream);
+    case 4: return launch_g<4, BS, FP8>(p, stream);
+    case 8: return launch_g<8, BS, FP8>(p, stream);
   }
   return cudaErrorInvalidValue;
 }
@@ -348,8 +429,12 @@ int short_max_units() { return 128; }
 cudaError_t short_attention_launch(const ShortParams &p, int G, int bs, cudaStream_t stream) {
   if (p.B * p.n_kv == 0) return cudaSuccess;
   if ((long long)p.MB * bs > short_max_tokens() || p.MB > sc::MAXB) return cudaErrorInvalidValue;
-  return bs == 16 ? sc::launch_bs<16>(p, G, stream)
-       : bs == 32 ? sc::launch_bs<32>(p, G, stream)
+  if (p.fp8)
+    return bs == 16 ? sc::launch_bs<16, true>(p, G, stream)
+         : bs == 32 ? sc::launch_bs<32, true>(p, G, stream)
+                    : cudaErrorInvalidValue;
+  return bs == 16 ? sc::launch_bs<16, false>(p, G, stream)
+       : bs == 32 ? sc::launch_bs<32, false>(p, G, stream)
                   : cudaErrorInvalidValue;
 }
 

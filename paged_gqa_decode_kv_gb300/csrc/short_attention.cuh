@@ -11,7 +11,8 @@ namespace pgd {
 struct ShortParams {
   __nv_bfloat16 *out;            // [B][n_q][D]
   const __nv_bfloat16 *q;        // [B][n_q][D]
-  unsigned char *k_cache;        // tiled pools (written only by the fused append)
+  unsigned char *k_cache;        // bf16 tiled pools or 8-bit pools (codes + scales), written
+                                 // only by the fused append
   unsigned char *v_cache;
   const __nv_bfloat16 *k_new;    // [B][n_kv][D] token to append at ctx - 1, or null
   const __nv_bfloat16 *v_new;
@@ -19,6 +20,7 @@ struct ShortParams {
   const int32_t *ctx;            // [B]
   int B, n_q, n_kv, MB, NB;
   float qk_scale_log2;           // scale * log2(e)
+  int fp8;                       // 1: 8-bit pools
   int32_t *err;
 };
 

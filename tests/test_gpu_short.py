@@ -227,3 +227,104 @@ def test_prepared_calls_match_the_oracle(limit):
     assert torch.equal(first, again)
     compare(alone, want, "prepared attention")
     assert_no_device_errors()
+
+
+# ------------------------------------------------------------ 8-bit cache
+def _batch8(B, n_q, n_kv, bs, lens, seed=2024, **kw):
+    return _batch(B, n_q, n_kv, bs, lens, seed=seed, kv_format="fp8", **kw)
+
+
+def _oracle8(pb, k=None, v=None):
+    return oracle.paged_attention_fp8(pb.q.cpu(), pb.k_cache.cpu() if k is None else k,
+                                      pb.v_cache.cpu() if v is None else v, pb.block_tables.cpu(),
+                                      pb.context_lens.cpu(), pb.scale, pb.block_size)
+
+
+def _gpu8(pb):
+    return pgd.paged_decode_attention_fp8(None, pb.q, pb.k_cache, pb.v_cache, pb.block_tables,
+                                          pb.context_lens, pb.scale)
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "nq%d_nkv%d_bs%d_%s" % (
+    c[0], c[1], c[2], "-".join(map(str, c[3][:6]))))
+def test_short_fp8_matches_oracle(case):
+    n_q, n_kv, bs, lens = case
+    pb = _batch8(len(lens), n_q, n_kv, bs, lens)
+    assert _short(pb)
+    compare(_gpu8(pb), _oracle8(pb), "short, 8-bit")
+    assert_no_device_errors()
+
+
+@pytest.mark.parametrize("case", CASES[2:6], ids=lambda c: "nq%d_nkv%d_bs%d" % c[:3])
+def test_short_fp8_and_tensor_core_kernels_agree(case):
+    n_q, n_kv, bs, lens = case
+    pb = _batch8(len(lens), n_q, n_kv, bs, lens, seed=78)
+    want = _oracle8(pb)
+    a = _gpu8(pb)
+    pgd.set_short_context_tokens(0)
+    b = _gpu8(pb)
+    torch.cuda.synchronize()
+    compare(a, want, "short, 8-bit")
+    compare(b, want, "tensor-core, 8-bit")
+    assert_no_device_errors()
+
+
+@pytest.mark.parametrize("case", APPEND_CASES, ids=lambda c: "nq%d_nkv%d_bs%d_%s" % (
+    c[0], c[1], c[2], "-".join(map(str, c[3]))))
+def test_short_fp8_fused_append(case):
+    """One launch quantises the new token into the 8-bit pools (codes and
+    scales bit exact with the oracle's kv_append_fp8) and attends over them."""
+    n_q, n_kv, bs, lens = case
+    pb = _batch8(len(lens), n_q, n_kv, bs, lens, append=True)
+    assert _short(pb)
+    want_k, want_v = oracle.kv_append_fp8(pb.k_cache.cpu(), pb.v_cache.cpu(), pb.k_new.cpu(),
+                                          pb.v_new.cpu(), pb.block_tables.cpu(),
+                                          pb.positions.cpu(), bs)
+    want = _oracle8(pb, want_k, want_v)
+    got = pgd.append_decode_attention_fp8(None, pb.q, pb.k_new, pb.v_new, pb.k_cache, pb.v_cache,
+                                          pb.block_tables, pb.context_lens, pb.scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(pb.k_cache.cpu().numpy(), want_k)
+    assert np.array_equal(pb.v_cache.cpu().numpy(), want_v)
+    compare(got, want, "fused 8-bit append")
+    assert_no_device_errors()
+
+
+def test_short_fp8_fused_append_extreme_rows():
+    """Rows of zeros, of one huge element, of tiny values and of values
+    reaching 448 after scaling, appended by the short kernel: bit exact."""
+    B, n_kv, bs = 4, 2, 16
+    pb = _batch8(B, 8, n_kv, bs, [5, 16, 17, 40], append=True)
+    kn = torch.zeros(B, n_kv, 128)
+    kn[1, 0, 7] = 3e38
+    kn[1, 1] = torch.linspace(-1e-30, 1e-30, 128)
+    kn[2] = torch.linspace(-448, 448, 128)
+    kn[3, 0] = torch.tensor([(-1) ** i * 2.0 ** (i % 40 - 20) for i in range(128)])
+    kn = kn.to(torch.bfloat16).cuda()
+    vn = (-kn).contiguous()
+    want_k, want_v = oracle.kv_append_fp8(pb.k_cache.cpu(), pb.v_cache.cpu(), kn.cpu(), vn.cpu(),
+                                          pb.block_tables.cpu(), pb.positions.cpu(), bs)
+    pgd.append_decode_attention_fp8(None, pb.q, kn, vn, pb.k_cache, pb.v_cache, pb.block_tables,
+                                    pb.context_lens, pb.scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(pb.k_cache.cpu().numpy(), want_k)
+    assert np.array_equal(pb.v_cache.cpu().numpy(), want_v)
+    pgd.device_errors(clear=True)  # (a 3e38 row may give non-finite scores: not checked here)
+
+
+def test_short_fp8_reference_moves():
+    """K scales of later blocks multiplied by 8 and then 32: the scores jump
+    by far more than 2^8 mid-context; every piece's maximum is exact, so the
+    online softmax stays within tolerance."""
+    lens = [1000, 700, 1024]
+    pb = _batch8(len(lens), 8, 2, 16, lens, seed=43)
+    codes, scales = inputs.unpack_pool8(pb.k_cache.cpu())
+    for b, n in enumerate(lens):
+        for jb in range(-(-n // 16)):
+            f = 32.0 if jb >= 40 else (8.0 if jb >= 20 else 1.0)
+            scales[int(pb.block_tables[b, jb])] *= f
+    pb.k_cache.copy_(inputs.pack_pool8(codes, scales).cuda())
+    pb.q[:, ::3] = 0
+    assert _short(pb)
+    compare(_gpu8(pb), _oracle8(pb), "8-bit, moved references")
+    assert_no_device_errors()
