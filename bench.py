@@ -46,6 +46,10 @@ PROFILE_SUMMARY_FP8 = os.path.join(ROOT, "profiles", "paged_attention_fp8_batch1
 MLA_SOURCES = [os.path.join(ROOT, "paged_gqa_decode_kv_gb300", "csrc", f)
                for f in ("mla_attention.cu", "attention_kernel.cuh", "pgd_device.cuh")]
 PROFILE_SUMMARY_MLA = os.path.join(ROOT, "profiles", "mla_attention_batch16_ctx8192_h128.md")
+SHORT_SOURCES = [os.path.join(ROOT, "paged_gqa_decode_kv_gb300", "csrc", f)
+                 for f in ("short_attention.cu", "short_attention.cuh", "kv_quant.cuh",
+                           "pgd_device.cuh")]
+PROFILE_SUMMARY_SHORT = os.path.join(ROOT, "profiles", "short_attention_single_ctx512.md")
 
 
 def parse_args(argv=None):
@@ -260,21 +264,27 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(kv: str = "bf16", workload: str = "batch16_ctx8192"):
+def profiled_traffic(kv: str = "bf16", workload: str = "batch16_ctx8192", short: bool = False):
     """DRAM bytes per launch from the committed ncu summary of the attention
     kernel on this workload, or None if there is none or the kernel source
     changed since that capture."""
-    if workload != "batch16_ctx8192":
+    if short:
+        if workload != "single_ctx512" or kv != "bf16":
+            return None
+        path, sources = PROFILE_SUMMARY_SHORT, SHORT_SOURCES
+    elif workload == "batch16_ctx8192":
+        path, sources = (PROFILE_SUMMARY_FP8 if kv == "fp8" else PROFILE_SUMMARY), None
+    else:
         return None
     try:
-        text = open(PROFILE_SUMMARY_FP8 if kv == "fp8" else PROFILE_SUMMARY).read()
+        text = open(path).read()
     except OSError:
         return None
     m_bytes = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
     m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not (m_bytes and m_sha):
         return None
-    return int(m_bytes.group(1)) if kernel_source_sha256() == m_sha.group(1) else None
+    return int(m_bytes.group(1)) if kernel_source_sha256(sources) == m_sha.group(1) else None
 
 
 def kernel_source_sha256(paths=None) -> str:
@@ -826,7 +836,7 @@ def run_ours(args, rank, world, local):
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if (args.cascade or T) else
-                     profiled_traffic(args.kv, args.workload),
+                     profiled_traffic(args.kv, args.workload, short),
                      "launch_ms": round(attn_ms, 5),
                      "bytes_per_launch": kv_bytes,
                      "frac_of_read_only": round(achieved / ro_best, 4)},
