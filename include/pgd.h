@@ -498,24 +498,29 @@ uint64_t pgd_wait_limit_ns(void);
 /* ---------------------------------------------------------------------- */
 /* short-context path                                                     */
 /* ---------------------------------------------------------------------- */
-/* A call of pgd_paged_decode_attention, pgd_append_decode_attention,
- * pgd_decode_step or pgd_paged_decode_attention_noalloc with num_splits = 0
- * whose every possible context is short -- MB * bs at most the limit below,
- * itself at most 1024 -- and that has at most 128 (sequence, KV head) units
- * runs a latency-first kernel instead of the tensor-core one: such a call is
- * bound by the start-up of a kernel, not by its bytes.  One cluster of 8
- * CTAs per unit, each taking an eighth of the context; q.k and p.v on the
- * CUDA cores in fp32 (exact exp2); the eight (max, sum, output) states merged
+/* A single-query call with num_splits = 0 of pgd_paged_decode_attention,
+ * pgd_append_decode_attention, pgd_decode_step, their 8-bit counterparts
+ * (_fp8), pgd_paged_decode_attention_noalloc or pgd_cascade_decode_attention
+ * without groups, whose every possible context is short -- MB * bs at most
+ * the limit below, itself at most 1024 -- with at most 64 (sequence, KV head)
+ * units and B * n_kv * MB * bs at most 40960, runs a latency-first kernel
+ * instead of the tensor-core one: such a call is bound by the start-up of a
+ * kernel, not by its bytes.  One cluster of 8 CTAs per unit, each taking an
+ * eighth of the context; q.k and p.v on the CUDA cores in fp32 (8-bit codes
+ * times their scales), exact exp2; the eight (max, sum, output) states merged
  * by log-sum-exp through distributed shared memory ("The math of Transformer
  * inference", section 8); for the append variants the new token's K/V are
- * written by the same launch, bit for bit as pgd_kv_append writes them.  The
- * results, errors and rules are those of the documented calls; the workspace
- * is checked but not touched.  The limit is 1024 tokens;
+ * written by the same launch, bit for bit as pgd_kv_append (pgd_kv_append_fp8)
+ * writes them.  The results, errors and rules are those of the documented
+ * calls; the workspace is checked but not touched.  The limit is 1024 tokens;
  * pgd_set_short_context_tokens sets it process-wide for the calls made after
  * it (0 sends every call to the tensor-core kernel, a negative value restores
- * 1024) and returns the previous limit.  Thread-safe.  No counterpart on the
- * pages: a choice between two kernels for the same operation. */
+ * 1024) and returns the previous limit; pgd_short_path returns 1 when a call
+ * with these sizes would run the short-context kernel now, else 0.
+ * Thread-safe.  No counterpart on the pages: a choice between two kernels for
+ * the same operation. */
 int32_t pgd_set_short_context_tokens(int32_t max_tokens);
+int32_t pgd_short_path(int32_t B, int32_t n_kv, int32_t bs, int32_t MB, int32_t num_splits);
 
 /* ---------------------------------------------------------------------- */
 /* device error word                                                      */

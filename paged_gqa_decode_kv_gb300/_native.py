@@ -66,6 +66,7 @@ SIGNATURES = {
     "pgd_set_wait_limit_ns": ([ctypes.c_uint64], None),
     "pgd_wait_limit_ns": ([], ctypes.c_uint64),
     "pgd_set_short_context_tokens": ([_I], _I),
+    "pgd_short_path": ([_I, _I, _I, _I, _I], _I),
     "pgd_alloc_create": ([_I, _P], _I),
     "pgd_alloc_destroy": ([_P], None),
     "pgd_alloc_allocate": ([_P, _I, _P], _I),
@@ -583,22 +584,17 @@ def wait_limit_ns() -> int:
     return int(lib().pgd_wait_limit_ns())
 
 
-SHORT_MAX_UNITS = 128     # (sequence, KV head) units the short-context kernel takes at most
-
-
 def set_short_context_tokens(max_tokens: int) -> int:
     """Largest MB * bs (at most 1024) for which an automatic single-query
-    bf16 call runs the short-context kernel (0: never; negative: the default
+    call may run the short-context kernel (0: never; negative: the default
     1024).  Returns the previous limit."""
     return int(lib().pgd_set_short_context_tokens(int(max_tokens)))
 
 
-def uses_short_path(B: int, n_kv: int, MB: int, bs: int, num_splits: int = 0,
-                    limit: int = 1024) -> bool:
-    """Whether a call with these sizes runs the short-context kernel under
-    the given limit (the rule of pgd_set_short_context_tokens)."""
-    return (num_splits == 0 and B * n_kv <= SHORT_MAX_UNITS
-            and MB * bs <= min(limit, 1024))
+def uses_short_path(B: int, n_kv: int, MB: int, bs: int, num_splits: int = 0) -> bool:
+    """Whether a call with these sizes runs the short-context kernel now
+    (pgd_short_path)."""
+    return bool(lib().pgd_short_path(int(B), int(n_kv), int(bs), int(MB), int(num_splits)))
 
 
 # ------------------------------------------------------------ host allocator

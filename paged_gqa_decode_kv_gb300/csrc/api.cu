@@ -281,14 +281,20 @@ pgd_status prepare_attention(void *out, const void *q, const void *k_cache, cons
   return PGD_OK;
 }
 
-// Whether an automatic single-query call goes to the short-context
-// kernel: every context it can hold (MB * bs tokens) is within the limit, and
-// its (sequence, KV head) units fit one wave of clusters.
+// Whether an automatic single-query call goes to the short-context kernel:
+// every context it can hold (MB * bs tokens) is within the limit, and its
+// (sequence, KV head) units and units x tokens are small enough for the
+// latency-first kernel to win (short_attention.cu gives the measurements).
+bool short_rule(long long B, long long n_kv, long long MB, long long bs, int32_t num_splits,
+                int T) {
+  const long long units = B * n_kv, tokens = MB * bs;
+  return T == 1 && num_splits == 0 && units >= 1 && units <= short_max_units() &&
+         tokens <= std::min(g_short_tokens.load(), short_max_tokens()) &&
+         units * tokens <= short_max_work();
+}
+
 bool short_path(const PreparedAttention &pa, int32_t num_splits, int32_t MB, int32_t bs) {
-  const long long tokens = (long long)MB * bs;
-  return pa.p.T == 1 && num_splits == 0 &&
-         (long long)pa.p.B * pa.p.n_kv <= short_max_units() &&
-         tokens <= std::min(g_short_tokens.load(), short_max_tokens());
+  return short_rule(pa.p.B, pa.p.n_kv, MB, bs, num_splits, pa.p.T);
 }
 
 // The short-context kernel on a prepared call's arguments; with k_new and
@@ -1069,6 +1075,10 @@ void pgd_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store((unsigned long l
 
 int32_t pgd_set_short_context_tokens(int32_t max_tokens) {
   return g_short_tokens.exchange(max_tokens < 0 ? 1024 : max_tokens);
+}
+
+int32_t pgd_short_path(int32_t B, int32_t n_kv, int32_t bs, int32_t MB, int32_t num_splits) {
+  return short_rule(B, n_kv, MB, bs, num_splits, 1) ? 1 : 0;
 }
 
 uint64_t pgd_wait_limit_ns(void) {

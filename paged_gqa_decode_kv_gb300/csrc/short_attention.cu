@@ -420,11 +420,16 @@ static cudaError_t launch_bs(const ShortParams &p, int G, cudaStream_t stream) {
 
 }  // namespace sc
 
-// Largest context (MB * bs tokens) and number of (sequence, KV head) units
-// the short-context kernel takes: at most two 64-token pieces per CTA, and
-// one wave of clusters.
+// Largest table width (MB * bs tokens), number of (sequence, KV head) units
+// and units x width the short-context kernel takes: at most two 64-token
+// pieces per CTA, about one wave of clusters (3 CTAs of 128 threads per SM by
+// registers), and the work below which it measured faster than the
+// tensor-core kernel (device time per append + attention step, bf16 and
+// 8-bit: 8 units x 512 tokens 5.7 against 11.6 us, 32 x 1024 13.1 / 18.8,
+// 64 x 512 11.7 / 13.8; beyond: 64 x 1024 19.3 / 16.6, 128 x 256 16.5 / 13.1).
 int short_max_tokens() { return sc::CL * 2 * sc::CH; }
-int short_max_units() { return 128; }
+int short_max_units() { return 64; }
+long long short_max_work() { return 40960; }
 
 cudaError_t short_attention_launch(const ShortParams &p, int G, int bs, cudaStream_t stream) {
   if (p.B * p.n_kv == 0) return cudaSuccess;

@@ -27,5 +27,6 @@ struct ShortParams {
 cudaError_t short_attention_launch(const ShortParams &p, int G, int bs, cudaStream_t stream);
 int short_max_tokens();
 int short_max_units();
+long long short_max_work();
 
 }  // namespace pgd

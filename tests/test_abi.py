@@ -169,4 +169,5 @@ def test_short_context_setting(L):
     finally:
         pgd.set_short_context_tokens(-1)
     assert pgd.set_short_context_tokens(-1) == 1024
-    assert pgd.uses_short_path(16, 8, 64, 16) and not pgd.uses_short_path(17, 8, 64, 16)
+    assert pgd.uses_short_path(8, 8, 40, 16) and not pgd.uses_short_path(8, 8, 41, 16)
+    assert not pgd.uses_short_path(9, 8, 8, 16) and not pgd.uses_short_path(1, 8, 65, 16)

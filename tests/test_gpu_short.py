@@ -1,8 +1,9 @@
-"""The short-context kernel (contexts of at most 1024 tokens, at most 128
-(sequence, KV head) units, automatic split): parity with the float64 oracle,
-the fused append bit for bit, masking and error flags, and agreement with the
-tensor-core kernel on the same inputs (the limit set to 0 routes a call
-there).  Every case asserts which kernel its sizes select."""
+"""The short-context kernel (contexts of at most 1024 tokens, at most 64
+(sequence, KV head) units and 40960 unit-tokens, automatic split): parity
+with the float64 oracle, the fused append bit for bit, masking and error
+flags, and agreement with the tensor-core kernel on the same inputs (the
+limit set to 0 routes a call there).  Every case asserts which kernel its
+sizes select."""
 import numpy as np
 import pytest
 import torch
@@ -44,8 +45,9 @@ CASES = [
     (32, 8, 32, [31, 32, 33, 700, 1024]),
     (64, 8, 32, [129, 1000, 32]),
     (8, 1, 16, [300, 5, 513]),
-    (40, 40, 16, [90, 250]),
-    (32, 8, 16, [511] * 16),  # 128 units: the largest batch the kernel takes
+    (40, 40, 16, [250]),
+    # 64 units x 640 tokens: the most units and the most work the kernel takes
+    (32, 8, 16, [633, 640, 1, 17, 600, 320, 5, 640]),
 ]
 
 
@@ -78,21 +80,25 @@ def test_short_and_tensor_core_kernels_agree(case):
 
 
 def test_unit_and_context_limits_select_the_kernel():
-    assert pgd.uses_short_path(16, 8, 64, 16)          # 128 units, 1024 tokens
-    assert not pgd.uses_short_path(17, 8, 64, 16)      # 136 units
+    assert pgd.uses_short_path(8, 8, 40, 16)           # 64 units x 640 tokens = 40960
+    assert pgd.uses_short_path(4, 8, 64, 16)           # 32 units x 1024 tokens
+    assert not pgd.uses_short_path(8, 8, 41, 16)       # 64 x 656 > 40960
+    assert not pgd.uses_short_path(9, 8, 8, 16)        # 72 units
     assert not pgd.uses_short_path(1, 8, 65, 16)       # 1040 tokens
     assert not pgd.uses_short_path(1, 8, 8, 16, num_splits=1)
-    assert not pgd.uses_short_path(1, 8, 8, 16, limit=0)
     prev = pgd.set_short_context_tokens(256)
     assert prev == 1024
-    assert pgd.set_short_context_tokens(-1) == 256
+    assert pgd.uses_short_path(1, 8, 16, 16) and not pgd.uses_short_path(1, 8, 17, 16)
+    pgd.set_short_context_tokens(0)
+    assert not pgd.uses_short_path(1, 8, 1, 16)
+    assert pgd.set_short_context_tokens(-1) == 0
 
 
-def test_just_past_the_unit_limit_uses_the_tensor_core_kernel():
-    lens = [300] * 17  # 136 units
+@pytest.mark.parametrize("lens", [[300] * 17, [650] * 8], ids=["136-units", "64x656-tokens"])
+def test_just_past_the_limits_uses_the_tensor_core_kernel(lens):
     pb = _batch(len(lens), 32, 8, 16, lens, seed=5)
     assert not _short(pb)
-    compare(gpu_attention(pb), oracle_attention(pb), "136 units")
+    compare(gpu_attention(pb), oracle_attention(pb), "past the limits")
     assert_no_device_errors()
 
 
