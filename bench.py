@@ -607,7 +607,7 @@ def run_ours(args, rank, world, local):
     # Short contexts (every context within 1024 tokens, at most 128 units)
     # run the short-context kernel: one launch, the append fused.
     short = (not args.cascade and not T and
-             pgd.uses_short_path(B, n_kv, pb.block_tables.shape[1], pb.block_size, args.splits))
+             pgd.uses_short_path(B, n_kv, pb.block_size, pb.block_tables.shape[1], args.splits))
     grid = (8 * B * n_kv) if short else pgd.attention_grid(B, n_q, n_kv, pb.block_size,
                                                             args.splits)
     stream = torch.cuda.current_stream()
@@ -701,7 +701,9 @@ def run_ours(args, rank, world, local):
     sampler.stop()
     nvml.stop()
     elapsed_ms = e0.elapsed_time(e1)
-    attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
+    attn_all = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    attn_ms = statistics.fmean(attn_all)
+    attn_med = statistics.median(attn_all)
     flags = pgd.device_errors(clear=True, stream=stream)
     if flags:
         raise RuntimeError("device error word %d after the timed steps" % flags)
@@ -837,7 +839,7 @@ def run_ours(args, rank, world, local):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None if (args.cascade or T) else
                      profiled_traffic(args.kv, args.workload, short),
-                     "launch_ms": round(attn_ms, 5),
+                     "launch_ms": round(attn_ms, 5), "launch_ms_median": round(attn_med, 5),
                      "bytes_per_launch": kv_bytes,
                      "frac_of_read_only": round(achieved / ro_best, 4)},
         "e2e": dict({"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -953,7 +955,9 @@ def run_mla(args, rank, world, local):
     sampler.stop()
     nvml.stop()
     elapsed_ms = e0.elapsed_time(e1)
-    attn_ms = statistics.fmean(a.elapsed_time(b) for a, b in zip(ev_a, ev_b))
+    attn_all = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    attn_ms = statistics.fmean(attn_all)
+    attn_med = statistics.median(attn_all)
     flags = pgd.device_errors(clear=True, stream=stream)
     if flags:
         raise RuntimeError("device error word %d after the timed steps" % flags)
@@ -1012,7 +1016,8 @@ def run_mla(args, rank, world, local):
                      % mb.block_size, "achieved": round(achieved, 2), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": profiled_mla_traffic(name) if args.splits == 0 else None,
-                     "launch_ms": round(attn_ms, 5), "bytes_per_launch": nbytes,
+                     "launch_ms": round(attn_ms, 5), "launch_ms_median": round(attn_med, 5),
+                     "bytes_per_launch": nbytes,
                      "frac_of_read_only": round(achieved / ro_best, 4),
                      "tflops_achieved": round(flops / (attn_ms / 1e3) / 1e12, 2),
                      "flop_per_byte": round(flops / nbytes, 1)},

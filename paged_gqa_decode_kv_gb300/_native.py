@@ -591,9 +591,9 @@ def set_short_context_tokens(max_tokens: int) -> int:
     return int(lib().pgd_set_short_context_tokens(int(max_tokens)))
 
 
-def uses_short_path(B: int, n_kv: int, MB: int, bs: int, num_splits: int = 0) -> bool:
-    """Whether a call with these sizes runs the short-context kernel now
-    (pgd_short_path)."""
+def uses_short_path(B: int, n_kv: int, bs: int, MB: int, num_splits: int = 0) -> bool:
+    """Whether a call with these sizes (B sequences, n_kv KV heads, block size
+    bs, table width MB) runs the short-context kernel now (pgd_short_path)."""
     return bool(lib().pgd_short_path(int(B), int(n_kv), int(bs), int(MB), int(num_splits)))
 
 

@@ -318,23 +318,29 @@ static __device__ __noinline__ void wait_spin(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, int32_t *err) {
   if (*abort_flag) return;
   const uint64_t limit = reinterpret_cast<const volatile WaitCtl *>(abort_flag)->limit_ns;
-  // A short limit (set only to exercise this exit) also bounds each poll's
-  // suspension, so that an unmet wait gives up after its first failed poll
-  // whatever the system's own suspension bound is.
-  const bool short_limit = limit < 1000000ull;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (short_limit ? mbar_try_wait_hint(bar, parity, (uint32_t)limit)
-                    : mbar_try_wait(bar, parity))
-      return;
-    if ((i & 31u) == 1) {  // after the first failed poll, then every 32
-      if (*abort_flag) return;
-      if (global_timer_ns() - t0 > limit) {
-        *abort_flag = 1;
-        atomicOr(err, PGD_DEVERR_TIMEOUT);
-        return;
-      }
+  // Every 32 failed polls: an earlier timeout in the CTA, or this wait's own.
+  auto gave_up = [&]() {
+    if (*abort_flag) return true;
+    if (global_timer_ns() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(err, PGD_DEVERR_TIMEOUT);
+      return true;
     }
+    return false;
+  };
+  if (limit < 1000000ull) {
+    // A short limit (set only to exercise this exit) also bounds each poll's
+    // suspension, and the clock is read after the first failed poll too, so
+    // that an unmet wait gives up whatever the system's own suspension bound.
+    for (uint32_t i = 1;; ++i) {
+      if (mbar_try_wait_hint(bar, parity, (uint32_t)limit)) return;
+      if ((i & 31u) == 1 && gave_up()) return;
+    }
+  }
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 31u) == 0 && gave_up()) return;
   }
 }
 __device__ __forceinline__ void wait_or_abort(uint64_t *bar, uint32_t parity,

@@ -169,5 +169,22 @@ def test_short_context_setting(L):
     finally:
         pgd.set_short_context_tokens(-1)
     assert pgd.set_short_context_tokens(-1) == 1024
-    assert pgd.uses_short_path(8, 8, 40, 16) and not pgd.uses_short_path(8, 8, 41, 16)
-    assert not pgd.uses_short_path(9, 8, 8, 16) and not pgd.uses_short_path(1, 8, 65, 16)
+    assert pgd.uses_short_path(8, 8, 16, 40) and not pgd.uses_short_path(8, 8, 16, 41)
+    assert not pgd.uses_short_path(9, 8, 16, 8) and not pgd.uses_short_path(1, 8, 16, 65)
+
+
+def test_prepare_checks_arguments_on_the_host(L):
+    """pgd.prepare runs the binding's checks once, before any C call: a CPU
+    tensor, a wrong dtype or an unknown operation are refused at once."""
+    import torch
+    q = torch.zeros(1, 8, 128, dtype=torch.bfloat16)
+    pool = torch.zeros(2, 2, 2, 16, 8, 8, dtype=torch.bfloat16)
+    tables = torch.zeros(1, 1, dtype=torch.int32)
+    lens = torch.ones(1, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        pgd.prepare("paged_decode_attention", None, q, pool, pool, tables, lens, 0.1,
+                    workspace=torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(TypeError):
+        pgd.prepare("paged_decode_attention", None, q.float(), pool, pool, tables, lens, 0.1)
+    with pytest.raises(ValueError):
+        pgd.prepare("no_such_call")

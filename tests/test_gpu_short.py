@@ -31,8 +31,8 @@ def _batch(B, n_q, n_kv, bs, lens, seed=2024, **kw):
 
 
 def _short(pb) -> bool:
-    return pgd.uses_short_path(pb.batch, pb.k_cache.shape[1], pb.block_tables.shape[1],
-                               pb.block_size)
+    return pgd.uses_short_path(pb.batch, pb.k_cache.shape[1], pb.block_size,
+                               pb.block_tables.shape[1])
 
 
 CASES = [
@@ -80,17 +80,17 @@ def test_short_and_tensor_core_kernels_agree(case):
 
 
 def test_unit_and_context_limits_select_the_kernel():
-    assert pgd.uses_short_path(8, 8, 40, 16)           # 64 units x 640 tokens = 40960
-    assert pgd.uses_short_path(4, 8, 64, 16)           # 32 units x 1024 tokens
-    assert not pgd.uses_short_path(8, 8, 41, 16)       # 64 x 656 > 40960
-    assert not pgd.uses_short_path(9, 8, 8, 16)        # 72 units
-    assert not pgd.uses_short_path(1, 8, 65, 16)       # 1040 tokens
-    assert not pgd.uses_short_path(1, 8, 8, 16, num_splits=1)
+    assert pgd.uses_short_path(8, 8, 16, 40)           # 64 units x 640 tokens = 40960
+    assert pgd.uses_short_path(4, 8, 16, 64)           # 32 units x 1024 tokens
+    assert not pgd.uses_short_path(8, 8, 16, 41)       # 64 x 656 > 40960
+    assert not pgd.uses_short_path(9, 8, 16, 8)        # 72 units
+    assert not pgd.uses_short_path(1, 8, 16, 65)       # 1040 tokens
+    assert not pgd.uses_short_path(1, 8, 16, 8, num_splits=1)
     prev = pgd.set_short_context_tokens(256)
     assert prev == 1024
-    assert pgd.uses_short_path(1, 8, 16, 16) and not pgd.uses_short_path(1, 8, 17, 16)
+    assert pgd.uses_short_path(1, 8, 16, 16) and not pgd.uses_short_path(1, 8, 16, 17)
     pgd.set_short_context_tokens(0)
-    assert not pgd.uses_short_path(1, 8, 1, 16)
+    assert not pgd.uses_short_path(1, 8, 16, 1)
     assert pgd.set_short_context_tokens(-1) == 0
 
 
