@@ -127,9 +127,13 @@ template <bool FP8> constexpr long long kCtaShare = FP8 ? 140 : 96;
 // 16.5, nineteen 19.0)
 constexpr long long kMergeFixedBytes = 24ll << 20;
 constexpr long long kMergePartBytes = 1ll << 20;
-// Fixed cost of a segment in blocks of streaming time: about two stages
-// (measured on a batch of short sequences).
-template <int BS> constexpr int kSegCost = 2 * TOK / BS;
+// Fixed cost of a segment in blocks of streaming time: about three stages.
+// (A per-CTA timeline of the cascade suffix pass, whose parts are made of
+// many short segments, shows a one-stage segment taking 2-3 us against about
+// 0.7 us per stage inside a long one; charging 2, 3, 4 and 6 stages gave
+// 39.9, 39.3, 39.3 and 40.3 us a step there and left the ragged and
+// single-sequence batches unchanged.)
+template <int BS> constexpr int kSegCost = 3 * TOK / BS;
 // Blocks of a CTA's likely first unit asked of L2 during the prologue: three
 // stages (about the data HBM can deliver to each CTA while the prologue runs).
 template <int BS> constexpr int kPrefetchBlocks = 3 * TOK / BS;
