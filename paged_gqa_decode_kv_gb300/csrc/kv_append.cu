@@ -19,12 +19,32 @@
 
 namespace pgd {
 
+// 128-thread launch with programmatic stream serialization: the kernel may be
+// scheduled while the previous kernel of the stream finishes (it waits for it,
+// griddepcontrol.wait, before touching memory), which takes the launch
+// latency off the step.
+template <typename... P, typename... A>
+static cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, cudaStream_t stream, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __global__ void __launch_bounds__(128)
 kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                  uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                  const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
                  int pos_offset, int B, int T, int n_kv, int bs, int MB, int NB, int32_t *err) {
   constexpr int kVecPerRow = kHeadDim * 2 / 16;  // 16 uint4 per 256-byte row
+  pdl_wait();               // the previous kernel (which may read these slots) has completed
   pdl_launch_dependents();  // the attention that follows may start its prologue
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (b * T + j) * n_kv + g
   const int lane = threadIdx.x & 31;
@@ -63,11 +83,10 @@ cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache
   const long long rows = (long long)B * T * n_kv;
   if (rows == 0) return cudaSuccess;
   const int grid = (int)((rows + 3) / 4);
-  kv_append_kernel<<<grid, 128, 0, stream>>>(
-      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
-      static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), tables, pos, pos_offset, B,
-      T, n_kv, bs, MB, NB, err);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(grid), stream, static_cast<const uint4 *>(k_new),
+                    static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_cache),
+                    static_cast<uint4 *>(v_cache), tables, pos, pos_offset, B, T, n_kv, bs, MB, NB,
+                    err);
 }
 
 // kv_append into an 8-bit cache ("Ch. 6 Inference efficiency and serving",
@@ -85,6 +104,7 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
                      unsigned char *__restrict__ k_cache, unsigned char *__restrict__ v_cache,
                      const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
                      int pos_offset, int B, int n_kv, int bs, int MB, int NB, int32_t *err) {
+  pdl_wait();               // the previous kernel (which may read these slots) has completed
   pdl_launch_dependents();  // the attention that follows may start its prologue
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -120,11 +140,10 @@ cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_c
   const int rows = B * n_kv;
   if (rows == 0) return cudaSuccess;
   const int grid = (rows + 3) / 4;
-  kv_append_fp8_kernel<<<grid, 128, 0, stream>>>(
-      static_cast<const uint4 *>(k_new), static_cast<const uint4 *>(v_new),
-      static_cast<unsigned char *>(k_cache), static_cast<unsigned char *>(v_cache), tables, pos,
-      pos_offset, B, n_kv, bs, MB, NB, err);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_fp8_kernel, dim3(grid), stream, static_cast<const uint4 *>(k_new),
+                    static_cast<const uint4 *>(v_new), static_cast<unsigned char *>(k_cache),
+                    static_cast<unsigned char *>(v_cache), tables, pos, pos_offset, B, n_kv, bs,
+                    MB, NB, err);
 }
 
 // Copy-on-write ("Module 10: inference and serving", section "Share only

@@ -659,6 +659,7 @@ __global__ void __launch_bounds__(128)
 mla_append_kernel(const uint4 *__restrict__ c_new, uint4 *__restrict__ cache,
                   const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
                   int pos_offset, int B, int bs, int MB, int NB, int32_t *err) {
+  pdl_wait();  // the previous kernel (which may read this slot) has completed
   pdl_launch_dependents();
   const int b = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (b >= B) return;
@@ -734,10 +735,20 @@ cudaError_t mla_append_launch(const void *c_new, void *cache, const int32_t *tab
                               const int32_t *pos, int pos_offset, int B, int bs, int MB, int NB,
                               int32_t *err, cudaStream_t stream) {
   if (B == 0) return cudaSuccess;
-  mla::mla_append_kernel<<<(B + 3) / 4, 128, 0, stream>>>(
-      static_cast<const uint4 *>(c_new), static_cast<uint4 *>(cache), tables, pos, pos_offset, B,
-      bs, MB, NB, err);
-  return cudaGetLastError();
+  // (launched with programmatic stream serialization: it may be scheduled
+  // while the previous kernel finishes, and waits for it before any access)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((B + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla::mla_append_kernel, static_cast<const uint4 *>(c_new),
+                            static_cast<uint4 *>(cache), tables, pos, pos_offset, B, bs, MB, NB,
+                            err);
 }
 
 }  // namespace pgd
