@@ -417,12 +417,14 @@ pgd_status pgd_append_decode_attention_fp8(void *out, const void *q, const void 
  * host memory: pgd_append_decode_attention (append at position
  * context_lens[b] - 1, then attention) on q_h, k_new_h, v_new_h and
  * context_lens_h, with the result in out_h -- all enqueued on `stream`.
- * q_h, k_new_h, v_new_h and out_h, when page-locked host memory that the
- * device addresses (as the CUDA runtime reports it) and 16-byte aligned, are
- * read and written in place by the kernels over the host link; otherwise
- * they go through the caller's device buffers (q_d, k_new_d, v_new_d, out_d)
- * and a copy each.  context_lens_h is always copied to context_lens_d.  The
- * host buffers must stay untouched until the stream has completed the step.
+ * q_h, k_new_h, v_new_h, context_lens_h and out_h, when page-locked host
+ * memory that the device addresses (as the CUDA runtime reports it) and
+ * 16-byte aligned, are read and written in place by the kernels over the host
+ * link; otherwise they go through the caller's device buffers (q_d, k_new_d,
+ * v_new_d, context_lens_d, out_d) and a copy each.  A copy breaks the chain
+ * of kernels that start while their predecessor finishes, so in-place buffers
+ * save about 5 us a step.  The host buffers must stay untouched until the
+ * stream has completed the step.
  * The cache, block tables and workspace stay on the device.  Shapes and rules
  * as above. */
 pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,

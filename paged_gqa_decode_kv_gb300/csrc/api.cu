@@ -994,17 +994,19 @@ static pgd_status decode_step_impl(bool fp8, void *out_h, const void *q_h, const
   const void *q_in = device_alias(q_h), *kn_in = device_alias(k_new_h),
              *vn_in = device_alias(v_new_h);
   void *out_to = device_alias(out_h);
+  const int32_t *cl_in = static_cast<const int32_t *>(device_alias(context_lens_h));
   cudaError_t e = cudaSuccess;
   if ((!q_in && (e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
       (!kn_in &&
        (e = cudaMemcpyAsync(k_new_d, k_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
       (!vn_in &&
        (e = cudaMemcpyAsync(v_new_d, v_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
-      (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4, cudaMemcpyHostToDevice,
-                           st)) != cudaSuccess)
+      (!cl_in && (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4,
+                                      cudaMemcpyHostToDevice, st)) != cudaSuccess))
     return cuda_fail(e, "decode step: host-to-device copy");
   s = append_then_attend(out_to ? out_to : out_d, q_in ? q_in : q_d, kn_in ? kn_in : k_new_d,
-                         vn_in ? vn_in : v_new_d, k_cache, v_cache, block_tables, context_lens_d,
+                         vn_in ? vn_in : v_new_d, k_cache, v_cache, block_tables,
+                         cl_in ? cl_in : context_lens_d,
                          B, n_q, n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes,
                          st, fp8);
   if (s != PGD_OK) return s;

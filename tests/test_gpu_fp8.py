@@ -136,6 +136,37 @@ def test_append_decode_attention_fp8_one_call(num_splits):
     compare(got, want, "fp8 append+attend splits=%d" % num_splits)
 
 
+@pytest.mark.parametrize("lens", [[5, 300, 17], [1, 16, 17, 700, 2048]], ids=["short", "tc"])
+@pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
+def test_decode_step_fp8_host_buffers(pinned, lens):
+    """The host-buffer step on an 8-bit pool: page-locked buffers read and
+    written in place, pageable ones copied, each on its own.  Output and pool
+    equal the device-buffer one-call step bit for bit, and the oracle."""
+    pb = _batch(len(lens), 32, 8, 16, lens, append=True)
+    kc0, vc0 = pb.k_cache.clone(), pb.v_cache.clone()
+    want = pgd.append_decode_attention_fp8(None, pb.q, pb.k_new, pb.v_new, kc0, vc0,
+                                           pb.block_tables, pb.context_lens, pb.scale)
+    want_k, want_v = oracle.kv_append_fp8(pb.k_cache.cpu(), pb.v_cache.cpu(), pb.k_new.cpu(),
+                                          pb.v_new.cpu(), pb.block_tables.cpu(),
+                                          pb.positions.cpu(), 16)
+    pin = lambda t: t.cpu().pin_memory()
+    page = lambda t: t.cpu().clone()
+    hq, hk, hv, ho, hc = {"all": (pin,) * 5, "none": (page,) * 5,
+                          "mixed": (page, pin, page, pin, pin)}[pinned]
+    q_h, kn_h, vn_h = hq(pb.q), hk(pb.k_new), hv(pb.v_new)
+    cl_h, out_h = hc(pb.context_lens), ho(torch.zeros_like(pb.q))
+    q_d, kn_d, vn_d = torch.empty_like(pb.q), torch.empty_like(pb.k_new), torch.empty_like(pb.v_new)
+    cl_d, out_d = torch.empty_like(pb.context_lens), torch.empty_like(pb.q)
+    ws = pgd.make_workspace(pb.batch, 32, 8)
+    pgd.decode_step(out_h, q_h, kn_h, vn_h, cl_h, out_d, q_d, kn_d, vn_d, cl_d, pb.k_cache,
+                    pb.v_cache, pb.block_tables, pb.scale, 0, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h, want.cpu())
+    assert np.array_equal(pb.k_cache.cpu().numpy(), want_k)
+    assert np.array_equal(pb.v_cache.cpu().numpy(), want_v)
+    compare(out_h, oracle_fp8(pb, want_k, want_v), "fp8 host-buffer step")
+
+
 @pytest.mark.parametrize("name", ["single_ctx512", "batch16_ctx8192", "mha40_batch4_ctx8192",
                                   "ragged64_g8", "single_ctx131072"])
 def test_workload_full_size_fp8(name):

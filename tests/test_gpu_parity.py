@@ -267,21 +267,23 @@ def test_copy_blocks_bit_exact():
     assert torch.equal(pb.v_cache.view(torch.int16), v0v)
 
 
+@pytest.mark.parametrize("lens", [[700, 16, 17, 1], [2048, 16, 17, 1]], ids=["short", "tc"])
 @pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
-def test_decode_step_host_buffers_match_device_path(pinned):
+def test_decode_step_host_buffers_match_device_path(pinned, lens):
     """Page-locked host buffers are read and written in place by the kernels,
     pageable ones go through the device buffers and copies (each buffer on its
-    own): every mix equals the device path bit for bit."""
+    own): every mix equals the device path bit for bit, on the short-context
+    kernel and on the tensor-core kernel."""
     B, n_q, n_kv, bs = 4, 32, 8, 16
-    pb = _batch(B, n_q, n_kv, bs, [700, 16, 17, 1], append=True)
+    pb = _batch(B, n_q, n_kv, bs, lens, append=True)
     ws = pgd.make_workspace(B, n_q, n_kv)
     pin = lambda t: t.cpu().pin_memory()
     page = lambda t: t.cpu().clone()
-    hq, hk, hv, ho = {"all": (pin,) * 4, "none": (page,) * 4,
-                      "mixed": (pin, page, pin, page)}[pinned]
+    hq, hk, hv, ho, hc = {"all": (pin,) * 5, "none": (page,) * 5,
+                          "mixed": (pin, page, pin, page, page)}[pinned]
     q_h = hq(pb.q)
     kn_h, vn_h = hk(pb.k_new), hv(pb.v_new)
-    cl_h = pin(pb.context_lens)
+    cl_h = hc(pb.context_lens)
     out_h = ho(torch.zeros_like(pb.q))
     q_d, kn_d, vn_d = torch.empty_like(pb.q), torch.empty_like(pb.k_new), torch.empty_like(pb.v_new)
     cl_d = torch.empty_like(pb.context_lens)
