@@ -155,7 +155,11 @@ struct Lay {
   static constexpr int OFF_VB = OFF_V + NSV * STAGE;
   static constexpr int OFF_Q = OFF_VB + VB_BYTES;  // Q double buffered by segment parity
   static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  // 8-bit cache: the key scales of the last NKS stages, f32 [NKS][TOK], copied
+  // out of each K stage by the q.k^T warp so that the stage frees with its MMA
+  static constexpr int NKS = 8;
+  static constexpr int OFF_KS = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_KS + (FP8 ? NKS * TOK * 4 : 0);
   static constexpr int OFF_RED = OFF_BAR + 512;    // f32 [2][4][RMAX] warp maxima
   static constexpr int OFF_LRED = OFF_RED + 2 * 4 * RMAX * 4;  // f32 [2][4][RMAX] warp sums
   static constexpr int OFF_MREF = OFF_LRED + 2 * 4 * RMAX * 4;  // f32 [2][RMAX] reference maxima
@@ -813,12 +817,12 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
   }
 
   if (tid == 0) {
-    // 8-bit cache: the softmax warps read each K stage's scales, so they too
-    // release K slots, and a Q buffer once they hold its scales; the V
-    // converter warps release the V slots.
+    // 8-bit cache: the whole q.k^T warp hands each stage's key scales to
+    // the softmax through m_ready; the softmax warps release a Q buffer once
+    // they hold its scales, and the V converter warps release the V slots.
     for (int i = 0; i < L::NSK; ++i) {
       mbar_init(&full_k[i], 1);
-      mbar_init(&empty_k[i], FP8 ? 1 + 4 : 1);
+      mbar_init(&empty_k[i], 1);
     }
     for (int i = 0; i < L::NSV; ++i) {
       mbar_init(&full_v[i], 1);
@@ -827,7 +831,7 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
     for (int i = 0; i < NSB; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
-      mbar_init(&m_ready[i], 1);
+      mbar_init(&m_ready[i], FP8 ? 32 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&p_full[i], 4);
@@ -952,7 +956,10 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
                                nullptr, nullptr, nullptr, nullptr, abort_flag, lane);
   } else if (warp == WARP_QK) {
     // ---------------------------------------------------- q.k^T issuer
-    if (lane == 0) {
+    // (one lane issues; under the 8-bit cache the whole warp first copies the
+    // stage's key scales into their ring, so that the K slot frees as soon
+    // as its q.k^T has completed)
+    if (FP8 || lane == 0) {
       const uint32_t q_base = smem_addr(smem + L::OFF_Q);
       SegCursor cur(sc);
       Segment sg;
@@ -962,14 +969,28 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         // Q of segment k is in buffer k & 1 (written by the K producer); it is
         // rewritten for segment k + 2 only after q_free signals that every
         // q.k^T of segment k has completed.
-        wait_or_abort(&q_ready[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
+        if (lane == 0)
+          wait_or_abort(&q_ready[k & 1], (uint32_t)(k >> 1) & 1u, abort_flag, p.err);
         const uint32_t q_seg = q_base + (uint32_t)((k & 1) * L::Q_BYTES);
         for (int st = 0; st < nstages; ++st, ++s) {
           const int slot = s % L::NSK, sb = s % NSB;
-          wait_or_abort(&full_k[slot], (uint32_t)(s / L::NSK) & 1u, abort_flag, p.err);
-          wait_or_abort(&s_free[sb], ((uint32_t)(s / NSB) & 1u) ^ 1u, abort_flag, p.err);
+          // (the key-scale slot s % NKS was last read for stage s - NKS, in
+          // an earlier softmax iteration than the one that freed S of s - NSB)
+          if (FP8 || lane == 0) {
+            wait_or_abort(&full_k[slot], (uint32_t)(s / L::NSK) & 1u, abort_flag, p.err);
+            wait_or_abort(&s_free[sb], ((uint32_t)(s / NSB) & 1u) ^ 1u, abort_flag, p.err);
+          }
+          if constexpr (FP8) {
+            // 16 token groups x 32 B of scales: lane l takes half l & 1 of group l >> 1
+            const int g = lane >> 1, hf = lane & 1;
+            const uint4 v = *reinterpret_cast<const uint4 *>(
+                smem + L::OFF_K + slot * L::STAGE + g * L::GROUP + 1024 + hf * 16);
+            *reinterpret_cast<uint4 *>(smem + L::OFF_KS + (s % L::NKS) * (TOK * 4) + g * 32 +
+                                       hf * 16) = v;
+            __syncwarp();
+          }
           tc_fence_after();
-          if (!*abort_flag) {
+          if (lane == 0 && !*abort_flag) {
             const uint32_t dS = tmem + col_s(sb);
             const uint32_t k_st = smem_addr(smem + L::OFF_K + slot * L::STAGE);
             if constexpr (FP8) {
@@ -996,17 +1017,20 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
                           kk > 0 ? 1u : 0u);
             }
           }
-          umma_commit(&s_full[sb]);
-          umma_commit(&empty_k[slot]);
+          if (lane == 0) {
+            umma_commit(&s_full[sb]);
+            umma_commit(&empty_k[slot]);
+          }
           // Hand the stage's invalid-block mask (written by the K producer
-          // before it armed full_k, which this thread acquired) to the softmax.
-          mbar_arrive(&m_ready[sb]);
+          // before it armed full_k, which lane 0 acquired) and, under the
+          // 8-bit cache, its key scales (each lane its own) to the softmax.
+          if (FP8 || lane == 0) mbar_arrive(&m_ready[sb]);
         }
-        umma_commit(&q_free[k & 1]);  // Q buffer reusable once these q.k^T complete
+        if (lane == 0) umma_commit(&q_free[k & 1]);  // Q buffer reusable once these complete
         ++k;
       }
       // every MMA has completed before tensor memory is released
-      if (s > 0) {
+      if (lane == 0 && s > 0) {
         umma_commit(&done[0]);
         mbar_wait_bounded(&done[0], 0);
       }
@@ -1114,21 +1138,16 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         int epos[SPI] = {};  // this row's token minus the first new token (T > 1)
         // Invalid-block mask of each stage: the K producer wrote it before
         // arming full_k; the q.k^T issuer acquired full_k and then released
-        // m_ready.  (Waiting on full_k here could alias under the bf16
-        // cache: a K stage is freed after its q.k^T alone, so full_k may run
-        // two phases ahead.)  The 8-entry mask ring cannot move on before
-        // these stages free their S buffers.
+        // m_ready.  (Waiting on full_k here could alias: a K stage is freed
+        // after its q.k^T alone, so full_k may run two phases ahead.)  The
+        // 8-entry mask ring cannot move on before these stages free their S
+        // buffers.
 #pragma unroll
         for (int u = 0; u < SPI; ++u) {
           if (u < n2) {
             const int su = s + u, sbu = su % NSB;
             wait_or_abort(&s_full[sbu], (uint32_t)(su / NSB) & 1u, abort_flag, p.err);
-            // (8-bit cache: K slots are released by these warps too, so
-            // full_k cannot run ahead and is waited on directly)
-            if (FP8)
-              wait_or_abort(&full_k[su % L::NSK], (uint32_t)(su / L::NSK) & 1u, abort_flag, p.err);
-            else
-              wait_or_abort(&m_ready[sbu], (uint32_t)(su / NSB) & 1u, abort_flag, p.err);
+            wait_or_abort(&m_ready[sbu], (uint32_t)(su / NSB) & 1u, abort_flag, p.err);
             msk[u] = stage_mask[su & 7];
             const int nb = min(SB, sg.n - (st + u) * SB);
             int nvalid = nb * BS;
@@ -1165,29 +1184,22 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
 
         float sc_[SPI][G];
         if constexpr (FP8) {
-          // Key scale of each token (the K slot is refilled only after these
-          // four warps release it, so waiting on full_k cannot alias), and at
-          // a segment's first stage the Q scales (the K producer wrote them
-          // before q_ready, which the q.k^T issuer acquired before m_ready).
+          // Key scale of each token (from the ring the q.k^T warp filled
+          // before m_ready), and at a segment's first stage the Q scales (the
+          // K producer wrote them before q_ready, which the q.k^T issuer
+          // acquired before m_ready).
           float ks[SPI] = {};
 #pragma unroll
-          for (int u = 0; u < SPI; ++u) {
-            if (u < n2) {
-              const int kslot = (s + u) % L::NSK;  // full_k already waited on above
-              ks[u] = *reinterpret_cast<const float *>(
-                  smem + L::OFF_K + kslot * L::STAGE + (t >> 3) * L::GROUP + 1024 + (t & 7) * 4);
-            }
-          }
+          for (int u = 0; u < SPI; ++u)
+            if (u < n2)
+              ks[u] = reinterpret_cast<const float *>(
+                  smem + L::OFF_KS)[((s + u) % L::NKS) * TOK + t];
           if (st == 0) {
 #pragma unroll
             for (int h = 0; h < G; ++h) qsc[h] = qscale[(k & 1) * 8 + h] * p.qk_scale_log2;
           }
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&empty_k[s % L::NSK]);
-            if (n2 > 1) mbar_arrive(&empty_k[(s + 1) % L::NSK]);
-            if (st == 0) mbar_arrive(&q_free[k & 1]);
-          }
+          if (lane == 0 && st == 0) mbar_arrive(&q_free[k & 1]);
 #pragma unroll
           for (int u = 0; u < SPI; ++u)
 #pragma unroll
