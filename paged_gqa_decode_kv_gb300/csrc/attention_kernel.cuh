@@ -179,6 +179,16 @@ static_assert((Lay<false>::OFF_MISC + 24) % 8 == 0 && (Lay<true>::OFF_MISC + 24)
 static_assert(smem_bytes<true>(PGD_MAX_BATCH) <= 232448, "8-bit layout exceeds 227 KB");
 
 __device__ __forceinline__ uint32_t col_s(int sb) { return (uint32_t)sb * 16u; }  // sb < NSB
+
+// 2^x by the hardware approximation, results below 2^-126 flushed to zero: a
+// probability is rounded to f16 (bf16) next, whose step near 1 is 2^-11
+// (2^-8), far above the approximation's error, and whose smallest value
+// (2^-24) lies far above the flush.
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ uint32_t col_o(int ob) { return 64u + (uint32_t)ob * 16u; }
 
 // ---------------------------------------------------------------- PTX helpers
@@ -1291,10 +1301,43 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
           if (u < n2) {
             const int su = s + u, pbuf = su & 1;
             uint32_t packed[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if constexpr (!FP8 && G >= 2) {
+#pragma unroll
+              for (int h = 0; h < G; h += 2) {
+                const float p0 =
+                    (valid[u] && tok[h] >= epos[u]) ? exp2_approx(sc_[u][h] - m_ref[h]) : 0.f;
+                const float p1 = (valid[u] && tok[h + 1] >= epos[u])
+                                     ? exp2_approx(sc_[u][h + 1] - m_ref[h + 1])
+                                     : 0.f;
+                const __nv_bfloat162 pb2 = __floats2bfloat162_rn(p0, p1);
+                const float2 back = __bfloat1622float2(pb2);
+                l_part[h] += back.x;
+                l_part[h + 1] += back.y;
+                packed[h >> 1] = *reinterpret_cast<const uint32_t *>(&pb2);
+              }
+            } else if constexpr (FP8 && G >= 2) {
+              // (two heads per conversion either way: under the 8-bit cache
+              // these warps share the SM's sub-partitions with the V
+              // converters, whose conversions dominate the issue slots)
+#pragma unroll
+              for (int h = 0; h < G; h += 2) {
+                const float p0 =
+                    (valid[u] && tok[h] >= epos[u]) ? exp2_approx(sc_[u][h] - m_ref[h]) : 0.f;
+                const float p1 = (valid[u] && tok[h + 1] >= epos[u])
+                                     ? exp2_approx(sc_[u][h + 1] - m_ref[h + 1])
+                                     : 0.f;
+                const __half2 ph = __floats2half2_rn(p0, p1);
+                const float2 back = __half22float2(ph);
+                l_part[h] += back.x;
+                l_part[h + 1] += back.y;
+                packed[h >> 1] = *reinterpret_cast<const uint32_t *>(&ph);
+              }
+            } else
 #pragma unroll
             for (int h = 0; h < G; ++h) {
-              const float pv =
-                  (valid[u] && tok[h] >= epos[u]) ? exp2f(sc_[u][h] - m_ref[h]) : 0.f;
+              const float pv = !(valid[u] && tok[h] >= epos[u]) ? 0.f
+                               : FP8 ? exp2_approx(sc_[u][h] - m_ref[h])
+                                     : exp2f(sc_[u][h] - m_ref[h]);
               uint16_t bits;
               if constexpr (FP8) {
                 const __half ph = __float2half_rn(pv);
