@@ -628,13 +628,18 @@ def run_ours(args, rank, world, local):
     # The plain decode paths time prepared C-ABI calls (arguments checked and
     # marshalled once per pool copy): the Python side of a regular binding
     # call costs about 10 us, more than a short-context step on the GPU.
-    prepared = not args.cascade and not T
+    # (multi-query verify: the one-call append + verify step, whose attention
+    # alone goes through the binding)
+    prepared = not args.cascade
+    prepared_attn = prepared and not T
     if prepared:
         op = "_fp8" if fp8 else ""
-        step_calls = [pgd.prepare("append_decode_attention" + op, out, pb.q, pb.k_new, pb.v_new,
+        step_op = "append_verify_attention" if T else "append_decode_attention" + op
+        step_calls = [pgd.prepare(step_op, out, pb.q, pb.k_new, pb.v_new,
                                   kc, vc, pb.block_tables, pb.context_lens, pb.scale,
                                   num_splits=args.splits, workspace=ws, stream=stream)
                       for kc, vc in pools]
+    if prepared_attn:
         attn_calls = [pgd.prepare("paged_decode_attention" + op, out, pb.q, kc, vc,
                                   pb.block_tables, pb.context_lens, pb.scale,
                                   num_splits=args.splits, workspace=ws, stream=stream)
@@ -651,7 +656,7 @@ def run_ours(args, rank, world, local):
                       pb.scale, num_splits=args.splits, workspace=ws, stream=stream)
 
     def attention_only():
-        if prepared:
+        if prepared_attn:
             attn_calls[it[0] % n_pools]()
             it[0] += 1
             return
@@ -723,9 +728,9 @@ def run_ours(args, rank, world, local):
     out_d = torch.empty_like(pb.q)
 
     if prepared:
-        e2e_calls = [pgd.prepare("decode_step", out_h, q_h, kn_h, vn_h, cl_h, out_d, q_d, kn_d,
-                                 vn_d, cl_d, kc, vc, pb.block_tables, pb.scale, args.splits, ws,
-                                 stream=stream) for kc, vc in pools]
+        e2e_calls = [pgd.prepare("verify_step" if T else "decode_step", out_h, q_h, kn_h, vn_h,
+                                 cl_h, out_d, q_d, kn_d, vn_d, cl_d, kc, vc, pb.block_tables,
+                                 pb.scale, args.splits, ws, stream=stream) for kc, vc in pools]
 
     def e2e_step():
         if prepared:
@@ -733,16 +738,6 @@ def run_ours(args, rank, world, local):
             it[0] += 1
             return
         kc, vc = next_pool()
-        if T:  # host buffers through the Python binding: H2D, append + verify, D2H
-            with torch.cuda.stream(stream):
-                q_d.copy_(q_h, non_blocking=True)
-                kn_d.copy_(kn_h, non_blocking=True)
-                vn_d.copy_(vn_h, non_blocking=True)
-                cl_d.copy_(cl_h, non_blocking=True)
-                append_attend(out_d, q_d, kn_d, vn_d, kc, vc, pb.block_tables, cl_d, pb.scale,
-                              num_splits=args.splits, stream=stream)
-                out_h.copy_(out_d, non_blocking=True)
-            return
         pgd.decode_step(out_h, q_h, kn_h, vn_h, cl_h, out_d, q_d, kn_d, vn_d, cl_d, kc, vc,
                         pb.block_tables, pb.scale, args.splits, ws, stream=stream)
 
@@ -846,9 +841,7 @@ def run_ours(args, rank, world, local):
                      "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms / K, 5)},
                     **({"path": "pgd_decode_step (host buffers; no cascade)"}
                        if args.cascade else
-                       {"path": "pinned host buffers copied on the stream, pgd_kv_append_tokens "
-                                "+ pgd_paged_verify_attention, output copied back"}
-                       if T else {})),
+                       {"path": "pgd_verify_step (host buffers)"} if T else {})),
         # kv_append + attention (cascade: + the prefix pass and the combine;
         # the short-context kernel appends in the same launch)
         "gpu_launches": (4 if args.cascade else 1 if short else 2) * K,

@@ -258,6 +258,38 @@ pgd_status pgd_paged_verify_attention(void *out, const void *q, const void *k_ca
                                       int32_t MB, int32_t NB, float scale, int32_t num_splits,
                                       void *workspace, size_t workspace_bytes, void *stream);
 
+/* pgd_append_verify_attention: one verify step in one call -- the T new
+ * tokens of every sequence appended at positions context_lens[b] - T + j
+ * (pgd_kv_append_tokens with positions = context_lens - T), then
+ * pgd_paged_verify_attention over the updated caches; the attention's CTAs
+ * run their prologue while the append runs.  Same arguments, layouts, rules
+ * and errors as those two calls; every argument is checked before the first
+ * launch.
+ *
+ * pgd_verify_step: the same step for a caller whose per-step tensors live in
+ * host memory -- q_h, k_new_h, v_new_h, context_lens_h in, out_h out -- with
+ * the handling of pgd_decode_step: page-locked host buffers that the device
+ * addresses (16-byte aligned) are read and written in place by the kernels
+ * over the host link, any other goes through its device buffer (q_d,
+ * k_new_d, v_new_d, context_lens_d, out_d) and a copy; everything is
+ * enqueued on `stream`, and the host buffers must stay untouched until the
+ * stream has completed the step.  The cache, block tables and workspace stay
+ * on the device. */
+pgd_status pgd_append_verify_attention(void *out, const void *q, const void *k_new,
+                                       const void *v_new, void *k_cache, void *v_cache,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       int32_t B, int32_t T, int32_t n_q, int32_t n_kv, int32_t d,
+                                       int32_t bs, int32_t MB, int32_t NB, float scale,
+                                       int32_t num_splits, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+pgd_status pgd_verify_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
+                           const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
+                           void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
+                           const int32_t *block_tables, int32_t B, int32_t T, int32_t n_q,
+                           int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB,
+                           float scale, int32_t num_splits, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* MLA latent cache (multi-head latent attention, absorbed form)           */
 /* ---------------------------------------------------------------------- */

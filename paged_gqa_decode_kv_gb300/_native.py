@@ -42,6 +42,10 @@ SIGNATURES = {
     "pgd_verify_workspace_size": ([_I, _I, _I, _I, _I, _I], _Z),
     "pgd_paged_verify_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                                     _I, _P, _Z, _P], _I),
+    "pgd_append_verify_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                                     _I, _F, _I, _P, _Z, _P], _I),
+    "pgd_verify_step": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                         _I, _I, _I, _F, _I, _P, _Z, _P], _I),
     "pgd_mla_workspace_size": ([_I, _I, _I], _Z),
     "pgd_mla_append": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _P], _I),
     "pgd_mla_decode_attention": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _Z,
@@ -323,8 +327,8 @@ class PreparedCall:
 def prepare(op: str, *args, **kwargs) -> PreparedCall:
     """A PreparedCall of one of the step calls, with the arguments that call
     takes: "paged_decode_attention", "paged_decode_attention_fp8",
-    "append_decode_attention", "append_decode_attention_fp8" or
-    "decode_step"."""
+    "append_decode_attention", "append_decode_attention_fp8", "decode_step",
+    "append_verify_attention" or "verify_step"."""
     if op == "paged_decode_attention":
         return PreparedCall(*_attention_call(False, *args, **kwargs))
     if op == "paged_decode_attention_fp8":
@@ -335,6 +339,10 @@ def prepare(op: str, *args, **kwargs) -> PreparedCall:
         return PreparedCall(*_append_attention_call(True, *args, **kwargs))
     if op == "decode_step":
         return PreparedCall(*_decode_step_call(*args, **kwargs))
+    if op == "append_verify_attention":
+        return PreparedCall(*_append_verify_call(*args, **kwargs))
+    if op == "verify_step":
+        return PreparedCall(*_verify_step_call(*args, **kwargs))
     raise ValueError("no prepared form of %r" % op)
 
 
@@ -383,6 +391,79 @@ def paged_verify_attention(out, q, k_cache, v_cache, block_tables, context_lens,
         B, T, n_q, n_kv, d, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+def _verify_workspace(workspace, B, T, n_q, n_kv, num_splits, device):
+    if workspace is None:
+        n = max(1, verify_workspace_size(B, T, n_q, n_kv, num_splits))
+        workspace = torch.zeros(n, dtype=torch.uint8, device=device)
+    return workspace
+
+
+def _append_verify_call(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                        scale, num_splits=0, workspace=None, stream=None):
+    for t, n in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (k_cache, "k_cache"),
+                 (v_cache, "v_cache")):
+        _need(t, torch.bfloat16, n)
+    _need(block_tables, torch.int32, "block_tables")
+    _need(context_lens, torch.int32, "context_lens")
+    B, T, n_q, d = q.shape
+    NB, n_kv, bs, _ = _cache_dims(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, "out")
+    workspace = _verify_workspace(workspace, B, T, n_q, n_kv, num_splits, q.device)
+    MB = block_tables.shape[1]
+    return "pgd_append_verify_attention", (
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), B, T, n_q, n_kv, d, bs, MB, NB, float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), out
+
+
+def append_verify_attention(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                            scale: float, num_splits: int = 0,
+                            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One verify step in one call: the T new tokens of every sequence
+    (k_new/v_new [B][T][n_kv][d]) appended at context_lens - T + j, then
+    paged_verify_attention over the updated caches (its prologue overlapping
+    the append)."""
+    name, args, out = _append_verify_call(out, q, k_new, v_new, k_cache, v_cache, block_tables,
+                                          context_lens, scale, num_splits, workspace, stream)
+    _check(getattr(lib(), name)(*args))
+    return out
+
+
+def _verify_step_call(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d,
+                      v_new_d, context_lens_d, k_cache, v_cache, block_tables, scale, num_splits,
+                      workspace, stream=None):
+    for t, n in ((out_h, "out_h"), (q_h, "q_h"), (k_new_h, "k_new_h"), (v_new_h, "v_new_h")):
+        _need(t, torch.bfloat16, n, cuda=False)
+    _need(context_lens_h, torch.int32, "context_lens_h", cuda=False)
+    _need(k_cache, torch.bfloat16, "k_cache")
+    B, T, n_q, d = q_h.shape
+    NB, n_kv, bs, _ = _cache_dims(k_cache)
+    MB = block_tables.shape[1]
+    return "pgd_verify_step", (
+        _ptr(out_h), _ptr(q_h), _ptr(k_new_h), _ptr(v_new_h), _ptr(context_lens_h), _ptr(out_d),
+        _ptr(q_d), _ptr(k_new_d), _ptr(v_new_d), _ptr(context_lens_d), _ptr(k_cache),
+        _ptr(v_cache), _ptr(block_tables), B, T, n_q, n_kv, d, bs, MB, NB, float(scale),
+        int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), None
+
+
+def verify_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d, v_new_d,
+                context_lens_d, k_cache, v_cache, block_tables, scale: float, num_splits: int,
+                workspace: torch.Tensor, stream=None) -> None:
+    """One verify step with host inputs/outputs (q and out [B][T][n_q][d],
+    k_new/v_new [B][T][n_kv][d]): append at context_lens - T + j, then verify
+    attention, all on `stream`.  Page-locked (pinned) host tensors are read
+    and written in place by the kernels; pageable ones go through the given
+    device tensors and a copy each."""
+    name, args, _ = _verify_step_call(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d,
+                                      k_new_d, v_new_d, context_lens_d, k_cache, v_cache,
+                                      block_tables, scale, num_splits, workspace, stream)
+    _check(getattr(lib(), name)(*args))
 
 
 def _mla_pool_dims(pool: torch.Tensor) -> Tuple[int, int, int]:

@@ -545,6 +545,17 @@ int32_t pgd_attention_grid(int32_t B, int32_t n_q, int32_t n_kv, int32_t bs, int
   return grid;
 }
 
+// Checks of a verify call (T new tokens per sequence) beyond those of a
+// decode call.
+static pgd_status check_verify(int32_t B, int32_t T, int32_t n_q, int32_t n_kv) {
+  if (T < 1) return fail(PGD_ERR_INVALID_ARG, "T = %d", T);
+  if (unit_rows(T, n_q / n_kv) == 0)
+    return fail(PGD_ERR_UNSUPPORTED, "T * (n_q / n_kv) = %d > 16 query rows per KV head",
+                T * (n_q / n_kv));
+  if ((long long)B * T * n_q >= 0x7fffffffLL) return fail(PGD_ERR_INVALID_ARG, "B * T * n_q");
+  return PGD_OK;
+}
+
 size_t pgd_verify_workspace_size(int32_t B, int32_t T, int32_t n_q, int32_t n_kv, int32_t d,
                                  int32_t num_splits) {
   if (B < 0 || n_kv <= 0 || n_q <= 0 || n_q % n_kv || d != kHeadDim || num_splits < 0) return 0;
@@ -574,17 +585,58 @@ pgd_status pgd_paged_verify_attention(void *out, const void *q, const void *k_ca
   pgd_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, B,
                                       n_q, n_kv, d, bs, MB, NB, scale, num_splits);
   if (s != PGD_OK) return s;
-  if (T < 1) return fail(PGD_ERR_INVALID_ARG, "T = %d", T);
-  if (unit_rows(T, n_q / n_kv) == 0)
-    return fail(PGD_ERR_UNSUPPORTED, "T * (n_q / n_kv) = %d > 16 query rows per KV head",
-                T * (n_q / n_kv));
-  if ((long long)B * T * n_q >= 0x7fffffffLL) return fail(PGD_ERR_INVALID_ARG, "B * T * n_q");
+  if ((s = check_verify(B, T, n_q, n_kv)) != PGD_OK) return s;
   if (B == 0) return ok();
   PreparedAttention pa;
   s = prepare_attention(out, q, k_cache, v_cache, block_tables, context_lens, B, n_q, n_kv, bs, MB,
                         NB, scale, num_splits, workspace, workspace_bytes, &pa, false, T);
   if (s != PGD_OK) return s;
   s = launch_prepared(pa, static_cast<cudaStream_t>(stream));
+  return s == PGD_OK ? ok() : s;
+}
+
+// kv_append of the T new tokens at context_lens[b] - T + j, then the verify
+// attention over the updated caches, told (as in append_then_attend) that
+// the kernel before it writes only the caches.  Every check runs before the
+// first launch.
+static pgd_status append_then_verify(void *out, const void *q, const void *k_new,
+                                     const void *v_new, void *k_cache, void *v_cache,
+                                     const int32_t *tables, const int32_t *ctx, int32_t B,
+                                     int32_t T, int32_t n_q, int32_t n_kv, int32_t bs, int32_t MB,
+                                     int32_t NB, float scale, int32_t num_splits, void *workspace,
+                                     size_t workspace_bytes, cudaStream_t stream) {
+  if (!k_new || !v_new) return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  if ((long long)B * T * n_kv > 0x7ffffffcLL)
+    return fail(PGD_ERR_INVALID_ARG, "B * T * n_kv too large");
+  PreparedAttention pa;
+  pgd_status s = prepare_attention(out, q, k_cache, v_cache, tables, ctx, B, n_q, n_kv, bs, MB,
+                                   NB, scale, num_splits, workspace, workspace_bytes, &pa, false,
+                                   T);
+  if (s != PGD_OK) return s;
+  cudaError_t e = kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -T, B, T, n_kv,
+                                   bs, MB, NB, pa.p.err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  pa.p.wait_late = 1;
+  return launch_prepared(pa, stream);
+}
+
+pgd_status pgd_append_verify_attention(void *out, const void *q, const void *k_new,
+                                       const void *v_new, void *k_cache, void *v_cache,
+                                       const int32_t *block_tables, const int32_t *context_lens,
+                                       int32_t B, int32_t T, int32_t n_q, int32_t n_kv, int32_t d,
+                                       int32_t bs, int32_t MB, int32_t NB, float scale,
+                                       int32_t num_splits, void *workspace,
+                                       size_t workspace_bytes, void *stream) {
+  pgd_status s = check_attention_args(out, q, k_cache, v_cache, block_tables, context_lens, B,
+                                      n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if ((s = check_verify(B, T, n_q, n_kv)) != PGD_OK) return s;
+  if (B == 0) return ok();
+  s = append_then_verify(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, B, T,
+                         n_q, n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes,
+                         static_cast<cudaStream_t>(stream));
   return s == PGD_OK ? ok() : s;
 }
 
@@ -961,6 +1013,44 @@ static void *device_alias(const void *h) {
   return a.devicePointer;
 }
 
+}  // extern "C"
+
+// The host half of a step with host buffers: page-locked host buffers that
+// the device addresses (16-byte aligned) are read -- q, k_new, v_new, the
+// context lengths -- and written -- out -- in place by the kernels over the
+// host link, instead of through a copy each (a copy in the stream would also
+// end the chain of kernels launched while their predecessor runs); any other
+// buffer goes through its device buffer and a copy.  `launch` enqueues the
+// step's kernels on the pointers it is given.  qb: bytes of q (and out), kvb:
+// bytes of k_new (and v_new).
+template <typename Launch>
+static pgd_status host_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
+                            const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
+                            void *v_new_d, int32_t *context_lens_d, int32_t B, size_t qb,
+                            size_t kvb, cudaStream_t st, Launch launch) {
+  const void *q_in = device_alias(q_h), *kn_in = device_alias(k_new_h),
+             *vn_in = device_alias(v_new_h);
+  void *out_to = device_alias(out_h);
+  const int32_t *cl_in = static_cast<const int32_t *>(device_alias(context_lens_h));
+  cudaError_t e = cudaSuccess;
+  if ((!q_in && (e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
+      (!kn_in &&
+       (e = cudaMemcpyAsync(k_new_d, k_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
+      (!vn_in &&
+       (e = cudaMemcpyAsync(v_new_d, v_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
+      (!cl_in && (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4,
+                                      cudaMemcpyHostToDevice, st)) != cudaSuccess))
+    return cuda_fail(e, "host-buffer step: host-to-device copy");
+  pgd_status s = launch(out_to ? out_to : out_d, q_in ? q_in : q_d, kn_in ? kn_in : k_new_d,
+                        vn_in ? vn_in : v_new_d, cl_in ? cl_in : context_lens_d, st);
+  if (s != PGD_OK) return s;
+  if (!out_to && (e = cudaMemcpyAsync(out_h, out_d, qb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "host-buffer step: device-to-host copy");
+  return ok();
+}
+
+extern "C" {
+
 static pgd_status decode_step_impl(bool fp8, void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
                            const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
                            void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
@@ -984,35 +1074,15 @@ static pgd_status decode_step_impl(bool fp8, void *out_h, const void *q_h, const
                           fp8);
     if (s != PGD_OK) return s;
   }
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t qb = (size_t)B * n_q * kHeadDim * 2, kvb = (size_t)B * n_kv * kHeadDim * 2;
-  // Page-locked host buffers that the device addresses (16-byte aligned)
-  // are read -- q, k_new, v_new -- and written -- out -- in place by the
-  // kernels over the host link, instead of through a copy each; any other
-  // buffer goes through its device buffer and a copy.  The context lengths,
-  // which every CTA reads in its prologue, are always copied.
-  const void *q_in = device_alias(q_h), *kn_in = device_alias(k_new_h),
-             *vn_in = device_alias(v_new_h);
-  void *out_to = device_alias(out_h);
-  const int32_t *cl_in = static_cast<const int32_t *>(device_alias(context_lens_h));
-  cudaError_t e = cudaSuccess;
-  if ((!q_in && (e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
-      (!kn_in &&
-       (e = cudaMemcpyAsync(k_new_d, k_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
-      (!vn_in &&
-       (e = cudaMemcpyAsync(v_new_d, v_new_h, kvb, cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
-      (!cl_in && (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4,
-                                      cudaMemcpyHostToDevice, st)) != cudaSuccess))
-    return cuda_fail(e, "decode step: host-to-device copy");
-  s = append_then_attend(out_to ? out_to : out_d, q_in ? q_in : q_d, kn_in ? kn_in : k_new_d,
-                         vn_in ? vn_in : v_new_d, k_cache, v_cache, block_tables,
-                         cl_in ? cl_in : context_lens_d,
-                         B, n_q, n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes,
-                         st, fp8);
-  if (s != PGD_OK) return s;
-  if (!out_to && (e = cudaMemcpyAsync(out_h, out_d, qb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-    return cuda_fail(e, "decode step: device-to-host copy");
-  return ok();
+  return host_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d, v_new_d,
+                   context_lens_d, B, qb, kvb, static_cast<cudaStream_t>(stream),
+                   [&](void *o, const void *q, const void *kn, const void *vn, const int32_t *cl,
+                       cudaStream_t st) {
+                     return append_then_attend(o, q, kn, vn, k_cache, v_cache, block_tables, cl,
+                                               B, n_q, n_kv, bs, MB, NB, scale, num_splits,
+                                               workspace, workspace_bytes, st, fp8);
+                   });
 }
 
 pgd_status pgd_decode_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
@@ -1037,6 +1107,43 @@ pgd_status pgd_decode_step_fp8(void *out_h, const void *q_h, const void *k_new_h
   return decode_step_impl(true, out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d,
                           v_new_d, context_lens_d, k_cache, v_cache, block_tables, B, n_q, n_kv, d,
                           bs, MB, NB, scale, num_splits, workspace, workspace_bytes, stream);
+}
+
+pgd_status pgd_verify_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
+                           const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
+                           void *v_new_d, int32_t *context_lens_d, void *k_cache, void *v_cache,
+                           const int32_t *block_tables, int32_t B, int32_t T, int32_t n_q,
+                           int32_t n_kv, int32_t d, int32_t bs, int32_t MB, int32_t NB,
+                           float scale, int32_t num_splits, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+  pgd_status s = check_attention_args(out_d, q_d, k_cache, v_cache, block_tables, context_lens_d,
+                                      B, n_q, n_kv, d, bs, MB, NB, scale, num_splits);
+  if (s != PGD_OK) return s;
+  if ((s = check_verify(B, T, n_q, n_kv)) != PGD_OK) return s;
+  if (B == 0) return ok();
+  if (!out_h || !q_h || !k_new_h || !v_new_h || !context_lens_h || !k_new_d || !v_new_d)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(k_new_d, 16) || !aligned(v_new_d, 16))
+    return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
+  if ((long long)B * T * n_kv > 0x7ffffffcLL)
+    return fail(PGD_ERR_INVALID_ARG, "B * T * n_kv too large");
+  {
+    // every check of the device half runs before the first copy is enqueued
+    PreparedAttention pa;
+    s = prepare_attention(out_d, q_d, k_cache, v_cache, block_tables, context_lens_d, B, n_q,
+                          n_kv, bs, MB, NB, scale, num_splits, workspace, workspace_bytes, &pa,
+                          false, T);
+    if (s != PGD_OK) return s;
+  }
+  const size_t qb = (size_t)B * T * n_q * kHeadDim * 2, kvb = (size_t)B * T * n_kv * kHeadDim * 2;
+  return host_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d, v_new_d,
+                   context_lens_d, B, qb, kvb, static_cast<cudaStream_t>(stream),
+                   [&](void *o, const void *q, const void *kn, const void *vn, const int32_t *cl,
+                       cudaStream_t st) {
+                     return append_then_verify(o, q, kn, vn, k_cache, v_cache, block_tables, cl,
+                                               B, T, n_q, n_kv, bs, MB, NB, scale, num_splits,
+                                               workspace, workspace_bytes, st);
+                   });
 }
 
 pgd_status pgd_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_ids,
