@@ -68,6 +68,7 @@ def _attn(L, **kw):
     (dict(n_q=7, n_kv=2), _native.ERR_INVALID_ARG),
     (dict(B=-1), _native.ERR_INVALID_ARG),
     (dict(B=5000), _native.ERR_UNSUPPORTED),
+    (dict(B=2049), _native.ERR_UNSUPPORTED),              # one past PGD_MAX_BATCH
     (dict(scale=0.0), _native.ERR_INVALID_ARG),
     (dict(scale=float("inf")), _native.ERR_INVALID_ARG),
     (dict(q=None), _native.ERR_INVALID_ARG),

@@ -70,6 +70,35 @@ def test_attention_ragged_many(G, bs):
         compare(gpu_attention(pb, num_splits=splits), want, "G=%d bs=%d splits=%d" % (G, bs, splits))
 
 
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_maximum_batch(kv):
+    """B = PGD_MAX_BATCH (2048) sequences of 1..100 tokens: the largest cost
+    prefix the kernel keeps in shared memory, 4096 units over the SMs, the
+    append of every sequence's token; against the oracle."""
+    g = torch.Generator().manual_seed(2048)
+    B = 2048
+    lens = torch.randint(1, 101, (B,), generator=g).tolist()
+    pb = _batch(B, 8, 2, 16, lens, seed=2048, append=True, kv_format=kv)
+    if kv == "fp8":
+        want_k, want_v = oracle.kv_append_fp8(pb.k_cache.cpu(), pb.v_cache.cpu(),
+                                              pb.k_new.cpu(), pb.v_new.cpu(),
+                                              pb.block_tables.cpu(), pb.positions.cpu(), 16)
+        want = oracle.paged_attention_fp8(pb.q.cpu(), want_k, want_v, pb.block_tables.cpu(),
+                                          pb.context_lens.cpu(), pb.scale, 16)
+        got = pgd.append_decode_attention_fp8(None, pb.q, pb.k_new, pb.v_new, pb.k_cache,
+                                              pb.v_cache, pb.block_tables, pb.context_lens,
+                                              pb.scale)
+    else:
+        want, want_k, want_v = oracle_append_then_attend(pb)
+        got = pgd.append_decode_attention(None, pb.q, pb.k_new, pb.v_new, pb.k_cache, pb.v_cache,
+                                          pb.block_tables, pb.context_lens, pb.scale)
+    torch.cuda.synchronize()
+    bits = (lambda t: t.cpu().numpy()) if kv == "fp8" else cache_bits
+    assert np.array_equal(bits(pb.k_cache), want_k)
+    assert np.array_equal(bits(pb.v_cache), want_v)
+    compare(got, want, "B = 2048 (%s)" % kv)
+
+
 def test_workspace_reuse_across_calls():
     # the per-unit arrival counters must return to zero after every call
     pb = _batch(3, 16, 4, 16, [500, 33, 1024])
