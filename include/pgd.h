@@ -271,10 +271,11 @@ pgd_status pgd_paged_verify_attention(void *out, const void *q, const void *k_ca
  * the handling of pgd_decode_step: page-locked host buffers that the device
  * addresses (16-byte aligned) are read and written in place by the kernels
  * over the host link, any other goes through its device buffer (q_d,
- * k_new_d, v_new_d, context_lens_d, out_d) and a copy; everything is
- * enqueued on `stream`, and the host buffers must stay untouched until the
- * stream has completed the step.  The cache, block tables and workspace stay
- * on the device. */
+ * k_new_d, v_new_d, context_lens_d, out_d) and a copy (inputs all read in
+ * place must hold the step's values when the call is made, as there);
+ * everything is enqueued on `stream`, and the host buffers must stay
+ * untouched until the stream has completed the step.  The cache, block
+ * tables and workspace stay on the device. */
 pgd_status pgd_append_verify_attention(void *out, const void *q, const void *k_new,
                                        const void *v_new, void *k_cache, void *v_cache,
                                        const int32_t *block_tables, const int32_t *context_lens,
@@ -455,7 +456,10 @@ pgd_status pgd_append_decode_attention_fp8(void *out, const void *q, const void 
  * link; otherwise they go through the caller's device buffers (q_d, k_new_d,
  * v_new_d, context_lens_d, out_d) and a copy each.  A copy breaks the chain
  * of kernels that start while their predecessor finishes, so in-place buffers
- * save about 5 us a step.  The host buffers must stay untouched until the
+ * save about 5 us a step.  When all four inputs are read in place, the
+ * kernels may read them before earlier work in the stream has finished: they
+ * must hold the step's values when the call is made (not be filled by work
+ * enqueued before it).  The host buffers must stay untouched until the
  * stream has completed the step.
  * The cache, block tables and workspace stay on the device.  Shapes and rules
  * as above. */

@@ -34,11 +34,11 @@ int mla_heads_per_cta();
 cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
                                  void *v_cache, const int32_t *tables, const int32_t *pos,
                                  int pos_offset, int B, int n_kv, int bs, int MB, int NB,
-                                 int32_t *err, cudaStream_t stream);
+                                 int32_t *err, cudaStream_t stream, int early = 0);
 cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                              const int32_t *tables, const int32_t *pos, int pos_offset, int B,
                              int T, int n_kv, int bs, int MB, int NB, int32_t *err,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int early = 0);
 cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src_ids,
                                const int32_t *dst_ids, int n, int n_kv, int bs, int NB,
                                int32_t *err, cudaStream_t stream);
@@ -300,7 +300,7 @@ bool short_path(const PreparedAttention &pa, int32_t num_splits, int32_t MB, int
 // The short-context kernel on a prepared call's arguments; with k_new and
 // v_new it appends the new token first, in the same launch.
 pgd_status launch_short(const PreparedAttention &pa, const void *k_new, const void *v_new,
-                        void *k_cache, void *v_cache, cudaStream_t stream) {
+                        void *k_cache, void *v_cache, cudaStream_t stream, bool early = false) {
   ShortParams sp;
   sp.out = pa.p.out;
   sp.q = pa.p.q;
@@ -317,6 +317,7 @@ pgd_status launch_short(const PreparedAttention &pa, const void *k_new, const vo
   sp.NB = pa.p.NB;
   sp.qk_scale_log2 = pa.p.qk_scale_log2;
   sp.fp8 = pa.fp8 ? 1 : 0;
+  sp.early = early ? 1 : 0;
   sp.err = pa.p.err;
   cudaError_t e = short_attention_launch(sp, pa.G, pa.bs, stream);
   if (e != cudaSuccess) return cuda_fail(e, "short-context attention launch");
@@ -349,13 +350,15 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
 // caches.  Every check runs before the first launch.  The attention kernel
 // is told that the kernel before it (kv_append) writes only the caches, so
 // its CTAs run their prologue while kv_append runs and wait only before the
-// first cache read.
+// first cache read.  `early`: q, k_new, v_new and ctx are caller memory that
+// no kernel of the stream writes (page-locked host buffers), which the
+// kernels may read before the previous kernel has completed.
 pgd_status append_then_attend(void *out, const void *q, const void *k_new, const void *v_new,
                               void *k_cache, void *v_cache, const int32_t *tables,
                               const int32_t *ctx, int32_t B, int32_t n_q, int32_t n_kv,
                               int32_t bs, int32_t MB, int32_t NB, float scale, int32_t num_splits,
                               void *workspace, size_t workspace_bytes, cudaStream_t stream,
-                              bool fp8 = false) {
+                              bool fp8 = false, bool early = false) {
   if (!k_new || !v_new) return fail(PGD_ERR_INVALID_ARG, "null pointer");
   if (!aligned(k_new, 16) || !aligned(v_new, 16))
     return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
@@ -364,11 +367,11 @@ pgd_status append_then_attend(void *out, const void *q, const void *k_new, const
                                    NB, scale, num_splits, workspace, workspace_bytes, &pa, fp8);
   if (s != PGD_OK) return s;
   if (short_path(pa, num_splits, MB, bs))  // one launch: the append is fused
-    return launch_short(pa, k_new, v_new, k_cache, v_cache, stream);
+    return launch_short(pa, k_new, v_new, k_cache, v_cache, stream, early);
   cudaError_t e = fp8 ? kv_append_fp8_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B,
-                                             n_kv, bs, MB, NB, pa.p.err, stream)
+                                             n_kv, bs, MB, NB, pa.p.err, stream, early)
                       : kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B, 1,
-                                         n_kv, bs, MB, NB, pa.p.err, stream);
+                                         n_kv, bs, MB, NB, pa.p.err, stream, early);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   pa.p.wait_late = 1;
   return launch_prepared(pa, stream);
@@ -604,7 +607,8 @@ static pgd_status append_then_verify(void *out, const void *q, const void *k_new
                                      const int32_t *tables, const int32_t *ctx, int32_t B,
                                      int32_t T, int32_t n_q, int32_t n_kv, int32_t bs, int32_t MB,
                                      int32_t NB, float scale, int32_t num_splits, void *workspace,
-                                     size_t workspace_bytes, cudaStream_t stream) {
+                                     size_t workspace_bytes, cudaStream_t stream,
+                                     bool early = false) {
   if (!k_new || !v_new) return fail(PGD_ERR_INVALID_ARG, "null pointer");
   if (!aligned(k_new, 16) || !aligned(v_new, 16))
     return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
@@ -616,7 +620,7 @@ static pgd_status append_then_verify(void *out, const void *q, const void *k_new
                                    T);
   if (s != PGD_OK) return s;
   cudaError_t e = kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -T, B, T, n_kv,
-                                   bs, MB, NB, pa.p.err, stream);
+                                   bs, MB, NB, pa.p.err, stream, early);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   pa.p.wait_late = 1;
   return launch_prepared(pa, stream);
@@ -1021,8 +1025,10 @@ static void *device_alias(const void *h) {
 // host link, instead of through a copy each (a copy in the stream would also
 // end the chain of kernels launched while their predecessor runs); any other
 // buffer goes through its device buffer and a copy.  `launch` enqueues the
-// step's kernels on the pointers it is given.  qb: bytes of q (and out), kvb:
-// bytes of k_new (and v_new).
+// step's kernels on the pointers it is given, told whether every input is
+// read in place (then no kernel of the stream writes them, and the kernels
+// may read them before the previous kernel has completed).  qb: bytes of q
+// (and out), kvb: bytes of k_new (and v_new).
 template <typename Launch>
 static pgd_status host_step(void *out_h, const void *q_h, const void *k_new_h, const void *v_new_h,
                             const int32_t *context_lens_h, void *out_d, void *q_d, void *k_new_d,
@@ -1041,8 +1047,9 @@ static pgd_status host_step(void *out_h, const void *q_h, const void *k_new_h, c
       (!cl_in && (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4,
                                       cudaMemcpyHostToDevice, st)) != cudaSuccess))
     return cuda_fail(e, "host-buffer step: host-to-device copy");
+  const bool in_place = q_in && kn_in && vn_in && cl_in;
   pgd_status s = launch(out_to ? out_to : out_d, q_in ? q_in : q_d, kn_in ? kn_in : k_new_d,
-                        vn_in ? vn_in : v_new_d, cl_in ? cl_in : context_lens_d, st);
+                        vn_in ? vn_in : v_new_d, cl_in ? cl_in : context_lens_d, st, in_place);
   if (s != PGD_OK) return s;
   if (!out_to && (e = cudaMemcpyAsync(out_h, out_d, qb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
     return cuda_fail(e, "host-buffer step: device-to-host copy");
@@ -1078,10 +1085,10 @@ static pgd_status decode_step_impl(bool fp8, void *out_h, const void *q_h, const
   return host_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d, v_new_d,
                    context_lens_d, B, qb, kvb, static_cast<cudaStream_t>(stream),
                    [&](void *o, const void *q, const void *kn, const void *vn, const int32_t *cl,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool in_place) {
                      return append_then_attend(o, q, kn, vn, k_cache, v_cache, block_tables, cl,
                                                B, n_q, n_kv, bs, MB, NB, scale, num_splits,
-                                               workspace, workspace_bytes, st, fp8);
+                                               workspace, workspace_bytes, st, fp8, in_place);
                    });
 }
 
@@ -1139,10 +1146,10 @@ pgd_status pgd_verify_step(void *out_h, const void *q_h, const void *k_new_h, co
   return host_step(out_h, q_h, k_new_h, v_new_h, context_lens_h, out_d, q_d, k_new_d, v_new_d,
                    context_lens_d, B, qb, kvb, static_cast<cudaStream_t>(stream),
                    [&](void *o, const void *q, const void *kn, const void *vn, const int32_t *cl,
-                       cudaStream_t st) {
+                       cudaStream_t st, bool in_place) {
                      return append_then_verify(o, q, kn, vn, k_cache, v_cache, block_tables, cl,
                                                B, T, n_q, n_kv, bs, MB, NB, scale, num_splits,
-                                               workspace, workspace_bytes, st);
+                                               workspace, workspace_bytes, st, in_place);
                    });
 }
 

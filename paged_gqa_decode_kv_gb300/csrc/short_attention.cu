@@ -29,8 +29,8 @@
 // With k_new / v_new given, the new token's K/V are first written at
 // position ctx - 1 exactly as kv_append does ("LLM inference systems
 // engineering", 2.1.3), by the CTA whose range holds that position (always
-// the last of the cluster), which also takes the token's values from k_new /
-// v_new directly: one launch for the whole decode step.
+// the last of the cluster), which also keeps the token's values in shared
+// memory for its own loads: one launch for the whole decode step.
 //
 // Tokens are masked exactly as in the large kernel: positions past the
 // context and blocks whose id is outside [0, NB) (flagged) take no weight.
@@ -91,20 +91,25 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
   __shared__ float st_o[G][kHeadDim];
   __shared__ __align__(16) unsigned char nk8[kHeadDim], nv8[kHeadDim];  // the appended token,
   __shared__ float nks, nvs;                                            // quantised (8-bit)
+  __shared__ uint4 nkb[kHeadDim / 8], nvb[kHeadDim / 8];  // the appended token (bf16)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t rank = cluster_ctarank();
   const int unit = (int)blockIdx.x / CL;
   const int b = unit / p.n_kv, g = unit % p.n_kv;
-  // Inputs may come from the previous kernel of the stream.
-  pdl_wait();
-  pdl_launch_dependents();
-
-  // Context length, table row and query rows, all loads in flight together.
-  const int c = __ldg(p.ctx + b);
-  const int32_t *trow = p.tables + (size_t)b * p.MB;
-  if (tid < p.MB && tid < MAXB) tbl[tid] = __ldg(trow + tid);
-  {
+  // Context length, query rows and (in warp 0 of the cluster's last CTA,
+  // whose range always holds the appended token) the new token's K/V row:
+  // all loads in flight together.  They may come from the previous kernel
+  // of the stream, so they wait for it -- unless they live in caller memory
+  // that no kernel writes (`early`), where they overlap its end.
+  const bool appender = p.k_new != nullptr && rank == CL - 1 && warp == 0;
+  int c = 0;
+  uint4 raw_new = make_uint4(0, 0, 0, 0);
+  auto load_inputs = [&]() {
+    c = __ldg(p.ctx + b);
+    if (appender)
+      raw_new = __ldg(reinterpret_cast<const uint4 *>(lane < 16 ? p.k_new : p.v_new) +
+                      (size_t)unit * VEC + (lane & 15));
     const uint4 *qsrc = reinterpret_cast<const uint4 *>(p.q + ((size_t)b * p.n_q + g * G) * kHeadDim);
     for (int i = tid; i < G * VEC; i += THREADS) {
       float f[8];
@@ -112,7 +117,17 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
 #pragma unroll
       for (int e = 0; e < 8; ++e) qs[i / VEC][(i % VEC) * 8 + e] = f[e];
     }
-  }
+  };
+  // (The next launch is let in only after the wait either way: triggered
+  // before the loads, the next step's CTAs queue on the SMs beside these and
+  // the host-buffer step measured 8.0 us against 5.9.)
+  if (p.early) load_inputs();
+  pdl_wait();
+  pdl_launch_dependents();
+  if (!p.early) load_inputs();
+  // the table row (device memory a previous kernel may write)
+  const int32_t *trow = p.tables + (size_t)b * p.MB;
+  if (tid < p.MB && tid < MAXB) tbl[tid] = __ldg(trow + tid);
   const bool ctx_ok = c >= 1 && c <= p.MB * BS;
   if (!ctx_ok && tid == 0 && rank == 0 && g == 0) {
     atomicOr(p.err, PGD_DEVERR_BAD_CONTEXT);
@@ -132,8 +147,7 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
     const int blk = tbl[t_new / BS];
     const bool blk_ok = (unsigned)blk < (unsigned)p.NB;
     const int slot = t_new % BS, v = lane & 15;
-    const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(lane < 16 ? p.k_new : p.v_new) +
-                            (size_t)unit * VEC + v);
+    const uint4 raw = raw_new;  // (this warp is the appender)
     unsigned char *pool = lane < 16 ? p.k_cache : p.v_cache;
     if constexpr (FP8) {
       uint32_t w[2];
@@ -147,14 +161,17 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
         *reinterpret_cast<uint2 *>(group + code_offset8(slot, v)) = make_uint2(w[0], w[1]);
         if (v == 0) *reinterpret_cast<float *>(group + scale_offset8(slot)) = scale;
       }
-    } else if (blk_ok) {
-      const size_t dst = ((size_t)blk * p.n_kv + g) * (TILE / 16) + (size_t)(slot >> 3) * 128 +
-                         (size_t)v * 8 + (size_t)(slot & 7);
-      reinterpret_cast<uint4 *>(pool)[dst] = raw;
+    } else {
+      (lane < 16 ? nkb : nvb)[v] = raw;
+      if (blk_ok) {
+        const size_t dst = ((size_t)blk * p.n_kv + g) * (TILE / 16) +
+                           (size_t)(slot >> 3) * 128 + (size_t)v * 8 + (size_t)(slot & 7);
+        reinterpret_cast<uint4 *>(pool)[dst] = raw;
+      }
     }
     if (!blk_ok && lane == 0) atomicOr(p.err, PGD_DEVERR_BAD_BLOCK_ID);
   }
-  if (FP8) __syncthreads();  // the quantised row is read by the loaders below
+  __syncthreads();  // the appended row is read from shared memory by the loaders below
 
   // Thread roles in a piece: q.k -- token j = tid / 2, dims [64 hf, 64 hf + 64);
   // V staging -- bf16: token rows 8 k + tid / 16 (k < 8), 16-byte chunk
@@ -198,14 +215,14 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
             kr[k] = __ldg(reinterpret_cast<const uint4 *>(group + (4 * hf + k) * 128 + (slot & 7) * 16));
           ksc = __ldg(reinterpret_cast<const float *>(group + scale_offset8(slot)));
         }
-      } else {
-        const uint4 *src = (t == t_new)
-            ? reinterpret_cast<const uint4 *>(p.k_new) + (size_t)unit * VEC + hf * 8
-            : reinterpret_cast<const uint4 *>(tile) + (size_t)(slot >> 3) * 128 +
-                  (size_t)(hf * 8) * 8 + (size_t)(slot & 7);
-        const int step = (t == t_new) ? 1 : 8;  // chunks 128 B apart in a tile
+      } else if (t == t_new) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) kr[k] = __ldg(src + (size_t)k * step);
+        for (int k = 0; k < 8; ++k) kr[k] = nkb[hf * 8 + k];
+      } else {
+        const uint4 *src = reinterpret_cast<const uint4 *>(tile) + (size_t)(slot >> 3) * 128 +
+                           (size_t)(hf * 8) * 8 + (size_t)(slot & 7);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) kr[k] = __ldg(src + (size_t)k * 8);  // chunks 128 B apart
       }
     }
 #pragma unroll
@@ -228,7 +245,7 @@ __global__ void __launch_bounds__(THREADS) short_attention_kernel(const ShortPar
                                         (slot & 7) * 16));
           } else {
             vr[k] = (tv == t_new)
-                ? __ldg(reinterpret_cast<const uint4 *>(p.v_new) + (size_t)unit * VEC + cv)
+                ? nvb[cv]
                 : __ldg(reinterpret_cast<const uint4 *>(tile) + (size_t)(slot >> 3) * 128 +
                         (size_t)cv * 8 + (size_t)(slot & 7));
           }

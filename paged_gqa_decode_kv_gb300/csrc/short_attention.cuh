@@ -21,6 +21,9 @@ struct ShortParams {
   int B, n_q, n_kv, MB, NB;
   float qk_scale_log2;           // scale * log2(e)
   int fp8;                       // 1: 8-bit pools
+  int early;                     // 1: q, k_new, v_new and ctx live in caller memory that no
+                                 // earlier kernel of the stream writes (page-locked host
+                                 // buffers): read before waiting for the previous kernel
   int32_t *err;
 };
 
