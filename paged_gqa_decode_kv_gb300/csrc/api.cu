@@ -34,11 +34,11 @@ int mla_heads_per_cta();
 cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
                                  void *v_cache, const int32_t *tables, const int32_t *pos,
                                  int pos_offset, int B, int n_kv, int bs, int MB, int NB,
-                                 int32_t *err, cudaStream_t stream, int early = 0);
+                                 int32_t *err, cudaStream_t stream);
 cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                              const int32_t *tables, const int32_t *pos, int pos_offset, int B,
                              int T, int n_kv, int bs, int MB, int NB, int32_t *err,
-                             cudaStream_t stream, int early = 0);
+                             cudaStream_t stream);
 cudaError_t copy_blocks_launch(void *k_cache, void *v_cache, const int32_t *src_ids,
                                const int32_t *dst_ids, int n, int n_kv, int bs, int NB,
                                int32_t *err, cudaStream_t stream);
@@ -352,7 +352,7 @@ pgd_status launch_attention(void *out, const void *q, const void *k_cache, const
 // its CTAs run their prologue while kv_append runs and wait only before the
 // first cache read.  `early`: q, k_new, v_new and ctx are caller memory that
 // no kernel of the stream writes (page-locked host buffers), which the
-// kernels may read before the previous kernel has completed.
+// short-context kernel may read before the previous kernel has completed.
 pgd_status append_then_attend(void *out, const void *q, const void *k_new, const void *v_new,
                               void *k_cache, void *v_cache, const int32_t *tables,
                               const int32_t *ctx, int32_t B, int32_t n_q, int32_t n_kv,
@@ -368,10 +368,13 @@ pgd_status append_then_attend(void *out, const void *q, const void *k_new, const
   if (s != PGD_OK) return s;
   if (short_path(pa, num_splits, MB, bs))  // one launch: the append is fused
     return launch_short(pa, k_new, v_new, k_cache, v_cache, stream, early);
+  // (The append kernels read their inputs only after waiting for the kernel
+  // before them and then let the attention launch, so that it never starts
+  // before earlier work that may write what its prologue reads: the tables.)
   cudaError_t e = fp8 ? kv_append_fp8_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B,
-                                             n_kv, bs, MB, NB, pa.p.err, stream, early)
+                                             n_kv, bs, MB, NB, pa.p.err, stream)
                       : kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -1, B, 1,
-                                         n_kv, bs, MB, NB, pa.p.err, stream, early);
+                                         n_kv, bs, MB, NB, pa.p.err, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   pa.p.wait_late = 1;
   return launch_prepared(pa, stream);
@@ -607,8 +610,7 @@ static pgd_status append_then_verify(void *out, const void *q, const void *k_new
                                      const int32_t *tables, const int32_t *ctx, int32_t B,
                                      int32_t T, int32_t n_q, int32_t n_kv, int32_t bs, int32_t MB,
                                      int32_t NB, float scale, int32_t num_splits, void *workspace,
-                                     size_t workspace_bytes, cudaStream_t stream,
-                                     bool early = false) {
+                                     size_t workspace_bytes, cudaStream_t stream) {
   if (!k_new || !v_new) return fail(PGD_ERR_INVALID_ARG, "null pointer");
   if (!aligned(k_new, 16) || !aligned(v_new, 16))
     return fail(PGD_ERR_INVALID_ARG, "bf16 arrays must be 16-byte aligned");
@@ -620,7 +622,7 @@ static pgd_status append_then_verify(void *out, const void *q, const void *k_new
                                    T);
   if (s != PGD_OK) return s;
   cudaError_t e = kv_append_launch(k_new, v_new, k_cache, v_cache, tables, ctx, -T, B, T, n_kv,
-                                   bs, MB, NB, pa.p.err, stream, early);
+                                   bs, MB, NB, pa.p.err, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
   pa.p.wait_late = 1;
   return launch_prepared(pa, stream);
@@ -1147,9 +1149,10 @@ pgd_status pgd_verify_step(void *out_h, const void *q_h, const void *k_new_h, co
                    context_lens_d, B, qb, kvb, static_cast<cudaStream_t>(stream),
                    [&](void *o, const void *q, const void *kn, const void *vn, const int32_t *cl,
                        cudaStream_t st, bool in_place) {
+                     (void)in_place;  // (the verify kernels read their inputs after the wait)
                      return append_then_verify(o, q, kn, vn, k_cache, v_cache, block_tables, cl,
                                                B, T, n_q, n_kv, bs, MB, NB, scale, num_splits,
-                                               workspace, workspace_bytes, st, in_place);
+                                               workspace, workspace_bytes, st);
                    });
 }
 

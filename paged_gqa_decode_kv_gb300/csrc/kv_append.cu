@@ -38,43 +38,20 @@ static cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, cudaStream_t stre
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// With `early`, pos, k_new and v_new live in caller memory that no kernel of
-// the stream writes (page-locked host buffers of a host-buffer step): they
-// are read before waiting for the previous kernel, so that their latency
-// overlaps its end; the tables and the caches always wait.
 __global__ void __launch_bounds__(128)
 kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                  uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                  const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
-                 int pos_offset, int B, int T, int n_kv, int bs, int MB, int NB, int32_t *err,
-                 int early) {
+                 int pos_offset, int B, int T, int n_kv, int bs, int MB, int NB, int32_t *err) {
   constexpr int kVecPerRow = kHeadDim * 2 / 16;  // 16 uint4 per 256-byte row
+  pdl_wait();               // the previous kernel (which may read these slots) has completed
+  pdl_launch_dependents();  // the attention that follows may start its prologue
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);  // (b * T + j) * n_kv + g
   const int lane = threadIdx.x & 31;
-  const bool live = row < B * T * n_kv;
+  if (row >= B * T * n_kv) return;
   const int bj = row / n_kv, g = row % n_kv;
   const int b = bj / T, j = bj % T;
-  const int v = lane & 15;
-  const size_t src = (size_t)row * kVecPerRow;
-  long long pl = 0;
-  uint4 val = make_uint4(0, 0, 0, 0);
-  auto load_inputs = [&]() {
-    pl = (long long)__ldg(pos + b) + pos_offset + j;
-    val = __ldg((lane < 16 ? k_new : v_new) + src + v);
-  };
-  if (early) {
-    // (the trigger first: the attention that follows launches without
-    // waiting for these loads -- the host-buffer step of batch16_ctx8192
-    // measured 81.1 us with the trigger after them, 80.6 before)
-    pdl_launch_dependents();
-    if (live) load_inputs();
-    pdl_wait();
-  } else {
-    pdl_wait();               // the previous kernel (which may read these slots) has completed
-    pdl_launch_dependents();  // the attention that follows may start its prologue
-  }
-  if (!live) return;
-  if (!early) load_inputs();
+  const long long pl = (long long)__ldg(pos + b) + pos_offset + j;
   if (pl < 0 || pl >= (long long)MB * bs) {
     if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_POSITION);
     return;
@@ -90,21 +67,26 @@ kv_append_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_ne
   // 8-token group, 8 uint4 per core matrix.
   const int slot = p % bs;
   const size_t tile = ((size_t)blk * n_kv + g) * (size_t)bs * kVecPerRow;
+  const size_t src = (size_t)row * kVecPerRow;
+  const int v = lane & 15;
   const size_t dst = tile + (size_t)(slot >> 3) * 128 + (size_t)v * 8 + (size_t)(slot & 7);
-  (lane < 16 ? k_cache : v_cache)[dst] = val;
+  if (lane < 16)
+    k_cache[dst] = __ldg(k_new + src + v);
+  else
+    v_cache[dst] = __ldg(v_new + src + v);
 }
 
 cudaError_t kv_append_launch(const void *k_new, const void *v_new, void *k_cache, void *v_cache,
                              const int32_t *tables, const int32_t *pos, int pos_offset, int B,
                              int T, int n_kv, int bs, int MB, int NB, int32_t *err,
-                             cudaStream_t stream, int early) {
+                             cudaStream_t stream) {
   const long long rows = (long long)B * T * n_kv;
   if (rows == 0) return cudaSuccess;
   const int grid = (int)((rows + 3) / 4);
   return launch_pdl(kv_append_kernel, dim3(grid), stream, static_cast<const uint4 *>(k_new),
                     static_cast<const uint4 *>(v_new), static_cast<uint4 *>(k_cache),
                     static_cast<uint4 *>(v_cache), tables, pos, pos_offset, B, T, n_kv, bs, MB, NB,
-                    err, early);
+                    err);
 }
 
 // kv_append into an 8-bit cache ("Ch. 6 Inference efficiency and serving",
@@ -121,35 +103,14 @@ __global__ void __launch_bounds__(128)
 kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ v_new,
                      unsigned char *__restrict__ k_cache, unsigned char *__restrict__ v_cache,
                      const int32_t *__restrict__ tables, const int32_t *__restrict__ pos,
-                     int pos_offset, int B, int n_kv, int bs, int MB, int NB, int32_t *err,
-                     int early) {
+                     int pos_offset, int B, int n_kv, int bs, int MB, int NB, int32_t *err) {
+  pdl_wait();               // the previous kernel (which may read these slots) has completed
+  pdl_launch_dependents();  // the attention that follows may start its prologue
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const bool live = row < B * n_kv;
+  if (row >= B * n_kv) return;
   const int b = row / n_kv, g = row % n_kv;
-  const int l = lane & 15;
-  // (`early`: as for kv_append_kernel; the row is quantised before the wait)
-  int p = 0;
-  uint32_t w[2] = {0, 0};
-  float scale = 0.f;
-  auto load_inputs = [&]() {
-    p = __ldg(pos + b) + pos_offset;
-    const uint4 raw = __ldg((lane < 16 ? k_new : v_new) + (size_t)row * 16 + l);
-    quantize_row_e4m3(raw, w, scale);
-  };
-  if (early) {
-    // (the trigger first: the attention that follows launches without
-    // waiting for these loads -- the host-buffer step of batch16_ctx8192
-    // measured 81.1 us with the trigger after them, 80.6 before)
-    pdl_launch_dependents();
-    if (live) load_inputs();
-    pdl_wait();
-  } else {
-    pdl_wait();               // the previous kernel (which may read these slots) has completed
-    pdl_launch_dependents();  // the attention that follows may start its prologue
-  }
-  if (!live) return;
-  if (!early) load_inputs();
+  const int p = __ldg(pos + b) + pos_offset;
   if (p < 0 || p >= MB * bs) {
     if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_POSITION);
     return;
@@ -159,6 +120,11 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
     if (lane == 0 && g == 0) atomicOr(err, PGD_DEVERR_BAD_BLOCK_ID);
     return;
   }
+  const int l = lane & 15;
+  const uint4 raw = __ldg((lane < 16 ? k_new : v_new) + (size_t)row * 16 + l);
+  uint32_t w[2];
+  float scale;
+  quantize_row_e4m3(raw, w, scale);
   const int slot = p % bs;
   unsigned char *group = (lane < 16 ? k_cache : v_cache) +
                          (((size_t)blk * n_kv + g) * (size_t)(bs / 8) + (size_t)(slot / 8)) *
@@ -170,14 +136,14 @@ kv_append_fp8_kernel(const uint4 *__restrict__ k_new, const uint4 *__restrict__ 
 cudaError_t kv_append_fp8_launch(const void *k_new, const void *v_new, void *k_cache,
                                  void *v_cache, const int32_t *tables, const int32_t *pos,
                                  int pos_offset, int B, int n_kv, int bs, int MB, int NB,
-                                 int32_t *err, cudaStream_t stream, int early) {
+                                 int32_t *err, cudaStream_t stream) {
   const int rows = B * n_kv;
   if (rows == 0) return cudaSuccess;
   const int grid = (rows + 3) / 4;
   return launch_pdl(kv_append_fp8_kernel, dim3(grid), stream, static_cast<const uint4 *>(k_new),
                     static_cast<const uint4 *>(v_new), static_cast<unsigned char *>(k_cache),
                     static_cast<unsigned char *>(v_cache), tables, pos, pos_offset, B, n_kv, bs,
-                    MB, NB, err, early);
+                    MB, NB, err);
 }
 
 // Copy-on-write ("Module 10: inference and serving", section "Share only
