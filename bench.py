@@ -957,20 +957,19 @@ def run_mla(args, rank, world, local):
     max_ms = max_over_ranks(elapsed_ms, world)
     value = sum_over_ranks(nbytes * K, world) / (max_ms / 1e3) / 1e9
 
-    # end to end: pinned host queries and new rows in, latent outputs back
+    # end to end through pgd_mla_step: pinned host queries (copied), new rows
+    # and context lengths (read in place) in, latent outputs (written in
+    # place) back
     q_h, cn_h = mb.q.cpu().pin_memory(), mb.c_new.cpu().pin_memory()
+    cl_h = mb.context_lens.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     q_d, cn_d = torch.empty_like(mb.q), torch.empty_like(mb.c_new)
+    cl_d = torch.empty_like(mb.context_lens)
 
     def e2e_step():
         c = next_pool()
-        with torch.cuda.stream(stream):
-            q_d.copy_(q_h, non_blocking=True)
-            cn_d.copy_(cn_h, non_blocking=True)
-            pgd.mla_append_decode_attention(out, q_d, cn_d, c, mb.block_tables,
-                                            mb.context_lens, mb.scale, num_splits=args.splits,
-                                            workspace=ws, stream=stream)
-            out_h.copy_(out, non_blocking=True)
+        pgd.mla_step(out_h, q_h, cn_h, cl_h, out, q_d, cn_d, cl_d, c, mb.block_tables, mb.scale,
+                     args.splits, ws, stream=stream)
 
     for _ in range(args.warmup):
         e2e_step()
@@ -1015,8 +1014,10 @@ def run_mla(args, rank, world, local):
                      "tflops_achieved": round(flops / (attn_ms / 1e3) / 1e12, 2),
                      "flop_per_byte": round(flops / nbytes, 1)},
         "e2e": {"value": round(sum_over_ranks(nbytes * K, world) / (e2e_ms / 1e3) / 1e9, 2),
-                "unit": "GB/s", "h2d_bytes_per_step": q_h.numel() * 2 + cn_h.numel() * 2,
-                "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": round(e2e_ms / K, 5)},
+                "unit": "GB/s",
+                "h2d_bytes_per_step": q_h.numel() * 2 + cn_h.numel() * 2 + cl_h.numel() * 4,
+                "d2h_bytes_per_step": out_h.numel() * 2, "ms_per_step": round(e2e_ms / K, 5),
+                "path": "pgd_mla_step (host buffers; q copied, the rest in place)"},
         # latent append, attention, merge of the parts
         "gpu_launches": (2 + (1 if parts > 1 else 0)) * K,
         "clocks": clocks_record(sampler, nvml, t_wall0, t_wall1, t_timed0, t_timed1),

@@ -340,6 +340,23 @@ pgd_status pgd_mla_append_decode_attention(void *out, const void *q, const void 
                                            void *workspace, size_t workspace_bytes,
                                            void *stream);
 
+/* pgd_mla_step: pgd_mla_append_decode_attention for a caller whose per-step
+ * tensors live in host memory -- q_h (bf16 [B][H][576]), c_new_h (bf16
+ * [B][576]), context_lens_h in, out_h (bf16 [B][H][512]) out.  q_h is always
+ * copied to q_d (every context part of a head group reads it); c_new_h,
+ * context_lens_h and out_h, when page-locked host memory that the device
+ * addresses, are read and written in place by the kernels over the host
+ * link, otherwise through c_new_d, context_lens_d, out_d and a copy each.
+ * Everything is enqueued on `stream`; the host buffers must stay untouched
+ * until the stream has completed the step.  The cache, tables and workspace
+ * stay on the device; arguments and errors as for the device-buffer call. */
+pgd_status pgd_mla_step(void *out_h, const void *q_h, const void *c_new_h,
+                        const int32_t *context_lens_h, void *out_d, void *q_d, void *c_new_d,
+                        int32_t *context_lens_d, void *cache, const int32_t *block_tables,
+                        int32_t B, int32_t H, int32_t d, int32_t dv, int32_t bs, int32_t MB,
+                        int32_t NB, float scale, int32_t num_splits, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
 /* ---------------------------------------------------------------------- */
 /* cascade: shared prefixes read once per group                            */
 /* ---------------------------------------------------------------------- */

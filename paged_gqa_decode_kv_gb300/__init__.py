@@ -12,8 +12,8 @@ from ._native import (  # noqa: F401
     paged_decode_attention_noalloc, append_decode_attention, decode_step, copy_blocks,
     kv_append_fp8, paged_decode_attention_fp8, append_decode_attention_fp8,
     cascade_decode_attention, cascade_workspace_size, kv_append_tokens, paged_verify_attention,
-    append_verify_attention, verify_step, verify_workspace_size, mla_append, mla_decode_attention, mla_append_decode_attention,
-    mla_workspace_size, device_errors,
+    append_verify_attention, verify_step, verify_workspace_size, mla_append, mla_decode_attention,
+    mla_append_decode_attention, mla_step, mla_workspace_size, device_errors,
     workspace_size, make_workspace, attention_grid, validate_tables, read_stream, set_wait_limit_ns,
     wait_limit_ns, set_short_context_tokens, uses_short_path, PreparedCall, prepare, lib,
     library_path)
@@ -26,7 +26,7 @@ __all__ = ["WORKLOADS", "Workload", "PagedBatch", "make_batch", "make_workload",
            "append_decode_attention_fp8", "cascade_decode_attention", "cascade_workspace_size",
            "kv_append_tokens", "paged_verify_attention", "append_verify_attention",
            "verify_step", "verify_workspace_size",
-           "mla_append", "mla_decode_attention", "mla_append_decode_attention",
+           "mla_append", "mla_decode_attention", "mla_append_decode_attention", "mla_step",
            "mla_workspace_size",
            "device_errors", "workspace_size", "make_workspace", "attention_grid",
            "validate_tables", "read_stream", "set_wait_limit_ns", "wait_limit_ns",

@@ -52,6 +52,8 @@ SIGNATURES = {
                                   _P], _I),
     "pgd_mla_append_decode_attention": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                          _I, _P, _Z, _P], _I),
+    "pgd_mla_step": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                      _P, _Z, _P], _I),
     "pgd_cascade_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _Z),
     "pgd_cascade_decode_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _I, _I, _I, _F, _I, _P, _Z, _P], _I),
@@ -539,6 +541,28 @@ def mla_append_decode_attention(out, q, c_new, cache, block_tables, context_lens
         H, D, 512, bs, MB, NB, float(scale), int(num_splits), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return out
+
+
+def mla_step(out_h, q_h, c_new_h, context_lens_h, out_d, q_d, c_new_d, context_lens_d, cache,
+             block_tables, scale: float, num_splits: int, workspace: torch.Tensor,
+             stream=None) -> None:
+    """One MLA decode step with host inputs/outputs (q [B][H][576], c_new
+    [B][576], out [B][H][512]): q copied to q_d, page-locked c_new, context
+    lengths and out read and written in place (pageable ones through the
+    given device tensors and a copy), then mla_append_decode_attention, all
+    on `stream`."""
+    for t, n in ((out_h, "out_h"), (q_h, "q_h"), (c_new_h, "c_new_h")):
+        _need(t, torch.bfloat16, n, cuda=False)
+    _need(context_lens_h, torch.int32, "context_lens_h", cuda=False)
+    _need(cache, torch.bfloat16, "cache")
+    B, H, D = q_h.shape
+    NB, bs, _ = _mla_pool_dims(cache)
+    MB = block_tables.shape[1]
+    _check(lib().pgd_mla_step(
+        _ptr(out_h), _ptr(q_h), _ptr(c_new_h), _ptr(context_lens_h), _ptr(out_d), _ptr(q_d),
+        _ptr(c_new_d), _ptr(context_lens_d), _ptr(cache), _ptr(block_tables), B, H, D, 512, bs,
+        MB, NB, float(scale), int(num_splits), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def cascade_workspace_size(B: int, n_q: int, n_kv: int, bs: int, max_group_size: int,

@@ -1156,6 +1156,52 @@ pgd_status pgd_verify_step(void *out_h, const void *q_h, const void *k_new_h, co
                    });
 }
 
+// The MLA step with host buffers.  q is always copied: every context part
+// of a (sequence, head group) loads it, so reading it in place would move it
+// over the host link several times; c_new, the context lengths and the output
+// are read and written in place when page-locked, like pgd_decode_step's.
+pgd_status pgd_mla_step(void *out_h, const void *q_h, const void *c_new_h,
+                        const int32_t *context_lens_h, void *out_d, void *q_d, void *c_new_d,
+                        int32_t *context_lens_d, void *cache, const int32_t *block_tables,
+                        int32_t B, int32_t H, int32_t d, int32_t dv, int32_t bs, int32_t MB,
+                        int32_t NB, float scale, int32_t num_splits, void *workspace,
+                        size_t workspace_bytes, void *stream) {
+  pgd_status s = check_mla_append(c_new_d, cache, block_tables, context_lens_d, B, d, bs, MB, NB);
+  if (s != PGD_OK) return s;
+  MlaParams p;
+  s = mla_prepare(out_d, q_d, cache, block_tables, context_lens_d, B, H, d, dv, bs, MB, NB, scale,
+                  num_splits, workspace, workspace_bytes, &p);
+  if (s != PGD_OK) return s;
+  if (B == 0) return ok();
+  if (!out_h || !q_h || !c_new_h || !context_lens_h)
+    return fail(PGD_ERR_INVALID_ARG, "null pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t qb = (size_t)B * H * kMlaD * 2, cb = (size_t)B * kMlaD * 2,
+               ob = (size_t)B * H * kMlaDv * 2;
+  const void *cn_in = device_alias(c_new_h);
+  const int32_t *cl_in = static_cast<const int32_t *>(device_alias(context_lens_h));
+  void *out_to = device_alias(out_h);
+  cudaError_t e = cudaSuccess;
+  if ((e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (!cn_in && (e = cudaMemcpyAsync(c_new_d, c_new_h, cb, cudaMemcpyHostToDevice, st)) !=
+                     cudaSuccess) ||
+      (!cl_in && (e = cudaMemcpyAsync(context_lens_d, context_lens_h, (size_t)B * 4,
+                                      cudaMemcpyHostToDevice, st)) != cudaSuccess))
+    return cuda_fail(e, "MLA step: host-to-device copy");
+  if (cl_in) p.ctx = cl_in;
+  if (out_to) p.out = static_cast<__nv_bfloat16 *>(out_to);
+  e = mla_append_launch(cn_in ? cn_in : c_new_d, cache, block_tables, p.ctx, -1, B, bs, MB, NB,
+                        p.err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "MLA append launch");
+  p.wait_late = 1;
+  e = mla_attention_launch(p, st);
+  if (e != cudaSuccess) return cuda_fail(e, "MLA attention launch");
+  if (!out_to && (e = cudaMemcpyAsync(out_h, out_d, ob, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+    return cuda_fail(e, "MLA step: device-to-host copy");
+  return ok();
+}
+
+
 pgd_status pgd_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_ids,
                            const int32_t *dst_ids, int32_t n, int32_t n_kv, int32_t d,
                            int32_t bs, int32_t NB, void *stream) {

@@ -135,6 +135,43 @@ def test_mla_append_decode_attention_one_call(num_splits):
     compare(got, want, "mla append+attend splits=%d" % num_splits)
 
 
+@pytest.mark.parametrize("pinned", ["all", "none", "mixed"])
+@pytest.mark.parametrize("num_splits", [0, 3])
+def test_mla_step_host_buffers(pinned, num_splits):
+    """pgd_mla_step: q copied, page-locked c_new / context lengths / out read
+    and written in place, pageable ones copied, each on its own; output and
+    pool equal the device-buffer one-call step bit for bit, and the oracle."""
+    lens = [1, 64, 65, 700, 2500]
+    mb = inputs.make_mla_batch(len(lens), 128, 32, lens, append=True, device="cuda", seed=46,
+                               table_seed=47)
+    pool = oracle.mla_append(mb.cache.cpu(), mb.c_new.cpu(), mb.block_tables.cpu(),
+                             mb.positions.cpu())
+    want = oracle.mla_attention(mb.q.cpu(), pool, mb.block_tables.cpu(), mb.context_lens.cpu(),
+                                mb.scale)
+    cache2 = mb.cache.clone()
+    ws = torch.empty(max(256, pgd.mla_workspace_size(len(lens), 128, num_splits)),
+                     dtype=torch.uint8, device="cuda")
+    dev = pgd.mla_append_decode_attention(None, mb.q, mb.c_new, cache2, mb.block_tables,
+                                          mb.context_lens, mb.scale, num_splits=num_splits,
+                                          workspace=ws)
+    torch.cuda.synchronize()
+    pin = lambda t: t.cpu().pin_memory()
+    page = lambda t: t.cpu().clone()
+    hq, hc, hl, ho = {"all": (pin,) * 4, "none": (page,) * 4,
+                      "mixed": (page, pin, page, pin)}[pinned]
+    out_d = torch.empty_like(dev)
+    out_h = ho(torch.zeros_like(dev))
+    pgd.mla_step(out_h, hq(mb.q), hc(mb.c_new), hl(mb.context_lens), out_d,
+                 torch.empty_like(mb.q), torch.empty_like(mb.c_new),
+                 torch.empty_like(mb.context_lens), mb.cache, mb.block_tables, mb.scale,
+                 num_splits, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int16), dev.cpu().view(torch.int16))
+    assert np.array_equal(_bits(mb.cache), _bits(cache2))
+    assert np.array_equal(_bits(mb.cache), pool)
+    compare(out_h, want, "mla host-buffer step %s splits=%d" % (pinned, num_splits))
+
+
 def test_mla_steps_back_to_back():
     """Six one-call steps on one stream with a growing context (each
     attention's prologue overlapping the append before it): every step sees
