@@ -189,3 +189,62 @@ def test_prepare_checks_arguments_on_the_host(L):
         pgd.prepare("paged_decode_attention", None, q.float(), pool, pool, tables, lens, 0.1)
     with pytest.raises(ValueError):
         pgd.prepare("no_such_call")
+
+
+def _verify_call(L, fn, **kw):
+    a = dict(out=16, q=16, kn=16, vn=16, k=16, v=16, t=16, c=16, B=2, T=2, n_q=8, n_kv=2,
+             d=128, bs=16, MB=4, NB=8, scale=0.1, splits=0, ws=None, wsb=0)
+    a.update(kw)
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    if fn == "append_verify":
+        return L.pgd_append_verify_attention(
+            P(a["out"]), P(a["q"]), P(a["kn"]), P(a["vn"]), P(a["k"]), P(a["v"]), P(a["t"]),
+            P(a["c"]), a["B"], a["T"], a["n_q"], a["n_kv"], a["d"], a["bs"], a["MB"], a["NB"],
+            a["scale"], a["splits"], P(a["ws"]), a["wsb"], None)
+    # verify_step: host buffers 32 bytes apart from the device ones
+    h = lambda x: None if x is None else x + 4096
+    return L.pgd_verify_step(
+        P(h(a["out"])), P(h(a["q"])), P(h(a["kn"])), P(h(a["vn"])), P(h(a["c"])), P(a["out"]),
+        P(a["q"]), P(a["kn"]), P(a["vn"]), P(a["c"]), P(a["k"]), P(a["v"]), P(a["t"]), a["B"],
+        a["T"], a["n_q"], a["n_kv"], a["d"], a["bs"], a["MB"], a["NB"], a["scale"], a["splits"],
+        P(a["ws"]), a["wsb"], None)
+
+
+@pytest.mark.parametrize("fn", ["append_verify", "verify_step"])
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), _native.ERR_INVALID_ARG),
+    (dict(T=5, n_q=8, n_kv=2), _native.ERR_UNSUPPORTED),   # 20 query rows per KV head
+    (dict(d=64), _native.ERR_UNSUPPORTED),
+    (dict(q=None), _native.ERR_INVALID_ARG),
+    (dict(kn=None), _native.ERR_INVALID_ARG),
+    (dict(vn=24), _native.ERR_INVALID_ARG),                 # misaligned
+    (dict(B=0, out=None, q=None, kn=None, vn=None, k=None, v=None, t=None, c=None), 0),
+])
+def test_verify_step_calls_reject_on_host(L, fn, kw, status):
+    """The one-call and host-buffer verify steps run their checks before any
+    copy or launch (no CUDA call is made here: there is no GPU)."""
+    assert _verify_call(L, fn, **kw) == status
+    if status:
+        assert L.pgd_last_error_detail()
+
+
+def test_verify_step_rejects_null_host_buffers(L):
+    P = ctypes.c_void_p
+    args = [P(16)] * 13 + [2, 2, 8, 2, 128, 16, 4, 8, 0.1, 0, None, 0, None]
+    for i in range(5):  # out_h, q_h, k_new_h, v_new_h, context_lens_h
+        a = list(args)
+        a[i] = None
+        assert L.pgd_verify_step(*a) == _native.ERR_INVALID_ARG
+
+
+def test_mla_step_rejects_on_host(L):
+    P = ctypes.c_void_p
+    def call(d=576, bs=32, c_new_d=16, B=2):
+        return L.pgd_mla_step(P(4112), P(4112), P(4112), P(4112), P(16), P(16),
+                              None if c_new_d is None else P(c_new_d), P(16), P(16), P(16), B,
+                              16, d, 512, bs, 4, 8, 0.1, 0, None, 0, None)
+    assert call(d=512) == _native.ERR_UNSUPPORTED
+    assert call(bs=8) == _native.ERR_UNSUPPORTED
+    assert call(c_new_d=None) == _native.ERR_INVALID_ARG
+    assert call(c_new_d=24) == _native.ERR_INVALID_ARG
+    assert call(B=-1) == _native.ERR_INVALID_ARG
