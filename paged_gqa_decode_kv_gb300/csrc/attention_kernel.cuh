@@ -695,8 +695,8 @@ __device__ __forceinline__ void produce(const AttnParams &p, const Schedule &sc,
 // obase + (h >> lg_gh) * n_q + h mod 2^lg_gh); run by the 128 epilogue threads,
 // thread e owning dim e.  The (max, sum) pairs are staged in shared memory
 // PPB parts at a time; the partial outputs are read U parts at a time, every
-// load of a group issued before any is used.  Cold (once per cut unit), so
-// out of line and not unrolled beyond one group.
+// load of a group issued before any is used, the first group's while the
+// maxima are formed.  Cold (once per cut unit), so out of line.
 template <int G, bool FP8>
 __device__ __noinline__ void merge_parts(const float *__restrict__ part_o,
                                          const float *__restrict__ part_ml,
@@ -705,7 +705,10 @@ __device__ __noinline__ void merge_parts(const float *__restrict__ part_o,
                                          int rows, int e, float2 *mlb) {
   constexpr int NET = 128;
   constexpr int PPB = MERGE_PAIRS / G;
-  constexpr int U = (FP8 ? 16 : 32) / G;  // (fewer under the 8-bit kernel's register budget)
+  // (at most 24 parts; fewer where the running state takes more registers,
+  // and under the 8-bit kernel's register budget)
+  constexpr int U0 = (FP8 ? 16 : G >= 8 ? 48 : 96) / G;
+  constexpr int U = U0 < 24 ? U0 : 24;
   const size_t row0 = ((size_t)unit + (size_t)c0) * G;
   float Mx[G], Lm[G], O[G];
 #pragma unroll
@@ -714,6 +717,17 @@ __device__ __noinline__ void merge_parts(const float *__restrict__ part_o,
   for (int base = 0; base < n_parts; base += PPB) {
     const int nb = min(PPB, n_parts - base);
     const size_t rb = row0 + (size_t)base * G;
+    float ov[U][G];
+    auto load_group = [&](int i0) {
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        if (i0 + i >= nb) break;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          ov[i][h] = __ldcg(part_o + (rb + (size_t)(i0 + i) * G + h) * kHeadDim + e);
+      }
+    };
+    load_group(0);  // (independent of the maxima: in flight while they are formed)
 #pragma unroll 1
     for (int j = e; j < nb * G; j += NET)
       mlb[j] = __ldcg(reinterpret_cast<const float2 *>(part_ml) + rb + j);
@@ -721,7 +735,7 @@ __device__ __noinline__ void merge_parts(const float *__restrict__ part_o,
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       float bm = Mx[h];
-#pragma unroll 1
+#pragma unroll 8
       for (int i = 0; i < nb; ++i) bm = fmaxf(bm, mlb[i * G + h].x);
       if (bm != Mx[h] && Mx[h] != -INFINITY) {
         const float cf = exp2f(Mx[h] - bm);
@@ -732,23 +746,18 @@ __device__ __noinline__ void merge_parts(const float *__restrict__ part_o,
     }
 #pragma unroll 1
     for (int i0 = 0; i0 < nb; i0 += U) {
-      float ov[U][G];
+      if (i0 > 0) load_group(i0);
 #pragma unroll
-      for (int i = 0; i < U; ++i)
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-          ov[i][h] = (i0 + i < nb)
-                         ? __ldcg(part_o + (rb + (size_t)(i0 + i) * G + h) * kHeadDim + e)
-                         : 0.f;
-#pragma unroll
-      for (int i = 0; i < U; ++i)
+      for (int i = 0; i < U; ++i) {
+        if (i0 + i >= nb) break;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-          const float2 ml = (i0 + i < nb) ? mlb[(i0 + i) * G + h] : make_float2(-INFINITY, 0.f);
+          const float2 ml = mlb[(i0 + i) * G + h];
           const float cf = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - Mx[h]);
           Lm[h] = fmaf(cf, ml.y, Lm[h]);
           O[h] = fmaf(cf, ov[i][h], O[h]);
         }
+      }
     }
     named_barrier_sync(2, NET);  // mlb is reused by the next batch
   }
@@ -1468,13 +1477,16 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         for (int h = 0; h < G; ++h)
           if (e == h)
             *reinterpret_cast<float2 *>(p.part_ml + (srow + h) * 2) = make_float2(M[h], Lsum[h]);
-        // publish this part; the last part of the unit to arrive merges all
-        __threadfence();
+        // publish this part; the last part of the unit to arrive merges all.
+        // The barrier orders the 128 threads' stores before thread 0's
+        // atomic, whose release makes them visible with it and whose acquire
+        // (in the last arriver) the other parts' stores; the second barrier
+        // passes that on to the threads that read them.
         named_barrier_sync(2, NET);
         if (e == 0) {
           // (whole-unit parts: the unit's only part is this CTA's)
           const int n_parts = (int)(c_last - c_first + 1);
-          const int before = atomicAdd(p.counters + unit, 1);
+          const int before = atomic_add_acq_rel_gpu(p.counters + unit, 1);
           const int last = (before == n_parts - 1);
           if (last) atomicExch(p.counters + unit, 0);  // ready for the next call
           flag[0] = last;
@@ -1483,7 +1495,6 @@ __global__ void __launch_bounds__(kThreads<FP8>, 1) paged_attention_kernel(const
         }
         named_barrier_sync(2, NET);
         if (flag[0]) {
-          __threadfence();
           merge_parts<G, FP8>(p.part_o, p.part_ml, p.out, unit, flag[1], flag[2], obase, p.lg_gh,
                               p.n_q, p.rows, e, reinterpret_cast<float2 *>(smem + L::OFF_MERGE));
         }

@@ -138,6 +138,16 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Atomic add at GPU scope with acquire-release semantics: the calling
+// thread's earlier writes (and those ordered before them by a CTA barrier)
+// become visible with it, and the writes released by earlier additions are
+// visible after it.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *addr, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+  return old;
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
